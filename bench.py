@@ -1,0 +1,456 @@
+"""Benchmark of paged decode attention on GB300: K/V GB/s, decode steps/s and the
+fraction of the measured HBM roofline.
+
+One step = one decode call (partial pass + merge pass) over every sequence of the
+workload; a two-layer workload (4-bit + 8-bit pages) runs both layers per step.
+Inputs are seeded synthetic data of the workload's shapes and length mix, already
+resident in HBM when the timed region starts. Workloads whose inputs are smaller
+than 3x the L2 cache rotate through enough independent input copies that every
+timed step reads from HBM. Steps are recorded once into a CUDA graph and the
+graph is replayed; time comes from CUDA events on the launching stream.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs its own instance of the workload (weak
+scaling: sequences are independent, there is no exchange between GPUs); the time
+is the maximum over ranks and the value counts every rank's bytes.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attention K/V GB/s and steps/s; % of GB300 HBM roofline"
+DEFAULT_WORKLOAD = "affine4_g64_1x8192_hq16_d256"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU oracle sample")
+    return ap.parse_args(argv)
+
+
+def workload_specs(name):
+    from quantized_kv_decode_partial_gb300.workloads import LAYER_GROUPS, WORKLOADS
+    if name in LAYER_GROUPS:
+        return [WORKLOADS[n] for n in LAYER_GROUPS[name]]
+    if name not in WORKLOADS:
+        raise SystemExit(f"unknown workload {name}; choose from {sorted(WORKLOADS) + sorted(LAYER_GROUPS)}")
+    return [WORKLOADS[name]]
+
+
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def _once(self):
+        try:
+            out = subprocess.run(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                                  "--format=csv,noheader,nounits"], capture_output=True, text=True, timeout=20)
+            return out.stdout.strip().splitlines()
+        except (OSError, subprocess.SubprocessError):
+            return []
+
+    def start(self):
+        self.lines = self._once()
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "100", "-f", self.path],
+                                         stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=10)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            try:
+                with open(self.path) as f:
+                    self.lines += f.read().strip().splitlines()
+            except OSError:
+                pass
+        self.lines += self._once()
+        if self.path and os.path.exists(self.path):
+            os.unlink(self.path)
+        return self.summary()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, flag in zip(names, parts[5:9]):
+                if flag.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle baseline (bounded sample, one thread, in a child process)
+# ---------------------------------------------------------------------------
+
+CPU_CHILD = r"""
+import json, math, os, sys, time
+sys.path.insert(0, {root!r})
+import numpy as np
+import torch
+torch.set_num_threads(1)
+import oracle
+from quantized_kv_decode_partial_gb300.workloads import WORKLOADS, make_case, required_kv_bytes
+budget = {budget}
+done_bytes, elapsed, samples = 0, 0.0, []
+for name in {names!r}:
+    spec = WORKLOADS[name]
+    case = make_case(spec, device="cpu", seed={seed})
+    f64 = lambda t: None if t is None else t.float().double().numpy()
+    kw = dict(bits=spec.bits, group_size=spec.group_size)
+    if spec.bits == 16:
+        kp, vp = f64(case.k_pool), f64(case.v_pool)
+    else:
+        kp, vp = case.k_pool.numpy(), case.v_pool.numpy()
+        kw.update(k_scales=f64(case.k_scales), k_biases=f64(case.k_biases), v_scales=f64(case.v_scales),
+                  v_biases=f64(case.v_biases))
+    q = f64(case.q)
+    tables, lens = case.block_tables.numpy(), case.seq_lens.numpy()
+    # one (sequence, KV head) unit at a time, until the time budget share is spent
+    units = [(b, kv) for b in range(spec.num_seqs) for kv in range(spec.num_kv_heads)]
+    share = budget / len({names!r})
+    t_start = time.perf_counter()
+    n = 0
+    for b, kv in units:
+        rows = [(b, h) for h in range(kv * spec.rep, (kv + 1) * spec.rep)]
+        t0 = time.perf_counter()
+        oracle.paged_decode_attention(q, kp, vp, tables, lens, case.scale, spec.n_query, rows=rows, **kw)
+        elapsed += time.perf_counter() - t0
+        done_bytes += int(lens[b]) * 2 * (2 * spec.head_dim if spec.bits == 16 else
+                                          spec.head_dim * spec.bits // 8 + spec.head_dim // spec.group_size * 4)
+        n += 1
+        if time.perf_counter() - t_start > share:
+            break
+    samples.append(f"{{name}}: {{n}} of {{len(units)}} (sequence, KV head) units")
+print(json.dumps({{"bytes": done_bytes, "seconds": elapsed, "sample": "; ".join(samples)}}))
+"""
+
+
+def cpu_oracle_baseline(names, seed, budget_s):
+    code = CPU_CHILD.format(root=ROOT, budget=budget_s, names=list(names), seed=seed)
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    res = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
+                         timeout=max(600, 20 * budget_s))
+    if res.returncode != 0:
+        raise RuntimeError(f"CPU oracle failed:\n{res.stderr[-2000:]}")
+    info = json.loads(res.stdout.strip().splitlines()[-1])
+    gbs = info["bytes"] / info["seconds"] / 1e9
+    return {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": info["sample"] + f"; {info['bytes']} K/V bytes in {info['seconds']:.2f} s, one thread",
+            "bytes": info["bytes"], "seconds": info["seconds"]}
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the oracle, timed on the host cores
+# ---------------------------------------------------------------------------
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    specs = workload_specs(args.workload)
+    names = [s.name for s in specs]
+    per_step = max(1.0, 60.0 / max(1, args.steps + args.warmup))
+    values = []
+    total_bytes, total_s, sample = 0, 0.0, ""
+    for i in range(args.warmup + args.steps):
+        r = cpu_oracle_baseline(names, specs[0].seed, per_step)
+        if i >= args.warmup:
+            values.append(r["value"])
+            total_bytes += r["bytes"]
+            total_s += r["seconds"]
+            sample = r["sample"]
+    value = total_bytes / total_s / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_s / max(1, args.steps),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "sample": "bounded CPU sample per step"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from quantized_kv_decode_partial_gb300 import (DecodeParams, load_library, make_plan, paged_decode_attention,
+                                                   paged_decode_passes)
+    from quantized_kv_decode_partial_gb300 import build as pkv_build
+    from quantized_kv_decode_partial_gb300.binding import layout_for
+    from quantized_kv_decode_partial_gb300.workloads import make_case, required_kv_bytes
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pkv_build.build()
+    load_library()
+
+    # CPU baseline first, in a child process, before this process does GPU work.
+    specs = workload_specs(args.workload)
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_oracle_baseline([s.name for s in specs], specs[0].seed, args.cpu_seconds)
+
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    layers = []
+    for sp in specs:
+        base = make_case(sp, device=dev, seed=sp.seed + 7919 * rank, poison=False)
+        in_bytes = sum(t.numel() * t.element_size() for t in
+                       (base.q, base.k_pool, base.v_pool, base.k_scales, base.k_biases, base.v_scales, base.v_biases,
+                        base.block_tables, base.seq_lens) if t is not None)
+        copies = max(1, math.ceil(3 * l2 / in_bytes))
+        insts = [base] + [make_case(sp, device=dev, seed=sp.seed + 7919 * rank + 104729 * (c + 1), poison=False,
+                                    lengths=base.lens_host) for c in range(copies - 1)]
+        layout = layout_for(base.k_pool, sp.head_dim, sp.bits, sp.group_size)
+        params = DecodeParams(sp.num_seqs, sp.num_q_heads, sp.n_query, base.block_tables.shape[1],
+                              base.partition_tokens)
+        plan = make_plan(layout, params)
+        ws = torch.empty(max(1, plan.workspace_bytes), dtype=torch.uint8, device=dev)
+        out = torch.empty_like(base.q)
+        layers.append(dict(spec=sp, insts=insts, plan=plan, ws=ws, out=out, copies=copies, in_bytes=in_bytes,
+                           kv_bytes=required_kv_bytes(sp, base.lens_host)))
+    step_bytes = sum(L["kv_bytes"] for L in layers)
+    n_copies = max(L["copies"] for L in layers)
+
+    def call(L, i, passes=None):
+        c = L["insts"][i % L["copies"]]
+        sp = L["spec"]
+        kw = dict(bits=sp.bits, group_size=sp.group_size, k_scales=c.k_scales, k_biases=c.k_biases,
+                  v_scales=c.v_scales, v_biases=c.v_biases, partition_tokens=c.partition_tokens, out=L["out"],
+                  workspace=L["ws"])
+        if passes is None:
+            paged_decode_attention(c.q, c.k_pool, c.v_pool, c.block_tables, c.seq_lens, c.scale, **kw)
+        else:
+            paged_decode_passes(c.q, c.k_pool, c.v_pool, c.block_tables, c.seq_lens, c.scale, passes=passes, **kw)
+
+    def step(i, passes=None):
+        for L in layers:
+            call(L, i, passes)
+
+    stream = torch.cuda.Stream(device=dev)
+
+    def capture(n, passes=None, offset=0):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n):
+                step(offset + i, passes)
+        return g
+
+    def replay_timed(graphs_reps):
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for g, reps in graphs_reps:
+                for _ in range(reps):
+                    g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms = float(t.item())
+            dist.barrier()
+        return ms
+
+    # warm-up: W eager steps on the launching stream
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step(i)
+    torch.cuda.synchronize(dev)
+
+    # graphs of whole rotations of the input copies, replayed to make exactly K steps
+    K = args.steps
+    chunk = min(K, max(n_copies, 50 if n_copies == 1 else n_copies))
+    g_full = capture(chunk)
+    rest = K % chunk
+    g_rest = capture(rest, offset=0) if rest else None
+    g_full.replay()  # first replay outside the timed region (graph upload)
+    if g_rest is not None:
+        g_rest.replay()
+    torch.cuda.synchronize(dev)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    ms = replay_timed([(g_full, K // chunk)] + ([(g_rest, 1)] if g_rest else []))
+    clk = clocks.stop()
+
+    # the partial pass alone (the dominant kernel), same inputs, same stream
+    g_part = capture(chunk, passes="partial")
+    g_part_rest = capture(rest, passes="partial") if rest else None
+    g_part.replay()
+    torch.cuda.synchronize(dev)
+    ms_partial = replay_timed([(g_part, K // chunk)] + ([(g_part_rest, 1)] if g_part_rest else []))
+
+    # end to end through the public call: per step, q / tables / lengths come from
+    # pinned host memory, the output goes back to pinned host memory
+    host_in, host_out = [], []
+    for L in layers:
+        c = L["insts"][0]
+        host_in.append([t.cpu().pin_memory() for t in (c.q, c.block_tables, c.seq_lens)])
+        host_out.append(torch.empty(L["out"].shape, dtype=L["out"].dtype, pin_memory=True))
+    h2d = sum(t.numel() * t.element_size() for hs in host_in for t in hs)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    dev_in = [[torch.empty_like(t, device=dev) for t in hs] for hs in host_in]
+    e2e_steps = min(K, 50)
+
+    def e2e_once():
+        for li, L in enumerate(layers):
+            for src, dst in zip(host_in[li], dev_in[li]):
+                dst.copy_(src, non_blocking=True)
+            c = L["insts"][0]
+            sp = L["spec"]
+            q, tb, sl = dev_in[li]
+            paged_decode_attention(q, c.k_pool, c.v_pool, tb, sl, c.scale, bits=sp.bits, group_size=sp.group_size,
+                                   k_scales=c.k_scales, k_biases=c.k_biases, v_scales=c.v_scales,
+                                   v_biases=c.v_biases, partition_tokens=c.partition_tokens, out=L["out"],
+                                   workspace=L["ws"])
+            host_out[li].copy_(L["out"], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            e2e_once()
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_once()
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    ms_step = ms / K
+    value = world * step_bytes / (ms_step * 1e-3) / 1e9
+    part_ms = ms_partial / K
+    peak, peak_kind = measured_hbm_peak()
+    achieved = step_bytes / (part_ms * 1e-3) / 1e9
+    launches_per_step = sum(1 + (L["plan"].max_partitions > 1) for L in layers)
+    if rank == 0:
+        sp0 = layers[0]["spec"]
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+            "ms_per_step": ms_step, "steps_per_s": 1e3 / ms_step * world, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16 tensor-core products, f32 softmax/accumulate",
+            "data": "synthetic",
+            "config": {
+                "workload": args.workload,
+                "layers": [L["spec"].description for L in layers],
+                "kv_bytes_per_step": step_bytes, "partition_tokens": [L["plan"].partition_tokens for L in layers],
+                "partitions_max": [L["plan"].max_partitions for L in layers],
+                "l2": (f"inputs rotate over {n_copies} independent copies ({n_copies} x "
+                       f"{layers[0]['in_bytes'] / 1e6:.1f} MB >= 3 x L2 {l2 / 1e6:.0f} MB)" if n_copies > 1 else
+                       f"inputs ({layers[0]['in_bytes'] / 1e9:.2f} GB) larger than L2 ({l2 / 1e6:.0f} MB)"),
+                "timing": "CUDA graph of the K steps replayed; CUDA events on the launching stream",
+                "parallelism": f"dp{world} (independent instances)",
+            },
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": None,
+                         "kernel": f"pkv_partial_kernel (partial pass alone, {part_ms * 1e3:.2f} us per step)",
+                         "peak_source": f"{peak_kind} hbm_gbs", "frac_of_nominal_7900": achieved / 7900.0},
+            "e2e": {"value": world * step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                    "what": "public call per step with q, block tables and lengths copied from pinned host memory "
+                            "and the output copied back; the KV pool is device-resident cache state"},
+            "gpu_launches": launches_per_step * K,
+            "clocks": clk,
+        }
+        if cpu is not None:
+            line["cpu_baseline"] = {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,188 @@
+/*
+ * pkv_decode.h -- paged decode attention over a block-pool KV cache (GB300, sm_103a).
+ *
+ * What the library computes
+ * -------------------------
+ * Single-step and few-query decode attention over a paged KV cache, the read
+ * described on the mlx-bun pages ("@mlx-bun/inference 0.0.0-stage -> 1.0.0",
+ * package/src/kernels/attention/paged.ts: ``paged_attention_partial``,
+ * ``paged_attention_affine_partial`` and ``paged_attention_merge`` behind
+ * ``pagedAttentionView(...).attend(q, scale, mask)``; the 4-bit decode of
+ * kernels/attention/kvq4-decode.ts; the few-query causal rule of
+ * kernels/attention/multi-query.ts). For sequence b, query row i < N and query
+ * head h:
+ *
+ *     kv    = h / (HQ / HK)                      consecutive heads share a KV head
+ *     key t is visible iff t <= len_b - N + i    (len_b counts the N new rows)
+ *     K[t]  = k_pool[block_tables[b][t / BS]][kv][t % BS][:]
+ *     affine pages: K[t][d] = scale[t][d/64] * code[t][d] + bias[t][d/64]
+ *     out[b][h][i] = softmax_t(scale * <q, K[t]>) . V[t]       rounded to bf16
+ *
+ * The work is split along the sequence into partitions; each partition keeps an
+ * f32 online-softmax state (running max, normaliser, unnormalised output) and
+ * a merge pass combines partitions by log-sum-exp. Each K/V row is read from
+ * HBM once and serves every query head of its KV head (GQA reuse).
+ *
+ * Data layout (row-major, all device memory unless stated otherwise)
+ * -----------------------------------------------------------------
+ *   q             bf16  [num_seqs, num_q_heads, n_query, head_dim]
+ *   k_pool,v_pool bits=16: bf16 [num_blocks, num_kv_heads, block_size, head_dim]
+ *                 bits=4/8: uint32 words [num_blocks, num_kv_heads, block_size,
+ *                 head_dim*bits/32]; code d of a row sits in word d/(32/bits) at
+ *                 bit offset (d % (32/bits))*bits (lowest bits first).
+ *   k_scales, k_biases, v_scales, v_biases
+ *                 bf16 [num_blocks, num_kv_heads, block_size, head_dim/64]
+ *                 (affine pages only; NULL for bf16 pages). Dim d uses group d/64.
+ *                 These are the layouts of the pages' BlockPool
+ *                 (state/paged/cache.ts): every plane [numBlocks, H, blockSize, width].
+ *   block_tables  int32 [num_seqs, max_blocks_per_seq]: logical page -> physical block.
+ *   seq_lens      int32 [num_seqs]: cached rows per sequence, including the n_query
+ *                 new ones.
+ *   out           bf16  [num_seqs, num_q_heads, n_query, head_dim]
+ *
+ * Ownership: every pointer is borrowed; the library frees nothing and keeps no
+ * pointer after a call returns. Calls are asynchronous on the given stream
+ * (a cudaStream_t passed as void*; NULL = the legacy default stream) and make
+ * no allocation and no host synchronisation, so they can be captured in a
+ * CUDA graph.
+ *
+ * Errors: host-side argument checks happen before any CUDA call and return a
+ * negative PKV_ERR_* code without launching anything. Problems that only the
+ * device can see (a block-table entry outside [0, num_blocks), a seq_len
+ * below n_query or above max_blocks_per_seq*block_size) never trap: the
+ * offending rows are skipped (bad block) or the sequence's outputs are written
+ * as zeros (bad length), and a PKV_DEVERR_* bit is OR-ed into *error_flag when
+ * error_flag is not NULL. Rows at or past seq_len in a sequence's last page
+ * are never used, whatever they hold.
+ */
+#ifndef PKV_DECODE_H
+#define PKV_DECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Host-side return codes. */
+#define PKV_OK 0
+#define PKV_ERR_NULL_POINTER (-1)        /* a required pointer is NULL */
+#define PKV_ERR_MISALIGNED (-2)          /* a device pointer is not 16-byte aligned */
+#define PKV_ERR_BAD_LAYOUT (-3)          /* unsupported bits / group_size / head_dim / block_size */
+#define PKV_ERR_BAD_PARAMS (-4)          /* bad num_seqs, heads, n_query, table width or partition size */
+#define PKV_ERR_UNSUPPORTED_SHAPE (-5)   /* (num_q_heads/num_kv_heads)*n_query above the limit for head_dim */
+#define PKV_ERR_WORKSPACE_TOO_SMALL (-6) /* workspace NULL or smaller than pkv_plan.workspace_bytes */
+#define PKV_ERR_CUDA (-7)                /* a CUDA runtime or driver call failed */
+
+/* Device-side error bits, OR-ed into *error_flag. */
+#define PKV_DEVERR_BAD_BLOCK 1   /* a referenced block id outside [0, num_blocks): its rows were skipped */
+#define PKV_DEVERR_BAD_SEQ_LEN 2 /* seq_len < n_query or > max_blocks_per_seq*block_size: outputs zeroed */
+#define PKV_DEVERR_TIMEOUT 4     /* an internal pipeline wait gave up after about a second */
+
+/* Pool layout descriptor (the pages' PagedAttentionStorage: blockSize, headDim,
+ * quantization {bits, groupSize}). */
+typedef struct pkv_pool_layout {
+  int32_t num_blocks;   /* blocks in the pool, > 0 */
+  int32_t num_kv_heads; /* HK, > 0 */
+  int32_t block_size;   /* BS: rows per block; a multiple of 16 (bf16) or 32 (affine), <= 1024 */
+  int32_t head_dim;     /* D: 64, 128 or 256 for bf16; 128 or 256 for affine */
+  int32_t bits;         /* 16 = bf16 pages; 4 or 8 = affine codes */
+  int32_t group_size;   /* affine group; must be 64 (ignored for bf16) */
+} pkv_pool_layout;
+
+/* Per-call decode parameters. */
+typedef struct pkv_decode_params {
+  int32_t num_seqs;           /* B, > 0 */
+  int32_t num_q_heads;        /* HQ, a multiple of num_kv_heads */
+  int32_t n_query;            /* N >= 1 new query rows per sequence */
+  int32_t max_blocks_per_seq; /* row stride of block_tables, > 0 */
+  int32_t partition_tokens;   /* rows per partition: 0 = chosen from lengths and SM count;
+                                 otherwise rounded up to the chunk rows (16 bf16, 32 affine).
+                                 A value >= max_blocks_per_seq*block_size gives one partition. */
+} pkv_decode_params;
+
+/* How a call will be carried out. */
+typedef struct pkv_plan {
+  int32_t partition_tokens; /* resolved rows per partition */
+  int32_t max_partitions;   /* partitions of the longest admissible sequence */
+  int32_t chunk_rows;       /* rows staged per pipeline step */
+  int32_t sm_count;         /* SM count the plan was made for */
+  int32_t threads_per_cta;  /* partial-kernel CTA size */
+  int32_t smem_bytes;       /* partial-kernel dynamic shared memory */
+  size_t workspace_bytes;   /* device scratch for the partials; 0 with one partition */
+} pkv_plan;
+
+/* Makes the plan for (layout, params) on a GPU with sm_count SMs. Pure host
+ * code, no CUDA call. Returns PKV_OK or a PKV_ERR_* code. */
+int pkv_make_plan(const pkv_pool_layout* layout, const pkv_decode_params* params, int32_t sm_count,
+                  pkv_plan* plan);
+
+/* pkv_make_plan for the current CUDA device (reads its SM count). */
+int pkv_plan_for_current_device(const pkv_pool_layout* layout, const pkv_decode_params* params,
+                                pkv_plan* plan);
+
+/* Paged decode attention: partial pass (and merge pass when there is more than
+ * one partition), asynchronous on `stream`.
+ *   scale            softmax scale applied to <q, K> (e.g. 1/sqrt(head_dim))
+ *   workspace        device scratch of at least plan.workspace_bytes (may be NULL
+ *                    when that is 0); the caller owns it; its contents need no
+ *                    initialisation and are overwritten.
+ *   error_flag       optional device int32 that receives PKV_DEVERR_* bits; the
+ *                    library only ORs into it, the caller clears it.
+ * Returns PKV_OK once the kernels are enqueued, or a PKV_ERR_* code. */
+int pkv_paged_decode_attention(const pkv_pool_layout* layout, const pkv_decode_params* params,
+                               const void* q, const void* k_pool, const void* v_pool,
+                               const void* k_scales, const void* k_biases, const void* v_scales,
+                               const void* v_biases, const int32_t* block_tables,
+                               const int32_t* seq_lens, float scale, void* out, void* workspace,
+                               size_t workspace_bytes, int32_t* error_flag, void* stream);
+
+/* The two passes of pkv_paged_decode_attention, for callers that schedule them
+ * apart (for example to combine partition states computed elsewhere, or to time
+ * the partial pass alone). pkv_paged_decode_partial takes the same arguments
+ * and enqueues only the partial pass: with one partition it writes the final
+ * `out`; otherwise it writes each partition's state (running max in log2 units,
+ * normaliser, unnormalised output, all f32) into `workspace`.
+ * pkv_merge_partitions then enqueues the log-sum-exp merge of those states into
+ * `out` for the same layout and params (it does nothing with one partition).
+ * Returns as pkv_paged_decode_attention. */
+int pkv_paged_decode_partial(const pkv_pool_layout* layout, const pkv_decode_params* params, const void* q,
+                             const void* k_pool, const void* v_pool, const void* k_scales,
+                             const void* k_biases, const void* v_scales, const void* v_biases,
+                             const int32_t* block_tables, const int32_t* seq_lens, float scale, void* out,
+                             void* workspace, size_t workspace_bytes, int32_t* error_flag, void* stream);
+
+int pkv_merge_partitions(const pkv_pool_layout* layout, const pkv_decode_params* params,
+                         const int32_t* seq_lens, const void* workspace, size_t workspace_bytes, void* out,
+                         int32_t* error_flag, void* stream);
+
+/* Bit-exact gather of one pool plane into contiguous per-sequence rows, the
+ * fetch copy of the pages' BlockPool.gather / pickBlocks (state/paged/cache.ts):
+ *   out[b][h][t][:] = pool[block_tables[b][t / block_size]][h][t % block_size][:]
+ * for t < seq_lens[b] (<= max_len); rows t >= seq_lens[b] of out are left as they
+ * were. pool: [num_blocks, num_kv_heads, block_size, row_bytes] bytes;
+ * out: [num_seqs, num_kv_heads, max_len, row_bytes] bytes. row_bytes must be a
+ * positive multiple of 4; pool and out 16-byte aligned. Bad block ids skip the
+ * row and set PKV_DEVERR_BAD_BLOCK; a seq_len outside [0, max_len] or above
+ * max_blocks_per_seq*block_size sets PKV_DEVERR_BAD_SEQ_LEN and copies nothing
+ * for that sequence. */
+int pkv_paged_gather(const void* pool, int32_t num_blocks, int32_t num_kv_heads, int32_t block_size,
+                     int32_t row_bytes, const int32_t* block_tables, const int32_t* seq_lens,
+                     int32_t num_seqs, int32_t max_blocks_per_seq, int32_t max_len, void* out,
+                     int32_t* error_flag, void* stream);
+
+/* Message for a PKV_ERR_* code (static storage). */
+const char* pkv_strerror(int code);
+
+/* Text of the last PKV_ERR_CUDA failure on this thread (static per-thread storage). */
+const char* pkv_last_cuda_error(void);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int pkv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_DECODE_H */

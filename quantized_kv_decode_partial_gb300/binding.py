@@ -1,0 +1,219 @@
+"""Thin Python binding of libpkvdecode.so (include/pkv_decode.h).
+
+Argument marshalling only: shapes are read off the tensors, pointers and the
+current CUDA stream are passed through, and PyTorch allocates the output and
+the workspace. Every step of the computation runs in the library's kernels;
+there is no fallback, and a missing library raises ``LibraryNotBuilt``.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+from .build import LIB_PATH
+
+EXPORTS = (
+    "pkv_make_plan",
+    "pkv_plan_for_current_device",
+    "pkv_paged_decode_attention",
+    "pkv_paged_decode_partial",
+    "pkv_merge_partitions",
+    "pkv_paged_gather",
+    "pkv_strerror",
+    "pkv_last_cuda_error",
+    "pkv_version",
+)
+
+PKV_OK = 0
+PKV_ERR_NULL_POINTER = -1
+PKV_ERR_MISALIGNED = -2
+PKV_ERR_BAD_LAYOUT = -3
+PKV_ERR_BAD_PARAMS = -4
+PKV_ERR_UNSUPPORTED_SHAPE = -5
+PKV_ERR_WORKSPACE_TOO_SMALL = -6
+PKV_ERR_CUDA = -7
+
+PKV_DEVERR_BAD_BLOCK = 1
+PKV_DEVERR_BAD_SEQ_LEN = 2
+PKV_DEVERR_TIMEOUT = 4
+
+
+class LibraryNotBuilt(RuntimeError):
+    pass
+
+
+class PkvError(RuntimeError):
+    def __init__(self, code: int, message: str):
+        super().__init__(f"pkv error {code}: {message}")
+        self.code = code
+
+
+class PoolLayout(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in
+                ("num_blocks", "num_kv_heads", "block_size", "head_dim", "bits", "group_size")]
+
+
+class DecodeParams(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in
+                ("num_seqs", "num_q_heads", "n_query", "max_blocks_per_seq", "partition_tokens")]
+
+
+class Plan(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in
+                ("partition_tokens", "max_partitions", "chunk_rows", "sm_count", "threads_per_cta",
+                 "smem_bytes")] + [("workspace_bytes", ctypes.c_size_t)]
+
+
+_lib = None
+
+
+def load_library(path: Optional[str] = None) -> ctypes.CDLL:
+    """Loads (once) and returns the library with its prototypes declared."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    path = path or LIB_PATH
+    if not os.path.exists(path):
+        raise LibraryNotBuilt(f"{path} is missing: run __graft_entry__.build() or "
+                              "python -m quantized_kv_decode_partial_gb300.build")
+    lib = ctypes.CDLL(path)
+    P, I32, SZ, F = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t, ctypes.c_float
+    lib.pkv_make_plan.argtypes = [ctypes.POINTER(PoolLayout), ctypes.POINTER(DecodeParams), I32, ctypes.POINTER(Plan)]
+    lib.pkv_make_plan.restype = ctypes.c_int
+    lib.pkv_plan_for_current_device.argtypes = [ctypes.POINTER(PoolLayout), ctypes.POINTER(DecodeParams),
+                                                ctypes.POINTER(Plan)]
+    lib.pkv_plan_for_current_device.restype = ctypes.c_int
+    lib.pkv_paged_decode_attention.argtypes = [ctypes.POINTER(PoolLayout), ctypes.POINTER(DecodeParams),
+                                               P, P, P, P, P, P, P, P, P, F, P, P, SZ, P, P]
+    lib.pkv_paged_decode_attention.restype = ctypes.c_int
+    lib.pkv_paged_decode_partial.argtypes = lib.pkv_paged_decode_attention.argtypes
+    lib.pkv_paged_decode_partial.restype = ctypes.c_int
+    lib.pkv_merge_partitions.argtypes = [ctypes.POINTER(PoolLayout), ctypes.POINTER(DecodeParams), P, P, SZ, P,
+                                         P, P]
+    lib.pkv_merge_partitions.restype = ctypes.c_int
+    lib.pkv_paged_gather.argtypes = [P, I32, I32, I32, I32, P, P, I32, I32, I32, P, P, P]
+    lib.pkv_paged_gather.restype = ctypes.c_int
+    lib.pkv_strerror.argtypes = [ctypes.c_int]
+    lib.pkv_strerror.restype = ctypes.c_char_p
+    lib.pkv_last_cuda_error.argtypes = []
+    lib.pkv_last_cuda_error.restype = ctypes.c_char_p
+    lib.pkv_version.argtypes = []
+    lib.pkv_version.restype = ctypes.c_int
+    if path == LIB_PATH:
+        _lib = lib
+    return lib
+
+
+def _check(rc: int, lib) -> None:
+    if rc != PKV_OK:
+        msg = lib.pkv_strerror(rc).decode()
+        if rc == PKV_ERR_CUDA:
+            msg += ": " + lib.pkv_last_cuda_error().decode()
+        raise PkvError(rc, msg)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def layout_for(k_pool: torch.Tensor, head_dim: int, bits: int, group_size: int = 64) -> PoolLayout:
+    nb, hk, bs, _ = k_pool.shape
+    return PoolLayout(nb, hk, bs, head_dim, bits, group_size)
+
+
+def make_plan(layout: PoolLayout, params: DecodeParams, sm_count: Optional[int] = None) -> Plan:
+    """The library's plan (partition size, workspace bytes) for these shapes."""
+    lib = load_library()
+    plan = Plan()
+    if sm_count is None:
+        rc = lib.pkv_plan_for_current_device(ctypes.byref(layout), ctypes.byref(params), ctypes.byref(plan))
+    else:
+        rc = lib.pkv_make_plan(ctypes.byref(layout), ctypes.byref(params), sm_count, ctypes.byref(plan))
+    _check(rc, lib)
+    return plan
+
+
+def paged_decode_attention(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+                           block_tables: torch.Tensor, seq_lens: torch.Tensor, scale: float, *,
+                           bits: int = 16, group_size: int = 64,
+                           k_scales: Optional[torch.Tensor] = None, k_biases: Optional[torch.Tensor] = None,
+                           v_scales: Optional[torch.Tensor] = None, v_biases: Optional[torch.Tensor] = None,
+                           partition_tokens: int = 0, out: Optional[torch.Tensor] = None,
+                           workspace: Optional[torch.Tensor] = None,
+                           error_flag: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Decode attention over a paged cache (see include/pkv_decode.h).
+
+    q bf16 [B, HQ, N, D]; pools bf16 [NB, HK, BS, D] (bits=16) or int32 code
+    words [NB, HK, BS, D*bits/32] with bf16 scale/bias planes [NB, HK, BS, D/64];
+    block_tables int32 [B, max_blocks]; seq_lens int32 [B]. Runs on the current
+    CUDA stream of q's device and returns bf16 [B, HQ, N, D].
+    """
+    lib = load_library()
+    B, HQ, N, D = q.shape
+    layout = layout_for(k_pool, D, bits, group_size)
+    params = DecodeParams(B, HQ, N, block_tables.shape[1], partition_tokens)
+    with torch.cuda.device(q.device):
+        plan = make_plan(layout, params)
+        if out is None:
+            out = torch.empty_like(q)
+        if workspace is None and plan.workspace_bytes:
+            workspace = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=q.device)
+        ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+        rc = lib.pkv_paged_decode_attention(
+            ctypes.byref(layout), ctypes.byref(params), _ptr(q), _ptr(k_pool), _ptr(v_pool),
+            _ptr(k_scales), _ptr(k_biases), _ptr(v_scales), _ptr(v_biases), _ptr(block_tables),
+            _ptr(seq_lens), float(scale), _ptr(out), _ptr(workspace), ws_bytes, _ptr(error_flag), stream)
+    _check(rc, lib)
+    return out
+
+
+def paged_decode_passes(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+                        block_tables: torch.Tensor, seq_lens: torch.Tensor, scale: float, *, passes: str,
+                        bits: int = 16, group_size: int = 64, k_scales=None, k_biases=None, v_scales=None,
+                        v_biases=None, partition_tokens: int = 0, out: Optional[torch.Tensor] = None,
+                        workspace: Optional[torch.Tensor] = None,
+                        error_flag: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """One pass of the decode: ``passes="partial"`` (pkv_paged_decode_partial) or
+    ``"merge"`` (pkv_merge_partitions). ``out`` and, with more than one
+    partition, ``workspace`` must be given so the two calls share them."""
+    lib = load_library()
+    B, HQ, N, D = q.shape
+    layout = layout_for(k_pool, D, bits, group_size)
+    params = DecodeParams(B, HQ, N, block_tables.shape[1], partition_tokens)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    with torch.cuda.device(q.device):
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+        if passes == "partial":
+            rc = lib.pkv_paged_decode_partial(
+                ctypes.byref(layout), ctypes.byref(params), _ptr(q), _ptr(k_pool), _ptr(v_pool),
+                _ptr(k_scales), _ptr(k_biases), _ptr(v_scales), _ptr(v_biases), _ptr(block_tables),
+                _ptr(seq_lens), float(scale), _ptr(out), _ptr(workspace), ws_bytes, _ptr(error_flag), stream)
+        elif passes == "merge":
+            rc = lib.pkv_merge_partitions(ctypes.byref(layout), ctypes.byref(params), _ptr(seq_lens),
+                                          _ptr(workspace), ws_bytes, _ptr(out), _ptr(error_flag), stream)
+        else:
+            raise ValueError(passes)
+    _check(rc, lib)
+    return out
+
+
+def paged_gather(pool: torch.Tensor, block_tables: torch.Tensor, seq_lens: torch.Tensor, max_len: int,
+                 out: Optional[torch.Tensor] = None, error_flag: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Bit-exact gather of one pool plane [NB, HK, BS, W] into [B, HK, max_len, W]."""
+    lib = load_library()
+    nb, hk, bs = pool.shape[:3]
+    row_bytes = pool[0, 0, 0].numel() * pool.element_size()
+    B = block_tables.shape[0]
+    if out is None:
+        out = torch.zeros((B, hk, max_len) + tuple(pool.shape[3:]), dtype=pool.dtype, device=pool.device)
+    with torch.cuda.device(pool.device):
+        stream = torch.cuda.current_stream(pool.device).cuda_stream
+        rc = lib.pkv_paged_gather(_ptr(pool), nb, hk, bs, row_bytes, _ptr(block_tables), _ptr(seq_lens), B,
+                                  block_tables.shape[1], max_len, _ptr(out), _ptr(error_flag), stream)
+    _check(rc, lib)
+    return out

@@ -1,0 +1,276 @@
+// Device helpers shared by the paged decode kernels: inline PTX for mbarriers,
+// TMA / bulk copies, ldmatrix, warp-level MMA and movmatrix, plus the kernel
+// parameter blocks. sm_103a only.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pkv {
+
+constexpr int kDevErrBadBlock = 1;
+constexpr int kDevErrBadSeqLen = 2;
+constexpr int kDevErrTimeout = 4;
+
+// Upper bound of one pipeline wait before the kernel gives up (nanoseconds).
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;
+
+struct PartialParams {
+  const __nv_bfloat16* q;     // [B, HQ, N, D]
+  const int32_t* block_tables;  // [B, max_blocks]
+  const int32_t* seq_lens;    // [B]
+  const __nv_bfloat16* k_scales;  // [NB, HK, BS, D/64]   (affine pages)
+  const __nv_bfloat16* k_biases;
+  const __nv_bfloat16* v_scales;
+  const __nv_bfloat16* v_biases;
+  __nv_bfloat16* out;   // [B, HQ, N, D], written directly with one partition
+  float* ws_o;          // [B*HQ*N, max_partitions, D]
+  float* ws_ml;         // [B*HQ*N, max_partitions, 2]  (running max in log2 units, normaliser)
+  int32_t* error_flag;  // optional
+  int num_blocks, num_kv_heads, block_size, max_blocks;
+  int num_q_heads, n_query, nq;  // nq = (HQ/HK) * n_query rows served per KV head
+  int partition_tokens, max_partitions;
+  float score_scale;  // softmax scale * log2(e)
+};
+
+struct MergeParams {
+  const float* ws_o;
+  const float* ws_ml;
+  const int32_t* seq_lens;
+  __nv_bfloat16* out;
+  int32_t* error_flag;
+  int rows_per_seq;  // HQ * N
+  int n_query, head_dim, max_len, partition_tokens, max_partitions;
+};
+
+struct GatherParams {
+  const uint8_t* pool;
+  const int32_t* block_tables;
+  const int32_t* seq_lens;
+  uint8_t* out;
+  int32_t* error_flag;
+  int num_blocks, num_kv_heads, block_size, row_words, max_blocks, max_len;
+};
+
+// ---------------------------------------------------------------------------
+// small PTX wrappers
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long global_timer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// Waits for the phase with the given parity. Gives up when `abort_flag` is set
+// by another warp or after kWaitLimitNs, in which case it raises the abort
+// flag and the timeout error bit. Returns true when the phase completed.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  volatile int* abort_flag, int32_t* error_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long start = global_timer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (global_timer_ns() - start > kWaitLimitNs) {
+      *abort_flag = 1;
+      if (error_flag) atomicOr(error_flag, kDevErrTimeout);
+      return false;
+    }
+  }
+}
+
+// Warp-collective form of mbar_wait_bounded: every lane observes the phase, and
+// the give-up decision is taken by lane 0 and shared, so the warp never splits.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                               int32_t* error_flag) {
+  bool done = mbar_try_wait(bar, parity);
+  if (__all_sync(0xffffffffu, done)) return true;
+  const bool leader = (threadIdx.x & 31) == 0;
+  const unsigned long long start = leader ? global_timer_ns() : 0ull;
+  while (true) {
+    if (!done) done = mbar_try_wait(bar, parity);
+    int stop = 0;
+    if (leader) {
+      if (*abort_flag) {
+        stop = 1;
+      } else if (global_timer_ns() - start > kWaitLimitNs) {
+        *abort_flag = 1;
+        if (error_flag) atomicOr(error_flag, kDevErrTimeout);
+        stop = 1;
+      }
+    }
+    stop = __shfl_sync(0xffffffffu, stop, 0);
+    if (__all_sync(0xffffffffu, done)) return true;
+    if (stop) return false;
+  }
+}
+
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t policy;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
+  return policy;
+}
+
+// 2-D tiled TMA load of one box into shared memory, completing on `bar`.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+// 1-D bulk copy global -> shared (addresses and size multiples of 16 bytes).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
+                                          uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+
+// D = A * B + D, m16n8k16, bf16 inputs, f32 accumulators.
+__device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// D = A * B + D, m16n8k16, fp16 inputs, f32 accumulators.
+__device__ __forceinline__ void mma_f16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                        uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Transpose an 8x8 matrix of 16-bit elements held one row-pair per thread.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Packs (lo, hi) into a bf16x2 word, round to nearest even; lo in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Packs (lo, hi) into an fp16x2 word, round to nearest even; lo in the low half.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ float f16_lo_to_f32(uint32_t x) {
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(x & 0xFFFFu)));
+}
+__device__ __forceinline__ float f16_hi_to_f32(uint32_t x) {
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(x >> 16)));
+}
+
+// Two 4-bit fields at bits [0,4) and [16,20) of x as the fp16 pair
+// (1024 + lo_field, 1024 + hi_field): 0x6400 is fp16 1024.0, whose ulp is 1.
+__device__ __forceinline__ uint32_t nibbles_to_f16x2_biased(uint32_t x) {
+  return (x & 0x000F000Fu) | 0x64006400u;  // one LOP3
+}
+
+// Bytes `b0` and `b1` of x as the fp16 pair (1024 + byte b0, 1024 + byte b1): one PRMT
+// that interleaves the code bytes with the 0x64 exponent byte.
+template <int SEL>
+__device__ __forceinline__ uint32_t bytes_to_f16x2_biased(uint32_t x) {
+  return __byte_perm(x, 0x64646464u, SEL);
+}
+
+__device__ __forceinline__ float bf16_lo_to_f32(uint32_t x) { return __uint_as_float(x << 16); }
+__device__ __forceinline__ float bf16_hi_to_f32(uint32_t x) { return __uint_as_float(x & 0xFFFF0000u); }
+
+// Two 4-bit fields at bits [0,4) and [16,20) of x, turned into the bf16 pair
+// (128 + lo_field, 128 + hi_field): 0x4300 is bf16 128.0 and a field below 16
+// lands in its low mantissa bits, so each half is exact.
+__device__ __forceinline__ uint32_t nibbles_to_bf16x2_biased(uint32_t x) {
+  return (x & 0x000F000Fu) | 0x43004300u;  // one LOP3
+}
+
+// Shared-memory address of 16-byte chunk `chunk` of row `row` inside a TMA box
+// written with the 128-byte (rows of 128 B) or 64-byte (rows of 64 B) swizzle.
+template <int RB>
+__device__ __forceinline__ uint32_t swizzled(uint32_t box_base, int row, int chunk) {
+  static_assert(RB == 128 || RB == 64, "box rows of 64 or 128 bytes");
+  if constexpr (RB == 128) {
+    return box_base + row * 128 + ((chunk ^ (row & 7)) << 4);
+  } else {
+    return box_base + row * 64 + ((chunk ^ ((row >> 1) & 3)) << 4);
+  }
+}
+
+}  // namespace pkv

@@ -1,0 +1,36 @@
+// Internal launch interface between the C-ABI host code and the kernel
+// translation units (one per page format, compiled in parallel).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "pkv_common.cuh"
+
+namespace pkv {
+
+// Static shape of one partial-kernel instantiation.
+struct PartialInfo {
+  bool exists;
+  int threads;
+  int smem_bytes;
+  int chunk_rows;
+  int box_row_bytes;  // bytes of one TMA box row (64 or 128)
+  int tensor_elem_bytes;  // element size of the pool tensor maps (2 bf16, 1 affine codes)
+};
+
+PartialInfo partial_info_bf16(int head_dim, int ntiles);
+PartialInfo partial_info_u4(int head_dim, int ntiles);
+PartialInfo partial_info_u8(int head_dim, int ntiles);
+
+cudaError_t launch_partial_bf16(int head_dim, int ntiles, const PartialParams& p, const CUtensorMap& tk,
+                                const CUtensorMap& tv, dim3 grid, cudaStream_t stream);
+cudaError_t launch_partial_u4(int head_dim, int ntiles, const PartialParams& p, const CUtensorMap& tk,
+                              const CUtensorMap& tv, dim3 grid, cudaStream_t stream);
+cudaError_t launch_partial_u8(int head_dim, int ntiles, const PartialParams& p, const CUtensorMap& tk,
+                              const CUtensorMap& tv, dim3 grid, cudaStream_t stream);
+
+cudaError_t launch_merge(const MergeParams& p, int rows, cudaStream_t stream);
+cudaError_t launch_gather(const GatherParams& p, int num_seqs, cudaStream_t stream);
+
+}  // namespace pkv

@@ -1,0 +1,96 @@
+// Merge pass (log-sum-exp combination of partition states) and the bit-exact
+// block-table gather.
+#include "pkv_launch.h"
+
+namespace pkv {
+
+// One CTA per output row (sequence, query head, query index); each thread owns
+// four consecutive head dims. The partition states hold the running maximum in
+// log2 units, the normaliser and the unnormalised output; partitions whose
+// maximum is -inf saw no visible key and are skipped (kvq4-decode.ts and
+// multi-query.ts merge kernels). Output = sum_p 2^(m_p-M) o_p / sum_p 2^(m_p-M) l_p.
+__global__ void __launch_bounds__(64) pkv_merge_kernel(const __grid_constant__ MergeParams p) {
+  const int row = blockIdx.x;
+  const int d = threadIdx.x * 4;
+  if (d >= p.head_dim) return;
+  const int b = row / p.rows_per_seq;
+  const int len = p.seq_lens[b];
+  __nv_bfloat162* out = reinterpret_cast<__nv_bfloat162*>(p.out + static_cast<size_t>(row) * p.head_dim + d);
+  if (len < p.n_query || len > p.max_len) {  // flagged by the partial pass
+    out[0] = __floats2bfloat162_rn(0.f, 0.f);
+    out[1] = __floats2bfloat162_rn(0.f, 0.f);
+    return;
+  }
+  const int np = (len + p.partition_tokens - 1) / p.partition_tokens;
+  const float2* ml = reinterpret_cast<const float2*>(p.ws_ml) + static_cast<size_t>(row) * p.max_partitions;
+  const float4* ob = reinterpret_cast<const float4*>(p.ws_o + static_cast<size_t>(row) * p.max_partitions * p.head_dim + d);
+  const int ostride = p.head_dim / 4;
+  float M = -INFINITY;
+  for (int i = 0; i < np; ++i) M = fmaxf(M, ml[i].x);
+  float den = 0.f, n0 = 0.f, n1 = 0.f, n2 = 0.f, n3 = 0.f;
+  if (M != -INFINITY) {
+    for (int i = 0; i < np; ++i) {
+      const float2 s = ml[i];
+      if (s.x == -INFINITY) continue;
+      const float w = fast_exp2(s.x - M);
+      const float4 v = ob[static_cast<size_t>(i) * ostride];
+      den = fmaf(w, s.y, den);
+      n0 = fmaf(w, v.x, n0);
+      n1 = fmaf(w, v.y, n1);
+      n2 = fmaf(w, v.z, n2);
+      n3 = fmaf(w, v.w, n3);
+    }
+  }
+  if (den > 0.f) {
+    out[0] = __floats2bfloat162_rn(n0 / den, n1 / den);
+    out[1] = __floats2bfloat162_rn(n2 / den, n3 / den);
+  } else {
+    out[0] = __floats2bfloat162_rn(0.f, 0.f);
+    out[1] = __floats2bfloat162_rn(0.f, 0.f);
+  }
+}
+
+cudaError_t launch_merge(const MergeParams& p, int rows, cudaStream_t stream) {
+  const int threads = p.head_dim / 4 < 32 ? 32 : p.head_dim / 4;
+  pkv_merge_kernel<<<rows, threads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+// Grid (row blocks, KV head, sequence); one warp per logical row, lanes copy
+// 32-bit words. Bytes are copied unchanged, so the result is bit-exact.
+constexpr int kGatherRowsPerCta = 32;
+
+__global__ void __launch_bounds__(256) pkv_gather_kernel(const __grid_constant__ GatherParams p) {
+  const int b = blockIdx.z, h = blockIdx.y;
+  const int len = p.seq_lens[b];
+  if (len < 0 || len > p.max_len || len > p.max_blocks * p.block_size) {
+    if (threadIdx.x == 0 && blockIdx.x == 0 && h == 0 && p.error_flag) atomicOr(p.error_flag, kDevErrBadSeqLen);
+    return;
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row_begin = blockIdx.x * kGatherRowsPerCta;
+  const uint32_t* pool = reinterpret_cast<const uint32_t*>(p.pool);
+  uint32_t* out = reinterpret_cast<uint32_t*>(p.out);
+  for (int r = warp; r < kGatherRowsPerCta; r += blockDim.x >> 5) {
+    const int tok = row_begin + r;
+    if (tok >= len) break;
+    const int phys = p.block_tables[static_cast<size_t>(b) * p.max_blocks + tok / p.block_size];
+    if (static_cast<unsigned>(phys) >= static_cast<unsigned>(p.num_blocks)) {
+      if (lane == 0 && p.error_flag) atomicOr(p.error_flag, kDevErrBadBlock);
+      continue;
+    }
+    const uint32_t* src =
+        pool + ((static_cast<size_t>(phys) * p.num_kv_heads + h) * p.block_size + tok % p.block_size) * p.row_words;
+    uint32_t* dst = out + ((static_cast<size_t>(b) * p.num_kv_heads + h) * p.max_len + tok) * p.row_words;
+    for (int w = lane; w < p.row_words; w += 32) dst[w] = src[w];
+  }
+}
+
+cudaError_t launch_gather(const GatherParams& p, int num_seqs, cudaStream_t stream) {
+  if (p.max_len == 0) return cudaSuccess;
+  dim3 grid((p.max_len + kGatherRowsPerCta - 1) / kGatherRowsPerCta, p.num_kv_heads, num_seqs);
+  pkv_gather_kernel<<<grid, 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace pkv

@@ -1,0 +1,633 @@
+// Partial pass of paged decode attention (one CTA per sequence x KV head x
+// partition) for bf16 pages and affine 4-/8-bit pages, sm_103a.
+//
+// What one CTA computes is the per-partition state of the pages' partial
+// kernels ("@mlx-bun/inference 0.0.0-stage -> 1.0.0", kernels/attention/paged.ts
+// ``paged_attention_partial`` / ``paged_attention_affine_partial``;
+// kvq4-decode.ts partial kernel): for every query row served by its KV head, the
+// running maximum of the scores, the normaliser and the unnormalised output over
+// the partition's visible keys. With a single partition the CTA finishes the
+// softmax itself and writes bf16 output.
+//
+// Design (GB300):
+//  * One producer warp streams the partition's K/V rows in chunks of 16 (bf16)
+//    or 32 (affine) rows. The block table is resolved once per chunk, by the
+//    producer, 32 entries per coalesced load. Each chunk of one page and KV head
+//    is contiguous in the pool, so it travels as 2-D TMA boxes (rows of 64 or
+//    128 bytes, hardware-swizzled so the ldmatrix reads below are free of bank
+//    conflicts) plus 1-D bulk copies of the affine scale/bias rows, into a ring
+//    of shared-memory stages guarded by mbarriers.
+//  * Four consumer warps take chunks round-robin. Each K/V row in shared memory
+//    is read once and multiplied against all REP*N query rows of its KV head
+//    (GQA reuse) with warp-level tensor-core MMA (m16n8k16, bf16 in, f32 out):
+//    S^T = K Q^T puts 16 keys on the M side and 8 query rows on N, and the
+//    probabilities are transposed in registers (movmatrix) into the B operand
+//    of O^T += V^T P^T. The online softmax (running max, normaliser, rescale)
+//    runs in f32 on the accumulators in base 2 (the softmax scale times log2 e
+//    is applied to the f32 scores; q itself is never re-rounded).
+//  * Affine pages never dequantise element by element. A code c enters the MMA
+//    as the exact bf16 value 128 + c, made by OR-ing the nibble into the
+//    mantissa of 128.0 (one LOP3 per two codes); 8-bit codes are split into
+//    their two nibbles, the high one weighted by 16. Per 64-dim group g:
+//        q.k = s_g * (sum_d q_d (128 + c_d)) + (b_g - 128 s_g) * sum_d q_d
+//    (offset 128 + 16*128 for 8-bit codes). The values go through fp16 MMA:
+//    a code enters as the exact fp16 value 1024 + c (nibble OR-ed into 1024.0,
+//    or a code byte permuted next to the 0x64 exponent byte: one PRMT per two
+//    codes), and with P'_g = p * s_g rounded to fp16,
+//        o_d = sum_t P'_g(t) (1024 + c_td) - 1024 sum_t P'_g(t) + sum_t p(t) b_g(t).
+//    The scale/bias terms are per key and per group, so they cost a few FMAs per
+//    key instead of two per element.
+//  * Rows at or past seq_len in the last page are masked before they can reach
+//    an accumulator (scores set to -inf by select; their V operand or V scale
+//    zeroed), so stale storage may hold anything, NaN included.
+#pragma once
+
+#include "pkv_common.cuh"
+
+namespace pkv {
+
+template <int BITS, int D, int NT>
+struct PartialCfg {
+  static constexpr bool kQuant = BITS != 16;
+  static constexpr int kCh = kQuant ? 32 : 16;                     // rows per stage
+  static constexpr int kElemBytes = kQuant ? 1 : 2;                // tensor-map element size
+  static constexpr int kRowBytes = kQuant ? D * BITS / 8 : 2 * D;  // stored bytes of one row
+  static constexpr int kRB = kRowBytes >= 128 ? 128 : kRowBytes;   // bytes of one box row
+  static constexpr int kBoxes = kRowBytes / kRB;
+  static constexpr int kBoxBytes = kCh * kRB;
+  static constexpr int kPlaneBytes = kBoxes * kBoxBytes;
+  static constexpr int kGroups = D / 64;
+  static constexpr int kSbBytes = kQuant ? kCh * kGroups * 2 : 0;  // one scale or bias plane
+  static constexpr int kTxBytes = 2 * kPlaneBytes + 4 * kSbBytes;
+  static constexpr int kStageBytes = (kTxBytes + 1023) / 1024 * 1024;
+  static constexpr int kWarps = 4;  // consumer warps
+  static constexpr int kThreads = (kWarps + 1) * 32;
+  static constexpr int kStages = (100 * 1024) / kStageBytes;
+  static constexpr int kNqp = 8 * NT;       // query rows per warp (padded)
+  static constexpr int kMt = D / 16;        // 16-dim m-tiles of O^T
+  static constexpr int kKs = D / 16;        // k16 steps of Q K^T
+  static constexpr int kTiles = kCh / 16;   // 16-key tiles per stage
+  static constexpr int kCombineBytes = kWarps * kNqp * (D + 2) * 4;
+  static constexpr int kDataBytes =
+      kStages * kStageBytes > kCombineBytes ? kStages * kStageBytes : kCombineBytes;
+  static constexpr int kBarrierBytes = 1024;
+  static constexpr int kSmemBytes = kDataBytes + kBarrierBytes + 1024;  // + alignment slack
+  static constexpr float kOffsetK = BITS == 8 ? 2176.f : 128.f;  // code bias inside the K-side MMA (bf16)
+  static constexpr float kOffsetV = 1024.f;                        // code bias inside the V-side MMA (fp16)
+
+  static_assert(kRB == 128 || kRB == 64, "box rows of 64 or 128 bytes");
+  static_assert(kRowBytes % kRB == 0, "whole boxes per row");
+  static_assert(kStages >= 2 && kStages * 20 <= kBarrierBytes, "stage count");
+  static_assert(!kQuant || D % 64 == 0, "affine head dims are whole 64-dim groups");
+};
+
+// Physical head dim held by row `half` (0: g, 1: g + 8) of O^T m-tile `mt`.
+template <int BITS>
+__device__ __forceinline__ int out_dim(int mt, int half, int g) {
+  if constexpr (BITS == 16) {
+    return 16 * mt + 8 * half + g;
+  } else if constexpr (BITS == 4) {
+    return 64 * (mt >> 2) + 32 * half + 4 * g + (mt & 3);
+  } else {
+    return 64 * (mt >> 2) + 32 * ((mt >> 1) & 1) + 16 * half + 2 * g + (mt & 1);
+  }
+}
+
+// Physical head dims feeding B-fragment register `reg` (0 or 1) of k-step kk for
+// the thread with tid_in_group t: (low half, high half).
+template <int BITS>
+__device__ __forceinline__ void q_dims(int kk, int reg, int t, int& d_lo, int& d_hi) {
+  if constexpr (BITS == 16) {
+    d_lo = 16 * kk + 8 * reg + 2 * t;
+    d_hi = d_lo + 1;
+  } else if constexpr (BITS == 4) {
+    const int grp = kk >> 2, cc = (kk >> 1) & 1, s = kk & 1;
+    const int base = 64 * grp + 32 * cc + 8 * t + 2 * s + reg;
+    d_lo = base;
+    d_hi = base + 4;
+  } else {
+    const int grp = kk >> 2, c = kk & 3;
+    const int base = 64 * grp + 16 * c + 4 * t + reg;
+    d_lo = base;
+    d_hi = base + 2;
+  }
+}
+
+__device__ __forceinline__ uint32_t bf16x2_times16(uint32_t x) {
+  __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&x);
+  v = __hmul2(v, __floats2bfloat162_rn(16.f, 16.f));
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+template <int BITS, int D, int NT>
+__global__ void __maxnreg__(200)
+    pkv_partial_kernel(const __grid_constant__ PartialParams p, const __grid_constant__ CUtensorMap tmap_k,
+                       const __grid_constant__ CUtensorMap tmap_v) {
+  using C = PartialCfg<BITS, D, NT>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + C::kDataBytes);
+  uint64_t* empty_bar = full_bar + C::kStages;
+  int* stage_ok = reinterpret_cast<int*>(empty_bar + C::kStages);
+  volatile int* abort_flag = stage_ok + C::kStages;
+
+  const int part = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const int N = p.n_query;
+  const int rep = p.nq / N;
+  const size_t row0 = (static_cast<size_t>(b) * p.num_q_heads + static_cast<size_t>(hk) * rep) * N;
+  const bool single = p.max_partitions == 1;
+  const int len = p.seq_lens[b];
+
+  if (len < N || len > p.max_blocks * p.block_size) {
+    if (threadIdx.x == 0 && part == 0 && p.error_flag) atomicOr(p.error_flag, kDevErrBadSeqLen);
+    if (single) {
+      for (int i = threadIdx.x; i < p.nq * D; i += C::kThreads) p.out[row0 * D + i] = __float2bfloat16_rn(0.f);
+    }
+    return;
+  }
+  const int t0 = part * p.partition_tokens;
+  if (t0 >= len) return;  // empty partition; the merge pass never reads it
+  const int t_end = min(len, t0 + p.partition_tokens);
+  const int nchunks = (t_end - t0 + C::kCh - 1) / C::kCh;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(smem_addr(&full_bar[s]), 1);
+      mbar_init(smem_addr(&empty_bar[s]), 1);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  // O^T accumulators and softmax state (consumer warps).
+  float o[C::kMt][NT][4];
+  float m_run[NT][2], l_run[NT][2];
+  float corr_v[C::kQuant ? C::kGroups : 1][NT][2];
+
+  if (warp == C::kWarps) {
+    // ------------------------------------------------------------------ producer
+    const uint64_t policy = l2_evict_first_policy();
+    const int32_t* table = p.block_tables + static_cast<size_t>(b) * p.max_blocks;
+    int issued = 0, stop = 0;
+    for (int j0 = 0; j0 < nchunks && !stop; j0 += 32) {
+      const int j = j0 + lane;
+      int phys = 0;
+      if (j < nchunks) phys = __ldg(table + (t0 + j * C::kCh) / p.block_size);
+      const int cnt = min(32, nchunks - j0);
+      for (int i = 0; i < cnt; ++i) {
+        const int ph = __shfl_sync(0xffffffffu, phys, i);
+        if (lane == 0) {
+          const int jj = j0 + i, s = jj % C::kStages;
+          bool go = true;
+          if (jj >= C::kStages)
+            go = mbar_wait_bounded(smem_addr(&empty_bar[s]), ((jj / C::kStages) - 1) & 1, abort_flag,
+                                   p.error_flag);
+          if (go) {
+            const bool ok = static_cast<unsigned>(ph) < static_cast<unsigned>(p.num_blocks);
+            stage_ok[s] = ok ? 1 : 0;
+            const uint32_t fb = smem_addr(&full_bar[s]);
+            if (ok) {
+              fence_proxy_async_smem();
+              mbar_arrive_expect_tx(fb, C::kTxBytes);
+              const int row = (ph * p.num_kv_heads + hk) * p.block_size + (t0 + jj * C::kCh) % p.block_size;
+              const uint32_t st = smem_addr(smem + s * C::kStageBytes);
+#pragma unroll
+              for (int bx = 0; bx < C::kBoxes; ++bx) {
+                const int x = bx * (C::kRB / C::kElemBytes);
+                tma_load_2d(st + bx * C::kBoxBytes, &tmap_k, x, row, fb, policy);
+                tma_load_2d(st + C::kPlaneBytes + bx * C::kBoxBytes, &tmap_v, x, row, fb, policy);
+              }
+              if constexpr (C::kQuant) {
+                const size_t so = static_cast<size_t>(row) * C::kGroups;
+                const uint32_t sb = st + 2 * C::kPlaneBytes;
+                bulk_load(sb, p.k_scales + so, C::kSbBytes, fb, policy);
+                bulk_load(sb + C::kSbBytes, p.k_biases + so, C::kSbBytes, fb, policy);
+                bulk_load(sb + 2 * C::kSbBytes, p.v_scales + so, C::kSbBytes, fb, policy);
+                bulk_load(sb + 3 * C::kSbBytes, p.v_biases + so, C::kSbBytes, fb, policy);
+              }
+            } else {
+              if (p.error_flag) atomicOr(p.error_flag, kDevErrBadBlock);
+              mbar_arrive(fb);
+            }
+            issued = jj + 1;
+          }
+        }
+        __syncwarp();
+        stop = __shfl_sync(0xffffffffu, static_cast<int>(*abort_flag), 0);  // one decision for the warp
+        if (stop) break;
+      }
+    }
+    if (lane == 0 && *abort_flag) {
+      // Let every copy still in flight land before the CTA's shared memory is reused.
+      for (int s = 0; s < C::kStages && s < issued; ++s) {
+        const int last = s + ((issued - 1 - s) / C::kStages) * C::kStages;
+        const uint32_t bar = smem_addr(&full_bar[s]);
+        const unsigned long long start = global_timer_ns();
+        while (!mbar_try_wait(bar, (last / C::kStages) & 1) && global_timer_ns() - start < kWaitLimitNs) {
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------------ consumers
+    // B fragments of Q^T for every k-step, rows r = 8*nt + g of this KV head.
+    uint32_t qf[C::kKs][NT][2];
+    const uint16_t* qrows = reinterpret_cast<const uint16_t*>(p.q) + row0 * D;
+#pragma unroll
+    for (int kk = 0; kk < C::kKs; ++kk) {
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const int r = 8 * nt + g;
+#pragma unroll
+        for (int reg = 0; reg < 2; ++reg) {
+          int dl, dh;
+          q_dims<BITS>(kk, reg, t, dl, dh);
+          uint32_t v = 0;
+          if (r < p.nq) {
+            v = static_cast<uint32_t>(__ldg(qrows + static_cast<size_t>(r) * D + dl)) |
+                (static_cast<uint32_t>(__ldg(qrows + static_cast<size_t>(r) * D + dh)) << 16);
+          }
+          qf[kk][nt][reg] = v;
+        }
+      }
+    }
+    // Per-group sums of q (columns 2t, 2t+1), through the same MMA path.
+    float qsum[C::kQuant ? C::kGroups : 1][NT][2];
+    if constexpr (C::kQuant) {
+      const uint32_t ones = 0x3F803F80u;  // bf16 (1.0, 1.0)
+#pragma unroll
+      for (int grp = 0; grp < C::kGroups; ++grp) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) mma_bf16(acc, ones, ones, ones, ones, qf[4 * grp + k][nt][0], qf[4 * grp + k][nt][1]);
+          qsum[grp][nt][0] = acc[0];
+          qsum[grp][nt][1] = acc[1];
+        }
+      }
+    }
+
+#pragma unroll
+    for (int mt = 0; mt < C::kMt; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[mt][nt][e] = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+      for (int e2 = 0; e2 < 2; ++e2) {
+        m_run[nt][e2] = -INFINITY;
+        l_run[nt][e2] = 0.f;
+#pragma unroll
+        for (int grp = 0; grp < (C::kQuant ? C::kGroups : 1); ++grp) corr_v[grp][nt][e2] = 0.f;
+      }
+    }
+
+    const int vis_base = len - N + 1;  // query row qi sees keys < vis_base + qi
+    // ldmatrix row/chunk of this lane: non-transposed (keys on M) and transposed (keys on K).
+    const int lrow_n = (lane & 7) + ((lane >> 3) & 1) * 8, lch_n = lane >> 4;
+    const int lrow_t = (lane & 7) + (lane >> 4) * 8, lch_t = (lane >> 3) & 1;
+
+    for (int jj = warp; jj < nchunks; jj += C::kWarps) {
+      const int s = jj % C::kStages;
+      if (!mbar_wait_warp(smem_addr(&full_bar[s]), (jj / C::kStages) & 1, abort_flag, p.error_flag)) break;
+      if (stage_ok[s]) {
+        const uint32_t kpl = smem_addr(smem + s * C::kStageBytes);
+        const uint32_t vpl = kpl + C::kPlaneBytes;
+        const __nv_bfloat16* sbp = reinterpret_cast<const __nv_bfloat16*>(smem + s * C::kStageBytes + 2 * C::kPlaneBytes);
+        const int kbase = t0 + jj * C::kCh;
+        const bool full_vis = kbase + C::kCh <= vis_base;
+        const bool stale = kbase + C::kCh > len;
+
+        // ---- scores x = (K q) * scale * log2(e), keys on rows
+        float x[C::kTiles][NT][4];
+#pragma unroll
+        for (int tile = 0; tile < C::kTiles; ++tile) {
+          float sacc[NT][4];
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sacc[nt][e] = 0.f;
+          const int lrow = tile * 16 + lrow_n;
+          if constexpr (BITS == 16) {
+#pragma unroll
+            for (int kk = 0; kk < C::kKs; ++kk) {
+              uint32_t a[4];
+              ldsm_x4(swizzled<C::kRB>(kpl + (kk >> 2) * C::kBoxBytes, lrow, (kk & 3) * 2 + lch_n), a);
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt) mma_bf16(sacc[nt], a[0], a[1], a[2], a[3], qf[kk][nt][0], qf[kk][nt][1]);
+            }
+          } else {
+            const __nv_bfloat16* ksp = sbp;
+            const __nv_bfloat16* kbp = sbp + C::kCh * C::kGroups;
+#pragma unroll
+            for (int grp = 0; grp < C::kGroups; ++grp) {
+              float sg[NT][4];
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) sg[nt][e] = 0.f;
+              if constexpr (BITS == 4) {
+                uint32_t xk[4];
+                ldsm_x4(swizzled<C::kRB>(kpl, lrow, 2 * grp + lch_n), xk);
+#pragma unroll
+                for (int cc = 0; cc < 2; ++cc) {
+#pragma unroll
+                  for (int sft = 0; sft < 2; ++sft) {
+                    const int kk = 4 * grp + 2 * cc + sft;
+                    const uint32_t a0 = nibbles_to_bf16x2_biased(xk[2 * cc] >> (8 * sft));
+                    const uint32_t a1 = nibbles_to_bf16x2_biased(xk[2 * cc + 1] >> (8 * sft));
+                    const uint32_t a2 = nibbles_to_bf16x2_biased(xk[2 * cc] >> (8 * sft + 4));
+                    const uint32_t a3 = nibbles_to_bf16x2_biased(xk[2 * cc + 1] >> (8 * sft + 4));
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) mma_bf16(sg[nt], a0, a1, a2, a3, qf[kk][nt][0], qf[kk][nt][1]);
+                  }
+                }
+              } else {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                  uint32_t xk[4];
+                  ldsm_x4(swizzled<C::kRB>(kpl + (grp >> 1) * C::kBoxBytes, lrow, (grp & 1) * 4 + 2 * h + lch_n), xk);
+#pragma unroll
+                  for (int cc = 0; cc < 2; ++cc) {
+                    const int kk = 4 * grp + 2 * h + cc;
+                    const uint32_t xg = xk[2 * cc], x8 = xk[2 * cc + 1];
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                      mma_bf16(sg[nt], nibbles_to_bf16x2_biased(xg), nibbles_to_bf16x2_biased(x8),
+                               nibbles_to_bf16x2_biased(xg >> 8), nibbles_to_bf16x2_biased(x8 >> 8),
+                               qf[kk][nt][0], qf[kk][nt][1]);
+                      mma_bf16(sg[nt], nibbles_to_bf16x2_biased(xg >> 4), nibbles_to_bf16x2_biased(x8 >> 4),
+                               nibbles_to_bf16x2_biased(xg >> 12), nibbles_to_bf16x2_biased(x8 >> 12),
+                               bf16x2_times16(qf[kk][nt][0]), bf16x2_times16(qf[kk][nt][1]));
+                    }
+                  }
+                }
+              }
+              // fold the affine terms of group grp for keys g and g + 8 of this tile
+              const int r_a = tile * 16 + g, r_b = r_a + 8;
+              const float ks0 = __bfloat162float(ksp[r_a * C::kGroups + grp]);
+              const float ks1 = __bfloat162float(ksp[r_b * C::kGroups + grp]);
+              const float kb0 = __bfloat162float(kbp[r_a * C::kGroups + grp]) - C::kOffsetK * ks0;
+              const float kb1 = __bfloat162float(kbp[r_b * C::kGroups + grp]) - C::kOffsetK * ks1;
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt) {
+                sacc[nt][0] = fmaf(ks0, sg[nt][0], fmaf(kb0, qsum[grp][nt][0], sacc[nt][0]));
+                sacc[nt][1] = fmaf(ks0, sg[nt][1], fmaf(kb0, qsum[grp][nt][1], sacc[nt][1]));
+                sacc[nt][2] = fmaf(ks1, sg[nt][2], fmaf(kb1, qsum[grp][nt][0], sacc[nt][2]));
+                sacc[nt][3] = fmaf(ks1, sg[nt][3], fmaf(kb1, qsum[grp][nt][1], sacc[nt][3]));
+              }
+            }
+          }
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) x[tile][nt][e] = sacc[nt][e] * p.score_scale;
+        }
+
+        // ---- causal tail and stale rows
+        if (!full_vis) {
+#pragma unroll
+          for (int tile = 0; tile < C::kTiles; ++tile)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int key = kbase + tile * 16 + g + 8 * (e >> 1);
+                const int qi = (8 * nt + 2 * t + (e & 1)) % N;
+                x[tile][nt][e] = key < vis_base + qi ? x[tile][nt][e] : -INFINITY;
+              }
+        }
+
+        // ---- online softmax (base 2)
+        float pr[C::kTiles][NT][4];
+        float corr[NT][2];
+        bool grew = false;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+          for (int e2 = 0; e2 < 2; ++e2) {
+            float mx = -INFINITY;
+#pragma unroll
+            for (int tile = 0; tile < C::kTiles; ++tile) mx = fmaxf(mx, fmaxf(x[tile][nt][e2], x[tile][nt][e2 + 2]));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+            const float mnew = fmaxf(m_run[nt][e2], mx);
+            const float muse = mnew == -INFINITY ? 0.f : mnew;
+            const float c = fast_exp2(m_run[nt][e2] - muse);
+            m_run[nt][e2] = mnew;
+            float ls = 0.f;
+#pragma unroll
+            for (int tile = 0; tile < C::kTiles; ++tile) {
+              pr[tile][nt][e2] = fast_exp2(x[tile][nt][e2] - muse);
+              pr[tile][nt][e2 + 2] = fast_exp2(x[tile][nt][e2 + 2] - muse);
+              ls += pr[tile][nt][e2] + pr[tile][nt][e2 + 2];
+            }
+            l_run[nt][e2] = fmaf(l_run[nt][e2], c, ls);
+            corr[nt][e2] = c;
+            grew |= c != 1.f;
+          }
+        }
+        if (__any_sync(0xffffffffu, grew)) {
+#pragma unroll
+          for (int mt = 0; mt < C::kMt; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) o[mt][nt][e] *= corr[nt][e & 1];
+          if constexpr (C::kQuant) {
+#pragma unroll
+            for (int grp = 0; grp < C::kGroups; ++grp)
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e2 = 0; e2 < 2; ++e2) corr_v[grp][nt][e2] *= corr[nt][e2];
+          }
+        }
+
+        // ---- O^T += V^T P^T
+#pragma unroll
+        for (int tile = 0; tile < C::kTiles; ++tile) {
+          const int lrow = tile * 16 + lrow_t;
+          if constexpr (BITS == 16) {
+            uint32_t pb[NT][2];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              pb[nt][0] = movmatrix_trans(pack_bf16x2(pr[tile][nt][0], pr[tile][nt][1]));
+              pb[nt][1] = movmatrix_trans(pack_bf16x2(pr[tile][nt][2], pr[tile][nt][3]));
+            }
+            uint32_t m01 = 0xffffffffu, m23 = 0xffffffffu;
+            if (stale) {
+              const int k0 = kbase + tile * 16 + 2 * t;
+              m01 = (k0 < len ? 0x0000ffffu : 0u) | (k0 + 1 < len ? 0xffff0000u : 0u);
+              m23 = (k0 + 8 < len ? 0x0000ffffu : 0u) | (k0 + 9 < len ? 0xffff0000u : 0u);
+            }
+#pragma unroll
+            for (int mt = 0; mt < C::kMt; ++mt) {
+              uint32_t a[4];
+              ldsm_x4_t(swizzled<C::kRB>(vpl + (mt >> 2) * C::kBoxBytes, lrow, (mt & 3) * 2 + lch_t), a);
+              a[0] &= m01;
+              a[1] &= m01;
+              a[2] &= m23;
+              a[3] &= m23;
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt) mma_bf16(o[mt][nt], a[0], a[1], a[2], a[3], pb[nt][0], pb[nt][1]);
+            }
+          } else {
+            const __nv_bfloat16* vsp = sbp + 2 * C::kCh * C::kGroups;
+            const __nv_bfloat16* vbp = sbp + 3 * C::kCh * C::kGroups;
+            const int r_a = tile * 16 + g, r_b = r_a + 8;
+            const bool va = !stale || kbase + r_a < len, vb = !stale || kbase + r_b < len;
+#pragma unroll
+            for (int grp = 0; grp < C::kGroups; ++grp) {
+              const float vs0 = va ? __bfloat162float(vsp[r_a * C::kGroups + grp]) : 0.f;
+              const float vs1 = vb ? __bfloat162float(vsp[r_b * C::kGroups + grp]) : 0.f;
+              const float vb0 = va ? __bfloat162float(vbp[r_a * C::kGroups + grp]) : 0.f;
+              const float vb1 = vb ? __bfloat162float(vbp[r_b * C::kGroups + grp]) : 0.f;
+              uint32_t pb[NT][2];
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt) {
+                const uint32_t lo = pack_f16x2(pr[tile][nt][0] * vs0, pr[tile][nt][1] * vs0);
+                const uint32_t hi = pack_f16x2(pr[tile][nt][2] * vs1, pr[tile][nt][3] * vs1);
+                pb[nt][0] = movmatrix_trans(lo);
+                pb[nt][1] = movmatrix_trans(hi);
+                corr_v[grp][nt][0] += fmaf(pr[tile][nt][0], vb0, pr[tile][nt][2] * vb1) -
+                                       C::kOffsetV * (f16_lo_to_f32(lo) + f16_lo_to_f32(hi));
+                corr_v[grp][nt][1] += fmaf(pr[tile][nt][1], vb0, pr[tile][nt][3] * vb1) -
+                                       C::kOffsetV * (f16_hi_to_f32(lo) + f16_hi_to_f32(hi));
+              }
+              if constexpr (BITS == 4) {
+                uint32_t y[4];
+                ldsm_x4_t(swizzled<C::kRB>(vpl, lrow, 2 * grp + lch_t), y);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  const uint32_t a0 = nibbles_to_f16x2_biased(y[0] >> (4 * j));
+                  const uint32_t a1 = nibbles_to_f16x2_biased(y[1] >> (4 * j));
+                  const uint32_t a2 = nibbles_to_f16x2_biased(y[2] >> (4 * j));
+                  const uint32_t a3 = nibbles_to_f16x2_biased(y[3] >> (4 * j));
+#pragma unroll
+                  for (int nt = 0; nt < NT; ++nt) mma_f16(o[4 * grp + j][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
+                }
+              } else {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                  uint32_t y[4];
+                  ldsm_x4_t(swizzled<C::kRB>(vpl + (grp >> 1) * C::kBoxBytes, lrow, (grp & 1) * 4 + 2 * h + lch_t), y);
+                  // byte 0 / byte 2 of y: dim 2g of keys 2t / 2t+1; bytes 1 / 3: dim 2g + 1
+#pragma unroll
+                  for (int nt = 0; nt < NT; ++nt) {
+                    mma_f16(o[4 * grp + 2 * h][nt], bytes_to_f16x2_biased<0x4240>(y[0]),
+                            bytes_to_f16x2_biased<0x4240>(y[1]), bytes_to_f16x2_biased<0x4240>(y[2]),
+                            bytes_to_f16x2_biased<0x4240>(y[3]), pb[nt][0], pb[nt][1]);
+                    mma_f16(o[4 * grp + 2 * h + 1][nt], bytes_to_f16x2_biased<0x4341>(y[0]),
+                            bytes_to_f16x2_biased<0x4341>(y[1]), bytes_to_f16x2_biased<0x4341>(y[2]),
+                            bytes_to_f16x2_biased<0x4341>(y[3]), pb[nt][0], pb[nt][1]);
+                  }
+                }
+              }
+            }
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&empty_bar[s]));
+    }
+
+    // ---- per-warp totals: normaliser and value corrections summed over the 8 key lanes
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+      for (int e2 = 0; e2 < 2; ++e2) {
+        float l = l_run[nt][e2];
+        l += __shfl_xor_sync(0xffffffffu, l, 4);
+        l += __shfl_xor_sync(0xffffffffu, l, 8);
+        l += __shfl_xor_sync(0xffffffffu, l, 16);
+        l_run[nt][e2] = l;
+        if constexpr (C::kQuant) {
+#pragma unroll
+          for (int grp = 0; grp < C::kGroups; ++grp) {
+            float cv = corr_v[grp][nt][e2];
+            cv += __shfl_xor_sync(0xffffffffu, cv, 4);
+            cv += __shfl_xor_sync(0xffffffffu, cv, 8);
+            cv += __shfl_xor_sync(0xffffffffu, cv, 16);
+            corr_v[grp][nt][e2] = cv;
+          }
+        }
+      }
+    }
+    if constexpr (C::kQuant) {
+#pragma unroll
+      for (int mt = 0; mt < C::kMt; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) o[mt][nt][e] += corr_v[mt >> 2][nt][e & 1];
+    }
+  }
+
+  __syncthreads();  // every stage consumed, every copy landed: the stage ring is free
+
+  // ---- combine the consumer warps' states and write out
+  float* cm = reinterpret_cast<float*>(smem);
+  float* cl = cm + C::kWarps * C::kNqp;
+  float* co = cl + C::kWarps * C::kNqp;
+  if (warp < C::kWarps) {
+    if (g == 0) {
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e2 = 0; e2 < 2; ++e2) {
+          const int r = 8 * nt + 2 * t + e2;
+          cm[warp * C::kNqp + r] = m_run[nt][e2];
+          cl[warp * C::kNqp + r] = l_run[nt][e2];
+        }
+    }
+#pragma unroll
+    for (int mt = 0; mt < C::kMt; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int r = 8 * nt + 2 * t + (e & 1);
+          co[(warp * C::kNqp + r) * D + out_dim<BITS>(mt, e >> 1, g)] = o[mt][nt][e];
+        }
+  }
+  __syncthreads();
+
+  for (int idx = threadIdx.x; idx < p.nq * D; idx += C::kThreads) {
+    const int r = idx / D, d = idx % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < C::kWarps; ++w) M = fmaxf(M, cm[w * C::kNqp + r]);
+    float L = 0.f, O = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < C::kWarps; ++w) {
+        const float mw = cm[w * C::kNqp + r];
+        if (mw != -INFINITY) {
+          const float wt = fast_exp2(mw - M);
+          L = fmaf(wt, cl[w * C::kNqp + r], L);
+          O = fmaf(wt, co[(w * C::kNqp + r) * D + d], O);
+        }
+      }
+    }
+    const size_t orow = row0 + r;
+    if (single) {
+      p.out[orow * D + d] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
+    } else {
+      const size_t slot = orow * p.max_partitions + part;
+      p.ws_o[slot * D + d] = O;
+      if (d == 0) {
+        p.ws_ml[slot * 2] = M;
+        p.ws_ml[slot * 2 + 1] = L;
+      }
+    }
+  }
+}
+
+}  // namespace pkv

@@ -1,0 +1,156 @@
+"""CPU checks of the C ABI: the library loads without a GPU, exports every entry
+point the header declares, plans partitions, and rejects bad arguments with
+its error codes before touching CUDA."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from quantized_kv_decode_partial_gb300 import binding as B
+from quantized_kv_decode_partial_gb300 import build as pkv_build
+from quantized_kv_decode_partial_gb300.workloads import WORKLOADS
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "pkv_decode.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    pkv_build.build()
+    return B.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\**\s+\**(pkv_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_binding_exports():
+    assert declared_functions() == sorted(B.EXPORTS)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert isinstance(getattr(lib, name), ctypes._CFuncPtr)
+
+
+def test_version_and_messages(lib):
+    assert lib.pkv_version() >= 100
+    for code in range(0, -8, -1):
+        msg = lib.pkv_strerror(code).decode()
+        assert msg and msg != "unknown error code"
+    assert lib.pkv_strerror(-99).decode() == "unknown error code"
+
+
+def _layout(spec, num_blocks=1000):
+    return B.PoolLayout(num_blocks, spec.num_kv_heads, spec.block_size, spec.head_dim, spec.bits, spec.group_size)
+
+
+def _params(spec, max_blocks, partition=None):
+    pt = spec.partition_tokens if partition is None else partition
+    if pt < 0:
+        pt = max_blocks * spec.block_size
+    return B.DecodeParams(spec.num_seqs, spec.num_q_heads, spec.n_query, max_blocks, pt)
+
+
+@pytest.mark.parametrize("name", sorted(WORKLOADS))
+def test_plan_for_workloads(lib, name):
+    sp = WORKLOADS[name]
+    lmax = max(sp.lengths) if sp.lengths else sp.length_range[1]
+    max_blocks = -(-lmax // sp.block_size)
+    plan = B.make_plan(_layout(sp), _params(sp, max_blocks), sm_count=152)
+    ch = 16 if sp.bits == 16 else 32
+    assert plan.chunk_rows == ch and plan.partition_tokens % ch == 0
+    assert plan.max_partitions == -(-max_blocks * sp.block_size // plan.partition_tokens)
+    if sp.partition_tokens > 0:
+        assert plan.partition_tokens == sp.partition_tokens
+    if plan.max_partitions == 1:
+        assert plan.workspace_bytes == 0
+    else:
+        slots = sp.num_seqs * sp.num_q_heads * sp.n_query * plan.max_partitions
+        assert plan.workspace_bytes >= slots * (sp.head_dim + 2) * 4
+        # auto plans launch several waves of 2 CTAs per SM, never partitions below 256 rows
+        if sp.partition_tokens == 0:
+            assert plan.partition_tokens >= 256
+            assert sp.num_seqs * sp.num_kv_heads * plan.max_partitions >= 8 * 152 or plan.partition_tokens == 256
+    assert plan.threads_per_cta == 160 and 0 < plan.smem_bytes <= 227 * 1024
+
+
+def test_plan_auto_is_monotone_in_sm_count(lib):
+    sp = WORKLOADS["bf16_8x131072_n4_hq32_d128"]
+    parts = [B.make_plan(_layout(sp), _params(sp, 8192, 0), sm_count=s).partition_tokens for s in (8, 76, 152, 304)]
+    assert parts == sorted(parts, reverse=True)
+
+
+@pytest.mark.parametrize("field,value,code", [
+    ("bits", 3, B.PKV_ERR_BAD_LAYOUT), ("bits", 2, B.PKV_ERR_BAD_LAYOUT), ("group_size", 32, B.PKV_ERR_BAD_LAYOUT),
+    ("head_dim", 96, B.PKV_ERR_BAD_LAYOUT), ("block_size", 8, B.PKV_ERR_BAD_LAYOUT),
+    ("num_blocks", 0, B.PKV_ERR_BAD_LAYOUT), ("num_blocks", 1 << 28, B.PKV_ERR_BAD_LAYOUT),
+])
+def test_plan_rejects_bad_layouts(lib, field, value, code):
+    sp = WORKLOADS["affine4_g64_1x8192_hq16_d256"]
+    lay = _layout(sp)
+    setattr(lay, field, value)
+    plan = B.Plan()
+    assert lib.pkv_make_plan(ctypes.byref(lay), ctypes.byref(_params(sp, 256)), 152, ctypes.byref(plan)) == code
+
+
+@pytest.mark.parametrize("field,value,code", [
+    ("num_q_heads", 6, B.PKV_ERR_BAD_PARAMS), ("n_query", 0, B.PKV_ERR_BAD_PARAMS),
+    ("num_seqs", 0, B.PKV_ERR_BAD_PARAMS), ("max_blocks_per_seq", 0, B.PKV_ERR_BAD_PARAMS),
+    ("partition_tokens", -1, B.PKV_ERR_BAD_PARAMS), ("n_query", 3, B.PKV_ERR_UNSUPPORTED_SHAPE),
+])
+def test_plan_rejects_bad_params(lib, field, value, code):
+    sp = WORKLOADS["affine4_g64_1x8192_hq16_d256"]  # HQ 16 / HK 4: REP 4, so n_query 3 asks for 12 > 8 rows at D 256
+    par = _params(sp, 256)
+    setattr(par, field, value)
+    plan = B.Plan()
+    assert lib.pkv_make_plan(ctypes.byref(_layout(sp)), ctypes.byref(par), 152, ctypes.byref(plan)) == code
+
+
+def test_decode_call_validates_before_cuda(lib):
+    sp = WORKLOADS["affine4_g64_1x8192_hq16_d256"]
+    lay, par = _layout(sp), _params(sp, 256)
+    fake = 1 << 20  # aligned, never dereferenced: validation fails first
+    args = [fake] * 9
+    call = lambda a, lay=lay: lib.pkv_paged_decode_attention(
+        ctypes.byref(lay), ctypes.byref(par), *a[:9], 0.0625, fake, fake, 1 << 30, None, None)
+    null_q = list(args)
+    null_q[0] = None
+    assert call(null_q) == B.PKV_ERR_NULL_POINTER
+    no_scales = list(args)
+    no_scales[3] = None  # affine pages need their scale planes
+    assert call(no_scales) == B.PKV_ERR_NULL_POINTER
+    mis = list(args)
+    mis[1] = fake + 8
+    assert call(mis) == B.PKV_ERR_MISALIGNED
+    bad = B.PoolLayout(lay.num_blocks, lay.num_kv_heads, lay.block_size, lay.head_dim, 5, 64)
+    assert call(args, bad) == B.PKV_ERR_BAD_LAYOUT
+
+
+def test_decode_without_gpu_fails_loudly(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    sp = WORKLOADS["bf16_1x1024_hq2_d256"]
+    lay, par = _layout(sp, 128), _params(sp, 64)
+    fake = 1 << 20
+    rc = lib.pkv_paged_decode_attention(ctypes.byref(lay), ctypes.byref(par), fake, fake, fake, None, None, None,
+                                        None, fake, fake, 0.0625, fake, None, 0, None, None)
+    assert rc == B.PKV_ERR_CUDA
+    assert lib.pkv_last_cuda_error().decode()
+
+
+def test_gather_validates(lib):
+    fake = 1 << 20
+    assert lib.pkv_paged_gather(fake, 10, 2, 16, 6, fake, fake, 1, 4, 64, fake, None, None) == B.PKV_ERR_BAD_PARAMS
+    assert lib.pkv_paged_gather(None, 10, 2, 16, 8, fake, fake, 1, 4, 64, fake, None, None) == B.PKV_ERR_NULL_POINTER
+    assert lib.pkv_paged_gather(fake + 4, 10, 2, 16, 8, fake, fake, 1, 4, 64, fake, None, None) == B.PKV_ERR_MISALIGNED
+
+
+def test_missing_library_raises(tmp_path):
+    with pytest.raises(B.LibraryNotBuilt):
+        B.load_library(str(tmp_path / "nope.so"))

@@ -1,0 +1,234 @@
+"""GPU parity: the CUDA path through the C ABI against the float64 CPU oracle.
+
+Tolerance (bf16 outputs vs the oracle): max-abs <= 1e-2 and mean-abs <= 1e-3.
+Gathers and layout changes are checked bit for bit.
+"""
+
+import math
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import assert_close, oracle_out, run_gpu, subcase
+from quantized_kv_decode_partial_gb300 import PkvError, paged_decode_attention, paged_gather
+from quantized_kv_decode_partial_gb300 import binding as B
+from quantized_kv_decode_partial_gb300.workloads import WORKLOADS, DecodeSpec, make_case
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+
+
+def spec(name, **kw):
+    base = dict(name=name, num_seqs=3, num_q_heads=8, num_kv_heads=2, head_dim=128, n_query=1, block_size=16,
+                bits=16, length_range=(1, 300), pool_factor=2.0, seed=zlib.crc32(name.encode()) % 10000)
+    base.update(kw)
+    return DecodeSpec(**base)
+
+
+# Every kernel instantiation, ragged lengths (1 row up to several partitions and
+# a ragged tail), GQA factors 1..32, n_query 1..4, page sizes 16..128.
+SMALL = [
+    (spec("bf16_d128_nq4"), [-1, 16, 48, 0]),
+    (spec("bf16_d128_nq16_n2", num_q_heads=16, n_query=2, block_size=32, length_range=(2, 500)), [-1, 64, 0]),
+    (spec("bf16_d64_nq32", num_q_heads=32, num_kv_heads=1, head_dim=64, lengths=(1, 17, 33, 250),
+          length_range=None, num_seqs=4), [-1, 32]),
+    (spec("bf16_d64_rep1_n3", num_q_heads=4, num_kv_heads=4, head_dim=64, n_query=3, block_size=64,
+          length_range=(3, 400)), [-1, 80]),
+    (spec("bf16_d64_nq16", num_q_heads=8, num_kv_heads=1, head_dim=64, n_query=2, block_size=16), [-1, 64]),
+    (spec("bf16_d256_nq8_n2", head_dim=256, n_query=2, length_range=(2, 400)), [-1, 64, 0]),
+    (spec("u4_d256_nq4", head_dim=256, bits=4, block_size=32, length_range=(1, 600)), [-1, 32, 64, 0]),
+    (spec("u4_d128_nq16_n2", num_q_heads=16, head_dim=128, bits=4, n_query=2, block_size=64,
+          length_range=(2, 500)), [-1, 96]),
+    (spec("u4_d128_nq4", head_dim=128, bits=4, block_size=32), [-1, 64]),
+    (spec("u8_d256_nq4", head_dim=256, bits=8, block_size=32, length_range=(1, 600)), [-1, 32, 0]),
+    (spec("u8_d128_nq16_n2", num_q_heads=8, num_kv_heads=1, head_dim=128, bits=8, n_query=2, block_size=32,
+          length_range=(2, 500)), [-1, 64]),
+    (spec("u8_d128_nq4", head_dim=128, bits=8, block_size=64), [-1, 128]),
+    (spec("u4_d256_nq8_n4", num_q_heads=4, num_kv_heads=2, head_dim=256, bits=4, n_query=4, block_size=32,
+          length_range=(4, 300)), [-1, 32]),
+]
+
+
+@pytest.mark.parametrize("sp,parts", SMALL, ids=[s.name for s, _ in SMALL])
+def test_small_cases_match_oracle(sp, parts):
+    case = make_case(sp)
+    ref = oracle_out(case)
+    dcase = case.to(DEV)
+    for pt in parts:
+        err = torch.zeros(1, dtype=torch.int32, device=DEV)
+        ptok = (max(case.lens_host) + 64) if pt == -1 else pt
+        out = run_gpu(dcase, partition_tokens=ptok, error_flag=err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        assert_close(out.double().cpu().numpy(), ref, f"{sp.name} partition={pt}")
+
+
+def test_partitioned_oracle_agrees_with_gpu_partitions():
+    sp = spec("u4_partitions", head_dim=256, bits=4, block_size=32, num_seqs=2, length_range=(300, 700))
+    case = make_case(sp)
+    for pt in (32, 96):
+        ref = oracle_out(case, partition_tokens=pt)
+        out = run_gpu(case.to(DEV), partition_tokens=pt)
+        assert_close(out.double().cpu().numpy(), ref, f"partition {pt}")
+
+
+# ---------------------------------------------------------------------------
+# the measured workloads at full size: sampled (sequence, KV head) sub-problems
+# ---------------------------------------------------------------------------
+
+FULL = ["bf16_1x1024_hq2_d256", "affine4_g64_1x8192_hq16_d256", "bf16_batch32_hq32_d128",
+        "affine4_batch64_hq32_d256", "affine8_batch64_hq32_d256", "bf16_8x131072_n4_hq32_d128"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_workloads_sampled(name):
+    sp = WORKLOADS[name]
+    case = make_case(sp, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = run_gpu(case, error_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.isfinite(out.float()).all()
+    rng = np.random.default_rng(99)
+    picks = {(0, 0), (sp.num_seqs - 1, sp.num_kv_heads - 1)}
+    while len(picks) < min(4, sp.num_seqs * sp.num_kv_heads):
+        picks.add((int(rng.integers(sp.num_seqs)), int(rng.integers(sp.num_kv_heads))))
+    for b, kv in sorted(picks):
+        sub = subcase(case, b, kv)
+        ref = oracle_out(sub)
+        got = out[b:b + 1, kv * sp.rep:(kv + 1) * sp.rep].double().cpu().numpy()
+        assert_close(got, ref, f"{name} b={b} kv={kv}")
+
+
+# ---------------------------------------------------------------------------
+# bit-exact properties
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("bits", [16, 4])
+def test_gather_is_bit_exact(bits):
+    sp = spec(f"gather_{bits}", head_dim=128, bits=bits, block_size=32, length_range=(1, 200))
+    case = make_case(sp)
+    d = case.to(DEV)
+    max_len = max(case.lens_host) + 7
+    planes = [("k", case.k_pool, d.k_pool), ("v", case.v_pool, d.v_pool)]
+    if bits != 16:
+        planes += [("ks", case.k_scales, d.k_scales), ("vb", case.v_biases, d.v_biases)]
+    for name, host, dev in planes:
+        got = paged_gather(dev, d.block_tables, d.seq_lens, max_len).cpu()
+        raw = host.view(torch.int16) if host.dtype == torch.bfloat16 else host
+        got_raw = got.view(torch.int16) if got.dtype == torch.bfloat16 else got
+        for b in range(sp.num_seqs):
+            L = case.lens_host[b]
+            ref = oracle.gather_pages(raw.numpy(), case.tables_host[b], L)
+            assert np.array_equal(got_raw[b, :, :L].numpy(), ref), name
+            assert not got_raw[b, :, L:].any(), name  # untouched rows stay zero
+
+
+@pytest.mark.parametrize("bits", [16, 8])
+def test_physical_block_permutation_is_bitwise_invariant(bits):
+    sp = spec(f"perm_{bits}", head_dim=128 if bits == 16 else 256, bits=bits, block_size=32,
+              length_range=(50, 600))
+    case = make_case(sp)
+    base = run_gpu(case.to(DEV), partition_tokens=64)
+    g = torch.Generator().manual_seed(3)
+    perm = torch.randperm(case.num_blocks, generator=g)
+    inv = torch.argsort(perm)
+    moved = case.to("cpu")
+    for f in ("k_pool", "v_pool", "k_scales", "k_biases", "v_scales", "v_biases"):
+        t = getattr(moved, f)
+        if t is not None:
+            setattr(moved, f, t[inv].contiguous())
+    tb = moved.block_tables.clone()
+    tb[tb >= 0] = perm[tb[tb >= 0].long()].to(torch.int32)
+    moved.block_tables = tb
+    out = run_gpu(moved.to(DEV), partition_tokens=64)
+    assert torch.equal(out.view(torch.int16), base.view(torch.int16))
+
+
+def test_cuda_graph_replay_matches_eager():
+    sp = spec("graph", head_dim=128, num_q_heads=32, num_kv_heads=8, length_range=(100, 3000), num_seqs=4)
+    case = make_case(sp, device=DEV)
+    eager = run_gpu(case, partition_tokens=256)
+    out = torch.empty_like(eager)
+    plan = B.make_plan(B.layout_for(case.k_pool, 128, 16), B.DecodeParams(4, 32, 1, case.block_tables.shape[1], 256))
+    ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=DEV)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        paged_decode_attention(case.q, case.k_pool, case.v_pool, case.block_tables, case.seq_lens, case.scale,
+                               partition_tokens=256, out=out, workspace=ws)
+    torch.cuda.current_stream().wait_stream(s)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        paged_decode_attention(case.q, case.k_pool, case.v_pool, case.block_tables, case.seq_lens, case.scale,
+                               partition_tokens=256, out=out, workspace=ws)
+    out.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
+
+
+# ---------------------------------------------------------------------------
+# invalid inputs: flagged on the device, never a fault
+# ---------------------------------------------------------------------------
+
+def test_bad_block_id_is_flagged_and_isolated():
+    sp = spec("badblock", num_seqs=3, length_range=(100, 300))
+    case = make_case(sp).to(DEV)
+    good = run_gpu(case, partition_tokens=64)
+    tb = case.block_tables.clone()
+    tb[1, 2] = case.num_blocks + 5
+    case.block_tables = tb
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = run_gpu(case, partition_tokens=64, error_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & B.PKV_DEVERR_BAD_BLOCK
+    assert torch.isfinite(out.float()).all()
+    assert torch.equal(out[[0, 2]].view(torch.int16), good[[0, 2]].view(torch.int16))
+
+
+@pytest.mark.parametrize("bad_len", ["short", "long"])
+def test_bad_seq_len_is_flagged_and_zeroed(bad_len):
+    sp = spec("badlen", num_seqs=3, n_query=2, length_range=(100, 300))
+    case = make_case(sp).to(DEV)
+    for pt in (64, 4096):
+        good = run_gpu(case, partition_tokens=pt)
+        lens = case.seq_lens.clone()
+        lens[1] = 1 if bad_len == "short" else case.block_tables.shape[1] * sp.block_size + 1
+        bad = case.to(DEV)
+        bad.seq_lens = lens
+        err = torch.zeros(1, dtype=torch.int32, device=DEV)
+        out = run_gpu(bad, partition_tokens=pt, error_flag=err)
+        torch.cuda.synchronize()
+        assert int(err.item()) & B.PKV_DEVERR_BAD_SEQ_LEN
+        assert not out[1].float().any()
+        assert torch.equal(out[[0, 2]].view(torch.int16), good[[0, 2]].view(torch.int16))
+
+
+def test_host_side_errors_return_codes():
+    sp = spec("hosterr")
+    case = make_case(sp).to(DEV)
+    flat = case.k_pool.view(-1)
+    shifted = torch.as_strided(flat, (case.k_pool.shape[0] - 1,) + tuple(case.k_pool.shape[1:]),
+                               case.k_pool.stride(), storage_offset=1)  # 2 bytes off a 16-byte boundary
+    with pytest.raises(PkvError) as e:
+        paged_decode_attention(case.q, shifted, case.v_pool, case.block_tables, case.seq_lens, case.scale)
+    assert e.value.code == B.PKV_ERR_MISALIGNED
+    with pytest.raises(PkvError) as e:
+        paged_decode_attention(case.q, case.k_pool, case.v_pool, case.block_tables, case.seq_lens, case.scale,
+                               partition_tokens=16, workspace=torch.empty(16, dtype=torch.uint8, device=DEV))
+    assert e.value.code == B.PKV_ERR_WORKSPACE_TOO_SMALL
+
+
+def test_minimum_lengths_and_exact_fill():
+    # len == n_query (only the new rows), and len filling every block of the table exactly
+    sp = spec("edges", num_seqs=2, n_query=3, num_q_heads=4, num_kv_heads=2, lengths=(3, 64), length_range=None,
+              block_size=16)
+    case = make_case(sp)
+    ref = oracle_out(case)
+    for pt in (16, 4096):
+        out = run_gpu(case.to(DEV), partition_tokens=pt)
+        assert_close(out.double().cpu().numpy(), ref, f"edges pt={pt}")
