@@ -46,6 +46,12 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU oracle sample")
+    ap.add_argument("--profile-calls", type=int, default=0,
+                    help="profiling mode: make the workload, run this many eager decode calls, exit")
+    ap.add_argument("--num-seqs", type=int, default=0,
+                    help="profiling mode: keep only the first N sequences of the workload")
+    ap.add_argument("--partition-tokens", type=int, default=-2,
+                    help="profiling mode: rows per partition instead of the workload's choice")
     return ap.parse_args(argv)
 
 
@@ -143,61 +149,68 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 
 CPU_CHILD = r"""
-import json, math, os, sys, time
+import json, os, sys, time
+from dataclasses import replace
 sys.path.insert(0, {root!r})
-import numpy as np
 import torch
 torch.set_num_threads(1)
 import oracle
-from quantized_kv_decode_partial_gb300.workloads import WORKLOADS, make_case, required_kv_bytes
-budget = {budget}
-done_bytes, elapsed, samples = 0, 0.0, []
+from quantized_kv_decode_partial_gb300.workloads import WORKLOADS, draw_lengths, make_case, required_kv_bytes
+# One (sequence, KV head) unit of each layer: the first sequence of the seeded
+# length draw, with its REP query heads. Every unit of a workload costs the same
+# per cached row, so the rate of one unit is the rate of the workload.
+units = []
 for name in {names!r}:
     spec = WORKLOADS[name]
-    case = make_case(spec, device="cpu", seed={seed})
+    lens = draw_lengths(spec, {seed})
+    unit = replace(spec, name=name + "_unit", num_seqs=1, num_kv_heads=1, num_q_heads=spec.rep,
+                   lengths=(lens[0],), length_range=None, pool_factor=1.0)
+    case = make_case(unit, device="cpu", seed={seed})
     f64 = lambda t: None if t is None else t.float().double().numpy()
-    kw = dict(bits=spec.bits, group_size=spec.group_size)
-    if spec.bits == 16:
+    kw = dict(bits=unit.bits, group_size=unit.group_size)
+    if unit.bits == 16:
         kp, vp = f64(case.k_pool), f64(case.v_pool)
     else:
         kp, vp = case.k_pool.numpy(), case.v_pool.numpy()
         kw.update(k_scales=f64(case.k_scales), k_biases=f64(case.k_biases), v_scales=f64(case.v_scales),
                   v_biases=f64(case.v_biases))
-    q = f64(case.q)
-    tables, lens = case.block_tables.numpy(), case.seq_lens.numpy()
-    # one (sequence, KV head) unit at a time, until the time budget share is spent
-    units = [(b, kv) for b in range(spec.num_seqs) for kv in range(spec.num_kv_heads)]
-    share = budget / len({names!r})
+    args = (f64(case.q), kp, vp, case.block_tables.numpy(), case.seq_lens.numpy(), case.scale, unit.n_query)
+    units.append((name, args, kw, required_kv_bytes(unit, case.lens_host), case.lens_host[0]))
+steps = []
+for _ in range({steps}):
     t_start = time.perf_counter()
-    n = 0
-    for b, kv in units:
-        rows = [(b, h) for h in range(kv * spec.rep, (kv + 1) * spec.rep)]
-        t0 = time.perf_counter()
-        oracle.paged_decode_attention(q, kp, vp, tables, lens, case.scale, spec.n_query, rows=rows, **kw)
-        elapsed += time.perf_counter() - t0
-        done_bytes += int(lens[b]) * 2 * (2 * spec.head_dim if spec.bits == 16 else
-                                          spec.head_dim * spec.bits // 8 + spec.head_dim // spec.group_size * 4)
-        n += 1
-        if time.perf_counter() - t_start > share:
+    done, secs, count = 0, 0.0, 0
+    while True:
+        for name, args, kw, nbytes, L in units:
+            t0 = time.perf_counter()
+            oracle.paged_decode_attention(*args, **kw)
+            secs += time.perf_counter() - t0
+            done += nbytes
+        count += 1
+        if time.perf_counter() - t_start >= {budget}:
             break
-    samples.append(f"{{name}}: {{n}} of {{len(units)}} (sequence, KV head) units")
-print(json.dumps({{"bytes": done_bytes, "seconds": elapsed, "sample": "; ".join(samples)}}))
+    steps.append({{"bytes": done, "seconds": secs, "repeats": count}})
+sample = "; ".join(f"{{n}}: 1 sequence x 1 KV head ({{L}} rows, {{nb}} K/V bytes)" for n, _, _, nb, L in units)
+print(json.dumps({{"steps": steps, "sample": sample}}))
 """
 
 
-def cpu_oracle_baseline(names, seed, budget_s):
-    code = CPU_CHILD.format(root=ROOT, budget=budget_s, names=list(names), seed=seed)
+def cpu_oracle_baseline(names, seed, budget_s, steps=1):
+    """The oracle on a bounded sample of the workload, one thread, in a child
+    process (started before or apart from any GPU work). Returns per-step rates."""
+    code = CPU_CHILD.format(root=ROOT, budget=budget_s, names=list(names), seed=seed, steps=steps)
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
                CUDA_VISIBLE_DEVICES="")
     res = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
-                         timeout=max(600, 20 * budget_s))
+                         timeout=max(900, 3 * steps * budget_s + 300))
     if res.returncode != 0:
         raise RuntimeError(f"CPU oracle failed:\n{res.stderr[-2000:]}")
     info = json.loads(res.stdout.strip().splitlines()[-1])
-    gbs = info["bytes"] / info["seconds"] / 1e9
-    return {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": info["sample"] + f"; {info['bytes']} K/V bytes in {info['seconds']:.2f} s, one thread",
-            "bytes": info["bytes"], "seconds": info["seconds"]}
+    tot_b = sum(s["bytes"] for s in info["steps"])
+    tot_s = sum(s["seconds"] for s in info["steps"])
+    return {"value": tot_b / tot_s / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": info["sample"] + f"; {tot_b} K/V bytes in {tot_s:.2f} s on one thread",
+            "steps": info["steps"], "bytes": tot_b, "seconds": tot_s}
 
 
 # ---------------------------------------------------------------------------
@@ -210,23 +223,19 @@ def run_reference(args):
         return
     specs = workload_specs(args.workload)
     names = [s.name for s in specs]
-    per_step = max(1.0, 60.0 / max(1, args.steps + args.warmup))
-    values = []
-    total_bytes, total_s, sample = 0, 0.0, ""
-    for i in range(args.warmup + args.steps):
-        r = cpu_oracle_baseline(names, specs[0].seed, per_step)
-        if i >= args.warmup:
-            values.append(r["value"])
-            total_bytes += r["bytes"]
-            total_s += r["seconds"]
-            sample = r["sample"]
-    value = total_bytes / total_s / 1e9
+    per_step = min(2.0, max(0.05, 120.0 / max(1, args.steps + args.warmup)))
+    r = cpu_oracle_baseline(names, specs[0].seed, per_step, steps=args.warmup + args.steps)
+    timed = r["steps"][args.warmup:]
+    tot_b = sum(s["bytes"] for s in timed)
+    tot_s = sum(s["seconds"] for s in timed)
+    value = tot_b / tot_s / 1e9
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_s / max(1, args.steps),
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_s / max(1, args.steps),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": args.workload, "sample": "bounded CPU sample per step"},
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "config": {"workload": args.workload,
+                   "sample": f"each step repeats the oracle on the sample for about {per_step:.2f} s"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": r["sample"]},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -246,9 +255,9 @@ def run_ours(args):
     from quantized_kv_decode_partial_gb300.binding import layout_for
     from quantized_kv_decode_partial_gb300.workloads import make_case, required_kv_bytes
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    from quantized_kv_decode_partial_gb300.dist import max_over_ranks, rank_seed, weak_scaling_rate, world as env_world
+
+    rank, world, local = env_world()
     if world > 1:
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
@@ -265,12 +274,12 @@ def run_ours(args):
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     layers = []
     for sp in specs:
-        base = make_case(sp, device=dev, seed=sp.seed + 7919 * rank, poison=False)
+        base = make_case(sp, device=dev, seed=rank_seed(sp.seed, rank), poison=False)
         in_bytes = sum(t.numel() * t.element_size() for t in
                        (base.q, base.k_pool, base.v_pool, base.k_scales, base.k_biases, base.v_scales, base.v_biases,
                         base.block_tables, base.seq_lens) if t is not None)
         copies = max(1, math.ceil(3 * l2 / in_bytes))
-        insts = [base] + [make_case(sp, device=dev, seed=sp.seed + 7919 * rank + 104729 * (c + 1), poison=False,
+        insts = [base] + [make_case(sp, device=dev, seed=rank_seed(sp.seed, rank) + 104729 * (c + 1), poison=False,
                                     lengths=base.lens_host) for c in range(copies - 1)]
         layout = layout_for(base.k_pool, sp.head_dim, sp.bits, sp.group_size)
         params = DecodeParams(sp.num_seqs, sp.num_q_heads, sp.n_query, base.block_tables.shape[1],
@@ -320,11 +329,8 @@ def run_ours(args):
                     g.replay()
             e1.record(stream)
         torch.cuda.synchronize(dev)
-        ms = e0.elapsed_time(e1)
+        ms = max_over_ranks(e0.elapsed_time(e1), dev)
         if world > 1:
-            t = torch.tensor([ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms = float(t.item())
             dist.barrier()
         return ms
 
@@ -396,14 +402,10 @@ def run_ours(args):
             e2e_once()
         e1.record(stream)
     torch.cuda.synchronize(dev)
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dev)
 
     ms_step = ms / K
-    value = world * step_bytes / (ms_step * 1e-3) / 1e9
+    value = weak_scaling_rate(step_bytes, world, ms_step)
     part_ms = ms_partial / K
     peak, peak_kind = measured_hbm_peak()
     achieved = step_bytes / (part_ms * 1e-3) / 1e9
@@ -430,7 +432,7 @@ def run_ours(args):
                          "frac": achieved / peak, "traffic": None,
                          "kernel": f"pkv_partial_kernel (partial pass alone, {part_ms * 1e3:.2f} us per step)",
                          "peak_source": f"{peak_kind} hbm_gbs", "frac_of_nominal_7900": achieved / 7900.0},
-            "e2e": {"value": world * step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+            "e2e": {"value": weak_scaling_rate(step_bytes, world, e2e_ms), "unit": "GB/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                     "what": "public call per step with q, block tables and lengths copied from pinned host memory "
                             "and the output copied back; the KV pool is device-resident cache state"},
@@ -444,9 +446,41 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def run_profile_calls(args):
+    """A plain sequence of eager decode calls on one instance (for ncu): no graphs,
+    no timing, no CPU work."""
+    from dataclasses import replace
+
+    import torch
+
+    from quantized_kv_decode_partial_gb300 import load_library, paged_decode_attention
+    from quantized_kv_decode_partial_gb300 import build as pkv_build
+    from quantized_kv_decode_partial_gb300.workloads import draw_lengths, make_case, required_kv_bytes
+
+    pkv_build.build()
+    load_library()
+    dev = torch.device("cuda", 0)
+    for sp in workload_specs(args.workload):
+        if args.num_seqs:
+            lens = draw_lengths(sp)[:args.num_seqs]
+            sp = replace(sp, num_seqs=len(lens), lengths=tuple(lens), length_range=None)
+        if args.partition_tokens != -2:
+            sp = replace(sp, partition_tokens=args.partition_tokens)
+        c = make_case(sp, device=dev, poison=False)
+        for _ in range(args.profile_calls):
+            paged_decode_attention(c.q, c.k_pool, c.v_pool, c.block_tables, c.seq_lens, c.scale, bits=sp.bits,
+                                   group_size=sp.group_size, k_scales=c.k_scales, k_biases=c.k_biases,
+                                   v_scales=c.v_scales, v_biases=c.v_biases, partition_tokens=c.partition_tokens)
+        torch.cuda.synchronize()
+        print(json.dumps({"profile_calls": args.profile_calls, "workload": sp.name, "num_seqs": sp.num_seqs,
+                          "kv_bytes_per_call": required_kv_bytes(sp, c.lens_host)}), flush=True)
+
+
 def main(argv=None):
     args = parse_args(argv)
-    if args.impl == "reference":
+    if args.profile_calls:
+        run_profile_calls(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

@@ -10,16 +10,18 @@
 // softmax itself and writes bf16 output.
 //
 // Design (GB300):
-//  * One producer warp streams the partition's K/V rows in chunks of 16 (bf16)
-//    or 32 (affine) rows. The block table is resolved once per chunk, by the
-//    producer, 32 entries per coalesced load. Each chunk of one page and KV head
-//    is contiguous in the pool, so it travels as 2-D TMA boxes (rows of 64 or
-//    128 bytes, hardware-swizzled so the ldmatrix reads below are free of bank
-//    conflicts) plus 1-D bulk copies of the affine scale/bias rows, into a ring
-//    of shared-memory stages guarded by mbarriers.
-//  * Four consumer warps take chunks round-robin. Each K/V row in shared memory
-//    is read once and multiplied against all REP*N query rows of its KV head
-//    (GQA reuse) with warp-level tensor-core MMA (m16n8k16, bf16 in, f32 out):
+//  * Four warps per CTA; warp w takes chunks w, w+4, w+8, ... of the partition
+//    (16 rows for bf16 pages, 32 or 16 for affine pages) and runs its own
+//    pipeline: lane 0 issues the copies of its chunk `kStagesPerWarp` ahead into a
+//    private ring of shared-memory stages guarded by mbarriers, so no warp waits
+//    on another. The block table is read 32 entries per coalesced load and
+//    resolved once per chunk. A chunk of one page and KV head is contiguous in
+//    the pool, so it travels as 2-D TMA boxes (rows of 64 or 128 bytes,
+//    hardware-swizzled so the ldmatrix reads below are free of bank conflicts)
+//    plus 1-D bulk copies of the affine scale/bias rows.
+//  * Each K/V row in shared memory is read once and multiplied against all
+//    REP*N query rows of its KV head (GQA reuse) with warp-level tensor-core
+//    MMA (m16n8k16, bf16 in, f32 out):
 //    S^T = K Q^T puts 16 keys on the M side and 8 query rows on N, and the
 //    probabilities are transposed in registers (movmatrix) into the B operand
 //    of O^T += V^T P^T. The online softmax (running max, normaliser, rescale)
@@ -49,35 +51,36 @@ namespace pkv {
 template <int BITS, int D, int NT>
 struct PartialCfg {
   static constexpr bool kQuant = BITS != 16;
-  static constexpr int kCh = kQuant ? 32 : 16;                     // rows per stage
   static constexpr int kElemBytes = kQuant ? 1 : 2;                // tensor-map element size
   static constexpr int kRowBytes = kQuant ? D * BITS / 8 : 2 * D;  // stored bytes of one row
+  static constexpr int kGroups = D / 64;
+  // Rows per stage: 32 for affine pages when a stage stays within ~9.5 KB, else 16.
+  static constexpr int kCh = (kQuant && 2 * 32 * kRowBytes + 4 * 32 * kGroups * 2 <= 9728) ? 32 : 16;
   static constexpr int kRB = kRowBytes >= 128 ? 128 : kRowBytes;   // bytes of one box row
   static constexpr int kBoxes = kRowBytes / kRB;
   static constexpr int kBoxBytes = kCh * kRB;
   static constexpr int kPlaneBytes = kBoxes * kBoxBytes;
-  static constexpr int kGroups = D / 64;
   static constexpr int kSbBytes = kQuant ? kCh * kGroups * 2 : 0;  // one scale or bias plane
   static constexpr int kTxBytes = 2 * kPlaneBytes + 4 * kSbBytes;
   static constexpr int kStageBytes = (kTxBytes + 1023) / 1024 * 1024;
-  static constexpr int kWarps = 4;  // consumer warps
-  static constexpr int kThreads = (kWarps + 1) * 32;
-  static constexpr int kStages = (100 * 1024) / kStageBytes;
+  static constexpr int kWarps = 4;                                   // every warp computes
+  static constexpr int kThreads = kWarps * 32;
+  static constexpr int kStagesPerWarp = kStageBytes <= 9 * 1024 ? 3 : 2;  // each warp's private ring
   static constexpr int kNqp = 8 * NT;       // query rows per warp (padded)
   static constexpr int kMt = D / 16;        // 16-dim m-tiles of O^T
   static constexpr int kKs = D / 16;        // k16 steps of Q K^T
   static constexpr int kTiles = kCh / 16;   // 16-key tiles per stage
   static constexpr int kCombineBytes = kWarps * kNqp * (D + 2) * 4;
-  static constexpr int kDataBytes =
-      kStages * kStageBytes > kCombineBytes ? kStages * kStageBytes : kCombineBytes;
-  static constexpr int kBarrierBytes = 1024;
+  static constexpr int kRingBytes = kWarps * kStagesPerWarp * kStageBytes;
+  static constexpr int kDataBytes = kRingBytes > kCombineBytes ? kRingBytes : kCombineBytes;
+  static constexpr int kBarrierBytes = 256;
   static constexpr int kSmemBytes = kDataBytes + kBarrierBytes + 1024;  // + alignment slack
   static constexpr float kOffsetK = BITS == 8 ? 2176.f : 128.f;  // code bias inside the K-side MMA (bf16)
   static constexpr float kOffsetV = 1024.f;                        // code bias inside the V-side MMA (fp16)
 
   static_assert(kRB == 128 || kRB == 64, "box rows of 64 or 128 bytes");
   static_assert(kRowBytes % kRB == 0, "whole boxes per row");
-  static_assert(kStages >= 2 && kStages * 20 <= kBarrierBytes, "stage count");
+  static_assert(kWarps * kStagesPerWarp * 12 + 4 <= kBarrierBytes, "barrier area");
   static_assert(!kQuant || D % 64 == 0, "affine head dims are whole 64-dim groups");
 };
 
@@ -126,10 +129,9 @@ __global__ void __maxnreg__(200)
   using C = PartialCfg<BITS, D, NT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + C::kDataBytes);
-  uint64_t* empty_bar = full_bar + C::kStages;
-  int* stage_ok = reinterpret_cast<int*>(empty_bar + C::kStages);
-  volatile int* abort_flag = stage_ok + C::kStages;
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + C::kDataBytes);  // [warp][stage]
+  int* stage_ok = reinterpret_cast<int*>(full_bar + C::kWarps * C::kStagesPerWarp);
+  volatile int* abort_flag = stage_ok + C::kWarps * C::kStagesPerWarp;
 
   const int part = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -153,85 +155,77 @@ __global__ void __maxnreg__(200)
   const int nchunks = (t_end - t0 + C::kCh - 1) / C::kCh;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(smem_addr(&full_bar[s]), 1);
-      mbar_init(smem_addr(&empty_bar[s]), 1);
-    }
+    for (int s = 0; s < C::kWarps * C::kStagesPerWarp; ++s) mbar_init(smem_addr(&full_bar[s]), 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
   __syncthreads();
 
-  // O^T accumulators and softmax state (consumer warps).
+  // O^T accumulators and softmax state.
   float o[C::kMt][NT][4];
   float m_run[NT][2], l_run[NT][2];
   float corr_v[C::kQuant ? C::kGroups : 1][NT][2];
 
-  if (warp == C::kWarps) {
-    // ------------------------------------------------------------------ producer
-    const uint64_t policy = l2_evict_first_policy();
+  {
+    // ------------------------------------------------------------------ this warp's pipeline
+    // Warp w owns chunks w, w + 4, w + 8, ... of the partition and a private ring of
+    // kStagesPerWarp stages: it issues its own TMA copies kStagesPerWarp chunks ahead,
+    // so no warp ever waits on another warp's progress.
+    const int my_chunks = nchunks > warp ? (nchunks - warp + C::kWarps - 1) / C::kWarps : 0;
+    uint64_t* my_full = full_bar + warp * C::kStagesPerWarp;
+    int* my_ok = stage_ok + warp * C::kStagesPerWarp;
+    uint8_t* my_ring = smem + warp * C::kStagesPerWarp * C::kStageBytes;
     const int32_t* table = p.block_tables + static_cast<size_t>(b) * p.max_blocks;
-    int issued = 0, stop = 0;
-    for (int j0 = 0; j0 < nchunks && !stop; j0 += 32) {
-      const int j = j0 + lane;
-      int phys = 0;
-      if (j < nchunks) phys = __ldg(table + (t0 + j * C::kCh) / p.block_size);
-      const int cnt = min(32, nchunks - j0);
-      for (int i = 0; i < cnt; ++i) {
-        const int ph = __shfl_sync(0xffffffffu, phys, i);
-        if (lane == 0) {
-          const int jj = j0 + i, s = jj % C::kStages;
-          bool go = true;
-          if (jj >= C::kStages)
-            go = mbar_wait_bounded(smem_addr(&empty_bar[s]), ((jj / C::kStages) - 1) & 1, abort_flag,
-                                   p.error_flag);
-          if (go) {
-            const bool ok = static_cast<unsigned>(ph) < static_cast<unsigned>(p.num_blocks);
-            stage_ok[s] = ok ? 1 : 0;
-            const uint32_t fb = smem_addr(&full_bar[s]);
-            if (ok) {
-              fence_proxy_async_smem();
-              mbar_arrive_expect_tx(fb, C::kTxBytes);
-              const int row = (ph * p.num_kv_heads + hk) * p.block_size + (t0 + jj * C::kCh) % p.block_size;
-              const uint32_t st = smem_addr(smem + s * C::kStageBytes);
+    const uint64_t policy = l2_evict_first_policy();
+    auto chunk_row = [&](int i) { return t0 + (warp + i * C::kWarps) * C::kCh; };  // first cache row of local chunk i
+    // Physical blocks of the next 32 (and following 32) chunks to issue, one per lane.
+    int tbl_cur = lane < my_chunks ? __ldg(table + chunk_row(lane) / p.block_size) : 0;
+    int tbl_next = 32 + lane < my_chunks ? __ldg(table + chunk_row(32 + lane) / p.block_size) : 0;
+    int issued = 0;
+
+    auto issue_next = [&]() {  // warp-uniform; lane 0 issues the copies
+      if (issued >= my_chunks) return;
+      if (issued > 0 && (issued & 31) == 0) {
+        tbl_cur = tbl_next;
+        const int k = issued + 32 + lane;
+        tbl_next = k < my_chunks ? __ldg(table + chunk_row(k) / p.block_size) : 0;
+      }
+      const int ph = __shfl_sync(0xffffffffu, tbl_cur, issued & 31);
+      const int s = issued % C::kStagesPerWarp;
+      if (lane == 0) {
+        const bool ok = static_cast<unsigned>(ph) < static_cast<unsigned>(p.num_blocks);
+        my_ok[s] = ok ? 1 : 0;
+        const uint32_t fb = smem_addr(&my_full[s]);
+        if (ok) {
+          fence_proxy_async_smem();  // this warp's reads of the stage precede the copy into it
+          mbar_arrive_expect_tx(fb, C::kTxBytes);
+          const int row = (ph * p.num_kv_heads + hk) * p.block_size + chunk_row(issued) % p.block_size;
+          const uint32_t st = smem_addr(my_ring + s * C::kStageBytes);
 #pragma unroll
-              for (int bx = 0; bx < C::kBoxes; ++bx) {
-                const int x = bx * (C::kRB / C::kElemBytes);
-                tma_load_2d(st + bx * C::kBoxBytes, &tmap_k, x, row, fb, policy);
-                tma_load_2d(st + C::kPlaneBytes + bx * C::kBoxBytes, &tmap_v, x, row, fb, policy);
-              }
-              if constexpr (C::kQuant) {
-                const size_t so = static_cast<size_t>(row) * C::kGroups;
-                const uint32_t sb = st + 2 * C::kPlaneBytes;
-                bulk_load(sb, p.k_scales + so, C::kSbBytes, fb, policy);
-                bulk_load(sb + C::kSbBytes, p.k_biases + so, C::kSbBytes, fb, policy);
-                bulk_load(sb + 2 * C::kSbBytes, p.v_scales + so, C::kSbBytes, fb, policy);
-                bulk_load(sb + 3 * C::kSbBytes, p.v_biases + so, C::kSbBytes, fb, policy);
-              }
-            } else {
-              if (p.error_flag) atomicOr(p.error_flag, kDevErrBadBlock);
-              mbar_arrive(fb);
-            }
-            issued = jj + 1;
+          for (int bx = 0; bx < C::kBoxes; ++bx) {
+            const int x = bx * (C::kRB / C::kElemBytes);
+            tma_load_2d(st + bx * C::kBoxBytes, &tmap_k, x, row, fb, policy);
+            tma_load_2d(st + C::kPlaneBytes + bx * C::kBoxBytes, &tmap_v, x, row, fb, policy);
           }
-        }
-        __syncwarp();
-        stop = __shfl_sync(0xffffffffu, static_cast<int>(*abort_flag), 0);  // one decision for the warp
-        if (stop) break;
-      }
-    }
-    if (lane == 0 && *abort_flag) {
-      // Let every copy still in flight land before the CTA's shared memory is reused.
-      for (int s = 0; s < C::kStages && s < issued; ++s) {
-        const int last = s + ((issued - 1 - s) / C::kStages) * C::kStages;
-        const uint32_t bar = smem_addr(&full_bar[s]);
-        const unsigned long long start = global_timer_ns();
-        while (!mbar_try_wait(bar, (last / C::kStages) & 1) && global_timer_ns() - start < kWaitLimitNs) {
+          if constexpr (C::kQuant) {
+            const size_t so = static_cast<size_t>(row) * C::kGroups;
+            const uint32_t sb = st + 2 * C::kPlaneBytes;
+            bulk_load(sb, p.k_scales + so, C::kSbBytes, fb, policy);
+            bulk_load(sb + C::kSbBytes, p.k_biases + so, C::kSbBytes, fb, policy);
+            bulk_load(sb + 2 * C::kSbBytes, p.v_scales + so, C::kSbBytes, fb, policy);
+            bulk_load(sb + 3 * C::kSbBytes, p.v_biases + so, C::kSbBytes, fb, policy);
+          }
+        } else {
+          if (p.error_flag) atomicOr(p.error_flag, kDevErrBadBlock);
+          mbar_arrive(fb);
         }
       }
-    }
-  } else {
-    // ------------------------------------------------------------------ consumers
+      ++issued;
+    };
+
+#pragma unroll 1
+    for (int s = 0; s < C::kStagesPerWarp; ++s) issue_next();
+
     // B fragments of Q^T for every k-step, rows r = 8*nt + g of this KV head.
     uint32_t qf[C::kKs][NT][2];
     const uint16_t* qrows = reinterpret_cast<const uint16_t*>(p.q) + row0 * D;
@@ -292,14 +286,16 @@ __global__ void __maxnreg__(200)
     const int lrow_n = (lane & 7) + ((lane >> 3) & 1) * 8, lch_n = lane >> 4;
     const int lrow_t = (lane & 7) + (lane >> 4) * 8, lch_t = (lane >> 3) & 1;
 
-    for (int jj = warp; jj < nchunks; jj += C::kWarps) {
-      const int s = jj % C::kStages;
-      if (!mbar_wait_warp(smem_addr(&full_bar[s]), (jj / C::kStages) & 1, abort_flag, p.error_flag)) break;
-      if (stage_ok[s]) {
-        const uint32_t kpl = smem_addr(smem + s * C::kStageBytes);
+    int done = 0;  // local chunks consumed
+    for (; done < my_chunks; ++done) {
+      const int s = done % C::kStagesPerWarp;
+      if (!mbar_wait_warp(smem_addr(&my_full[s]), (done / C::kStagesPerWarp) & 1, abort_flag, p.error_flag)) break;
+      if (my_ok[s]) {
+        uint8_t* stage = my_ring + s * C::kStageBytes;
+        const uint32_t kpl = smem_addr(stage);
         const uint32_t vpl = kpl + C::kPlaneBytes;
-        const __nv_bfloat16* sbp = reinterpret_cast<const __nv_bfloat16*>(smem + s * C::kStageBytes + 2 * C::kPlaneBytes);
-        const int kbase = t0 + jj * C::kCh;
+        const __nv_bfloat16* sbp = reinterpret_cast<const __nv_bfloat16*>(stage + 2 * C::kPlaneBytes);
+        const int kbase = chunk_row(done);
         const bool full_vis = kbase + C::kCh <= vis_base;
         const bool stale = kbase + C::kCh > len;
 
@@ -534,8 +530,17 @@ __global__ void __maxnreg__(200)
           }
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(&empty_bar[s]));
+      __syncwarp();   // every lane is done with the stage before it is refilled
+      issue_next();
+    }
+    if (done < issued && lane == 0) {
+      // Aborted: let this warp's copies still in flight land before the ring is reused.
+      for (int c = done; c < issued; ++c) {
+        const uint32_t bar = smem_addr(&my_full[c % C::kStagesPerWarp]);
+        const unsigned long long start = global_timer_ns();
+        while (!mbar_try_wait(bar, (c / C::kStagesPerWarp) & 1) && global_timer_ns() - start < kWaitLimitNs) {
+        }
+      }
     }
 
     // ---- per-warp totals: normaliser and value corrections summed over the 8 key lanes

@@ -153,6 +153,12 @@ def _draw_lengths(spec: DecodeSpec, gen: torch.Generator) -> list:
     return [int(x) for x in torch.randint(lo, hi + 1, (spec.num_seqs,), generator=gen)]
 
 
+def draw_lengths(spec: DecodeSpec, seed: Optional[int] = None) -> list:
+    """The seeded per-sequence lengths ``make_case`` uses for ``spec``."""
+    seed = spec.seed if seed is None else seed
+    return _draw_lengths(spec, torch.Generator(device="cpu").manual_seed(seed))
+
+
 def make_case(spec: DecodeSpec, device="cpu", seed: Optional[int] = None, poison: bool = True,
               lengths: Optional[list] = None) -> DecodeCase:
     """Draw one seeded instance of ``spec`` on ``device``.
