@@ -88,7 +88,7 @@ int plan_impl(const pkv_pool_layout* L, const pkv_decode_params* P, int sm_count
   const PartialInfo info = partial_info(L->bits, L->head_dim, ceil_div(nq, 8));
   out->partition_tokens = static_cast<int32_t>(part);
   out->max_partitions = max_parts;
-  out->chunk_rows = ch;
+  out->chunk_rows = info.chunk_rows;
   out->sm_count = sm_count;
   out->threads_per_cta = info.threads;
   out->smem_bytes = info.smem_bytes;

@@ -213,6 +213,18 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
   return y;
 }
 
+// Programmatic dependent launch: let the next kernel on the stream be scheduled
+// now (it still waits for this grid's completion before reading its results).
+__device__ __forceinline__ void allow_dependent_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Wait until the grids this kernel depends on have completed and their memory
+// operations are visible (no-op when launched without a programmatic dependency).
+__device__ __forceinline__ void wait_for_prerequisite_grids() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -229,36 +241,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   __half2 v = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
-}
-
-__device__ __forceinline__ float f16_lo_to_f32(uint32_t x) {
-  return __half2float(__ushort_as_half(static_cast<unsigned short>(x & 0xFFFFu)));
-}
-__device__ __forceinline__ float f16_hi_to_f32(uint32_t x) {
-  return __half2float(__ushort_as_half(static_cast<unsigned short>(x >> 16)));
-}
-
-// Two 4-bit fields at bits [0,4) and [16,20) of x as the fp16 pair
-// (1024 + lo_field, 1024 + hi_field): 0x6400 is fp16 1024.0, whose ulp is 1.
-__device__ __forceinline__ uint32_t nibbles_to_f16x2_biased(uint32_t x) {
-  return (x & 0x000F000Fu) | 0x64006400u;  // one LOP3
-}
-
-// Bytes `b0` and `b1` of x as the fp16 pair (1024 + byte b0, 1024 + byte b1): one PRMT
-// that interleaves the code bytes with the 0x64 exponent byte.
-template <int SEL>
-__device__ __forceinline__ uint32_t bytes_to_f16x2_biased(uint32_t x) {
-  return __byte_perm(x, 0x64646464u, SEL);
-}
-
-__device__ __forceinline__ float bf16_lo_to_f32(uint32_t x) { return __uint_as_float(x << 16); }
-__device__ __forceinline__ float bf16_hi_to_f32(uint32_t x) { return __uint_as_float(x & 0xFFFF0000u); }
-
-// Two 4-bit fields at bits [0,4) and [16,20) of x, turned into the bf16 pair
-// (128 + lo_field, 128 + hi_field): 0x4300 is bf16 128.0 and a field below 16
-// lands in its low mantissa bits, so each half is exact.
-__device__ __forceinline__ uint32_t nibbles_to_bf16x2_biased(uint32_t x) {
-  return (x & 0x000F000Fu) | 0x43004300u;  // one LOP3
 }
 
 // Shared-memory address of 16-byte chunk `chunk` of row `row` inside a TMA box

@@ -12,6 +12,7 @@ namespace pkv {
 __global__ void __launch_bounds__(64) pkv_merge_kernel(const __grid_constant__ MergeParams p) {
   const int row = blockIdx.x;
   const int d = threadIdx.x * 4;
+  wait_for_prerequisite_grids();  // launched early behind the partial pass; its states are ready after this
   if (d >= p.head_dim) return;
   const int b = row / p.rows_per_seq;
   const int len = p.seq_lens[b];
@@ -51,9 +52,17 @@ __global__ void __launch_bounds__(64) pkv_merge_kernel(const __grid_constant__ M
 }
 
 cudaError_t launch_merge(const MergeParams& p, int rows, cudaStream_t stream) {
-  const int threads = p.head_dim / 4 < 32 ? 32 : p.head_dim / 4;
-  pkv_merge_kernel<<<rows, threads, 0, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(rows);
+  cfg.blockDim = dim3(p.head_dim / 4 < 32 ? 32 : p.head_dim / 4);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // overlap with the partial pass's tail
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, pkv_merge_kernel, p);
 }
 
 // Grid (row blocks, KV head, sequence); one warp per logical row, lanes copy

@@ -27,16 +27,16 @@
 //    of O^T += V^T P^T. The online softmax (running max, normaliser, rescale)
 //    runs in f32 on the accumulators in base 2 (the softmax scale times log2 e
 //    is applied to the f32 scores; q itself is never re-rounded).
-//  * Affine pages never dequantise element by element. A code c enters the MMA
-//    as the exact bf16 value 128 + c, made by OR-ing the nibble into the
-//    mantissa of 128.0 (one LOP3 per two codes); 8-bit codes are split into
-//    their two nibbles, the high one weighted by 16. Per 64-dim group g:
-//        q.k = s_g * (sum_d q_d (128 + c_d)) + (b_g - 128 s_g) * sum_d q_d
-//    (offset 128 + 16*128 for 8-bit codes). The values go through fp16 MMA:
-//    a code enters as the exact fp16 value 1024 + c (nibble OR-ed into 1024.0,
-//    or a code byte permuted next to the 0x64 exponent byte: one PRMT per two
-//    codes), and with P'_g = p * s_g rounded to fp16,
-//        o_d = sum_t P'_g(t) (1024 + c_td) - 1024 sum_t P'_g(t) + sum_t p(t) b_g(t).
+//  * Affine pages never dequantise element by element. Both products run as
+//    fp16 MMAs in which a code c enters as the fp16 value with bit pattern c,
+//    i.e. the exact subnormal c * 2^-24 (a 4-bit field at bit 4 of a 16-bit
+//    half reads as 16 c * 2^-24, compensated by q/16 on the K side and by a
+//    1/16 m-tile factor on the V side). A pair of codes costs one LOP3 (4-bit)
+//    or one PRMT (8-bit), with no offset to undo. Per 64-dim group g,
+//        q.k = s_g * sum_d q_d c_d + b_g * sum_d q_d
+//    (q converted to fp16 with an exact per-row power-of-two prescale), and with
+//    P'_g = p * s_g rounded to fp16,
+//        o_d = sum_t P'_g(t) c_td + sum_t p(t) b_g(t).
 //    The scale/bias terms are per key and per group, so they cost a few FMAs per
 //    key instead of two per element.
 //  * Rows at or past seq_len in the last page are masked before they can reach
@@ -75,8 +75,7 @@ struct PartialCfg {
   static constexpr int kDataBytes = kRingBytes > kCombineBytes ? kRingBytes : kCombineBytes;
   static constexpr int kBarrierBytes = 256;
   static constexpr int kSmemBytes = kDataBytes + kBarrierBytes + 1024;  // + alignment slack
-  static constexpr float kOffsetK = BITS == 8 ? 2176.f : 128.f;  // code bias inside the K-side MMA (bf16)
-  static constexpr float kOffsetV = 1024.f;                        // code bias inside the V-side MMA (fp16)
+  static constexpr float kCodeUnit = 5.9604644775390625e-8f;  // 2^-24: value of fp16 bit pattern 1
 
   static_assert(kRB == 128 || kRB == 64, "box rows of 64 or 128 bytes");
   static_assert(kRowBytes % kRB == 0, "whole boxes per row");
@@ -104,8 +103,10 @@ __device__ __forceinline__ void q_dims(int kk, int reg, int t, int& d_lo, int& d
     d_lo = 16 * kk + 8 * reg + 2 * t;
     d_hi = d_lo + 1;
   } else if constexpr (BITS == 4) {
+    // word t of 16-byte chunk (2 grp + cc) holds dims base..base+7, nibble n = dim base+n;
+    // k-step s=0 takes nibbles (0,4) and (2,6), s=1 takes (1,5) and (3,7).
     const int grp = kk >> 2, cc = (kk >> 1) & 1, s = kk & 1;
-    const int base = 64 * grp + 32 * cc + 8 * t + 2 * s + reg;
+    const int base = 64 * grp + 32 * cc + 8 * t + s + 2 * reg;
     d_lo = base;
     d_hi = base + 4;
   } else {
@@ -116,10 +117,40 @@ __device__ __forceinline__ void q_dims(int kk, int reg, int t, int& d_lo, int& d
   }
 }
 
-__device__ __forceinline__ uint32_t bf16x2_times16(uint32_t x) {
-  __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&x);
-  v = __hmul2(v, __floats2bfloat162_rn(16.f, 16.f));
-  return *reinterpret_cast<uint32_t*>(&v);
+// 4-bit k-steps with odd index read their codes at bit 4 of each half (16 c); their
+// B fragments carry q / 16.
+template <int BITS>
+__device__ __forceinline__ bool q_over16(int kk) {
+  return BITS == 4 && (kk & 1);
+}
+
+// Factor that brings O^T m-tile `mt` of the V-side MMA back to code units (4-bit
+// m-tiles 4g+1 and 4g+3 read their nibble at bit 4: 16 c).
+template <int BITS>
+__device__ __forceinline__ float v_tile_factor(int mt) {
+  return (BITS == 4 && (mt & 1)) ? 1.f / 16.f : 1.f;
+}
+
+// Two consecutive bf16 values (low half first) as floats.
+__device__ __forceinline__ void bf16x2_to_f32(uint32_t w, float& lo, float& hi) {
+  lo = __uint_as_float(w << 16);
+  hi = __uint_as_float(w & 0xFFFF0000u);
+}
+
+// The G bf16 group values of one row of a scale/bias plane in shared memory.
+template <int G>
+__device__ __forceinline__ void load_group_row(uint32_t addr, float (&v)[G]) {
+  static_assert(G == 2 || G == 4, "head dims 128 or 256");
+  if constexpr (G == 4) {
+    uint32_t w0, w1;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(w0), "=r"(w1) : "r"(addr) : "memory");
+    bf16x2_to_f32(w0, v[0], v[1]);
+    bf16x2_to_f32(w1, v[2], v[3]);
+  } else {
+    uint32_t w0;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w0) : "r"(addr) : "memory");
+    bf16x2_to_f32(w0, v[0], v[1]);
+  }
 }
 
 template <int BITS, int D, int NT>
@@ -226,41 +257,87 @@ __global__ void __maxnreg__(200)
 #pragma unroll 1
     for (int s = 0; s < C::kStagesPerWarp; ++s) issue_next();
 
-    // B fragments of Q^T for every k-step, rows r = 8*nt + g of this KV head.
+    // B fragments of Q^T for every k-step, rows r = 8*nt + g of this KV head: bf16 as
+    // stored for bf16 pages; for affine pages fp16, after an exact power-of-two
+    // prescale per row that puts the row's largest |q| in [2^14, 2^15).
     uint32_t qf[C::kKs][NT][2];
-    const uint16_t* qrows = reinterpret_cast<const uint16_t*>(p.q) + row0 * D;
+    float colscale[NT][2];  // factor from accumulator to base-2 score, per query column 2t, 2t+1
+    float qsum[C::kQuant ? C::kGroups : 1][NT][2];  // affine: 2^-24 * sum of prescaled q over each group
+    {
+      const uint16_t* qrows = reinterpret_cast<const uint16_t*>(p.q) + row0 * D;
+      float qv[C::kKs][NT][4];
 #pragma unroll
-    for (int kk = 0; kk < C::kKs; ++kk) {
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const int r = 8 * nt + g;
-#pragma unroll
-        for (int reg = 0; reg < 2; ++reg) {
-          int dl, dh;
-          q_dims<BITS>(kk, reg, t, dl, dh);
-          uint32_t v = 0;
-          if (r < p.nq) {
-            v = static_cast<uint32_t>(__ldg(qrows + static_cast<size_t>(r) * D + dl)) |
-                (static_cast<uint32_t>(__ldg(qrows + static_cast<size_t>(r) * D + dh)) << 16);
-          }
-          qf[kk][nt][reg] = v;
-        }
-      }
-    }
-    // Per-group sums of q (columns 2t, 2t+1), through the same MMA path.
-    float qsum[C::kQuant ? C::kGroups : 1][NT][2];
-    if constexpr (C::kQuant) {
-      const uint32_t ones = 0x3F803F80u;  // bf16 (1.0, 1.0)
-#pragma unroll
-      for (int grp = 0; grp < C::kGroups; ++grp) {
+      for (int kk = 0; kk < C::kKs; ++kk) {
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
+          const int r = 8 * nt + g;
+#pragma unroll
+          for (int reg = 0; reg < 2; ++reg) {
+            int dl, dh;
+            q_dims<BITS>(kk, reg, t, dl, dh);
+            uint32_t lo = 0, hi = 0;
+            if (r < p.nq) {
+              lo = __ldg(qrows + static_cast<size_t>(r) * D + dl);
+              hi = __ldg(qrows + static_cast<size_t>(r) * D + dh);
+            }
+            qv[kk][nt][2 * reg] = __uint_as_float(lo << 16);
+            qv[kk][nt][2 * reg + 1] = __uint_as_float(hi << 16);
+          }
+        }
+      }
+      if constexpr (!C::kQuant) {
+#pragma unroll
+        for (int kk = 0; kk < C::kKs; ++kk)
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int reg = 0; reg < 2; ++reg)
+              qf[kk][nt][reg] = pack_bf16x2(qv[kk][nt][2 * reg], qv[kk][nt][2 * reg + 1]);  // exact
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) colscale[nt][0] = colscale[nt][1] = p.score_scale;
+      } else {
+        int kexp[NT];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          float mx = 0.f;
+#pragma unroll
+          for (int kk = 0; kk < C::kKs; ++kk)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) mx = fmaxf(mx, fabsf(qv[kk][nt][i]));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));  // the row's max over its 4 lanes
+          const int e = static_cast<int>((__float_as_uint(mx) >> 23) & 0xFF) - 127;
+          kexp[nt] = mx > 0.f ? min(max(14 - e, -100), 126) : 0;  // |q| below 2^114 is assumed
+          const float up = __uint_as_float(static_cast<uint32_t>(127 + kexp[nt]) << 23);  // 2^kexp
           float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int k = 0; k < 4; ++k) mma_bf16(acc, ones, ones, ones, ones, qf[4 * grp + k][nt][0], qf[4 * grp + k][nt][1]);
-          qsum[grp][nt][0] = acc[0];
-          qsum[grp][nt][1] = acc[1];
+          for (int kk = 0; kk < C::kKs; ++kk) {
+            uint32_t fr[2];
+#pragma unroll
+            for (int reg = 0; reg < 2; ++reg)
+              fr[reg] = pack_f16x2(qv[kk][nt][2 * reg] * up, qv[kk][nt][2 * reg + 1] * up);
+            // Per-group sums of the prescaled q (columns 2t, 2t+1), through the MMA path.
+            mma_f16(acc, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u, fr[0], fr[1]);
+            if ((kk & 3) == 3) {
+              qsum[kk >> 2][nt][0] = acc[0] * C::kCodeUnit;
+              qsum[kk >> 2][nt][1] = acc[1] * C::kCodeUnit;
+              acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+            }
+            const float f = q_over16<BITS>(kk) ? up * (1.f / 16.f) : up;
+#pragma unroll
+            for (int reg = 0; reg < 2; ++reg)
+              qf[kk][nt][reg] = pack_f16x2(qv[kk][nt][2 * reg] * f, qv[kk][nt][2 * reg + 1] * f);
+          }
         }
+        // Column c = 2t + e2 of n-tile nt is query row 8 nt + 2t + e2, prescaled by the
+        // lanes whose g equals 2t + e2. Codes are counted in units of 2^-24.
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int e2 = 0; e2 < 2; ++e2) {
+            const int k = __shfl_sync(0xffffffffu, kexp[nt], (2 * t + e2) * 4);
+            colscale[nt][e2] = p.score_scale * __uint_as_float(static_cast<uint32_t>(127 + 24 - k) << 23);
+          }
       }
     }
 
@@ -294,7 +371,7 @@ __global__ void __maxnreg__(200)
         uint8_t* stage = my_ring + s * C::kStageBytes;
         const uint32_t kpl = smem_addr(stage);
         const uint32_t vpl = kpl + C::kPlaneBytes;
-        const __nv_bfloat16* sbp = reinterpret_cast<const __nv_bfloat16*>(stage + 2 * C::kPlaneBytes);
+        const uint32_t sbq = kpl + 2 * C::kPlaneBytes;  // scale/bias planes (affine pages)
         const int kbase = chunk_row(done);
         const bool full_vis = kbase + C::kCh <= vis_base;
         const bool stale = kbase + C::kCh > len;
@@ -318,8 +395,12 @@ __global__ void __maxnreg__(200)
               for (int nt = 0; nt < NT; ++nt) mma_bf16(sacc[nt], a[0], a[1], a[2], a[3], qf[kk][nt][0], qf[kk][nt][1]);
             }
           } else {
-            const __nv_bfloat16* ksp = sbp;
-            const __nv_bfloat16* kbp = sbp + C::kCh * C::kGroups;
+            // scales and biases of keys g and g + 8 of this tile, all groups
+            float ks0[C::kGroups], ks1[C::kGroups], kb0[C::kGroups], kb1[C::kGroups];
+            load_group_row<C::kGroups>(sbq + (tile * 16 + g) * C::kGroups * 2, ks0);
+            load_group_row<C::kGroups>(sbq + (tile * 16 + g + 8) * C::kGroups * 2, ks1);
+            load_group_row<C::kGroups>(sbq + C::kSbBytes + (tile * 16 + g) * C::kGroups * 2, kb0);
+            load_group_row<C::kGroups>(sbq + C::kSbBytes + (tile * 16 + g + 8) * C::kGroups * 2, kb1);
 #pragma unroll
             for (int grp = 0; grp < C::kGroups; ++grp) {
               float sg[NT][4];
@@ -328,19 +409,20 @@ __global__ void __maxnreg__(200)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) sg[nt][e] = 0.f;
               if constexpr (BITS == 4) {
+                // words t of chunks 2 grp, 2 grp + 1 for rows g, g + 8
                 uint32_t xk[4];
                 ldsm_x4(swizzled<C::kRB>(kpl, lrow, 2 * grp + lch_n), xk);
 #pragma unroll
                 for (int cc = 0; cc < 2; ++cc) {
+                  const uint32_t xg = xk[2 * cc], x8 = xk[2 * cc + 1];
+                  const uint32_t xg8 = xg >> 8, x88 = x8 >> 8;
 #pragma unroll
-                  for (int sft = 0; sft < 2; ++sft) {
-                    const int kk = 4 * grp + 2 * cc + sft;
-                    const uint32_t a0 = nibbles_to_bf16x2_biased(xk[2 * cc] >> (8 * sft));
-                    const uint32_t a1 = nibbles_to_bf16x2_biased(xk[2 * cc + 1] >> (8 * sft));
-                    const uint32_t a2 = nibbles_to_bf16x2_biased(xk[2 * cc] >> (8 * sft + 4));
-                    const uint32_t a3 = nibbles_to_bf16x2_biased(xk[2 * cc + 1] >> (8 * sft + 4));
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) mma_bf16(sg[nt], a0, a1, a2, a3, qf[kk][nt][0], qf[kk][nt][1]);
+                  for (int nt = 0; nt < NT; ++nt) {
+                    const int kk = 4 * grp + 2 * cc;
+                    mma_f16(sg[nt], xg & 0x000F000Fu, x8 & 0x000F000Fu, xg8 & 0x000F000Fu, x88 & 0x000F000Fu,
+                            qf[kk][nt][0], qf[kk][nt][1]);
+                    mma_f16(sg[nt], xg & 0x00F000F0u, x8 & 0x00F000F0u, xg8 & 0x00F000F0u, x88 & 0x00F000F0u,
+                            qf[kk + 1][nt][0], qf[kk + 1][nt][1]);
                   }
                 }
               } else {
@@ -352,37 +434,28 @@ __global__ void __maxnreg__(200)
                   for (int cc = 0; cc < 2; ++cc) {
                     const int kk = 4 * grp + 2 * h + cc;
                     const uint32_t xg = xk[2 * cc], x8 = xk[2 * cc + 1];
+                    // bytes (0, 2) and (1, 3) of a word: dims (4t, 4t+2) and (4t+1, 4t+3)
 #pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                      mma_bf16(sg[nt], nibbles_to_bf16x2_biased(xg), nibbles_to_bf16x2_biased(x8),
-                               nibbles_to_bf16x2_biased(xg >> 8), nibbles_to_bf16x2_biased(x8 >> 8),
-                               qf[kk][nt][0], qf[kk][nt][1]);
-                      mma_bf16(sg[nt], nibbles_to_bf16x2_biased(xg >> 4), nibbles_to_bf16x2_biased(x8 >> 4),
-                               nibbles_to_bf16x2_biased(xg >> 12), nibbles_to_bf16x2_biased(x8 >> 12),
-                               bf16x2_times16(qf[kk][nt][0]), bf16x2_times16(qf[kk][nt][1]));
-                    }
+                    for (int nt = 0; nt < NT; ++nt)
+                      mma_f16(sg[nt], __byte_perm(xg, 0u, 0x4240), __byte_perm(x8, 0u, 0x4240),
+                              __byte_perm(xg, 0u, 0x4341), __byte_perm(x8, 0u, 0x4341), qf[kk][nt][0], qf[kk][nt][1]);
                   }
                 }
               }
               // fold the affine terms of group grp for keys g and g + 8 of this tile
-              const int r_a = tile * 16 + g, r_b = r_a + 8;
-              const float ks0 = __bfloat162float(ksp[r_a * C::kGroups + grp]);
-              const float ks1 = __bfloat162float(ksp[r_b * C::kGroups + grp]);
-              const float kb0 = __bfloat162float(kbp[r_a * C::kGroups + grp]) - C::kOffsetK * ks0;
-              const float kb1 = __bfloat162float(kbp[r_b * C::kGroups + grp]) - C::kOffsetK * ks1;
 #pragma unroll
               for (int nt = 0; nt < NT; ++nt) {
-                sacc[nt][0] = fmaf(ks0, sg[nt][0], fmaf(kb0, qsum[grp][nt][0], sacc[nt][0]));
-                sacc[nt][1] = fmaf(ks0, sg[nt][1], fmaf(kb0, qsum[grp][nt][1], sacc[nt][1]));
-                sacc[nt][2] = fmaf(ks1, sg[nt][2], fmaf(kb1, qsum[grp][nt][0], sacc[nt][2]));
-                sacc[nt][3] = fmaf(ks1, sg[nt][3], fmaf(kb1, qsum[grp][nt][1], sacc[nt][3]));
+                sacc[nt][0] = fmaf(ks0[grp], sg[nt][0], fmaf(kb0[grp], qsum[grp][nt][0], sacc[nt][0]));
+                sacc[nt][1] = fmaf(ks0[grp], sg[nt][1], fmaf(kb0[grp], qsum[grp][nt][1], sacc[nt][1]));
+                sacc[nt][2] = fmaf(ks1[grp], sg[nt][2], fmaf(kb1[grp], qsum[grp][nt][0], sacc[nt][2]));
+                sacc[nt][3] = fmaf(ks1[grp], sg[nt][3], fmaf(kb1[grp], qsum[grp][nt][1], sacc[nt][3]));
               }
             }
           }
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) x[tile][nt][e] = sacc[nt][e] * p.score_scale;
+            for (int e = 0; e < 4; ++e) x[tile][nt][e] = sacc[nt][e] * colscale[nt][e & 1];
         }
 
         // ---- causal tail and stale rows
@@ -475,39 +548,50 @@ __global__ void __maxnreg__(200)
               for (int nt = 0; nt < NT; ++nt) mma_bf16(o[mt][nt], a[0], a[1], a[2], a[3], pb[nt][0], pb[nt][1]);
             }
           } else {
-            const __nv_bfloat16* vsp = sbp + 2 * C::kCh * C::kGroups;
-            const __nv_bfloat16* vbp = sbp + 3 * C::kCh * C::kGroups;
             const int r_a = tile * 16 + g, r_b = r_a + 8;
-            const bool va = !stale || kbase + r_a < len, vb = !stale || kbase + r_b < len;
+            float vs0[C::kGroups], vs1[C::kGroups], vb0[C::kGroups], vb1[C::kGroups];
+            load_group_row<C::kGroups>(sbq + 2 * C::kSbBytes + r_a * C::kGroups * 2, vs0);
+            load_group_row<C::kGroups>(sbq + 2 * C::kSbBytes + r_b * C::kGroups * 2, vs1);
+            load_group_row<C::kGroups>(sbq + 3 * C::kSbBytes + r_a * C::kGroups * 2, vb0);
+            load_group_row<C::kGroups>(sbq + 3 * C::kSbBytes + r_b * C::kGroups * 2, vb1);
+            if (stale) {  // rows at or past len may hold anything: keep them out of P' and the bias sums
+              const bool va = kbase + r_a < len, vb = kbase + r_b < len;
+#pragma unroll
+              for (int grp = 0; grp < C::kGroups; ++grp) {
+                vs0[grp] = va ? vs0[grp] : 0.f;
+                vb0[grp] = va ? vb0[grp] : 0.f;
+                vs1[grp] = vb ? vs1[grp] : 0.f;
+                vb1[grp] = vb ? vb1[grp] : 0.f;
+              }
+            }
 #pragma unroll
             for (int grp = 0; grp < C::kGroups; ++grp) {
-              const float vs0 = va ? __bfloat162float(vsp[r_a * C::kGroups + grp]) : 0.f;
-              const float vs1 = vb ? __bfloat162float(vsp[r_b * C::kGroups + grp]) : 0.f;
-              const float vb0 = va ? __bfloat162float(vbp[r_a * C::kGroups + grp]) : 0.f;
-              const float vb1 = vb ? __bfloat162float(vbp[r_b * C::kGroups + grp]) : 0.f;
               uint32_t pb[NT][2];
 #pragma unroll
               for (int nt = 0; nt < NT; ++nt) {
-                const uint32_t lo = pack_f16x2(pr[tile][nt][0] * vs0, pr[tile][nt][1] * vs0);
-                const uint32_t hi = pack_f16x2(pr[tile][nt][2] * vs1, pr[tile][nt][3] * vs1);
-                pb[nt][0] = movmatrix_trans(lo);
-                pb[nt][1] = movmatrix_trans(hi);
-                corr_v[grp][nt][0] += fmaf(pr[tile][nt][0], vb0, pr[tile][nt][2] * vb1) -
-                                       C::kOffsetV * (f16_lo_to_f32(lo) + f16_lo_to_f32(hi));
-                corr_v[grp][nt][1] += fmaf(pr[tile][nt][1], vb0, pr[tile][nt][3] * vb1) -
-                                       C::kOffsetV * (f16_hi_to_f32(lo) + f16_hi_to_f32(hi));
+                pb[nt][0] = movmatrix_trans(pack_f16x2(pr[tile][nt][0] * vs0[grp], pr[tile][nt][1] * vs0[grp]));
+                pb[nt][1] = movmatrix_trans(pack_f16x2(pr[tile][nt][2] * vs1[grp], pr[tile][nt][3] * vs1[grp]));
+                corr_v[grp][nt][0] = fmaf(pr[tile][nt][0], vb0[grp], fmaf(pr[tile][nt][2], vb1[grp], corr_v[grp][nt][0]));
+                corr_v[grp][nt][1] = fmaf(pr[tile][nt][1], vb0[grp], fmaf(pr[tile][nt][3], vb1[grp], corr_v[grp][nt][1]));
               }
               if constexpr (BITS == 4) {
+                // y: unit g (dims 4g..4g+3) of keys 2t (low half) and 2t+1 (high half),
+                // chunks 2 grp / 2 grp + 1, keys 0-7 / 8-15 of the tile
                 uint32_t y[4];
                 ldsm_x4_t(swizzled<C::kRB>(vpl, lrow, 2 * grp + lch_t), y);
+                uint32_t y8[4];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                  const uint32_t a0 = nibbles_to_f16x2_biased(y[0] >> (4 * j));
-                  const uint32_t a1 = nibbles_to_f16x2_biased(y[1] >> (4 * j));
-                  const uint32_t a2 = nibbles_to_f16x2_biased(y[2] >> (4 * j));
-                  const uint32_t a3 = nibbles_to_f16x2_biased(y[3] >> (4 * j));
+                for (int i = 0; i < 4; ++i) y8[i] = y[i] >> 8;
 #pragma unroll
-                  for (int nt = 0; nt < NT; ++nt) mma_f16(o[4 * grp + j][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
+                for (int nt = 0; nt < NT; ++nt) {
+                  mma_f16(o[4 * grp + 0][nt], y[0] & 0x000F000Fu, y[1] & 0x000F000Fu, y[2] & 0x000F000Fu,
+                          y[3] & 0x000F000Fu, pb[nt][0], pb[nt][1]);
+                  mma_f16(o[4 * grp + 1][nt], y[0] & 0x00F000F0u, y[1] & 0x00F000F0u, y[2] & 0x00F000F0u,
+                          y[3] & 0x00F000F0u, pb[nt][0], pb[nt][1]);
+                  mma_f16(o[4 * grp + 2][nt], y8[0] & 0x000F000Fu, y8[1] & 0x000F000Fu, y8[2] & 0x000F000Fu,
+                          y8[3] & 0x000F000Fu, pb[nt][0], pb[nt][1]);
+                  mma_f16(o[4 * grp + 3][nt], y8[0] & 0x00F000F0u, y8[1] & 0x00F000F0u, y8[2] & 0x00F000F0u,
+                          y8[3] & 0x00F000F0u, pb[nt][0], pb[nt][1]);
                 }
               } else {
 #pragma unroll
@@ -517,12 +601,10 @@ __global__ void __maxnreg__(200)
                   // byte 0 / byte 2 of y: dim 2g of keys 2t / 2t+1; bytes 1 / 3: dim 2g + 1
 #pragma unroll
                   for (int nt = 0; nt < NT; ++nt) {
-                    mma_f16(o[4 * grp + 2 * h][nt], bytes_to_f16x2_biased<0x4240>(y[0]),
-                            bytes_to_f16x2_biased<0x4240>(y[1]), bytes_to_f16x2_biased<0x4240>(y[2]),
-                            bytes_to_f16x2_biased<0x4240>(y[3]), pb[nt][0], pb[nt][1]);
-                    mma_f16(o[4 * grp + 2 * h + 1][nt], bytes_to_f16x2_biased<0x4341>(y[0]),
-                            bytes_to_f16x2_biased<0x4341>(y[1]), bytes_to_f16x2_biased<0x4341>(y[2]),
-                            bytes_to_f16x2_biased<0x4341>(y[3]), pb[nt][0], pb[nt][1]);
+                    mma_f16(o[4 * grp + 2 * h][nt], __byte_perm(y[0], 0u, 0x4240), __byte_perm(y[1], 0u, 0x4240),
+                            __byte_perm(y[2], 0u, 0x4240), __byte_perm(y[3], 0u, 0x4240), pb[nt][0], pb[nt][1]);
+                    mma_f16(o[4 * grp + 2 * h + 1][nt], __byte_perm(y[0], 0u, 0x4341), __byte_perm(y[1], 0u, 0x4341),
+                            __byte_perm(y[2], 0u, 0x4341), __byte_perm(y[3], 0u, 0x4341), pb[nt][0], pb[nt][1]);
                   }
                 }
               }
@@ -571,10 +653,12 @@ __global__ void __maxnreg__(200)
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) o[mt][nt][e] += corr_v[mt >> 2][nt][e & 1];
+          for (int e = 0; e < 4; ++e)
+            o[mt][nt][e] = fmaf(o[mt][nt][e], (1.f / C::kCodeUnit) * v_tile_factor<BITS>(mt), corr_v[mt >> 2][nt][e & 1]);
     }
   }
 
+  allow_dependent_launch();  // the merge pass may be scheduled while this epilogue runs
   __syncthreads();  // every stage consumed, every copy landed: the stage ring is free
 
   // ---- combine the consumer warps' states and write out

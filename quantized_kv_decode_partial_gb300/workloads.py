@@ -19,7 +19,8 @@ random 32-bit words, so the generator draws words directly and never packs.
 
 Stale storage is poisoned with NaN so that any read of it shows up: blocks
 that no table references, and the rows at or past ``len`` in each sequence's
-last page ("stale bytes past offset are never read", cache.ts ``trim``).
+last page (the cache's trim leaves old bytes there and reads stop at the
+sequence length, cache.ts ``trim``).
 For affine pages the scales of those rows are NaN.
 """
 
