@@ -74,6 +74,10 @@ extern "C" {
 #define PKV_ERR_UNSUPPORTED_SHAPE (-5)   /* (num_q_heads/num_kv_heads)*n_query above the limit for head_dim */
 #define PKV_ERR_WORKSPACE_TOO_SMALL (-6) /* workspace NULL or smaller than pkv_plan.workspace_bytes */
 #define PKV_ERR_CUDA (-7)                /* a CUDA runtime or driver call failed */
+#define PKV_ERR_SCRATCH_TOO_SMALL (-8)   /* no-alloc entry: partition states larger than its static scratch */
+
+/* Size of the static device scratch behind pkv_paged_decode_attention_no_alloc. */
+#define PKV_STATIC_SCRATCH_BYTES (16u << 20)
 
 /* Device-side error bits, OR-ed into *error_flag. */
 #define PKV_DEVERR_BAD_BLOCK 1   /* a referenced block id outside [0, num_blocks): its rows were skipped */
@@ -156,6 +160,39 @@ int pkv_paged_decode_partial(const pkv_pool_layout* layout, const pkv_decode_par
 int pkv_merge_partitions(const pkv_pool_layout* layout, const pkv_decode_params* params,
                          const int32_t* seq_lens, const void* workspace, size_t workspace_bytes, void* out,
                          int32_t* error_flag, void* stream);
+
+/* pkv_paged_decode_attention for callers that cannot allocate device memory.
+ * The pages have no counterpart of this entry point.
+ *
+ * Some callers cannot call cudaMalloc: runtimes whose device memory is owned by
+ * their own allocator, which reserves every byte up front and forbids other
+ * allocations, and plugins that are handed only the tensors of one call. They
+ * cannot provide the workspace the main entry point needs. This entry point
+ * needs none. It keeps the f32 partition states in a file-scope static device
+ * array of PKV_STATIC_SCRATCH_BYTES (16 MiB), which every GPU that loads the
+ * library holds until the process exits. It calls no cudaMalloc, cudaFree or
+ * allocating library routine. The caller still passes every input and `out`.
+ *
+ * Arguments and results are those of pkv_paged_decode_attention, without the
+ * workspace. With partition_tokens = 0 the library picks the partition size as
+ * usual and coarsens it until the states fit (one partition needs no scratch).
+ * A caller-fixed partition_tokens whose states would exceed the scratch is
+ * rejected with PKV_ERR_SCRATCH_TOO_SMALL.
+ *
+ * Set-up: the first call on each device looks up the scratch's device address
+ * (cudaGetSymbolAddress, with that device current) and caches it. Make that
+ * first call before any stream capture on the device.
+ *
+ * Sharing: every call on a device uses the same scratch, which keeps the last
+ * call's contents; nothing in it needs to start at zero. Calls whose kernels
+ * overlap on the GPU (different streams, or concurrent host threads) race on
+ * the scratch and must be ordered by the caller. */
+int pkv_paged_decode_attention_no_alloc(const pkv_pool_layout* layout, const pkv_decode_params* params,
+                                        const void* q, const void* k_pool, const void* v_pool,
+                                        const void* k_scales, const void* k_biases, const void* v_scales,
+                                        const void* v_biases, const int32_t* block_tables,
+                                        const int32_t* seq_lens, float scale, void* out, int32_t* error_flag,
+                                        void* stream);
 
 /* Bit-exact gather of one pool plane into contiguous per-sequence rows, the
  * fetch copy of the pages' BlockPool.gather / pickBlocks (state/paged/cache.ts):

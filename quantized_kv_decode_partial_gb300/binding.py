@@ -22,6 +22,7 @@ EXPORTS = (
     "pkv_paged_decode_attention",
     "pkv_paged_decode_partial",
     "pkv_merge_partitions",
+    "pkv_paged_decode_attention_no_alloc",
     "pkv_paged_gather",
     "pkv_strerror",
     "pkv_last_cuda_error",
@@ -36,6 +37,8 @@ PKV_ERR_BAD_PARAMS = -4
 PKV_ERR_UNSUPPORTED_SHAPE = -5
 PKV_ERR_WORKSPACE_TOO_SMALL = -6
 PKV_ERR_CUDA = -7
+PKV_ERR_SCRATCH_TOO_SMALL = -8
+PKV_STATIC_SCRATCH_BYTES = 16 << 20
 
 PKV_DEVERR_BAD_BLOCK = 1
 PKV_DEVERR_BAD_SEQ_LEN = 2
@@ -95,6 +98,9 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.pkv_merge_partitions.argtypes = [ctypes.POINTER(PoolLayout), ctypes.POINTER(DecodeParams), P, P, SZ, P,
                                          P, P]
     lib.pkv_merge_partitions.restype = ctypes.c_int
+    lib.pkv_paged_decode_attention_no_alloc.argtypes = [ctypes.POINTER(PoolLayout), ctypes.POINTER(DecodeParams),
+                                                        P, P, P, P, P, P, P, P, P, F, P, P, P]
+    lib.pkv_paged_decode_attention_no_alloc.restype = ctypes.c_int
     lib.pkv_paged_gather.argtypes = [P, I32, I32, I32, I32, P, P, I32, I32, I32, P, P, P]
     lib.pkv_paged_gather.restype = ctypes.c_int
     lib.pkv_strerror.argtypes = [ctypes.c_int]

@@ -5,6 +5,7 @@
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 
 #include "pkv_decode.h"
 #include "pkv_launch.h"
@@ -344,6 +345,91 @@ int pkv_paged_gather(const void* pool, int32_t num_blocks, int32_t num_kv_heads,
   return PKV_OK;
 }
 
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// The entry point that allocates nothing (pkv_paged_decode_attention_no_alloc)
+// ---------------------------------------------------------------------------
+namespace {
+
+// Scratch for the partition states of the no-alloc entry point. Every GPU that
+// loads this library holds it until the process exits; every call on a device
+// shares it.
+static __device__ __align__(256) unsigned char g_static_scratch[PKV_STATIC_SCRATCH_BYTES];
+
+constexpr int kMaxScratchDevices = 256;
+std::mutex g_scratch_mutex;
+void* g_scratch_address[kMaxScratchDevices] = {};
+
+// Device address of g_static_scratch on the current device. Host code only has a
+// host-side stand-in for the array's name, so the address is looked up once per
+// device, with that device current, and cached.
+int static_scratch_address(void** ptr) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail("cudaGetDevice", e);
+  if (dev < 0 || dev >= kMaxScratchDevices) return PKV_ERR_BAD_PARAMS;
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  if (!g_scratch_address[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e != cudaSuccess) return cuda_fail("cudaGetSymbolAddress", e);
+    g_scratch_address[dev] = p;
+  }
+  *ptr = g_scratch_address[dev];
+  return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pkv_paged_decode_attention_no_alloc(const pkv_pool_layout* layout, const pkv_decode_params* params,
+                                        const void* q, const void* k_pool, const void* v_pool,
+                                        const void* k_scales, const void* k_biases, const void* v_scales,
+                                        const void* v_biases, const int32_t* block_tables,
+                                        const int32_t* seq_lens, float scale, void* out, int32_t* error_flag,
+                                        void* stream) {
+  int rc = check_layout(layout);
+  if (rc) return rc;
+  rc = check_params(layout, params);
+  if (rc) return rc;
+  const bool quant = layout->bits != 16;
+  if (!q || !k_pool || !v_pool || !block_tables || !seq_lens || !out) return PKV_ERR_NULL_POINTER;
+  if (quant && (!k_scales || !k_biases || !v_scales || !v_biases)) return PKV_ERR_NULL_POINTER;
+  if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(out, 16) ||
+      !aligned(block_tables, 4) || !aligned(seq_lens, 4) || !aligned(error_flag, 4))
+    return PKV_ERR_MISALIGNED;
+  if (quant && (!aligned(k_scales, 16) || !aligned(k_biases, 16) || !aligned(v_scales, 16) || !aligned(v_biases, 16)))
+    return PKV_ERR_MISALIGNED;
+
+  int sms = 0;
+  rc = device_sm_count(&sms);
+  if (rc) return rc;
+  pkv_decode_params local = *params;
+  pkv_plan plan;
+  rc = plan_impl(layout, &local, sms, &plan);
+  if (rc) return rc;
+  if (plan.workspace_bytes > PKV_STATIC_SCRATCH_BYTES) {
+    if (params->partition_tokens > 0) return PKV_ERR_SCRATCH_TOO_SMALL;  // the caller's partition size does not fit
+    // A library-chosen plan coarsens its partitions until their states fit
+    // (a single partition needs no scratch at all).
+    long long part = plan.partition_tokens;
+    while (plan.workspace_bytes > PKV_STATIC_SCRATCH_BYTES) {
+      part *= 2;
+      local.partition_tokens = static_cast<int32_t>(part < (1ll << 30) ? part : (1ll << 30));
+      rc = plan_impl(layout, &local, sms, &plan);
+      if (rc) return rc;
+    }
+  }
+  void* scratch = nullptr;
+  rc = static_scratch_address(&scratch);
+  if (rc) return rc;
+  return pkv_paged_decode_attention(layout, &local, q, k_pool, v_pool, k_scales, k_biases, v_scales, v_biases,
+                                    block_tables, seq_lens, scale, out, scratch, PKV_STATIC_SCRATCH_BYTES,
+                                    error_flag, stream);
+}
+
 const char* pkv_strerror(int code) {
   switch (code) {
     case PKV_OK: return "success";
@@ -354,6 +440,9 @@ const char* pkv_strerror(int code) {
     case PKV_ERR_UNSUPPORTED_SHAPE: return "too many query rows per KV head for this head_dim";
     case PKV_ERR_WORKSPACE_TOO_SMALL: return "workspace missing or smaller than the plan needs";
     case PKV_ERR_CUDA: return "a CUDA call failed (see pkv_last_cuda_error)";
+    case PKV_ERR_SCRATCH_TOO_SMALL:
+      return "the partition states exceed the static scratch of the no-alloc entry point (PKV_STATIC_SCRATCH_BYTES); "
+             "use larger partition_tokens or 0";
     default: return "unknown error code";
   }
 }

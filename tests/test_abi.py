@@ -39,7 +39,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_version_and_messages(lib):
     assert lib.pkv_version() >= 100
-    for code in range(0, -8, -1):
+    for code in range(0, -9, -1):
         msg = lib.pkv_strerror(code).decode()
         assert msg and msg != "unknown error code"
     assert lib.pkv_strerror(-99).decode() == "unknown error code"
