@@ -51,7 +51,7 @@ def parse_args(argv=None):
     ap.add_argument("--num-seqs", type=int, default=0,
                     help="profiling mode: keep only the first N sequences of the workload")
     ap.add_argument("--partition-tokens", type=int, default=-2,
-                    help="profiling mode: rows per partition instead of the workload's choice")
+                    help="rows per partition instead of the workload's choice (0: the library's plan)")
     return ap.parse_args(argv)
 
 
@@ -246,6 +246,8 @@ def run_reference(args):
 # ---------------------------------------------------------------------------
 
 def run_ours(args):
+    from dataclasses import replace
+
     import torch
     import torch.distributed as dist
 
@@ -274,6 +276,8 @@ def run_ours(args):
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     layers = []
     for sp in specs:
+        if args.partition_tokens != -2:
+            sp = replace(sp, partition_tokens=args.partition_tokens)
         base = make_case(sp, device=dev, seed=rank_seed(sp.seed, rank), poison=False)
         in_bytes = sum(t.numel() * t.element_size() for t in
                        (base.q, base.k_pool, base.v_pool, base.k_scales, base.k_biases, base.v_scales, base.v_biases,
@@ -283,7 +287,7 @@ def run_ours(args):
                                     lengths=base.lens_host) for c in range(copies - 1)]
         layout = layout_for(base.k_pool, sp.head_dim, sp.bits, sp.group_size)
         params = DecodeParams(sp.num_seqs, sp.num_q_heads, sp.n_query, base.block_tables.shape[1],
-                              base.partition_tokens)
+                              base.partition_tokens, sp.window)
         plan = make_plan(layout, params)
         ws = torch.empty(max(1, plan.workspace_bytes), dtype=torch.uint8, device=dev)
         out = torch.empty_like(base.q)
@@ -296,8 +300,8 @@ def run_ours(args):
         c = L["insts"][i % L["copies"]]
         sp = L["spec"]
         kw = dict(bits=sp.bits, group_size=sp.group_size, k_scales=c.k_scales, k_biases=c.k_biases,
-                  v_scales=c.v_scales, v_biases=c.v_biases, partition_tokens=c.partition_tokens, out=L["out"],
-                  workspace=L["ws"])
+                  v_scales=c.v_scales, v_biases=c.v_biases, partition_tokens=c.partition_tokens, window=sp.window,
+                  out=L["out"], workspace=L["ws"])
         if passes is None:
             paged_decode_attention(c.q, c.k_pool, c.v_pool, c.block_tables, c.seq_lens, c.scale, **kw)
         else:
@@ -364,28 +368,39 @@ def run_ours(args):
     ms_partial = replay_timed([(g_part, K // chunk)] + ([(g_part_rest, 1)] if g_part_rest else []))
 
     # end to end through the public call: per step, q / tables / lengths come from
-    # pinned host memory, the output goes back to pinned host memory
-    host_in, host_out = [], []
+    # pinned host memory (one packed staging copy per layer) and the output goes back
+    # to pinned host memory
+    stage_host, stage_dev, views, host_out = [], [], [], []
     for L in layers:
         c = L["insts"][0]
-        host_in.append([t.cpu().pin_memory() for t in (c.q, c.block_tables, c.seq_lens)])
+        parts = [c.q, c.block_tables, c.seq_lens]
+        sizes = [t.numel() * t.element_size() for t in parts]
+        offs = [sum(-(-x // 256) * 256 for x in sizes[:i]) for i in range(len(sizes))]
+        total = offs[-1] + sizes[-1]
+        hbuf = torch.empty(total, dtype=torch.uint8, pin_memory=True)
+        dbuf = torch.empty(total, dtype=torch.uint8, device=dev)
+        v_dev = []
+        for t, o, n in zip(parts, offs, sizes):
+            hbuf[o:o + n].copy_(t.contiguous().view(torch.uint8).reshape(-1).cpu())
+            v_dev.append(dbuf[o:o + n].view(t.dtype).view(t.shape))
+        stage_host.append(hbuf)
+        stage_dev.append(dbuf)
+        views.append(v_dev)
         host_out.append(torch.empty(L["out"].shape, dtype=L["out"].dtype, pin_memory=True))
-    h2d = sum(t.numel() * t.element_size() for hs in host_in for t in hs)
+    h2d = sum(t.numel() for t in stage_host)
     d2h = sum(t.numel() * t.element_size() for t in host_out)
-    dev_in = [[torch.empty_like(t, device=dev) for t in hs] for hs in host_in]
     e2e_steps = min(K, 50)
 
     def e2e_once():
         for li, L in enumerate(layers):
-            for src, dst in zip(host_in[li], dev_in[li]):
-                dst.copy_(src, non_blocking=True)
+            stage_dev[li].copy_(stage_host[li], non_blocking=True)
             c = L["insts"][0]
             sp = L["spec"]
-            q, tb, sl = dev_in[li]
+            q, tb, sl = views[li]
             paged_decode_attention(q, c.k_pool, c.v_pool, tb, sl, c.scale, bits=sp.bits, group_size=sp.group_size,
                                    k_scales=c.k_scales, k_biases=c.k_biases, v_scales=c.v_scales,
-                                   v_biases=c.v_biases, partition_tokens=c.partition_tokens, out=L["out"],
-                                   workspace=L["ws"])
+                                   v_biases=c.v_biases, partition_tokens=c.partition_tokens, window=sp.window,
+                                   out=L["out"], workspace=L["ws"])
             host_out[li].copy_(L["out"], non_blocking=True)
 
     with torch.cuda.stream(stream):
@@ -470,7 +485,8 @@ def run_profile_calls(args):
         for _ in range(args.profile_calls):
             paged_decode_attention(c.q, c.k_pool, c.v_pool, c.block_tables, c.seq_lens, c.scale, bits=sp.bits,
                                    group_size=sp.group_size, k_scales=c.k_scales, k_biases=c.k_biases,
-                                   v_scales=c.v_scales, v_biases=c.v_biases, partition_tokens=c.partition_tokens)
+                                   v_scales=c.v_scales, v_biases=c.v_biases, partition_tokens=c.partition_tokens,
+                                   window=sp.window)
         torch.cuda.synchronize()
         print(json.dumps({"profile_calls": args.profile_calls, "workload": sp.name, "num_seqs": sp.num_seqs,
                           "kv_bytes_per_call": required_kv_bytes(sp, c.lens_host)}), flush=True)

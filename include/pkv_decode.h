@@ -14,6 +14,7 @@
  *
  *     kv    = h / (HQ / HK)                      consecutive heads share a KV head
  *     key t is visible iff t <= len_b - N + i    (len_b counts the N new rows)
+ *                     and, with a sliding window W, t > len_b - N + i - W
  *     K[t]  = k_pool[block_tables[b][t / BS]][kv][t % BS][:]
  *     affine pages: K[t][d] = scale[t][d/64] * code[t][d] + bias[t][d/64]
  *     out[b][h][i] = softmax_t(scale * <q, K[t]>) . V[t]       rounded to bf16
@@ -104,17 +105,27 @@ typedef struct pkv_decode_params {
   int32_t partition_tokens;   /* rows per partition: 0 = chosen from lengths and SM count;
                                  otherwise rounded up to the chunk rows (16 bf16, 32 affine).
                                  A value >= max_blocks_per_seq*block_size gives one partition. */
+  int32_t window;             /* sliding window W in rows, 0 = none: query i then sees only keys
+                                 t with len-N+i-W < t <= len-N+i (the W most recent positions,
+                                 its own included), as the pages' causal mask with a window
+                                 size (kernels/attention/masks.ts, createCausalMask) */
 } pkv_decode_params;
 
 /* How a call will be carried out. */
 typedef struct pkv_plan {
   int32_t partition_tokens; /* resolved rows per partition */
-  int32_t max_partitions;   /* partitions of the longest admissible sequence */
+  int32_t max_partitions;   /* partitions per (sequence, KV head) in the grid and the workspace: those
+                               of the longest admissible sequence, or with a window the most that
+                               window + n_query - 1 rows can touch */
   int32_t chunk_rows;       /* rows staged per pipeline step */
   int32_t sm_count;         /* SM count the plan was made for */
   int32_t threads_per_cta;  /* partial-kernel CTA size */
   int32_t smem_bytes;       /* partial-kernel dynamic shared memory */
-  size_t workspace_bytes;   /* device scratch for the partials; 0 with one partition */
+  int32_t merge_in_cluster; /* 1: the partitions of each (sequence, KV head) form one thread-block
+                               cluster and merge through distributed shared memory inside the
+                               partial kernel (2..16 partitions on a grid of at most one wave) */
+  size_t workspace_bytes;   /* device scratch for the partition states; 0 with one partition
+                               or with merge_in_cluster */
 } pkv_plan;
 
 /* Makes the plan for (layout, params) on a GPU with sm_count SMs. Pure host
@@ -145,11 +156,12 @@ int pkv_paged_decode_attention(const pkv_pool_layout* layout, const pkv_decode_p
 /* The two passes of pkv_paged_decode_attention, for callers that schedule them
  * apart (for example to combine partition states computed elsewhere, or to time
  * the partial pass alone). pkv_paged_decode_partial takes the same arguments
- * and enqueues only the partial pass: with one partition it writes the final
- * `out`; otherwise it writes each partition's state (running max in log2 units,
- * normaliser, unnormalised output, all f32) into `workspace`.
- * pkv_merge_partitions then enqueues the log-sum-exp merge of those states into
- * `out` for the same layout and params (it does nothing with one partition).
+ * and enqueues only the partial pass: with one partition, or when the plan merges
+ * in a cluster, it writes the final `out`; otherwise it writes each partition's
+ * state (running max in log2 units, normaliser, unnormalised output, all f32)
+ * into `workspace`. pkv_merge_partitions then enqueues the log-sum-exp merge of
+ * those states into `out` for the same layout and params (it does nothing when
+ * the plan needs no merge pass).
  * Returns as pkv_paged_decode_attention. */
 int pkv_paged_decode_partial(const pkv_pool_layout* layout, const pkv_decode_params* params, const void* q,
                              const void* k_pool, const void* v_pool, const void* k_scales,
@@ -193,6 +205,28 @@ int pkv_paged_decode_attention_no_alloc(const pkv_pool_layout* layout, const pkv
                                         const void* v_biases, const int32_t* block_tables,
                                         const int32_t* seq_lens, float scale, void* out, int32_t* error_flag,
                                         void* stream);
+
+/* Write side: appends each sequence's n_new new K and V rows into its pages at
+ * cache positions seq_lens[b] .. seq_lens[b] + n_new - 1 (position t goes to block
+ * block_tables[b][t / block_size], row t % block_size), the pages'
+ * PagedKVCache.append / BlockPool.writeBlock (state/paged/cache.ts). Blocks must
+ * already be in the tables; allocating them is the caller's.
+ *   k_new, v_new  bf16 [num_seqs, num_kv_heads, n_new, head_dim], 16-byte aligned
+ *   seq_lens      rows held BEFORE the append (the caller then adds n_new)
+ * bf16 pages are copied. Affine pages are quantised per row and 64-dim group
+ * (the pages do not give the quantiser's formula; this is the min/max reading,
+ * every step in f32):
+ *     scale = bf16((max - min) / (2^bits - 1)), bias = bf16(min),
+ *     code  = clamp(round_half_even((x - bias) / scale), 0, 2^bits - 1)
+ *             (0 when the stored scale is 0),
+ * codes packed lowest bits first. Bad block ids skip their row and set
+ * PKV_DEVERR_BAD_BLOCK; seq_lens[b] + n_new above max_blocks_per_seq*block_size
+ * sets PKV_DEVERR_BAD_SEQ_LEN and writes nothing for that sequence.
+ * Layouts: bf16 head_dim 64/128/256, affine 128/256. Asynchronous on `stream`. */
+int pkv_paged_append(const pkv_pool_layout* layout, int32_t num_seqs, int32_t max_blocks_per_seq, int32_t n_new,
+                     const void* k_new, const void* v_new, const int32_t* block_tables, const int32_t* seq_lens,
+                     void* k_pool, void* v_pool, void* k_scales, void* k_biases, void* v_scales, void* v_biases,
+                     int32_t* error_flag, void* stream);
 
 /* Bit-exact gather of one pool plane into contiguous per-sequence rows, the
  * fetch copy of the pages' BlockPool.gather / pickBlocks (state/paged/cache.ts):

@@ -15,4 +15,5 @@ from .paged_decode import (  # noqa: F401
     lse_merge,
     paged_decode_attention,
     paged_decode_attention_partitioned,
+    visible_range,
 )

@@ -18,13 +18,16 @@ For every sequence b, query row i in [0, N) and query head h::
 
     kv = h // (HQ // HK)                         consecutive query heads share a KV head
     T  = len_b - N + i + 1                       key t is visible iff t <= len_b - N + i
+    lo = max(0, T - W) with a sliding window W   ... and t >= lo (the W most recent rows)
     K[t] = k_pool[table_b[t // BS], kv, t % BS]  block-table gather, t < T
     affine pages: K[t][d] = s[t][d // G] * code[t][d] + b[t][d // G]
     score_t = scale * sum_d q[d] * K[t][d]
     p = softmax(score);  out = sum_t p_t * V[t]
 
 ``len_b`` counts the N new rows, which are appended before the read
-(state/paged/cache.ts, ``PagedKVCache.appendDecode``).
+(state/paged/cache.ts, ``PagedKVCache.appendDecode``). The window follows the
+causal mask with a window size of kernels/attention/masks.ts
+(``createCausalMask``): a query at position pos sees keys in (pos - W, pos].
 
 Every function below is pinned by the CPU tests in ``tests/test_oracle.py``
 (closed forms, special cases, brute force against a library routine).
@@ -174,9 +177,16 @@ def _rows(B, HQ, rows):
     return [(b, h) for b in range(B) for h in range(HQ)] if rows is None else list(rows)
 
 
+def visible_range(length: int, n_query: int, i: int, window: int = 0):
+    """Keys [lo, hi) visible to query row i of a sequence holding ``length`` rows."""
+    hi = length - n_query + i + 1
+    lo = max(0, hi - window) if window > 0 else 0
+    return lo, hi
+
+
 def paged_decode_attention(q, k_pool, v_pool, block_tables, seq_lens, scale: float, n_query: int, *,
                            bits: int = 16, group_size: int = 64, k_scales=None, k_biases=None,
-                           v_scales=None, v_biases=None, rows=None) -> np.ndarray:
+                           v_scales=None, v_biases=None, rows=None, window: int = 0) -> np.ndarray:
     """Decode attention over a paged cache, float64 ``[B, HQ, N, Dv]``.
 
     ``q``: float ``[B, HQ, N, D]``; ``k_pool``/``v_pool``: float values
@@ -210,8 +220,8 @@ def paged_decode_attention(q, k_pool, v_pool, block_tables, seq_lens, scale: flo
                 Dv = V.shape[1]
                 out = np.full((B, HQ, N, Dv), np.nan)
             for i in range(N):
-                T = L - N + i + 1
-                out[b, h, i] = attend(q[b, h, i], K[:T], V[:T], scale)
+                lo, hi = visible_range(L, N, i, window)
+                out[b, h, i] = attend(q[b, h, i], K[lo:hi], V[lo:hi], scale)
     if out is None:
         out = np.full((B, HQ, N, Dv if Dv else D), np.nan)
     return out
@@ -220,7 +230,7 @@ def paged_decode_attention(q, k_pool, v_pool, block_tables, seq_lens, scale: flo
 def paged_decode_attention_partitioned(q, k_pool, v_pool, block_tables, seq_lens, scale: float,
                                        n_query: int, partition_tokens: int, *, bits: int = 16,
                                        group_size: int = 64, k_scales=None, k_biases=None,
-                                       v_scales=None, v_biases=None, rows=None) -> np.ndarray:
+                                       v_scales=None, v_biases=None, rows=None, window: int = 0) -> np.ndarray:
     """The split-sequence form: partitions of ``partition_tokens`` cache rows.
 
     Partition ``p`` of sequence b covers rows ``[p*P, min((p+1)*P, len_b))``;
@@ -252,7 +262,7 @@ def paged_decode_attention_partitioned(q, k_pool, v_pool, block_tables, seq_lens
             if out is None:
                 out = np.full((B, HQ, N, V.shape[1]), np.nan)
             for i in range(N):
-                T = L - N + i + 1
-                bounds = [(p * P, min((p + 1) * P, T)) for p in range(nparts)]
+                lo, hi = visible_range(L, N, i, window)
+                bounds = [(max(p * P, lo), min((p + 1) * P, hi)) for p in range(nparts)]
                 out[b, h, i] = lse_merge(partition_states(q[b, h, i], K, V, scale, bounds))
     return out

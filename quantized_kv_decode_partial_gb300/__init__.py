@@ -13,5 +13,6 @@ from .binding import (  # noqa: F401
     make_plan,
     paged_decode_attention,
     paged_decode_passes,
+    paged_append,
     paged_gather,
 )

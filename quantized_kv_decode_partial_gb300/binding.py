@@ -23,6 +23,7 @@ EXPORTS = (
     "pkv_paged_decode_partial",
     "pkv_merge_partitions",
     "pkv_paged_decode_attention_no_alloc",
+    "pkv_paged_append",
     "pkv_paged_gather",
     "pkv_strerror",
     "pkv_last_cuda_error",
@@ -62,13 +63,13 @@ class PoolLayout(ctypes.Structure):
 
 class DecodeParams(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in
-                ("num_seqs", "num_q_heads", "n_query", "max_blocks_per_seq", "partition_tokens")]
+                ("num_seqs", "num_q_heads", "n_query", "max_blocks_per_seq", "partition_tokens", "window")]
 
 
 class Plan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in
                 ("partition_tokens", "max_partitions", "chunk_rows", "sm_count", "threads_per_cta",
-                 "smem_bytes")] + [("workspace_bytes", ctypes.c_size_t)]
+                 "smem_bytes", "merge_in_cluster")] + [("workspace_bytes", ctypes.c_size_t)]
 
 
 _lib = None
@@ -101,6 +102,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.pkv_paged_decode_attention_no_alloc.argtypes = [ctypes.POINTER(PoolLayout), ctypes.POINTER(DecodeParams),
                                                         P, P, P, P, P, P, P, P, P, F, P, P, P]
     lib.pkv_paged_decode_attention_no_alloc.restype = ctypes.c_int
+    lib.pkv_paged_append.argtypes = [ctypes.POINTER(PoolLayout), I32, I32, I32, P, P, P, P, P, P, P, P, P, P, P, P]
+    lib.pkv_paged_append.restype = ctypes.c_int
     lib.pkv_paged_gather.argtypes = [P, I32, I32, I32, I32, P, P, I32, I32, I32, P, P, P]
     lib.pkv_paged_gather.restype = ctypes.c_int
     lib.pkv_strerror.argtypes = [ctypes.c_int]
@@ -131,6 +134,25 @@ def layout_for(k_pool: torch.Tensor, head_dim: int, bits: int, group_size: int =
     return PoolLayout(nb, hk, bs, head_dim, bits, group_size)
 
 
+_plan_cache = {}
+
+
+def _plan_key(layout: PoolLayout, params: DecodeParams):
+    return (torch.cuda.current_device(),) + tuple(getattr(layout, f) for f, _ in PoolLayout._fields_) + \
+        tuple(getattr(params, f) for f, _ in DecodeParams._fields_)
+
+
+def _cached_plan(layout: PoolLayout, params: DecodeParams) -> Plan:
+    key = _plan_key(layout, params)
+    plan = _plan_cache.get(key)
+    if plan is None:
+        plan = make_plan(layout, params)
+        if len(_plan_cache) > 1024:
+            _plan_cache.clear()
+        _plan_cache[key] = plan
+    return plan
+
+
 def make_plan(layout: PoolLayout, params: DecodeParams, sm_count: Optional[int] = None) -> Plan:
     """The library's plan (partition size, workspace bytes) for these shapes."""
     lib = load_library()
@@ -148,7 +170,7 @@ def paged_decode_attention(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.
                            bits: int = 16, group_size: int = 64,
                            k_scales: Optional[torch.Tensor] = None, k_biases: Optional[torch.Tensor] = None,
                            v_scales: Optional[torch.Tensor] = None, v_biases: Optional[torch.Tensor] = None,
-                           partition_tokens: int = 0, out: Optional[torch.Tensor] = None,
+                           partition_tokens: int = 0, window: int = 0, out: Optional[torch.Tensor] = None,
                            workspace: Optional[torch.Tensor] = None,
                            error_flag: Optional[torch.Tensor] = None) -> torch.Tensor:
     """Decode attention over a paged cache (see include/pkv_decode.h).
@@ -161,9 +183,9 @@ def paged_decode_attention(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.
     lib = load_library()
     B, HQ, N, D = q.shape
     layout = layout_for(k_pool, D, bits, group_size)
-    params = DecodeParams(B, HQ, N, block_tables.shape[1], partition_tokens)
-    with torch.cuda.device(q.device):
-        plan = make_plan(layout, params)
+    params = DecodeParams(B, HQ, N, block_tables.shape[1], partition_tokens, window)
+    with _on_device(q.device):
+        plan = _cached_plan(layout, params)
         if out is None:
             out = torch.empty_like(q)
         if workspace is None and plan.workspace_bytes:
@@ -178,10 +200,31 @@ def paged_decode_attention(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.
     return out
 
 
+class _on_device:
+    """Makes `device` current for the call (a no-op when it already is)."""
+
+    def __init__(self, device: torch.device):
+        self.index = device.index if device.index is not None else torch.cuda.current_device()
+        self.prev = None
+
+    def __enter__(self):
+        cur = torch.cuda.current_device()
+        if cur != self.index:
+            self.prev = cur
+            torch.cuda.set_device(self.index)
+        return self
+
+    def __exit__(self, *exc):
+        if self.prev is not None:
+            torch.cuda.set_device(self.prev)
+        return False
+
+
 def paged_decode_passes(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
                         block_tables: torch.Tensor, seq_lens: torch.Tensor, scale: float, *, passes: str,
                         bits: int = 16, group_size: int = 64, k_scales=None, k_biases=None, v_scales=None,
-                        v_biases=None, partition_tokens: int = 0, out: Optional[torch.Tensor] = None,
+                        v_biases=None, partition_tokens: int = 0, window: int = 0,
+                        out: Optional[torch.Tensor] = None,
                         workspace: Optional[torch.Tensor] = None,
                         error_flag: Optional[torch.Tensor] = None) -> torch.Tensor:
     """One pass of the decode: ``passes="partial"`` (pkv_paged_decode_partial) or
@@ -190,9 +233,9 @@ def paged_decode_passes(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Ten
     lib = load_library()
     B, HQ, N, D = q.shape
     layout = layout_for(k_pool, D, bits, group_size)
-    params = DecodeParams(B, HQ, N, block_tables.shape[1], partition_tokens)
+    params = DecodeParams(B, HQ, N, block_tables.shape[1], partition_tokens, window)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    with torch.cuda.device(q.device):
+    with _on_device(q.device):
         stream = torch.cuda.current_stream(q.device).cuda_stream
         if passes == "partial":
             rc = lib.pkv_paged_decode_partial(
@@ -208,6 +251,23 @@ def paged_decode_passes(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Ten
     return out
 
 
+def paged_append(k_new: torch.Tensor, v_new: torch.Tensor, block_tables: torch.Tensor, seq_lens: torch.Tensor,
+                 k_pool: torch.Tensor, v_pool: torch.Tensor, *, bits: int = 16, group_size: int = 64,
+                 k_scales=None, k_biases=None, v_scales=None, v_biases=None,
+                 error_flag: Optional[torch.Tensor] = None) -> None:
+    """Writes k_new/v_new bf16 [B, HK, n_new, D] at positions seq_lens[b].. of each
+    sequence (quantising affine pages); see include/pkv_decode.h."""
+    lib = load_library()
+    B, HK, n_new, D = k_new.shape
+    layout = layout_for(k_pool, D, bits, group_size)
+    with _on_device(k_new.device):
+        stream = torch.cuda.current_stream(k_new.device).cuda_stream
+        rc = lib.pkv_paged_append(ctypes.byref(layout), B, block_tables.shape[1], n_new, _ptr(k_new), _ptr(v_new),
+                                  _ptr(block_tables), _ptr(seq_lens), _ptr(k_pool), _ptr(v_pool), _ptr(k_scales),
+                                  _ptr(k_biases), _ptr(v_scales), _ptr(v_biases), _ptr(error_flag), stream)
+    _check(rc, lib)
+
+
 def paged_gather(pool: torch.Tensor, block_tables: torch.Tensor, seq_lens: torch.Tensor, max_len: int,
                  out: Optional[torch.Tensor] = None, error_flag: Optional[torch.Tensor] = None) -> torch.Tensor:
     """Bit-exact gather of one pool plane [NB, HK, BS, W] into [B, HK, max_len, W]."""
@@ -217,7 +277,7 @@ def paged_gather(pool: torch.Tensor, block_tables: torch.Tensor, seq_lens: torch
     B = block_tables.shape[0]
     if out is None:
         out = torch.zeros((B, hk, max_len) + tuple(pool.shape[3:]), dtype=pool.dtype, device=pool.device)
-    with torch.cuda.device(pool.device):
+    with _on_device(pool.device):
         stream = torch.cuda.current_stream(pool.device).cuda_stream
         rc = lib.pkv_paged_gather(_ptr(pool), nb, hk, bs, row_bytes, _ptr(block_tables), _ptr(seq_lens), B,
                                   block_tables.shape[1], max_len, _ptr(out), _ptr(error_flag), stream)

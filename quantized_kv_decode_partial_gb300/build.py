@@ -24,6 +24,7 @@ LIB_PATH = os.path.join(PKG_DIR, LIB_NAME)
 SOURCES = [
     "pkv_api.cu",
     "pkv_merge_gather.cu",
+    "pkv_append.cu",
     "pkv_partial_bf16.cu",
     "pkv_partial_u4.cu",
     "pkv_partial_u8.cu",

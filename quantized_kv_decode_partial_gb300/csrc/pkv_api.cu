@@ -2,6 +2,8 @@
 // plan, TMA descriptors and kernel launches. See include/pkv_decode.h.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
+#include <atomic>
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
@@ -25,10 +27,10 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
 
-PartialInfo partial_info(int bits, int head_dim, int ntiles) {
-  if (bits == 16) return pkv::partial_info_bf16(head_dim, ntiles);
-  if (bits == 4) return pkv::partial_info_u4(head_dim, ntiles);
-  if (bits == 8) return pkv::partial_info_u8(head_dim, ntiles);
+PartialInfo partial_info(int bits, int head_dim, int nq) {
+  if (bits == 16) return pkv::partial_info_bf16(head_dim, nq);
+  if (bits == 4) return pkv::partial_info_u4(head_dim, nq);
+  if (bits == 8) return pkv::partial_info_u8(head_dim, nq);
   return PartialInfo{false, 0, 0, 0, 0, 0};
 }
 
@@ -55,11 +57,12 @@ int check_params(const pkv_pool_layout* L, const pkv_decode_params* P) {
   if (!P) return PKV_ERR_NULL_POINTER;
   if (P->num_seqs <= 0 || P->num_seqs > 65535) return PKV_ERR_BAD_PARAMS;
   if (P->num_q_heads <= 0 || P->num_q_heads % L->num_kv_heads) return PKV_ERR_BAD_PARAMS;
-  if (P->n_query < 1 || P->max_blocks_per_seq <= 0 || P->partition_tokens < 0) return PKV_ERR_BAD_PARAMS;
+  if (P->n_query < 1 || P->max_blocks_per_seq <= 0 || P->partition_tokens < 0 || P->window < 0)
+    return PKV_ERR_BAD_PARAMS;
   if (static_cast<long long>(P->max_blocks_per_seq) * L->block_size >= (1ll << 31)) return PKV_ERR_BAD_PARAMS;
   const long long nq = static_cast<long long>(P->num_q_heads / L->num_kv_heads) * P->n_query;
   if (nq > 64) return PKV_ERR_UNSUPPORTED_SHAPE;
-  if (!partial_info(L->bits, L->head_dim, ceil_div(nq, 8)).exists) return PKV_ERR_UNSUPPORTED_SHAPE;
+  if (!partial_info(L->bits, L->head_dim, static_cast<int>(nq)).exists) return PKV_ERR_UNSUPPORTED_SHAPE;
   return PKV_OK;
 }
 
@@ -72,21 +75,38 @@ int plan_impl(const pkv_pool_layout* L, const pkv_decode_params* P, int sm_count
   if (P->partition_tokens > 0) {
     part = round_up(P->partition_tokens, ch);
   } else {
-    // Enough partitions of the longest sequence that the grid covers the GPU a
-    // few times over (2 CTAs fit per SM), but never below 256 rows a partition.
-    const long long target = 4ll * (sm_count > 0 ? sm_count : 1) * 2;
+    // Halve the partition until the grid covers the GPU about four times over (two
+    // CTAs per SM), never below 256 rows. Once the grid fills a wave, stop before a
+    // CTA would get less than 512 KB of K/V: below that its fixed costs (prologue,
+    // pipeline fill, epilogue) start to show (measured on the windowed workload).
+    const long long slots = 2ll * (sm_count > 0 ? sm_count : 1);
+    const long long target = 4 * slots;
     const long long units = static_cast<long long>(P->num_seqs) * L->num_kv_heads;
+    const long long plane_row = L->bits == 16 ? 2ll * L->head_dim
+                                              : static_cast<long long>(L->head_dim) * L->bits / 8 + L->head_dim / 64 * 4;
     const long long floor_rows = 256;
-    part = round_up(max_len, ch);
-    while (units * ((max_len + part - 1) / part) < target && part > floor_rows) {
-      long long half = round_up(part / 2, ch);
-      part = half < floor_rows ? floor_rows : half;
+    const long long rich_rows = std::max<long long>(floor_rows, (512ll << 10) / (2 * plane_row));
+    // rows a step can read per sequence: the table, or the window's span
+    const long long span = P->window > 0 ? std::min<long long>(max_len, P->window + P->n_query - 1) : max_len;
+    part = round_up(span, ch);
+    while (part > floor_rows) {
+      const long long ctas = units * ((span + part - 1) / part);
+      if (ctas >= target) break;
+      const long long half = std::max<long long>(floor_rows, round_up(part / 2, ch));
+      if (half < rich_rows && ctas >= slots) break;
+      part = half;
     }
   }
   if (part >= max_len) part = round_up(max_len, ch);
-  const int max_parts = ceil_div(max_len, part);
+  // Partitions per (sequence, KV head) in the grid and the workspace: all of the table,
+  // or, with a window, the most that its span of rows can touch.
+  int max_parts = ceil_div(max_len, part);
+  if (P->window > 0) {
+    const long long span = std::min<long long>(max_len, static_cast<long long>(P->window) + P->n_query - 1);
+    max_parts = std::min<int>(max_parts, ceil_div(span, part) + 1);
+  }
   const long long nq = static_cast<long long>(P->num_q_heads / L->num_kv_heads) * P->n_query;
-  const PartialInfo info = partial_info(L->bits, L->head_dim, ceil_div(nq, 8));
+  const PartialInfo info = partial_info(L->bits, L->head_dim, static_cast<int>(nq));
   out->partition_tokens = static_cast<int32_t>(part);
   out->max_partitions = max_parts;
   out->chunk_rows = info.chunk_rows;
@@ -94,7 +114,15 @@ int plan_impl(const pkv_pool_layout* L, const pkv_decode_params* P, int sm_count
   out->threads_per_cta = info.threads;
   out->smem_bytes = info.smem_bytes;
   out->workspace_bytes = 0;
-  if (max_parts > 1) {
+  // Merge inside a thread-block cluster when a (sequence, KV head) has 2..16
+  // partitions and the grid is at most one wave: the CTAs of a cluster are then
+  // resident together anyway, and the merge needs no workspace and no second launch.
+  // A cluster of up to 16 CTAs fits 8 SMs at two CTAs per SM (one per SM up to 8).
+  const long long ctas = static_cast<long long>(P->num_seqs) * L->num_kv_heads * max_parts;
+  const bool two_per_sm = info.smem_bytes <= 114 * 1024;
+  out->merge_in_cluster = max_parts >= 2 && max_parts <= (two_per_sm ? 16 : 8) &&
+                          ctas <= static_cast<long long>(sm_count > 0 ? sm_count : 1) * (two_per_sm ? 2 : 1);
+  if (max_parts > 1 && !out->merge_in_cluster) {
     const size_t slots = static_cast<size_t>(P->num_seqs) * P->num_q_heads * P->n_query * max_parts;
     const size_t o_bytes = (slots * L->head_dim * sizeof(float) + 255) / 256 * 256;
     out->workspace_bytes = o_bytes + slots * 2 * sizeof(float);
@@ -102,12 +130,24 @@ int plan_impl(const pkv_pool_layout* L, const pkv_decode_params* P, int sm_count
   return PKV_OK;
 }
 
-int device_sm_count(int* sms) {
+constexpr int kMaxDevices = 256;
+std::atomic<int> g_sm_count[kMaxDevices];  // 0 until first read
+
+int device_sm_count(int* sms, int* device = nullptr) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail("cudaGetDevice", e);
+  if (device) *device = dev;
+  if (dev >= 0 && dev < kMaxDevices) {
+    const int cached = g_sm_count[dev].load(std::memory_order_relaxed);
+    if (cached > 0) {
+      *sms = cached;
+      return PKV_OK;
+    }
+  }
   e = cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return cuda_fail("cudaDeviceGetAttribute", e);
+  if (dev >= 0 && dev < kMaxDevices) g_sm_count[dev].store(*sms, std::memory_order_relaxed);
   return PKV_OK;
 }
 
@@ -126,8 +166,8 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 // 2-D view of one pool plane: rows = num_blocks*HK*BS, `row_elems` elements per
 // row; boxes of `box_rows` rows by `box_row_bytes` bytes with the matching swizzle.
-int pool_tensor_map(CUtensorMap* map, const void* base, int elem_bytes, long long row_elems, long long rows,
-                    const PartialInfo& info) {
+int encode_pool_tensor_map(CUtensorMap* map, const void* base, int elem_bytes, long long row_elems, long long rows,
+                           const PartialInfo& info) {
   auto encode = tensor_map_encoder();
   if (!encode) {
     std::snprintf(g_cuda_error, sizeof(g_cuda_error), "cuTensorMapEncodeTiled entry point unavailable");
@@ -146,6 +186,40 @@ int pool_tensor_map(CUtensorMap* map, const void* base, int elem_bytes, long lon
     std::snprintf(g_cuda_error, sizeof(g_cuda_error), "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
     return PKV_ERR_CUDA;
   }
+  return PKV_OK;
+}
+
+// Descriptors of recently used pool planes: a decode loop calls with the same
+// pools every step, so the encoding is done once per plane.
+struct TensorMapEntry {
+  const void* base;
+  long long row_elems, rows;
+  int elem_bytes, box_row_bytes, chunk_rows;
+  CUtensorMap map;
+};
+constexpr int kTensorMapCacheSize = 16;
+std::mutex g_tmap_mutex;
+TensorMapEntry g_tmap_cache[kTensorMapCacheSize];
+int g_tmap_next = 0;
+
+int pool_tensor_map(CUtensorMap* map, const void* base, int elem_bytes, long long row_elems, long long rows,
+                    const PartialInfo& info) {
+  {
+    std::lock_guard<std::mutex> lock(g_tmap_mutex);
+    for (const TensorMapEntry& e : g_tmap_cache) {
+      if (e.base == base && e.row_elems == row_elems && e.rows == rows && e.elem_bytes == elem_bytes &&
+          e.box_row_bytes == info.box_row_bytes && e.chunk_rows == info.chunk_rows) {
+        *map = e.map;
+        return PKV_OK;
+      }
+    }
+  }
+  int rc = encode_pool_tensor_map(map, base, elem_bytes, row_elems, rows, info);
+  if (rc) return rc;
+  std::lock_guard<std::mutex> lock(g_tmap_mutex);
+  TensorMapEntry& e = g_tmap_cache[g_tmap_next];
+  g_tmap_next = (g_tmap_next + 1) % kTensorMapCacheSize;
+  e = TensorMapEntry{base, row_elems, rows, elem_bytes, info.box_row_bytes, info.chunk_rows, *map};
   return PKV_OK;
 }
 
@@ -203,19 +277,21 @@ int enqueue_decode(const pkv_pool_layout* layout, const pkv_decode_params* param
   if (quant && (!aligned(k_scales, 16) || !aligned(k_biases, 16) || !aligned(v_scales, 16) || !aligned(v_biases, 16)))
     return PKV_ERR_MISALIGNED;
 
-  int sms = 0;
-  rc = device_sm_count(&sms);
+  int sms = 0, dev = 0;
+  rc = device_sm_count(&sms, &dev);
   if (rc) return rc;
   pkv_plan plan;
   rc = plan_impl(layout, params, sms, &plan);
   if (rc) return rc;
-  if (plan.workspace_bytes > 0 && (!workspace || workspace_bytes < plan.workspace_bytes))
+  const int mode = plan.max_partitions == 1 ? pkv::kModeSingle
+                   : plan.merge_in_cluster   ? pkv::kModeCluster
+                                             : pkv::kModeWorkspace;
+  if (mode == pkv::kModeWorkspace && (!workspace || workspace_bytes < plan.workspace_bytes))
     return PKV_ERR_WORKSPACE_TOO_SMALL;
 
   const int D = layout->head_dim, HK = layout->num_kv_heads;
   const int nq = (params->num_q_heads / HK) * params->n_query;
-  const int ntiles = ceil_div(nq, 8);
-  const PartialInfo info = partial_info(layout->bits, D, ntiles);
+  const PartialInfo info = partial_info(layout->bits, D, nq);
   const long long rows = static_cast<long long>(layout->num_blocks) * HK * layout->block_size;
   const int elem = info.tensor_elem_bytes;
   const long long row_elems = quant ? static_cast<long long>(D) * layout->bits / 8 : D;
@@ -239,8 +315,10 @@ int enqueue_decode(const pkv_pool_layout* layout, const pkv_decode_params* param
   p.out = static_cast<__nv_bfloat16*>(out);
   const size_t slots = static_cast<size_t>(params->num_seqs) * params->num_q_heads * params->n_query * plan.max_partitions;
   const size_t o_bytes = (slots * D * sizeof(float) + 255) / 256 * 256;
-  p.ws_o = plan.max_partitions > 1 ? static_cast<float*>(workspace) : nullptr;
-  p.ws_ml = plan.max_partitions > 1 ? reinterpret_cast<float*>(static_cast<char*>(workspace) + o_bytes) : nullptr;
+  p.ws_o = mode == pkv::kModeWorkspace ? static_cast<float*>(workspace) : nullptr;
+  p.ws_ml = mode == pkv::kModeWorkspace ? reinterpret_cast<float*>(static_cast<char*>(workspace) + o_bytes) : nullptr;
+  p.mode = mode;
+  p.window = params->window;
   p.error_flag = error_flag;
   p.num_blocks = layout->num_blocks;
   p.num_kv_heads = HK;
@@ -259,15 +337,15 @@ int enqueue_decode(const pkv_pool_layout* layout, const pkv_decode_params* param
   cudaError_t e = cudaSuccess;
   if (partial) {
     if (layout->bits == 16)
-      e = pkv::launch_partial_bf16(D, ntiles, p, tk, tv, grid, st);
+      e = pkv::launch_partial_bf16(D, nq, p, tk, tv, grid, st, dev);
     else if (layout->bits == 4)
-      e = pkv::launch_partial_u4(D, ntiles, p, tk, tv, grid, st);
+      e = pkv::launch_partial_u4(D, nq, p, tk, tv, grid, st, dev);
     else
-      e = pkv::launch_partial_u8(D, ntiles, p, tk, tv, grid, st);
+      e = pkv::launch_partial_u8(D, nq, p, tk, tv, grid, st, dev);
     if (e != cudaSuccess) return cuda_fail("partial kernel launch", e);
   }
 
-  if ((passes & kPassMerge) && plan.max_partitions > 1) {
+  if ((passes & kPassMerge) && mode == pkv::kModeWorkspace) {
     pkv::MergeParams m{};
     m.ws_o = p.ws_o;
     m.ws_ml = p.ws_ml;
@@ -280,6 +358,7 @@ int enqueue_decode(const pkv_pool_layout* layout, const pkv_decode_params* param
     m.max_len = params->max_blocks_per_seq * layout->block_size;
     m.partition_tokens = plan.partition_tokens;
     m.max_partitions = plan.max_partitions;
+    m.window = params->window;
     e = pkv::launch_merge(m, params->num_seqs * params->num_q_heads * params->n_query, st);
     if (e != cudaSuccess) return cuda_fail("merge kernel launch", e);
   }
@@ -315,6 +394,49 @@ int pkv_merge_partitions(const pkv_pool_layout* layout, const pkv_decode_params*
   return enqueue_decode(layout, params, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
                         seq_lens, 0.f, out, const_cast<void*>(workspace), workspace_bytes, error_flag, stream,
                         kPassMerge);
+}
+
+int pkv_paged_append(const pkv_pool_layout* layout, int32_t num_seqs, int32_t max_blocks_per_seq, int32_t n_new,
+                     const void* k_new, const void* v_new, const int32_t* block_tables, const int32_t* seq_lens,
+                     void* k_pool, void* v_pool, void* k_scales, void* k_biases, void* v_scales, void* v_biases,
+                     int32_t* error_flag, void* stream) {
+  int rc = check_layout(layout);
+  if (rc) return rc;
+  if (!pkv::append_supported(layout->bits, layout->head_dim)) return PKV_ERR_BAD_LAYOUT;
+  if (num_seqs <= 0 || num_seqs > 65535 || max_blocks_per_seq <= 0 || n_new < 0 || n_new > 65535)
+    return PKV_ERR_BAD_PARAMS;
+  if (static_cast<long long>(max_blocks_per_seq) * layout->block_size >= (1ll << 31)) return PKV_ERR_BAD_PARAMS;
+  const bool quant = layout->bits != 16;
+  if (!k_new || !v_new || !block_tables || !seq_lens || !k_pool || !v_pool) return PKV_ERR_NULL_POINTER;
+  if (quant && (!k_scales || !k_biases || !v_scales || !v_biases)) return PKV_ERR_NULL_POINTER;
+  if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) ||
+      !aligned(block_tables, 4) || !aligned(seq_lens, 4) || !aligned(error_flag, 4))
+    return PKV_ERR_MISALIGNED;
+  if (quant && (!aligned(k_scales, 4) || !aligned(k_biases, 4) || !aligned(v_scales, 4) || !aligned(v_biases, 4)))
+    return PKV_ERR_MISALIGNED;
+  pkv::AppendParams a{};
+  a.k_new = static_cast<const __nv_bfloat16*>(k_new);
+  a.v_new = static_cast<const __nv_bfloat16*>(v_new);
+  a.block_tables = block_tables;
+  a.seq_lens = seq_lens;
+  a.k_pool_bf16 = quant ? nullptr : static_cast<__nv_bfloat16*>(k_pool);
+  a.v_pool_bf16 = quant ? nullptr : static_cast<__nv_bfloat16*>(v_pool);
+  a.k_pool_words = quant ? static_cast<uint32_t*>(k_pool) : nullptr;
+  a.v_pool_words = quant ? static_cast<uint32_t*>(v_pool) : nullptr;
+  a.k_scales = static_cast<__nv_bfloat16*>(k_scales);
+  a.k_biases = static_cast<__nv_bfloat16*>(k_biases);
+  a.v_scales = static_cast<__nv_bfloat16*>(v_scales);
+  a.v_biases = static_cast<__nv_bfloat16*>(v_biases);
+  a.error_flag = error_flag;
+  a.num_blocks = layout->num_blocks;
+  a.num_kv_heads = layout->num_kv_heads;
+  a.block_size = layout->block_size;
+  a.max_blocks = max_blocks_per_seq;
+  a.n_new = n_new;
+  (void)cudaGetLastError();
+  cudaError_t e = pkv::launch_append(a, layout->bits, layout->head_dim, num_seqs, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail("append kernel launch", e);
+  return PKV_OK;
 }
 
 int pkv_paged_gather(const void* pool, int32_t num_blocks, int32_t num_kv_heads, int32_t block_size,

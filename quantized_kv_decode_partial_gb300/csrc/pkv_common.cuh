@@ -33,8 +33,16 @@ struct PartialParams {
   int num_blocks, num_kv_heads, block_size, max_blocks;
   int num_q_heads, n_query, nq;  // nq = (HQ/HK) * n_query rows served per KV head
   int partition_tokens, max_partitions;
+  int mode;           // kModeSingle / kModeWorkspace / kModeCluster
+  int window;         // sliding window in rows (0: none)
   float score_scale;  // softmax scale * log2(e)
 };
+
+// How the partial kernel finishes.
+constexpr int kModeSingle = 0;     // one partition: the CTA writes bf16 output
+constexpr int kModeWorkspace = 1;  // partition states go to the workspace; the merge kernel follows
+constexpr int kModeCluster = 2;    // the partitions of a (sequence, KV head) form one thread-block
+                                   // cluster and merge through distributed shared memory
 
 struct MergeParams {
   const float* ws_o;
@@ -44,6 +52,24 @@ struct MergeParams {
   int32_t* error_flag;
   int rows_per_seq;  // HQ * N
   int n_query, head_dim, max_len, partition_tokens, max_partitions;
+  int window;  // sliding window in rows (0: none)
+};
+
+struct AppendParams {
+  const __nv_bfloat16* k_new;  // [B, HK, n_new, D]
+  const __nv_bfloat16* v_new;
+  const int32_t* block_tables;
+  const int32_t* seq_lens;     // rows before the append
+  __nv_bfloat16* k_pool_bf16;  // bf16 pages
+  __nv_bfloat16* v_pool_bf16;
+  uint32_t* k_pool_words;      // affine pages
+  uint32_t* v_pool_words;
+  __nv_bfloat16* k_scales;
+  __nv_bfloat16* k_biases;
+  __nv_bfloat16* v_scales;
+  __nv_bfloat16* v_biases;
+  int32_t* error_flag;
+  int num_blocks, num_kv_heads, block_size, max_blocks, n_new;
 };
 
 struct GatherParams {
@@ -211,6 +237,39 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
   uint32_t y;
   asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
   return y;
+}
+
+// Thread-block cluster barrier: every thread of every CTA of the cluster arrives;
+// writes before it (shared memory included) are visible to the cluster after it.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Reads an f32 at shared-memory address `addr` (this CTA's layout) in the shared
+// memory of cluster CTA `rank`.
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr, uint32_t rank) {
+  uint32_t remote;
+  float v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(addr), "r"(rank));
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+  return v;
+}
+
+// Named CTA barrier over `count` threads that also ORs a predicate across them: every
+// participant gets the same answer.
+__device__ __forceinline__ bool group_barrier_any(int id, int count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "barrier.cta.red.or.pred p, %2, %3, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
 }
 
 // Programmatic dependent launch: let the next kernel on the stream be scheduled

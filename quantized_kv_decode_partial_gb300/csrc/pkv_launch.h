@@ -19,18 +19,22 @@ struct PartialInfo {
   int tensor_elem_bytes;  // element size of the pool tensor maps (2 bf16, 1 affine codes)
 };
 
-PartialInfo partial_info_bf16(int head_dim, int ntiles);
-PartialInfo partial_info_u4(int head_dim, int ntiles);
-PartialInfo partial_info_u8(int head_dim, int ntiles);
+// Partial-kernel instantiation for `nq` query rows per KV head.
+PartialInfo partial_info_bf16(int head_dim, int nq);
+PartialInfo partial_info_u4(int head_dim, int nq);
+PartialInfo partial_info_u8(int head_dim, int nq);
 
-cudaError_t launch_partial_bf16(int head_dim, int ntiles, const PartialParams& p, const CUtensorMap& tk,
-                                const CUtensorMap& tv, dim3 grid, cudaStream_t stream);
-cudaError_t launch_partial_u4(int head_dim, int ntiles, const PartialParams& p, const CUtensorMap& tk,
-                              const CUtensorMap& tv, dim3 grid, cudaStream_t stream);
-cudaError_t launch_partial_u8(int head_dim, int ntiles, const PartialParams& p, const CUtensorMap& tk,
-                              const CUtensorMap& tv, dim3 grid, cudaStream_t stream);
+cudaError_t launch_partial_bf16(int head_dim, int nq, const PartialParams& p, const CUtensorMap& tk,
+                                const CUtensorMap& tv, dim3 grid, cudaStream_t stream, int device);
+cudaError_t launch_partial_u4(int head_dim, int nq, const PartialParams& p, const CUtensorMap& tk,
+                              const CUtensorMap& tv, dim3 grid, cudaStream_t stream, int device);
+cudaError_t launch_partial_u8(int head_dim, int nq, const PartialParams& p, const CUtensorMap& tk,
+                              const CUtensorMap& tv, dim3 grid, cudaStream_t stream, int device);
 
 cudaError_t launch_merge(const MergeParams& p, int rows, cudaStream_t stream);
 cudaError_t launch_gather(const GatherParams& p, int num_seqs, cudaStream_t stream);
+
+bool append_supported(int bits, int head_dim);
+cudaError_t launch_append(const AppendParams& p, int bits, int head_dim, int num_seqs, cudaStream_t stream);
 
 }  // namespace pkv

@@ -22,7 +22,10 @@ __global__ void __launch_bounds__(64) pkv_merge_kernel(const __grid_constant__ M
     out[1] = __floats2bfloat162_rn(0.f, 0.f);
     return;
   }
-  const int np = (len + p.partition_tokens - 1) / p.partition_tokens;
+  // Workspace slot i holds partition first + i: with a sliding window the partial pass
+  // starts at the partition holding the lowest visible row.
+  const int first = p.window > 0 ? max(0, len - p.n_query + 1 - p.window) / p.partition_tokens : 0;
+  const int np = (len + p.partition_tokens - 1) / p.partition_tokens - first;
   const float2* ml = reinterpret_cast<const float2*>(p.ws_ml) + static_cast<size_t>(row) * p.max_partitions;
   const float4* ob = reinterpret_cast<const float4*>(p.ws_o + static_cast<size_t>(row) * p.max_partitions * p.head_dim + d);
   const int ostride = p.head_dim / 4;

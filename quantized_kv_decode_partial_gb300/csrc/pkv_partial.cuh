@@ -48,7 +48,7 @@
 
 namespace pkv {
 
-template <int BITS, int D, int NT>
+template <int BITS, int D, int NT, int WQ>
 struct PartialCfg {
   static constexpr bool kQuant = BITS != 16;
   static constexpr int kElemBytes = kQuant ? 1 : 2;                // tensor-map element size
@@ -65,12 +65,18 @@ struct PartialCfg {
   static constexpr int kStageBytes = (kTxBytes + 1023) / 1024 * 1024;
   static constexpr int kWarps = 4;                                   // every warp computes
   static constexpr int kThreads = kWarps * 32;
-  static constexpr int kStagesPerWarp = kStageBytes <= 9 * 1024 ? 3 : 2;  // each warp's private ring
+  // The warps form kWP page groups of WQ warps. A page group takes every kWP-th chunk;
+  // its WQ warps read each of its chunks, each for its own 8*NT query rows.
+  static constexpr int kWP = kWarps / WQ;
+  static constexpr int kStagesPerWarp = kStageBytes <= 9 * 1024 ? 3 : 2;
+  static constexpr int kStagesPerGroup = kStagesPerWarp * WQ;  // each page group's private ring
   static constexpr int kNqp = 8 * NT;       // query rows per warp (padded)
+  static constexpr int kNqAll = WQ * kNqp;  // query rows per CTA (padded)
   static constexpr int kMt = D / 16;        // 16-dim m-tiles of O^T
   static constexpr int kKs = D / 16;        // k16 steps of Q K^T
   static constexpr int kTiles = kCh / 16;   // 16-key tiles per stage
-  static constexpr int kCombineBytes = kWarps * kNqp * (D + 2) * 4;
+  // per-page-group states (m, l, o) for the in-CTA combine, then the CTA's own state for a cluster merge
+  static constexpr int kCombineBytes = (kWP + 1) * kNqAll * (D + 2) * 4;
   static constexpr int kRingBytes = kWarps * kStagesPerWarp * kStageBytes;
   static constexpr int kDataBytes = kRingBytes > kCombineBytes ? kRingBytes : kCombineBytes;
   static constexpr int kBarrierBytes = 256;
@@ -81,6 +87,7 @@ struct PartialCfg {
   static_assert(kRowBytes % kRB == 0, "whole boxes per row");
   static_assert(kWarps * kStagesPerWarp * 12 + 4 <= kBarrierBytes, "barrier area");
   static_assert(!kQuant || D % 64 == 0, "affine head dims are whole 64-dim groups");
+  static_assert(WQ == 1 || WQ == 2 || WQ == 4, "query groups of 1, 2 or 4 warps");
 };
 
 // Physical head dim held by row `half` (0: g, 1: g + 8) of O^T m-tile `mt`.
@@ -153,37 +160,51 @@ __device__ __forceinline__ void load_group_row(uint32_t addr, float (&v)[G]) {
   }
 }
 
-template <int BITS, int D, int NT>
+template <int BITS, int D, int NT, int WQ>
 __global__ void __maxnreg__(200)
     pkv_partial_kernel(const __grid_constant__ PartialParams p, const __grid_constant__ CUtensorMap tmap_k,
                        const __grid_constant__ CUtensorMap tmap_v) {
-  using C = PartialCfg<BITS, D, NT>;
+  using C = PartialCfg<BITS, D, NT, WQ>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + C::kDataBytes);  // [warp][stage]
   int* stage_ok = reinterpret_cast<int*>(full_bar + C::kWarps * C::kStagesPerWarp);
   volatile int* abort_flag = stage_ok + C::kWarps * C::kStagesPerWarp;
 
-  const int part = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
+  const int slot = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;  // slot: rank in the cluster / workspace
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
+  const int qg = warp % WQ, pg = warp / WQ;  // query group, page group
+  const int rbase = qg * C::kNqp;            // first query row of this warp within the CTA
+  const bool leader = qg == 0;               // issues its page group's copies
   const int N = p.n_query;
   const int rep = p.nq / N;
   const size_t row0 = (static_cast<size_t>(b) * p.num_q_heads + static_cast<size_t>(hk) * rep) * N;
-  const bool single = p.max_partitions == 1;
+  const bool single = p.mode == kModeSingle;
+  const bool in_cluster = p.mode == kModeCluster;
   const int len = p.seq_lens[b];
 
   if (len < N || len > p.max_blocks * p.block_size) {
-    if (threadIdx.x == 0 && part == 0 && p.error_flag) atomicOr(p.error_flag, kDevErrBadSeqLen);
-    if (single) {
+    // Every CTA of this sequence sees the same length and leaves here (before any
+    // cluster barrier); the CTA of partition 0 zeroes the outputs unless the merge
+    // pass does.
+    if (threadIdx.x == 0 && slot == 0 && p.error_flag) atomicOr(p.error_flag, kDevErrBadSeqLen);
+    if (single || (in_cluster && slot == 0)) {
       for (int i = threadIdx.x; i < p.nq * D; i += C::kThreads) p.out[row0 * D + i] = __float2bfloat16_rn(0.f);
     }
     return;
   }
+  // With a sliding window only rows >= len - N + 1 - window are visible to any query;
+  // the grid covers the partitions from the one holding that row on.
+  const int win_lo = p.window > 0 ? max(0, len - N + 1 - p.window) : 0;
+  const int part = win_lo / p.partition_tokens + slot;
   const int t0 = part * p.partition_tokens;
-  if (t0 >= len) return;  // empty partition; the merge pass never reads it
   const int t_end = min(len, t0 + p.partition_tokens);
-  const int nchunks = (t_end - t0 + C::kCh - 1) / C::kCh;
+  const bool empty = t0 >= len || t_end <= win_lo;
+  if (empty && !in_cluster) return;  // the merge pass never reads this partition
+  // first row this CTA reads: the partition start, or the chunk holding the window's lowest row
+  const int t_first = max(t0, win_lo / C::kCh * C::kCh);
+  const int nchunks = empty ? 0 : (t_end - t_first + C::kCh - 1) / C::kCh;  // an empty cluster member still merges
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kWarps * C::kStagesPerWarp; ++s) mbar_init(smem_addr(&full_bar[s]), 1);
@@ -199,22 +220,22 @@ __global__ void __maxnreg__(200)
 
   {
     // ------------------------------------------------------------------ this warp's pipeline
-    // Warp w owns chunks w, w + 4, w + 8, ... of the partition and a private ring of
-    // kStagesPerWarp stages: it issues its own TMA copies kStagesPerWarp chunks ahead,
-    // so no warp ever waits on another warp's progress.
-    const int my_chunks = nchunks > warp ? (nchunks - warp + C::kWarps - 1) / C::kWarps : 0;
-    uint64_t* my_full = full_bar + warp * C::kStagesPerWarp;
-    int* my_ok = stage_ok + warp * C::kStagesPerWarp;
-    uint8_t* my_ring = smem + warp * C::kStagesPerWarp * C::kStageBytes;
+    // Page group pg owns chunks pg, pg + kWP, pg + 2 kWP, ... of the partition and a
+    // private ring of kStagesPerGroup stages; its leader warp issues the TMA copies
+    // kStagesPerGroup chunks ahead, so no group waits on another group's progress.
+    const int my_chunks = nchunks > pg ? (nchunks - pg + C::kWP - 1) / C::kWP : 0;
+    uint64_t* my_full = full_bar + pg * C::kStagesPerGroup;
+    int* my_ok = stage_ok + pg * C::kStagesPerGroup;
+    uint8_t* my_ring = smem + pg * C::kStagesPerGroup * C::kStageBytes;
     const int32_t* table = p.block_tables + static_cast<size_t>(b) * p.max_blocks;
     const uint64_t policy = l2_evict_first_policy();
-    auto chunk_row = [&](int i) { return t0 + (warp + i * C::kWarps) * C::kCh; };  // first cache row of local chunk i
+    auto chunk_row = [&](int i) { return t_first + (pg + i * C::kWP) * C::kCh; };  // first cache row of local chunk i
     // Physical blocks of the next 32 (and following 32) chunks to issue, one per lane.
-    int tbl_cur = lane < my_chunks ? __ldg(table + chunk_row(lane) / p.block_size) : 0;
-    int tbl_next = 32 + lane < my_chunks ? __ldg(table + chunk_row(32 + lane) / p.block_size) : 0;
+    int tbl_cur = leader && lane < my_chunks ? __ldg(table + chunk_row(lane) / p.block_size) : 0;
+    int tbl_next = leader && 32 + lane < my_chunks ? __ldg(table + chunk_row(32 + lane) / p.block_size) : 0;
     int issued = 0;
 
-    auto issue_next = [&]() {  // warp-uniform; lane 0 issues the copies
+    auto issue_next = [&]() {  // the leader warp, warp-uniform; its lane 0 issues the copies
       if (issued >= my_chunks) return;
       if (issued > 0 && (issued & 31) == 0) {
         tbl_cur = tbl_next;
@@ -222,7 +243,7 @@ __global__ void __maxnreg__(200)
         tbl_next = k < my_chunks ? __ldg(table + chunk_row(k) / p.block_size) : 0;
       }
       const int ph = __shfl_sync(0xffffffffu, tbl_cur, issued & 31);
-      const int s = issued % C::kStagesPerWarp;
+      const int s = issued % C::kStagesPerGroup;
       if (lane == 0) {
         const bool ok = static_cast<unsigned>(ph) < static_cast<unsigned>(p.num_blocks);
         my_ok[s] = ok ? 1 : 0;
@@ -255,7 +276,8 @@ __global__ void __maxnreg__(200)
     };
 
 #pragma unroll 1
-    for (int s = 0; s < C::kStagesPerWarp; ++s) issue_next();
+    for (int s = 0; s < C::kStagesPerGroup; ++s)
+      if (leader) issue_next();
 
     // B fragments of Q^T for every k-step, rows r = 8*nt + g of this KV head: bf16 as
     // stored for bf16 pages; for affine pages fp16, after an exact power-of-two
@@ -270,7 +292,7 @@ __global__ void __maxnreg__(200)
       for (int kk = 0; kk < C::kKs; ++kk) {
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-          const int r = 8 * nt + g;
+          const int r = rbase + 8 * nt + g;
 #pragma unroll
           for (int reg = 0; reg < 2; ++reg) {
             int dl, dh;
@@ -359,21 +381,23 @@ __global__ void __maxnreg__(200)
     }
 
     const int vis_base = len - N + 1;  // query row qi sees keys < vis_base + qi
+    const int win = p.window;          // ... and, when win > 0, keys >= vis_base + qi - win
     // ldmatrix row/chunk of this lane: non-transposed (keys on M) and transposed (keys on K).
     const int lrow_n = (lane & 7) + ((lane >> 3) & 1) * 8, lch_n = lane >> 4;
     const int lrow_t = (lane & 7) + (lane >> 4) * 8, lch_t = (lane >> 3) & 1;
 
     int done = 0;  // local chunks consumed
     for (; done < my_chunks; ++done) {
-      const int s = done % C::kStagesPerWarp;
-      if (!mbar_wait_warp(smem_addr(&my_full[s]), (done / C::kStagesPerWarp) & 1, abort_flag, p.error_flag)) break;
-      if (my_ok[s]) {
+      const int s = done % C::kStagesPerGroup;
+      const bool landed = mbar_wait_warp(smem_addr(&my_full[s]), (done / C::kStagesPerGroup) & 1, abort_flag,
+                                         p.error_flag);
+      if (landed && my_ok[s]) {
         uint8_t* stage = my_ring + s * C::kStageBytes;
         const uint32_t kpl = smem_addr(stage);
         const uint32_t vpl = kpl + C::kPlaneBytes;
         const uint32_t sbq = kpl + 2 * C::kPlaneBytes;  // scale/bias planes (affine pages)
         const int kbase = chunk_row(done);
-        const bool full_vis = kbase + C::kCh <= vis_base;
+        const bool full_vis = kbase + C::kCh <= vis_base && (win == 0 || kbase >= vis_base + N - 1 - win);
         const bool stale = kbase + C::kCh > len;
 
         // ---- scores x = (K q) * scale * log2(e), keys on rows
@@ -467,8 +491,9 @@ __global__ void __maxnreg__(200)
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
                 const int key = kbase + tile * 16 + g + 8 * (e >> 1);
-                const int qi = (8 * nt + 2 * t + (e & 1)) % N;
-                x[tile][nt][e] = key < vis_base + qi ? x[tile][nt][e] : -INFINITY;
+                const int qi = (rbase + 8 * nt + 2 * t + (e & 1)) % N;
+                const bool vis = key < vis_base + qi && (win == 0 || key >= vis_base + qi - win);
+                x[tile][nt][e] = vis ? x[tile][nt][e] : -INFINITY;
               }
         }
 
@@ -612,15 +637,22 @@ __global__ void __maxnreg__(200)
           }
         }
       }
-      __syncwarp();   // every lane is done with the stage before it is refilled
-      issue_next();
+      if constexpr (WQ == 1) {
+        if (!landed) break;
+        __syncwarp();  // every lane is done with the stage before it is refilled
+        issue_next();
+      } else {
+        // every warp of the group is done with the stage; one give-up decision for all
+        if (group_barrier_any(1 + pg, WQ * 32, !landed)) break;
+        if (leader) issue_next();
+      }
     }
-    if (done < issued && lane == 0) {
-      // Aborted: let this warp's copies still in flight land before the ring is reused.
+    if (leader && done < issued && lane == 0) {
+      // Aborted: let this group's copies still in flight land before the ring is reused.
       for (int c = done; c < issued; ++c) {
-        const uint32_t bar = smem_addr(&my_full[c % C::kStagesPerWarp]);
+        const uint32_t bar = smem_addr(&my_full[c % C::kStagesPerGroup]);
         const unsigned long long start = global_timer_ns();
-        while (!mbar_try_wait(bar, (c / C::kStagesPerWarp) & 1) && global_timer_ns() - start < kWaitLimitNs) {
+        while (!mbar_try_wait(bar, (c / C::kStagesPerGroup) & 1) && global_timer_ns() - start < kWaitLimitNs) {
         }
       }
     }
@@ -663,8 +695,11 @@ __global__ void __maxnreg__(200)
 
   // ---- combine the consumer warps' states and write out
   float* cm = reinterpret_cast<float*>(smem);
-  float* cl = cm + C::kWarps * C::kNqp;
-  float* co = cl + C::kWarps * C::kNqp;
+  float* cl = cm + C::kWP * C::kNqAll;
+  float* co = cl + C::kWP * C::kNqAll;
+  float* st_m = co + C::kWP * C::kNqAll * D;  // this CTA's merged state (cluster merge)
+  float* st_l = st_m + C::kNqAll;
+  float* st_o = st_l + C::kNqAll;
   if (warp < C::kWarps) {
     if (g == 0) {
 #pragma unroll
@@ -672,8 +707,8 @@ __global__ void __maxnreg__(200)
 #pragma unroll
         for (int e2 = 0; e2 < 2; ++e2) {
           const int r = 8 * nt + 2 * t + e2;
-          cm[warp * C::kNqp + r] = m_run[nt][e2];
-          cl[warp * C::kNqp + r] = l_run[nt][e2];
+          cm[pg * C::kNqAll + rbase + r] = m_run[nt][e2];
+          cl[pg * C::kNqAll + rbase + r] = l_run[nt][e2];
         }
     }
 #pragma unroll
@@ -683,7 +718,7 @@ __global__ void __maxnreg__(200)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int r = 8 * nt + 2 * t + (e & 1);
-          co[(warp * C::kNqp + r) * D + out_dim<BITS>(mt, e >> 1, g)] = o[mt][nt][e];
+          co[(pg * C::kNqAll + rbase + r) * D + out_dim<BITS>(mt, e >> 1, g)] = o[mt][nt][e];
         }
   }
   __syncthreads();
@@ -692,30 +727,64 @@ __global__ void __maxnreg__(200)
     const int r = idx / D, d = idx % D;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < C::kWarps; ++w) M = fmaxf(M, cm[w * C::kNqp + r]);
+    for (int w = 0; w < C::kWP; ++w) M = fmaxf(M, cm[w * C::kNqAll + r]);
     float L = 0.f, O = 0.f;
     if (M != -INFINITY) {
 #pragma unroll
-      for (int w = 0; w < C::kWarps; ++w) {
-        const float mw = cm[w * C::kNqp + r];
+      for (int w = 0; w < C::kWP; ++w) {
+        const float mw = cm[w * C::kNqAll + r];
         if (mw != -INFINITY) {
           const float wt = fast_exp2(mw - M);
-          L = fmaf(wt, cl[w * C::kNqp + r], L);
-          O = fmaf(wt, co[(w * C::kNqp + r) * D + d], O);
+          L = fmaf(wt, cl[w * C::kNqAll + r], L);
+          O = fmaf(wt, co[(w * C::kNqAll + r) * D + d], O);
         }
       }
     }
     const size_t orow = row0 + r;
     if (single) {
       p.out[orow * D + d] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
-    } else {
-      const size_t slot = orow * p.max_partitions + part;
-      p.ws_o[slot * D + d] = O;
+    } else if (in_cluster) {
+      st_o[r * D + d] = O;
       if (d == 0) {
-        p.ws_ml[slot * 2] = M;
-        p.ws_ml[slot * 2 + 1] = L;
+        st_m[r] = M;
+        st_l[r] = L;
+      }
+    } else {
+      const size_t ws = orow * p.max_partitions + slot;
+      p.ws_o[ws * D + d] = O;
+      if (d == 0) {
+        p.ws_ml[ws * 2] = M;
+        p.ws_ml[ws * 2 + 1] = L;
       }
     }
+  }
+
+  if (in_cluster) {
+    // ---- merge the cluster's partition states (log-sum-exp) through distributed
+    // shared memory; cluster CTA j holds the state of slot j. Each CTA finishes one
+    // slice of the (row, dim) outputs.
+    cluster_sync();
+    const int cs = p.max_partitions;
+    const int total = p.nq * D;
+    const int per = (total + cs - 1) / cs;
+    const int end = min(total, (slot + 1) * per);
+    for (int idx = slot * per + threadIdx.x; idx < end; idx += C::kThreads) {
+      const int r = idx / D, d = idx % D;
+      float M = -INFINITY;
+      for (int j = 0; j < cs; ++j) M = fmaxf(M, ld_cluster_f32(smem_addr(&st_m[r]), j));
+      float L = 0.f, O = 0.f;
+      if (M != -INFINITY) {
+        for (int j = 0; j < cs; ++j) {
+          const float mj = ld_cluster_f32(smem_addr(&st_m[r]), j);
+          if (mj == -INFINITY) continue;
+          const float wt = fast_exp2(mj - M);
+          L = fmaf(wt, ld_cluster_f32(smem_addr(&st_l[r]), j), L);
+          O = fmaf(wt, ld_cluster_f32(smem_addr(&st_o[r * D + d]), j), O);
+        }
+      }
+      p.out[(row0 + r) * D + d] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
+    }
+    cluster_sync();  // no CTA leaves while another still reads its shared memory
   }
 }
 

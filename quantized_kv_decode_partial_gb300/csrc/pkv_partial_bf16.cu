@@ -1,26 +1,31 @@
-// bf16 pages: head_dim 64 (up to 32 query rows per KV head), 128 (up to 16), 256 (up to 8).
+// bf16 pages: head_dim 64 / 128 / 256 with up to 64 / 64 / 32 query rows per KV head.
 #include "pkv_partial_instances.cuh"
 
 namespace pkv {
 
-PartialInfo partial_info_bf16(int d, int nt) {
-  if (d == 64 && nt == 1) return info_of<16, 64, 1>();
-  if (d == 64 && nt == 2) return info_of<16, 64, 2>();
-  if (d == 64 && nt == 4) return info_of<16, 64, 4>();
-  if (d == 128 && nt == 1) return info_of<16, 128, 1>();
-  if (d == 128 && nt == 2) return info_of<16, 128, 2>();
-  if (d == 256 && nt == 1) return info_of<16, 256, 1>();
+#define PKV_BF16_INSTANCES(X) \
+  X(64, 1, 1) X(64, 2, 1) X(64, 4, 1) X(64, 4, 2) \
+  X(128, 1, 1) X(128, 2, 1) X(128, 2, 2) X(128, 2, 4) \
+  X(256, 1, 1) X(256, 1, 2) X(256, 1, 4)
+
+PartialInfo partial_info_bf16(int d, int nq) {
+  int nt, wq;
+  tiles_for(d, nq, nt, wq);
+#define X(D_, NT_, WQ_) \
+  if (d == D_ && nt == NT_ && wq == WQ_) return info_of<16, D_, NT_, WQ_>();
+  PKV_BF16_INSTANCES(X)
+#undef X
   return PartialInfo{false, 0, 0, 0, 0, 0};
 }
 
-cudaError_t launch_partial_bf16(int d, int nt, const PartialParams& p, const CUtensorMap& tk,
-                                const CUtensorMap& tv, dim3 grid, cudaStream_t s) {
-  if (d == 64 && nt == 1) return launch_of<16, 64, 1>(p, tk, tv, grid, s);
-  if (d == 64 && nt == 2) return launch_of<16, 64, 2>(p, tk, tv, grid, s);
-  if (d == 64 && nt == 4) return launch_of<16, 64, 4>(p, tk, tv, grid, s);
-  if (d == 128 && nt == 1) return launch_of<16, 128, 1>(p, tk, tv, grid, s);
-  if (d == 128 && nt == 2) return launch_of<16, 128, 2>(p, tk, tv, grid, s);
-  if (d == 256 && nt == 1) return launch_of<16, 256, 1>(p, tk, tv, grid, s);
+cudaError_t launch_partial_bf16(int d, int nq, const PartialParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                                dim3 grid, cudaStream_t s, int dev) {
+  int nt, wq;
+  tiles_for(d, nq, nt, wq);
+#define X(D_, NT_, WQ_) \
+  if (d == D_ && nt == NT_ && wq == WQ_) return launch_of<16, D_, NT_, WQ_>(p, tk, tv, grid, s, dev);
+  PKV_BF16_INSTANCES(X)
+#undef X
   return cudaErrorInvalidValue;
 }
 

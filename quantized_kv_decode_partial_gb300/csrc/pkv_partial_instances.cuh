@@ -2,27 +2,79 @@
 // pkv_partial_bf16.cu / pkv_partial_u4.cu / pkv_partial_u8.cu with PKV_BITS set.
 #pragma once
 
+#include <atomic>
+
 #include "pkv_launch.h"
 #include "pkv_partial.cuh"
 
 namespace pkv {
 namespace {
 
-template <int BITS, int D, int NT>
+template <int BITS, int D, int NT, int WQ>
 PartialInfo info_of() {
-  using C = PartialCfg<BITS, D, NT>;
+  using C = PartialCfg<BITS, D, NT, WQ>;
   return PartialInfo{true, C::kThreads, C::kSmemBytes, C::kCh, C::kRB, C::kElemBytes};
 }
 
-template <int BITS, int D, int NT>
-cudaError_t launch_of(const PartialParams& p, const CUtensorMap& tk, const CUtensorMap& tv, dim3 grid,
-                      cudaStream_t stream) {
-  using C = PartialCfg<BITS, D, NT>;
-  auto kern = pkv_partial_kernel<BITS, D, NT>;
+// Devices on which an instantiation's function attributes are set (bit per device < 64).
+template <int BITS, int D, int NT, int WQ>
+std::atomic<unsigned long long> g_configured{0};
+
+template <int BITS, int D, int NT, int WQ>
+cudaError_t configure_once(int device) {
+  using C = PartialCfg<BITS, D, NT, WQ>;
+  auto kern = pkv_partial_kernel<BITS, D, NT, WQ>;
+  const unsigned long long bit = device >= 0 && device < 64 ? (1ull << device) : 0ull;
+  if (bit && (g_configured<BITS, D, NT, WQ>.load(std::memory_order_acquire) & bit)) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(p, tk, tv);
-  return cudaGetLastError();
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);  // clusters of up to 16
+  if (e != cudaSuccess) return e;
+  if (bit) g_configured<BITS, D, NT, WQ>.fetch_or(bit, std::memory_order_acq_rel);
+  return cudaSuccess;
+}
+
+template <int BITS, int D, int NT, int WQ>
+cudaError_t launch_of(const PartialParams& p, const CUtensorMap& tk, const CUtensorMap& tv, dim3 grid,
+                      cudaStream_t stream, int device) {
+  using C = PartialCfg<BITS, D, NT, WQ>;
+  auto kern = pkv_partial_kernel<BITS, D, NT, WQ>;
+  cudaError_t e = configure_once<BITS, D, NT, WQ>(device);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  if (p.mode == kModeCluster) {  // the partitions of one (sequence, KV head) form a cluster
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = grid.x;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  return cudaLaunchKernelEx(&cfg, kern, p, tk, tv);
+}
+
+// Instantiation for `nq` query rows per KV head: NT n-tiles of 8 rows per warp and
+// WQ warps per query group (NT * WQ * 8 >= nq), or (0, 0) when unsupported.
+inline void tiles_for(int head_dim, int nq, int& nt, int& wq) {
+  nt = wq = 0;
+  if (nq < 1) return;
+  const int ntiles = (nq + 7) / 8;
+  const int nt_max = 256 / head_dim;  // accumulator registers: head_dim * NT / 32 per thread
+  if (ntiles <= nt_max) {
+    nt = ntiles <= 1 ? 1 : ntiles <= 2 ? 2 : 4;
+    wq = 1;
+  } else if (ntiles <= 2 * nt_max) {
+    nt = nt_max;
+    wq = 2;
+  } else if (ntiles <= 4 * nt_max && head_dim >= 128) {
+    nt = nt_max;
+    wq = 4;
+  }
 }
 
 }  // namespace

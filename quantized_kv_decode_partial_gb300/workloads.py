@@ -52,6 +52,7 @@ class DecodeSpec:
     length_range: Optional[tuple] = None  # (lo, hi) inclusive, drawn uniformly
     pool_factor: float = 2.0  # pool blocks = ceil(factor * blocks needed)
     partition_tokens: int = 0  # 0 = library choice; -1 = one partition
+    window: int = 0  # sliding window in rows (0 = none)
     seed: int = 0
     description: str = ""
 
@@ -138,6 +139,12 @@ WORKLOADS = {
         partition_tokens=0, seed=1005,
         description="long-context few-query paged decode, 8 sequences x 4 queries, len 131072, "
                     "HQ=32 HK=8 D=128, BS=16, fragmented 2x pool"),
+    "bf16_8x131072_n4_w8192_hq32_d128": DecodeSpec(
+        name="bf16_8x131072_n4_w8192_hq32_d128", num_seqs=8, num_q_heads=32, num_kv_heads=8, head_dim=128,
+        n_query=4, block_size=16, bits=16, lengths=(131072,) * 8, pool_factor=2.0, window=8192,
+        partition_tokens=0, seed=1006,
+        description="sliding-window few-query paged decode: the long-context workload with an 8192-row "
+                    "window (each query sees its 8192 most recent rows)"),
 }
 
 # The two layers of the affine batch workload form one decode step.
@@ -249,5 +256,7 @@ def row_bytes(spec: DecodeSpec) -> int:
 
 
 def required_kv_bytes(spec: DecodeSpec, lens) -> int:
-    """K/V bytes a decode step must read: every cached row once per KV head, K and V."""
-    return int(sum(lens)) * spec.num_kv_heads * 2 * row_bytes(spec)
+    """K/V bytes a decode step must read: every visible cached row once per KV head, K and V.
+    With a sliding window W the N queries of a sequence together see its last W + N - 1 rows."""
+    rows = sum(min(l, spec.window + spec.n_query - 1) if spec.window > 0 else l for l in lens)
+    return int(rows) * spec.num_kv_heads * 2 * row_bytes(spec)

@@ -43,6 +43,7 @@ def oracle_inputs(case: DecodeCase):
 
 def oracle_out(case: DecodeCase, partition_tokens=None, rows=None):
     args, kw = oracle_inputs(case)
+    kw["window"] = case.spec.window
     if partition_tokens:
         return oracle.paged_decode_attention_partitioned(*args, partition_tokens, rows=rows, **kw)
     return oracle.paged_decode_attention(*args, rows=rows, **kw)
@@ -53,7 +54,7 @@ def run_gpu(case: DecodeCase, partition_tokens=None, error_flag=None):
     return paged_decode_attention(case.q, case.k_pool, case.v_pool, case.block_tables, case.seq_lens, case.scale,
                                   bits=case.spec.bits, group_size=case.spec.group_size, k_scales=case.k_scales,
                                   k_biases=case.k_biases, v_scales=case.v_scales, v_biases=case.v_biases,
-                                  partition_tokens=pt, error_flag=error_flag)
+                                  partition_tokens=pt, window=case.spec.window, error_flag=error_flag)
 
 
 def assert_close(got, ref, what=""):
@@ -95,7 +96,7 @@ def subcase(case: DecodeCase, b: int, kv: int) -> DecodeCase:
 
     sub_spec = DecodeSpec(name=s.name + f"_b{b}_kv{kv}", num_seqs=1, num_q_heads=rep, num_kv_heads=1,
                           head_dim=s.head_dim, n_query=s.n_query, block_size=s.block_size, bits=s.bits,
-                          group_size=s.group_size, lengths=(L,))
+                          group_size=s.group_size, lengths=(L,), window=s.window)
     return DecodeCase(
         spec=sub_spec, q=case.q[b:b + 1, kv * rep:(kv + 1) * rep].contiguous().cpu(),
         k_pool=pick(case.k_pool), v_pool=pick(case.v_pool),

@@ -53,7 +53,7 @@ def _params(spec, max_blocks, partition=None):
     pt = spec.partition_tokens if partition is None else partition
     if pt < 0:
         pt = max_blocks * spec.block_size
-    return B.DecodeParams(spec.num_seqs, spec.num_q_heads, spec.n_query, max_blocks, pt)
+    return B.DecodeParams(spec.num_seqs, spec.num_q_heads, spec.n_query, max_blocks, pt, spec.window)
 
 
 @pytest.mark.parametrize("name", sorted(WORKLOADS))
@@ -64,21 +64,52 @@ def test_plan_for_workloads(lib, name):
     plan = B.make_plan(_layout(sp), _params(sp, max_blocks), sm_count=152)
     ch = 16 if sp.bits == 16 else 32  # partitions are whole multiples of this
     assert plan.chunk_rows in (16, 32) and plan.partition_tokens % ch == 0 and ch % plan.chunk_rows == 0
-    assert plan.max_partitions == -(-max_blocks * sp.block_size // plan.partition_tokens)
+    table_parts = -(-max_blocks * sp.block_size // plan.partition_tokens)
+    if sp.window:  # only the partitions a window can touch
+        assert plan.max_partitions == min(table_parts, -(-(sp.window + sp.n_query - 1) // plan.partition_tokens) + 1)
+    else:
+        assert plan.max_partitions == table_parts
     if sp.partition_tokens > 0:
         assert plan.partition_tokens == sp.partition_tokens
-    if plan.max_partitions == 1:
+    # one wave of CTAs with 2..16 partitions merges inside a thread-block cluster
+    ctas = sp.num_seqs * sp.num_kv_heads * plan.max_partitions
+    assert plan.merge_in_cluster == (2 <= plan.max_partitions <= 16 and ctas <= 2 * 152)
+    if plan.max_partitions == 1 or plan.merge_in_cluster:
         assert plan.workspace_bytes == 0
     else:
         slots = sp.num_seqs * sp.num_q_heads * sp.n_query * plan.max_partitions
         assert plan.workspace_bytes >= slots * (sp.head_dim + 2) * 4
-        # auto plans launch several waves of 2 CTAs per SM, never partitions below 256 rows
+        # auto plans: never below 256 rows; either about four waves of 2 CTAs per SM, or at least one
+        # wave of CTAs that each still get 512 KB of K/V, or the 256-row floor
         if sp.partition_tokens == 0:
             assert plan.partition_tokens >= 256
-            assert sp.num_seqs * sp.num_kv_heads * plan.max_partitions >= 8 * 152 or plan.partition_tokens == 256
+            ctas = sp.num_seqs * sp.num_kv_heads * plan.max_partitions
+            kv_row = 2 * (2 * sp.head_dim if sp.bits == 16 else sp.head_dim * sp.bits // 8 + sp.head_dim // 16)
+            assert (ctas >= 8 * 152 or plan.partition_tokens == 256
+                    or (ctas >= 2 * 152 and plan.partition_tokens // 2 < (512 << 10) // kv_row))
     assert plan.threads_per_cta == 128 and 0 < plan.smem_bytes <= 227 * 1024
     if not (sp.bits == 16 and sp.head_dim == 256):  # 16 KB stages of bf16 D=256 take one CTA per SM
         assert plan.smem_bytes <= 114 * 1024  # two CTAs per SM
+
+
+def test_single_sequence_plans_merge_in_a_cluster(lib):
+    sp = WORKLOADS["affine4_g64_1x8192_hq16_d256"]  # 16 partitions x 4 KV heads = 64 CTAs
+    plan = B.make_plan(_layout(sp), _params(sp, 256), sm_count=152)
+    assert plan.max_partitions == 16 and plan.merge_in_cluster == 1 and plan.workspace_bytes == 0
+    # 17 partitions do not fit a cluster; a grid of more than one wave does not use one either
+    assert B.make_plan(_layout(sp), _params(sp, 256, 480), sm_count=152).merge_in_cluster == 0
+    assert B.make_plan(_layout(sp), _params(sp, 256), sm_count=16).merge_in_cluster == 0
+
+
+@pytest.mark.parametrize("bits,head_dim,max_rows", [(16, 64, 64), (16, 128, 64), (16, 256, 32), (4, 128, 64),
+                                                     (4, 256, 32), (8, 128, 64), (8, 256, 32)])
+def test_query_rows_per_kv_head_limits(lib, bits, head_dim, max_rows):
+    for nq in (1, 8, 9, 16, 17, 32, 33, 64, 65):
+        lay = B.PoolLayout(100, 1, 32, head_dim, bits, 64)
+        par = B.DecodeParams(1, nq, 1, 4, 0, 0)  # REP = nq, N = 1
+        plan = B.Plan()
+        rc = lib.pkv_make_plan(ctypes.byref(lay), ctypes.byref(par), 152, ctypes.byref(plan))
+        assert rc == (B.PKV_OK if nq <= max_rows else B.PKV_ERR_UNSUPPORTED_SHAPE), (nq, rc)
 
 
 def test_plan_auto_is_monotone_in_sm_count(lib):
@@ -103,10 +134,11 @@ def test_plan_rejects_bad_layouts(lib, field, value, code):
 @pytest.mark.parametrize("field,value,code", [
     ("num_q_heads", 6, B.PKV_ERR_BAD_PARAMS), ("n_query", 0, B.PKV_ERR_BAD_PARAMS),
     ("num_seqs", 0, B.PKV_ERR_BAD_PARAMS), ("max_blocks_per_seq", 0, B.PKV_ERR_BAD_PARAMS),
-    ("partition_tokens", -1, B.PKV_ERR_BAD_PARAMS), ("n_query", 3, B.PKV_ERR_UNSUPPORTED_SHAPE),
+    ("partition_tokens", -1, B.PKV_ERR_BAD_PARAMS), ("n_query", 9, B.PKV_ERR_UNSUPPORTED_SHAPE),
+    ("window", -1, B.PKV_ERR_BAD_PARAMS),
 ])
 def test_plan_rejects_bad_params(lib, field, value, code):
-    sp = WORKLOADS["affine4_g64_1x8192_hq16_d256"]  # HQ 16 / HK 4: REP 4, so n_query 3 asks for 12 > 8 rows at D 256
+    sp = WORKLOADS["affine4_g64_1x8192_hq16_d256"]  # HQ 16 / HK 4: REP 4, so n_query 9 asks for 36 > 32 rows at D 256
     par = _params(sp, 256)
     setattr(par, field, value)
     plan = B.Plan()

@@ -1,0 +1,102 @@
+"""GPU parity of the write side: pkv_paged_append against the write oracle, bit
+for bit (codes, scales, biases and bf16 rows), then a decode over the appended
+cache against the attention oracle."""
+
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+from helpers import assert_close, oracle_out, run_gpu
+from oracle import paged_write as pw
+from quantized_kv_decode_partial_gb300 import binding as B
+from quantized_kv_decode_partial_gb300 import paged_append
+from quantized_kv_decode_partial_gb300.workloads import DecodeSpec, make_case
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+
+
+def bits_of(t):
+    if t is None:
+        return None
+    if t.dtype == torch.bfloat16:
+        return t.detach().cpu().view(torch.int16).numpy().view(np.uint16)
+    return t.detach().cpu().numpy()
+
+
+def setup(bits, D, n_new, num_seqs=3, seed_name=""):
+    name = f"app_{bits}_{D}_{n_new}_{seed_name}"
+    seed = zlib.crc32(name.encode()) % 10000
+    bs = 16 if bits == 16 else 32
+    sp = DecodeSpec(name=name, num_seqs=num_seqs, num_q_heads=4, num_kv_heads=2, head_dim=D, n_query=1,
+                    block_size=bs, bits=bits, length_range=(1, 150), pool_factor=2.0, seed=seed)
+    g = torch.Generator().manual_seed(seed + 1)
+    lens = [int(x) for x in torch.randint(0, 150, (num_seqs,), generator=g)]
+    lens[0] = bs - 1  # the new rows of sequence 0 cross a page boundary
+    case = make_case(sp, lengths=[l + n_new for l in lens], poison=False)  # tables hold the new rows' pages
+    # new rows with very different ranges per group (including a constant group)
+    k_new = torch.randn((num_seqs, 2, n_new, D), generator=g) * torch.rand((num_seqs, 2, n_new, D // 16), generator=g).repeat_interleave(16, -1) * 8
+    v_new = torch.randn((num_seqs, 2, n_new, D), generator=g)
+    k_new[..., :64] = k_new[..., :1]
+    return sp, case, lens, k_new.to(torch.bfloat16), v_new.to(torch.bfloat16)
+
+
+CASES = [(16, 128, 1), (16, 64, 3), (16, 256, 2), (4, 256, 1), (4, 128, 3), (8, 256, 2), (8, 128, 1)]
+
+
+@pytest.mark.parametrize("bits,D,n_new", CASES)
+def test_append_is_bit_exact(bits, D, n_new):
+    sp, case, lens, k_new, v_new = setup(bits, D, n_new)
+    ref = pw.append_rows(k_new.float().numpy(), v_new.float().numpy(), case.block_tables.numpy(), lens,
+                         bits_of(case.k_pool), bits_of(case.v_pool), bits=bits,
+                         k_scales=bits_of(case.k_scales), k_biases=bits_of(case.k_biases),
+                         v_scales=bits_of(case.v_scales), v_biases=bits_of(case.v_biases))
+    d = case.to(DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    paged_append(k_new.to(DEV), v_new.to(DEV), d.block_tables, torch.tensor(lens, dtype=torch.int32, device=DEV),
+                 d.k_pool, d.v_pool, bits=bits, k_scales=d.k_scales, k_biases=d.k_biases, v_scales=d.v_scales,
+                 v_biases=d.v_biases, error_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    got = {"k_pool": d.k_pool, "v_pool": d.v_pool}
+    if bits != 16:
+        got.update(k_scales=d.k_scales, k_biases=d.k_biases, v_scales=d.v_scales, v_biases=d.v_biases)
+    for name, t in got.items():
+        assert np.array_equal(bits_of(t), ref[name]), name
+
+
+@pytest.mark.parametrize("bits", [16, 4, 8])
+def test_decode_after_append_matches_oracle(bits):
+    D = 256 if bits == 4 else 128
+    sp, case, lens, k_new, v_new = setup(bits, D, 2, seed_name="decode")
+    d = case.to(DEV)
+    lens_d = torch.tensor(lens, dtype=torch.int32, device=DEV)
+    paged_append(k_new.to(DEV), v_new.to(DEV), d.block_tables, lens_d, d.k_pool, d.v_pool, bits=bits,
+                 k_scales=d.k_scales, k_biases=d.k_biases, v_scales=d.v_scales, v_biases=d.v_biases)
+    d.seq_lens = lens_d + 2
+    host = d.to("cpu")  # the appended cache, read back for the oracle
+    out = run_gpu(d, partition_tokens=32)
+    assert_close(out.double().cpu().numpy(), oracle_out(host), f"decode after append {bits}")
+
+
+def test_append_flags_bad_blocks_and_lengths():
+    sp, case, lens, k_new, v_new = setup(4, 256, 1, seed_name="bad")
+    d = case.to(DEV)
+    tb = d.block_tables.clone()
+    tb[1, lens[1] // sp.block_size] = case.num_blocks + 3
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    paged_append(k_new.to(DEV), v_new.to(DEV), tb, torch.tensor(lens, dtype=torch.int32, device=DEV), d.k_pool,
+                 d.v_pool, bits=4, k_scales=d.k_scales, k_biases=d.k_biases, v_scales=d.v_scales,
+                 v_biases=d.v_biases, error_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & B.PKV_DEVERR_BAD_BLOCK
+    err.zero_()
+    too_long = torch.tensor([tb.shape[1] * sp.block_size] * 3, dtype=torch.int32, device=DEV)
+    snapshot = d.k_pool.clone()
+    paged_append(k_new.to(DEV), v_new.to(DEV), d.block_tables, too_long, d.k_pool, d.v_pool, bits=4,
+                 k_scales=d.k_scales, k_biases=d.k_biases, v_scales=d.v_scales, v_biases=d.v_biases, error_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & B.PKV_DEVERR_BAD_SEQ_LEN
+    assert torch.equal(d.k_pool, snapshot)  # nothing written

@@ -49,11 +49,61 @@ SMALL = [
     (spec("u8_d128_nq4", head_dim=128, bits=8, block_size=64), [-1, 128]),
     (spec("u4_d256_nq8_n4", num_q_heads=4, num_kv_heads=2, head_dim=256, bits=4, n_query=4, block_size=32,
           length_range=(4, 300)), [-1, 32]),
+    # more query rows per KV head than one warp holds: warps share chunks, each with its own rows
+    (spec("bf16_d128_nq32", num_q_heads=32, num_kv_heads=1, length_range=(1, 400)), [-1, 48, 0]),
+    (spec("bf16_d128_nq64_n4", num_q_heads=16, num_kv_heads=1, n_query=4, length_range=(4, 400)), [-1, 64]),
+    (spec("bf16_d64_nq64_n2", num_q_heads=64, num_kv_heads=2, head_dim=64, n_query=2, length_range=(2, 300)), [-1, 32]),
+    (spec("bf16_d256_nq32_n4", num_q_heads=8, num_kv_heads=1, head_dim=256, n_query=4, length_range=(4, 300)), [-1, 64]),
+    (spec("bf16_d256_nq16", num_q_heads=16, num_kv_heads=1, head_dim=256, length_range=(1, 300)), [-1, 48]),
+    (spec("u4_d256_nq16", num_q_heads=16, num_kv_heads=1, head_dim=256, bits=4, block_size=32,
+          length_range=(1, 400)), [-1, 64]),
+    (spec("u4_d128_nq64_n2", num_q_heads=32, num_kv_heads=1, head_dim=128, bits=4, n_query=2, block_size=32,
+          length_range=(2, 400)), [-1, 96]),
+    (spec("u8_d256_nq32_n2", num_q_heads=16, num_kv_heads=1, head_dim=256, bits=8, n_query=2, block_size=32,
+          length_range=(2, 400)), [-1, 64]),
+    (spec("u8_d128_nq32", num_q_heads=32, num_kv_heads=1, head_dim=128, bits=8, block_size=32,
+          length_range=(1, 400)), [-1, 32]),
 ]
 
 
 @pytest.mark.parametrize("sp,parts", SMALL, ids=[s.name for s, _ in SMALL])
 def test_small_cases_match_oracle(sp, parts):
+    case = make_case(sp)
+    ref = oracle_out(case)
+    dcase = case.to(DEV)
+    for pt in parts:
+        err = torch.zeros(1, dtype=torch.int32, device=DEV)
+        ptok = (max(case.lens_host) + 64) if pt == -1 else pt
+        out = run_gpu(dcase, partition_tokens=ptok, error_flag=err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        assert_close(out.double().cpu().numpy(), ref, f"{sp.name} partition={pt}")
+
+
+@pytest.mark.parametrize("bits,parts", [(16, 16), (4, 16), (8, 2), (16, 9)])
+def test_cluster_merge_matches_oracle(bits, parts):
+    # one sequence: the partitions of each KV head merge inside a thread-block cluster
+    sp = spec(f"cluster_{bits}_{parts}", num_seqs=1, head_dim=128 if bits != 4 else 256, bits=bits, block_size=32,
+              lengths=(parts * 64 - 5,), length_range=None)
+    case = make_case(sp)
+    plan = B.make_plan(B.layout_for(case.k_pool, sp.head_dim, bits),
+                       B.DecodeParams(1, sp.num_q_heads, 1, case.block_tables.shape[1], 64))
+    assert plan.merge_in_cluster == 1 and plan.max_partitions == parts
+    out = run_gpu(case.to(DEV), partition_tokens=64)
+    assert_close(out.double().cpu().numpy(), oracle_out(case), f"cluster {bits} {parts}")
+
+
+WINDOWED = [
+    (spec("win_bf16_n1", length_range=(20, 900), window=100), [-1, 64, 0]),
+    (spec("win_bf16_n4", num_q_heads=4, num_kv_heads=1, n_query=4, length_range=(4, 700), window=37), [-1, 32, 96]),
+    (spec("win_u4", head_dim=256, bits=4, block_size=32, length_range=(50, 900), window=300), [-1, 64, 0]),
+    (spec("win_u8_n2", head_dim=128, bits=8, block_size=32, n_query=2, length_range=(2, 600), window=1), [-1, 96]),
+    (spec("win_bf16_one_seq", num_seqs=1, lengths=(2000,), length_range=None, window=700), [128, 256]),
+]
+
+
+@pytest.mark.parametrize("sp,parts", WINDOWED, ids=[s.name for s, _ in WINDOWED])
+def test_sliding_window_matches_oracle(sp, parts):
     case = make_case(sp)
     ref = oracle_out(case)
     dcase = case.to(DEV)
@@ -80,7 +130,8 @@ def test_partitioned_oracle_agrees_with_gpu_partitions():
 # ---------------------------------------------------------------------------
 
 FULL = ["bf16_1x1024_hq2_d256", "affine4_g64_1x8192_hq16_d256", "bf16_batch32_hq32_d128",
-        "affine4_batch64_hq32_d256", "affine8_batch64_hq32_d256", "bf16_8x131072_n4_hq32_d128"]
+        "affine4_batch64_hq32_d256", "affine8_batch64_hq32_d256", "bf16_8x131072_n4_hq32_d128",
+        "bf16_8x131072_n4_w8192_hq32_d128"]
 
 
 @pytest.mark.parametrize("name", FULL)

@@ -79,6 +79,8 @@ def dense_reference(case):
         i = torch.arange(N)[:, None]
         t = torch.arange(L)[None, :]
         mask = t <= (L - N + i)
+        if s.window > 0:  # the W most recent positions of each query, its own included
+            mask &= t > (L - N + i - s.window)
         outs.append(torch.nn.functional.scaled_dot_product_attention(
             q[b], Ke, Ve, attn_mask=mask, scale=case.scale).numpy())
     return np.stack(outs)
@@ -98,6 +100,8 @@ TINY = [
     tiny("u4_bs4", bits=4, seed=13),
     tiny("u8_bs4_n2", bits=8, n_query=2, length_range=(2, 33), seed=14),
     tiny("u4_bs16_g16", bits=4, head_dim=32, group_size=16, block_size=16, length_range=(5, 40), seed=15),
+    tiny("bf16_window7_n3", n_query=3, window=7, length_range=(3, 40), seed=16),
+    tiny("u8_window1_n2", bits=8, n_query=2, window=1, length_range=(2, 30), seed=17),
 ]
 
 
@@ -222,14 +226,31 @@ def test_identical_keys_and_zero_scale_give_mean_of_v():
             assert np.max(np.abs(zero[0, h, i] - mean)) < 1e-12
 
 
+def test_window_of_one_returns_the_own_row_and_a_wide_window_changes_nothing():
+    spec = tiny("win", num_seqs=2, n_query=3, length_range=(5, 40), seed=23)
+    case = make_case(spec)
+    args, kw = np_inputs(case)
+    own = oracle.paged_decode_attention(*args, window=1, **kw)
+    for b in range(2):
+        L = case.lens_host[b]
+        V = oracle.gather_pages(case.v_pool.double().numpy(), case.tables_host[b], L)
+        for h in range(spec.num_q_heads):
+            for i in range(3):
+                assert np.array_equal(own[b, h, i], V[h // spec.rep, L - 3 + i])
+    full = oracle.paged_decode_attention(*args, **kw)
+    wide = oracle.paged_decode_attention(*args, window=max(case.lens_host), **kw)
+    assert np.array_equal(full, wide)
+
+
 # ---------------------------------------------------------------------------
 # partitions and the log-sum-exp merge
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("spec", [TINY[1], TINY[4]], ids=lambda s: s.name)
+@pytest.mark.parametrize("spec", [TINY[1], TINY[4], TINY[6]], ids=lambda s: s.name)
 def test_merge_equals_unsplit_for_every_partition_size(spec):
     case = make_case(spec)
     args, kw = np_inputs(case)
+    kw["window"] = spec.window
     whole = oracle.paged_decode_attention(*args, **kw)
     Lmax = max(case.lens_host)
     for P in list(range(1, 9)) + [13, Lmax, Lmax + 5]:
@@ -253,7 +274,7 @@ def test_lse_merge_skips_empty_partitions():
 def test_matches_dense_sdpa(spec):
     case = make_case(spec)
     args, kw = np_inputs(case)
-    got = oracle.paged_decode_attention(*args, **kw)
+    got = oracle.paged_decode_attention(*args, window=spec.window, **kw)
     ref = dense_reference(case)
     assert np.isfinite(got).all()  # poisoned stale rows and blocks were never read
     assert np.max(np.abs(got - ref)) < 1e-12
@@ -305,7 +326,7 @@ def _pins_fail(monkeypatch, name, mutant):
     for spec in TINY:
         case = make_case(spec)
         args, kw = np_inputs(case)
-        got = opd.paged_decode_attention(*args, **kw)
+        got = opd.paged_decode_attention(*args, window=spec.window, **kw)
         ref = dense_reference(case)
         if not (np.isfinite(got).all() and np.max(np.abs(got - ref)) < 1e-12):
             failures += 1
@@ -366,3 +387,12 @@ def test_mutant_head_map_and_causal_offset_are_caught(monkeypatch):
         return h % num_kv_heads
 
     assert _pins_fail(monkeypatch, "kv_head", interleaved) > 0
+    monkeypatch.setattr(opd, "kv_head", lambda h, q, k: h // (q // k))
+
+    real_range = opd.visible_range
+
+    def window_too_wide(length, n_query, i, window=0):  # one extra row below the window
+        lo, hi = real_range(length, n_query, i, window)
+        return (max(0, lo - 1) if window > 0 else lo), hi
+
+    assert _pins_fail(monkeypatch, "visible_range", window_too_wide) > 0

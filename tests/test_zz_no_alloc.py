@@ -61,15 +61,15 @@ def test_no_alloc_matches_main_entry_twice(sp, partition):
 
 def test_no_alloc_coarsens_library_partitions_and_rejects_oversized_ones():
     lib = B.load_library()
-    # 2 sequences x 32 query heads (2 KV heads) x 2 queries; a 131072-row table. The library's own plan
-    # (256-row partitions) would need 512 partition states of (64 + 2) floats per
-    # row, about 17.3 MB: more than the 16 MiB scratch, so the no-alloc entry doubles
-    # the partition size. A caller-fixed 16-row partition cannot fit at all.
-    sp = spec("na_big", num_seqs=2, num_q_heads=32, num_kv_heads=2, head_dim=64, n_query=2,
-              lengths=(131072, 70000), length_range=None)
-    case = make_case(sp).to(DEV)
-    plan = B.make_plan(B.layout_for(case.k_pool, 64, 16),
-                       B.DecodeParams(2, 32, 2, case.block_tables.shape[1], 0))
+    # One sequence, 8 query heads on 1 KV head, 8 queries (64 query rows), a 262144-row
+    # table: the library's own plan (512-row partitions, 512 of them) needs about 17 MB of
+    # partition states, more than the 16 MiB scratch, so the no-alloc entry doubles the
+    # partition size. A caller-fixed 16-row partition cannot fit at all.
+    sp = spec("na_big", num_seqs=1, num_q_heads=8, num_kv_heads=1, head_dim=128, n_query=8,
+              lengths=(262144,), length_range=None, pool_factor=1.0)
+    case = make_case(sp, device=DEV, poison=False)
+    plan = B.make_plan(B.layout_for(case.k_pool, 128, 16),
+                       B.DecodeParams(1, 8, 8, case.block_tables.shape[1], 0))
     assert plan.workspace_bytes > B.PKV_STATIC_SCRATCH_BYTES
     out = torch.empty_like(case.q)
     assert no_alloc_call(lib, case, 16, out) == B.PKV_ERR_SCRATCH_TOO_SMALL
