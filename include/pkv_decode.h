@@ -90,7 +90,7 @@ extern "C" {
 typedef struct pkv_pool_layout {
   int32_t num_blocks;   /* blocks in the pool, > 0 */
   int32_t num_kv_heads; /* HK, > 0 */
-  int32_t block_size;   /* BS: rows per block; a multiple of 16 (bf16) or 32 (affine), <= 1024 */
+  int32_t block_size;   /* BS: rows per block; a multiple of 16 (bf16) or 32 (affine) */
   int32_t head_dim;     /* D: 64, 128 or 256 for bf16; 128 or 256 for affine */
   int32_t bits;         /* 16 = bf16 pages; 4 or 8 = affine codes */
   int32_t group_size;   /* affine group; must be 64 (ignored for bf16) */
@@ -227,6 +227,32 @@ int pkv_paged_append(const pkv_pool_layout* layout, int32_t num_seqs, int32_t ma
                      const void* k_new, const void* v_new, const int32_t* block_tables, const int32_t* seq_lens,
                      void* k_pool, void* v_pool, void* k_scales, void* k_biases, void* v_scales, void* v_biases,
                      int32_t* error_flag, void* stream);
+
+/* One decode step with its write: appends each sequence's N = n_query new K and
+ * V rows into their pages, then attends over the cache that holds them, in the
+ * same launches as pkv_paged_decode_attention. This is the pages' appendDecode
+ * (PagedKVCache.appendDecode: append, then read the paged view of the grown
+ * cache, "@mlx-bun/inference 0.0.0-stage -> 1.0.0", state/paged/cache.ts).
+ *   k_new, v_new  bf16 [num_seqs, num_kv_heads, n_query, head_dim], 16-byte
+ *                 aligned: the K and V rows of the step's query tokens
+ *   seq_lens      rows held AFTER the append, as for pkv_paged_decode_attention:
+ *                 the new rows go to cache positions seq_lens[b] - n_query ..
+ *                 seq_lens[b] - 1, whose blocks must already be in the tables
+ * Every other argument is that of pkv_paged_decode_attention; k_pool, v_pool and,
+ * for affine pages, the scale and bias planes are written. The rows written and
+ * the output are bit for bit those of pkv_paged_append (with seq_lens - n_query)
+ * followed by pkv_paged_decode_attention with the same plan. Each new row is
+ * written by the CTA whose partition holds it, before that CTA reads the
+ * partition, so no second launch and no re-read of the rows from another CTA is
+ * needed. Blocks shared by several sequences must not receive new rows (the
+ * caller copies them first). A row whose block id is bad is neither written nor
+ * read and sets PKV_DEVERR_BAD_BLOCK. */
+int pkv_paged_decode_append_attention(const pkv_pool_layout* layout, const pkv_decode_params* params,
+                                      const void* q, const void* k_new, const void* v_new, void* k_pool,
+                                      void* v_pool, void* k_scales, void* k_biases, void* v_scales,
+                                      void* v_biases, const int32_t* block_tables, const int32_t* seq_lens,
+                                      float scale, void* out, void* workspace, size_t workspace_bytes,
+                                      int32_t* error_flag, void* stream);
 
 /* Bit-exact gather of one pool plane into contiguous per-sequence rows, the
  * fetch copy of the pages' BlockPool.gather / pickBlocks (state/paged/cache.ts):

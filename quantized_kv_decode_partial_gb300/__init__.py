@@ -13,6 +13,7 @@ from .binding import (  # noqa: F401
     make_plan,
     paged_decode_attention,
     paged_decode_passes,
+    paged_decode_append_attention,
     paged_append,
     paged_gather,
 )

@@ -23,6 +23,7 @@ EXPORTS = (
     "pkv_paged_decode_partial",
     "pkv_merge_partitions",
     "pkv_paged_decode_attention_no_alloc",
+    "pkv_paged_decode_append_attention",
     "pkv_paged_append",
     "pkv_paged_gather",
     "pkv_strerror",
@@ -102,6 +103,9 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.pkv_paged_decode_attention_no_alloc.argtypes = [ctypes.POINTER(PoolLayout), ctypes.POINTER(DecodeParams),
                                                         P, P, P, P, P, P, P, P, P, F, P, P, P]
     lib.pkv_paged_decode_attention_no_alloc.restype = ctypes.c_int
+    lib.pkv_paged_decode_append_attention.argtypes = [ctypes.POINTER(PoolLayout), ctypes.POINTER(DecodeParams),
+                                                      P, P, P, P, P, P, P, P, P, P, P, F, P, P, SZ, P, P]
+    lib.pkv_paged_decode_append_attention.restype = ctypes.c_int
     lib.pkv_paged_append.argtypes = [ctypes.POINTER(PoolLayout), I32, I32, I32, P, P, P, P, P, P, P, P, P, P, P, P]
     lib.pkv_paged_append.restype = ctypes.c_int
     lib.pkv_paged_gather.argtypes = [P, I32, I32, I32, I32, P, P, I32, I32, I32, P, P, P]
@@ -195,6 +199,37 @@ def paged_decode_attention(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.
         rc = lib.pkv_paged_decode_attention(
             ctypes.byref(layout), ctypes.byref(params), _ptr(q), _ptr(k_pool), _ptr(v_pool),
             _ptr(k_scales), _ptr(k_biases), _ptr(v_scales), _ptr(v_biases), _ptr(block_tables),
+            _ptr(seq_lens), float(scale), _ptr(out), _ptr(workspace), ws_bytes, _ptr(error_flag), stream)
+    _check(rc, lib)
+    return out
+
+
+def paged_decode_append_attention(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                                  k_pool: torch.Tensor, v_pool: torch.Tensor, block_tables: torch.Tensor,
+                                  seq_lens: torch.Tensor, scale: float, *, bits: int = 16, group_size: int = 64,
+                                  k_scales: Optional[torch.Tensor] = None, k_biases: Optional[torch.Tensor] = None,
+                                  v_scales: Optional[torch.Tensor] = None, v_biases: Optional[torch.Tensor] = None,
+                                  partition_tokens: int = 0, window: int = 0, out: Optional[torch.Tensor] = None,
+                                  workspace: Optional[torch.Tensor] = None,
+                                  error_flag: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """One decode step with its write (pkv_paged_decode_append_attention): writes
+    k_new/v_new bf16 [B, HK, N, D] at cache positions seq_lens[b]-N .. seq_lens[b]-1
+    (seq_lens counts the new rows), then attends as ``paged_decode_attention``."""
+    lib = load_library()
+    B, HQ, N, D = q.shape
+    layout = layout_for(k_pool, D, bits, group_size)
+    params = DecodeParams(B, HQ, N, block_tables.shape[1], partition_tokens, window)
+    with _on_device(q.device):
+        plan = _cached_plan(layout, params)
+        if out is None:
+            out = torch.empty_like(q)
+        if workspace is None and plan.workspace_bytes:
+            workspace = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=q.device)
+        ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+        rc = lib.pkv_paged_decode_append_attention(
+            ctypes.byref(layout), ctypes.byref(params), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_pool),
+            _ptr(v_pool), _ptr(k_scales), _ptr(k_biases), _ptr(v_scales), _ptr(v_biases), _ptr(block_tables),
             _ptr(seq_lens), float(scale), _ptr(out), _ptr(workspace), ws_bytes, _ptr(error_flag), stream)
     _check(rc, lib)
     return out

@@ -254,6 +254,20 @@ int pkv_plan_for_current_device(const pkv_pool_layout* layout, const pkv_decode_
 
 namespace {
 
+pkv::AppendTarget append_target(bool quant, void* k_pool, void* v_pool, void* k_scales, void* k_biases,
+                                void* v_scales, void* v_biases) {
+  pkv::AppendTarget t{};
+  t.k_pool_bf16 = quant ? nullptr : static_cast<__nv_bfloat16*>(k_pool);
+  t.v_pool_bf16 = quant ? nullptr : static_cast<__nv_bfloat16*>(v_pool);
+  t.k_pool_words = quant ? static_cast<uint32_t*>(k_pool) : nullptr;
+  t.v_pool_words = quant ? static_cast<uint32_t*>(v_pool) : nullptr;
+  t.k_scales = static_cast<__nv_bfloat16*>(k_scales);
+  t.k_biases = static_cast<__nv_bfloat16*>(k_biases);
+  t.v_scales = static_cast<__nv_bfloat16*>(v_scales);
+  t.v_biases = static_cast<__nv_bfloat16*>(v_biases);
+  return t;
+}
+
 constexpr int kPassPartial = 1;
 constexpr int kPassMerge = 2;
 
@@ -261,7 +275,8 @@ int enqueue_decode(const pkv_pool_layout* layout, const pkv_decode_params* param
                    const void* k_pool, const void* v_pool, const void* k_scales, const void* k_biases,
                    const void* v_scales, const void* v_biases, const int32_t* block_tables,
                    const int32_t* seq_lens, float scale, void* out, void* workspace, size_t workspace_bytes,
-                   int32_t* error_flag, void* stream, int passes) {
+                   int32_t* error_flag, void* stream, int passes, const void* k_new = nullptr,
+                   const void* v_new = nullptr) {
   int rc = check_layout(layout);
   if (rc) return rc;
   rc = check_params(layout, params);
@@ -276,6 +291,8 @@ int enqueue_decode(const pkv_pool_layout* layout, const pkv_decode_params* param
     return PKV_ERR_MISALIGNED;
   if (quant && (!aligned(k_scales, 16) || !aligned(k_biases, 16) || !aligned(v_scales, 16) || !aligned(v_biases, 16)))
     return PKV_ERR_MISALIGNED;
+  if ((k_new == nullptr) != (v_new == nullptr)) return PKV_ERR_NULL_POINTER;
+  if (!aligned(k_new, 16) || !aligned(v_new, 16)) return PKV_ERR_MISALIGNED;
 
   int sms = 0, dev = 0;
   rc = device_sm_count(&sms, &dev);
@@ -330,6 +347,12 @@ int enqueue_decode(const pkv_pool_layout* layout, const pkv_decode_params* param
   p.partition_tokens = plan.partition_tokens;
   p.max_partitions = plan.max_partitions;
   p.score_scale = scale * 1.4426950408889634f;  // log2(e): scores run in base 2
+  if (k_new) {  // the pools are the caller's writable planes (the fused entry takes them non-const)
+    p.k_new = static_cast<const __nv_bfloat16*>(k_new);
+    p.v_new = static_cast<const __nv_bfloat16*>(v_new);
+    p.app = append_target(quant, const_cast<void*>(k_pool), const_cast<void*>(v_pool), const_cast<void*>(k_scales),
+                          const_cast<void*>(k_biases), const_cast<void*>(v_scales), const_cast<void*>(v_biases));
+  }
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   (void)cudaGetLastError();  // start from a clean error state
@@ -396,6 +419,17 @@ int pkv_merge_partitions(const pkv_pool_layout* layout, const pkv_decode_params*
                         kPassMerge);
 }
 
+int pkv_paged_decode_append_attention(const pkv_pool_layout* layout, const pkv_decode_params* params,
+                                      const void* q, const void* k_new, const void* v_new, void* k_pool,
+                                      void* v_pool, void* k_scales, void* k_biases, void* v_scales, void* v_biases,
+                                      const int32_t* block_tables, const int32_t* seq_lens, float scale, void* out,
+                                      void* workspace, size_t workspace_bytes, int32_t* error_flag, void* stream) {
+  if (!k_new || !v_new) return PKV_ERR_NULL_POINTER;
+  return enqueue_decode(layout, params, q, k_pool, v_pool, k_scales, k_biases, v_scales, v_biases, block_tables,
+                        seq_lens, scale, out, workspace, workspace_bytes, error_flag, stream,
+                        kPassPartial | kPassMerge, k_new, v_new);
+}
+
 int pkv_paged_append(const pkv_pool_layout* layout, int32_t num_seqs, int32_t max_blocks_per_seq, int32_t n_new,
                      const void* k_new, const void* v_new, const int32_t* block_tables, const int32_t* seq_lens,
                      void* k_pool, void* v_pool, void* k_scales, void* k_biases, void* v_scales, void* v_biases,
@@ -419,14 +453,7 @@ int pkv_paged_append(const pkv_pool_layout* layout, int32_t num_seqs, int32_t ma
   a.v_new = static_cast<const __nv_bfloat16*>(v_new);
   a.block_tables = block_tables;
   a.seq_lens = seq_lens;
-  a.k_pool_bf16 = quant ? nullptr : static_cast<__nv_bfloat16*>(k_pool);
-  a.v_pool_bf16 = quant ? nullptr : static_cast<__nv_bfloat16*>(v_pool);
-  a.k_pool_words = quant ? static_cast<uint32_t*>(k_pool) : nullptr;
-  a.v_pool_words = quant ? static_cast<uint32_t*>(v_pool) : nullptr;
-  a.k_scales = static_cast<__nv_bfloat16*>(k_scales);
-  a.k_biases = static_cast<__nv_bfloat16*>(k_biases);
-  a.v_scales = static_cast<__nv_bfloat16*>(v_scales);
-  a.v_biases = static_cast<__nv_bfloat16*>(v_biases);
+  a.dst = append_target(quant, k_pool, v_pool, k_scales, k_biases, v_scales, v_biases);
   a.error_flag = error_flag;
   a.num_blocks = layout->num_blocks;
   a.num_kv_heads = layout->num_kv_heads;

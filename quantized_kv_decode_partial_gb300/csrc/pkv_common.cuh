@@ -18,6 +18,19 @@ constexpr int kDevErrTimeout = 4;
 // Upper bound of one pipeline wait before the kernel gives up (nanoseconds).
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
 
+// Where appended rows are written: the pools and, for affine pages, the scale and
+// bias planes (all [NB, HK, BS, ...]).
+struct AppendTarget {
+  __nv_bfloat16* k_pool_bf16;  // bf16 pages
+  __nv_bfloat16* v_pool_bf16;
+  uint32_t* k_pool_words;      // affine pages
+  uint32_t* v_pool_words;
+  __nv_bfloat16* k_scales;
+  __nv_bfloat16* k_biases;
+  __nv_bfloat16* v_scales;
+  __nv_bfloat16* v_biases;
+};
+
 struct PartialParams {
   const __nv_bfloat16* q;     // [B, HQ, N, D]
   const int32_t* block_tables;  // [B, max_blocks]
@@ -36,6 +49,12 @@ struct PartialParams {
   int mode;           // kModeSingle / kModeWorkspace / kModeCluster
   int window;         // sliding window in rows (0: none)
   float score_scale;  // softmax scale * log2(e)
+  // Fused append (k_new != nullptr): the N new rows of every (sequence, KV head),
+  // cache rows len-N .. len-1, are written into their pages by the CTA whose
+  // partition holds them, before it reads that partition.
+  const __nv_bfloat16* k_new;  // [B, HK, N, D]
+  const __nv_bfloat16* v_new;
+  AppendTarget app;
 };
 
 // How the partial kernel finishes.
@@ -60,14 +79,7 @@ struct AppendParams {
   const __nv_bfloat16* v_new;
   const int32_t* block_tables;
   const int32_t* seq_lens;     // rows before the append
-  __nv_bfloat16* k_pool_bf16;  // bf16 pages
-  __nv_bfloat16* v_pool_bf16;
-  uint32_t* k_pool_words;      // affine pages
-  uint32_t* v_pool_words;
-  __nv_bfloat16* k_scales;
-  __nv_bfloat16* k_biases;
-  __nv_bfloat16* v_scales;
-  __nv_bfloat16* v_biases;
+  AppendTarget dst;
   int32_t* error_flag;
   int num_blocks, num_kv_heads, block_size, max_blocks, n_new;
 };
@@ -105,6 +117,12 @@ __device__ __forceinline__ void fence_barrier_init() {
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Orders this thread's generic-proxy global writes before later async-proxy (TMA,
+// bulk copy) reads of the same memory.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {

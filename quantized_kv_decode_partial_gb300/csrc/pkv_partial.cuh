@@ -44,6 +44,7 @@
 //    zeroed), so stale storage may hold anything, NaN included.
 #pragma once
 
+#include "pkv_append.cuh"
 #include "pkv_common.cuh"
 
 namespace pkv {
@@ -205,6 +206,20 @@ __global__ void __maxnreg__(200)
   // first row this CTA reads: the partition start, or the chunk holding the window's lowest row
   const int t_first = max(t0, win_lo / C::kCh * C::kCh);
   const int nchunks = empty ? 0 : (t_end - t_first + C::kCh - 1) / C::kCh;  // an empty cluster member still merges
+
+  if (p.k_new != nullptr && !empty) {
+    // Fused append: write the step's new rows len-N .. len-1 that fall in this
+    // partition (one warp per row), then make them visible to the TMA reads below.
+    const int32_t* table = p.block_tables + static_cast<size_t>(b) * p.max_blocks;
+    for (int tr = max(len - N, t0) + warp; tr < t_end; tr += C::kWarps) {
+      const int ph = __ldg(table + tr / p.block_size);
+      if (static_cast<unsigned>(ph) >= static_cast<unsigned>(p.num_blocks)) continue;  // flagged by the read
+      const size_t src = (static_cast<size_t>(b) * p.num_kv_heads + hk) * N + (tr - (len - N));
+      const size_t row = (static_cast<size_t>(ph) * p.num_kv_heads + hk) * p.block_size + tr % p.block_size;
+      append_row<BITS, D>(p.k_new + src * D, p.v_new + src * D, p.app, row, lane);
+    }
+    fence_proxy_async_global();
+  }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kWarps * C::kStagesPerWarp; ++s) mbar_init(smem_addr(&full_bar[s]), 1);

@@ -100,3 +100,103 @@ def test_append_flags_bad_blocks_and_lengths():
     torch.cuda.synchronize()
     assert int(err.item()) & B.PKV_DEVERR_BAD_SEQ_LEN
     assert torch.equal(d.k_pool, snapshot)  # nothing written
+
+
+# ---------------------------------------------------------------- fused append + attend
+
+def setup_fused(bits, D, N, hq, hk, seed_name, num_seqs=3, length_range=(1, 300), window=0):
+    name = f"fused_{bits}_{D}_{N}_{hq}_{seed_name}"
+    seed = zlib.crc32(name.encode()) % 10000
+    bs = 16 if bits == 16 else 32
+    g = torch.Generator().manual_seed(seed + 1)
+    lens = [int(x) for x in torch.randint(*length_range, (num_seqs,), generator=g)]
+    lens[0] = bs - 1  # the new rows of sequence 0 cross a page boundary
+    sp = DecodeSpec(name=name, num_seqs=num_seqs, num_q_heads=hq, num_kv_heads=hk, head_dim=D, n_query=N,
+                    block_size=bs, bits=bits, length_range=length_range, pool_factor=2.0, seed=seed, window=window)
+    case = make_case(sp, lengths=[l + N for l in lens], poison=False)  # seq_lens count the new rows
+    k_new = (torch.randn((num_seqs, hk, N, D), generator=g) * 3).to(torch.bfloat16)
+    v_new = torch.randn((num_seqs, hk, N, D), generator=g).to(torch.bfloat16)
+    return sp, case, lens, k_new, v_new
+
+
+FUSED = [
+    # bits, D, N, HQ, HK, partition_tokens (-1 single, 0 auto), window
+    (16, 128, 1, 8, 2, -1, 0),
+    (16, 128, 4, 8, 2, 32, 0),
+    (16, 256, 2, 4, 2, 64, 0),
+    (16, 64, 3, 8, 1, 48, 0),
+    (4, 256, 2, 8, 2, 64, 0),
+    (4, 128, 1, 4, 1, 0, 0),
+    (8, 128, 3, 8, 2, 32, 0),
+    (8, 256, 1, 8, 2, -1, 0),
+    (16, 128, 4, 8, 2, 32, 40),
+]
+
+
+@pytest.mark.parametrize("bits,D,N,hq,hk,part,window", FUSED,
+                         ids=[f"b{c[0]}_d{c[1]}_n{c[2]}_p{c[5]}_w{c[6]}" for c in FUSED])
+def test_fused_append_attend_matches_append_then_decode(bits, D, N, hq, hk, part, window):
+    sp, case, lens, k_new, v_new = setup_fused(bits, D, N, hq, hk, f"p{part}w{window}", window=window)
+    part = 1 << 20 if part < 0 else part  # one partition: any size past the table
+    # the write oracle's pools, then the attention oracle over them
+    ref = pw.append_rows(k_new.float().numpy(), v_new.float().numpy(), case.block_tables.numpy(), lens,
+                         bits_of(case.k_pool), bits_of(case.v_pool), bits=bits,
+                         k_scales=bits_of(case.k_scales), k_biases=bits_of(case.k_biases),
+                         v_scales=bits_of(case.v_scales), v_biases=bits_of(case.v_biases))
+    planes = ("k_pool", "v_pool") + (() if bits == 16 else ("k_scales", "k_biases", "v_scales", "v_biases"))
+
+    # two-call path: pkv_paged_append, then pkv_paged_decode_attention
+    two = case.to(DEV)
+    paged_append(k_new.to(DEV), v_new.to(DEV), two.block_tables, two.seq_lens - N, two.k_pool, two.v_pool,
+                 bits=bits, k_scales=two.k_scales, k_biases=two.k_biases, v_scales=two.v_scales,
+                 v_biases=two.v_biases)
+    out_two = run_gpu(two, partition_tokens=part)
+
+    # fused path
+    one = case.to(DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out_one = B.paged_decode_append_attention(
+        one.q, k_new.to(DEV), v_new.to(DEV), one.k_pool, one.v_pool, one.block_tables, one.seq_lens, case.scale,
+        bits=bits, k_scales=one.k_scales, k_biases=one.k_biases, v_scales=one.v_scales, v_biases=one.v_biases,
+        partition_tokens=part, window=window, error_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    for name in planes:  # the rows written are the write oracle's, bit for bit
+        assert np.array_equal(bits_of(getattr(one, name)), ref[name]), name
+    assert torch.equal(out_one.view(torch.int16), out_two.view(torch.int16))  # same plan, same bits
+    host = one.to("cpu")
+    assert_close(out_one.double().cpu().numpy(), oracle_out(host), f"fused {bits} {D} {N}")
+
+
+def test_fused_append_skips_and_flags_a_bad_block():
+    sp, case, lens, k_new, v_new = setup_fused(16, 128, 2, 4, 2, "bad")
+    d = case.to(DEV)
+    tb = d.block_tables.clone()
+    t_new = lens[1]  # first new row of sequence 1
+    tb[1, t_new // sp.block_size] = case.num_blocks + 5
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    snapshot = d.k_pool.clone()
+    B.paged_decode_append_attention(d.q, k_new.to(DEV), v_new.to(DEV), d.k_pool, d.v_pool, tb, d.seq_lens,
+                                    case.scale, partition_tokens=32, error_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & B.PKV_DEVERR_BAD_BLOCK
+    # sequence 1's rows in the bad block were not written anywhere else
+    changed = (d.k_pool.view(torch.int16) != snapshot.view(torch.int16)).any(dim=-1).nonzero().tolist()
+    good_rows = set()
+    for b in range(3):
+        for j in range(2):
+            t = lens[b] + j
+            blk = int(tb[b, t // sp.block_size])
+            if blk < case.num_blocks:
+                for h in range(2):
+                    good_rows.add((blk, h, t % sp.block_size))
+    assert {tuple(r) for r in changed} <= good_rows
+
+
+def test_fused_append_rejects_a_missing_new_row():
+    sp, case, lens, k_new, v_new = setup_fused(16, 128, 1, 4, 2, "null")
+    d = case.to(DEV)
+    with pytest.raises(B.PkvError) as e:
+        B.paged_decode_append_attention(d.q, None, v_new.to(DEV), d.k_pool, d.v_pool, d.block_tables, d.seq_lens,
+                                        case.scale)
+    assert e.value.code == B.PKV_ERR_NULL_POINTER
