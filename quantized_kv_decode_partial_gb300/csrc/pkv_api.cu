@@ -27,10 +27,10 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
 
-PartialInfo partial_info(int bits, int head_dim, int nq) {
-  if (bits == 16) return pkv::partial_info_bf16(head_dim, nq);
-  if (bits == 4) return pkv::partial_info_u4(head_dim, nq);
-  if (bits == 8) return pkv::partial_info_u8(head_dim, nq);
+PartialInfo partial_info(int bits, int head_dim, int nq, bool solo = false) {
+  if (bits == 16) return pkv::partial_info_bf16(head_dim, nq, solo);
+  if (bits == 4) return pkv::partial_info_u4(head_dim, nq, solo);
+  if (bits == 8) return pkv::partial_info_u8(head_dim, nq, solo);
   return PartialInfo{false, 0, 0, 0, 0, 0};
 }
 
@@ -68,7 +68,10 @@ int check_params(const pkv_pool_layout* L, const pkv_decode_params* P) {
 
 int round_up(long long x, int m) { return static_cast<int>((x + m - 1) / m * m); }
 
-int plan_impl(const pkv_pool_layout* L, const pkv_decode_params* P, int sm_count, pkv_plan* out) {
+// `solo` (optional) receives whether the plan launches the variant for grids of at
+// most one CTA per SM.
+int plan_impl(const pkv_pool_layout* L, const pkv_decode_params* P, int sm_count, pkv_plan* out,
+              bool* solo = nullptr) {
   const int ch = chunk_rows_of(L->bits);
   const long long max_len = static_cast<long long>(P->max_blocks_per_seq) * L->block_size;
   long long part;
@@ -106,7 +109,13 @@ int plan_impl(const pkv_pool_layout* L, const pkv_decode_params* P, int sm_count
     max_parts = std::min<int>(max_parts, ceil_div(span, part) + 1);
   }
   const long long nq = static_cast<long long>(P->num_q_heads / L->num_kv_heads) * P->n_query;
-  const PartialInfo info = partial_info(L->bits, L->head_dim, static_cast<int>(nq));
+  // A grid of at most one CTA per SM takes the variant with more warps and stages
+  // per CTA, where there is one for this shape.
+  const long long sms = sm_count > 0 ? sm_count : 1;
+  const long long ctas = static_cast<long long>(P->num_seqs) * L->num_kv_heads * max_parts;
+  const bool use_solo = ctas <= sms && partial_info(L->bits, L->head_dim, static_cast<int>(nq), true).exists;
+  if (solo) *solo = use_solo;
+  const PartialInfo info = partial_info(L->bits, L->head_dim, static_cast<int>(nq), use_solo);
   out->partition_tokens = static_cast<int32_t>(part);
   out->max_partitions = max_parts;
   out->chunk_rows = info.chunk_rows;
@@ -117,11 +126,12 @@ int plan_impl(const pkv_pool_layout* L, const pkv_decode_params* P, int sm_count
   // Merge inside a thread-block cluster when a (sequence, KV head) has 2..16
   // partitions and the grid is at most one wave: the CTAs of a cluster are then
   // resident together anyway, and the merge needs no workspace and no second launch.
-  // A cluster of up to 16 CTAs fits 8 SMs at two CTAs per SM (one per SM up to 8).
-  const long long ctas = static_cast<long long>(P->num_seqs) * L->num_kv_heads * max_parts;
-  const bool two_per_sm = info.smem_bytes <= 114 * 1024;
-  out->merge_in_cluster = max_parts >= 2 && max_parts <= (two_per_sm ? 16 : 8) &&
-                          ctas <= static_cast<long long>(sm_count > 0 ? sm_count : 1) * (two_per_sm ? 2 : 1);
+  // A cluster of up to 16 CTAs fits 8 SMs at two CTAs per SM; at one CTA per SM it
+  // takes 16 SMs of one GPC (GB300 GPCs hold more), which the one-CTA-per-SM variant
+  // relies on, while the four-warp variant with large stages keeps to 8.
+  const bool two_per_sm = !use_solo && info.smem_bytes <= 114 * 1024;
+  out->merge_in_cluster = max_parts >= 2 && max_parts <= (two_per_sm || use_solo ? 16 : 8) &&
+                          ctas <= sms * (two_per_sm ? 2 : 1);
   if (max_parts > 1 && !out->merge_in_cluster) {
     const size_t slots = static_cast<size_t>(P->num_seqs) * P->num_q_heads * P->n_query * max_parts;
     const size_t o_bytes = (slots * L->head_dim * sizeof(float) + 255) / 256 * 256;
@@ -298,7 +308,8 @@ int enqueue_decode(const pkv_pool_layout* layout, const pkv_decode_params* param
   rc = device_sm_count(&sms, &dev);
   if (rc) return rc;
   pkv_plan plan;
-  rc = plan_impl(layout, params, sms, &plan);
+  bool solo = false;
+  rc = plan_impl(layout, params, sms, &plan, &solo);
   if (rc) return rc;
   const int mode = plan.max_partitions == 1 ? pkv::kModeSingle
                    : plan.merge_in_cluster   ? pkv::kModeCluster
@@ -308,7 +319,7 @@ int enqueue_decode(const pkv_pool_layout* layout, const pkv_decode_params* param
 
   const int D = layout->head_dim, HK = layout->num_kv_heads;
   const int nq = (params->num_q_heads / HK) * params->n_query;
-  const PartialInfo info = partial_info(layout->bits, D, nq);
+  const PartialInfo info = partial_info(layout->bits, D, nq, solo);
   const long long rows = static_cast<long long>(layout->num_blocks) * HK * layout->block_size;
   const int elem = info.tensor_elem_bytes;
   const long long row_elems = quant ? static_cast<long long>(D) * layout->bits / 8 : D;
@@ -360,11 +371,11 @@ int enqueue_decode(const pkv_pool_layout* layout, const pkv_decode_params* param
   cudaError_t e = cudaSuccess;
   if (partial) {
     if (layout->bits == 16)
-      e = pkv::launch_partial_bf16(D, nq, p, tk, tv, grid, st, dev);
+      e = pkv::launch_partial_bf16(D, nq, solo, p, tk, tv, grid, st, dev);
     else if (layout->bits == 4)
-      e = pkv::launch_partial_u4(D, nq, p, tk, tv, grid, st, dev);
+      e = pkv::launch_partial_u4(D, nq, solo, p, tk, tv, grid, st, dev);
     else
-      e = pkv::launch_partial_u8(D, nq, p, tk, tv, grid, st, dev);
+      e = pkv::launch_partial_u8(D, nq, solo, p, tk, tv, grid, st, dev);
     if (e != cudaSuccess) return cuda_fail("partial kernel launch", e);
   }
 

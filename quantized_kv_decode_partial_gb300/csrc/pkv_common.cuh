@@ -62,6 +62,7 @@ constexpr int kModeSingle = 0;     // one partition: the CTA writes bf16 output
 constexpr int kModeWorkspace = 1;  // partition states go to the workspace; the merge kernel follows
 constexpr int kModeCluster = 2;    // the partitions of a (sequence, KV head) form one thread-block
                                    // cluster and merge through distributed shared memory
+constexpr int kMaxClusterParts = 16;  // largest cluster (non-portable size)
 
 struct MergeParams {
   const float* ws_o;
@@ -194,6 +195,11 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   uint64_t policy;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
   return policy;
+}
+
+// Fetches a TMA descriptor (a __grid_constant__ kernel parameter) ahead of its first use.
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
 // 2-D tiled TMA load of one box into shared memory, completing on `bar`.

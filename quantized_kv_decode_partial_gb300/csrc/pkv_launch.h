@@ -19,16 +19,17 @@ struct PartialInfo {
   int tensor_elem_bytes;  // element size of the pool tensor maps (2 bf16, 1 affine codes)
 };
 
-// Partial-kernel instantiation for `nq` query rows per KV head.
-PartialInfo partial_info_bf16(int head_dim, int nq);
-PartialInfo partial_info_u4(int head_dim, int nq);
-PartialInfo partial_info_u8(int head_dim, int nq);
+// Partial-kernel instantiation for `nq` query rows per KV head; `solo` selects the
+// variant for grids of at most one CTA per SM (exists = false where there is none).
+PartialInfo partial_info_bf16(int head_dim, int nq, bool solo);
+PartialInfo partial_info_u4(int head_dim, int nq, bool solo);
+PartialInfo partial_info_u8(int head_dim, int nq, bool solo);
 
-cudaError_t launch_partial_bf16(int head_dim, int nq, const PartialParams& p, const CUtensorMap& tk,
+cudaError_t launch_partial_bf16(int head_dim, int nq, bool solo, const PartialParams& p, const CUtensorMap& tk,
                                 const CUtensorMap& tv, dim3 grid, cudaStream_t stream, int device);
-cudaError_t launch_partial_u4(int head_dim, int nq, const PartialParams& p, const CUtensorMap& tk,
+cudaError_t launch_partial_u4(int head_dim, int nq, bool solo, const PartialParams& p, const CUtensorMap& tk,
                               const CUtensorMap& tv, dim3 grid, cudaStream_t stream, int device);
-cudaError_t launch_partial_u8(int head_dim, int nq, const PartialParams& p, const CUtensorMap& tk,
+cudaError_t launch_partial_u8(int head_dim, int nq, bool solo, const PartialParams& p, const CUtensorMap& tk,
                               const CUtensorMap& tv, dim3 grid, cudaStream_t stream, int device);
 
 cudaError_t launch_merge(const MergeParams& p, int rows, cudaStream_t stream);

@@ -4,22 +4,34 @@
 
 namespace pkv {
 
-// One CTA per output row (sequence, query head, query index); each thread owns
-// four consecutive head dims. The partition states hold the running maximum in
-// log2 units, the normaliser and the unnormalised output; partitions whose
-// maximum is -inf saw no visible key and are skipped (kvq4-decode.ts and
-// multi-query.ts merge kernels). Output = sum_p 2^(m_p-M) o_p / sum_p 2^(m_p-M) l_p.
-__global__ void __launch_bounds__(64) pkv_merge_kernel(const __grid_constant__ MergeParams p) {
+// One CTA per output row (sequence, query head, query index). The partition states
+// hold the running maximum in log2 units, the normaliser and the unnormalised
+// output; partitions whose maximum is -inf saw no visible key and are skipped
+// (kvq4-decode.ts and multi-query.ts merge kernels).
+// Output = sum_p 2^(m_p-M) o_p / sum_p 2^(m_p-M) l_p.
+// The CTA's threads form kMergeGroups groups of D/4 threads; a thread owns four
+// consecutive head dims and every kMergeGroups-th partition, with four partitions'
+// loads in flight at a time, and the groups' sums are added in shared memory.
+constexpr int kMergeThreads = 256;
+constexpr int kMergeUnroll = 4;
+
+__global__ void __launch_bounds__(kMergeThreads) pkv_merge_kernel(const __grid_constant__ MergeParams p) {
+  __shared__ float red_m[kMergeThreads];
+  __shared__ float4 red_o[kMergeThreads];
+  __shared__ float red_l[kMergeThreads];
   const int row = blockIdx.x;
-  const int d = threadIdx.x * 4;
+  const int lanes = p.head_dim / 4;         // threads per group
+  const int groups = kMergeThreads / lanes;  // 4 (D=256), 8 (D=128), 16 (D=64)
+  const int grp = threadIdx.x / lanes, d = (threadIdx.x % lanes) * 4;
   wait_for_prerequisite_grids();  // launched early behind the partial pass; its states are ready after this
-  if (d >= p.head_dim) return;
   const int b = row / p.rows_per_seq;
   const int len = p.seq_lens[b];
   __nv_bfloat162* out = reinterpret_cast<__nv_bfloat162*>(p.out + static_cast<size_t>(row) * p.head_dim + d);
   if (len < p.n_query || len > p.max_len) {  // flagged by the partial pass
-    out[0] = __floats2bfloat162_rn(0.f, 0.f);
-    out[1] = __floats2bfloat162_rn(0.f, 0.f);
+    if (grp == 0) {
+      out[0] = __floats2bfloat162_rn(0.f, 0.f);
+      out[1] = __floats2bfloat162_rn(0.f, 0.f);
+    }
     return;
   }
   // Workspace slot i holds partition first + i: with a sliding window the partial pass
@@ -29,25 +41,61 @@ __global__ void __launch_bounds__(64) pkv_merge_kernel(const __grid_constant__ M
   const float2* ml = reinterpret_cast<const float2*>(p.ws_ml) + static_cast<size_t>(row) * p.max_partitions;
   const float4* ob = reinterpret_cast<const float4*>(p.ws_o + static_cast<size_t>(row) * p.max_partitions * p.head_dim + d);
   const int ostride = p.head_dim / 4;
+
   float M = -INFINITY;
-  for (int i = 0; i < np; ++i) M = fmaxf(M, ml[i].x);
-  float den = 0.f, n0 = 0.f, n1 = 0.f, n2 = 0.f, n3 = 0.f;
+  for (int i0 = grp; i0 < np; i0 += groups * kMergeUnroll) {
+    float mu[kMergeUnroll];
+#pragma unroll
+    for (int u = 0; u < kMergeUnroll; ++u) {
+      const int i = i0 + u * groups;
+      mu[u] = i < np ? ml[i].x : -INFINITY;
+    }
+#pragma unroll
+    for (int u = 0; u < kMergeUnroll; ++u) M = fmaxf(M, mu[u]);
+  }
+  red_m[threadIdx.x] = M;
+  __syncthreads();
+  for (int g = 0; g < groups; ++g) M = fmaxf(M, red_m[g * lanes]);  // one value per group (its first thread's)
+
+  float den = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   if (M != -INFINITY) {
-    for (int i = 0; i < np; ++i) {
-      const float2 s = ml[i];
-      if (s.x == -INFINITY) continue;
-      const float w = fast_exp2(s.x - M);
-      const float4 v = ob[static_cast<size_t>(i) * ostride];
-      den = fmaf(w, s.y, den);
-      n0 = fmaf(w, v.x, n0);
-      n1 = fmaf(w, v.y, n1);
-      n2 = fmaf(w, v.z, n2);
-      n3 = fmaf(w, v.w, n3);
+    for (int i0 = grp; i0 < np; i0 += groups * kMergeUnroll) {
+      float2 s[kMergeUnroll];
+      float4 v[kMergeUnroll];
+#pragma unroll
+      for (int u = 0; u < kMergeUnroll; ++u) {
+        const int i = i0 + u * groups;
+        s[u] = i < np ? ml[i] : make_float2(-INFINITY, 0.f);
+        v[u] = i < np ? ob[static_cast<size_t>(i) * ostride] : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < kMergeUnroll; ++u) {
+        if (s[u].x == -INFINITY) continue;
+        const float w = fast_exp2(s[u].x - M);
+        den = fmaf(w, s[u].y, den);
+        acc.x = fmaf(w, v[u].x, acc.x);
+        acc.y = fmaf(w, v[u].y, acc.y);
+        acc.z = fmaf(w, v[u].z, acc.z);
+        acc.w = fmaf(w, v[u].w, acc.w);
+      }
     }
   }
+  red_o[threadIdx.x] = acc;
+  red_l[threadIdx.x] = den;
+  __syncthreads();
+  if (grp != 0) return;
+  for (int g = 1; g < groups; ++g) {
+    const float4 o = red_o[g * lanes + threadIdx.x];
+    den += red_l[g * lanes + threadIdx.x];
+    acc.x += o.x;
+    acc.y += o.y;
+    acc.z += o.z;
+    acc.w += o.w;
+  }
   if (den > 0.f) {
-    out[0] = __floats2bfloat162_rn(n0 / den, n1 / den);
-    out[1] = __floats2bfloat162_rn(n2 / den, n3 / den);
+    out[0] = __floats2bfloat162_rn(acc.x / den, acc.y / den);
+    out[1] = __floats2bfloat162_rn(acc.z / den, acc.w / den);
   } else {
     out[0] = __floats2bfloat162_rn(0.f, 0.f);
     out[1] = __floats2bfloat162_rn(0.f, 0.f);
@@ -57,7 +105,7 @@ __global__ void __launch_bounds__(64) pkv_merge_kernel(const __grid_constant__ M
 cudaError_t launch_merge(const MergeParams& p, int rows, cudaStream_t stream) {
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(rows);
-  cfg.blockDim = dim3(p.head_dim / 4 < 32 ? 32 : p.head_dim / 4);
+  cfg.blockDim = dim3(kMergeThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];

@@ -10,7 +10,8 @@
 // softmax itself and writes bf16 output.
 //
 // Design (GB300):
-//  * Four warps per CTA; warp w takes chunks w, w+4, w+8, ... of the partition
+//  * Four warps per CTA (eight for grids of at most one CTA per SM); warp w takes
+//    chunks w, w+4, w+8, ... of the partition
 //    (16 rows for bf16 pages, 32 or 16 for affine pages) and runs its own
 //    pipeline: lane 0 issues the copies of its chunk `kStagesPerWarp` ahead into a
 //    private ring of shared-memory stages guarded by mbarriers, so no warp waits
@@ -49,7 +50,11 @@
 
 namespace pkv {
 
-template <int BITS, int D, int NT, int WQ>
+// SOLO: the variant for grids of at most one CTA per SM. Such a CTA has the SM to
+// itself, so it takes 8 warps (two per scheduler, so one warp's dependent chain
+// hides behind the other's) when two stages per warp fit in shared memory, and as
+// many stages per warp (up to 4) as fit.
+template <int BITS, int D, int NT, int WQ, bool SOLO>
 struct PartialCfg {
   static constexpr bool kQuant = BITS != 16;
   static constexpr int kElemBytes = kQuant ? 1 : 2;                // tensor-map element size
@@ -64,12 +69,15 @@ struct PartialCfg {
   static constexpr int kSbBytes = kQuant ? kCh * kGroups * 2 : 0;  // one scale or bias plane
   static constexpr int kTxBytes = 2 * kPlaneBytes + 4 * kSbBytes;
   static constexpr int kStageBytes = (kTxBytes + 1023) / 1024 * 1024;
-  static constexpr int kWarps = 4;                                   // every warp computes
+  static constexpr int kBarrierBytes = SOLO ? 512 : 256;
+  static constexpr int kSoloBudget = 227 * 1024 - kBarrierBytes - 1024;  // stage ring of a CTA alone on its SM
+  static constexpr int kWarps = (SOLO && 8 * 2 * kStageBytes <= kSoloBudget) ? 8 : 4;  // every warp computes
   static constexpr int kThreads = kWarps * 32;
   // The warps form kWP page groups of WQ warps. A page group takes every kWP-th chunk;
   // its WQ warps read each of its chunks, each for its own 8*NT query rows.
   static constexpr int kWP = kWarps / WQ;
-  static constexpr int kStagesPerWarp = kStageBytes <= 9 * 1024 ? 3 : 2;
+  static constexpr int kSoloStages = kSoloBudget / (kWarps * kStageBytes);
+  static constexpr int kStagesPerWarp = SOLO ? (kSoloStages < 4 ? kSoloStages : 4) : (kStageBytes <= 9 * 1024 ? 3 : 2);
   static constexpr int kStagesPerGroup = kStagesPerWarp * WQ;  // each page group's private ring
   static constexpr int kNqp = 8 * NT;       // query rows per warp (padded)
   static constexpr int kNqAll = WQ * kNqp;  // query rows per CTA (padded)
@@ -80,7 +88,6 @@ struct PartialCfg {
   static constexpr int kCombineBytes = (kWP + 1) * kNqAll * (D + 2) * 4;
   static constexpr int kRingBytes = kWarps * kStagesPerWarp * kStageBytes;
   static constexpr int kDataBytes = kRingBytes > kCombineBytes ? kRingBytes : kCombineBytes;
-  static constexpr int kBarrierBytes = 256;
   static constexpr int kSmemBytes = kDataBytes + kBarrierBytes + 1024;  // + alignment slack
   static constexpr float kCodeUnit = 5.9604644775390625e-8f;  // 2^-24: value of fp16 bit pattern 1
 
@@ -89,6 +96,8 @@ struct PartialCfg {
   static_assert(kWarps * kStagesPerWarp * 12 + 4 <= kBarrierBytes, "barrier area");
   static_assert(!kQuant || D % 64 == 0, "affine head dims are whole 64-dim groups");
   static_assert(WQ == 1 || WQ == 2 || WQ == 4, "query groups of 1, 2 or 4 warps");
+  static_assert(kStagesPerWarp >= 2, "at least two stages per warp");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory of one CTA");
 };
 
 // Physical head dim held by row `half` (0: g, 1: g + 8) of O^T m-tile `mt`.
@@ -161,11 +170,11 @@ __device__ __forceinline__ void load_group_row(uint32_t addr, float (&v)[G]) {
   }
 }
 
-template <int BITS, int D, int NT, int WQ>
+template <int BITS, int D, int NT, int WQ, bool SOLO>
 __global__ void __maxnreg__(200)
     pkv_partial_kernel(const __grid_constant__ PartialParams p, const __grid_constant__ CUtensorMap tmap_k,
                        const __grid_constant__ CUtensorMap tmap_v) {
-  using C = PartialCfg<BITS, D, NT, WQ>;
+  using C = PartialCfg<BITS, D, NT, WQ, SOLO>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + C::kDataBytes);  // [warp][stage]
@@ -184,6 +193,14 @@ __global__ void __maxnreg__(200)
   const bool single = p.mode == kModeSingle;
   const bool in_cluster = p.mode == kModeCluster;
   const int len = p.seq_lens[b];
+  // Without a window the partition (and so this warp's first 32 chunks) does not
+  // depend on len: fetch their block-table entries while len is still in flight.
+  int tbl_pre = 0;
+  if (p.window == 0 && leader) {
+    const long long r = static_cast<long long>(slot) * p.partition_tokens + (pg + lane * C::kWP) * C::kCh;
+    const long long blk = r / p.block_size < p.max_blocks ? r / p.block_size : p.max_blocks - 1;
+    tbl_pre = __ldg(p.block_tables + static_cast<size_t>(b) * p.max_blocks + blk);
+  }
 
   if (len < N || len > p.max_blocks * p.block_size) {
     // Every CTA of this sequence sees the same length and leaves here (before any
@@ -222,6 +239,8 @@ __global__ void __maxnreg__(200)
   }
 
   if (threadIdx.x == 0) {
+    prefetch_tensormap(&tmap_k);  // the first copies need both descriptors
+    prefetch_tensormap(&tmap_v);
     for (int s = 0; s < C::kWarps * C::kStagesPerWarp; ++s) mbar_init(smem_addr(&full_bar[s]), 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -246,7 +265,8 @@ __global__ void __maxnreg__(200)
     const uint64_t policy = l2_evict_first_policy();
     auto chunk_row = [&](int i) { return t_first + (pg + i * C::kWP) * C::kCh; };  // first cache row of local chunk i
     // Physical blocks of the next 32 (and following 32) chunks to issue, one per lane.
-    int tbl_cur = leader && lane < my_chunks ? __ldg(table + chunk_row(lane) / p.block_size) : 0;
+    int tbl_cur = p.window == 0 ? tbl_pre
+                                : (leader && lane < my_chunks ? __ldg(table + chunk_row(lane) / p.block_size) : 0);
     int tbl_next = leader && 32 + lane < my_chunks ? __ldg(table + chunk_row(32 + lane) / p.block_size) : 0;
     int issued = 0;
 
@@ -785,16 +805,29 @@ __global__ void __maxnreg__(200)
     const int end = min(total, (slot + 1) * per);
     for (int idx = slot * per + threadIdx.x; idx < end; idx += C::kThreads) {
       const int r = idx / D, d = idx % D;
+      // every member's (m, l, o) for this output, all remote loads in flight together
+      float mj[kMaxClusterParts], lj[kMaxClusterParts], oj[kMaxClusterParts];
+#pragma unroll
+      for (int j = 0; j < kMaxClusterParts; ++j) {
+        mj[j] = -INFINITY;
+        lj[j] = oj[j] = 0.f;
+        if (j < cs) {
+          mj[j] = ld_cluster_f32(smem_addr(&st_m[r]), j);
+          lj[j] = ld_cluster_f32(smem_addr(&st_l[r]), j);
+          oj[j] = ld_cluster_f32(smem_addr(&st_o[r * D + d]), j);
+        }
+      }
       float M = -INFINITY;
-      for (int j = 0; j < cs; ++j) M = fmaxf(M, ld_cluster_f32(smem_addr(&st_m[r]), j));
+#pragma unroll
+      for (int j = 0; j < kMaxClusterParts; ++j) M = fmaxf(M, mj[j]);
       float L = 0.f, O = 0.f;
       if (M != -INFINITY) {
-        for (int j = 0; j < cs; ++j) {
-          const float mj = ld_cluster_f32(smem_addr(&st_m[r]), j);
-          if (mj == -INFINITY) continue;
-          const float wt = fast_exp2(mj - M);
-          L = fmaf(wt, ld_cluster_f32(smem_addr(&st_l[r]), j), L);
-          O = fmaf(wt, ld_cluster_f32(smem_addr(&st_o[r * D + d]), j), O);
+#pragma unroll
+        for (int j = 0; j < kMaxClusterParts; ++j) {
+          if (mj[j] == -INFINITY) continue;
+          const float wt = fast_exp2(mj[j] - M);
+          L = fmaf(wt, lj[j], L);
+          O = fmaf(wt, oj[j], O);
         }
       }
       p.out[(row0 + r) * D + d] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);

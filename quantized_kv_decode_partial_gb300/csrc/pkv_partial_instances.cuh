@@ -10,36 +10,36 @@
 namespace pkv {
 namespace {
 
-template <int BITS, int D, int NT, int WQ>
+template <int BITS, int D, int NT, int WQ, bool SOLO>
 PartialInfo info_of() {
-  using C = PartialCfg<BITS, D, NT, WQ>;
+  using C = PartialCfg<BITS, D, NT, WQ, SOLO>;
   return PartialInfo{true, C::kThreads, C::kSmemBytes, C::kCh, C::kRB, C::kElemBytes};
 }
 
 // Devices on which an instantiation's function attributes are set (bit per device < 64).
-template <int BITS, int D, int NT, int WQ>
+template <int BITS, int D, int NT, int WQ, bool SOLO>
 std::atomic<unsigned long long> g_configured{0};
 
-template <int BITS, int D, int NT, int WQ>
+template <int BITS, int D, int NT, int WQ, bool SOLO>
 cudaError_t configure_once(int device) {
-  using C = PartialCfg<BITS, D, NT, WQ>;
-  auto kern = pkv_partial_kernel<BITS, D, NT, WQ>;
+  using C = PartialCfg<BITS, D, NT, WQ, SOLO>;
+  auto kern = pkv_partial_kernel<BITS, D, NT, WQ, SOLO>;
   const unsigned long long bit = device >= 0 && device < 64 ? (1ull << device) : 0ull;
-  if (bit && (g_configured<BITS, D, NT, WQ>.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  if (bit && (g_configured<BITS, D, NT, WQ, SOLO>.load(std::memory_order_acquire) & bit)) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);  // clusters of up to 16
   if (e != cudaSuccess) return e;
-  if (bit) g_configured<BITS, D, NT, WQ>.fetch_or(bit, std::memory_order_acq_rel);
+  if (bit) g_configured<BITS, D, NT, WQ, SOLO>.fetch_or(bit, std::memory_order_acq_rel);
   return cudaSuccess;
 }
 
-template <int BITS, int D, int NT, int WQ>
+template <int BITS, int D, int NT, int WQ, bool SOLO>
 cudaError_t launch_of(const PartialParams& p, const CUtensorMap& tk, const CUtensorMap& tv, dim3 grid,
                       cudaStream_t stream, int device) {
-  using C = PartialCfg<BITS, D, NT, WQ>;
-  auto kern = pkv_partial_kernel<BITS, D, NT, WQ>;
-  cudaError_t e = configure_once<BITS, D, NT, WQ>(device);
+  using C = PartialCfg<BITS, D, NT, WQ, SOLO>;
+  auto kern = pkv_partial_kernel<BITS, D, NT, WQ, SOLO>;
+  cudaError_t e = configure_once<BITS, D, NT, WQ, SOLO>(device);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = grid;

@@ -71,9 +71,14 @@ def test_plan_for_workloads(lib, name):
         assert plan.max_partitions == table_parts
     if sp.partition_tokens > 0:
         assert plan.partition_tokens == sp.partition_tokens
-    # one wave of CTAs with 2..16 partitions merges inside a thread-block cluster
+    # grids of at most one CTA per SM take the variant with more warps and stages (4 query-row
+    # tiles of 8 at most); one wave of CTAs with 2..16 partitions merges inside a thread-block cluster
     ctas = sp.num_seqs * sp.num_kv_heads * plan.max_partitions
-    assert plan.merge_in_cluster == (2 <= plan.max_partitions <= 16 and ctas <= 2 * 152)
+    solo = ctas <= 152 and sp.rep * sp.n_query <= 8
+    assert (plan.smem_bytes > 114 * 1024) if solo else plan.threads_per_cta == 128
+    two_per_sm = not solo and plan.smem_bytes <= 114 * 1024
+    assert plan.merge_in_cluster == (2 <= plan.max_partitions <= (16 if two_per_sm or solo else 8)
+                                     and ctas <= (2 if two_per_sm else 1) * 152)
     if plan.max_partitions == 1 or plan.merge_in_cluster:
         assert plan.workspace_bytes == 0
     else:
@@ -87,9 +92,22 @@ def test_plan_for_workloads(lib, name):
             kv_row = 2 * (2 * sp.head_dim if sp.bits == 16 else sp.head_dim * sp.bits // 8 + sp.head_dim // 16)
             assert (ctas >= 8 * 152 or plan.partition_tokens == 256
                     or (ctas >= 2 * 152 and plan.partition_tokens // 2 < (512 << 10) // kv_row))
-    assert plan.threads_per_cta == 128 and 0 < plan.smem_bytes <= 227 * 1024
-    if not (sp.bits == 16 and sp.head_dim == 256):  # 16 KB stages of bf16 D=256 take one CTA per SM
+    assert plan.threads_per_cta in (128, 256) and 0 < plan.smem_bytes <= 227 * 1024
+    if not solo and not (sp.bits == 16 and sp.head_dim == 256):  # 16 KB stages of bf16 D=256: one CTA per SM
         assert plan.smem_bytes <= 114 * 1024  # two CTAs per SM
+
+
+@pytest.mark.parametrize("bits,head_dim,threads", [(16, 64, 256), (16, 128, 256), (16, 256, 128), (4, 128, 256),
+                                                   (4, 256, 256), (8, 128, 256), (8, 256, 256)])
+def test_small_grids_take_the_one_cta_per_sm_variant(lib, bits, head_dim, threads):
+    lay = B.PoolLayout(4096, 4, 32, head_dim, bits, 64)
+    small = B.make_plan(lay, B.DecodeParams(1, 16, 1, 256, 512, 0), sm_count=152)  # 4 heads x 16 parts
+    assert small.threads_per_cta == threads and 114 * 1024 < small.smem_bytes <= 227 * 1024
+    assert small.merge_in_cluster == 1 and small.workspace_bytes == 0
+    big = B.make_plan(lay, B.DecodeParams(3, 16, 1, 256, 512, 0), sm_count=152)  # 192 CTAs: more than one per SM
+    assert big.threads_per_cta == 128 and big.smem_bytes < small.smem_bytes
+    wide_q = B.make_plan(lay, B.DecodeParams(1, 16, 4, 256, 512, 0), sm_count=152)  # 16 query rows per KV head
+    assert wide_q.threads_per_cta == (256 if (bits, head_dim) == (16, 128) else 128)
 
 
 def test_single_sequence_plans_merge_in_a_cluster(lib):

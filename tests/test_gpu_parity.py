@@ -80,6 +80,30 @@ def test_small_cases_match_oracle(sp, parts):
         assert_close(out.double().cpu().numpy(), ref, f"{sp.name} partition={pt}")
 
 
+# The small cases above launch at most one CTA per SM for up to 8 query rows per KV head,
+# which takes the eight-warp variant; these grids of more than one CTA per SM take the
+# four-warp one for the same shapes.
+BIG_GRID = [(16, 64), (16, 128), (16, 256), (4, 128), (4, 256), (8, 128), (8, 256)]
+
+
+@pytest.mark.parametrize("bits,D", BIG_GRID, ids=[f"b{b}_d{d}" for b, d in BIG_GRID])
+def test_grids_of_several_ctas_per_sm_match_oracle(bits, D):
+    sp = spec(f"big_grid_{bits}_{D}", num_seqs=44, num_q_heads=16, num_kv_heads=4, head_dim=D, bits=bits,
+              block_size=16 if bits == 16 else 32, length_range=(1, 260))
+    case = make_case(sp)
+    ref = oracle_out(case)
+    dcase = case.to(DEV)
+    for pt in (max(case.lens_host) + 64, 32):
+        plan = B.make_plan(B.layout_for(case.k_pool, D, bits),
+                           B.DecodeParams(sp.num_seqs, 16, 1, case.block_tables.shape[1], pt))
+        assert plan.threads_per_cta == 128
+        err = torch.zeros(1, dtype=torch.int32, device=DEV)
+        out = run_gpu(dcase, partition_tokens=pt, error_flag=err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        assert_close(out.double().cpu().numpy(), ref, f"{sp.name} partition={pt}")
+
+
 @pytest.mark.parametrize("bits,parts", [(16, 16), (4, 16), (8, 2), (16, 9)])
 def test_cluster_merge_matches_oracle(bits, parts):
     # one sequence: the partitions of each KV head merge inside a thread-block cluster
