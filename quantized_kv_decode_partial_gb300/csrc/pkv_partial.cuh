@@ -264,30 +264,40 @@ __global__ void __maxnreg__(200)
     const int32_t* table = p.block_tables + static_cast<size_t>(b) * p.max_blocks;
     const uint64_t policy = l2_evict_first_policy();
     auto chunk_row = [&](int i) { return t_first + (pg + i * C::kWP) * C::kCh; };  // first cache row of local chunk i
-    // Physical blocks of the next 32 (and following 32) chunks to issue, one per lane.
-    int tbl_cur = p.window == 0 ? tbl_pre
-                                : (leader && lane < my_chunks ? __ldg(table + chunk_row(lane) / p.block_size) : 0);
-    int tbl_next = leader && 32 + lane < my_chunks ? __ldg(table + chunk_row(32 + lane) / p.block_size) : 0;
-    int issued = 0;
+    // TMA row coordinate of local chunk i in physical block ph (the block's rows of this
+    // KV head plus the chunk's offset in the block), or -1 for a bad block id. Each lane
+    // of the leader warp holds the coordinate of one of the next 32 chunks to issue,
+    // and the raw block ids of the 32 after those.
+    auto coord_of = [&](int ph, int i) {
+      return static_cast<unsigned>(ph) < static_cast<unsigned>(p.num_blocks)
+                 ? (ph * p.num_kv_heads + hk) * p.block_size + chunk_row(i) % p.block_size
+                 : -1;
+    };
+    int crd_cur = 0, tbl_next = 0;
+    if (leader) {
+      const int ph0 = p.window == 0 ? tbl_pre : (lane < my_chunks ? __ldg(table + chunk_row(lane) / p.block_size) : 0);
+      tbl_next = 32 + lane < my_chunks ? __ldg(table + chunk_row(32 + lane) / p.block_size) : 0;
+      crd_cur = coord_of(ph0, lane);
+    }
+    int issued = 0;  // chunks issued so far
 
-    auto issue_next = [&]() {  // the leader warp, warp-uniform; its lane 0 issues the copies
+    // Issues the next chunk into stage `is` (the one just consumed: with one stage per
+    // chunk in flight, chunk i always lands in stage i mod kStagesPerGroup).
+    auto issue_next = [&](int is) {  // the leader warp, warp-uniform
       if (issued >= my_chunks) return;
       if (issued > 0 && (issued & 31) == 0) {
-        tbl_cur = tbl_next;
+        crd_cur = coord_of(tbl_next, issued + lane);
         const int k = issued + 32 + lane;
         tbl_next = k < my_chunks ? __ldg(table + chunk_row(k) / p.block_size) : 0;
       }
-      const int ph = __shfl_sync(0xffffffffu, tbl_cur, issued & 31);
-      const int s = issued % C::kStagesPerGroup;
+      const int row = __shfl_sync(0xffffffffu, crd_cur, issued & 31);
       if (lane == 0) {
-        const bool ok = static_cast<unsigned>(ph) < static_cast<unsigned>(p.num_blocks);
-        my_ok[s] = ok ? 1 : 0;
-        const uint32_t fb = smem_addr(&my_full[s]);
-        if (ok) {
-          fence_proxy_async_smem();  // this warp's reads of the stage precede the copy into it
+        const uint32_t fb = smem_addr(&my_full[is]);
+        my_ok[is] = row >= 0 ? 1 : 0;
+        if (row >= 0) {
+          fence_proxy_async_smem();  // this warp's reads of the stage precede the copies into it
           mbar_arrive_expect_tx(fb, C::kTxBytes);
-          const int row = (ph * p.num_kv_heads + hk) * p.block_size + chunk_row(issued) % p.block_size;
-          const uint32_t st = smem_addr(my_ring + s * C::kStageBytes);
+          const uint32_t st = smem_addr(my_ring + is * C::kStageBytes);
 #pragma unroll
           for (int bx = 0; bx < C::kBoxes; ++bx) {
             const int x = bx * (C::kRB / C::kElemBytes);
@@ -312,15 +322,17 @@ __global__ void __maxnreg__(200)
 
 #pragma unroll 1
     for (int s = 0; s < C::kStagesPerGroup; ++s)
-      if (leader) issue_next();
+      if (leader) issue_next(s);
 
     // B fragments of Q^T for every k-step, rows r = 8*nt + g of this KV head: bf16 as
     // stored for bf16 pages; for affine pages fp16, after an exact power-of-two
     // prescale per row that puts the row's largest |q| in [2^14, 2^15).
     uint32_t qf[C::kKs][NT][2];
     float colscale[NT][2];  // factor from accumulator to base-2 score, per query column 2t, 2t+1
-    float qsum[C::kQuant ? C::kGroups : 1][NT][2];  // affine: 2^-24 * sum of prescaled q over each group
+    // affine: B fragment (k 0-7) of the K-bias MMA, per n-tile (k 8-15 are zero)
+    uint32_t qsb[C::kQuant ? NT : 1];
     {
+      float qsum[C::kQuant ? C::kGroups : 1][NT][2];  // affine: 2^-24 * sum of prescaled q over each group
       const uint16_t* qrows = reinterpret_cast<const uint16_t*>(p.q) + row0 * D;
       float qv[C::kKs][NT][4];
 #pragma unroll
@@ -395,6 +407,33 @@ __global__ void __maxnreg__(200)
             const int k = __shfl_sync(0xffffffffu, kexp[nt], (2 * t + e2) * 4);
             colscale[nt][e2] = p.score_scale * __uint_as_float(static_cast<uint32_t>(127 + 24 - k) << 23);
           }
+        // The bias part of the scores, sum_g b_g * sum_{d in g} q_d, runs as one bf16 MMA per
+        // 16-key tile: A holds each key's G biases twice (k slots 0..G-1 and G..2G-1), B
+        // holds query column g's group sums split into bf16 high parts (slots 0..G-1) and
+        // the bf16 rounding of the remainders (slots G..2G-1), so the product keeps about
+        // 16 significant bits of each sum. The lane with t = g/2 holds column g's sums.
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          float cq[C::kGroups];
+#pragma unroll
+          for (int j = 0; j < C::kGroups; ++j) {
+            const float v0 = __shfl_sync(0xffffffffu, qsum[j][nt][0], g >> 1);
+            const float v1 = __shfl_sync(0xffffffffu, qsum[j][nt][1], g >> 1);
+            cq[j] = (g & 1) ? v1 : v0;
+          }
+          float slot_val[2] = {0.f, 0.f};
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int slot = 2 * t + e;
+#pragma unroll
+            for (int j = 0; j < C::kGroups; ++j) {
+              const float hi = __bfloat162float(__float2bfloat16_rn(cq[j]));
+              const float lo = __bfloat162float(__float2bfloat16_rn(cq[j] - hi));
+              slot_val[e] = slot == j ? hi : slot == C::kGroups + j ? lo : slot_val[e];
+            }
+          }
+          qsb[nt] = pack_bf16x2(slot_val[0], slot_val[1]);  // exact: both are bf16 values
+        }
       }
     }
 
@@ -423,11 +462,11 @@ __global__ void __maxnreg__(200)
 
     int done = 0;  // local chunks consumed
     for (; done < my_chunks; ++done) {
-      const int s = done % C::kStagesPerGroup;
-      const bool landed = mbar_wait_warp(smem_addr(&my_full[s]), (done / C::kStagesPerGroup) & 1, abort_flag,
+      const int cs = done % C::kStagesPerGroup;  // its stage
+      const bool landed = mbar_wait_warp(smem_addr(&my_full[cs]), (done / C::kStagesPerGroup) & 1, abort_flag,
                                          p.error_flag);
-      if (landed && my_ok[s]) {
-        uint8_t* stage = my_ring + s * C::kStageBytes;
+      if (landed && my_ok[cs]) {
+        uint8_t* stage = my_ring + cs * C::kStageBytes;
         const uint32_t kpl = smem_addr(stage);
         const uint32_t vpl = kpl + C::kPlaneBytes;
         const uint32_t sbq = kpl + 2 * C::kPlaneBytes;  // scale/bias planes (affine pages)
@@ -454,12 +493,23 @@ __global__ void __maxnreg__(200)
               for (int nt = 0; nt < NT; ++nt) mma_bf16(sacc[nt], a[0], a[1], a[2], a[3], qf[kk][nt][0], qf[kk][nt][1]);
             }
           } else {
-            // scales and biases of keys g and g + 8 of this tile, all groups
-            float ks0[C::kGroups], ks1[C::kGroups], kb0[C::kGroups], kb1[C::kGroups];
+            // scales of keys g and g + 8 of this tile, all groups
+            float ks0[C::kGroups], ks1[C::kGroups];
             load_group_row<C::kGroups>(sbq + (tile * 16 + g) * C::kGroups * 2, ks0);
             load_group_row<C::kGroups>(sbq + (tile * 16 + g + 8) * C::kGroups * 2, ks1);
-            load_group_row<C::kGroups>(sbq + C::kSbBytes + (tile * 16 + g) * C::kGroups * 2, kb0);
-            load_group_row<C::kGroups>(sbq + C::kSbBytes + (tile * 16 + g + 8) * C::kGroups * 2, kb1);
+            {
+              // bias MMA: this lane's A words are the biases of k slots 2t, 2t+1 (groups
+              // 2t mod G, 2t mod G + 1) of keys g and g + 8
+              uint32_t ba0 = 0u, ba1 = 0u;
+              const uint32_t kb = sbq + C::kSbBytes + (tile * 16 + g) * C::kGroups * 2;
+              if (C::kGroups == 4 || t < 2) {
+                const uint32_t off = C::kGroups == 4 ? (t & 1) * 4 : 0;
+                ba0 = ld_shared_u32(kb + off);
+                ba1 = ld_shared_u32(kb + 8 * C::kGroups * 2 + off);
+              }
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt) mma_bf16(sacc[nt], ba0, ba1, 0u, 0u, qsb[nt], 0u);
+            }
 #pragma unroll
             for (int grp = 0; grp < C::kGroups; ++grp) {
               float sg[NT][4];
@@ -501,13 +551,13 @@ __global__ void __maxnreg__(200)
                   }
                 }
               }
-              // fold the affine terms of group grp for keys g and g + 8 of this tile
+              // fold the scale of group grp for keys g and g + 8 of this tile
 #pragma unroll
               for (int nt = 0; nt < NT; ++nt) {
-                sacc[nt][0] = fmaf(ks0[grp], sg[nt][0], fmaf(kb0[grp], qsum[grp][nt][0], sacc[nt][0]));
-                sacc[nt][1] = fmaf(ks0[grp], sg[nt][1], fmaf(kb0[grp], qsum[grp][nt][1], sacc[nt][1]));
-                sacc[nt][2] = fmaf(ks1[grp], sg[nt][2], fmaf(kb1[grp], qsum[grp][nt][0], sacc[nt][2]));
-                sacc[nt][3] = fmaf(ks1[grp], sg[nt][3], fmaf(kb1[grp], qsum[grp][nt][1], sacc[nt][3]));
+                sacc[nt][0] = fmaf(ks0[grp], sg[nt][0], sacc[nt][0]);
+                sacc[nt][1] = fmaf(ks0[grp], sg[nt][1], sacc[nt][1]);
+                sacc[nt][2] = fmaf(ks1[grp], sg[nt][2], sacc[nt][2]);
+                sacc[nt][3] = fmaf(ks1[grp], sg[nt][3], sacc[nt][3]);
               }
             }
           }
@@ -675,11 +725,11 @@ __global__ void __maxnreg__(200)
       if constexpr (WQ == 1) {
         if (!landed) break;
         __syncwarp();  // every lane is done with the stage before it is refilled
-        issue_next();
+        issue_next(cs);
       } else {
         // every warp of the group is done with the stage; one give-up decision for all
         if (group_barrier_any(1 + pg, WQ * 32, !landed)) break;
-        if (leader) issue_next();
+        if (leader) issue_next(cs);
       }
     }
     if (leader && done < issued && lane == 0) {

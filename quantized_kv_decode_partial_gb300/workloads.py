@@ -9,10 +9,13 @@ Layouts follow the paged KV pool of the mlx-bun pages
 ("@mlx-bun/inference 0.0.0-stage -> 1.0.0", state/paged/cache.ts, class
 ``BlockPool``: every plane is ``[numBlocks, H_kv, blockSize, width]``):
 
-* bf16 pages: ``k_pool``/``v_pool`` bf16 ``[NB, HK, BS, D]``;
+* bf16 pages: ``k_pool`` bf16 ``[NB, HK, BS, D]``, ``v_pool`` ``[NB, HK, BS, Dv]``;
 * affine pages: packed codes as int32 bit patterns of uint32 words
   ``[NB, HK, BS, D*bits/32]`` plus bf16 ``scales``/``biases``
-  ``[NB, HK, BS, D/group]`` for each of K and V.
+  ``[NB, HK, BS, D/group]`` for K, and the same with Dv for V.
+
+D is the key (and query) head dim, Dv the value head dim (the pages'
+``headDim`` and ``vHeadDim``; equal unless a spec sets ``v_head_dim``).
 
 Uniform codes packed 8 (4-bit) or 4 (8-bit) per word are exactly uniform
 random 32-bit words, so the generator draws words directly and never packs.
@@ -55,10 +58,15 @@ class DecodeSpec:
     window: int = 0  # sliding window in rows (0 = none)
     seed: int = 0
     description: str = ""
+    v_head_dim: int = 0  # value head dim; 0 = head_dim
 
     @property
     def rep(self) -> int:
         return self.num_q_heads // self.num_kv_heads
+
+    @property
+    def dv(self) -> int:
+        return self.v_head_dim or self.head_dim
 
 
 @dataclass
@@ -198,31 +206,32 @@ def make_case(spec: DecodeSpec, device="cpu", seed: Optional[int] = None, poison
     used = perm[:needed]
 
     gen = torch.Generator(device=device).manual_seed(seed)
+    DV = spec.dv
     q = torch.randn((B, HQ, N, D), generator=gen, device=device, dtype=torch.float32).to(torch.bfloat16)
     ks = kb = vs = vb = None
     if spec.bits == 16:
         k_pool = torch.randn((num_blocks, HK, BS, D), generator=gen, device=device, dtype=torch.bfloat16)
-        v_pool = torch.randn((num_blocks, HK, BS, D), generator=gen, device=device, dtype=torch.bfloat16)
+        v_pool = torch.randn((num_blocks, HK, BS, DV), generator=gen, device=device, dtype=torch.bfloat16)
     else:
-        assert spec.bits in (4, 8) and D % spec.group_size == 0
-        words = D * spec.bits // 32
-        G = D // spec.group_size
+        assert spec.bits in (4, 8) and D % spec.group_size == 0 and DV % spec.group_size == 0
 
-        def codes():
-            w = torch.randint(0, 1 << 32, (num_blocks, HK, BS, words), generator=gen, device=device,
-                              dtype=torch.int64)
+        def codes(dim):
+            w = torch.randint(0, 1 << 32, (num_blocks, HK, BS, dim * spec.bits // 32), generator=gen,
+                              device=device, dtype=torch.int64)
             return w.to(torch.int32)
 
-        def scales():
-            s = torch.randn((num_blocks, HK, BS, G), generator=gen, device=device, dtype=torch.float32)
+        def scales(dim):
+            s = torch.randn((num_blocks, HK, BS, dim // spec.group_size), generator=gen, device=device,
+                            dtype=torch.float32)
             return (s.abs_() * 0.05 + 0.01).to(torch.bfloat16)
 
-        def biases():
-            s = torch.randn((num_blocks, HK, BS, G), generator=gen, device=device, dtype=torch.float32)
+        def biases(dim):
+            s = torch.randn((num_blocks, HK, BS, dim // spec.group_size), generator=gen, device=device,
+                            dtype=torch.float32)
             return (s * 0.2).to(torch.bfloat16)
 
-        k_pool, ks, kb = codes(), scales(), biases()
-        v_pool, vs, vb = codes(), scales(), biases()
+        k_pool, ks, kb = codes(D), scales(D), biases(D)
+        v_pool, vs, vb = codes(DV), scales(DV), biases(DV)
 
     if poison:
         value_planes = [k_pool, v_pool] if spec.bits == 16 else [ks, kb, vs, vb]
@@ -247,9 +256,10 @@ def make_case(spec: DecodeSpec, device="cpu", seed: Optional[int] = None, poison
     )
 
 
-def row_bytes(spec: DecodeSpec) -> int:
-    """Bytes of one K (or V) row as stored: bf16 row, or codes + bf16 scale and bias."""
-    D = spec.head_dim
+def row_bytes(spec: DecodeSpec, dim: Optional[int] = None) -> int:
+    """Bytes of one stored row of head dim ``dim`` (default the key head dim): a bf16
+    row, or codes + bf16 scale and bias."""
+    D = spec.head_dim if dim is None else dim
     if spec.bits == 16:
         return 2 * D
     return D * spec.bits // 8 + (D // spec.group_size) * 4
@@ -259,4 +269,4 @@ def required_kv_bytes(spec: DecodeSpec, lens) -> int:
     """K/V bytes a decode step must read: every visible cached row once per KV head, K and V.
     With a sliding window W the N queries of a sequence together see its last W + N - 1 rows."""
     rows = sum(min(l, spec.window + spec.n_query - 1) if spec.window > 0 else l for l in lens)
-    return int(rows) * spec.num_kv_heads * 2 * row_bytes(spec)
+    return int(rows) * spec.num_kv_heads * (row_bytes(spec) + row_bytes(spec, spec.dv))

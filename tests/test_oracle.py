@@ -102,6 +102,10 @@ TINY = [
     tiny("u4_bs16_g16", bits=4, head_dim=32, group_size=16, block_size=16, length_range=(5, 40), seed=15),
     tiny("bf16_window7_n3", n_query=3, window=7, length_range=(3, 40), seed=16),
     tiny("u8_window1_n2", bits=8, n_query=2, window=1, length_range=(2, 30), seed=17),
+    # value head dim different from the key head dim (the pages' vHeadDim)
+    tiny("bf16_dk16_dv8_n2", v_head_dim=8, n_query=2, length_range=(2, 40), seed=18),
+    tiny("u4_dk16_dv32", bits=4, v_head_dim=32, seed=19),
+    tiny("u8_dk32_dv16_window5", bits=8, head_dim=32, v_head_dim=16, group_size=16, window=5, seed=20),
 ]
 
 
@@ -193,9 +197,9 @@ def test_two_key_closed_form():
     assert np.allclose(oracle.attend(q, K, V, 1.0), expect, rtol=0, atol=1e-15)
 
 
-@pytest.mark.parametrize("bits", [16, 4])
-def test_one_token_cache_returns_its_v_row(bits):
-    spec = tiny("one", num_seqs=1, lengths=(1,), length_range=None, bits=bits, seed=21)
+@pytest.mark.parametrize("bits,dv", [(16, 0), (4, 0), (16, 24), (8, 8)])
+def test_one_token_cache_returns_its_v_row(bits, dv):
+    spec = tiny("one", num_seqs=1, lengths=(1,), length_range=None, bits=bits, seed=21, v_head_dim=dv)
     case = make_case(spec)
     args, kw = np_inputs(case)
     out = oracle.paged_decode_attention(*args, **kw)
@@ -326,9 +330,13 @@ def _pins_fail(monkeypatch, name, mutant):
     for spec in TINY:
         case = make_case(spec)
         args, kw = np_inputs(case)
-        got = opd.paged_decode_attention(*args, window=spec.window, **kw)
+        try:
+            got = opd.paged_decode_attention(*args, window=spec.window, **kw)
+        except (ValueError, IndexError):  # e.g. K and V planes of different head dims exchanged
+            failures += 1
+            continue
         ref = dense_reference(case)
-        if not (np.isfinite(got).all() and np.max(np.abs(got - ref)) < 1e-12):
+        if got.shape != ref.shape or not (np.isfinite(got).all() and np.max(np.abs(got - ref)) < 1e-12):
             failures += 1
     return failures
 
