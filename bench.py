@@ -52,6 +52,9 @@ def parse_args(argv=None):
                     help="profiling mode: keep only the first N sequences of the workload")
     ap.add_argument("--partition-tokens", type=int, default=-2,
                     help="rows per partition instead of the workload's choice (0: the library's plan)")
+    ap.add_argument("--step", choices=["decode", "fused"], default="decode",
+                    help="decode: the decode call; fused: the decode step with its write "
+                         "(pkv_paged_decode_append_attention: append the N new K/V rows, then attend)")
     return ap.parse_args(argv)
 
 
@@ -252,7 +255,7 @@ def run_ours(args):
     import torch.distributed as dist
 
     from quantized_kv_decode_partial_gb300 import (DecodeParams, load_library, make_plan, paged_decode_attention,
-                                                   paged_decode_passes)
+                                                   paged_decode_append_attention, paged_decode_passes)
     from quantized_kv_decode_partial_gb300 import build as pkv_build
     from quantized_kv_decode_partial_gb300.binding import layout_for
     from quantized_kv_decode_partial_gb300.workloads import make_case, required_kv_bytes
@@ -285,12 +288,18 @@ def run_ours(args):
         copies = max(1, math.ceil(3 * l2 / in_bytes))
         insts = [base] + [make_case(sp, device=dev, seed=rank_seed(sp.seed, rank) + 104729 * (c + 1), poison=False,
                                     lengths=base.lens_host) for c in range(copies - 1)]
-        layout = layout_for(base.k_pool, sp.head_dim, sp.bits, sp.group_size)
+        layout = layout_for(base.k_pool, sp.head_dim, sp.bits, sp.group_size, v_pool=base.v_pool)
         params = DecodeParams(sp.num_seqs, sp.num_q_heads, sp.n_query, base.block_tables.shape[1],
                               base.partition_tokens, sp.window)
         plan = make_plan(layout, params)
         ws = torch.empty(max(1, plan.workspace_bytes), dtype=torch.uint8, device=dev)
-        out = torch.empty_like(base.q)
+        out = torch.empty(base.q.shape[:-1] + (sp.dv,), dtype=base.q.dtype, device=dev)
+        if args.step == "fused":  # the step's new K/V rows (rows len-N .. len-1 of each sequence)
+            gen = torch.Generator(device=dev).manual_seed(rank_seed(sp.seed, rank) + 7)
+            for c in insts:
+                shape = (sp.num_seqs, sp.num_kv_heads, sp.n_query)
+                c.k_new = torch.randn(shape + (sp.head_dim,), generator=gen, device=dev).to(torch.bfloat16)
+                c.v_new = torch.randn(shape + (sp.dv,), generator=gen, device=dev).to(torch.bfloat16)
         layers.append(dict(spec=sp, insts=insts, plan=plan, ws=ws, out=out, copies=copies, in_bytes=in_bytes,
                            kv_bytes=required_kv_bytes(sp, base.lens_host)))
     step_bytes = sum(L["kv_bytes"] for L in layers)
@@ -302,7 +311,10 @@ def run_ours(args):
         kw = dict(bits=sp.bits, group_size=sp.group_size, k_scales=c.k_scales, k_biases=c.k_biases,
                   v_scales=c.v_scales, v_biases=c.v_biases, partition_tokens=c.partition_tokens, window=sp.window,
                   out=L["out"], workspace=L["ws"])
-        if passes is None:
+        if args.step == "fused":
+            paged_decode_append_attention(c.q, c.k_new, c.v_new, c.k_pool, c.v_pool, c.block_tables, c.seq_lens,
+                                          c.scale, **kw)
+        elif passes is None:
             paged_decode_attention(c.q, c.k_pool, c.v_pool, c.block_tables, c.seq_lens, c.scale, **kw)
         else:
             paged_decode_passes(c.q, c.k_pool, c.v_pool, c.block_tables, c.seq_lens, c.scale, passes=passes, **kw)
@@ -360,12 +372,16 @@ def run_ours(args):
     ms = replay_timed([(g_full, K // chunk)] + ([(g_rest, 1)] if g_rest else []))
     clk = clocks.stop()
 
-    # the partial pass alone (the dominant kernel), same inputs, same stream
-    g_part = capture(chunk, passes="partial")
-    g_part_rest = capture(rest, passes="partial") if rest else None
-    g_part.replay()
-    torch.cuda.synchronize(dev)
-    ms_partial = replay_timed([(g_part, K // chunk)] + ([(g_part_rest, 1)] if g_part_rest else []))
+    # the partial pass alone (the dominant kernel), same inputs, same stream; the fused
+    # step has no separate partial pass, so its roofline is the whole step's
+    if args.step == "fused":
+        ms_partial = ms
+    else:
+        g_part = capture(chunk, passes="partial")
+        g_part_rest = capture(rest, passes="partial") if rest else None
+        g_part.replay()
+        torch.cuda.synchronize(dev)
+        ms_partial = replay_timed([(g_part, K // chunk)] + ([(g_part_rest, 1)] if g_part_rest else []))
 
     # end to end through the public call: per step, q / tables / lengths come from
     # pinned host memory (one packed staging copy per layer) and the output goes back
@@ -373,7 +389,7 @@ def run_ours(args):
     stage_host, stage_dev, views, host_out = [], [], [], []
     for L in layers:
         c = L["insts"][0]
-        parts = [c.q, c.block_tables, c.seq_lens]
+        parts = [c.q, c.block_tables, c.seq_lens] + ([c.k_new, c.v_new] if args.step == "fused" else [])
         sizes = [t.numel() * t.element_size() for t in parts]
         offs = [sum(-(-x // 256) * 256 for x in sizes[:i]) for i in range(len(sizes))]
         total = offs[-1] + sizes[-1]
@@ -396,11 +412,15 @@ def run_ours(args):
             stage_dev[li].copy_(stage_host[li], non_blocking=True)
             c = L["insts"][0]
             sp = L["spec"]
-            q, tb, sl = views[li]
-            paged_decode_attention(q, c.k_pool, c.v_pool, tb, sl, c.scale, bits=sp.bits, group_size=sp.group_size,
-                                   k_scales=c.k_scales, k_biases=c.k_biases, v_scales=c.v_scales,
-                                   v_biases=c.v_biases, partition_tokens=c.partition_tokens, window=sp.window,
-                                   out=L["out"], workspace=L["ws"])
+            q, tb, sl = views[li][:3]
+            kw = dict(bits=sp.bits, group_size=sp.group_size, k_scales=c.k_scales, k_biases=c.k_biases,
+                      v_scales=c.v_scales, v_biases=c.v_biases, partition_tokens=c.partition_tokens,
+                      window=sp.window, out=L["out"], workspace=L["ws"])
+            if args.step == "fused":
+                kn, vn = views[li][3:]
+                paged_decode_append_attention(q, kn, vn, c.k_pool, c.v_pool, tb, sl, c.scale, **kw)
+            else:
+                paged_decode_attention(q, c.k_pool, c.v_pool, tb, sl, c.scale, **kw)
             host_out[li].copy_(L["out"], non_blocking=True)
 
     with torch.cuda.stream(stream):
@@ -424,7 +444,7 @@ def run_ours(args):
     part_ms = ms_partial / K
     peak, peak_kind = measured_hbm_peak()
     achieved = step_bytes / (part_ms * 1e-3) / 1e9
-    launches_per_step = sum(1 + (L["plan"].max_partitions > 1) for L in layers)
+    launches_per_step = sum(1 + (L["plan"].max_partitions > 1 and not L["plan"].merge_in_cluster) for L in layers)
     if rank == 0:
         sp0 = layers[0]["spec"]
         line = {
@@ -441,16 +461,23 @@ def run_ours(args):
                        f"{layers[0]['in_bytes'] / 1e6:.1f} MB >= 3 x L2 {l2 / 1e6:.0f} MB)" if n_copies > 1 else
                        f"inputs ({layers[0]['in_bytes'] / 1e9:.2f} GB) larger than L2 ({l2 / 1e6:.0f} MB)"),
                 "timing": "CUDA graph of the K steps replayed; CUDA events on the launching stream",
+                "step": ("decode call (pkv_paged_decode_attention)" if args.step == "decode" else
+                         "decode step with its write (pkv_paged_decode_append_attention): the N new K/V rows of "
+                         "every (sequence, KV head) are written into their pages, then the grown cache is read"),
                 "parallelism": f"dp{world} (independent instances)",
             },
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": None,
-                         "kernel": f"pkv_partial_kernel (partial pass alone, {part_ms * 1e3:.2f} us per step)",
+                         "kernel": (f"pkv_partial_kernel (partial pass alone, {part_ms * 1e3:.2f} us per step)"
+                                    if args.step == "decode" else
+                                    f"the fused step (write + partial + merge, {part_ms * 1e3:.2f} us per step)"),
                          "peak_source": f"{peak_kind} hbm_gbs", "frac_of_nominal_7900": achieved / 7900.0},
             "e2e": {"value": weak_scaling_rate(step_bytes, world, e2e_ms), "unit": "GB/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-                    "what": "public call per step with q, block tables and lengths copied from pinned host memory "
-                            "and the output copied back; the KV pool is device-resident cache state"},
+                    "what": "public call per step with q, block tables and lengths"
+                            + (", and the new K/V rows," if args.step == "fused" else "")
+                            + " copied from pinned host memory and the output copied back; the KV pool is "
+                              "device-resident cache state"},
             "gpu_launches": launches_per_step * K,
             "clocks": clk,
         }

@@ -27,19 +27,20 @@
  * Data layout (row-major, all device memory unless stated otherwise)
  * -----------------------------------------------------------------
  *   q             bf16  [num_seqs, num_q_heads, n_query, head_dim]
- *   k_pool,v_pool bits=16: bf16 [num_blocks, num_kv_heads, block_size, head_dim]
+ *   k_pool,v_pool bits=16: bf16 [num_blocks, num_kv_heads, block_size, W]
  *                 bits=4/8: uint32 words [num_blocks, num_kv_heads, block_size,
- *                 head_dim*bits/32]; code d of a row sits in word d/(32/bits) at
+ *                 W*bits/32]; code d of a row sits in word d/(32/bits) at
  *                 bit offset (d % (32/bits))*bits (lowest bits first).
+ *                 W is head_dim for K and v_head_dim for V.
  *   k_scales, k_biases, v_scales, v_biases
- *                 bf16 [num_blocks, num_kv_heads, block_size, head_dim/64]
+ *                 bf16 [num_blocks, num_kv_heads, block_size, W/64]
  *                 (affine pages only; NULL for bf16 pages). Dim d uses group d/64.
  *                 These are the layouts of the pages' BlockPool
  *                 (state/paged/cache.ts): every plane [numBlocks, H, blockSize, width].
  *   block_tables  int32 [num_seqs, max_blocks_per_seq]: logical page -> physical block.
  *   seq_lens      int32 [num_seqs]: cached rows per sequence, including the n_query
  *                 new ones.
- *   out           bf16  [num_seqs, num_q_heads, n_query, head_dim]
+ *   out           bf16  [num_seqs, num_q_heads, n_query, v_head_dim]
  *
  * Ownership: every pointer is borrowed; the library frees nothing and keeps no
  * pointer after a call returns. Calls are asynchronous on the given stream
@@ -70,9 +71,9 @@ extern "C" {
 #define PKV_OK 0
 #define PKV_ERR_NULL_POINTER (-1)        /* a required pointer is NULL */
 #define PKV_ERR_MISALIGNED (-2)          /* a device pointer is not 16-byte aligned */
-#define PKV_ERR_BAD_LAYOUT (-3)          /* unsupported bits / group_size / head_dim / block_size */
+#define PKV_ERR_BAD_LAYOUT (-3)          /* unsupported bits / group_size / head dims / block_size */
 #define PKV_ERR_BAD_PARAMS (-4)          /* bad num_seqs, heads, n_query, table width or partition size */
-#define PKV_ERR_UNSUPPORTED_SHAPE (-5)   /* (num_q_heads/num_kv_heads)*n_query above the limit for head_dim */
+#define PKV_ERR_UNSUPPORTED_SHAPE (-5)   /* no kernel for these head dims with (num_q_heads/num_kv_heads)*n_query rows */
 #define PKV_ERR_WORKSPACE_TOO_SMALL (-6) /* workspace NULL or smaller than pkv_plan.workspace_bytes */
 #define PKV_ERR_CUDA (-7)                /* a CUDA runtime or driver call failed */
 #define PKV_ERR_SCRATCH_TOO_SMALL (-8)   /* no-alloc entry: partition states larger than its static scratch */
@@ -86,14 +87,20 @@ extern "C" {
 #define PKV_DEVERR_TIMEOUT 4     /* an internal pipeline wait gave up after about a second */
 
 /* Pool layout descriptor (the pages' PagedAttentionStorage: blockSize, headDim,
- * quantization {bits, groupSize}). */
+ * vHeadDim, quantization {bits, groupSize}).
+ * Head dims with a kernel (key/value; the host rejects the rest):
+ *   equal dims: 64, 128, 256 (bf16) and 128, 256 (affine), with up to 64 / 64 / 32
+ *   query rows per KV head (64 / 32 for affine);
+ *   bf16 192/128 (up to 32 query rows), 256/128 and 128/256 (up to 8);
+ *   affine 256/128 and 128/256 (up to 8). */
 typedef struct pkv_pool_layout {
   int32_t num_blocks;   /* blocks in the pool, > 0 */
   int32_t num_kv_heads; /* HK, > 0 */
   int32_t block_size;   /* BS: rows per block; a multiple of 16 (bf16) or 32 (affine) */
-  int32_t head_dim;     /* D: 64, 128 or 256 for bf16; 128 or 256 for affine */
+  int32_t head_dim;     /* D: key (and query) head dim */
   int32_t bits;         /* 16 = bf16 pages; 4 or 8 = affine codes */
   int32_t group_size;   /* affine group; must be 64 (ignored for bf16) */
+  int32_t v_head_dim;   /* Dv: value (and output) head dim; 0 = head_dim */
 } pkv_pool_layout;
 
 /* Per-call decode parameters. */
@@ -211,7 +218,8 @@ int pkv_paged_decode_attention_no_alloc(const pkv_pool_layout* layout, const pkv
  * block_tables[b][t / block_size], row t % block_size), the pages'
  * PagedKVCache.append / BlockPool.writeBlock (state/paged/cache.ts). Blocks must
  * already be in the tables; allocating them is the caller's.
- *   k_new, v_new  bf16 [num_seqs, num_kv_heads, n_new, head_dim], 16-byte aligned
+ *   k_new, v_new  bf16 [num_seqs, num_kv_heads, n_new, head_dim / v_head_dim],
+ *                 16-byte aligned
  *   seq_lens      rows held BEFORE the append (the caller then adds n_new)
  * bf16 pages are copied. Affine pages are quantised per row and 64-dim group
  * (the pages do not give the quantiser's formula; this is the min/max reading,
@@ -222,7 +230,8 @@ int pkv_paged_decode_attention_no_alloc(const pkv_pool_layout* layout, const pkv
  * codes packed lowest bits first. Bad block ids skip their row and set
  * PKV_DEVERR_BAD_BLOCK; seq_lens[b] + n_new above max_blocks_per_seq*block_size
  * sets PKV_DEVERR_BAD_SEQ_LEN and writes nothing for that sequence.
- * Layouts: bf16 head_dim 64/128/256, affine 128/256. Asynchronous on `stream`. */
+ * Layouts: every (bits, head dims) pair the decode has a kernel for.
+ * Asynchronous on `stream`. */
 int pkv_paged_append(const pkv_pool_layout* layout, int32_t num_seqs, int32_t max_blocks_per_seq, int32_t n_new,
                      const void* k_new, const void* v_new, const int32_t* block_tables, const int32_t* seq_lens,
                      void* k_pool, void* v_pool, void* k_scales, void* k_biases, void* v_scales, void* v_biases,
@@ -233,7 +242,7 @@ int pkv_paged_append(const pkv_pool_layout* layout, int32_t num_seqs, int32_t ma
  * same launches as pkv_paged_decode_attention. This is the pages' appendDecode
  * (PagedKVCache.appendDecode: append, then read the paged view of the grown
  * cache, "@mlx-bun/inference 0.0.0-stage -> 1.0.0", state/paged/cache.ts).
- *   k_new, v_new  bf16 [num_seqs, num_kv_heads, n_query, head_dim], 16-byte
+ *   k_new, v_new  bf16 [num_seqs, num_kv_heads, n_query, head_dim / v_head_dim], 16-byte
  *                 aligned: the K and V rows of the step's query tokens
  *   seq_lens      rows held AFTER the append, as for pkv_paged_decode_attention:
  *                 the new rows go to cache positions seq_lens[b] - n_query ..

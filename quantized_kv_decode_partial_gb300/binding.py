@@ -59,7 +59,7 @@ class PkvError(RuntimeError):
 
 class PoolLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in
-                ("num_blocks", "num_kv_heads", "block_size", "head_dim", "bits", "group_size")]
+                ("num_blocks", "num_kv_heads", "block_size", "head_dim", "bits", "group_size", "v_head_dim")]
 
 
 class DecodeParams(ctypes.Structure):
@@ -133,9 +133,22 @@ def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
     return None if t is None else t.data_ptr()
 
 
-def layout_for(k_pool: torch.Tensor, head_dim: int, bits: int, group_size: int = 64) -> PoolLayout:
+def v_head_dim_of(v_pool: torch.Tensor, bits: int) -> int:
+    """Value head dim of a V pool: its row width, in values (bf16) or codes (affine words)."""
+    w = v_pool.shape[-1]
+    return w if bits == 16 else w * 32 // bits
+
+
+def layout_for(k_pool: torch.Tensor, head_dim: int, bits: int, group_size: int = 64,
+               v_pool: Optional[torch.Tensor] = None) -> PoolLayout:
     nb, hk, bs, _ = k_pool.shape
-    return PoolLayout(nb, hk, bs, head_dim, bits, group_size)
+    dv = 0 if v_pool is None else v_head_dim_of(v_pool, bits)
+    return PoolLayout(nb, hk, bs, head_dim, bits, group_size, 0 if dv == head_dim else dv)
+
+
+def _out_like(q: torch.Tensor, layout: PoolLayout) -> torch.Tensor:
+    dv = layout.v_head_dim or layout.head_dim
+    return torch.empty(q.shape[:-1] + (dv,), dtype=q.dtype, device=q.device)
 
 
 _plan_cache = {}
@@ -186,12 +199,12 @@ def paged_decode_attention(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.
     """
     lib = load_library()
     B, HQ, N, D = q.shape
-    layout = layout_for(k_pool, D, bits, group_size)
+    layout = layout_for(k_pool, D, bits, group_size, v_pool)
     params = DecodeParams(B, HQ, N, block_tables.shape[1], partition_tokens, window)
     with _on_device(q.device):
         plan = _cached_plan(layout, params)
         if out is None:
-            out = torch.empty_like(q)
+            out = _out_like(q, layout)
         if workspace is None and plan.workspace_bytes:
             workspace = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=q.device)
         ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
@@ -217,12 +230,12 @@ def paged_decode_append_attention(q: torch.Tensor, k_new: torch.Tensor, v_new: t
     (seq_lens counts the new rows), then attends as ``paged_decode_attention``."""
     lib = load_library()
     B, HQ, N, D = q.shape
-    layout = layout_for(k_pool, D, bits, group_size)
+    layout = layout_for(k_pool, D, bits, group_size, v_pool)
     params = DecodeParams(B, HQ, N, block_tables.shape[1], partition_tokens, window)
     with _on_device(q.device):
         plan = _cached_plan(layout, params)
         if out is None:
-            out = torch.empty_like(q)
+            out = _out_like(q, layout)
         if workspace is None and plan.workspace_bytes:
             workspace = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=q.device)
         ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
@@ -267,7 +280,7 @@ def paged_decode_passes(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Ten
     partition, ``workspace`` must be given so the two calls share them."""
     lib = load_library()
     B, HQ, N, D = q.shape
-    layout = layout_for(k_pool, D, bits, group_size)
+    layout = layout_for(k_pool, D, bits, group_size, v_pool)
     params = DecodeParams(B, HQ, N, block_tables.shape[1], partition_tokens, window)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     with _on_device(q.device):
@@ -294,7 +307,7 @@ def paged_append(k_new: torch.Tensor, v_new: torch.Tensor, block_tables: torch.T
     sequence (quantising affine pages); see include/pkv_decode.h."""
     lib = load_library()
     B, HK, n_new, D = k_new.shape
-    layout = layout_for(k_pool, D, bits, group_size)
+    layout = layout_for(k_pool, D, bits, group_size, v_pool)
     with _on_device(k_new.device):
         stream = torch.cuda.current_stream(k_new.device).cuda_stream
         rc = lib.pkv_paged_append(ctypes.byref(layout), B, block_tables.shape[1], n_new, _ptr(k_new), _ptr(v_new),

@@ -27,11 +27,19 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
 
-PartialInfo partial_info(int bits, int head_dim, int nq, bool solo = false) {
-  if (bits == 16) return pkv::partial_info_bf16(head_dim, nq, solo);
-  if (bits == 4) return pkv::partial_info_u4(head_dim, nq, solo);
-  if (bits == 8) return pkv::partial_info_u8(head_dim, nq, solo);
-  return PartialInfo{false, 0, 0, 0, 0, 0};
+PartialInfo partial_info(int bits, int dk, int dv, int nq, bool solo = false) {
+  if (bits == 16) return pkv::partial_info_bf16(dk, dv, nq, solo);
+  if (bits == 4) return pkv::partial_info_u4(dk, dv, nq, solo);
+  if (bits == 8) return pkv::partial_info_u8(dk, dv, nq, solo);
+  return PartialInfo{false, 0, 0, 0, 0, 0, 0};
+}
+
+// Value head dim of a layout (0 in the descriptor means the key head dim).
+int v_dim(const pkv_pool_layout* L) { return L->v_head_dim > 0 ? L->v_head_dim : L->head_dim; }
+
+// Stored bytes of one row of head dim `d`: bf16 values, or codes plus bf16 scale and bias.
+long long stored_row_bytes(const pkv_pool_layout* L, int d) {
+  return L->bits == 16 ? 2ll * d : static_cast<long long>(d) * L->bits / 8 + d / 64 * 4;
 }
 
 int chunk_rows_of(int bits) { return bits == 16 ? 16 : 32; }
@@ -41,10 +49,12 @@ int check_layout(const pkv_pool_layout* L) {
   if (L->num_blocks <= 0 || L->num_kv_heads <= 0 || L->block_size <= 0) return PKV_ERR_BAD_LAYOUT;
   if (L->bits != 16 && L->bits != 4 && L->bits != 8) return PKV_ERR_BAD_LAYOUT;
   if (L->bits == 16) {
-    if (L->head_dim != 64 && L->head_dim != 128 && L->head_dim != 256) return PKV_ERR_BAD_LAYOUT;
+    if (L->head_dim != 64 && L->head_dim != 128 && L->head_dim != 192 && L->head_dim != 256) return PKV_ERR_BAD_LAYOUT;
+    if (v_dim(L) != 64 && v_dim(L) != 128 && v_dim(L) != 256) return PKV_ERR_BAD_LAYOUT;
   } else {
     if (L->group_size != 64) return PKV_ERR_BAD_LAYOUT;
     if (L->head_dim != 128 && L->head_dim != 256) return PKV_ERR_BAD_LAYOUT;
+    if (v_dim(L) != 128 && v_dim(L) != 256) return PKV_ERR_BAD_LAYOUT;
   }
   if (L->block_size % chunk_rows_of(L->bits)) return PKV_ERR_BAD_LAYOUT;
   const long long rows = static_cast<long long>(L->num_blocks) * L->num_kv_heads * L->block_size;
@@ -62,7 +72,7 @@ int check_params(const pkv_pool_layout* L, const pkv_decode_params* P) {
   if (static_cast<long long>(P->max_blocks_per_seq) * L->block_size >= (1ll << 31)) return PKV_ERR_BAD_PARAMS;
   const long long nq = static_cast<long long>(P->num_q_heads / L->num_kv_heads) * P->n_query;
   if (nq > 64) return PKV_ERR_UNSUPPORTED_SHAPE;
-  if (!partial_info(L->bits, L->head_dim, static_cast<int>(nq)).exists) return PKV_ERR_UNSUPPORTED_SHAPE;
+  if (!partial_info(L->bits, L->head_dim, v_dim(L), static_cast<int>(nq)).exists) return PKV_ERR_UNSUPPORTED_SHAPE;
   return PKV_OK;
 }
 
@@ -85,10 +95,9 @@ int plan_impl(const pkv_pool_layout* L, const pkv_decode_params* P, int sm_count
     const long long slots = 2ll * (sm_count > 0 ? sm_count : 1);
     const long long target = 4 * slots;
     const long long units = static_cast<long long>(P->num_seqs) * L->num_kv_heads;
-    const long long plane_row = L->bits == 16 ? 2ll * L->head_dim
-                                              : static_cast<long long>(L->head_dim) * L->bits / 8 + L->head_dim / 64 * 4;
+    const long long kv_row = stored_row_bytes(L, L->head_dim) + stored_row_bytes(L, v_dim(L));  // K + V
     const long long floor_rows = 256;
-    const long long rich_rows = std::max<long long>(floor_rows, (512ll << 10) / (2 * plane_row));
+    const long long rich_rows = std::max<long long>(floor_rows, (512ll << 10) / kv_row);
     // rows a step can read per sequence: the table, or the window's span
     const long long span = P->window > 0 ? std::min<long long>(max_len, P->window + P->n_query - 1) : max_len;
     part = round_up(span, ch);
@@ -113,9 +122,10 @@ int plan_impl(const pkv_pool_layout* L, const pkv_decode_params* P, int sm_count
   // per CTA, where there is one for this shape.
   const long long sms = sm_count > 0 ? sm_count : 1;
   const long long ctas = static_cast<long long>(P->num_seqs) * L->num_kv_heads * max_parts;
-  const bool use_solo = ctas <= sms && partial_info(L->bits, L->head_dim, static_cast<int>(nq), true).exists;
+  const bool use_solo =
+      ctas <= sms && partial_info(L->bits, L->head_dim, v_dim(L), static_cast<int>(nq), true).exists;
   if (solo) *solo = use_solo;
-  const PartialInfo info = partial_info(L->bits, L->head_dim, static_cast<int>(nq), use_solo);
+  const PartialInfo info = partial_info(L->bits, L->head_dim, v_dim(L), static_cast<int>(nq), use_solo);
   out->partition_tokens = static_cast<int32_t>(part);
   out->max_partitions = max_parts;
   out->chunk_rows = info.chunk_rows;
@@ -134,7 +144,7 @@ int plan_impl(const pkv_pool_layout* L, const pkv_decode_params* P, int sm_count
                           ctas <= sms * (two_per_sm ? 2 : 1);
   if (max_parts > 1 && !out->merge_in_cluster) {
     const size_t slots = static_cast<size_t>(P->num_seqs) * P->num_q_heads * P->n_query * max_parts;
-    const size_t o_bytes = (slots * L->head_dim * sizeof(float) + 255) / 256 * 256;
+    const size_t o_bytes = (slots * v_dim(L) * sizeof(float) + 255) / 256 * 256;
     out->workspace_bytes = o_bytes + slots * 2 * sizeof(float);
   }
   return PKV_OK;
@@ -177,7 +187,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 // 2-D view of one pool plane: rows = num_blocks*HK*BS, `row_elems` elements per
 // row; boxes of `box_rows` rows by `box_row_bytes` bytes with the matching swizzle.
 int encode_pool_tensor_map(CUtensorMap* map, const void* base, int elem_bytes, long long row_elems, long long rows,
-                           const PartialInfo& info) {
+                           int box_row_bytes, int box_rows) {
   auto encode = tensor_map_encoder();
   if (!encode) {
     std::snprintf(g_cuda_error, sizeof(g_cuda_error), "cuTensorMapEncodeTiled entry point unavailable");
@@ -186,10 +196,9 @@ int encode_pool_tensor_map(CUtensorMap* map, const void* base, int elem_bytes, l
   const CUtensorMapDataType dt = elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_elems), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_elems * elem_bytes)};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(info.box_row_bytes / elem_bytes),
-                       static_cast<cuuint32_t>(info.chunk_rows)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_row_bytes / elem_bytes), static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[2] = {1, 1};
-  const CUtensorMapSwizzle sw = info.box_row_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  const CUtensorMapSwizzle sw = box_row_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
   CUresult r = encode(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                       sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
@@ -213,23 +222,23 @@ TensorMapEntry g_tmap_cache[kTensorMapCacheSize];
 int g_tmap_next = 0;
 
 int pool_tensor_map(CUtensorMap* map, const void* base, int elem_bytes, long long row_elems, long long rows,
-                    const PartialInfo& info) {
+                    int box_row_bytes, int box_rows) {
   {
     std::lock_guard<std::mutex> lock(g_tmap_mutex);
     for (const TensorMapEntry& e : g_tmap_cache) {
       if (e.base == base && e.row_elems == row_elems && e.rows == rows && e.elem_bytes == elem_bytes &&
-          e.box_row_bytes == info.box_row_bytes && e.chunk_rows == info.chunk_rows) {
+          e.box_row_bytes == box_row_bytes && e.chunk_rows == box_rows) {
         *map = e.map;
         return PKV_OK;
       }
     }
   }
-  int rc = encode_pool_tensor_map(map, base, elem_bytes, row_elems, rows, info);
+  int rc = encode_pool_tensor_map(map, base, elem_bytes, row_elems, rows, box_row_bytes, box_rows);
   if (rc) return rc;
   std::lock_guard<std::mutex> lock(g_tmap_mutex);
   TensorMapEntry& e = g_tmap_cache[g_tmap_next];
   g_tmap_next = (g_tmap_next + 1) % kTensorMapCacheSize;
-  e = TensorMapEntry{base, row_elems, rows, elem_bytes, info.box_row_bytes, info.chunk_rows, *map};
+  e = TensorMapEntry{base, row_elems, rows, elem_bytes, box_row_bytes, box_rows, *map};
   return PKV_OK;
 }
 
@@ -317,18 +326,19 @@ int enqueue_decode(const pkv_pool_layout* layout, const pkv_decode_params* param
   if (mode == pkv::kModeWorkspace && (!workspace || workspace_bytes < plan.workspace_bytes))
     return PKV_ERR_WORKSPACE_TOO_SMALL;
 
-  const int D = layout->head_dim, HK = layout->num_kv_heads;
+  const int D = layout->head_dim, DV = v_dim(layout), HK = layout->num_kv_heads;
   const int nq = (params->num_q_heads / HK) * params->n_query;
-  const PartialInfo info = partial_info(layout->bits, D, nq, solo);
+  const PartialInfo info = partial_info(layout->bits, D, DV, nq, solo);
   const long long rows = static_cast<long long>(layout->num_blocks) * HK * layout->block_size;
   const int elem = info.tensor_elem_bytes;
-  const long long row_elems = quant ? static_cast<long long>(D) * layout->bits / 8 : D;
+  const long long row_elems_k = quant ? static_cast<long long>(D) * layout->bits / 8 : D;
+  const long long row_elems_v = quant ? static_cast<long long>(DV) * layout->bits / 8 : DV;
 
   CUtensorMap tk, tv;
   if (partial) {
-    rc = pool_tensor_map(&tk, k_pool, elem, row_elems, rows, info);
+    rc = pool_tensor_map(&tk, k_pool, elem, row_elems_k, rows, info.box_row_bytes, info.chunk_rows);
     if (rc) return rc;
-    rc = pool_tensor_map(&tv, v_pool, elem, row_elems, rows, info);
+    rc = pool_tensor_map(&tv, v_pool, elem, row_elems_v, rows, info.box_row_bytes_v, info.chunk_rows);
     if (rc) return rc;
   }
 
@@ -371,11 +381,11 @@ int enqueue_decode(const pkv_pool_layout* layout, const pkv_decode_params* param
   cudaError_t e = cudaSuccess;
   if (partial) {
     if (layout->bits == 16)
-      e = pkv::launch_partial_bf16(D, nq, solo, p, tk, tv, grid, st, dev);
+      e = pkv::launch_partial_bf16(D, DV, nq, solo, p, tk, tv, grid, st, dev);
     else if (layout->bits == 4)
-      e = pkv::launch_partial_u4(D, nq, solo, p, tk, tv, grid, st, dev);
+      e = pkv::launch_partial_u4(D, DV, nq, solo, p, tk, tv, grid, st, dev);
     else
-      e = pkv::launch_partial_u8(D, nq, solo, p, tk, tv, grid, st, dev);
+      e = pkv::launch_partial_u8(D, DV, nq, solo, p, tk, tv, grid, st, dev);
     if (e != cudaSuccess) return cuda_fail("partial kernel launch", e);
   }
 
@@ -388,7 +398,7 @@ int enqueue_decode(const pkv_pool_layout* layout, const pkv_decode_params* param
     m.error_flag = error_flag;
     m.rows_per_seq = params->num_q_heads * params->n_query;
     m.n_query = params->n_query;
-    m.head_dim = D;
+    m.head_dim = DV;
     m.max_len = params->max_blocks_per_seq * layout->block_size;
     m.partition_tokens = plan.partition_tokens;
     m.max_partitions = plan.max_partitions;
@@ -447,7 +457,7 @@ int pkv_paged_append(const pkv_pool_layout* layout, int32_t num_seqs, int32_t ma
                      int32_t* error_flag, void* stream) {
   int rc = check_layout(layout);
   if (rc) return rc;
-  if (!pkv::append_supported(layout->bits, layout->head_dim)) return PKV_ERR_BAD_LAYOUT;
+  if (!pkv::append_supported(layout->bits, layout->head_dim, v_dim(layout))) return PKV_ERR_BAD_LAYOUT;
   if (num_seqs <= 0 || num_seqs > 65535 || max_blocks_per_seq <= 0 || n_new < 0 || n_new > 65535)
     return PKV_ERR_BAD_PARAMS;
   if (static_cast<long long>(max_blocks_per_seq) * layout->block_size >= (1ll << 31)) return PKV_ERR_BAD_PARAMS;
@@ -472,7 +482,8 @@ int pkv_paged_append(const pkv_pool_layout* layout, int32_t num_seqs, int32_t ma
   a.max_blocks = max_blocks_per_seq;
   a.n_new = n_new;
   (void)cudaGetLastError();
-  cudaError_t e = pkv::launch_append(a, layout->bits, layout->head_dim, num_seqs, static_cast<cudaStream_t>(stream));
+  cudaError_t e = pkv::launch_append(a, layout->bits, layout->head_dim, v_dim(layout), num_seqs,
+                                     static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail("append kernel launch", e);
   return PKV_OK;
 }
@@ -595,9 +606,10 @@ const char* pkv_strerror(int code) {
     case PKV_OK: return "success";
     case PKV_ERR_NULL_POINTER: return "a required pointer is NULL";
     case PKV_ERR_MISALIGNED: return "a pointer is not aligned (16 bytes for data planes, 4 for int32 arrays)";
-    case PKV_ERR_BAD_LAYOUT: return "unsupported pool layout (bits, group_size, head_dim or block_size)";
+    case PKV_ERR_BAD_LAYOUT: return "unsupported pool layout (bits, group_size, head dims or block_size)";
     case PKV_ERR_BAD_PARAMS: return "bad decode parameters (sequences, heads, n_query, table width or partition)";
-    case PKV_ERR_UNSUPPORTED_SHAPE: return "too many query rows per KV head for this head_dim";
+    case PKV_ERR_UNSUPPORTED_SHAPE:
+      return "no kernel for this pair of key/value head dims with this many query rows per KV head";
     case PKV_ERR_WORKSPACE_TOO_SMALL: return "workspace missing or smaller than the plan needs";
     case PKV_ERR_CUDA: return "a CUDA call failed (see pkv_last_cuda_error)";
     case PKV_ERR_SCRATCH_TOO_SMALL:
@@ -609,6 +621,6 @@ const char* pkv_strerror(int code) {
 
 const char* pkv_last_cuda_error(void) { return g_cuda_error; }
 
-int pkv_version(void) { return 100; }
+int pkv_version(void) { return 200; }
 
 }  // extern "C"

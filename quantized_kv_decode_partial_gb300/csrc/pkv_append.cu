@@ -13,7 +13,7 @@ namespace {
 constexpr int kAppendWarps = 4;  // KV heads per CTA
 
 // One warp per (sequence, new row, KV head).
-template <int BITS, int D>
+template <int BITS, int DK, int DV>
 __global__ void __launch_bounds__(kAppendWarps * 32) pkv_append_kernel(const __grid_constant__ AppendParams p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.x * kAppendWarps + warp;
@@ -32,32 +32,40 @@ __global__ void __launch_bounds__(kAppendWarps * 32) pkv_append_kernel(const __g
   }
   const size_t row = (static_cast<size_t>(phys) * p.num_kv_heads + h) * p.block_size + t % p.block_size;
   const size_t src_row = (static_cast<size_t>(b) * p.num_kv_heads + h) * p.n_new + j;
-  append_row<BITS, D>(p.k_new + src_row * D, p.v_new + src_row * D, p.dst, row, lane);
+  append_row<BITS, DK, DV>(p.k_new + src_row * DK, p.v_new + src_row * DV, p.dst, row, lane);
 }
 
-template <int BITS, int D>
+template <int BITS, int DK, int DV>
 cudaError_t launch_append_of(const AppendParams& p, int num_seqs, cudaStream_t stream) {
   dim3 grid((p.num_kv_heads + kAppendWarps - 1) / kAppendWarps, p.n_new, num_seqs);
-  pkv_append_kernel<BITS, D><<<grid, kAppendWarps * 32, 0, stream>>>(p);
+  pkv_append_kernel<BITS, DK, DV><<<grid, kAppendWarps * 32, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
+// (bits, key head dim, value head dim) combinations of the append kernel: every
+// layout the partial kernel reads.
+#define PKV_APPEND_SHAPES(X)                                                       \
+  X(16, 64, 64) X(16, 128, 128) X(16, 256, 256) X(16, 192, 128) X(16, 256, 128) \
+  X(16, 128, 256) X(4, 128, 128) X(4, 256, 256) X(4, 256, 128) X(4, 128, 256)   \
+  X(8, 128, 128) X(8, 256, 256) X(8, 256, 128) X(8, 128, 256)
+
 }  // namespace
 
-bool append_supported(int bits, int head_dim) {
-  if (bits == 16) return head_dim == 64 || head_dim == 128 || head_dim == 256;
-  return (bits == 4 || bits == 8) && (head_dim == 128 || head_dim == 256);
+bool append_supported(int bits, int head_dim, int v_head_dim) {
+#define X(B_, DK_, DV_) \
+  if (bits == B_ && head_dim == DK_ && v_head_dim == DV_) return true;
+  PKV_APPEND_SHAPES(X)
+#undef X
+  return false;
 }
 
-cudaError_t launch_append(const AppendParams& p, int bits, int head_dim, int num_seqs, cudaStream_t stream) {
+cudaError_t launch_append(const AppendParams& p, int bits, int head_dim, int v_head_dim, int num_seqs,
+                          cudaStream_t stream) {
   if (p.n_new == 0) return cudaSuccess;
-  if (bits == 16 && head_dim == 64) return launch_append_of<16, 64>(p, num_seqs, stream);
-  if (bits == 16 && head_dim == 128) return launch_append_of<16, 128>(p, num_seqs, stream);
-  if (bits == 16 && head_dim == 256) return launch_append_of<16, 256>(p, num_seqs, stream);
-  if (bits == 4 && head_dim == 128) return launch_append_of<4, 128>(p, num_seqs, stream);
-  if (bits == 4 && head_dim == 256) return launch_append_of<4, 256>(p, num_seqs, stream);
-  if (bits == 8 && head_dim == 128) return launch_append_of<8, 128>(p, num_seqs, stream);
-  if (bits == 8 && head_dim == 256) return launch_append_of<8, 256>(p, num_seqs, stream);
+#define X(B_, DK_, DV_) \
+  if (bits == B_ && head_dim == DK_ && v_head_dim == DV_) return launch_append_of<B_, DK_, DV_>(p, num_seqs, stream);
+  PKV_APPEND_SHAPES(X)
+#undef X
   return cudaErrorInvalidValue;
 }
 

@@ -16,77 +16,87 @@
 
 namespace pkv {
 
-// Writes K row `k_src` and V row `v_src` (bf16, D values each) to pool row `row`
-// (= (phys * HK + h) * BS + offset in block). Warp-collective: lane l handles dims
-// [l*E, l*E + E), E = D / 32; every lane of the warp must call it.
+// Writes one row of D values from `src` (bf16) into pool row `row` of one plane: a
+// bf16 row, or codes plus the row's per-group scale and bias. Warp-collective: lane
+// l handles dims [l*E, l*E + E), E = D / 32; every lane of the warp must call it.
 template <int BITS, int D>
-__device__ __forceinline__ void append_row(const __nv_bfloat16* k_src, const __nv_bfloat16* v_src,
-                                           const AppendTarget& dst, size_t row, int lane) {
+__device__ __forceinline__ void append_plane(const __nv_bfloat16* src_row, __nv_bfloat16* pool_bf16,
+                                             uint32_t* pool_words, __nv_bfloat16* scales, __nv_bfloat16* biases,
+                                             size_t row, int lane) {
   constexpr int E = D / 32;  // elements per lane
-#pragma unroll
-  for (int plane = 0; plane < 2; ++plane) {
-    const __nv_bfloat16* src = (plane == 0 ? k_src : v_src) + lane * E;
-    if constexpr (BITS == 16) {
-      __nv_bfloat16* out = (plane == 0 ? dst.k_pool_bf16 : dst.v_pool_bf16) + row * D + lane * E;
-      if constexpr (E == 8) {
-        *reinterpret_cast<uint4*>(out) = *reinterpret_cast<const uint4*>(src);
-      } else if constexpr (E == 4) {
-        *reinterpret_cast<uint2*>(out) = *reinterpret_cast<const uint2*>(src);
-      } else {
-        *reinterpret_cast<uint32_t*>(out) = *reinterpret_cast<const uint32_t*>(src);
-      }
+  static_assert(D % 64 == 0 || (BITS == 16 && D % 32 == 0), "whole lanes (and whole 64-dim groups for affine)");
+  const __nv_bfloat16* src = src_row + lane * E;
+  if constexpr (BITS == 16) {
+    __nv_bfloat16* out = pool_bf16 + row * D + lane * E;
+    if constexpr (E == 8) {
+      *reinterpret_cast<uint4*>(out) = *reinterpret_cast<const uint4*>(src);
+    } else if constexpr (E == 4) {
+      *reinterpret_cast<uint2*>(out) = *reinterpret_cast<const uint2*>(src);
     } else {
-      static_assert(D == 128 || D == 256, "affine head dims 128 or 256");
-      constexpr int kLanesPerGroup = 64 / E;
-      constexpr float kLevels = static_cast<float>((1 << BITS) - 1);
-      float x[E];
 #pragma unroll
-      for (int e = 0; e < E; e += 2) {
-        const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(src + e);
-        x[e] = __low2float(v);
-        x[e + 1] = __high2float(v);
-      }
-      float lo = x[0], hi = x[0];
+      for (int w = 0; w < E / 2; ++w)
+        reinterpret_cast<uint32_t*>(out)[w] = reinterpret_cast<const uint32_t*>(src)[w];
+    }
+  } else {
+    static_assert(D == 128 || D == 256, "affine head dims 128 or 256");
+    constexpr int kLanesPerGroup = 64 / E;
+    constexpr float kLevels = static_cast<float>((1 << BITS) - 1);
+    float x[E];
 #pragma unroll
-      for (int e = 1; e < E; ++e) {
-        lo = fminf(lo, x[e]);
-        hi = fmaxf(hi, x[e]);
-      }
+    for (int e = 0; e < E; e += 2) {
+      const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(src + e);
+      x[e] = __low2float(v);
+      x[e + 1] = __high2float(v);
+    }
+    float lo = x[0], hi = x[0];
 #pragma unroll
-      for (int off = 1; off < kLanesPerGroup; off <<= 1) {  // the group's lanes are consecutive
-        lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, off));
-        hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, off));
-      }
-      const __nv_bfloat16 s16 = __float2bfloat16_rn(__fdiv_rn(hi - lo, kLevels));
-      const __nv_bfloat16 b16 = __float2bfloat16_rn(lo);
-      const float s = __bfloat162float(s16), bias = __bfloat162float(b16);
-      uint32_t packed[E * BITS / 32 > 0 ? E * BITS / 32 : 1] = {};
-      uint32_t half_word = 0;  // 4-bit codes of a lane with E = 4 fill 16 bits
+    for (int e = 1; e < E; ++e) {
+      lo = fminf(lo, x[e]);
+      hi = fmaxf(hi, x[e]);
+    }
 #pragma unroll
-      for (int e = 0; e < E; ++e) {
-        uint32_t code = 0;
-        if (s != 0.f) code = static_cast<uint32_t>(fminf(fmaxf(rintf(__fdiv_rn(x[e] - bias, s)), 0.f), kLevels));
-        if constexpr (E * BITS >= 32) {
-          packed[(e * BITS) / 32] |= code << ((e * BITS) % 32);
-        } else {
-          half_word |= code << (e * BITS);
-        }
-      }
-      uint32_t* words = (plane == 0 ? dst.k_pool_words : dst.v_pool_words) + row * (D * BITS / 32);
+    for (int off = 1; off < kLanesPerGroup; off <<= 1) {  // the group's lanes are consecutive
+      lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, off));
+      hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, off));
+    }
+    const __nv_bfloat16 s16 = __float2bfloat16_rn(__fdiv_rn(hi - lo, kLevels));
+    const __nv_bfloat16 b16 = __float2bfloat16_rn(lo);
+    const float s = __bfloat162float(s16), bias = __bfloat162float(b16);
+    uint32_t packed[E * BITS / 32 > 0 ? E * BITS / 32 : 1] = {};
+    uint32_t half_word = 0;  // 4-bit codes of a lane with E = 4 fill 16 bits
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      uint32_t code = 0;
+      if (s != 0.f) code = static_cast<uint32_t>(fminf(fmaxf(rintf(__fdiv_rn(x[e] - bias, s)), 0.f), kLevels));
       if constexpr (E * BITS >= 32) {
-#pragma unroll
-        for (int w = 0; w < E * BITS / 32; ++w) words[lane * (E * BITS / 32) + w] = packed[w];
-      } else {  // two lanes per word: the even lane holds the low half
-        const uint32_t other = __shfl_xor_sync(0xffffffffu, half_word, 1);
-        if ((lane & 1) == 0) words[lane >> 1] = half_word | (other << 16);
-      }
-      if (lane % kLanesPerGroup == 0) {
-        const int grp = lane / kLanesPerGroup;
-        (plane == 0 ? dst.k_scales : dst.v_scales)[row * (D / 64) + grp] = s16;
-        (plane == 0 ? dst.k_biases : dst.v_biases)[row * (D / 64) + grp] = b16;
+        packed[(e * BITS) / 32] |= code << ((e * BITS) % 32);
+      } else {
+        half_word |= code << (e * BITS);
       }
     }
+    uint32_t* words = pool_words + row * (D * BITS / 32);
+    if constexpr (E * BITS >= 32) {
+#pragma unroll
+      for (int w = 0; w < E * BITS / 32; ++w) words[lane * (E * BITS / 32) + w] = packed[w];
+    } else {  // two lanes per word: the even lane holds the low half
+      const uint32_t other = __shfl_xor_sync(0xffffffffu, half_word, 1);
+      if ((lane & 1) == 0) words[lane >> 1] = half_word | (other << 16);
+    }
+    if (lane % kLanesPerGroup == 0) {
+      const int grp = lane / kLanesPerGroup;
+      scales[row * (D / 64) + grp] = s16;
+      biases[row * (D / 64) + grp] = b16;
+    }
   }
+}
+
+// Writes K row `k_src` (DK values) and V row `v_src` (DV values) to pool row `row`
+// (= (phys * HK + h) * BS + offset in block) of their planes. Warp-collective.
+template <int BITS, int DK, int DV>
+__device__ __forceinline__ void append_row(const __nv_bfloat16* k_src, const __nv_bfloat16* v_src,
+                                           const AppendTarget& dst, size_t row, int lane) {
+  append_plane<BITS, DK>(k_src, dst.k_pool_bf16, dst.k_pool_words, dst.k_scales, dst.k_biases, row, lane);
+  append_plane<BITS, DV>(v_src, dst.v_pool_bf16, dst.v_pool_words, dst.v_scales, dst.v_biases, row, lane);
 }
 
 }  // namespace pkv

@@ -15,27 +15,30 @@ struct PartialInfo {
   int threads;
   int smem_bytes;
   int chunk_rows;
-  int box_row_bytes;  // bytes of one TMA box row (64 or 128)
+  int box_row_bytes;    // bytes of one TMA box row of the K plane (64 or 128)
+  int box_row_bytes_v;  // ... of the V plane
   int tensor_elem_bytes;  // element size of the pool tensor maps (2 bf16, 1 affine codes)
 };
 
-// Partial-kernel instantiation for `nq` query rows per KV head; `solo` selects the
-// variant for grids of at most one CTA per SM (exists = false where there is none).
-PartialInfo partial_info_bf16(int head_dim, int nq, bool solo);
-PartialInfo partial_info_u4(int head_dim, int nq, bool solo);
-PartialInfo partial_info_u8(int head_dim, int nq, bool solo);
+// Partial-kernel instantiation for key head dim dk, value head dim dv and `nq` query
+// rows per KV head; `solo` selects the variant for grids of at most one CTA per SM
+// (exists = false where there is none).
+PartialInfo partial_info_bf16(int dk, int dv, int nq, bool solo);
+PartialInfo partial_info_u4(int dk, int dv, int nq, bool solo);
+PartialInfo partial_info_u8(int dk, int dv, int nq, bool solo);
 
-cudaError_t launch_partial_bf16(int head_dim, int nq, bool solo, const PartialParams& p, const CUtensorMap& tk,
+cudaError_t launch_partial_bf16(int dk, int dv, int nq, bool solo, const PartialParams& p, const CUtensorMap& tk,
                                 const CUtensorMap& tv, dim3 grid, cudaStream_t stream, int device);
-cudaError_t launch_partial_u4(int head_dim, int nq, bool solo, const PartialParams& p, const CUtensorMap& tk,
+cudaError_t launch_partial_u4(int dk, int dv, int nq, bool solo, const PartialParams& p, const CUtensorMap& tk,
                               const CUtensorMap& tv, dim3 grid, cudaStream_t stream, int device);
-cudaError_t launch_partial_u8(int head_dim, int nq, bool solo, const PartialParams& p, const CUtensorMap& tk,
+cudaError_t launch_partial_u8(int dk, int dv, int nq, bool solo, const PartialParams& p, const CUtensorMap& tk,
                               const CUtensorMap& tv, dim3 grid, cudaStream_t stream, int device);
 
 cudaError_t launch_merge(const MergeParams& p, int rows, cudaStream_t stream);
 cudaError_t launch_gather(const GatherParams& p, int num_seqs, cudaStream_t stream);
 
-bool append_supported(int bits, int head_dim);
-cudaError_t launch_append(const AppendParams& p, int bits, int head_dim, int num_seqs, cudaStream_t stream);
+bool append_supported(int bits, int head_dim, int v_head_dim);
+cudaError_t launch_append(const AppendParams& p, int bits, int head_dim, int v_head_dim, int num_seqs,
+                          cudaStream_t stream);
 
 }  // namespace pkv

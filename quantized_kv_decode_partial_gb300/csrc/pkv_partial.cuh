@@ -54,20 +54,36 @@ namespace pkv {
 // itself, so it takes 8 warps (two per scheduler, so one warp's dependent chain
 // hides behind the other's) when two stages per warp fit in shared memory, and as
 // many stages per warp (up to 4) as fit.
-template <int BITS, int D, int NT, int WQ, bool SOLO>
+// D is the key (and query) head dim, DV the value head dim. Names without a V
+// describe the K plane, names with one the V plane.
+template <int BITS, int D, int DV, int NT, int WQ, bool SOLO>
 struct PartialCfg {
   static constexpr bool kQuant = BITS != 16;
-  static constexpr int kElemBytes = kQuant ? 1 : 2;                // tensor-map element size
-  static constexpr int kRowBytes = kQuant ? D * BITS / 8 : 2 * D;  // stored bytes of one row
+  static constexpr int kElemBytes = kQuant ? 1 : 2;                    // tensor-map element size
+  static constexpr int kRowBytes = kQuant ? D * BITS / 8 : 2 * D;      // stored bytes of one K row
+  static constexpr int kRowBytesV = kQuant ? DV * BITS / 8 : 2 * DV;   // ... and of one V row
   static constexpr int kGroups = D / 64;
+  static constexpr int kGroupsV = DV / 64;
   // Rows per stage: 32 for affine pages when a stage stays within ~9.5 KB, else 16.
-  static constexpr int kCh = (kQuant && 2 * 32 * kRowBytes + 4 * 32 * kGroups * 2 <= 9728) ? 32 : 16;
-  static constexpr int kRB = kRowBytes >= 128 ? 128 : kRowBytes;   // bytes of one box row
+  static constexpr int kCh =
+      (kQuant && 32 * (kRowBytes + kRowBytesV) + 2 * 32 * (kGroups + kGroupsV) * 2 <= 9728) ? 32 : 16;
+  static constexpr int kRB = kRowBytes >= 128 ? 128 : kRowBytes;      // bytes of one box row
+  static constexpr int kRBV = kRowBytesV >= 128 ? 128 : kRowBytesV;
   static constexpr int kBoxes = kRowBytes / kRB;
+  static constexpr int kBoxesV = kRowBytesV / kRBV;
   static constexpr int kBoxBytes = kCh * kRB;
+  static constexpr int kBoxBytesV = kCh * kRBV;
   static constexpr int kPlaneBytes = kBoxes * kBoxBytes;
-  static constexpr int kSbBytes = kQuant ? kCh * kGroups * 2 : 0;  // one scale or bias plane
-  static constexpr int kTxBytes = 2 * kPlaneBytes + 4 * kSbBytes;
+  static constexpr int kPlaneBytesV = kBoxesV * kBoxBytesV;
+  static constexpr int kSbBytes = kQuant ? kCh * kGroups * 2 : 0;     // one K scale or bias plane
+  static constexpr int kSbBytesV = kQuant ? kCh * kGroupsV * 2 : 0;   // one V scale or bias plane
+  // stage layout: K rows, V rows, K scales, K biases, V scales, V biases
+  static constexpr int kOffV = kPlaneBytes;
+  static constexpr int kOffKs = kPlaneBytes + kPlaneBytesV;
+  static constexpr int kOffKb = kOffKs + kSbBytes;
+  static constexpr int kOffVs = kOffKb + kSbBytes;
+  static constexpr int kOffVb = kOffVs + kSbBytesV;
+  static constexpr int kTxBytes = kOffVb + kSbBytesV;
   static constexpr int kStageBytes = (kTxBytes + 1023) / 1024 * 1024;
   static constexpr int kBarrierBytes = SOLO ? 512 : 256;
   static constexpr int kSoloBudget = 227 * 1024 - kBarrierBytes - 1024;  // stage ring of a CTA alone on its SM
@@ -81,20 +97,21 @@ struct PartialCfg {
   static constexpr int kStagesPerGroup = kStagesPerWarp * WQ;  // each page group's private ring
   static constexpr int kNqp = 8 * NT;       // query rows per warp (padded)
   static constexpr int kNqAll = WQ * kNqp;  // query rows per CTA (padded)
-  static constexpr int kMt = D / 16;        // 16-dim m-tiles of O^T
+  static constexpr int kMt = DV / 16;       // 16-dim m-tiles of O^T
   static constexpr int kKs = D / 16;        // k16 steps of Q K^T
   static constexpr int kTiles = kCh / 16;   // 16-key tiles per stage
   // per-page-group states (m, l, o) for the in-CTA combine, then the CTA's own state for a cluster merge
-  static constexpr int kCombineBytes = (kWP + 1) * kNqAll * (D + 2) * 4;
+  static constexpr int kCombineBytes = (kWP + 1) * kNqAll * (DV + 2) * 4;
   static constexpr int kRingBytes = kWarps * kStagesPerWarp * kStageBytes;
   static constexpr int kDataBytes = kRingBytes > kCombineBytes ? kRingBytes : kCombineBytes;
   static constexpr int kSmemBytes = kDataBytes + kBarrierBytes + 1024;  // + alignment slack
   static constexpr float kCodeUnit = 5.9604644775390625e-8f;  // 2^-24: value of fp16 bit pattern 1
 
-  static_assert(kRB == 128 || kRB == 64, "box rows of 64 or 128 bytes");
-  static_assert(kRowBytes % kRB == 0, "whole boxes per row");
+  static_assert((kRB == 128 || kRB == 64) && (kRBV == 128 || kRBV == 64), "box rows of 64 or 128 bytes");
+  static_assert(kRowBytes % kRB == 0 && kRowBytesV % kRBV == 0, "whole boxes per row");
   static_assert(kWarps * kStagesPerWarp * 12 + 4 <= kBarrierBytes, "barrier area");
-  static_assert(!kQuant || D % 64 == 0, "affine head dims are whole 64-dim groups");
+  static_assert(!kQuant || (D % 64 == 0 && DV % 64 == 0), "affine head dims are whole 64-dim groups");
+  static_assert(DV % 64 == 0, "value head dims are whole 4-m-tile groups");
   static_assert(WQ == 1 || WQ == 2 || WQ == 4, "query groups of 1, 2 or 4 warps");
   static_assert(kStagesPerWarp >= 2, "at least two stages per warp");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory of one CTA");
@@ -170,11 +187,11 @@ __device__ __forceinline__ void load_group_row(uint32_t addr, float (&v)[G]) {
   }
 }
 
-template <int BITS, int D, int NT, int WQ, bool SOLO>
+template <int BITS, int D, int DV, int NT, int WQ, bool SOLO>
 __global__ void __maxnreg__(200)
     pkv_partial_kernel(const __grid_constant__ PartialParams p, const __grid_constant__ CUtensorMap tmap_k,
                        const __grid_constant__ CUtensorMap tmap_v) {
-  using C = PartialCfg<BITS, D, NT, WQ, SOLO>;
+  using C = PartialCfg<BITS, D, DV, NT, WQ, SOLO>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + C::kDataBytes);  // [warp][stage]
@@ -208,7 +225,7 @@ __global__ void __maxnreg__(200)
     // pass does.
     if (threadIdx.x == 0 && slot == 0 && p.error_flag) atomicOr(p.error_flag, kDevErrBadSeqLen);
     if (single || (in_cluster && slot == 0)) {
-      for (int i = threadIdx.x; i < p.nq * D; i += C::kThreads) p.out[row0 * D + i] = __float2bfloat16_rn(0.f);
+      for (int i = threadIdx.x; i < p.nq * DV; i += C::kThreads) p.out[row0 * DV + i] = __float2bfloat16_rn(0.f);
     }
     return;
   }
@@ -233,7 +250,7 @@ __global__ void __maxnreg__(200)
       if (static_cast<unsigned>(ph) >= static_cast<unsigned>(p.num_blocks)) continue;  // flagged by the read
       const size_t src = (static_cast<size_t>(b) * p.num_kv_heads + hk) * N + (tr - (len - N));
       const size_t row = (static_cast<size_t>(ph) * p.num_kv_heads + hk) * p.block_size + tr % p.block_size;
-      append_row<BITS, D>(p.k_new + src * D, p.v_new + src * D, p.app, row, lane);
+      append_row<BITS, D, DV>(p.k_new + src * D, p.v_new + src * DV, p.app, row, lane);
     }
     fence_proxy_async_global();
   }
@@ -250,7 +267,7 @@ __global__ void __maxnreg__(200)
   // O^T accumulators and softmax state.
   float o[C::kMt][NT][4];
   float m_run[NT][2], l_run[NT][2];
-  float corr_v[C::kQuant ? C::kGroups : 1][NT][2];
+  float corr_v[C::kQuant ? C::kGroupsV : 1][NT][2];
 
   {
     // ------------------------------------------------------------------ this warp's pipeline
@@ -299,18 +316,17 @@ __global__ void __maxnreg__(200)
           mbar_arrive_expect_tx(fb, C::kTxBytes);
           const uint32_t st = smem_addr(my_ring + is * C::kStageBytes);
 #pragma unroll
-          for (int bx = 0; bx < C::kBoxes; ++bx) {
-            const int x = bx * (C::kRB / C::kElemBytes);
-            tma_load_2d(st + bx * C::kBoxBytes, &tmap_k, x, row, fb, policy);
-            tma_load_2d(st + C::kPlaneBytes + bx * C::kBoxBytes, &tmap_v, x, row, fb, policy);
-          }
+          for (int bx = 0; bx < C::kBoxes; ++bx)
+            tma_load_2d(st + bx * C::kBoxBytes, &tmap_k, bx * (C::kRB / C::kElemBytes), row, fb, policy);
+#pragma unroll
+          for (int bx = 0; bx < C::kBoxesV; ++bx)
+            tma_load_2d(st + C::kOffV + bx * C::kBoxBytesV, &tmap_v, bx * (C::kRBV / C::kElemBytes), row, fb, policy);
           if constexpr (C::kQuant) {
-            const size_t so = static_cast<size_t>(row) * C::kGroups;
-            const uint32_t sb = st + 2 * C::kPlaneBytes;
-            bulk_load(sb, p.k_scales + so, C::kSbBytes, fb, policy);
-            bulk_load(sb + C::kSbBytes, p.k_biases + so, C::kSbBytes, fb, policy);
-            bulk_load(sb + 2 * C::kSbBytes, p.v_scales + so, C::kSbBytes, fb, policy);
-            bulk_load(sb + 3 * C::kSbBytes, p.v_biases + so, C::kSbBytes, fb, policy);
+            const size_t sk = static_cast<size_t>(row) * C::kGroups, sv = static_cast<size_t>(row) * C::kGroupsV;
+            bulk_load(st + C::kOffKs, p.k_scales + sk, C::kSbBytes, fb, policy);
+            bulk_load(st + C::kOffKb, p.k_biases + sk, C::kSbBytes, fb, policy);
+            bulk_load(st + C::kOffVs, p.v_scales + sv, C::kSbBytesV, fb, policy);
+            bulk_load(st + C::kOffVb, p.v_biases + sv, C::kSbBytesV, fb, policy);
           }
         } else {
           if (p.error_flag) atomicOr(p.error_flag, kDevErrBadBlock);
@@ -450,7 +466,7 @@ __global__ void __maxnreg__(200)
         m_run[nt][e2] = -INFINITY;
         l_run[nt][e2] = 0.f;
 #pragma unroll
-        for (int grp = 0; grp < (C::kQuant ? C::kGroups : 1); ++grp) corr_v[grp][nt][e2] = 0.f;
+        for (int grp = 0; grp < (C::kQuant ? C::kGroupsV : 1); ++grp) corr_v[grp][nt][e2] = 0.f;
       }
     }
 
@@ -468,8 +484,8 @@ __global__ void __maxnreg__(200)
       if (landed && my_ok[cs]) {
         uint8_t* stage = my_ring + cs * C::kStageBytes;
         const uint32_t kpl = smem_addr(stage);
-        const uint32_t vpl = kpl + C::kPlaneBytes;
-        const uint32_t sbq = kpl + 2 * C::kPlaneBytes;  // scale/bias planes (affine pages)
+        const uint32_t vpl = kpl + C::kOffV;
+        const uint32_t sbq = kpl + C::kOffKs;  // scale/bias planes (affine pages)
         const int kbase = chunk_row(done);
         const bool full_vis = kbase + C::kCh <= vis_base && (win == 0 || kbase >= vis_base + N - 1 - win);
         const bool stale = kbase + C::kCh > len;
@@ -501,7 +517,7 @@ __global__ void __maxnreg__(200)
               // bias MMA: this lane's A words are the biases of k slots 2t, 2t+1 (groups
               // 2t mod G, 2t mod G + 1) of keys g and g + 8
               uint32_t ba0 = 0u, ba1 = 0u;
-              const uint32_t kb = sbq + C::kSbBytes + (tile * 16 + g) * C::kGroups * 2;
+              const uint32_t kb = kpl + C::kOffKb + (tile * 16 + g) * C::kGroups * 2;
               if (C::kGroups == 4 || t < 2) {
                 const uint32_t off = C::kGroups == 4 ? (t & 1) * 4 : 0;
                 ba0 = ld_shared_u32(kb + off);
@@ -621,7 +637,7 @@ __global__ void __maxnreg__(200)
               for (int e = 0; e < 4; ++e) o[mt][nt][e] *= corr[nt][e & 1];
           if constexpr (C::kQuant) {
 #pragma unroll
-            for (int grp = 0; grp < C::kGroups; ++grp)
+            for (int grp = 0; grp < C::kGroupsV; ++grp)
 #pragma unroll
               for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -649,7 +665,7 @@ __global__ void __maxnreg__(200)
 #pragma unroll
             for (int mt = 0; mt < C::kMt; ++mt) {
               uint32_t a[4];
-              ldsm_x4_t(swizzled<C::kRB>(vpl + (mt >> 2) * C::kBoxBytes, lrow, (mt & 3) * 2 + lch_t), a);
+              ldsm_x4_t(swizzled<C::kRBV>(vpl + (mt >> 2) * C::kBoxBytesV, lrow, (mt & 3) * 2 + lch_t), a);
               a[0] &= m01;
               a[1] &= m01;
               a[2] &= m23;
@@ -659,15 +675,15 @@ __global__ void __maxnreg__(200)
             }
           } else {
             const int r_a = tile * 16 + g, r_b = r_a + 8;
-            float vs0[C::kGroups], vs1[C::kGroups], vb0[C::kGroups], vb1[C::kGroups];
-            load_group_row<C::kGroups>(sbq + 2 * C::kSbBytes + r_a * C::kGroups * 2, vs0);
-            load_group_row<C::kGroups>(sbq + 2 * C::kSbBytes + r_b * C::kGroups * 2, vs1);
-            load_group_row<C::kGroups>(sbq + 3 * C::kSbBytes + r_a * C::kGroups * 2, vb0);
-            load_group_row<C::kGroups>(sbq + 3 * C::kSbBytes + r_b * C::kGroups * 2, vb1);
+            float vs0[C::kGroupsV], vs1[C::kGroupsV], vb0[C::kGroupsV], vb1[C::kGroupsV];
+            load_group_row<C::kGroupsV>(kpl + C::kOffVs + r_a * C::kGroupsV * 2, vs0);
+            load_group_row<C::kGroupsV>(kpl + C::kOffVs + r_b * C::kGroupsV * 2, vs1);
+            load_group_row<C::kGroupsV>(kpl + C::kOffVb + r_a * C::kGroupsV * 2, vb0);
+            load_group_row<C::kGroupsV>(kpl + C::kOffVb + r_b * C::kGroupsV * 2, vb1);
             if (stale) {  // rows at or past len may hold anything: keep them out of P' and the bias sums
               const bool va = kbase + r_a < len, vb = kbase + r_b < len;
 #pragma unroll
-              for (int grp = 0; grp < C::kGroups; ++grp) {
+              for (int grp = 0; grp < C::kGroupsV; ++grp) {
                 vs0[grp] = va ? vs0[grp] : 0.f;
                 vb0[grp] = va ? vb0[grp] : 0.f;
                 vs1[grp] = vb ? vs1[grp] : 0.f;
@@ -675,7 +691,7 @@ __global__ void __maxnreg__(200)
               }
             }
 #pragma unroll
-            for (int grp = 0; grp < C::kGroups; ++grp) {
+            for (int grp = 0; grp < C::kGroupsV; ++grp) {
               uint32_t pb[NT][2];
 #pragma unroll
               for (int nt = 0; nt < NT; ++nt) {
@@ -688,7 +704,7 @@ __global__ void __maxnreg__(200)
                 // y: unit g (dims 4g..4g+3) of keys 2t (low half) and 2t+1 (high half),
                 // chunks 2 grp / 2 grp + 1, keys 0-7 / 8-15 of the tile
                 uint32_t y[4];
-                ldsm_x4_t(swizzled<C::kRB>(vpl, lrow, 2 * grp + lch_t), y);
+                ldsm_x4_t(swizzled<C::kRBV>(vpl, lrow, 2 * grp + lch_t), y);
                 uint32_t y8[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) y8[i] = y[i] >> 8;
@@ -707,7 +723,7 @@ __global__ void __maxnreg__(200)
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                   uint32_t y[4];
-                  ldsm_x4_t(swizzled<C::kRB>(vpl + (grp >> 1) * C::kBoxBytes, lrow, (grp & 1) * 4 + 2 * h + lch_t), y);
+                  ldsm_x4_t(swizzled<C::kRBV>(vpl + (grp >> 1) * C::kBoxBytesV, lrow, (grp & 1) * 4 + 2 * h + lch_t), y);
                   // byte 0 / byte 2 of y: dim 2g of keys 2t / 2t+1; bytes 1 / 3: dim 2g + 1
 #pragma unroll
                   for (int nt = 0; nt < NT; ++nt) {
@@ -754,7 +770,7 @@ __global__ void __maxnreg__(200)
         l_run[nt][e2] = l;
         if constexpr (C::kQuant) {
 #pragma unroll
-          for (int grp = 0; grp < C::kGroups; ++grp) {
+          for (int grp = 0; grp < C::kGroupsV; ++grp) {
             float cv = corr_v[grp][nt][e2];
             cv += __shfl_xor_sync(0xffffffffu, cv, 4);
             cv += __shfl_xor_sync(0xffffffffu, cv, 8);
@@ -782,7 +798,7 @@ __global__ void __maxnreg__(200)
   float* cm = reinterpret_cast<float*>(smem);
   float* cl = cm + C::kWP * C::kNqAll;
   float* co = cl + C::kWP * C::kNqAll;
-  float* st_m = co + C::kWP * C::kNqAll * D;  // this CTA's merged state (cluster merge)
+  float* st_m = co + C::kWP * C::kNqAll * DV;  // this CTA's merged state (cluster merge)
   float* st_l = st_m + C::kNqAll;
   float* st_o = st_l + C::kNqAll;
   if (warp < C::kWarps) {
@@ -803,13 +819,13 @@ __global__ void __maxnreg__(200)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int r = 8 * nt + 2 * t + (e & 1);
-          co[(pg * C::kNqAll + rbase + r) * D + out_dim<BITS>(mt, e >> 1, g)] = o[mt][nt][e];
+          co[(pg * C::kNqAll + rbase + r) * DV + out_dim<BITS>(mt, e >> 1, g)] = o[mt][nt][e];
         }
   }
   __syncthreads();
 
-  for (int idx = threadIdx.x; idx < p.nq * D; idx += C::kThreads) {
-    const int r = idx / D, d = idx % D;
+  for (int idx = threadIdx.x; idx < p.nq * DV; idx += C::kThreads) {
+    const int r = idx / DV, d = idx % DV;
     float M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < C::kWP; ++w) M = fmaxf(M, cm[w * C::kNqAll + r]);
@@ -821,22 +837,22 @@ __global__ void __maxnreg__(200)
         if (mw != -INFINITY) {
           const float wt = fast_exp2(mw - M);
           L = fmaf(wt, cl[w * C::kNqAll + r], L);
-          O = fmaf(wt, co[(w * C::kNqAll + r) * D + d], O);
+          O = fmaf(wt, co[(w * C::kNqAll + r) * DV + d], O);
         }
       }
     }
     const size_t orow = row0 + r;
     if (single) {
-      p.out[orow * D + d] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
+      p.out[orow * DV + d] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
     } else if (in_cluster) {
-      st_o[r * D + d] = O;
+      st_o[r * DV + d] = O;
       if (d == 0) {
         st_m[r] = M;
         st_l[r] = L;
       }
     } else {
       const size_t ws = orow * p.max_partitions + slot;
-      p.ws_o[ws * D + d] = O;
+      p.ws_o[ws * DV + d] = O;
       if (d == 0) {
         p.ws_ml[ws * 2] = M;
         p.ws_ml[ws * 2 + 1] = L;
@@ -850,11 +866,11 @@ __global__ void __maxnreg__(200)
     // slice of the (row, dim) outputs.
     cluster_sync();
     const int cs = p.max_partitions;
-    const int total = p.nq * D;
+    const int total = p.nq * DV;
     const int per = (total + cs - 1) / cs;
     const int end = min(total, (slot + 1) * per);
     for (int idx = slot * per + threadIdx.x; idx < end; idx += C::kThreads) {
-      const int r = idx / D, d = idx % D;
+      const int r = idx / DV, d = idx % DV;
       // every member's (m, l, o) for this output, all remote loads in flight together
       float mj[kMaxClusterParts], lj[kMaxClusterParts], oj[kMaxClusterParts];
 #pragma unroll
@@ -864,7 +880,7 @@ __global__ void __maxnreg__(200)
         if (j < cs) {
           mj[j] = ld_cluster_f32(smem_addr(&st_m[r]), j);
           lj[j] = ld_cluster_f32(smem_addr(&st_l[r]), j);
-          oj[j] = ld_cluster_f32(smem_addr(&st_o[r * D + d]), j);
+          oj[j] = ld_cluster_f32(smem_addr(&st_o[r * DV + d]), j);
         }
       }
       float M = -INFINITY;
@@ -880,7 +896,7 @@ __global__ void __maxnreg__(200)
           O = fmaf(wt, oj[j], O);
         }
       }
-      p.out[(row0 + r) * D + d] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
+      p.out[(row0 + r) * DV + d] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
     }
     cluster_sync();  // no CTA leaves while another still reads its shared memory
   }

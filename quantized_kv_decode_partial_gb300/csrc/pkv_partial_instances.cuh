@@ -10,36 +10,36 @@
 namespace pkv {
 namespace {
 
-template <int BITS, int D, int NT, int WQ, bool SOLO>
+template <int BITS, int D, int DV, int NT, int WQ, bool SOLO>
 PartialInfo info_of() {
-  using C = PartialCfg<BITS, D, NT, WQ, SOLO>;
-  return PartialInfo{true, C::kThreads, C::kSmemBytes, C::kCh, C::kRB, C::kElemBytes};
+  using C = PartialCfg<BITS, D, DV, NT, WQ, SOLO>;
+  return PartialInfo{true, C::kThreads, C::kSmemBytes, C::kCh, C::kRB, C::kRBV, C::kElemBytes};
 }
 
 // Devices on which an instantiation's function attributes are set (bit per device < 64).
-template <int BITS, int D, int NT, int WQ, bool SOLO>
+template <int BITS, int D, int DV, int NT, int WQ, bool SOLO>
 std::atomic<unsigned long long> g_configured{0};
 
-template <int BITS, int D, int NT, int WQ, bool SOLO>
+template <int BITS, int D, int DV, int NT, int WQ, bool SOLO>
 cudaError_t configure_once(int device) {
-  using C = PartialCfg<BITS, D, NT, WQ, SOLO>;
-  auto kern = pkv_partial_kernel<BITS, D, NT, WQ, SOLO>;
+  using C = PartialCfg<BITS, D, DV, NT, WQ, SOLO>;
+  auto kern = pkv_partial_kernel<BITS, D, DV, NT, WQ, SOLO>;
   const unsigned long long bit = device >= 0 && device < 64 ? (1ull << device) : 0ull;
-  if (bit && (g_configured<BITS, D, NT, WQ, SOLO>.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  if (bit && (g_configured<BITS, D, DV, NT, WQ, SOLO>.load(std::memory_order_acquire) & bit)) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);  // clusters of up to 16
   if (e != cudaSuccess) return e;
-  if (bit) g_configured<BITS, D, NT, WQ, SOLO>.fetch_or(bit, std::memory_order_acq_rel);
+  if (bit) g_configured<BITS, D, DV, NT, WQ, SOLO>.fetch_or(bit, std::memory_order_acq_rel);
   return cudaSuccess;
 }
 
-template <int BITS, int D, int NT, int WQ, bool SOLO>
+template <int BITS, int D, int DV, int NT, int WQ, bool SOLO>
 cudaError_t launch_of(const PartialParams& p, const CUtensorMap& tk, const CUtensorMap& tv, dim3 grid,
                       cudaStream_t stream, int device) {
-  using C = PartialCfg<BITS, D, NT, WQ, SOLO>;
-  auto kern = pkv_partial_kernel<BITS, D, NT, WQ, SOLO>;
-  cudaError_t e = configure_once<BITS, D, NT, WQ, SOLO>(device);
+  using C = PartialCfg<BITS, D, DV, NT, WQ, SOLO>;
+  auto kern = pkv_partial_kernel<BITS, D, DV, NT, WQ, SOLO>;
+  cudaError_t e = configure_once<BITS, D, DV, NT, WQ, SOLO>(device);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = grid;
@@ -59,19 +59,22 @@ cudaError_t launch_of(const PartialParams& p, const CUtensorMap& tk, const CUten
 }
 
 // Instantiation for `nq` query rows per KV head: NT n-tiles of 8 rows per warp and
-// WQ warps per query group (NT * WQ * 8 >= nq), or (0, 0) when unsupported.
-inline void tiles_for(int head_dim, int nq, int& nt, int& wq) {
+// WQ warps per query group (NT * WQ * 8 >= nq), or (0, 0) when unsupported. A warp
+// holds NT * (dv/4 + dk/8) registers of accumulators and query fragments; NT is the
+// largest of 1, 2, 4 that keeps them within the 96 of a 256-dim head at NT = 1.
+inline void tiles_for(int dk, int dv, int nq, int& nt, int& wq) {
   nt = wq = 0;
   if (nq < 1) return;
+  const int per_tile = dv / 4 + dk / 8;
+  const int nt_max = 96 / per_tile >= 4 ? 4 : 96 / per_tile >= 2 ? 2 : 1;
   const int ntiles = (nq + 7) / 8;
-  const int nt_max = 256 / head_dim;  // accumulator registers: head_dim * NT / 32 per thread
   if (ntiles <= nt_max) {
     nt = ntiles <= 1 ? 1 : ntiles <= 2 ? 2 : 4;
     wq = 1;
   } else if (ntiles <= 2 * nt_max) {
     nt = nt_max;
     wq = 2;
-  } else if (ntiles <= 4 * nt_max && head_dim >= 128) {
+  } else if (ntiles <= 4 * nt_max && (dk >= 128 || dv >= 128)) {
     nt = nt_max;
     wq = 4;
   }

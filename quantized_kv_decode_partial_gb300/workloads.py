@@ -153,6 +153,12 @@ WORKLOADS = {
         partition_tokens=0, seed=1006,
         description="sliding-window few-query paged decode: the long-context workload with an 8192-row "
                     "window (each query sees its 8192 most recent rows)"),
+    "bf16_batch32_hq32_dk192_dv128": DecodeSpec(
+        name="bf16_batch32_hq32_dk192_dv128", num_seqs=32, num_q_heads=32, num_kv_heads=8, head_dim=192,
+        v_head_dim=128, n_query=1, block_size=16, bits=16, length_range=(512, 16384), pool_factor=1.1,
+        partition_tokens=0, seed=1007,
+        description="bf16 paged decode batch with key head dim 192 and value head dim 128: 32 sequences x "
+                    "1 query, lengths U[512,16384], HQ=32 HK=8, BS=16, shared pool +10% free blocks"),
 }
 
 # The two layers of the affine batch workload form one decode step.

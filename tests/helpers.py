@@ -96,7 +96,7 @@ def subcase(case: DecodeCase, b: int, kv: int) -> DecodeCase:
 
     sub_spec = DecodeSpec(name=s.name + f"_b{b}_kv{kv}", num_seqs=1, num_q_heads=rep, num_kv_heads=1,
                           head_dim=s.head_dim, n_query=s.n_query, block_size=s.block_size, bits=s.bits,
-                          group_size=s.group_size, lengths=(L,), window=s.window)
+                          group_size=s.group_size, lengths=(L,), window=s.window, v_head_dim=s.v_head_dim)
     return DecodeCase(
         spec=sub_spec, q=case.q[b:b + 1, kv * rep:(kv + 1) * rep].contiguous().cpu(),
         k_pool=pick(case.k_pool), v_pool=pick(case.v_pool),

@@ -46,7 +46,8 @@ def test_version_and_messages(lib):
 
 
 def _layout(spec, num_blocks=1000):
-    return B.PoolLayout(num_blocks, spec.num_kv_heads, spec.block_size, spec.head_dim, spec.bits, spec.group_size)
+    return B.PoolLayout(num_blocks, spec.num_kv_heads, spec.block_size, spec.head_dim, spec.bits, spec.group_size,
+                        spec.v_head_dim)
 
 
 def _params(spec, max_blocks, partition=None):
@@ -83,13 +84,13 @@ def test_plan_for_workloads(lib, name):
         assert plan.workspace_bytes == 0
     else:
         slots = sp.num_seqs * sp.num_q_heads * sp.n_query * plan.max_partitions
-        assert plan.workspace_bytes >= slots * (sp.head_dim + 2) * 4
+        assert plan.workspace_bytes >= slots * (sp.dv + 2) * 4
         # auto plans: never below 256 rows; either about four waves of 2 CTAs per SM, or at least one
         # wave of CTAs that each still get 512 KB of K/V, or the 256-row floor
         if sp.partition_tokens == 0:
             assert plan.partition_tokens >= 256
             ctas = sp.num_seqs * sp.num_kv_heads * plan.max_partitions
-            kv_row = 2 * (2 * sp.head_dim if sp.bits == 16 else sp.head_dim * sp.bits // 8 + sp.head_dim // 16)
+            kv_row = sum(2 * d if sp.bits == 16 else d * sp.bits // 8 + d // 16 for d in (sp.head_dim, sp.dv))
             assert (ctas >= 8 * 152 or plan.partition_tokens == 256
                     or (ctas >= 2 * 152 and plan.partition_tokens // 2 < (512 << 10) // kv_row))
     assert plan.threads_per_cta in (128, 256) and 0 < plan.smem_bytes <= 227 * 1024
@@ -128,6 +129,34 @@ def test_query_rows_per_kv_head_limits(lib, bits, head_dim, max_rows):
         plan = B.Plan()
         rc = lib.pkv_make_plan(ctypes.byref(lay), ctypes.byref(par), 152, ctypes.byref(plan))
         assert rc == (B.PKV_OK if nq <= max_rows else B.PKV_ERR_UNSUPPORTED_SHAPE), (nq, rc)
+
+
+@pytest.mark.parametrize("bits,dk,dv,max_rows", [(16, 192, 128, 32), (16, 256, 128, 8), (16, 128, 256, 8),
+                                                  (4, 256, 128, 8), (4, 128, 256, 8), (8, 256, 128, 8),
+                                                  (8, 128, 256, 8)])
+def test_key_and_value_head_dims_may_differ(lib, bits, dk, dv, max_rows):
+    for nq in (1, 8, 9, 32, 33):
+        lay = B.PoolLayout(100, 2, 32, dk, bits, 64, dv)
+        par = B.DecodeParams(1, 2 * nq, 1, 4, 64, 0)
+        plan = B.Plan()
+        rc = lib.pkv_make_plan(ctypes.byref(lay), ctypes.byref(par), 1, ctypes.byref(plan))  # 1 SM: no cluster
+        assert rc == (B.PKV_OK if nq <= max_rows else B.PKV_ERR_UNSUPPORTED_SHAPE), (nq, rc)
+        if rc == B.PKV_OK:  # partition states hold value-dim rows: 2 partitions x 2 nq query heads
+            slots = 2 * 2 * nq
+            assert plan.max_partitions == 2 and plan.merge_in_cluster == 0
+            assert plan.workspace_bytes == -(-slots * dv * 4 // 256) * 256 + slots * 2 * 4
+
+
+@pytest.mark.parametrize("bits,dk,dv,code", [(16, 64, 128, B.PKV_ERR_UNSUPPORTED_SHAPE),
+                                             (16, 192, 192, B.PKV_ERR_BAD_LAYOUT),
+                                             (16, 128, 96, B.PKV_ERR_BAD_LAYOUT),
+                                             (4, 192, 128, B.PKV_ERR_BAD_LAYOUT),
+                                             (8, 256, 64, B.PKV_ERR_BAD_LAYOUT)])
+def test_head_dim_pairs_without_a_kernel_are_rejected(lib, bits, dk, dv, code):
+    lay = B.PoolLayout(100, 1, 32, dk, bits, 64, dv)
+    plan = B.Plan()
+    assert lib.pkv_make_plan(ctypes.byref(lay), ctypes.byref(B.DecodeParams(1, 4, 1, 4, 0, 0)), 152,
+                             ctypes.byref(plan)) == code
 
 
 def test_plan_auto_is_monotone_in_sm_count(lib):

@@ -26,29 +26,31 @@ def bits_of(t):
     return t.detach().cpu().numpy()
 
 
-def setup(bits, D, n_new, num_seqs=3, seed_name=""):
-    name = f"app_{bits}_{D}_{n_new}_{seed_name}"
+def setup(bits, D, n_new, num_seqs=3, seed_name="", dv=0):
+    name = f"app_{bits}_{D}_{n_new}_{seed_name}" + (f"_dv{dv}" if dv else "")
     seed = zlib.crc32(name.encode()) % 10000
     bs = 16 if bits == 16 else 32
+    DV = dv or D
     sp = DecodeSpec(name=name, num_seqs=num_seqs, num_q_heads=4, num_kv_heads=2, head_dim=D, n_query=1,
-                    block_size=bs, bits=bits, length_range=(1, 150), pool_factor=2.0, seed=seed)
+                    block_size=bs, bits=bits, length_range=(1, 150), pool_factor=2.0, seed=seed, v_head_dim=dv)
     g = torch.Generator().manual_seed(seed + 1)
     lens = [int(x) for x in torch.randint(0, 150, (num_seqs,), generator=g)]
     lens[0] = bs - 1  # the new rows of sequence 0 cross a page boundary
     case = make_case(sp, lengths=[l + n_new for l in lens], poison=False)  # tables hold the new rows' pages
     # new rows with very different ranges per group (including a constant group)
     k_new = torch.randn((num_seqs, 2, n_new, D), generator=g) * torch.rand((num_seqs, 2, n_new, D // 16), generator=g).repeat_interleave(16, -1) * 8
-    v_new = torch.randn((num_seqs, 2, n_new, D), generator=g)
+    v_new = torch.randn((num_seqs, 2, n_new, DV), generator=g)
     k_new[..., :64] = k_new[..., :1]
     return sp, case, lens, k_new.to(torch.bfloat16), v_new.to(torch.bfloat16)
 
 
-CASES = [(16, 128, 1), (16, 64, 3), (16, 256, 2), (4, 256, 1), (4, 128, 3), (8, 256, 2), (8, 128, 1)]
+CASES = [(16, 128, 1, 0), (16, 64, 3, 0), (16, 256, 2, 0), (4, 256, 1, 0), (4, 128, 3, 0), (8, 256, 2, 0),
+         (8, 128, 1, 0), (16, 192, 2, 128), (4, 128, 2, 256), (8, 256, 1, 128)]
 
 
-@pytest.mark.parametrize("bits,D,n_new", CASES)
-def test_append_is_bit_exact(bits, D, n_new):
-    sp, case, lens, k_new, v_new = setup(bits, D, n_new)
+@pytest.mark.parametrize("bits,D,n_new,dv", CASES)
+def test_append_is_bit_exact(bits, D, n_new, dv):
+    sp, case, lens, k_new, v_new = setup(bits, D, n_new, dv=dv)
     ref = pw.append_rows(k_new.float().numpy(), v_new.float().numpy(), case.block_tables.numpy(), lens,
                          bits_of(case.k_pool), bits_of(case.v_pool), bits=bits,
                          k_scales=bits_of(case.k_scales), k_biases=bits_of(case.k_biases),
@@ -104,39 +106,42 @@ def test_append_flags_bad_blocks_and_lengths():
 
 # ---------------------------------------------------------------- fused append + attend
 
-def setup_fused(bits, D, N, hq, hk, seed_name, num_seqs=3, length_range=(1, 300), window=0):
-    name = f"fused_{bits}_{D}_{N}_{hq}_{seed_name}"
+def setup_fused(bits, D, N, hq, hk, seed_name, num_seqs=3, length_range=(1, 300), window=0, dv=0):
+    name = f"fused_{bits}_{D}_{N}_{hq}_{seed_name}" + (f"_dv{dv}" if dv else "")
     seed = zlib.crc32(name.encode()) % 10000
     bs = 16 if bits == 16 else 32
     g = torch.Generator().manual_seed(seed + 1)
     lens = [int(x) for x in torch.randint(*length_range, (num_seqs,), generator=g)]
     lens[0] = bs - 1  # the new rows of sequence 0 cross a page boundary
     sp = DecodeSpec(name=name, num_seqs=num_seqs, num_q_heads=hq, num_kv_heads=hk, head_dim=D, n_query=N,
-                    block_size=bs, bits=bits, length_range=length_range, pool_factor=2.0, seed=seed, window=window)
+                    block_size=bs, bits=bits, length_range=length_range, pool_factor=2.0, seed=seed, window=window,
+                    v_head_dim=dv)
     case = make_case(sp, lengths=[l + N for l in lens], poison=False)  # seq_lens count the new rows
     k_new = (torch.randn((num_seqs, hk, N, D), generator=g) * 3).to(torch.bfloat16)
-    v_new = torch.randn((num_seqs, hk, N, D), generator=g).to(torch.bfloat16)
+    v_new = torch.randn((num_seqs, hk, N, dv or D), generator=g).to(torch.bfloat16)
     return sp, case, lens, k_new, v_new
 
 
 FUSED = [
-    # bits, D, N, HQ, HK, partition_tokens (-1 single, 0 auto), window
-    (16, 128, 1, 8, 2, -1, 0),
-    (16, 128, 4, 8, 2, 32, 0),
-    (16, 256, 2, 4, 2, 64, 0),
-    (16, 64, 3, 8, 1, 48, 0),
-    (4, 256, 2, 8, 2, 64, 0),
-    (4, 128, 1, 4, 1, 0, 0),
-    (8, 128, 3, 8, 2, 32, 0),
-    (8, 256, 1, 8, 2, -1, 0),
-    (16, 128, 4, 8, 2, 32, 40),
+    # bits, D, N, HQ, HK, partition_tokens (-1 single, 0 auto), window, value head dim (0: D)
+    (16, 128, 1, 8, 2, -1, 0, 0),
+    (16, 128, 4, 8, 2, 32, 0, 0),
+    (16, 256, 2, 4, 2, 64, 0, 0),
+    (16, 64, 3, 8, 1, 48, 0, 0),
+    (4, 256, 2, 8, 2, 64, 0, 0),
+    (4, 128, 1, 4, 1, 0, 0, 0),
+    (8, 128, 3, 8, 2, 32, 0, 0),
+    (8, 256, 1, 8, 2, -1, 0, 0),
+    (16, 128, 4, 8, 2, 32, 40, 0),
+    (16, 192, 2, 8, 2, 32, 0, 128),
+    (4, 256, 1, 8, 2, 64, 0, 128),
 ]
 
 
-@pytest.mark.parametrize("bits,D,N,hq,hk,part,window", FUSED,
-                         ids=[f"b{c[0]}_d{c[1]}_n{c[2]}_p{c[5]}_w{c[6]}" for c in FUSED])
-def test_fused_append_attend_matches_append_then_decode(bits, D, N, hq, hk, part, window):
-    sp, case, lens, k_new, v_new = setup_fused(bits, D, N, hq, hk, f"p{part}w{window}", window=window)
+@pytest.mark.parametrize("bits,D,N,hq,hk,part,window,dv", FUSED,
+                         ids=[f"b{c[0]}_d{c[1]}_n{c[2]}_p{c[5]}_w{c[6]}_v{c[7]}" for c in FUSED])
+def test_fused_append_attend_matches_append_then_decode(bits, D, N, hq, hk, part, window, dv):
+    sp, case, lens, k_new, v_new = setup_fused(bits, D, N, hq, hk, f"p{part}w{window}", window=window, dv=dv)
     part = 1 << 20 if part < 0 else part  # one partition: any size past the table
     # the write oracle's pools, then the attention oracle over them
     ref = pw.append_rows(k_new.float().numpy(), v_new.float().numpy(), case.block_tables.numpy(), lens,

@@ -63,6 +63,20 @@ SMALL = [
           length_range=(2, 400)), [-1, 64]),
     (spec("u8_d128_nq32", num_q_heads=32, num_kv_heads=1, head_dim=128, bits=8, block_size=32,
           length_range=(1, 400)), [-1, 32]),
+    # key and value head dims that differ (the pages' vHeadDim)
+    (spec("bf16_dk192_dv128_nq4", head_dim=192, v_head_dim=128), [-1, 32, 0]),
+    (spec("bf16_dk192_dv128_nq16_n2", num_q_heads=16, head_dim=192, v_head_dim=128, n_query=2,
+          length_range=(2, 400)), [-1, 64]),
+    (spec("bf16_dk192_dv128_nq32", num_q_heads=32, num_kv_heads=1, head_dim=192, v_head_dim=128,
+          length_range=(1, 400)), [-1, 48]),
+    (spec("bf16_dk256_dv128", head_dim=256, v_head_dim=128, length_range=(1, 400)), [-1, 64]),
+    (spec("bf16_dk128_dv256_n2", num_q_heads=4, head_dim=128, v_head_dim=256, n_query=2,
+          length_range=(2, 400)), [-1, 64]),
+    (spec("u4_dk256_dv128", head_dim=256, v_head_dim=128, bits=4, block_size=32, length_range=(1, 500)), [-1, 64]),
+    (spec("u4_dk128_dv256", head_dim=128, v_head_dim=256, bits=4, block_size=32, length_range=(1, 500)), [-1, 96]),
+    (spec("u8_dk256_dv128", head_dim=256, v_head_dim=128, bits=8, block_size=32, length_range=(1, 500)), [-1, 32]),
+    (spec("u8_dk128_dv256_n2", num_q_heads=4, head_dim=128, v_head_dim=256, bits=8, n_query=2, block_size=32,
+          length_range=(2, 500)), [-1, 64]),
 ]
 
 
@@ -83,18 +97,19 @@ def test_small_cases_match_oracle(sp, parts):
 # The small cases above launch at most one CTA per SM for up to 8 query rows per KV head,
 # which takes the eight-warp variant; these grids of more than one CTA per SM take the
 # four-warp one for the same shapes.
-BIG_GRID = [(16, 64), (16, 128), (16, 256), (4, 128), (4, 256), (8, 128), (8, 256)]
+BIG_GRID = [(16, 64, 0), (16, 128, 0), (16, 256, 0), (4, 128, 0), (4, 256, 0), (8, 128, 0), (8, 256, 0),
+            (16, 192, 128)]
 
 
-@pytest.mark.parametrize("bits,D", BIG_GRID, ids=[f"b{b}_d{d}" for b, d in BIG_GRID])
-def test_grids_of_several_ctas_per_sm_match_oracle(bits, D):
-    sp = spec(f"big_grid_{bits}_{D}", num_seqs=44, num_q_heads=16, num_kv_heads=4, head_dim=D, bits=bits,
-              block_size=16 if bits == 16 else 32, length_range=(1, 260))
+@pytest.mark.parametrize("bits,D,DV", BIG_GRID, ids=[f"b{b}_d{d}_{v}" for b, d, v in BIG_GRID])
+def test_grids_of_several_ctas_per_sm_match_oracle(bits, D, DV):
+    sp = spec(f"big_grid_{bits}_{D}_{DV}", num_seqs=44, num_q_heads=16, num_kv_heads=4, head_dim=D, v_head_dim=DV,
+              bits=bits, block_size=16 if bits == 16 else 32, length_range=(1, 260))
     case = make_case(sp)
     ref = oracle_out(case)
     dcase = case.to(DEV)
     for pt in (max(case.lens_host) + 64, 32):
-        plan = B.make_plan(B.layout_for(case.k_pool, D, bits),
+        plan = B.make_plan(B.layout_for(case.k_pool, D, bits, v_pool=case.v_pool),
                            B.DecodeParams(sp.num_seqs, 16, 1, case.block_tables.shape[1], pt))
         assert plan.threads_per_cta == 128
         err = torch.zeros(1, dtype=torch.int32, device=DEV)
@@ -155,7 +170,7 @@ def test_partitioned_oracle_agrees_with_gpu_partitions():
 
 FULL = ["bf16_1x1024_hq2_d256", "affine4_g64_1x8192_hq16_d256", "bf16_batch32_hq32_d128",
         "affine4_batch64_hq32_d256", "affine8_batch64_hq32_d256", "bf16_8x131072_n4_hq32_d128",
-        "bf16_8x131072_n4_w8192_hq32_d128"]
+        "bf16_8x131072_n4_w8192_hq32_d128", "bf16_batch32_hq32_dk192_dv128"]
 
 
 @pytest.mark.parametrize("name", FULL)
