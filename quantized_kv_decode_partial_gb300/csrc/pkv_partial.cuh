@@ -100,8 +100,12 @@ struct PartialCfg {
   static constexpr int kMt = DV / 16;       // 16-dim m-tiles of O^T
   static constexpr int kKs = D / 16;        // k16 steps of Q K^T
   static constexpr int kTiles = kCh / 16;   // 16-key tiles per stage
+  // Row stride (floats) of the per-page-group outputs in the combine area: padded so a
+  // warp's stores of one accumulator register spread over the banks (conflict-free for
+  // bf16 pages, two lanes per bank for affine pages).
+  static constexpr int kCoStride = DV + (BITS == 4 ? 1 : 4);
   // per-page-group states (m, l, o) for the in-CTA combine, then the CTA's own state for a cluster merge
-  static constexpr int kCombineBytes = (kWP + 1) * kNqAll * (DV + 2) * 4;
+  static constexpr int kCombineBytes = (kWP * kNqAll * (kCoStride + 2) + kNqAll * (DV + 2)) * 4;
   static constexpr int kRingBytes = kWarps * kStagesPerWarp * kStageBytes;
   static constexpr int kDataBytes = kRingBytes > kCombineBytes ? kRingBytes : kCombineBytes;
   static constexpr int kSmemBytes = kDataBytes + kBarrierBytes + 1024;  // + alignment slack
@@ -148,6 +152,52 @@ __device__ __forceinline__ void q_dims(int kk, int reg, int t, int& d_lo, int& d
     const int base = 64 * grp + 16 * c + 4 * t + reg;
     d_lo = base;
     d_hi = base + 2;
+  }
+}
+
+// Loads the query values one lane needs from row `qrow` (D bf16 values) as 2 * D/16
+// words of bf16 pairs, with vector loads of the contiguous runs q_dims addresses
+// (zeros when !valid): bf16 pages take a word per (k-step, register); 4-bit pages 16
+// bytes per 32-dim half group; 8-bit pages 8 bytes per 16-dim quarter group.
+template <int BITS, int D>
+__device__ __forceinline__ void q_load_words(const __nv_bfloat16* qrow, int t, bool valid, uint32_t (&w)[D / 8]) {
+  if constexpr (BITS == 16) {
+#pragma unroll
+    for (int i = 0; i < D / 8; ++i) {  // i = 2 kk + reg: dims 16 kk + 8 reg + 2t, +1
+      w[i] = valid ? __ldg(reinterpret_cast<const uint32_t*>(qrow + 8 * i + 2 * t)) : 0u;
+    }
+  } else if constexpr (BITS == 4) {
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {  // c = 2 grp + cc: dims 32 c + 8t .. + 7
+      const uint4 v = valid ? __ldg(reinterpret_cast<const uint4*>(qrow + 32 * c + 8 * t)) : make_uint4(0, 0, 0, 0);
+      w[4 * c] = v.x;
+      w[4 * c + 1] = v.y;
+      w[4 * c + 2] = v.z;
+      w[4 * c + 3] = v.w;
+    }
+  } else {
+#pragma unroll
+    for (int c = 0; c < D / 16; ++c) {  // c = 4 grp + quarter: dims 16 c + 4t .. + 3
+      const uint2 v = valid ? __ldg(reinterpret_cast<const uint2*>(qrow + 16 * c + 4 * t)) : make_uint2(0, 0);
+      w[2 * c] = v.x;
+      w[2 * c + 1] = v.y;
+    }
+  }
+}
+
+// The bf16 pair (dims d_lo, d_hi of q_dims(kk, reg)) from the words of q_load_words.
+template <int BITS, int W>
+__device__ __forceinline__ uint32_t q_pair(const uint32_t (&w)[W], int kk, int reg) {
+  if constexpr (BITS == 16) {
+    return w[2 * kk + reg];
+  } else if constexpr (BITS == 4) {
+    // 16-byte run c = kk/2 holds dims base..base+7 as words of pairs; the lane needs
+    // elements j = (kk & 1) + 2 reg and j + 4
+    const int c = kk >> 1, j = (kk & 1) + 2 * reg;
+    return __byte_perm(w[4 * c + (j >> 1)], w[4 * c + 2 + (j >> 1)], (j & 1) ? 0x7632 : 0x5410);
+  } else {
+    // 8-byte run kk holds dims base..base+3; the lane needs elements reg and reg + 2
+    return __byte_perm(w[2 * kk], w[2 * kk + 1], reg ? 0x7632 : 0x5410);
   }
 }
 
@@ -210,6 +260,15 @@ __global__ void __maxnreg__(200)
   const bool single = p.mode == kModeSingle;
   const bool in_cluster = p.mode == kModeCluster;
   const int len = p.seq_lens[b];
+  // This lane's query values, fetched now so their latency overlaps the length's:
+  // 2 * kKs words of bf16 pairs per n-tile, in the order q_load_words reads them.
+  uint32_t qw[NT][2 * C::kKs];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int r = rbase + 8 * nt + g;
+    const __nv_bfloat16* qrow = p.q + (row0 + (r < p.nq ? r : 0)) * D;
+    q_load_words<BITS, D>(qrow, t, r < p.nq, qw[nt]);
+  }
   // Without a window the partition (and so this warp's first 32 chunks) does not
   // depend on len: fetch their block-table entries while len is still in flight.
   int tbl_pre = 0;
@@ -240,20 +299,6 @@ __global__ void __maxnreg__(200)
   // first row this CTA reads: the partition start, or the chunk holding the window's lowest row
   const int t_first = max(t0, win_lo / C::kCh * C::kCh);
   const int nchunks = empty ? 0 : (t_end - t_first + C::kCh - 1) / C::kCh;  // an empty cluster member still merges
-
-  if (p.k_new != nullptr && !empty) {
-    // Fused append: write the step's new rows len-N .. len-1 that fall in this
-    // partition (one warp per row), then make them visible to the TMA reads below.
-    const int32_t* table = p.block_tables + static_cast<size_t>(b) * p.max_blocks;
-    for (int tr = max(len - N, t0) + warp; tr < t_end; tr += C::kWarps) {
-      const int ph = __ldg(table + tr / p.block_size);
-      if (static_cast<unsigned>(ph) >= static_cast<unsigned>(p.num_blocks)) continue;  // flagged by the read
-      const size_t src = (static_cast<size_t>(b) * p.num_kv_heads + hk) * N + (tr - (len - N));
-      const size_t row = (static_cast<size_t>(ph) * p.num_kv_heads + hk) * p.block_size + tr % p.block_size;
-      append_row<BITS, D, DV>(p.k_new + src * D, p.v_new + src * DV, p.app, row, lane);
-    }
-    fence_proxy_async_global();
-  }
 
   if (threadIdx.x == 0) {
     prefetch_tensormap(&tmap_k);  // the first copies need both descriptors
@@ -308,6 +353,23 @@ __global__ void __maxnreg__(200)
         tbl_next = k < my_chunks ? __ldg(table + chunk_row(k) / p.block_size) : 0;
       }
       const int row = __shfl_sync(0xffffffffu, crd_cur, issued & 31);
+      if (p.k_new != nullptr) {
+        // Fused append: the step's new rows len-N .. len-1 that fall in this chunk are
+        // written into its page first (the warp writes, fences its generic-proxy stores
+        // against the async proxy, then lane 0 copies the chunk). Chunks lie inside one
+        // partition and one block, so no other CTA or warp reads these rows.
+        const int cr = chunk_row(issued);
+        const int a0 = max(len - N, cr), a1 = min(len, cr + C::kCh);
+        if (a0 < a1 && row >= 0) {
+          for (int tr = a0; tr < a1; ++tr) {
+            const size_t src = (static_cast<size_t>(b) * p.num_kv_heads + hk) * N + (tr - (len - N));
+            append_row<BITS, D, DV>(p.k_new + src * D, p.v_new + src * DV, p.app, static_cast<size_t>(row) + (tr - cr),
+                                    lane);
+          }
+          fence_proxy_async_global();
+          __syncwarp();
+        }
+      }
       if (lane == 0) {
         const uint32_t fb = smem_addr(&my_full[is]);
         my_ok[is] = row >= 0 ? 1 : 0;
@@ -349,27 +411,14 @@ __global__ void __maxnreg__(200)
     uint32_t qsb[C::kQuant ? NT : 1];
     {
       float qsum[C::kQuant ? C::kGroups : 1][NT][2];  // affine: 2^-24 * sum of prescaled q over each group
-      const uint16_t* qrows = reinterpret_cast<const uint16_t*>(p.q) + row0 * D;
       float qv[C::kKs][NT][4];
 #pragma unroll
-      for (int kk = 0; kk < C::kKs; ++kk) {
+      for (int kk = 0; kk < C::kKs; ++kk)
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          const int r = rbase + 8 * nt + g;
+        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-          for (int reg = 0; reg < 2; ++reg) {
-            int dl, dh;
-            q_dims<BITS>(kk, reg, t, dl, dh);
-            uint32_t lo = 0, hi = 0;
-            if (r < p.nq) {
-              lo = __ldg(qrows + static_cast<size_t>(r) * D + dl);
-              hi = __ldg(qrows + static_cast<size_t>(r) * D + dh);
-            }
-            qv[kk][nt][2 * reg] = __uint_as_float(lo << 16);
-            qv[kk][nt][2 * reg + 1] = __uint_as_float(hi << 16);
-          }
-        }
-      }
+          for (int reg = 0; reg < 2; ++reg)
+            bf16x2_to_f32(q_pair<BITS>(qw[nt], kk, reg), qv[kk][nt][2 * reg], qv[kk][nt][2 * reg + 1]);
       if constexpr (!C::kQuant) {
 #pragma unroll
         for (int kk = 0; kk < C::kKs; ++kk)
@@ -798,7 +847,7 @@ __global__ void __maxnreg__(200)
   float* cm = reinterpret_cast<float*>(smem);
   float* cl = cm + C::kWP * C::kNqAll;
   float* co = cl + C::kWP * C::kNqAll;
-  float* st_m = co + C::kWP * C::kNqAll * DV;  // this CTA's merged state (cluster merge)
+  float* st_m = co + C::kWP * C::kNqAll * C::kCoStride;  // this CTA's merged state (cluster merge)
   float* st_l = st_m + C::kNqAll;
   float* st_o = st_l + C::kNqAll;
   if (warp < C::kWarps) {
@@ -819,7 +868,8 @@ __global__ void __maxnreg__(200)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int r = 8 * nt + 2 * t + (e & 1);
-          co[(pg * C::kNqAll + rbase + r) * DV + out_dim<BITS>(mt, e >> 1, g)] = o[mt][nt][e];
+          if (rbase + r < p.nq)  // padding rows of the last n-tile are never read
+            co[(pg * C::kNqAll + rbase + r) * C::kCoStride + out_dim<BITS>(mt, e >> 1, g)] = o[mt][nt][e];
         }
   }
   __syncthreads();
@@ -837,7 +887,7 @@ __global__ void __maxnreg__(200)
         if (mw != -INFINITY) {
           const float wt = fast_exp2(mw - M);
           L = fmaf(wt, cl[w * C::kNqAll + r], L);
-          O = fmaf(wt, co[(w * C::kNqAll + r) * DV + d], O);
+          O = fmaf(wt, co[(w * C::kNqAll + r) * C::kCoStride + d], O);
         }
       }
     }
