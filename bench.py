@@ -52,6 +52,8 @@ def parse_args(argv=None):
                     help="profiling mode: keep only the first N sequences of the workload")
     ap.add_argument("--partition-tokens", type=int, default=-2,
                     help="rows per partition instead of the workload's choice (0: the library's plan)")
+    ap.add_argument("--print-kernel-hash", action="store_true",
+                    help="print the hash of the CUDA sources that profiles/dram_traffic.md rows refer to, and exit")
     ap.add_argument("--step", choices=["decode", "fused"], default="decode",
                     help="decode: the decode call; fused: the decode step with its write "
                          "(pkv_paged_decode_append_attention: append the N new K/V rows, then attend)")
@@ -65,6 +67,44 @@ def workload_specs(name):
     if name not in WORKLOADS:
         raise SystemExit(f"unknown workload {name}; choose from {sorted(WORKLOADS) + sorted(LAYER_GROUPS)}")
     return [WORKLOADS[name]]
+
+
+def kernel_source_hash():
+    """Hash of the CUDA sources: DRAM traffic recorded for one version of the kernels
+    applies to that version only."""
+    import hashlib
+    csrc = os.path.join(ROOT, "quantized_kv_decode_partial_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.md")
+
+
+def recorded_traffic(workload, step):
+    """DRAM bytes (read + write) of the partial-pass launches of one step, from the ncu
+    capture recorded in profiles/dram_traffic.md for the current kernel sources, or None
+    (no capture, or the kernels changed since)."""
+    if step != "decode":
+        return None
+    try:
+        with open(TRAFFIC_FILE) as f:
+            lines = f.read().splitlines()
+    except OSError:
+        return None
+    want = kernel_source_hash()
+    for line in lines:
+        cells = [c.strip().strip("`") for c in line.strip().strip("|").split("|")]
+        if len(cells) >= 3 and cells[0] == workload and cells[1] == want:
+            try:
+                return int(cells[2].replace(",", ""))
+            except ValueError:
+                return None
+    return None
 
 
 def measured_hbm_peak():
@@ -467,7 +507,10 @@ def run_ours(args):
                 "parallelism": f"dp{world} (independent instances)",
             },
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": None,
+                         "frac": achieved / peak, "traffic": recorded_traffic(args.workload, args.step),
+                         "traffic_unit": "DRAM bytes read + written by the partial-pass launches of one step "
+                                         "(ncu, profiles/dram_traffic.md); algorithmic bytes per step: "
+                                         f"{step_bytes}",
                          "kernel": (f"pkv_partial_kernel (partial pass alone, {part_ms * 1e3:.2f} us per step)"
                                     if args.step == "decode" else
                                     f"the fused step (write + partial + merge, {part_ms * 1e3:.2f} us per step)"),
@@ -521,7 +564,9 @@ def run_profile_calls(args):
 
 def main(argv=None):
     args = parse_args(argv)
-    if args.profile_calls:
+    if args.print_kernel_hash:
+        print(kernel_source_hash())
+    elif args.profile_calls:
         run_profile_calls(args)
     elif args.impl == "reference":
         run_reference(args)
