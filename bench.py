@@ -295,7 +295,8 @@ def run_ours(args):
     import torch.distributed as dist
 
     from quantized_kv_decode_partial_gb300 import (DecodeParams, load_library, make_plan, paged_decode_attention,
-                                                   paged_decode_append_attention, paged_decode_passes)
+                                                   paged_decode_append_attention, paged_decode_passes,
+                                                   HostDecodeStep)
     from quantized_kv_decode_partial_gb300 import build as pkv_build
     from quantized_kv_decode_partial_gb300.binding import layout_for
     from quantized_kv_decode_partial_gb300.workloads import make_case, required_kv_bytes
@@ -423,45 +424,27 @@ def run_ours(args):
         torch.cuda.synchronize(dev)
         ms_partial = replay_timed([(g_part, K // chunk)] + ([(g_part_rest, 1)] if g_part_rest else []))
 
-    # end to end through the public call: per step, q / tables / lengths come from
-    # pinned host memory (one packed staging copy per layer) and the output goes back
-    # to pinned host memory
-    stage_host, stage_dev, views, host_out = [], [], [], []
+    # end to end through the public call: per step, one copy of the step's inputs (q,
+    # block tables, lengths and, for the fused step, the new K/V rows) from pinned host
+    # memory, the decode, and the copy of the output back to pinned host memory, all
+    # enqueued by one C call (pkv_paged_decode_attention_host)
+    host_steps = []
     for L in layers:
         c = L["insts"][0]
-        parts = [c.q, c.block_tables, c.seq_lens] + ([c.k_new, c.v_new] if args.step == "fused" else [])
-        sizes = [t.numel() * t.element_size() for t in parts]
-        offs = [sum(-(-x // 256) * 256 for x in sizes[:i]) for i in range(len(sizes))]
-        total = offs[-1] + sizes[-1]
-        hbuf = torch.empty(total, dtype=torch.uint8, pin_memory=True)
-        dbuf = torch.empty(total, dtype=torch.uint8, device=dev)
-        v_dev = []
-        for t, o, n in zip(parts, offs, sizes):
-            hbuf[o:o + n].copy_(t.contiguous().view(torch.uint8).reshape(-1).cpu())
-            v_dev.append(dbuf[o:o + n].view(t.dtype).view(t.shape))
-        stage_host.append(hbuf)
-        stage_dev.append(dbuf)
-        views.append(v_dev)
-        host_out.append(torch.empty(L["out"].shape, dtype=L["out"].dtype, pin_memory=True))
-    h2d = sum(t.numel() for t in stage_host)
-    d2h = sum(t.numel() * t.element_size() for t in host_out)
+        sp = L["spec"]
+        host_steps.append(HostDecodeStep(
+            c.q, c.block_tables, c.seq_lens, c.k_pool, c.v_pool, c.scale,
+            k_new=c.k_new if args.step == "fused" else None, v_new=c.v_new if args.step == "fused" else None,
+            bits=sp.bits, group_size=sp.group_size, k_scales=c.k_scales, k_biases=c.k_biases, v_scales=c.v_scales,
+            v_biases=c.v_biases, partition_tokens=c.partition_tokens, window=sp.window, workspace=L["ws"],
+            stream=stream))
+    h2d = sum(h.h2d_bytes for h in host_steps)
+    d2h = sum(h.d2h_bytes for h in host_steps)
     e2e_steps = min(K, 50)
 
     def e2e_once():
-        for li, L in enumerate(layers):
-            stage_dev[li].copy_(stage_host[li], non_blocking=True)
-            c = L["insts"][0]
-            sp = L["spec"]
-            q, tb, sl = views[li][:3]
-            kw = dict(bits=sp.bits, group_size=sp.group_size, k_scales=c.k_scales, k_biases=c.k_biases,
-                      v_scales=c.v_scales, v_biases=c.v_biases, partition_tokens=c.partition_tokens,
-                      window=sp.window, out=L["out"], workspace=L["ws"])
-            if args.step == "fused":
-                kn, vn = views[li][3:]
-                paged_decode_append_attention(q, kn, vn, c.k_pool, c.v_pool, tb, sl, c.scale, **kw)
-            else:
-                paged_decode_attention(q, c.k_pool, c.v_pool, tb, sl, c.scale, **kw)
-            host_out[li].copy_(L["out"], non_blocking=True)
+        for h in host_steps:
+            h()
 
     with torch.cuda.stream(stream):
         for _ in range(3):
@@ -517,9 +500,10 @@ def run_ours(args):
                          "peak_source": f"{peak_kind} hbm_gbs", "frac_of_nominal_7900": achieved / 7900.0},
             "e2e": {"value": weak_scaling_rate(step_bytes, world, e2e_ms), "unit": "GB/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-                    "what": "public call per step with q, block tables and lengths"
-                            + (", and the new K/V rows," if args.step == "fused" else "")
-                            + " copied from pinned host memory and the output copied back; the KV pool is "
+                    "what": "pkv_paged_decode_attention_host per step: one copy of q, block tables, lengths"
+                            + (" and the new K/V rows" if args.step == "fused" else "")
+                            + " from pinned host memory, the " + ("fused step" if args.step == "fused" else "decode")
+                            + " and the output copied back, enqueued by one C call; the KV pool is "
                               "device-resident cache state"},
             "gpu_launches": launches_per_step * K,
             "clocks": clk,

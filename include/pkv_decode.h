@@ -180,6 +180,27 @@ int pkv_merge_partitions(const pkv_pool_layout* layout, const pkv_decode_params*
                          const int32_t* seq_lens, const void* workspace, size_t workspace_bytes, void* out,
                          int32_t* error_flag, void* stream);
 
+/* One decode step driven from host memory, as a host-side serving loop runs it
+ * (and what the end-to-end figure of bench.py times). On `stream` the call
+ * enqueues:
+ *   1. one copy of in_bytes from in_host (host) to in_dev (device): the caller's
+ *      packing of this step's inputs, e.g. q, seq_lens and changed block tables,
+ *      laid out as their device counterparts; the device pointers below may
+ *      point into in_dev (in_bytes = 0 skips the copy);
+ *   2. the decode: pkv_paged_decode_append_attention when k_new and v_new are
+ *      given (they may also point into in_dev), else pkv_paged_decode_attention
+ *      (the pools are then only read);
+ *   3. one copy of the bf16 output from `out` to out_host (NULL skips it).
+ * Host memory should be page-locked (pinned) for the copies to be asynchronous;
+ * with pageable memory the CUDA runtime synchronises them. All other arguments
+ * are those of the two decode calls; a failed copy returns PKV_ERR_CUDA. */
+int pkv_paged_decode_attention_host(const pkv_pool_layout* layout, const pkv_decode_params* params,
+                                    const void* in_host, void* in_dev, size_t in_bytes, void* out_host,
+                                    const void* q, const void* k_new, const void* v_new, void* k_pool, void* v_pool,
+                                    void* k_scales, void* k_biases, void* v_scales, void* v_biases,
+                                    const int32_t* block_tables, const int32_t* seq_lens, float scale, void* out,
+                                    void* workspace, size_t workspace_bytes, int32_t* error_flag, void* stream);
+
 /* pkv_paged_decode_attention for callers that cannot allocate device memory.
  * The pages have no counterpart of this entry point.
  *

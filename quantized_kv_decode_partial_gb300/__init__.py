@@ -14,6 +14,7 @@ from .binding import (  # noqa: F401
     paged_decode_attention,
     paged_decode_passes,
     paged_decode_append_attention,
+    HostDecodeStep,
     paged_append,
     paged_gather,
 )

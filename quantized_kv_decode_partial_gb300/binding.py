@@ -23,6 +23,7 @@ EXPORTS = (
     "pkv_paged_decode_partial",
     "pkv_merge_partitions",
     "pkv_paged_decode_attention_no_alloc",
+    "pkv_paged_decode_attention_host",
     "pkv_paged_decode_append_attention",
     "pkv_paged_append",
     "pkv_paged_gather",
@@ -103,6 +104,9 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.pkv_paged_decode_attention_no_alloc.argtypes = [ctypes.POINTER(PoolLayout), ctypes.POINTER(DecodeParams),
                                                         P, P, P, P, P, P, P, P, P, F, P, P, P]
     lib.pkv_paged_decode_attention_no_alloc.restype = ctypes.c_int
+    lib.pkv_paged_decode_attention_host.argtypes = [ctypes.POINTER(PoolLayout), ctypes.POINTER(DecodeParams),
+                                                    P, P, SZ, P, P, P, P, P, P, P, P, P, P, P, P, F, P, P, SZ, P, P]
+    lib.pkv_paged_decode_attention_host.restype = ctypes.c_int
     lib.pkv_paged_decode_append_attention.argtypes = [ctypes.POINTER(PoolLayout), ctypes.POINTER(DecodeParams),
                                                       P, P, P, P, P, P, P, P, P, P, P, F, P, P, SZ, P, P]
     lib.pkv_paged_decode_append_attention.restype = ctypes.c_int
@@ -246,6 +250,79 @@ def paged_decode_append_attention(q: torch.Tensor, k_new: torch.Tensor, v_new: t
             _ptr(seq_lens), float(scale), _ptr(out), _ptr(workspace), ws_bytes, _ptr(error_flag), stream)
     _check(rc, lib)
     return out
+
+
+class HostDecodeStep:
+    """One decode step driven from host memory (pkv_paged_decode_attention_host).
+
+    The step's host inputs (q, block tables, lengths and, for the fused step, the
+    new K/V rows) live in one pinned block with a device twin; each call enqueues a
+    single host-to-device copy of the block, the decode (fused with the append when
+    ``k_new``/``v_new`` are given), and the copy of the output into pinned
+    ``out_host``, on ``stream``. Write the next step's values into ``host[name]``
+    (views of the pinned block) before calling again; ``copy_tables=False`` leaves
+    the block tables out of the per-step copy (they then stay as first copied, until
+    ``refresh_tables()``). Pools, scale/bias planes and the workspace are device
+    tensors, as for ``paged_decode_attention``.
+    """
+
+    def __init__(self, q: torch.Tensor, block_tables: torch.Tensor, seq_lens: torch.Tensor, k_pool: torch.Tensor,
+                 v_pool: torch.Tensor, scale: float, *, k_new: Optional[torch.Tensor] = None,
+                 v_new: Optional[torch.Tensor] = None, bits: int = 16, group_size: int = 64, k_scales=None,
+                 k_biases=None, v_scales=None, v_biases=None, partition_tokens: int = 0, window: int = 0,
+                 workspace: Optional[torch.Tensor] = None, error_flag: Optional[torch.Tensor] = None, stream=None,
+                 copy_tables: bool = True):
+        self.lib = lib = load_library()
+        dev = k_pool.device
+        B, HQ, N, D = q.shape
+        self.layout = layout_for(k_pool, D, bits, group_size, v_pool)
+        self.params = DecodeParams(B, HQ, N, block_tables.shape[1], partition_tokens, window)
+        named = [("q", q), ("seq_lens", seq_lens)]
+        if k_new is not None:
+            named += [("k_new", k_new), ("v_new", v_new)]
+        named.append(("block_tables", block_tables))  # last: a per-step copy can stop before it
+        offs, total = {}, 0
+        for name, t in named:  # 256-byte aligned slots
+            offs[name] = total
+            total += -(-(t.numel() * t.element_size()) // 256) * 256
+        self.block_host = torch.empty(total, dtype=torch.uint8, pin_memory=True)
+        self.block_dev = torch.empty(total, dtype=torch.uint8, device=dev)
+        self.host, self.dev = {}, {}
+        for name, t in named:
+            n = t.numel() * t.element_size()
+            self.host[name] = self.block_host[offs[name]:offs[name] + n].view(t.dtype).view(t.shape)
+            self.dev[name] = self.block_dev[offs[name]:offs[name] + n].view(t.dtype).view(t.shape)
+            self.host[name].copy_(t.cpu())
+        self.dev["block_tables"].copy_(self.host["block_tables"])
+        # bytes copied per step: everything up to the tables' slot, or the whole block
+        self.in_bytes = total if copy_tables else offs["block_tables"]
+        with _on_device(dev):
+            plan = _cached_plan(self.layout, self.params)
+            self.out = _out_like(self.dev["q"], self.layout)
+            if workspace is None and plan.workspace_bytes:
+                workspace = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev)
+            st = (stream or torch.cuda.current_stream(dev)).cuda_stream
+        self.out_host = torch.empty(self.out.shape, dtype=self.out.dtype, pin_memory=True)
+        self.h2d_bytes, self.d2h_bytes = self.in_bytes, self.out_host.numel() * self.out_host.element_size()
+        ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+        self._keep = (k_pool, v_pool, k_scales, k_biases, v_scales, v_biases, workspace, error_flag)
+        d = self.dev
+        self._args = (ctypes.byref(self.layout), ctypes.byref(self.params), _ptr(self.block_host),
+                      _ptr(self.block_dev), self.in_bytes, _ptr(self.out_host), _ptr(d["q"]), _ptr(d.get("k_new")),
+                      _ptr(d.get("v_new")), _ptr(k_pool), _ptr(v_pool), _ptr(k_scales), _ptr(k_biases),
+                      _ptr(v_scales), _ptr(v_biases), _ptr(d["block_tables"]), _ptr(d["seq_lens"]), float(scale),
+                      _ptr(self.out), _ptr(workspace), ws_bytes, _ptr(error_flag), st)
+        self._fn = lib.pkv_paged_decode_attention_host
+
+    def refresh_tables(self):
+        """Copies the host block tables to the device now (synchronously)."""
+        self.dev["block_tables"].copy_(self.host["block_tables"])
+
+    def __call__(self) -> torch.Tensor:
+        rc = self._fn(*self._args)
+        if rc != PKV_OK:
+            _check(rc, self.lib)
+        return self.out_host
 
 
 class _on_device:

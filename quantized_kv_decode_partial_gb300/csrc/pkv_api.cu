@@ -440,6 +440,37 @@ int pkv_merge_partitions(const pkv_pool_layout* layout, const pkv_decode_params*
                         kPassMerge);
 }
 
+int pkv_paged_decode_attention_host(const pkv_pool_layout* layout, const pkv_decode_params* params,
+                                    const void* in_host, void* in_dev, size_t in_bytes, void* out_host,
+                                    const void* q, const void* k_new, const void* v_new, void* k_pool, void* v_pool,
+                                    void* k_scales, void* k_biases, void* v_scales, void* v_biases,
+                                    const int32_t* block_tables, const int32_t* seq_lens, float scale, void* out,
+                                    void* workspace, size_t workspace_bytes, int32_t* error_flag, void* stream) {
+  int rc = check_layout(layout);
+  if (rc) return rc;
+  rc = check_params(layout, params);
+  if (rc) return rc;
+  if (in_bytes > 0 && (!in_host || !in_dev)) return PKV_ERR_NULL_POINTER;
+  if ((k_new == nullptr) != (v_new == nullptr)) return PKV_ERR_NULL_POINTER;
+  if (!out) return PKV_ERR_NULL_POINTER;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  (void)cudaGetLastError();
+  if (in_bytes > 0) {
+    cudaError_t e = cudaMemcpyAsync(in_dev, in_host, in_bytes, cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) return cuda_fail("input copy", e);
+  }
+  rc = enqueue_decode(layout, params, q, k_pool, v_pool, k_scales, k_biases, v_scales, v_biases, block_tables,
+                      seq_lens, scale, out, workspace, workspace_bytes, error_flag, stream, kPassPartial | kPassMerge,
+                      k_new, v_new);
+  if (rc) return rc;
+  if (out_host) {
+    const size_t rows = static_cast<size_t>(params->num_seqs) * params->num_q_heads * params->n_query;
+    cudaError_t e = cudaMemcpyAsync(out_host, out, rows * v_dim(layout) * 2, cudaMemcpyDeviceToHost, st);
+    if (e != cudaSuccess) return cuda_fail("output copy", e);
+  }
+  return PKV_OK;
+}
+
 int pkv_paged_decode_append_attention(const pkv_pool_layout* layout, const pkv_decode_params* params,
                                       const void* q, const void* k_new, const void* v_new, void* k_pool,
                                       void* v_pool, void* k_scales, void* k_biases, void* v_scales, void* v_biases,

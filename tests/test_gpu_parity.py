@@ -322,3 +322,58 @@ def test_minimum_lengths_and_exact_fill():
     for pt in (16, 4096):
         out = run_gpu(case.to(DEV), partition_tokens=pt)
         assert_close(out.double().cpu().numpy(), ref, f"edges pt={pt}")
+
+
+def test_host_driven_step_matches_device_entry():
+    # pkv_paged_decode_attention_host: one packed input copy, decode, output copy, on one stream
+    from quantized_kv_decode_partial_gb300 import HostDecodeStep
+    sp = spec("host_io", head_dim=256, bits=4, block_size=32, length_range=(1, 600))
+    case = make_case(sp)
+    d = case.to(DEV)
+    ref = run_gpu(d, partition_tokens=64)
+    stream = torch.cuda.Stream(device=DEV)
+    kw = dict(bits=4, k_scales=d.k_scales, k_biases=d.k_biases, v_scales=d.v_scales, v_biases=d.v_biases,
+              partition_tokens=64, stream=stream)
+    step = HostDecodeStep(case.q, case.block_tables, case.seq_lens, d.k_pool, d.v_pool, case.scale, **kw)
+    for _ in range(2):
+        step.out_host.fill_(float("nan"))
+        step()
+        stream.synchronize()
+        assert torch.equal(step.out_host.view(torch.int16), ref.cpu().view(torch.int16))
+    # new per-step values written into the host block reach the device: the second
+    # sequence's query rows are zeroed, and only they change (to the mean of their V rows)
+    step.host["q"][1].zero_()
+    step()
+    stream.synchronize()
+    d.q[1].zero_()
+    ref2 = run_gpu(d, partition_tokens=64)
+    assert torch.equal(step.out_host.view(torch.int16), ref2.cpu().view(torch.int16))
+    assert not torch.equal(ref2[1], ref[1]) and torch.equal(ref2[0], ref[0])
+    # tables left out of the per-step copy stay as first copied
+    step2 = HostDecodeStep(case.q, case.block_tables, case.seq_lens, d.k_pool, d.v_pool, case.scale,
+                           copy_tables=False, **kw)
+    assert step2.in_bytes < step.in_bytes
+    step2.host["block_tables"].fill_(-7)  # would be flagged as bad blocks if copied
+    step2()
+    stream.synchronize()
+    assert torch.equal(step2.out_host.view(torch.int16), ref.cpu().view(torch.int16))
+
+
+def test_host_driven_fused_step_matches_device_fused_step():
+    from quantized_kv_decode_partial_gb300 import HostDecodeStep
+    sp = spec("host_fused", num_q_heads=8, num_kv_heads=2, n_query=2, length_range=(3, 300))
+    case = make_case(sp, poison=False)
+    g = torch.Generator().manual_seed(5)
+    k_new = torch.randn((3, 2, 2, 128), generator=g).to(torch.bfloat16)
+    v_new = torch.randn((3, 2, 2, 128), generator=g).to(torch.bfloat16)
+    a, b = case.to(DEV), case.to(DEV)
+    ref = B.paged_decode_append_attention(a.q, k_new.to(DEV), v_new.to(DEV), a.k_pool, a.v_pool, a.block_tables,
+                                          a.seq_lens, case.scale, partition_tokens=32)
+    stream = torch.cuda.Stream(device=DEV)
+    step = HostDecodeStep(case.q, case.block_tables, case.seq_lens, b.k_pool, b.v_pool, case.scale, k_new=k_new,
+                          v_new=v_new, partition_tokens=32, stream=stream)
+    step()
+    stream.synchronize()
+    assert torch.equal(step.out_host.view(torch.int16), ref.cpu().view(torch.int16))
+    assert torch.equal(a.k_pool.view(torch.int16), b.k_pool.view(torch.int16))
+    assert torch.equal(a.v_pool.view(torch.int16), b.v_pool.view(torch.int16))
