@@ -10,16 +10,18 @@
 // softmax itself and writes bf16 output.
 //
 // Design (GB300):
-//  * Four warps per CTA (eight for grids of at most one CTA per SM); warp w takes
-//    chunks w, w+4, w+8, ... of the partition
-//    (16 rows for bf16 pages, 32 or 16 for affine pages) and runs its own
-//    pipeline: lane 0 issues the copies of its chunk `kStagesPerWarp` ahead into a
-//    private ring of shared-memory stages guarded by mbarriers, so no warp waits
-//    on another. The block table is read 32 entries per coalesced load and
-//    resolved once per chunk. A chunk of one page and KV head is contiguous in
-//    the pool, so it travels as 2-D TMA boxes (rows of 64 or 128 bytes,
-//    hardware-swizzled so the ldmatrix reads below are free of bank conflicts)
-//    plus 1-D bulk copies of the affine scale/bias rows.
+//  * Four warps per CTA (eight for grids of at most one CTA per SM); with W warps,
+//    warp w takes chunks w, w+W, w+2W, ... of the partition (16 rows for bf16
+//    pages, 32 or 16 for affine pages) and runs its own pipeline: lane 0 issues
+//    the copies of its chunk `kStagesPerWarp` ahead into a private ring of
+//    shared-memory stages guarded by mbarriers, so no warp waits on another.
+//    (With more query rows than one warp holds, WQ warps share a ring and read
+//    each chunk for their own rows.) The block table is read 32 entries per
+//    coalesced load and resolved into TMA row coordinates once per 32 chunks. A
+//    chunk of one page and KV head is contiguous in the pool, so it travels as
+//    2-D TMA boxes (rows of 64 or 128 bytes, hardware-swizzled so the ldmatrix
+//    reads below are free of bank conflicts) plus 1-D bulk copies of the affine
+//    scale/bias rows. K and V rows may have different head dims.
 //  * Each K/V row in shared memory is read once and multiplied against all
 //    REP*N query rows of its KV head (GQA reuse) with warp-level tensor-core
 //    MMA (m16n8k16, bf16 in, f32 out):
@@ -38,8 +40,8 @@
 //    (q converted to fp16 with an exact per-row power-of-two prescale), and with
 //    P'_g = p * s_g rounded to fp16,
 //        o_d = sum_t P'_g(t) c_td + sum_t p(t) b_g(t).
-//    The scale/bias terms are per key and per group, so they cost a few FMAs per
-//    key instead of two per element.
+//    The scale terms cost a few FMAs per key and group instead of two per
+//    element; the bias terms of the scores run as one extra bf16 MMA per tile.
 //  * Rows at or past seq_len in the last page are masked before they can reach
 //    an accumulator (scores set to -inf by select; their V operand or V scale
 //    zeroed), so stale storage may hold anything, NaN included.
@@ -874,39 +876,45 @@ __global__ void __maxnreg__(200)
   }
   __syncthreads();
 
-  for (int idx = threadIdx.x; idx < p.nq * DV; idx += C::kThreads) {
-    const int r = idx / DV, d = idx % DV;
+  // Per query row: the combined maximum and normaliser of the page groups' states
+  // (this CTA's state, kept in st_m / st_l) and each group's weight 2^(m_w - M),
+  // written over its m; then every output only sums weighted o values.
+  if (threadIdx.x < p.nq) {
+    const int r = threadIdx.x;
     float M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < C::kWP; ++w) M = fmaxf(M, cm[w * C::kNqAll + r]);
-    float L = 0.f, O = 0.f;
-    if (M != -INFINITY) {
+    float L = 0.f;
 #pragma unroll
-      for (int w = 0; w < C::kWP; ++w) {
-        const float mw = cm[w * C::kNqAll + r];
-        if (mw != -INFINITY) {
-          const float wt = fast_exp2(mw - M);
-          L = fmaf(wt, cl[w * C::kNqAll + r], L);
-          O = fmaf(wt, co[(w * C::kNqAll + r) * C::kCoStride + d], O);
-        }
-      }
+    for (int w = 0; w < C::kWP; ++w) {
+      const float mw = cm[w * C::kNqAll + r];
+      const float wt = mw == -INFINITY ? 0.f : fast_exp2(mw - M);
+      L = fmaf(wt, cl[w * C::kNqAll + r], L);
+      cm[w * C::kNqAll + r] = wt;
     }
+    st_m[r] = M;
+    st_l[r] = L;
+    if (!single && !in_cluster) {
+      const size_t ws = (row0 + r) * p.max_partitions + slot;
+      p.ws_ml[ws * 2] = M;
+      p.ws_ml[ws * 2 + 1] = L;
+    }
+  }
+  __syncthreads();
+
+  for (int idx = threadIdx.x; idx < p.nq * DV; idx += C::kThreads) {
+    const int r = idx / DV, d = idx % DV;
+    float O = 0.f;
+#pragma unroll
+    for (int w = 0; w < C::kWP; ++w) O = fmaf(cm[w * C::kNqAll + r], co[(w * C::kNqAll + r) * C::kCoStride + d], O);
     const size_t orow = row0 + r;
     if (single) {
+      const float L = st_l[r];
       p.out[orow * DV + d] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
     } else if (in_cluster) {
       st_o[r * DV + d] = O;
-      if (d == 0) {
-        st_m[r] = M;
-        st_l[r] = L;
-      }
     } else {
-      const size_t ws = orow * p.max_partitions + slot;
-      p.ws_o[ws * DV + d] = O;
-      if (d == 0) {
-        p.ws_ml[ws * 2] = M;
-        p.ws_ml[ws * 2 + 1] = L;
-      }
+      p.ws_o[(orow * p.max_partitions + slot) * DV + d] = O;
     }
   }
 
