@@ -352,7 +352,7 @@ int enqueue_decode(const pkv_pool_layout* layout, const pkv_decode_params* param
   p.v_biases = static_cast<const __nv_bfloat16*>(v_biases);
   p.out = static_cast<__nv_bfloat16*>(out);
   const size_t slots = static_cast<size_t>(params->num_seqs) * params->num_q_heads * params->n_query * plan.max_partitions;
-  const size_t o_bytes = (slots * D * sizeof(float) + 255) / 256 * 256;
+  const size_t o_bytes = (slots * DV * sizeof(float) + 255) / 256 * 256;  // as plan_impl sizes it
   p.ws_o = mode == pkv::kModeWorkspace ? static_cast<float*>(workspace) : nullptr;
   p.ws_ml = mode == pkv::kModeWorkspace ? reinterpret_cast<float*>(static_cast<char*>(workspace) + o_bytes) : nullptr;
   p.mode = mode;

@@ -377,3 +377,25 @@ def test_host_driven_fused_step_matches_device_fused_step():
     assert torch.equal(step.out_host.view(torch.int16), ref.cpu().view(torch.int16))
     assert torch.equal(a.k_pool.view(torch.int16), b.k_pool.view(torch.int16))
     assert torch.equal(a.v_pool.view(torch.int16), b.v_pool.view(torch.int16))
+
+
+@pytest.mark.parametrize("bits,D,DV", [(16, 128, 128), (16, 192, 128), (16, 128, 256), (4, 128, 256), (8, 256, 128)])
+def test_workspace_writes_stay_inside_the_planned_bytes(bits, D, DV):
+    # a grid of more than one wave with several partitions: states go through the workspace
+    sp = spec(f"ws_bounds_{bits}_{D}_{DV}", num_seqs=40, num_q_heads=8, num_kv_heads=4, head_dim=D, v_head_dim=DV,
+              bits=bits, block_size=16 if bits == 16 else 32, length_range=(100, 400))
+    case = make_case(sp)
+    d = case.to(DEV)
+    pt = 64
+    plan = B.make_plan(B.layout_for(d.k_pool, D, bits, v_pool=d.v_pool),
+                       B.DecodeParams(sp.num_seqs, sp.num_q_heads, 1, d.block_tables.shape[1], pt))
+    assert plan.merge_in_cluster == 0 and plan.max_partitions > 1 and plan.workspace_bytes > 0
+    guard = 1 << 16
+    buf = torch.full((plan.workspace_bytes + guard,), 0x5A, dtype=torch.uint8, device=DEV)
+    ws = buf[:plan.workspace_bytes]
+    out = paged_decode_attention(d.q, d.k_pool, d.v_pool, d.block_tables, d.seq_lens, case.scale, bits=bits,
+                                 k_scales=d.k_scales, k_biases=d.k_biases, v_scales=d.v_scales, v_biases=d.v_biases,
+                                 partition_tokens=pt, workspace=ws)
+    torch.cuda.synchronize()
+    assert bool((buf[plan.workspace_bytes:] == 0x5A).all()), "write past the planned workspace"
+    assert_close(out.double().cpu().numpy(), oracle_out(case), f"{sp.name}")
