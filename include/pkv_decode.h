@@ -43,7 +43,8 @@
  *   out           bf16  [num_seqs, num_q_heads, n_query, v_head_dim]
  *
  * Ownership: every pointer is borrowed; the library frees nothing and keeps no
- * pointer after a call returns. Calls are asynchronous on the given stream
+ * pointer after a call returns (except a pkv_step handle, which keeps the pointers
+ * it was created with until it is destroyed). Calls are asynchronous on the given stream
  * (a cudaStream_t passed as void*; NULL = the legacy default stream) and make
  * no allocation and no host synchronisation, so they can be captured in a
  * CUDA graph.
@@ -200,6 +201,31 @@ int pkv_paged_decode_attention_host(const pkv_pool_layout* layout, const pkv_dec
                                     void* k_scales, void* k_biases, void* v_scales, void* v_biases,
                                     const int32_t* block_tables, const int32_t* seq_lens, float scale, void* out,
                                     void* workspace, size_t workspace_bytes, int32_t* error_flag, void* stream);
+
+/* A prepared host-driven step: the arguments of pkv_paged_decode_attention_host
+ * checked, planned and resolved into kernel parameters and TMA descriptors once,
+ * so that each step costs the host only the copies and launches. The step keeps
+ * every pointer it is given: the buffers must outlive it and stay at their
+ * addresses (a resized pool or workspace needs a new step), and the device that
+ * was current at creation must be current when it runs. The handle lives in host
+ * memory (the one host allocation of this library); no device memory is
+ * allocated.
+ *   pkv_step_create   arguments as pkv_paged_decode_attention_host, plus the
+ *                     handle's address; returns PKV_OK or a PKV_ERR_* code
+ *                     (nothing is created then)
+ *   pkv_step_run      enqueues the step on the stream given at creation: the
+ *                     input copy, the decode (or fused step), the output copy
+ *   pkv_step_destroy  frees the handle (NULL is allowed); it does not wait for
+ *                     work in flight, which keeps using the caller's buffers */
+typedef struct pkv_step pkv_step;
+
+int pkv_step_create(const pkv_pool_layout* layout, const pkv_decode_params* params, const void* in_host, void* in_dev,
+                    size_t in_bytes, void* out_host, const void* q, const void* k_new, const void* v_new,
+                    void* k_pool, void* v_pool, void* k_scales, void* k_biases, void* v_scales, void* v_biases,
+                    const int32_t* block_tables, const int32_t* seq_lens, float scale, void* out, void* workspace,
+                    size_t workspace_bytes, int32_t* error_flag, void* stream, pkv_step** step);
+int pkv_step_run(pkv_step* step);
+void pkv_step_destroy(pkv_step* step);
 
 /* pkv_paged_decode_attention for callers that cannot allocate device memory.
  * The pages have no counterpart of this entry point.

@@ -24,6 +24,9 @@ EXPORTS = (
     "pkv_merge_partitions",
     "pkv_paged_decode_attention_no_alloc",
     "pkv_paged_decode_attention_host",
+    "pkv_step_create",
+    "pkv_step_run",
+    "pkv_step_destroy",
     "pkv_paged_decode_append_attention",
     "pkv_paged_append",
     "pkv_paged_gather",
@@ -107,6 +110,14 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.pkv_paged_decode_attention_host.argtypes = [ctypes.POINTER(PoolLayout), ctypes.POINTER(DecodeParams),
                                                     P, P, SZ, P, P, P, P, P, P, P, P, P, P, P, P, F, P, P, SZ, P, P]
     lib.pkv_paged_decode_attention_host.restype = ctypes.c_int
+    lib.pkv_step_create.argtypes = [ctypes.POINTER(PoolLayout), ctypes.POINTER(DecodeParams),
+                                    P, P, SZ, P, P, P, P, P, P, P, P, P, P, P, P, F, P, P, SZ, P, P,
+                                    ctypes.POINTER(ctypes.c_void_p)]
+    lib.pkv_step_create.restype = ctypes.c_int
+    lib.pkv_step_run.argtypes = [P]
+    lib.pkv_step_run.restype = ctypes.c_int
+    lib.pkv_step_destroy.argtypes = [P]
+    lib.pkv_step_destroy.restype = None
     lib.pkv_paged_decode_append_attention.argtypes = [ctypes.POINTER(PoolLayout), ctypes.POINTER(DecodeParams),
                                                       P, P, P, P, P, P, P, P, P, P, P, F, P, P, SZ, P, P]
     lib.pkv_paged_decode_append_attention.restype = ctypes.c_int
@@ -253,7 +264,8 @@ def paged_decode_append_attention(q: torch.Tensor, k_new: torch.Tensor, v_new: t
 
 
 class HostDecodeStep:
-    """One decode step driven from host memory (pkv_paged_decode_attention_host).
+    """One decode step driven from host memory (a pkv_step: pkv_paged_decode_attention_host
+    prepared once).
 
     The step's host inputs (q, block tables, lengths and, for the fused step, the
     new K/V rows) live in one pinned block with a device twin; each call enqueues a
@@ -307,22 +319,39 @@ class HostDecodeStep:
         ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
         self._keep = (k_pool, v_pool, k_scales, k_biases, v_scales, v_biases, workspace, error_flag)
         d = self.dev
-        self._args = (ctypes.byref(self.layout), ctypes.byref(self.params), _ptr(self.block_host),
-                      _ptr(self.block_dev), self.in_bytes, _ptr(self.out_host), _ptr(d["q"]), _ptr(d.get("k_new")),
-                      _ptr(d.get("v_new")), _ptr(k_pool), _ptr(v_pool), _ptr(k_scales), _ptr(k_biases),
-                      _ptr(v_scales), _ptr(v_biases), _ptr(d["block_tables"]), _ptr(d["seq_lens"]), float(scale),
-                      _ptr(self.out), _ptr(workspace), ws_bytes, _ptr(error_flag), st)
-        self._fn = lib.pkv_paged_decode_attention_host
+        handle = ctypes.c_void_p()
+        with _on_device(dev):
+            rc = lib.pkv_step_create(
+                ctypes.byref(self.layout), ctypes.byref(self.params), _ptr(self.block_host), _ptr(self.block_dev),
+                self.in_bytes, _ptr(self.out_host), _ptr(d["q"]), _ptr(d.get("k_new")), _ptr(d.get("v_new")),
+                _ptr(k_pool), _ptr(v_pool), _ptr(k_scales), _ptr(k_biases), _ptr(v_scales), _ptr(v_biases),
+                _ptr(d["block_tables"]), _ptr(d["seq_lens"]), float(scale), _ptr(self.out), _ptr(workspace),
+                ws_bytes, _ptr(error_flag), st, ctypes.byref(handle))
+        _check(rc, lib)
+        self._handle = handle
+        self._run = lib.pkv_step_run
+        self._destroy = lib.pkv_step_destroy
+        self._device = dev
 
     def refresh_tables(self):
         """Copies the host block tables to the device now (synchronously)."""
         self.dev["block_tables"].copy_(self.host["block_tables"])
 
     def __call__(self) -> torch.Tensor:
-        rc = self._fn(*self._args)
+        """Enqueues the step (pkv_step_run) and returns the pinned output tensor,
+        which holds the result once the stream reaches this point."""
+        rc = self._run(self._handle)
         if rc != PKV_OK:
             _check(rc, self.lib)
         return self.out_host
+
+    def __del__(self):
+        # the handle is host memory only; work in flight keeps using the tensors, which
+        # the caller keeps alive as long as it needs the results
+        handle = getattr(self, "_handle", None)
+        if handle is not None and handle.value:
+            self._destroy(handle)
+            self._handle = None
 
 
 class _on_device:

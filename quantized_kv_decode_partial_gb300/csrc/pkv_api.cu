@@ -8,6 +8,7 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <new>
 
 #include "pkv_decode.h"
 #include "pkv_launch.h"
@@ -290,12 +291,24 @@ pkv::AppendTarget append_target(bool quant, void* k_pool, void* v_pool, void* k_
 constexpr int kPassPartial = 1;
 constexpr int kPassMerge = 2;
 
-int enqueue_decode(const pkv_pool_layout* layout, const pkv_decode_params* params, const void* q,
+// Everything one decode call launches, resolved from its arguments: the kernels'
+// parameter blocks, the TMA descriptors of the pools and the launch shapes.
+struct PreparedDecode {
+  pkv::PartialParams p;
+  pkv::MergeParams m;
+  CUtensorMap tk, tv;
+  dim3 grid;
+  int bits, dk, dv, nq, device, merge_rows;
+  bool solo, partial, merge;
+};
+
+// Checks the arguments of a decode call (the passes in `passes`) and prepares its
+// launches; no CUDA work is enqueued.
+int prepare_decode(const pkv_pool_layout* layout, const pkv_decode_params* params, const void* q,
                    const void* k_pool, const void* v_pool, const void* k_scales, const void* k_biases,
                    const void* v_scales, const void* v_biases, const int32_t* block_tables,
                    const int32_t* seq_lens, float scale, void* out, void* workspace, size_t workspace_bytes,
-                   int32_t* error_flag, void* stream, int passes, const void* k_new = nullptr,
-                   const void* v_new = nullptr) {
+                   int32_t* error_flag, int passes, const void* k_new, const void* v_new, PreparedDecode* pd) {
   int rc = check_layout(layout);
   if (rc) return rc;
   rc = check_params(layout, params);
@@ -334,15 +347,15 @@ int enqueue_decode(const pkv_pool_layout* layout, const pkv_decode_params* param
   const long long row_elems_k = quant ? static_cast<long long>(D) * layout->bits / 8 : D;
   const long long row_elems_v = quant ? static_cast<long long>(DV) * layout->bits / 8 : DV;
 
-  CUtensorMap tk, tv;
+  *pd = PreparedDecode{};
   if (partial) {
-    rc = pool_tensor_map(&tk, k_pool, elem, row_elems_k, rows, info.box_row_bytes, info.chunk_rows);
+    rc = pool_tensor_map(&pd->tk, k_pool, elem, row_elems_k, rows, info.box_row_bytes, info.chunk_rows);
     if (rc) return rc;
-    rc = pool_tensor_map(&tv, v_pool, elem, row_elems_v, rows, info.box_row_bytes_v, info.chunk_rows);
+    rc = pool_tensor_map(&pd->tv, v_pool, elem, row_elems_v, rows, info.box_row_bytes_v, info.chunk_rows);
     if (rc) return rc;
   }
 
-  pkv::PartialParams p{};
+  pkv::PartialParams& p = pd->p;
   p.q = static_cast<const __nv_bfloat16*>(q);
   p.block_tables = block_tables;
   p.seq_lens = seq_lens;
@@ -375,22 +388,17 @@ int enqueue_decode(const pkv_pool_layout* layout, const pkv_decode_params* param
                           const_cast<void*>(k_biases), const_cast<void*>(v_scales), const_cast<void*>(v_biases));
   }
 
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  (void)cudaGetLastError();  // start from a clean error state
-  const dim3 grid(plan.max_partitions, HK, params->num_seqs);
-  cudaError_t e = cudaSuccess;
-  if (partial) {
-    if (layout->bits == 16)
-      e = pkv::launch_partial_bf16(D, DV, nq, solo, p, tk, tv, grid, st, dev);
-    else if (layout->bits == 4)
-      e = pkv::launch_partial_u4(D, DV, nq, solo, p, tk, tv, grid, st, dev);
-    else
-      e = pkv::launch_partial_u8(D, DV, nq, solo, p, tk, tv, grid, st, dev);
-    if (e != cudaSuccess) return cuda_fail("partial kernel launch", e);
-  }
-
-  if ((passes & kPassMerge) && mode == pkv::kModeWorkspace) {
-    pkv::MergeParams m{};
+  pd->grid = dim3(plan.max_partitions, HK, params->num_seqs);
+  pd->bits = layout->bits;
+  pd->dk = D;
+  pd->dv = DV;
+  pd->nq = nq;
+  pd->device = dev;
+  pd->solo = solo;
+  pd->partial = partial;
+  pd->merge = (passes & kPassMerge) && mode == pkv::kModeWorkspace;
+  if (pd->merge) {
+    pkv::MergeParams& m = pd->m;
     m.ws_o = p.ws_o;
     m.ws_ml = p.ws_ml;
     m.seq_lens = seq_lens;
@@ -403,10 +411,43 @@ int enqueue_decode(const pkv_pool_layout* layout, const pkv_decode_params* param
     m.partition_tokens = plan.partition_tokens;
     m.max_partitions = plan.max_partitions;
     m.window = params->window;
-    e = pkv::launch_merge(m, params->num_seqs * params->num_q_heads * params->n_query, st);
+    pd->merge_rows = params->num_seqs * params->num_q_heads * params->n_query;
+  }
+  return PKV_OK;
+}
+
+// Enqueues the launches of a prepared decode call on `stream` (the device current
+// when it was prepared must be current).
+int launch_prepared(const PreparedDecode& pd, cudaStream_t st) {
+  (void)cudaGetLastError();  // start from a clean error state
+  cudaError_t e = cudaSuccess;
+  if (pd.partial) {
+    if (pd.bits == 16)
+      e = pkv::launch_partial_bf16(pd.dk, pd.dv, pd.nq, pd.solo, pd.p, pd.tk, pd.tv, pd.grid, st, pd.device);
+    else if (pd.bits == 4)
+      e = pkv::launch_partial_u4(pd.dk, pd.dv, pd.nq, pd.solo, pd.p, pd.tk, pd.tv, pd.grid, st, pd.device);
+    else
+      e = pkv::launch_partial_u8(pd.dk, pd.dv, pd.nq, pd.solo, pd.p, pd.tk, pd.tv, pd.grid, st, pd.device);
+    if (e != cudaSuccess) return cuda_fail("partial kernel launch", e);
+  }
+  if (pd.merge) {
+    e = pkv::launch_merge(pd.m, pd.merge_rows, st);
     if (e != cudaSuccess) return cuda_fail("merge kernel launch", e);
   }
   return PKV_OK;
+}
+
+int enqueue_decode(const pkv_pool_layout* layout, const pkv_decode_params* params, const void* q,
+                   const void* k_pool, const void* v_pool, const void* k_scales, const void* k_biases,
+                   const void* v_scales, const void* v_biases, const int32_t* block_tables,
+                   const int32_t* seq_lens, float scale, void* out, void* workspace, size_t workspace_bytes,
+                   int32_t* error_flag, void* stream, int passes, const void* k_new = nullptr,
+                   const void* v_new = nullptr) {
+  PreparedDecode pd;
+  int rc = prepare_decode(layout, params, q, k_pool, v_pool, k_scales, k_biases, v_scales, v_biases, block_tables,
+                          seq_lens, scale, out, workspace, workspace_bytes, error_flag, passes, k_new, v_new, &pd);
+  if (rc) return rc;
+  return launch_prepared(pd, static_cast<cudaStream_t>(stream));
 }
 
 }  // namespace
@@ -470,6 +511,68 @@ int pkv_paged_decode_attention_host(const pkv_pool_layout* layout, const pkv_dec
   }
   return PKV_OK;
 }
+
+}  // extern "C"
+
+struct pkv_step {
+  PreparedDecode pd;
+  const void* in_host;
+  void* in_dev;
+  size_t in_bytes;
+  void* out_host;
+  const void* out_dev;
+  size_t out_bytes;
+  cudaStream_t stream;
+};
+
+extern "C" {
+
+int pkv_step_create(const pkv_pool_layout* layout, const pkv_decode_params* params, const void* in_host, void* in_dev,
+                    size_t in_bytes, void* out_host, const void* q, const void* k_new, const void* v_new,
+                    void* k_pool, void* v_pool, void* k_scales, void* k_biases, void* v_scales, void* v_biases,
+                    const int32_t* block_tables, const int32_t* seq_lens, float scale, void* out, void* workspace,
+                    size_t workspace_bytes, int32_t* error_flag, void* stream, pkv_step** step) {
+  if (!step) return PKV_ERR_NULL_POINTER;
+  *step = nullptr;
+  if (in_bytes > 0 && (!in_host || !in_dev)) return PKV_ERR_NULL_POINTER;
+  pkv_step* s = new (std::nothrow) pkv_step{};
+  if (!s) return PKV_ERR_BAD_PARAMS;
+  int rc = prepare_decode(layout, params, q, k_pool, v_pool, k_scales, k_biases, v_scales, v_biases, block_tables,
+                          seq_lens, scale, out, workspace, workspace_bytes, error_flag, kPassPartial | kPassMerge,
+                          k_new, v_new, &s->pd);
+  if (rc) {
+    delete s;
+    return rc;
+  }
+  s->in_host = in_host;
+  s->in_dev = in_dev;
+  s->in_bytes = in_bytes;
+  s->out_host = out_host;
+  s->out_dev = out;
+  s->out_bytes = static_cast<size_t>(params->num_seqs) * params->num_q_heads * params->n_query * v_dim(layout) * 2;
+  s->stream = static_cast<cudaStream_t>(stream);
+  *step = s;
+  return PKV_OK;
+}
+
+int pkv_step_run(pkv_step* step) {
+  if (!step) return PKV_ERR_NULL_POINTER;
+  (void)cudaGetLastError();
+  if (step->in_bytes > 0) {
+    cudaError_t e = cudaMemcpyAsync(step->in_dev, step->in_host, step->in_bytes, cudaMemcpyHostToDevice, step->stream);
+    if (e != cudaSuccess) return cuda_fail("input copy", e);
+  }
+  int rc = launch_prepared(step->pd, step->stream);
+  if (rc) return rc;
+  if (step->out_host) {
+    cudaError_t e = cudaMemcpyAsync(step->out_host, step->out_dev, step->out_bytes, cudaMemcpyDeviceToHost,
+                                    step->stream);
+    if (e != cudaSuccess) return cuda_fail("output copy", e);
+  }
+  return PKV_OK;
+}
+
+void pkv_step_destroy(pkv_step* step) { delete step; }
 
 int pkv_paged_decode_append_attention(const pkv_pool_layout* layout, const pkv_decode_params* params,
                                       const void* q, const void* k_new, const void* v_new, void* k_pool,

@@ -225,6 +225,28 @@ def test_decode_without_gpu_fails_loudly(lib):
     assert lib.pkv_last_cuda_error().decode()
 
 
+def test_step_handle_validates_before_cuda(lib):
+    sp = WORKLOADS["bf16_1x1024_hq2_d256"]
+    lay, par = _layout(sp, 128), _params(sp, 64)
+    fake = 1 << 20
+    h = ctypes.c_void_p(123)
+
+    def create(layout, in_bytes=0, in_host=None, out=fake, handle=True):
+        return lib.pkv_step_create(ctypes.byref(layout), ctypes.byref(par), in_host, fake, in_bytes, None, fake,
+                                   None, None, fake, fake, None, None, None, None, fake, fake, 0.0625, out, None, 0,
+                                   None, None, ctypes.byref(h) if handle else None)
+
+    assert create(lay, handle=False) == B.PKV_ERR_NULL_POINTER
+    assert create(B.PoolLayout(128, 1, 16, 96, 16, 64)) == B.PKV_ERR_BAD_LAYOUT and not h.value
+    assert create(lay, in_bytes=64) == B.PKV_ERR_NULL_POINTER  # bytes to copy but no host block
+    assert create(lay, out=None) == B.PKV_ERR_NULL_POINTER
+    lib.pkv_step_destroy(None)  # allowed
+    assert lib.pkv_step_run(None) == B.PKV_ERR_NULL_POINTER
+    import torch
+    if not torch.cuda.is_available():  # valid arguments reach CUDA, which fails loudly here
+        assert create(lay) == B.PKV_ERR_CUDA and not h.value
+
+
 def test_gather_validates(lib):
     fake = 1 << 20
     assert lib.pkv_paged_gather(fake, 10, 2, 16, 6, fake, fake, 1, 4, 64, fake, None, None) == B.PKV_ERR_BAD_PARAMS
