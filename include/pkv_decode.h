@@ -182,19 +182,27 @@ int pkv_merge_partitions(const pkv_pool_layout* layout, const pkv_decode_params*
                          int32_t* error_flag, void* stream);
 
 /* One decode step driven from host memory, as a host-side serving loop runs it
- * (and what the end-to-end figure of bench.py times). On `stream` the call
- * enqueues:
- *   1. one copy of in_bytes from in_host (host) to in_dev (device): the caller's
- *      packing of this step's inputs, e.g. q, seq_lens and changed block tables,
- *      laid out as their device counterparts; the device pointers below may
- *      point into in_dev (in_bytes = 0 skips the copy);
- *   2. the decode: pkv_paged_decode_append_attention when k_new and v_new are
- *      given (they may also point into in_dev), else pkv_paged_decode_attention
- *      (the pools are then only read);
- *   3. one copy of the bf16 output from `out` to out_host (NULL skips it).
- * Host memory should be page-locked (pinned) for the copies to be asynchronous;
- * with pageable memory the CUDA runtime synchronises them. All other arguments
- * are those of the two decode calls; a failed copy returns PKV_ERR_CUDA. */
+ * (and what the end-to-end figure of bench.py times). The step's inputs (q,
+ * seq_lens, changed block tables and, for the fused step, the new K/V rows) sit
+ * packed in a host block in_host of in_bytes bytes, laid out as their device
+ * counterparts in in_dev; the device pointers q, block_tables, seq_lens, k_new,
+ * v_new may point into in_dev. On `stream` the call enqueues the decode
+ * (pkv_paged_decode_append_attention when k_new and v_new are given, else
+ * pkv_paged_decode_attention, the pools then only read) with the step's data
+ * moving as follows:
+ *   - in_host page-locked and mapped into the device's address space (the default
+ *     for cudaHostAlloc / pinned memory on a GB300), with in_host and in_dev
+ *     16-byte aligned: the kernels read every input that lies in in_dev's range
+ *     directly from in_host, over NVLink-C2C, and in_dev is not written;
+ *   - otherwise: one cudaMemcpyAsync of the block into in_dev first (synchronised
+ *     by the runtime when in_host is pageable); in_bytes = 0 copies nothing;
+ *   - out_host such mapped memory (16-byte aligned): the kernels write the bf16
+ *     output to it as well as to `out`; other host memory gets a cudaMemcpyAsync
+ *     of `out` after the decode; NULL: nothing.
+ * The kernels reach mapped host memory with ordinary loads and stores; the
+ * copy engine's start-up latency would be far larger than the transfer of a few
+ * KB. All other arguments are those of the two decode calls; a failed copy
+ * returns PKV_ERR_CUDA. */
 int pkv_paged_decode_attention_host(const pkv_pool_layout* layout, const pkv_decode_params* params,
                                     const void* in_host, void* in_dev, size_t in_bytes, void* out_host,
                                     const void* q, const void* k_new, const void* v_new, void* k_pool, void* v_pool,
@@ -204,7 +212,7 @@ int pkv_paged_decode_attention_host(const pkv_pool_layout* layout, const pkv_dec
 
 /* A prepared host-driven step: the arguments of pkv_paged_decode_attention_host
  * checked, planned and resolved into kernel parameters and TMA descriptors once,
- * so that each step costs the host only the copies and launches. The step keeps
+ * so that each step costs the host only its launches (and copies, if any). The step keeps
  * every pointer it is given: the buffers must outlive it and stay at their
  * addresses (a resized pool or workspace needs a new step), and the device that
  * was current at creation must be current when it runs. The handle lives in host
@@ -213,8 +221,8 @@ int pkv_paged_decode_attention_host(const pkv_pool_layout* layout, const pkv_dec
  *   pkv_step_create   arguments as pkv_paged_decode_attention_host, plus the
  *                     handle's address; returns PKV_OK or a PKV_ERR_* code
  *                     (nothing is created then)
- *   pkv_step_run      enqueues the step on the stream given at creation: the
- *                     input copy, the decode (or fused step), the output copy
+ *   pkv_step_run      enqueues the step on the stream given at creation, moving
+ *                     its data as pkv_paged_decode_attention_host does
  *   pkv_step_destroy  frees the handle (NULL is allowed); it does not wait for
  *                     work in flight, which keeps using the caller's buffers */
 typedef struct pkv_step pkv_step;

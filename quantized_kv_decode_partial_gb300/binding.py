@@ -267,13 +267,14 @@ class HostDecodeStep:
     """One decode step driven from host memory (a pkv_step: pkv_paged_decode_attention_host
     prepared once).
 
-    The step's host inputs (q, block tables, lengths and, for the fused step, the
-    new K/V rows) live in one pinned block with a device twin; each call enqueues a
-    single host-to-device copy of the block, the decode (fused with the append when
-    ``k_new``/``v_new`` are given), and the copy of the output into pinned
-    ``out_host``, on ``stream``. Write the next step's values into ``host[name]``
-    (views of the pinned block) before calling again; ``copy_tables=False`` leaves
-    the block tables out of the per-step copy (they then stay as first copied, until
+    The step's host inputs (q, lengths, the new K/V rows for the fused step, block
+    tables) live in one pinned block with a device twin. Each call enqueues the decode
+    (fused with the append when ``k_new``/``v_new`` are given); the kernels read the
+    inputs from the pinned block and write the output into pinned ``out_host`` over
+    NVLink-C2C (the library falls back to copies where the memory is not mapped).
+    Write the next step's values into ``host[name]`` (views of the pinned block)
+    before calling again; ``copy_tables=False`` keeps the block tables out of the
+    per-step data (the device copy made at construction is used, until
     ``refresh_tables()``). Pools, scale/bias planes and the workspace are device
     tensors, as for ``paged_decode_attention``.
     """

@@ -245,6 +245,23 @@ int pool_tensor_map(CUtensorMap* map, const void* base, int elem_bytes, long lon
 
 }  // namespace
 
+namespace {
+
+// The device-space address of page-locked host memory at `p`, or nullptr when it is
+// not mapped for the current device (pageable memory, say).
+void* mapped_host_address(const void* p) {
+  if (!p) return nullptr;
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return nullptr;
+  }
+  if (a.type != cudaMemoryTypeHost || !a.devicePointer) return nullptr;
+  return a.devicePointer;
+}
+
+}  // namespace
+
 extern "C" {
 
 int pkv_make_plan(const pkv_pool_layout* layout, const pkv_decode_params* params, int32_t sm_count,
@@ -481,37 +498,6 @@ int pkv_merge_partitions(const pkv_pool_layout* layout, const pkv_decode_params*
                         kPassMerge);
 }
 
-int pkv_paged_decode_attention_host(const pkv_pool_layout* layout, const pkv_decode_params* params,
-                                    const void* in_host, void* in_dev, size_t in_bytes, void* out_host,
-                                    const void* q, const void* k_new, const void* v_new, void* k_pool, void* v_pool,
-                                    void* k_scales, void* k_biases, void* v_scales, void* v_biases,
-                                    const int32_t* block_tables, const int32_t* seq_lens, float scale, void* out,
-                                    void* workspace, size_t workspace_bytes, int32_t* error_flag, void* stream) {
-  int rc = check_layout(layout);
-  if (rc) return rc;
-  rc = check_params(layout, params);
-  if (rc) return rc;
-  if (in_bytes > 0 && (!in_host || !in_dev)) return PKV_ERR_NULL_POINTER;
-  if ((k_new == nullptr) != (v_new == nullptr)) return PKV_ERR_NULL_POINTER;
-  if (!out) return PKV_ERR_NULL_POINTER;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  (void)cudaGetLastError();
-  if (in_bytes > 0) {
-    cudaError_t e = cudaMemcpyAsync(in_dev, in_host, in_bytes, cudaMemcpyHostToDevice, st);
-    if (e != cudaSuccess) return cuda_fail("input copy", e);
-  }
-  rc = enqueue_decode(layout, params, q, k_pool, v_pool, k_scales, k_biases, v_scales, v_biases, block_tables,
-                      seq_lens, scale, out, workspace, workspace_bytes, error_flag, stream, kPassPartial | kPassMerge,
-                      k_new, v_new);
-  if (rc) return rc;
-  if (out_host) {
-    const size_t rows = static_cast<size_t>(params->num_seqs) * params->num_q_heads * params->n_query;
-    cudaError_t e = cudaMemcpyAsync(out_host, out, rows * v_dim(layout) * 2, cudaMemcpyDeviceToHost, st);
-    if (e != cudaSuccess) return cuda_fail("output copy", e);
-  }
-  return PKV_OK;
-}
-
 }  // extern "C"
 
 struct pkv_step {
@@ -523,9 +509,90 @@ struct pkv_step {
   const void* out_dev;
   size_t out_bytes;
   cudaStream_t stream;
+  bool copy_in;   // the inputs go through the copy engine (host memory the device cannot address)
+  bool copy_out;  // likewise the output
 };
 
+namespace {
+
+// Prepares a host-driven step into *s. Inputs inside [in_dev, in_dev + in_bytes) of
+// mapped page-locked host memory are read by the kernels where they are; a mapped
+// out_host is written by the kernels beside `out`; anything else is copied.
+int build_step(const pkv_pool_layout* layout, const pkv_decode_params* params, const void* in_host, void* in_dev,
+               size_t in_bytes, void* out_host, const void* q, const void* k_new, const void* v_new, void* k_pool,
+               void* v_pool, void* k_scales, void* k_biases, void* v_scales, void* v_biases,
+               const int32_t* block_tables, const int32_t* seq_lens, float scale, void* out, void* workspace,
+               size_t workspace_bytes, int32_t* error_flag, void* stream, pkv_step* s) {
+  if (in_bytes > 0 && (!in_host || !in_dev)) return PKV_ERR_NULL_POINTER;
+  int rc = prepare_decode(layout, params, q, k_pool, v_pool, k_scales, k_biases, v_scales, v_biases, block_tables,
+                          seq_lens, scale, out, workspace, workspace_bytes, error_flag, kPassPartial | kPassMerge,
+                          k_new, v_new, &s->pd);
+  if (rc) return rc;
+  s->in_host = in_host;
+  s->in_dev = in_dev;
+  s->in_bytes = in_bytes;
+  s->out_host = out_host;
+  s->out_dev = out;
+  s->out_bytes = static_cast<size_t>(params->num_seqs) * params->num_q_heads * params->n_query * v_dim(layout) * 2;
+  s->stream = static_cast<cudaStream_t>(stream);
+  const void* in_map =
+      in_bytes > 0 && aligned(in_host, 16) && aligned(in_dev, 16) ? mapped_host_address(in_host) : nullptr;
+  s->copy_in = in_bytes > 0 && !in_map;
+  if (in_map) {
+    const char* lo = static_cast<const char*>(in_dev);
+    auto in_place = [&](const void* ptr) -> const void* {
+      const char* c = static_cast<const char*>(ptr);
+      return c && c >= lo && c < lo + in_bytes ? static_cast<const char*>(in_map) + (c - lo) : ptr;
+    };
+    pkv::PartialParams& p = s->pd.p;
+    p.q = static_cast<const __nv_bfloat16*>(in_place(p.q));
+    p.block_tables = static_cast<const int32_t*>(in_place(p.block_tables));
+    p.seq_lens = static_cast<const int32_t*>(in_place(p.seq_lens));
+    p.k_new = static_cast<const __nv_bfloat16*>(in_place(p.k_new));
+    p.v_new = static_cast<const __nv_bfloat16*>(in_place(p.v_new));
+    s->pd.m.seq_lens = static_cast<const int32_t*>(in_place(s->pd.m.seq_lens));
+  }
+  void* out_map = out_host && aligned(out_host, 16) ? mapped_host_address(out_host) : nullptr;
+  s->copy_out = out_host && !out_map;
+  if (out_map) {
+    s->pd.p.out_mirror = static_cast<__nv_bfloat16*>(out_map);
+    s->pd.m.out_mirror = static_cast<__nv_bfloat16*>(out_map);
+  }
+  return PKV_OK;
+}
+
+int run_step(const pkv_step& s) {
+  (void)cudaGetLastError();
+  if (s.copy_in) {
+    cudaError_t e = cudaMemcpyAsync(s.in_dev, s.in_host, s.in_bytes, cudaMemcpyHostToDevice, s.stream);
+    if (e != cudaSuccess) return cuda_fail("input copy", e);
+  }
+  int rc = launch_prepared(s.pd, s.stream);
+  if (rc) return rc;
+  if (s.copy_out) {
+    cudaError_t e = cudaMemcpyAsync(s.out_host, s.out_dev, s.out_bytes, cudaMemcpyDeviceToHost, s.stream);
+    if (e != cudaSuccess) return cuda_fail("output copy", e);
+  }
+  return PKV_OK;
+}
+
+}  // namespace
+
 extern "C" {
+
+int pkv_paged_decode_attention_host(const pkv_pool_layout* layout, const pkv_decode_params* params,
+                                    const void* in_host, void* in_dev, size_t in_bytes, void* out_host,
+                                    const void* q, const void* k_new, const void* v_new, void* k_pool, void* v_pool,
+                                    void* k_scales, void* k_biases, void* v_scales, void* v_biases,
+                                    const int32_t* block_tables, const int32_t* seq_lens, float scale, void* out,
+                                    void* workspace, size_t workspace_bytes, int32_t* error_flag, void* stream) {
+  pkv_step s{};
+  int rc = build_step(layout, params, in_host, in_dev, in_bytes, out_host, q, k_new, v_new, k_pool, v_pool, k_scales,
+                      k_biases, v_scales, v_biases, block_tables, seq_lens, scale, out, workspace, workspace_bytes,
+                      error_flag, stream, &s);
+  if (rc) return rc;
+  return run_step(s);
+}
 
 int pkv_step_create(const pkv_pool_layout* layout, const pkv_decode_params* params, const void* in_host, void* in_dev,
                     size_t in_bytes, void* out_host, const void* q, const void* k_new, const void* v_new,
@@ -534,42 +601,22 @@ int pkv_step_create(const pkv_pool_layout* layout, const pkv_decode_params* para
                     size_t workspace_bytes, int32_t* error_flag, void* stream, pkv_step** step) {
   if (!step) return PKV_ERR_NULL_POINTER;
   *step = nullptr;
-  if (in_bytes > 0 && (!in_host || !in_dev)) return PKV_ERR_NULL_POINTER;
   pkv_step* s = new (std::nothrow) pkv_step{};
   if (!s) return PKV_ERR_BAD_PARAMS;
-  int rc = prepare_decode(layout, params, q, k_pool, v_pool, k_scales, k_biases, v_scales, v_biases, block_tables,
-                          seq_lens, scale, out, workspace, workspace_bytes, error_flag, kPassPartial | kPassMerge,
-                          k_new, v_new, &s->pd);
+  int rc = build_step(layout, params, in_host, in_dev, in_bytes, out_host, q, k_new, v_new, k_pool, v_pool, k_scales,
+                      k_biases, v_scales, v_biases, block_tables, seq_lens, scale, out, workspace, workspace_bytes,
+                      error_flag, stream, s);
   if (rc) {
     delete s;
     return rc;
   }
-  s->in_host = in_host;
-  s->in_dev = in_dev;
-  s->in_bytes = in_bytes;
-  s->out_host = out_host;
-  s->out_dev = out;
-  s->out_bytes = static_cast<size_t>(params->num_seqs) * params->num_q_heads * params->n_query * v_dim(layout) * 2;
-  s->stream = static_cast<cudaStream_t>(stream);
   *step = s;
   return PKV_OK;
 }
 
 int pkv_step_run(pkv_step* step) {
   if (!step) return PKV_ERR_NULL_POINTER;
-  (void)cudaGetLastError();
-  if (step->in_bytes > 0) {
-    cudaError_t e = cudaMemcpyAsync(step->in_dev, step->in_host, step->in_bytes, cudaMemcpyHostToDevice, step->stream);
-    if (e != cudaSuccess) return cuda_fail("input copy", e);
-  }
-  int rc = launch_prepared(step->pd, step->stream);
-  if (rc) return rc;
-  if (step->out_host) {
-    cudaError_t e = cudaMemcpyAsync(step->out_host, step->out_dev, step->out_bytes, cudaMemcpyDeviceToHost,
-                                    step->stream);
-    if (e != cudaSuccess) return cuda_fail("output copy", e);
-  }
-  return PKV_OK;
+  return run_step(*step);
 }
 
 void pkv_step_destroy(pkv_step* step) { delete step; }

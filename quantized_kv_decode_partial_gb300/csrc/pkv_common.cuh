@@ -39,7 +39,8 @@ struct PartialParams {
   const __nv_bfloat16* k_biases;
   const __nv_bfloat16* v_scales;
   const __nv_bfloat16* v_biases;
-  __nv_bfloat16* out;   // [B, HQ, N, D], written directly with one partition
+  __nv_bfloat16* out;   // [B, HQ, N, DV], written directly with one partition or a cluster merge
+  __nv_bfloat16* out_mirror;  // optional second destination of those writes (mapped host memory)
   float* ws_o;          // [B*HQ*N, max_partitions, D]
   float* ws_ml;         // [B*HQ*N, max_partitions, 2]  (running max in log2 units, normaliser)
   int32_t* error_flag;  // optional
@@ -69,6 +70,7 @@ struct MergeParams {
   const float* ws_ml;
   const int32_t* seq_lens;
   __nv_bfloat16* out;
+  __nv_bfloat16* out_mirror;  // optional second destination (mapped host memory)
   int32_t* error_flag;
   int rows_per_seq;  // HQ * N
   int n_query, head_dim, max_len, partition_tokens, max_partitions;

@@ -26,11 +26,13 @@ __global__ void __launch_bounds__(kMergeThreads) pkv_merge_kernel(const __grid_c
   wait_for_prerequisite_grids();  // launched early behind the partial pass; its states are ready after this
   const int b = row / p.rows_per_seq;
   const int len = p.seq_lens[b];
-  __nv_bfloat162* out = reinterpret_cast<__nv_bfloat162*>(p.out + static_cast<size_t>(row) * p.head_dim + d);
+  const size_t o_off = static_cast<size_t>(row) * p.head_dim + d;
+  __nv_bfloat162* out = reinterpret_cast<__nv_bfloat162*>(p.out + o_off);
+  __nv_bfloat162* mirror = p.out_mirror ? reinterpret_cast<__nv_bfloat162*>(p.out_mirror + o_off) : nullptr;
   if (len < p.n_query || len > p.max_len) {  // flagged by the partial pass
     if (grp == 0) {
-      out[0] = __floats2bfloat162_rn(0.f, 0.f);
-      out[1] = __floats2bfloat162_rn(0.f, 0.f);
+      out[0] = out[1] = __floats2bfloat162_rn(0.f, 0.f);
+      if (mirror) mirror[0] = mirror[1] = __floats2bfloat162_rn(0.f, 0.f);
     }
     return;
   }
@@ -93,12 +95,13 @@ __global__ void __launch_bounds__(kMergeThreads) pkv_merge_kernel(const __grid_c
     acc.z += o.z;
     acc.w += o.w;
   }
-  if (den > 0.f) {
-    out[0] = __floats2bfloat162_rn(acc.x / den, acc.y / den);
-    out[1] = __floats2bfloat162_rn(acc.z / den, acc.w / den);
-  } else {
-    out[0] = __floats2bfloat162_rn(0.f, 0.f);
-    out[1] = __floats2bfloat162_rn(0.f, 0.f);
+  const __nv_bfloat162 v0 = den > 0.f ? __floats2bfloat162_rn(acc.x / den, acc.y / den) : __floats2bfloat162_rn(0.f, 0.f);
+  const __nv_bfloat162 v1 = den > 0.f ? __floats2bfloat162_rn(acc.z / den, acc.w / den) : __floats2bfloat162_rn(0.f, 0.f);
+  out[0] = v0;
+  out[1] = v1;
+  if (mirror) {
+    mirror[0] = v0;
+    mirror[1] = v1;
   }
 }
 

@@ -203,6 +203,13 @@ __device__ __forceinline__ uint32_t q_pair(const uint32_t (&w)[W], int kk, int r
   }
 }
 
+// Final output element i (bf16), to `out` and to its mirror when there is one.
+__device__ __forceinline__ void write_out(const PartialParams& p, size_t i, float v) {
+  const __nv_bfloat16 b = __float2bfloat16_rn(v);
+  p.out[i] = b;
+  if (p.out_mirror) p.out_mirror[i] = b;
+}
+
 // 4-bit k-steps with odd index read their codes at bit 4 of each half (16 c); their
 // B fragments carry q / 16.
 template <int BITS>
@@ -286,7 +293,7 @@ __global__ void __maxnreg__(200)
     // pass does.
     if (threadIdx.x == 0 && slot == 0 && p.error_flag) atomicOr(p.error_flag, kDevErrBadSeqLen);
     if (single || (in_cluster && slot == 0)) {
-      for (int i = threadIdx.x; i < p.nq * DV; i += C::kThreads) p.out[row0 * DV + i] = __float2bfloat16_rn(0.f);
+      for (int i = threadIdx.x; i < p.nq * DV; i += C::kThreads) write_out(p, row0 * DV + i, 0.f);
     }
     return;
   }
@@ -910,7 +917,7 @@ __global__ void __maxnreg__(200)
     const size_t orow = row0 + r;
     if (single) {
       const float L = st_l[r];
-      p.out[orow * DV + d] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
+      write_out(p, orow * DV + d, L > 0.f ? O / L : 0.f);
     } else if (in_cluster) {
       st_o[r * DV + d] = O;
     } else {
@@ -954,7 +961,7 @@ __global__ void __maxnreg__(200)
           O = fmaf(wt, oj[j], O);
         }
       }
-      p.out[(row0 + r) * DV + d] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
+      write_out(p, (row0 + r) * DV + d, L > 0.f ? O / L : 0.f);
     }
     cluster_sync();  // no CTA leaves while another still reads its shared memory
   }

@@ -399,3 +399,34 @@ def test_workspace_writes_stay_inside_the_planned_bytes(bits, D, DV):
     torch.cuda.synchronize()
     assert bool((buf[plan.workspace_bytes:] == 0x5A).all()), "write past the planned workspace"
     assert_close(out.double().cpu().numpy(), oracle_out(case), f"{sp.name}")
+
+
+@pytest.mark.parametrize("pinned", [True, False], ids=["mapped_pinned", "pageable"])
+def test_one_shot_host_entry_with_pinned_and_pageable_memory(pinned):
+    # mapped page-locked memory is copied by the SMs, pageable memory by the copy engine
+    import ctypes
+    lib = B.load_library()
+    sp = spec(f"host_one_shot_{pinned}", length_range=(1, 300))
+    case = make_case(sp)
+    d = case.to(DEV)
+    ref = run_gpu(d, partition_tokens=48)
+    qb = case.q.numel() * 2
+    blk_host = torch.empty(qb, dtype=torch.uint8)
+    blk_host = blk_host.pin_memory() if pinned else blk_host
+    blk_host.copy_(case.q.view(torch.uint8).reshape(-1))
+    q_dev = torch.zeros_like(d.q)
+    out_host = torch.full(ref.shape, float("nan"), dtype=torch.bfloat16)
+    out_host = out_host.pin_memory() if pinned else out_host
+    out_dev = torch.empty_like(ref)
+    layout = B.layout_for(d.k_pool, sp.head_dim, 16, v_pool=d.v_pool)
+    params = B.DecodeParams(sp.num_seqs, sp.num_q_heads, 1, d.block_tables.shape[1], 48)
+    plan = B.make_plan(layout, params)
+    ws = torch.empty(max(1, plan.workspace_bytes), dtype=torch.uint8, device=DEV)
+    rc = lib.pkv_paged_decode_attention_host(
+        ctypes.byref(layout), ctypes.byref(params), blk_host.data_ptr(), q_dev.data_ptr(), qb, out_host.data_ptr(),
+        q_dev.data_ptr(), None, None, d.k_pool.data_ptr(), d.v_pool.data_ptr(), None, None, None, None,
+        d.block_tables.data_ptr(), d.seq_lens.data_ptr(), float(case.scale), out_dev.data_ptr(), ws.data_ptr(),
+        ws.numel(), None, torch.cuda.current_stream(DEV).cuda_stream)
+    assert rc == B.PKV_OK
+    torch.cuda.synchronize()
+    assert torch.equal(out_host.view(torch.int16), ref.cpu().view(torch.int16))
