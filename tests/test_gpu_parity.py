@@ -430,3 +430,35 @@ def test_one_shot_host_entry_with_pinned_and_pageable_memory(pinned):
     assert rc == B.PKV_OK
     torch.cuda.synchronize()
     assert torch.equal(out_host.view(torch.int16), ref.cpu().view(torch.int16))
+
+
+@pytest.mark.parametrize("bits", [16, 4])
+def test_table_entries_past_the_length_are_never_used(bits):
+    # The partial pass issues a partition's first chunks before the length is known.
+    # Table entries past each sequence's length (here valid block ids of other data, or
+    # ids far out of range) must change neither the output nor the error word.
+    sp = spec(f"stale_tables_{bits}", num_seqs=4, head_dim=256 if bits == 4 else 128, bits=bits,
+              block_size=32 if bits == 4 else 16, length_range=(1, 200))
+    case = make_case(sp)
+    # leave room past every length: a wider table
+    wide = torch.full((sp.num_seqs, case.block_tables.shape[1] + 16), -1, dtype=torch.int32)
+    wide[:, :case.block_tables.shape[1]] = case.block_tables
+    ref = None
+    for fill in ("valid", "out_of_range"):
+        tb = wide.clone()
+        g = torch.Generator().manual_seed(3)
+        for b in range(sp.num_seqs):
+            used = -(-case.lens_host[b] // sp.block_size)
+            n = tb.shape[1] - used
+            tb[b, used:] = (torch.randint(0, case.num_blocks, (n,), generator=g) if fill == "valid"
+                            else torch.full((n,), case.num_blocks + 1000, dtype=torch.int64)).to(torch.int32)
+        d = case.to(DEV)
+        d.block_tables = tb.to(DEV)
+        for pt in (16 if bits == 16 else 32, 64, 1 << 12):
+            err = torch.zeros(1, dtype=torch.int32, device=DEV)
+            out = run_gpu(d, partition_tokens=pt, error_flag=err)
+            torch.cuda.synchronize()
+            assert int(err.item()) == 0, (fill, pt)
+            if ref is None:
+                ref = oracle_out(case)
+            assert_close(out.double().cpu().numpy(), ref, f"{sp.name} {fill} partition={pt}")
