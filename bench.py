@@ -424,10 +424,10 @@ def run_ours(args):
         torch.cuda.synchronize(dev)
         ms_partial = replay_timed([(g_part, K // chunk)] + ([(g_part_rest, 1)] if g_part_rest else []))
 
-    # end to end through the public call: per step, one copy of the step's inputs (q,
-    # block tables, lengths and, for the fused step, the new K/V rows) from pinned host
-    # memory, the decode, and the copy of the output back to pinned host memory, all
-    # enqueued by one C call (pkv_paged_decode_attention_host)
+    # end to end through the public host-driven step (pkv_step_run): per step the
+    # kernels read the step's inputs (q, block tables, lengths and, for the fused step,
+    # the new K/V rows) from pinned host memory and write the output back into pinned
+    # host memory, over NVLink-C2C
     host_steps = []
     for L in layers:
         c = L["insts"][0]
@@ -500,10 +500,10 @@ def run_ours(args):
                          "peak_source": f"{peak_kind} hbm_gbs", "frac_of_nominal_7900": achieved / 7900.0},
             "e2e": {"value": weak_scaling_rate(step_bytes, world, e2e_ms), "unit": "GB/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-                    "what": "pkv_paged_decode_attention_host per step: one copy of q, block tables, lengths"
+                    "what": "host-driven step (pkv_step_run) per step: q, block tables, lengths"
                             + (" and the new K/V rows" if args.step == "fused" else "")
-                            + " from pinned host memory, the " + ("fused step" if args.step == "fused" else "decode")
-                            + " and the output copied back, enqueued by one C call; the KV pool is "
+                            + " read from pinned host memory and the output written back to pinned host memory by "
+                              "the kernels (over NVLink-C2C, counted in h2d/d2h bytes); the KV pool is "
                               "device-resident cache state"},
             "gpu_launches": launches_per_step * K,
             "clocks": clk,
