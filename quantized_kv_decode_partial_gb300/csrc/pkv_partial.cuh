@@ -559,12 +559,29 @@ __global__ void __maxnreg__(200)
             for (int e = 0; e < 4; ++e) sacc[nt][e] = 0.f;
           const int lrow = tile * 16 + lrow_n;
           if constexpr (BITS == 16) {
+            // A CTA alone on its SM is bound by latency: two accumulators (even and odd
+            // k-steps) halve its dependent MMA chain. Elsewhere one chain costs fewer
+            // instructions.
+            constexpr int kChains = SOLO ? 2 : 1;
+            float sacc2[NT][4];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) sacc2[nt][e] = 0.f;
 #pragma unroll
             for (int kk = 0; kk < C::kKs; ++kk) {
               uint32_t a[4];
               ldsm_x4(swizzled<C::kRB>(kpl + (kk >> 2) * C::kBoxBytes, lrow, (kk & 3) * 2 + lch_n), a);
 #pragma unroll
-              for (int nt = 0; nt < NT; ++nt) mma_bf16(sacc[nt], a[0], a[1], a[2], a[3], qf[kk][nt][0], qf[kk][nt][1]);
+              for (int nt = 0; nt < NT; ++nt)
+                mma_bf16((kChains == 2 && (kk & 1)) ? sacc2[nt] : sacc[nt], a[0], a[1], a[2], a[3], qf[kk][nt][0],
+                         qf[kk][nt][1]);
+            }
+            if constexpr (kChains == 2) {
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) sacc[nt][e] += sacc2[nt][e];
             }
           } else {
             // scales of keys g and g + 8 of this tile, all groups
