@@ -123,8 +123,9 @@ typedef struct pkv_decode_params {
 typedef struct pkv_plan {
   int32_t partition_tokens; /* resolved rows per partition */
   int32_t max_partitions;   /* partitions per (sequence, KV head) in the grid and the workspace: those
-                               of the longest admissible sequence, or with a window the most that
-                               window + n_query - 1 rows can touch */
+                               of the longest admissible sequence, or with a window those that tile
+                               window + n_query - 1 rows from a base rounded down to a multiple of 32
+                               rows (at most window + n_query + 30 rows) */
   int32_t chunk_rows;       /* rows staged per pipeline step */
   int32_t sm_count;         /* SM count the plan was made for */
   int32_t threads_per_cta;  /* partial-kernel CTA size */

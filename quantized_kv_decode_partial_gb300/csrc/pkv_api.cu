@@ -79,6 +79,14 @@ int check_params(const pkv_pool_layout* L, const pkv_decode_params* P) {
 
 int round_up(long long x, int m) { return static_cast<int>((x + m - 1) / m * m); }
 
+// Rows a step can read per sequence, counted from its partition base: the whole
+// table, or with a window the span of W + N - 1 rows its queries see plus the
+// alignment of the base to a chunk boundary below it.
+long long window_rows(const pkv_decode_params* P, long long max_len) {
+  if (P->window <= 0) return max_len;
+  return std::min<long long>(max_len, static_cast<long long>(P->window) + P->n_query - 1 + (pkv::kWindowAlign - 1));
+}
+
 // `solo` (optional) receives whether the plan launches the variant for grids of at
 // most one CTA per SM.
 int plan_impl(const pkv_pool_layout* L, const pkv_decode_params* P, int sm_count, pkv_plan* out,
@@ -99,8 +107,7 @@ int plan_impl(const pkv_pool_layout* L, const pkv_decode_params* P, int sm_count
     const long long kv_row = stored_row_bytes(L, L->head_dim) + stored_row_bytes(L, v_dim(L));  // K + V
     const long long floor_rows = 256;
     const long long rich_rows = std::max<long long>(floor_rows, (512ll << 10) / kv_row);
-    // rows a step can read per sequence: the table, or the window's span
-    const long long span = P->window > 0 ? std::min<long long>(max_len, P->window + P->n_query - 1) : max_len;
+    const long long span = window_rows(P, max_len);
     part = round_up(span, ch);
     while (part > floor_rows) {
       const long long ctas = units * ((span + part - 1) / part);
@@ -112,12 +119,8 @@ int plan_impl(const pkv_pool_layout* L, const pkv_decode_params* P, int sm_count
   }
   if (part >= max_len) part = round_up(max_len, ch);
   // Partitions per (sequence, KV head) in the grid and the workspace: all of the table,
-  // or, with a window, the most that its span of rows can touch.
-  int max_parts = ceil_div(max_len, part);
-  if (P->window > 0) {
-    const long long span = std::min<long long>(max_len, static_cast<long long>(P->window) + P->n_query - 1);
-    max_parts = std::min<int>(max_parts, ceil_div(span, part) + 1);
-  }
+  // or, with a window, enough to tile the rows from the aligned window base on.
+  const int max_parts = ceil_div(window_rows(P, max_len), part);
   const long long nq = static_cast<long long>(P->num_q_heads / L->num_kv_heads) * P->n_query;
   // A grid of at most one CTA per SM takes the variant with more warps and stages
   // per CTA, where there is one for this shape.

@@ -316,6 +316,20 @@ __device__ __forceinline__ void wait_for_prerequisite_grids() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// Alignment of the first partition of a windowed sequence: a multiple of every
+// chunk size (16 or 32 rows), so partition starts stay on chunk boundaries.
+constexpr int kWindowAlign = 32;
+
+// Row at which partition 0 of a sequence starts. Without a window, row 0. With a
+// window of W rows, the chunk boundary at or below the lowest row any of the N
+// queries sees (len - N + 1 - W), so the partitions tile the visible span and
+// nothing below it.
+__host__ __device__ __forceinline__ int partition_base(int len, int n_query, int window) {
+  if (window <= 0) return 0;
+  const int lo = len - n_query + 1 - window;
+  return lo > 0 ? lo / kWindowAlign * kWindowAlign : 0;
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

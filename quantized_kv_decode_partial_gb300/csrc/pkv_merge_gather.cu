@@ -9,11 +9,34 @@ namespace pkv {
 // output; partitions whose maximum is -inf saw no visible key and are skipped
 // (kvq4-decode.ts and multi-query.ts merge kernels).
 // Output = sum_p 2^(m_p-M) o_p / sum_p 2^(m_p-M) l_p.
-// The CTA's threads form kMergeGroups groups of D/4 threads; a thread owns four
-// consecutive head dims and every kMergeGroups-th partition, with four partitions'
-// loads in flight at a time, and the groups' sums are added in shared memory.
+// The CTA's threads form 256 / (D/4) groups of D/4 threads; a thread owns four
+// consecutive head dims and every groups-th partition. Each group merges its
+// partitions online against its own running maximum, and the groups' states are
+// combined once in shared memory. A thread's first kMergeUnroll partition slots are
+// requested together with the sequence length (the slots exist for every row; those
+// past the row's partition count are dropped once the length arrives), so a row with
+// at most kMergeUnroll partitions per group costs one memory round trip.
 constexpr int kMergeThreads = 256;
 constexpr int kMergeUnroll = 4;
+
+__device__ __forceinline__ void merge_one(float2 s, const float4& v, float& M, float& den, float4& acc) {
+  if (s.x == -INFINITY) return;  // no visible key in this partition
+  if (s.x > M) {                 // new running maximum: rescale what is summed so far
+    const float c = fast_exp2(M - s.x);  // 0 while nothing is summed (M = -inf)
+    den *= c;
+    acc.x *= c;
+    acc.y *= c;
+    acc.z *= c;
+    acc.w *= c;
+    M = s.x;
+  }
+  const float w = fast_exp2(s.x - M);
+  den = fmaf(w, s.y, den);
+  acc.x = fmaf(w, v.x, acc.x);
+  acc.y = fmaf(w, v.y, acc.y);
+  acc.z = fmaf(w, v.z, acc.z);
+  acc.w = fmaf(w, v.w, acc.w);
+}
 
 __global__ void __launch_bounds__(kMergeThreads) pkv_merge_kernel(const __grid_constant__ MergeParams p) {
   __shared__ float red_m[kMergeThreads];
@@ -25,6 +48,17 @@ __global__ void __launch_bounds__(kMergeThreads) pkv_merge_kernel(const __grid_c
   const int grp = threadIdx.x / lanes, d = (threadIdx.x % lanes) * 4;
   wait_for_prerequisite_grids();  // launched early behind the partial pass; its states are ready after this
   const int b = row / p.rows_per_seq;
+  const float2* ml = reinterpret_cast<const float2*>(p.ws_ml) + static_cast<size_t>(row) * p.max_partitions;
+  const float4* ob = reinterpret_cast<const float4*>(p.ws_o + static_cast<size_t>(row) * p.max_partitions * p.head_dim + d);
+  const int ostride = p.head_dim / 4;
+  float2 s[kMergeUnroll];
+  float4 v[kMergeUnroll];
+#pragma unroll
+  for (int u = 0; u < kMergeUnroll; ++u) {
+    const int i = grp + u * groups;
+    s[u] = i < p.max_partitions ? ml[i] : make_float2(-INFINITY, 0.f);
+    v[u] = i < p.max_partitions ? ob[static_cast<size_t>(i) * ostride] : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   const int len = p.seq_lens[b];
   const size_t o_off = static_cast<size_t>(row) * p.head_dim + d;
   __nv_bfloat162* out = reinterpret_cast<__nv_bfloat162*>(p.out + o_off);
@@ -36,64 +70,47 @@ __global__ void __launch_bounds__(kMergeThreads) pkv_merge_kernel(const __grid_c
     }
     return;
   }
-  // Workspace slot i holds partition first + i: with a sliding window the partial pass
-  // starts at the partition holding the lowest visible row.
-  const int first = p.window > 0 ? max(0, len - p.n_query + 1 - p.window) / p.partition_tokens : 0;
-  const int np = (len + p.partition_tokens - 1) / p.partition_tokens - first;
-  const float2* ml = reinterpret_cast<const float2*>(p.ws_ml) + static_cast<size_t>(row) * p.max_partitions;
-  const float4* ob = reinterpret_cast<const float4*>(p.ws_o + static_cast<size_t>(row) * p.max_partitions * p.head_dim + d);
-  const int ostride = p.head_dim / 4;
+  // Slot i holds the partition of rows [base + i P, base + (i + 1) P).
+  const int base = partition_base(len, p.n_query, p.window);
+  const int np = (len - base + p.partition_tokens - 1) / p.partition_tokens;
 
-  float M = -INFINITY;
-  for (int i0 = grp; i0 < np; i0 += groups * kMergeUnroll) {
-    float mu[kMergeUnroll];
+  float M = -INFINITY, den = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int u = 0; u < kMergeUnroll; ++u)
+    if (grp + u * groups < np) merge_one(s[u], v[u], M, den, acc);
+  for (int i0 = grp + kMergeUnroll * groups; i0 < np; i0 += groups * kMergeUnroll) {
 #pragma unroll
     for (int u = 0; u < kMergeUnroll; ++u) {
       const int i = i0 + u * groups;
-      mu[u] = i < np ? ml[i].x : -INFINITY;
+      s[u] = i < np ? ml[i] : make_float2(-INFINITY, 0.f);
+      v[u] = i < np ? ob[static_cast<size_t>(i) * ostride] : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
-    for (int u = 0; u < kMergeUnroll; ++u) M = fmaxf(M, mu[u]);
+    for (int u = 0; u < kMergeUnroll; ++u) merge_one(s[u], v[u], M, den, acc);
   }
   red_m[threadIdx.x] = M;
-  __syncthreads();
-  for (int g = 0; g < groups; ++g) M = fmaxf(M, red_m[g * lanes]);  // one value per group (its first thread's)
-
-  float den = 0.f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (M != -INFINITY) {
-    for (int i0 = grp; i0 < np; i0 += groups * kMergeUnroll) {
-      float2 s[kMergeUnroll];
-      float4 v[kMergeUnroll];
-#pragma unroll
-      for (int u = 0; u < kMergeUnroll; ++u) {
-        const int i = i0 + u * groups;
-        s[u] = i < np ? ml[i] : make_float2(-INFINITY, 0.f);
-        v[u] = i < np ? ob[static_cast<size_t>(i) * ostride] : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-#pragma unroll
-      for (int u = 0; u < kMergeUnroll; ++u) {
-        if (s[u].x == -INFINITY) continue;
-        const float w = fast_exp2(s[u].x - M);
-        den = fmaf(w, s[u].y, den);
-        acc.x = fmaf(w, v[u].x, acc.x);
-        acc.y = fmaf(w, v[u].y, acc.y);
-        acc.z = fmaf(w, v[u].z, acc.z);
-        acc.w = fmaf(w, v[u].w, acc.w);
-      }
-    }
-  }
   red_o[threadIdx.x] = acc;
   red_l[threadIdx.x] = den;
   __syncthreads();
   if (grp != 0) return;
-  for (int g = 1; g < groups; ++g) {
-    const float4 o = red_o[g * lanes + threadIdx.x];
-    den += red_l[g * lanes + threadIdx.x];
-    acc.x += o.x;
-    acc.y += o.y;
-    acc.z += o.z;
-    acc.w += o.w;
+  float Mall = M;
+  for (int g = 1; g < groups; ++g) Mall = fmaxf(Mall, red_m[g * lanes + threadIdx.x]);
+  den = 0.f;
+  acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (Mall != -INFINITY) {
+    for (int g = 0; g < groups; ++g) {
+      const int k = g * lanes + threadIdx.x;
+      const float mg = red_m[k];
+      if (mg == -INFINITY) continue;
+      const float w = fast_exp2(mg - Mall);
+      const float4 o = red_o[k];
+      den = fmaf(w, red_l[k], den);
+      acc.x = fmaf(w, o.x, acc.x);
+      acc.y = fmaf(w, o.y, acc.y);
+      acc.z = fmaf(w, o.z, acc.z);
+      acc.w = fmaf(w, o.w, acc.w);
+    }
   }
   const __nv_bfloat162 v0 = den > 0.f ? __floats2bfloat162_rn(acc.x / den, acc.y / den) : __floats2bfloat162_rn(0.f, 0.f);
   const __nv_bfloat162 v1 = den > 0.f ? __floats2bfloat162_rn(acc.z / den, acc.w / den) : __floats2bfloat162_rn(0.f, 0.f);

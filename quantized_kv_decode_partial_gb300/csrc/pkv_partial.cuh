@@ -298,12 +298,12 @@ __global__ void __maxnreg__(200)
     return;
   }
   // With a sliding window only rows >= len - N + 1 - window are visible to any query;
-  // the grid covers the partitions from the one holding that row on.
+  // the partitions then start at the chunk boundary below that row, so the grid
+  // tiles the visible span evenly.
   const int win_lo = p.window > 0 ? max(0, len - N + 1 - p.window) : 0;
-  const int part = win_lo / p.partition_tokens + slot;
-  const int t0 = part * p.partition_tokens;
+  const int t0 = partition_base(len, N, p.window) + slot * p.partition_tokens;
   const int t_end = min(len, t0 + p.partition_tokens);
-  const bool empty = t0 >= len || t_end <= win_lo;
+  const bool empty = t0 >= len;
   if (empty && !in_cluster) return;  // the merge pass never reads this partition
   // first row this CTA reads: the partition start, or the chunk holding the window's lowest row
   const int t_first = max(t0, win_lo / C::kCh * C::kCh);

@@ -66,8 +66,9 @@ def test_plan_for_workloads(lib, name):
     ch = 16 if sp.bits == 16 else 32  # partitions are whole multiples of this
     assert plan.chunk_rows in (16, 32) and plan.partition_tokens % ch == 0 and ch % plan.chunk_rows == 0
     table_parts = -(-max_blocks * sp.block_size // plan.partition_tokens)
-    if sp.window:  # only the partitions a window can touch
-        assert plan.max_partitions == min(table_parts, -(-(sp.window + sp.n_query - 1) // plan.partition_tokens) + 1)
+    if sp.window:  # only the partitions that tile the window's span from its 32-row aligned base
+        rows = min(max_blocks * sp.block_size, sp.window + sp.n_query - 1 + 31)
+        assert plan.max_partitions == -(-rows // plan.partition_tokens)
     else:
         assert plan.max_partitions == table_parts
     if sp.partition_tokens > 0:
