@@ -116,6 +116,25 @@ int plan_impl(const pkv_pool_layout* L, const pkv_decode_params* P, int sm_count
       if (half < rich_rows && ctas >= slots) break;
       part = half;
     }
+    // With a window, every sequence longer than it reads the same span, so the
+    // (sequence, KV head) units carry even work. When the grid above is at most two
+    // waves (a short step, where the merge launch shows) and 2..16 partitions per unit
+    // make a grid of one wave that fills at least three quarters of it, with CTAs of
+    // at least 512 KB, take the most partitions that do: the partitions then merge
+    // inside their clusters, with no workspace and no second launch.
+    const long long nq_rows = static_cast<long long>(P->num_q_heads / L->num_kv_heads) * P->n_query;
+    const PartialInfo two = partial_info(L->bits, L->head_dim, v_dim(L), static_cast<int>(nq_rows), false);
+    const long long default_ctas = units * ((span + part - 1) / part);
+    if (P->window > 0 && default_ctas <= 2 * slots && two.exists && two.smem_bytes <= 114 * 1024) {
+      for (int k = pkv::kMaxClusterParts; k >= 2; --k) {
+        const long long pk = round_up((span + k - 1) / k, ch);
+        const long long ctas = units * ((span + pk - 1) / pk);
+        if (pk >= rich_rows && ctas <= slots && 4 * ctas >= 3 * slots) {
+          part = pk;
+          break;
+        }
+      }
+    }
   }
   if (part >= max_len) part = round_up(max_len, ch);
   // Partitions per (sequence, KV head) in the grid and the workspace: all of the table,

@@ -316,6 +316,26 @@ __device__ __forceinline__ void wait_for_prerequisite_grids() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// Read-only global loads kept in program order (volatile): a load issued before a
+// branch is never moved past it, so its latency overlaps whatever the branch waits for.
+__device__ __forceinline__ uint4 ld_nc_keep_v4(const void* ptr) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(ptr));
+  return v;
+}
+__device__ __forceinline__ uint2 ld_nc_keep_v2(const void* ptr) {
+  uint2 v;
+  asm volatile("ld.global.nc.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(ptr));
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_nc_keep_u32(const void* ptr) {
+  uint32_t v;
+  asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(ptr));
+  return v;
+}
+
 // Alignment of the first partition of a windowed sequence: a multiple of every
 // chunk size (16 or 32 rows), so partition starts stay on chunk boundaries.
 constexpr int kWindowAlign = 32;

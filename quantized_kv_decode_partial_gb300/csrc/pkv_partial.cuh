@@ -166,12 +166,12 @@ __device__ __forceinline__ void q_load_words(const __nv_bfloat16* qrow, int t, b
   if constexpr (BITS == 16) {
 #pragma unroll
     for (int i = 0; i < D / 8; ++i) {  // i = 2 kk + reg: dims 16 kk + 8 reg + 2t, +1
-      w[i] = valid ? __ldg(reinterpret_cast<const uint32_t*>(qrow + 8 * i + 2 * t)) : 0u;
+      w[i] = valid ? ld_nc_keep_u32(qrow + 8 * i + 2 * t) : 0u;
     }
   } else if constexpr (BITS == 4) {
 #pragma unroll
     for (int c = 0; c < D / 32; ++c) {  // c = 2 grp + cc: dims 32 c + 8t .. + 7
-      const uint4 v = valid ? __ldg(reinterpret_cast<const uint4*>(qrow + 32 * c + 8 * t)) : make_uint4(0, 0, 0, 0);
+      const uint4 v = valid ? ld_nc_keep_v4(qrow + 32 * c + 8 * t) : make_uint4(0, 0, 0, 0);
       w[4 * c] = v.x;
       w[4 * c + 1] = v.y;
       w[4 * c + 2] = v.z;
@@ -180,7 +180,7 @@ __device__ __forceinline__ void q_load_words(const __nv_bfloat16* qrow, int t, b
   } else {
 #pragma unroll
     for (int c = 0; c < D / 16; ++c) {  // c = 4 grp + quarter: dims 16 c + 4t .. + 3
-      const uint2 v = valid ? __ldg(reinterpret_cast<const uint2*>(qrow + 16 * c + 4 * t)) : make_uint2(0, 0);
+      const uint2 v = valid ? ld_nc_keep_v2(qrow + 16 * c + 4 * t) : make_uint2(0, 0);
       w[2 * c] = v.x;
       w[2 * c + 1] = v.y;
     }
@@ -284,8 +284,17 @@ __global__ void __maxnreg__(200)
   if (p.window == 0 && leader) {
     const long long r = static_cast<long long>(slot) * p.partition_tokens + (pg + lane * C::kWP) * C::kCh;
     const long long blk = r / p.block_size < p.max_blocks ? r / p.block_size : p.max_blocks - 1;
-    tbl_pre = __ldg(p.block_tables + static_cast<size_t>(b) * p.max_blocks + blk);
+    tbl_pre = static_cast<int>(ld_nc_keep_u32(p.block_tables + static_cast<size_t>(b) * p.max_blocks + blk));
   }
+  // The stage barriers do not depend on len either: set them up while it is in flight.
+  if (threadIdx.x == 0) {
+    prefetch_tensormap(&tmap_k);  // the first copies need both descriptors
+    prefetch_tensormap(&tmap_v);
+    for (int s = 0; s < C::kWarps * C::kStagesPerWarp; ++s) mbar_init(smem_addr(&full_bar[s]), 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
 
   if (len < N || len > p.max_blocks * p.block_size) {
     // Every CTA of this sequence sees the same length and leaves here (before any
@@ -308,15 +317,6 @@ __global__ void __maxnreg__(200)
   // first row this CTA reads: the partition start, or the chunk holding the window's lowest row
   const int t_first = max(t0, win_lo / C::kCh * C::kCh);
   const int nchunks = empty ? 0 : (t_end - t_first + C::kCh - 1) / C::kCh;  // an empty cluster member still merges
-
-  if (threadIdx.x == 0) {
-    prefetch_tensormap(&tmap_k);  // the first copies need both descriptors
-    prefetch_tensormap(&tmap_v);
-    for (int s = 0; s < C::kWarps * C::kStagesPerWarp; ++s) mbar_init(smem_addr(&full_bar[s]), 1);
-    *abort_flag = 0;
-    fence_barrier_init();
-  }
-  __syncthreads();
 
   // O^T accumulators and softmax state.
   float o[C::kMt][NT][4];
