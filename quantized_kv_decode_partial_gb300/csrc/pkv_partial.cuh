@@ -20,8 +20,9 @@
 //    coalesced load and resolved into TMA row coordinates once per 32 chunks. A
 //    chunk of one page and KV head is contiguous in the pool, so it travels as
 //    2-D TMA boxes (rows of 64 or 128 bytes, hardware-swizzled so the ldmatrix
-//    reads below are free of bank conflicts) plus 1-D bulk copies of the affine
-//    scale/bias rows. K and V rows may have different head dims.
+//    reads below are free of bank conflicts); the affine scale/bias rows come by
+//    16-byte cp.async copies of the warp's lanes, tracked by the same mbarrier.
+//    K and V rows may have different head dims.
 //  * Each K/V row in shared memory is read once and multiplied against all
 //    REP*N query rows of its KV head (GQA reuse) with warp-level tensor-core
 //    MMA (m16n8k16, bf16 in, f32 out):
@@ -86,6 +87,8 @@ struct PartialCfg {
   static constexpr int kOffVs = kOffKb + kSbBytes;
   static constexpr int kOffVb = kOffVs + kSbBytesV;
   static constexpr int kTxBytes = kOffVb + kSbBytesV;
+  static constexpr int kTmaBytes = kPlaneBytes + kPlaneBytesV;  // the part the TMA copies bring
+  static constexpr int kSbCopies = (2 * kSbBytes + 2 * kSbBytesV) / 16;  // 16-byte copies of scales and biases
   static constexpr int kStageBytes = (kTxBytes + 1023) / 1024 * 1024;
   static constexpr int kBarrierBytes = SOLO ? 512 : 256;
   static constexpr int kSoloBudget = 227 * 1024 - kBarrierBytes - 1024;  // stage ring of a CTA alone on its SM
@@ -379,26 +382,45 @@ __global__ void __maxnreg__(200)
           __syncwarp();
         }
       }
+      const uint32_t fb = smem_addr(&my_full[is]);
+      const uint32_t st = smem_addr(my_ring + is * C::kStageBytes);
+      if constexpr (C::kQuant) {
+        // The chunk's scale and bias rows: 16-byte cp.async copies spread over the lanes,
+        // which keeps the TMA unit to two copies per stage. Each lane makes the stage's
+        // barrier wait for its copies before lane 0 arrives, so the phase cannot complete
+        // without them.
+        if (row >= 0) {
+          constexpr int nk = C::kSbBytes / 16, nv = C::kSbBytesV / 16;
+          const size_t sk = static_cast<size_t>(row) * C::kGroups, sv = static_cast<size_t>(row) * C::kGroupsV;
+#pragma unroll
+          for (int c0 = 0; c0 < C::kSbCopies; c0 += 32) {
+            const int c = c0 + lane;
+            if (c < C::kSbCopies) {
+              const int plane = c < 2 * nk ? c / nk : 2 + (c - 2 * nk) / nv;
+              const int k = c < 2 * nk ? c % nk : (c - 2 * nk) % nv;
+              const __nv_bfloat16* src = plane == 0   ? p.k_scales + sk
+                                         : plane == 1 ? p.k_biases + sk
+                                         : plane == 2 ? p.v_scales + sv
+                                                      : p.v_biases + sv;
+              const int off = plane == 0 ? C::kOffKs : plane == 1 ? C::kOffKb : plane == 2 ? C::kOffVs : C::kOffVb;
+              cp_async_16(st + off + 16 * k, reinterpret_cast<const char*>(src) + 16 * k, policy);
+            }
+          }
+          cp_async_mbar_arrive(fb);
+        }
+        __syncwarp();
+      }
       if (lane == 0) {
-        const uint32_t fb = smem_addr(&my_full[is]);
         my_ok[is] = row >= 0 ? 1 : 0;
         if (row >= 0) {
           fence_proxy_async_smem();  // this warp's reads of the stage precede the copies into it
-          mbar_arrive_expect_tx(fb, C::kTxBytes);
-          const uint32_t st = smem_addr(my_ring + is * C::kStageBytes);
+          mbar_arrive_expect_tx(fb, C::kTmaBytes);
 #pragma unroll
           for (int bx = 0; bx < C::kBoxes; ++bx)
             tma_load_2d(st + bx * C::kBoxBytes, &tmap_k, bx * (C::kRB / C::kElemBytes), row, fb, policy);
 #pragma unroll
           for (int bx = 0; bx < C::kBoxesV; ++bx)
             tma_load_2d(st + C::kOffV + bx * C::kBoxBytesV, &tmap_v, bx * (C::kRBV / C::kElemBytes), row, fb, policy);
-          if constexpr (C::kQuant) {
-            const size_t sk = static_cast<size_t>(row) * C::kGroups, sv = static_cast<size_t>(row) * C::kGroupsV;
-            bulk_load(st + C::kOffKs, p.k_scales + sk, C::kSbBytes, fb, policy);
-            bulk_load(st + C::kOffKb, p.k_biases + sk, C::kSbBytes, fb, policy);
-            bulk_load(st + C::kOffVs, p.v_scales + sv, C::kSbBytesV, fb, policy);
-            bulk_load(st + C::kOffVb, p.v_biases + sv, C::kSbBytesV, fb, policy);
-          }
         } else {
           if (p.error_flag) atomicOr(p.error_flag, kDevErrBadBlock);
           mbar_arrive(fb);
