@@ -207,8 +207,12 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// 2-D view of one pool plane: rows = num_blocks*HK*BS, `row_elems` elements per
-// row; boxes of `box_rows` rows by `box_row_bytes` bytes with the matching swizzle.
+// 3-D view of one pool plane: rows = num_blocks*HK*BS of `row_elems` elements, each
+// row seen as row_bytes / box_row_bytes segments of `box_row_bytes` bytes, with the
+// segment index outermost (dims: element in segment, row, segment; strides: the row
+// pitch, then the segment width). One box takes `box_rows` rows of every segment and
+// lands segment-major ([segment][row][box_row_bytes], swizzled to match), so a chunk
+// of a plane is one TMA copy whatever its width.
 int encode_pool_tensor_map(CUtensorMap* map, const void* base, int elem_bytes, long long row_elems, long long rows,
                            int box_row_bytes, int box_rows) {
   auto encode = tensor_map_encoder();
@@ -217,12 +221,16 @@ int encode_pool_tensor_map(CUtensorMap* map, const void* base, int elem_bytes, l
     return PKV_ERR_CUDA;
   }
   const CUtensorMapDataType dt = elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_elems), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_elems * elem_bytes)};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_row_bytes / elem_bytes), static_cast<cuuint32_t>(box_rows)};
-  cuuint32_t estr[2] = {1, 1};
+  const long long row_bytes = row_elems * elem_bytes;
+  const long long segments = row_bytes / box_row_bytes;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(box_row_bytes / elem_bytes), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(segments)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(box_row_bytes)};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(box_row_bytes / elem_bytes), static_cast<cuuint32_t>(box_rows),
+                       static_cast<cuuint32_t>(segments)};
+  cuuint32_t estr[3] = {1, 1, 1};
   const CUtensorMapSwizzle sw = box_row_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-  CUresult r = encode(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+  CUresult r = encode(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                       sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     std::snprintf(g_cuda_error, sizeof(g_cuda_error), "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));

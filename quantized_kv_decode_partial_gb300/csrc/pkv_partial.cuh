@@ -19,8 +19,9 @@
 //    each chunk for their own rows.) The block table is read 32 entries per
 //    coalesced load and resolved into TMA row coordinates once per 32 chunks. A
 //    chunk of one page and KV head is contiguous in the pool, so it travels as
-//    2-D TMA boxes (rows of 64 or 128 bytes, hardware-swizzled so the ldmatrix
-//    reads below are free of bank conflicts); the affine scale/bias rows come by
+//    one 3-D TMA copy per plane (each row split into segments of 64 or 128 bytes,
+//    segment-major in shared memory and hardware-swizzled so the ldmatrix reads
+//    below are free of bank conflicts); the affine scale/bias rows come by
 //    16-byte cp.async copies of the warp's lanes, tracked by the same mbarrier.
 //    K and V rows may have different head dims.
 //  * Each K/V row in shared memory is read once and multiplied against all
@@ -415,12 +416,8 @@ __global__ void __maxnreg__(200)
         if (row >= 0) {
           fence_proxy_async_smem();  // this warp's reads of the stage precede the copies into it
           mbar_arrive_expect_tx(fb, C::kTmaBytes);
-#pragma unroll
-          for (int bx = 0; bx < C::kBoxes; ++bx)
-            tma_load_2d(st + bx * C::kBoxBytes, &tmap_k, bx * (C::kRB / C::kElemBytes), row, fb, policy);
-#pragma unroll
-          for (int bx = 0; bx < C::kBoxesV; ++bx)
-            tma_load_2d(st + C::kOffV + bx * C::kBoxBytesV, &tmap_v, bx * (C::kRBV / C::kElemBytes), row, fb, policy);
+          tma_load_3d(st, &tmap_k, 0, row, 0, fb, policy);  // all kBoxes segments of the K rows
+          tma_load_3d(st + C::kOffV, &tmap_v, 0, row, 0, fb, policy);
         } else {
           if (p.error_flag) atomicOr(p.error_flag, kDevErrBadBlock);
           mbar_arrive(fb);
