@@ -292,6 +292,19 @@ __device__ __forceinline__ float ld_cluster_f32(uint32_t addr, uint32_t rank) {
   return v;
 }
 
+// Reads the 16-byte-aligned float4 at `addr` (this CTA's layout) in the shared memory
+// of cluster CTA `rank`.
+__device__ __forceinline__ float4 ld_cluster_f32x4(uint32_t addr, uint32_t rank) {
+  uint32_t remote;
+  float4 v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(addr), "r"(rank));
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(remote)
+               : "memory");
+  return v;
+}
+
 // Named CTA barrier over `count` threads that also ORs a predicate across them: every
 // participant gets the same answer.
 __device__ __forceinline__ bool group_barrier_any(int id, int count, bool pred) {

@@ -106,10 +106,9 @@ struct PartialCfg {
   static constexpr int kMt = DV / 16;       // 16-dim m-tiles of O^T
   static constexpr int kKs = D / 16;        // k16 steps of Q K^T
   static constexpr int kTiles = kCh / 16;   // 16-key tiles per stage
-  // Row stride (floats) of the per-page-group outputs in the combine area: padded so a
-  // warp's stores of one accumulator register spread over the banks (conflict-free for
-  // bf16 pages, two lanes per bank for affine pages).
-  static constexpr int kCoStride = DV + (BITS == 4 ? 1 : 4);
+  // Row stride (floats) of the per-page-group outputs in the combine area: padded by 4 so
+  // rows stay 16-byte aligned for vector access and a warp's stores spread over the banks.
+  static constexpr int kCoStride = DV + 4;
   // per-page-group states (m, l, o) for the in-CTA combine, then the CTA's own state for a cluster merge
   static constexpr int kCombineBytes = (kWP * kNqAll * (kCoStride + 2) + kNqAll * (DV + 2)) * 4;
   static constexpr int kRingBytes = kWarps * kStagesPerWarp * kStageBytes;
@@ -212,6 +211,15 @@ __device__ __forceinline__ void write_out(const PartialParams& p, size_t i, floa
   const __nv_bfloat16 b = __float2bfloat16_rn(v);
   p.out[i] = b;
   if (p.out_mirror) p.out_mirror[i] = b;
+}
+
+// Final output elements i .. i+3 (i a multiple of 4), one 8-byte store each.
+__device__ __forceinline__ void write_out4(const PartialParams& p, size_t i, float4 v) {
+  uint2 w;
+  w.x = pack_bf16x2(v.x, v.y);
+  w.y = pack_bf16x2(v.z, v.w);
+  *reinterpret_cast<uint2*>(p.out + i) = w;
+  if (p.out_mirror) *reinterpret_cast<uint2*>(p.out_mirror + i) = w;
 }
 
 // 4-bit k-steps with odd index read their codes at bit 4 of each half (16 c); their
@@ -906,98 +914,115 @@ __global__ void __maxnreg__(200)
           cl[pg * C::kNqAll + rbase + r] = l_run[nt][e2];
         }
     }
+    // o values, four (4-bit pages) or two (8-bit) consecutive head dims per store where
+    // the accumulator layout puts them in one thread; padding rows of the last n-tile
+    // are never read
+    constexpr int kRun = BITS == 4 ? 4 : BITS == 8 ? 2 : 1;
 #pragma unroll
-    for (int mt = 0; mt < C::kMt; ++mt)
+    for (int mt = 0; mt < C::kMt; mt += kRun)
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int r = 8 * nt + 2 * t + (e & 1);
-          if (rbase + r < p.nq)  // padding rows of the last n-tile are never read
-            co[(pg * C::kNqAll + rbase + r) * C::kCoStride + out_dim<BITS>(mt, e >> 1, g)] = o[mt][nt][e];
+          if (rbase + r >= p.nq) continue;
+          float* dst = co + (pg * C::kNqAll + rbase + r) * C::kCoStride + out_dim<BITS>(mt, e >> 1, g);
+          if constexpr (kRun == 4) {
+            *reinterpret_cast<float4*>(dst) = make_float4(o[mt][nt][e], o[mt + 1][nt][e], o[mt + 2][nt][e], o[mt + 3][nt][e]);
+          } else if constexpr (kRun == 2) {
+            *reinterpret_cast<float2*>(dst) = make_float2(o[mt][nt][e], o[mt + 1][nt][e]);
+          } else {
+            *dst = o[mt][nt][e];
+          }
         }
   }
   __syncthreads();
 
-  // Per query row: the combined maximum and normaliser of the page groups' states
-  // (this CTA's state, kept in st_m / st_l) and each group's weight 2^(m_w - M),
-  // written over its m; then every output only sums weighted o values.
-  if (threadIdx.x < p.nq) {
-    const int r = threadIdx.x;
+  // Each thread merges the page groups' states for four consecutive outputs of one query
+  // row: M = max of the groups' maxima, weights 2^(m_w - M), L and O their weighted sums.
+  constexpr int kQuads = DV / 4;  // four-dim runs per row
+  for (int i4 = threadIdx.x; i4 < p.nq * kQuads; i4 += C::kThreads) {
+    const int r = i4 / kQuads, d0 = 4 * (i4 % kQuads);
     float M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < C::kWP; ++w) M = fmaxf(M, cm[w * C::kNqAll + r]);
     float L = 0.f;
+    float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int w = 0; w < C::kWP; ++w) {
       const float mw = cm[w * C::kNqAll + r];
       const float wt = mw == -INFINITY ? 0.f : fast_exp2(mw - M);
       L = fmaf(wt, cl[w * C::kNqAll + r], L);
-      cm[w * C::kNqAll + r] = wt;
+      const float4 v = *reinterpret_cast<const float4*>(co + (w * C::kNqAll + r) * C::kCoStride + d0);
+      O.x = fmaf(wt, v.x, O.x);
+      O.y = fmaf(wt, v.y, O.y);
+      O.z = fmaf(wt, v.z, O.z);
+      O.w = fmaf(wt, v.w, O.w);
     }
-    st_m[r] = M;
-    st_l[r] = L;
-    if (!single && !in_cluster) {
-      const size_t ws = (row0 + r) * p.max_partitions + slot;
-      p.ws_ml[ws * 2] = M;
-      p.ws_ml[ws * 2 + 1] = L;
-    }
-  }
-  __syncthreads();
-
-  for (int idx = threadIdx.x; idx < p.nq * DV; idx += C::kThreads) {
-    const int r = idx / DV, d = idx % DV;
-    float O = 0.f;
-#pragma unroll
-    for (int w = 0; w < C::kWP; ++w) O = fmaf(cm[w * C::kNqAll + r], co[(w * C::kNqAll + r) * C::kCoStride + d], O);
     const size_t orow = row0 + r;
     if (single) {
-      const float L = st_l[r];
-      write_out(p, orow * DV + d, L > 0.f ? O / L : 0.f);
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+      write_out4(p, orow * DV + d0, make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv));
     } else if (in_cluster) {
-      st_o[r * DV + d] = O;
+      *reinterpret_cast<float4*>(st_o + r * DV + d0) = O;
+      if (d0 == 0) {
+        st_m[r] = M;
+        st_l[r] = L;
+      }
     } else {
-      p.ws_o[(orow * p.max_partitions + slot) * DV + d] = O;
+      const size_t ws = orow * p.max_partitions + slot;
+      *reinterpret_cast<float4*>(p.ws_o + ws * DV + d0) = O;
+      if (d0 == 0) {
+        p.ws_ml[ws * 2] = M;
+        p.ws_ml[ws * 2 + 1] = L;
+      }
     }
   }
 
   if (in_cluster) {
     // ---- merge the cluster's partition states (log-sum-exp) through distributed
     // shared memory; cluster CTA j holds the state of slot j. Each CTA finishes one
-    // slice of the (row, dim) outputs.
+    // slice of the four-dim output runs.
     cluster_sync();
     const int cs = p.max_partitions;
-    const int total = p.nq * DV;
-    const int per = (total + cs - 1) / cs;
-    const int end = min(total, (slot + 1) * per);
-    for (int idx = slot * per + threadIdx.x; idx < end; idx += C::kThreads) {
-      const int r = idx / DV, d = idx % DV;
-      // every member's (m, l, o) for this output, all remote loads in flight together
-      float mj[kMaxClusterParts], lj[kMaxClusterParts], oj[kMaxClusterParts];
+    const int runs = p.nq * kQuads;
+    const int per = (runs + cs - 1) / cs;
+    const int end = min(runs, (slot + 1) * per);
+    for (int i4 = slot * per + threadIdx.x; i4 < end; i4 += C::kThreads) {
+      const int r = i4 / kQuads, d0 = 4 * (i4 % kQuads);
+      // every member's (m, l, o) for these outputs, all remote loads in flight together
+      float mj[kMaxClusterParts], lj[kMaxClusterParts];
+      float4 oj[kMaxClusterParts];
 #pragma unroll
       for (int j = 0; j < kMaxClusterParts; ++j) {
         mj[j] = -INFINITY;
-        lj[j] = oj[j] = 0.f;
+        lj[j] = 0.f;
+        oj[j] = make_float4(0.f, 0.f, 0.f, 0.f);
         if (j < cs) {
           mj[j] = ld_cluster_f32(smem_addr(&st_m[r]), j);
           lj[j] = ld_cluster_f32(smem_addr(&st_l[r]), j);
-          oj[j] = ld_cluster_f32(smem_addr(&st_o[r * DV + d]), j);
+          oj[j] = ld_cluster_f32x4(smem_addr(&st_o[r * DV + d0]), j);
         }
       }
       float M = -INFINITY;
 #pragma unroll
       for (int j = 0; j < kMaxClusterParts; ++j) M = fmaxf(M, mj[j]);
-      float L = 0.f, O = 0.f;
+      float L = 0.f;
+      float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
       if (M != -INFINITY) {
 #pragma unroll
         for (int j = 0; j < kMaxClusterParts; ++j) {
           if (mj[j] == -INFINITY) continue;
           const float wt = fast_exp2(mj[j] - M);
           L = fmaf(wt, lj[j], L);
-          O = fmaf(wt, oj[j], O);
+          O.x = fmaf(wt, oj[j].x, O.x);
+          O.y = fmaf(wt, oj[j].y, O.y);
+          O.z = fmaf(wt, oj[j].z, O.z);
+          O.w = fmaf(wt, oj[j].w, O.w);
         }
       }
-      write_out(p, (row0 + r) * DV + d, L > 0.f ? O / L : 0.f);
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+      write_out4(p, (row0 + r) * DV + d0, make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv));
     }
     cluster_sync();  // no CTA leaves while another still reads its shared memory
   }
