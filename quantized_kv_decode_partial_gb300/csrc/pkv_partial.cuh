@@ -93,7 +93,12 @@ struct PartialCfg {
   static constexpr int kStageBytes = (kTxBytes + 1023) / 1024 * 1024;
   static constexpr int kBarrierBytes = SOLO ? 512 : 256;
   static constexpr int kSoloBudget = 227 * 1024 - kBarrierBytes - 1024;  // stage ring of a CTA alone on its SM
-  static constexpr int kWarps = (SOLO && 8 * 2 * kStageBytes <= kSoloBudget) ? 8 : 4;  // every warp computes
+  // every warp computes: 8 when two stages per warp fit a CTA alone on its SM, else 6 (two
+  // of the four schedulers then hold two warps), else 4
+  static constexpr int kWarps = !SOLO                                ? 4
+                                : 8 * 2 * kStageBytes <= kSoloBudget ? 8
+                                : 6 * 2 * kStageBytes <= kSoloBudget ? 6
+                                                                     : 4;
   static constexpr int kThreads = kWarps * 32;
   // The warps form kWP page groups of WQ warps. A page group takes every kWP-th chunk;
   // its WQ warps read each of its chunks, each for its own 8*NT query rows.
