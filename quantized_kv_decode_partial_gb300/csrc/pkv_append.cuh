@@ -62,12 +62,23 @@ __device__ __forceinline__ void append_plane(const __nv_bfloat16* src_row, __nv_
     const __nv_bfloat16 s16 = __float2bfloat16_rn(__fdiv_rn(hi - lo, kLevels));
     const __nv_bfloat16 b16 = __float2bfloat16_rn(lo);
     const float s = __bfloat162float(s16), bias = __bfloat162float(b16);
+    // (x - bias) / s correctly rounded decides each code. The product with the correctly
+    // rounded reciprocal is within 1.5 * 2^-23 relative of that quotient. Outside
+    // [-0.5, 2^bits - 0.5] both clamp to the same code; inside, the two differ by less
+    // than 2^-14, so the product rounds to the same integer unless it lies within 2^-13
+    // of a half-integer. Those few take the division itself.
+    const float rs = s != 0.f ? __frcp_rn(s) : 0.f;
     uint32_t packed[E * BITS / 32 > 0 ? E * BITS / 32 : 1] = {};
     uint32_t half_word = 0;  // 4-bit codes of a lane with E = 4 fill 16 bits
 #pragma unroll
     for (int e = 0; e < E; ++e) {
       uint32_t code = 0;
-      if (s != 0.f) code = static_cast<uint32_t>(fminf(fmaxf(rintf(__fdiv_rn(x[e] - bias, s)), 0.f), kLevels));
+      if (s != 0.f) {
+        const float d = x[e] - bias;
+        float qt = d * rs;
+        if (fabsf(qt - floorf(qt) - 0.5f) < 1.f / 8192.f) qt = __fdiv_rn(d, s);
+        code = static_cast<uint32_t>(fminf(fmaxf(rintf(qt), 0.f), kLevels));
+      }
       if constexpr (E * BITS >= 32) {
         packed[(e * BITS) / 32] |= code << ((e * BITS) % 32);
       } else {

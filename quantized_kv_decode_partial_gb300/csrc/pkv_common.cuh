@@ -200,6 +200,11 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
 }
 
 // Fetches a TMA descriptor (a __grid_constant__ kernel parameter) ahead of its first use.
+// Starts fetching the 128-byte line holding `ptr` into L1 (and L2).
+__device__ __forceinline__ void prefetch_l1(const void* ptr) {
+  asm volatile("prefetch.global.L1 [%0];" ::"l"(ptr));
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

@@ -303,6 +303,18 @@ __global__ void __maxnreg__(200)
     const long long blk = r / p.block_size < p.max_blocks ? r / p.block_size : p.max_blocks - 1;
     tbl_pre = static_cast<int>(ld_nc_keep_u32(p.block_tables + static_cast<size_t>(b) * p.max_blocks + blk));
   }
+  // Fused append: the step's new K/V rows of this (sequence, KV head) are read by the
+  // warp whose chunk holds them just before it issues that chunk; fetch them now.
+  if (p.k_new != nullptr) {
+    const size_t nrow = (static_cast<size_t>(b) * p.num_kv_heads + hk) * N;
+    const int k_lines = (N * D * 2 + 127) / 128, v_lines = (N * DV * 2 + 127) / 128;
+    const int i = threadIdx.x;
+    if (i < k_lines) {
+      prefetch_l1(reinterpret_cast<const char*>(p.k_new + nrow * D) + 128 * i);
+    } else if (i < k_lines + v_lines) {
+      prefetch_l1(reinterpret_cast<const char*>(p.v_new + nrow * DV) + 128 * (i - k_lines));
+    }
+  }
   // The stage barriers do not depend on len either: set them up while it is in flight.
   if (threadIdx.x == 0) {
     prefetch_tensormap(&tmap_k);  // the first copies need both descriptors

@@ -119,17 +119,19 @@ def test_grids_of_several_ctas_per_sm_match_oracle(bits, D, DV):
         assert_close(out.double().cpu().numpy(), ref, f"{sp.name} partition={pt}")
 
 
-@pytest.mark.parametrize("bits,parts", [(16, 16), (4, 16), (8, 2), (16, 9)])
-def test_cluster_merge_matches_oracle(bits, parts):
-    # one sequence: the partitions of each KV head merge inside a thread-block cluster
-    sp = spec(f"cluster_{bits}_{parts}", num_seqs=1, head_dim=128 if bits != 4 else 256, bits=bits, block_size=32,
+@pytest.mark.parametrize("bits,parts,head_dim", [(16, 16, 128), (4, 16, 256), (8, 2, 128), (16, 9, 128),
+                                                  (16, 12, 256), (16, 5, 64)])
+def test_cluster_merge_matches_oracle(bits, parts, head_dim):
+    # one sequence: the partitions of each KV head merge inside a thread-block cluster (CTAs alone on
+    # their SMs: 8 warps, or 6 for bf16 D=256)
+    sp = spec(f"cluster_{bits}_{parts}_{head_dim}", num_seqs=1, head_dim=head_dim, bits=bits, block_size=32,
               lengths=(parts * 64 - 5,), length_range=None)
     case = make_case(sp)
     plan = B.make_plan(B.layout_for(case.k_pool, sp.head_dim, bits),
                        B.DecodeParams(1, sp.num_q_heads, 1, case.block_tables.shape[1], 64))
     assert plan.merge_in_cluster == 1 and plan.max_partitions == parts
     out = run_gpu(case.to(DEV), partition_tokens=64)
-    assert_close(out.double().cpu().numpy(), oracle_out(case), f"cluster {bits} {parts}")
+    assert_close(out.double().cpu().numpy(), oracle_out(case), f"cluster {bits} {parts} {head_dim}")
 
 
 WINDOWED = [
