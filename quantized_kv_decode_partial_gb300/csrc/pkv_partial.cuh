@@ -285,6 +285,14 @@ __global__ void __maxnreg__(200)
   const size_t row0 = (static_cast<size_t>(b) * p.num_q_heads + static_cast<size_t>(hk) * rep) * N;
   const bool single = p.mode == kModeSingle;
   const bool in_cluster = p.mode == kModeCluster;
+  // When launched as a programmatic dependent (grids of one CTA per SM), everything the
+  // previous kernel on the stream writes (inputs, pools, the output) is read or written
+  // only after it has completed; otherwise the wait returns at once.
+  if (threadIdx.x == 0) {
+    prefetch_tensormap(&tmap_k);  // kernel parameters: no dependence
+    prefetch_tensormap(&tmap_v);
+  }
+  wait_for_prerequisite_grids();
   const int len = p.seq_lens[b];
   // This lane's query values, fetched now so their latency overlaps the length's:
   // 2 * kKs words of bf16 pairs per n-tile, in the order q_load_words reads them.
@@ -317,8 +325,6 @@ __global__ void __maxnreg__(200)
   }
   // The stage barriers do not depend on len either: set them up while it is in flight.
   if (threadIdx.x == 0) {
-    prefetch_tensormap(&tmap_k);  // the first copies need both descriptors
-    prefetch_tensormap(&tmap_v);
     for (int s = 0; s < C::kWarps * C::kStagesPerWarp; ++s) mbar_init(smem_addr(&full_bar[s]), 1);
     *abort_flag = 0;
     fence_barrier_init();

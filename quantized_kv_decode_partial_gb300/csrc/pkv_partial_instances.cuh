@@ -46,14 +46,25 @@ cudaError_t launch_of(const PartialParams& p, const CUtensorMap& tk, const CUten
   cfg.blockDim = dim3(C::kThreads);
   cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
+  cfg.attrs = attr;
+  cfg.numAttrs = 0;
+  if constexpr (SOLO) {
+    // Programmatic dependent launch for grids of at most one CTA per SM: the CTAs may be
+    // placed on idle SMs while the previous kernel on the stream finishes, and wait for
+    // it (griddepcontrol.wait) before they touch global memory. The launch latency then
+    // hides behind that kernel's tail. (Grids of two CTAs per SM lost 2% this way: early
+    // CTAs take the slots the previous grid frees unevenly.)
+    attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
+    ++cfg.numAttrs;
+  }
   if (p.mode == kModeCluster) {  // the partitions of one (sequence, KV head) form a cluster
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = grid.x;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    attr[cfg.numAttrs].id = cudaLaunchAttributeClusterDimension;
+    attr[cfg.numAttrs].val.clusterDim.x = grid.x;
+    attr[cfg.numAttrs].val.clusterDim.y = 1;
+    attr[cfg.numAttrs].val.clusterDim.z = 1;
+    ++cfg.numAttrs;
   }
   return cudaLaunchKernelEx(&cfg, kern, p, tk, tv);
 }
