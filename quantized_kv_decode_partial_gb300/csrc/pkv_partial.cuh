@@ -115,8 +115,14 @@ struct PartialCfg {
   // rows stay 16-byte aligned for vector access and a warp's stores spread over the banks.
   static constexpr int kCoStride = DV + 4;
   // per-page-group states (m, l, o) for the in-CTA combine, then the CTA's own state for a cluster merge
-  static constexpr int kCombineBytes = (kWP * kNqAll * (kCoStride + 2) + kNqAll * (DV + 2)) * 4;
+  static constexpr int kGroupStateFloats = kNqAll * (kCoStride + 2);
+  static constexpr int kCtaStateFloats = kNqAll * (DV + 2);
+  static constexpr int kCombineBytes = (kWP * kGroupStateFloats + kCtaStateFloats) * 4;
   static constexpr int kRingBytes = kWarps * kStagesPerWarp * kStageBytes;
+  static constexpr int kGroupBytes = kStagesPerGroup * kStageBytes;  // one page group's ring
+  // When a page group's state (and the CTA's, after the last group's) fits its own ring,
+  // each group writes it there as soon as its chunks are done, with no CTA barrier first.
+  static constexpr bool kOwnRegions = (kGroupStateFloats + kCtaStateFloats) * 4 <= kGroupBytes;
   static constexpr int kDataBytes = kRingBytes > kCombineBytes ? kRingBytes : kCombineBytes;
   static constexpr int kSmemBytes = kDataBytes + kBarrierBytes + 1024;  // + alignment slack
   static constexpr float kCodeUnit = 5.9604644775390625e-8f;  // 2^-24: value of fp16 bit pattern 1
@@ -917,24 +923,33 @@ __global__ void __maxnreg__(200)
   }
 
   allow_dependent_launch();  // the merge pass may be scheduled while this epilogue runs
-  __syncthreads();  // every stage consumed, every copy landed: the stage ring is free
-
-  // ---- combine the consumer warps' states and write out
-  float* cm = reinterpret_cast<float*>(smem);
-  float* cl = cm + C::kWP * C::kNqAll;
-  float* co = cl + C::kWP * C::kNqAll;
-  float* st_m = co + C::kWP * C::kNqAll * C::kCoStride;  // this CTA's merged state (cluster merge)
-  float* st_l = st_m + C::kNqAll;
-  float* st_o = st_l + C::kNqAll;
-  if (warp < C::kWarps) {
+  // ---- combine the page groups' states and write out. Group w's state is m[kNqAll],
+  // l[kNqAll], o[kNqAll][kCoStride] at gstate(w): in its own ring region when it fits
+  // there (free once the group's chunks are consumed and its copies have landed), else
+  // packed from the start of shared memory once every group is done.
+  if constexpr (C::kOwnRegions) {
+    if constexpr (WQ > 1) group_barrier_any(1 + pg, WQ * 32, false);  // the group's warps have left its ring
+  } else {
+    __syncthreads();  // every stage consumed, every copy landed: the stage ring is free
+  }
+  float* const sf = reinterpret_cast<float*>(smem);
+  constexpr int kGS = C::kOwnRegions ? C::kGroupBytes / 4 : C::kGroupStateFloats;  // floats between group states
+  auto gstate = [&](int w) { return sf + w * kGS; };
+  float* const st_m = gstate(C::kWP - 1) + C::kGroupStateFloats;  // this CTA's merged state (cluster merge)
+  float* const st_l = st_m + C::kNqAll;
+  float* const st_o = st_l + C::kNqAll;
+  {
+    float* const cm = gstate(pg);
+    float* const cl = cm + C::kNqAll;
+    float* const co = cl + C::kNqAll;
     if (g == 0) {
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int e2 = 0; e2 < 2; ++e2) {
           const int r = 8 * nt + 2 * t + e2;
-          cm[pg * C::kNqAll + rbase + r] = m_run[nt][e2];
-          cl[pg * C::kNqAll + rbase + r] = l_run[nt][e2];
+          cm[rbase + r] = m_run[nt][e2];
+          cl[rbase + r] = l_run[nt][e2];
         }
     }
     // o values, four (4-bit pages) or two (8-bit) consecutive head dims per store where
@@ -949,7 +964,7 @@ __global__ void __maxnreg__(200)
         for (int e = 0; e < 4; ++e) {
           const int r = 8 * nt + 2 * t + (e & 1);
           if (rbase + r >= p.nq) continue;
-          float* dst = co + (pg * C::kNqAll + rbase + r) * C::kCoStride + out_dim<BITS>(mt, e >> 1, g);
+          float* dst = co + (rbase + r) * C::kCoStride + out_dim<BITS>(mt, e >> 1, g);
           if constexpr (kRun == 4) {
             *reinterpret_cast<float4*>(dst) = make_float4(o[mt][nt][e], o[mt + 1][nt][e], o[mt + 2][nt][e], o[mt + 3][nt][e]);
           } else if constexpr (kRun == 2) {
@@ -968,15 +983,16 @@ __global__ void __maxnreg__(200)
     const int r = i4 / kQuads, d0 = 4 * (i4 % kQuads);
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < C::kWP; ++w) M = fmaxf(M, cm[w * C::kNqAll + r]);
+    for (int w = 0; w < C::kWP; ++w) M = fmaxf(M, gstate(w)[r]);
     float L = 0.f;
     float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int w = 0; w < C::kWP; ++w) {
-      const float mw = cm[w * C::kNqAll + r];
+      const float* gw = gstate(w);
+      const float mw = gw[r];
       const float wt = mw == -INFINITY ? 0.f : fast_exp2(mw - M);
-      L = fmaf(wt, cl[w * C::kNqAll + r], L);
-      const float4 v = *reinterpret_cast<const float4*>(co + (w * C::kNqAll + r) * C::kCoStride + d0);
+      L = fmaf(wt, gw[C::kNqAll + r], L);
+      const float4 v = *reinterpret_cast<const float4*>(gw + 2 * C::kNqAll + r * C::kCoStride + d0);
       O.x = fmaf(wt, v.x, O.x);
       O.y = fmaf(wt, v.y, O.y);
       O.z = fmaf(wt, v.z, O.z);
