@@ -3,6 +3,7 @@ for bit (codes, scales, biases and bf16 rows), then a decode over the appended
 cache against the attention oracle."""
 
 import zlib
+from dataclasses import replace
 
 import numpy as np
 import pytest
@@ -205,3 +206,52 @@ def test_fused_append_rejects_a_missing_new_row():
         B.paged_decode_append_attention(d.q, None, v_new.to(DEV), d.k_pool, d.v_pool, d.block_tables, d.seq_lens,
                                         case.scale)
     assert e.value.code == B.PKV_ERR_NULL_POINTER
+
+
+def _as_tensor(arr, like):
+    """A numpy plane from the write oracle as a CPU tensor of `like`'s dtype."""
+    if like.dtype == torch.bfloat16:
+        return torch.from_numpy(np.ascontiguousarray(arr).view(np.int16)).view(torch.bfloat16)
+    return torch.from_numpy(np.ascontiguousarray(arr).view(np.int32))
+
+
+@pytest.mark.parametrize("bits,D", [(4, 256), (16, 256), (16, 128)])
+def test_back_to_back_fused_steps_read_each_others_rows(bits, D):
+    # A decode loop: S fused steps on one stream with no synchronisation between them. Step s
+    # appends row L0 + s and attends over L0 + s + 1 rows, the rows earlier steps wrote included.
+    # One sequence on a small grid: the partial kernels launch as programmatic dependents of the
+    # step before, so this checks that nothing is read before that step has finished.
+    S, L0, hq, hk = 4, 700, 8, 2
+    name = f"loop_{bits}_{D}"
+    seed = zlib.crc32(name.encode()) % 10000
+    bs = 16 if bits == 16 else 32
+    sp = DecodeSpec(name=name, num_seqs=1, num_q_heads=hq, num_kv_heads=hk, head_dim=D, n_query=1, block_size=bs,
+                    bits=bits, length_range=None, lengths=(L0 + S,), pool_factor=2.0, seed=seed)
+    case = make_case(sp, lengths=[L0 + S], poison=False)
+    g = torch.Generator().manual_seed(seed + 1)
+    qs = [torch.randn((1, hq, 1, D), generator=g).to(torch.bfloat16) for _ in range(S)]
+    kn = [(torch.randn((1, hk, 1, D), generator=g) * 2).to(torch.bfloat16) for _ in range(S)]
+    vn = [torch.randn((1, hk, 1, D), generator=g).to(torch.bfloat16) for _ in range(S)]
+    d = case.to(DEV)
+    lens = [torch.tensor([L0 + s + 1], dtype=torch.int32, device=DEV) for s in range(S)]
+    plan = B.make_plan(B.layout_for(d.k_pool, D, bits), B.DecodeParams(1, hq, 1, d.block_tables.shape[1], 128))
+    assert plan.merge_in_cluster == 1 and plan.max_partitions >= 2  # one CTA per SM, cluster merge
+    outs = []
+    for s in range(S):
+        outs.append(B.paged_decode_append_attention(
+            qs[s].to(DEV), kn[s].to(DEV), vn[s].to(DEV), d.k_pool, d.v_pool, d.block_tables, lens[s], case.scale,
+            bits=bits, k_scales=d.k_scales, k_biases=d.k_biases, v_scales=d.v_scales, v_biases=d.v_biases,
+            partition_tokens=128))
+    torch.cuda.synchronize()
+    planes = ("k_pool", "v_pool") + (() if bits == 16 else ("k_scales", "k_biases", "v_scales", "v_biases"))
+    state = {name: bits_of(getattr(case, name)) for name in planes}
+    for s in range(S):
+        state = pw.append_rows(kn[s].float().numpy(), vn[s].float().numpy(), case.block_tables.numpy(), [L0 + s],
+                               state["k_pool"], state["v_pool"], bits=bits, k_scales=state.get("k_scales"),
+                               k_biases=state.get("k_biases"), v_scales=state.get("v_scales"),
+                               v_biases=state.get("v_biases"))
+        host = replace(case, q=qs[s], seq_lens=torch.tensor([L0 + s + 1], dtype=torch.int32), lens_host=[L0 + s + 1],
+                       **{name: _as_tensor(state[name], getattr(case, name)) for name in planes})
+        assert_close(outs[s].double().cpu().numpy(), oracle_out(host), f"loop step {s} {bits} {D}")
+    for name in planes:  # after the loop the pools hold every step's row, bit for bit
+        assert np.array_equal(bits_of(getattr(d, name)), state[name]), name
