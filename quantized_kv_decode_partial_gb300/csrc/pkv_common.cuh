@@ -287,6 +287,31 @@ __device__ __forceinline__ void cluster_sync() {
       "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// First half of a cluster barrier without memory ordering, and the second half with
+// acquire: together they tell that every member has started. Every thread of every
+// member takes part, arrive before wait.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Stores at shared-memory address `addr` (this CTA's layout) in the shared memory of
+// cluster CTA `rank`: one f32, or a 16-byte-aligned float4.
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, uint32_t rank, float v) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(addr), "r"(rank));
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
+}
+__device__ __forceinline__ void st_cluster_f32x4(uint32_t addr, uint32_t rank, float4 v) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(addr), "r"(rank));
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(remote), "f"(v.x), "f"(v.y), "f"(v.z),
+               "f"(v.w)
+               : "memory");
+}
+
 // Reads an f32 at shared-memory address `addr` (this CTA's layout) in the shared
 // memory of cluster CTA `rank`.
 __device__ __forceinline__ float ld_cluster_f32(uint32_t addr, uint32_t rank) {

@@ -92,7 +92,14 @@ struct PartialCfg {
   static constexpr int kSbCopies = (2 * kSbBytes + 2 * kSbBytesV) / 16;  // 16-byte copies of scales and biases
   static constexpr int kStageBytes = (kTxBytes + 1023) / 1024 * 1024;
   static constexpr int kBarrierBytes = SOLO ? 512 : 256;
-  static constexpr int kSoloBudget = 227 * 1024 - kBarrierBytes - 1024;  // stage ring of a CTA alone on its SM
+  static constexpr int kNqp = 8 * NT;       // query rows per warp (padded)
+  static constexpr int kNqAll = WQ * kNqp;  // query rows per CTA (padded)
+  // Cluster merge of a CTA alone on its SM: a receive area of its own, which the other
+  // members write into (their (m, l) of every row, and their o runs of this CTA's share
+  // of the outputs) while this CTA may still be streaming.
+  static constexpr int kRecvFloats = SOLO ? 2 * kMaxClusterParts * kNqAll + kNqAll * DV + 4 * kMaxClusterParts : 0;
+  static constexpr int kRecvBytes = kRecvFloats * 4;
+  static constexpr int kSoloBudget = 227 * 1024 - kBarrierBytes - 1024 - kRecvBytes;  // stage ring of a CTA alone on its SM
   // every warp computes: 8 when two stages per warp fit a CTA alone on its SM, else 6 (two
   // of the four schedulers then hold two warps), else 4
   static constexpr int kWarps = !SOLO                                ? 4
@@ -106,8 +113,6 @@ struct PartialCfg {
   static constexpr int kSoloStages = kSoloBudget / (kWarps * kStageBytes);
   static constexpr int kStagesPerWarp = SOLO ? (kSoloStages < 4 ? kSoloStages : 4) : (kStageBytes <= 9 * 1024 ? 3 : 2);
   static constexpr int kStagesPerGroup = kStagesPerWarp * WQ;  // each page group's private ring
-  static constexpr int kNqp = 8 * NT;       // query rows per warp (padded)
-  static constexpr int kNqAll = WQ * kNqp;  // query rows per CTA (padded)
   static constexpr int kMt = DV / 16;       // 16-dim m-tiles of O^T
   static constexpr int kKs = D / 16;        // k16 steps of Q K^T
   static constexpr int kTiles = kCh / 16;   // 16-key tiles per stage
@@ -123,7 +128,8 @@ struct PartialCfg {
   // When a page group's state (and the CTA's, after the last group's) fits its own ring,
   // each group writes it there as soon as its chunks are done, with no CTA barrier first.
   static constexpr bool kOwnRegions = (kGroupStateFloats + kCtaStateFloats) * 4 <= kGroupBytes;
-  static constexpr int kDataBytes = kRingBytes > kCombineBytes ? kRingBytes : kCombineBytes;
+  static constexpr int kWorkBytes = kRingBytes > kCombineBytes ? kRingBytes : kCombineBytes;
+  static constexpr int kDataBytes = kWorkBytes + kRecvBytes;  // the receive area follows the ring
   static constexpr int kSmemBytes = kDataBytes + kBarrierBytes + 1024;  // + alignment slack
   static constexpr float kCodeUnit = 5.9604644775390625e-8f;  // 2^-24: value of fp16 bit pattern 1
 
@@ -336,6 +342,11 @@ __global__ void __maxnreg__(200)
     fence_barrier_init();
   }
   __syncthreads();
+  // A CTA alone on its SM pushes its cluster-merge share into the other members' shared
+  // memory; that needs every member running, which this first cluster phase tells.
+  if constexpr (SOLO) {
+    if (in_cluster) cluster_arrive_relaxed();
+  }
 
   if (len < N || len > p.max_blocks * p.block_size) {
     // Every CTA of this sequence sees the same length and leaves here (before any
@@ -979,7 +990,16 @@ __global__ void __maxnreg__(200)
   // Each thread merges the page groups' states for four consecutive outputs of one query
   // row: M = max of the groups' maxima, weights 2^(m_w - M), L and O their weighted sums.
   constexpr int kQuads = DV / 4;  // four-dim runs per row
-  for (int i4 = threadIdx.x; i4 < p.nq * kQuads; i4 += C::kThreads) {
+  const int cs = p.max_partitions;        // cluster size in cluster mode
+  const int runs = p.nq * kQuads;
+  const int per = (runs + cs - 1) / cs;  // runs each cluster CTA finishes
+  float* const rm = reinterpret_cast<float*>(smem + C::kWorkBytes);  // receive area: [member][kNqAll]
+  float* const rl = rm + kMaxClusterParts * C::kNqAll;
+  float* const ro = rl + kMaxClusterParts * C::kNqAll;  // [member][per runs][4]
+  if constexpr (SOLO) {
+    if (in_cluster) cluster_wait();  // every member is running: its receive area may be written
+  }
+  for (int i4 = threadIdx.x; i4 < runs; i4 += C::kThreads) {
     const int r = i4 / kQuads, d0 = 4 * (i4 % kQuads);
     float M = -INFINITY;
 #pragma unroll
@@ -1003,10 +1023,19 @@ __global__ void __maxnreg__(200)
       const float inv = L > 0.f ? 1.f / L : 0.f;
       write_out4(p, orow * DV + d0, make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv));
     } else if (in_cluster) {
-      *reinterpret_cast<float4*>(st_o + r * DV + d0) = O;
-      if (d0 == 0) {
-        st_m[r] = M;
-        st_l[r] = L;
+      if constexpr (SOLO) {
+        const int owner = i4 / per;
+        st_cluster_f32x4(smem_addr(ro + 4 * (slot * per + (i4 - owner * per))), owner, O);
+        if (d0 / 4 < cs) {  // the row's (m, l) to member d0 / 4
+          st_cluster_f32(smem_addr(&rm[slot * C::kNqAll + r]), d0 / 4, M);
+          st_cluster_f32(smem_addr(&rl[slot * C::kNqAll + r]), d0 / 4, L);
+        }
+      } else {
+        *reinterpret_cast<float4*>(st_o + r * DV + d0) = O;
+        if (d0 == 0) {
+          st_m[r] = M;
+          st_l[r] = L;
+        }
       }
     } else {
       const size_t ws = orow * p.max_partitions + slot;
@@ -1018,14 +1047,40 @@ __global__ void __maxnreg__(200)
     }
   }
 
-  if (in_cluster) {
-    // ---- merge the cluster's partition states (log-sum-exp) through distributed
-    // shared memory; cluster CTA j holds the state of slot j. Each CTA finishes one
-    // slice of the four-dim output runs.
+  if (in_cluster && SOLO) {
+    // ---- cluster merge, push form: after one cluster barrier every member's (m, l) and
+    // o runs for this CTA's share sit in its receive area; nothing reads this CTA's
+    // shared memory afterwards, so it may leave when done.
     cluster_sync();
-    const int cs = p.max_partitions;
-    const int runs = p.nq * kQuads;
-    const int per = (runs + cs - 1) / cs;
+    const int end = min(runs, (slot + 1) * per);
+    for (int i4 = slot * per + threadIdx.x; i4 < end; i4 += C::kThreads) {
+      const int r = i4 / kQuads, d0 = 4 * (i4 % kQuads), e = i4 - slot * per;
+      float M = -INFINITY;
+      for (int j = 0; j < cs; ++j) M = fmaxf(M, rm[j * C::kNqAll + r]);
+      float L = 0.f;
+      float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (M != -INFINITY) {
+        for (int j = 0; j < cs; ++j) {
+          const float mj = rm[j * C::kNqAll + r];
+          if (mj == -INFINITY) continue;
+          const float wt = fast_exp2(mj - M);
+          const float4 v = *reinterpret_cast<const float4*>(ro + 4 * (j * per + e));
+          L = fmaf(wt, rl[j * C::kNqAll + r], L);
+          O.x = fmaf(wt, v.x, O.x);
+          O.y = fmaf(wt, v.y, O.y);
+          O.z = fmaf(wt, v.z, O.z);
+          O.w = fmaf(wt, v.w, O.w);
+        }
+      }
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+      write_out4(p, (row0 + r) * DV + d0, make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv));
+    }
+  } else if (in_cluster) {
+    // ---- merge the cluster's partition states (log-sum-exp) through distributed
+    // shared memory, pull form (CTAs sharing an SM have no room for a receive area);
+    // cluster CTA j holds the state of slot j. Each CTA finishes one slice of the
+    // four-dim output runs.
+    cluster_sync();
     const int end = min(runs, (slot + 1) * per);
     for (int i4 = slot * per + threadIdx.x; i4 < end; i4 += C::kThreads) {
       const int r = i4 / kQuads, d0 = 4 * (i4 % kQuads);
