@@ -94,12 +94,12 @@ struct PartialCfg {
   static constexpr int kBarrierBytes = SOLO ? 512 : 256;
   static constexpr int kNqp = 8 * NT;       // query rows per warp (padded)
   static constexpr int kNqAll = WQ * kNqp;  // query rows per CTA (padded)
-  // Cluster merge of a CTA alone on its SM: a receive area of its own, which the other
-  // members write into (their (m, l) of every row, and their o runs of this CTA's share
-  // of the outputs) while this CTA may still be streaming.
-  static constexpr int kRecvFloats = SOLO ? 2 * kMaxClusterParts * kNqAll + kNqAll * DV + 4 * kMaxClusterParts : 0;
-  static constexpr int kRecvBytes = kRecvFloats * 4;
-  static constexpr int kSoloBudget = 227 * 1024 - kBarrierBytes - 1024 - kRecvBytes;  // stage ring of a CTA alone on its SM
+  // Push-form cluster merge: a receive area of the CTA's own, which the other members
+  // write into (their (m, l) of every row, and their o runs of this CTA's share of the
+  // outputs) while this CTA may still be streaming.
+  static constexpr int kRecvNeedBytes = (2 * kMaxClusterParts * kNqAll + kNqAll * DV + 4 * kMaxClusterParts) * 4;
+  // stage ring of a CTA alone on its SM, which always has a receive area
+  static constexpr int kSoloBudget = 227 * 1024 - kBarrierBytes - 1024 - (SOLO ? kRecvNeedBytes : 0);
   // every warp computes: 8 when two stages per warp fit a CTA alone on its SM, else 6 (two
   // of the four schedulers then hold two warps), else 4
   static constexpr int kWarps = !SOLO                                ? 4
@@ -129,7 +129,13 @@ struct PartialCfg {
   // each group writes it there as soon as its chunks are done, with no CTA barrier first.
   static constexpr bool kOwnRegions = (kGroupStateFloats + kCtaStateFloats) * 4 <= kGroupBytes;
   static constexpr int kWorkBytes = kRingBytes > kCombineBytes ? kRingBytes : kCombineBytes;
-  static constexpr int kDataBytes = kWorkBytes + kRecvBytes;  // the receive area follows the ring
+  // The receive area (after the ring) is there when the CTA is alone on its SM, or when it
+  // does not cost the second CTA per SM (or the CTA already has its SM to itself).
+  static constexpr int kBaseSmem = kWorkBytes + kBarrierBytes + 1024;
+  static constexpr bool kPush = SOLO || kBaseSmem + kRecvNeedBytes <= 114 * 1024 ||
+                                (kBaseSmem > 114 * 1024 && kBaseSmem + kRecvNeedBytes <= 227 * 1024);
+  static constexpr int kRecvBytes = kPush ? kRecvNeedBytes : 0;
+  static constexpr int kDataBytes = kWorkBytes + kRecvBytes;
   static constexpr int kSmemBytes = kDataBytes + kBarrierBytes + 1024;  // + alignment slack
   static constexpr float kCodeUnit = 5.9604644775390625e-8f;  // 2^-24: value of fp16 bit pattern 1
 
@@ -342,9 +348,9 @@ __global__ void __maxnreg__(200)
     fence_barrier_init();
   }
   __syncthreads();
-  // A CTA alone on its SM pushes its cluster-merge share into the other members' shared
+  // In the push form a CTA stores its cluster-merge share into the other members' shared
   // memory; that needs every member running, which this first cluster phase tells.
-  if constexpr (SOLO) {
+  if constexpr (C::kPush) {
     if (in_cluster) cluster_arrive_relaxed();
   }
 
@@ -996,7 +1002,7 @@ __global__ void __maxnreg__(200)
   float* const rm = reinterpret_cast<float*>(smem + C::kWorkBytes);  // receive area: [member][kNqAll]
   float* const rl = rm + kMaxClusterParts * C::kNqAll;
   float* const ro = rl + kMaxClusterParts * C::kNqAll;  // [member][per runs][4]
-  if constexpr (SOLO) {
+  if constexpr (C::kPush) {
     if (in_cluster) cluster_wait();  // every member is running: its receive area may be written
   }
   for (int i4 = threadIdx.x; i4 < runs; i4 += C::kThreads) {
@@ -1023,7 +1029,7 @@ __global__ void __maxnreg__(200)
       const float inv = L > 0.f ? 1.f / L : 0.f;
       write_out4(p, orow * DV + d0, make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv));
     } else if (in_cluster) {
-      if constexpr (SOLO) {
+      if constexpr (C::kPush) {
         const int owner = i4 / per;
         st_cluster_f32x4(smem_addr(ro + 4 * (slot * per + (i4 - owner * per))), owner, O);
         if (d0 / 4 < cs) {  // the row's (m, l) to member d0 / 4
@@ -1047,7 +1053,7 @@ __global__ void __maxnreg__(200)
     }
   }
 
-  if (in_cluster && SOLO) {
+  if (in_cluster && C::kPush) {
     // ---- cluster merge, push form: after one cluster barrier every member's (m, l) and
     // o runs for this CTA's share sit in its receive area; nothing reads this CTA's
     // shared memory afterwards, so it may leave when done.
@@ -1077,7 +1083,7 @@ __global__ void __maxnreg__(200)
     }
   } else if (in_cluster) {
     // ---- merge the cluster's partition states (log-sum-exp) through distributed
-    // shared memory, pull form (CTAs sharing an SM have no room for a receive area);
+    // shared memory, pull form (where a receive area would cost the second CTA per SM);
     // cluster CTA j holds the state of slot j. Each CTA finishes one slice of the
     // four-dim output runs.
     cluster_sync();
