@@ -282,7 +282,7 @@ __device__ __forceinline__ void load_group_row(uint32_t addr, float (&v)[G]) {
 }
 
 template <int BITS, int D, int DV, int NT, int WQ, bool SOLO>
-__global__ void __maxnreg__(200)
+__global__ void __maxnreg__(SOLO ? 255 : 200)
     pkv_partial_kernel(const __grid_constant__ PartialParams p, const __grid_constant__ CUtensorMap tmap_k,
                        const __grid_constant__ CUtensorMap tmap_v) {
   using C = PartialCfg<BITS, D, DV, NT, WQ, SOLO>;
