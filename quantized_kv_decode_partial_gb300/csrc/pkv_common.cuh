@@ -1,6 +1,6 @@
 // Device helpers shared by the paged decode kernels: inline PTX for mbarriers,
-// TMA / bulk copies, ldmatrix, warp-level MMA and movmatrix, plus the kernel
-// parameter blocks. sm_103a only.
+// TMA and cp.async copies, ldmatrix, warp-level MMA and movmatrix, cluster barriers
+// and distributed shared memory, plus the kernel parameter blocks. sm_103a only.
 #pragma once
 
 #include <cuda.h>

@@ -10,7 +10,7 @@
 // softmax itself and writes bf16 output.
 //
 // Design (GB300):
-//  * Four warps per CTA (eight for grids of at most one CTA per SM); with W warps,
+//  * Four warps per CTA (six or eight for grids of at most one CTA per SM); with W warps,
 //    warp w takes chunks w, w+W, w+2W, ... of the partition (16 rows for bf16
 //    pages, 32 or 16 for affine pages) and runs its own pipeline: lane 0 issues
 //    the copies of its chunk `kStagesPerWarp` ahead into a private ring of
@@ -56,8 +56,9 @@ namespace pkv {
 
 // SOLO: the variant for grids of at most one CTA per SM. Such a CTA has the SM to
 // itself, so it takes 8 warps (two per scheduler, so one warp's dependent chain
-// hides behind the other's) when two stages per warp fit in shared memory, and as
-// many stages per warp (up to 4) as fit.
+// hides behind the other's) when two stages per warp fit in shared memory, else 6,
+// as many stages per warp (up to 4) as fit, up to 255 registers per thread, and a
+// receive area for the push-form cluster merge.
 // D is the key (and query) head dim, DV the value head dim. Names without a V
 // describe the K plane, names with one the V plane.
 template <int BITS, int D, int DV, int NT, int WQ, bool SOLO>
