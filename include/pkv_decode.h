@@ -197,7 +197,10 @@ int pkv_merge_partitions(const pkv_pool_layout* layout, const pkv_decode_params*
  *   - in_host page-locked and mapped into the device's address space (the default
  *     for cudaHostAlloc / pinned memory on a GB300), with in_host and in_dev
  *     16-byte aligned: the kernels read every input that lies in in_dev's range
- *     directly from in_host, over NVLink-C2C, and in_dev is not written;
+ *     directly from in_host, over NVLink-C2C, and in_dev is not written. The
+ *     block must hold the step's final values when the call is made: a grid of
+ *     one CTA per SM may read q, seq_lens and the block tables from it before the
+ *     previous kernel on the stream has finished;
  *   - otherwise: one cudaMemcpyAsync of the block into in_dev first (synchronised
  *     by the runtime when in_host is pageable); in_bytes = 0 copies nothing;
  *   - out_host such mapped memory (16-byte aligned): the kernels write the bf16

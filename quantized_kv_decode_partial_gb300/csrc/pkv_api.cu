@@ -417,6 +417,7 @@ int prepare_decode(const pkv_pool_layout* layout, const pkv_decode_params* param
   p.ws_ml = mode == pkv::kModeWorkspace ? reinterpret_cast<float*>(static_cast<char*>(workspace) + o_bytes) : nullptr;
   p.mode = mode;
   p.window = params->window;
+  p.host_inputs = 0;
   p.error_flag = error_flag;
   p.num_blocks = layout->num_blocks;
   p.num_kv_heads = HK;
@@ -575,9 +576,14 @@ int build_step(const pkv_pool_layout* layout, const pkv_decode_params* params, c
       return c && c >= lo && c < lo + in_bytes ? static_cast<const char*>(in_map) + (c - lo) : ptr;
     };
     pkv::PartialParams& p = s->pd.p;
+    const void* q0 = p.q;
+    const void* t0 = p.block_tables;
+    const void* l0 = p.seq_lens;
     p.q = static_cast<const __nv_bfloat16*>(in_place(p.q));
     p.block_tables = static_cast<const int32_t*>(in_place(p.block_tables));
     p.seq_lens = static_cast<const int32_t*>(in_place(p.seq_lens));
+    p.host_inputs = (p.seq_lens != l0 ? pkv::kHostSeqLens : 0) | (p.q != q0 ? pkv::kHostQuery : 0) |
+                    (p.block_tables != t0 ? pkv::kHostTables : 0);
     p.k_new = static_cast<const __nv_bfloat16*>(in_place(p.k_new));
     p.v_new = static_cast<const __nv_bfloat16*>(in_place(p.v_new));
     s->pd.m.seq_lens = static_cast<const int32_t*>(in_place(s->pd.m.seq_lens));

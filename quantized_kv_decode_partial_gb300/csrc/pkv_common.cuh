@@ -49,6 +49,7 @@ struct PartialParams {
   int partition_tokens, max_partitions;
   int mode;           // kModeSingle / kModeWorkspace / kModeCluster
   int window;         // sliding window in rows (0: none)
+  int host_inputs;    // kHost* bits: inputs a host-driven step keeps in host memory
   float score_scale;  // softmax scale * log2(e)
   // Fused append (k_new != nullptr): the N new rows of every (sequence, KV head),
   // cache rows len-N .. len-1, are written into their pages by the CTA whose
@@ -57,6 +58,12 @@ struct PartialParams {
   const __nv_bfloat16* v_new;
   AppendTarget app;
 };
+
+// Inputs of a host-driven step that live in (mapped) host memory, written by the host
+// before the launch and by no kernel.
+constexpr int kHostSeqLens = 1;
+constexpr int kHostQuery = 2;
+constexpr int kHostTables = 4;
 
 // How the partial kernel finishes.
 constexpr int kModeSingle = 0;     // one partition: the CTA writes bf16 output

@@ -282,7 +282,10 @@ __device__ __forceinline__ void load_group_row(uint32_t addr, float (&v)[G]) {
   }
 }
 
-template <int BITS, int D, int DV, int NT, int WQ, bool SOLO>
+// HOSTIN: a host-driven step whose length, query and block tables all live in host
+// memory the host wrote before the launch (no kernel writes them): they are read before
+// the wait for the previous kernel on the stream, so their NVLink-C2C latency overlaps it.
+template <int BITS, int D, int DV, int NT, int WQ, bool SOLO, bool HOSTIN>
 __global__ void __maxnreg__(SOLO ? 255 : 200)
     pkv_partial_kernel(const __grid_constant__ PartialParams p, const __grid_constant__ CUtensorMap tmap_k,
                        const __grid_constant__ CUtensorMap tmap_v) {
@@ -311,7 +314,7 @@ __global__ void __maxnreg__(SOLO ? 255 : 200)
     prefetch_tensormap(&tmap_k);  // kernel parameters: no dependence
     prefetch_tensormap(&tmap_v);
   }
-  wait_for_prerequisite_grids();
+  if constexpr (!HOSTIN) wait_for_prerequisite_grids();
   const int len = p.seq_lens[b];
   // This lane's query values, fetched now so their latency overlaps the length's:
   // 2 * kKs words of bf16 pairs per n-tile, in the order q_load_words reads them.
@@ -330,6 +333,7 @@ __global__ void __maxnreg__(SOLO ? 255 : 200)
     const long long blk = r / p.block_size < p.max_blocks ? r / p.block_size : p.max_blocks - 1;
     tbl_pre = static_cast<int>(ld_nc_keep_u32(p.block_tables + static_cast<size_t>(b) * p.max_blocks + blk));
   }
+  if constexpr (HOSTIN) wait_for_prerequisite_grids();  // the host inputs are in flight; the rest may depend on it
   // Fused append: the step's new K/V rows of this (sequence, KV head) are read by the
   // warp whose chunk holds them just before it issues that chunk; fetch them now.
   if (p.k_new != nullptr) {

@@ -17,20 +17,21 @@ PartialInfo info_of() {
 }
 
 // Devices on which an instantiation's function attributes are set (bit per device < 64).
-template <int BITS, int D, int DV, int NT, int WQ, bool SOLO>
+template <int BITS, int D, int DV, int NT, int WQ, bool SOLO, bool HOSTIN>
 std::atomic<unsigned long long> g_configured{0};
 
-template <int BITS, int D, int DV, int NT, int WQ, bool SOLO>
+template <int BITS, int D, int DV, int NT, int WQ, bool SOLO, bool HOSTIN>
 cudaError_t configure_once(int device) {
   using C = PartialCfg<BITS, D, DV, NT, WQ, SOLO>;
-  auto kern = pkv_partial_kernel<BITS, D, DV, NT, WQ, SOLO>;
+  auto kern = pkv_partial_kernel<BITS, D, DV, NT, WQ, SOLO, HOSTIN>;
   const unsigned long long bit = device >= 0 && device < 64 ? (1ull << device) : 0ull;
-  if (bit && (g_configured<BITS, D, DV, NT, WQ, SOLO>.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  if (bit && (g_configured<BITS, D, DV, NT, WQ, SOLO, HOSTIN>.load(std::memory_order_acquire) & bit))
+    return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);  // clusters of up to 16
   if (e != cudaSuccess) return e;
-  if (bit) g_configured<BITS, D, DV, NT, WQ, SOLO>.fetch_or(bit, std::memory_order_acq_rel);
+  if (bit) g_configured<BITS, D, DV, NT, WQ, SOLO, HOSTIN>.fetch_or(bit, std::memory_order_acq_rel);
   return cudaSuccess;
 }
 
@@ -38,8 +39,22 @@ template <int BITS, int D, int DV, int NT, int WQ, bool SOLO>
 cudaError_t launch_of(const PartialParams& p, const CUtensorMap& tk, const CUtensorMap& tv, dim3 grid,
                       cudaStream_t stream, int device) {
   using C = PartialCfg<BITS, D, DV, NT, WQ, SOLO>;
-  auto kern = pkv_partial_kernel<BITS, D, DV, NT, WQ, SOLO>;
-  cudaError_t e = configure_once<BITS, D, DV, NT, WQ, SOLO>(device);
+  auto kern = pkv_partial_kernel<BITS, D, DV, NT, WQ, SOLO, false>;
+  cudaError_t e;
+  // A grid of one CTA per SM launches as a programmatic dependent (below); when all of
+  // its length, query and block tables are host memory of a host-driven step, the
+  // variant that reads them before the dependency wait runs.
+  constexpr int kAllHost = kHostSeqLens | kHostQuery | kHostTables;
+  if constexpr (SOLO) {
+    if (p.host_inputs == kAllHost) {
+      kern = pkv_partial_kernel<BITS, D, DV, NT, WQ, SOLO, true>;
+      e = configure_once<BITS, D, DV, NT, WQ, SOLO, true>(device);
+    } else {
+      e = configure_once<BITS, D, DV, NT, WQ, SOLO, false>(device);
+    }
+  } else {
+    e = configure_once<BITS, D, DV, NT, WQ, SOLO, false>(device);
+  }
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = grid;
