@@ -361,6 +361,32 @@ def test_host_driven_step_matches_device_entry():
     assert torch.equal(step2.out_host.view(torch.int16), ref.cpu().view(torch.int16))
 
 
+def test_back_to_back_host_driven_steps():
+    # Host-driven steps of two instances enqueued back to back, with no synchronisation: the
+    # second step's kernel may start (and read its host-memory inputs) while the first is still
+    # running; each output must still be its own instance's.
+    from quantized_kv_decode_partial_gb300 import HostDecodeStep
+    stream = torch.cuda.Stream(device=DEV)
+    steps, refs = [], []
+    for k in range(3):
+        sp = spec(f"host_b2b_{k}", head_dim=256, bits=4, block_size=32, length_range=(200, 600))
+        case = make_case(sp)
+        d = case.to(DEV)
+        refs.append(run_gpu(d, partition_tokens=64).cpu())
+        steps.append(HostDecodeStep(case.q, case.block_tables, case.seq_lens, d.k_pool, d.v_pool, case.scale, bits=4,
+                                    k_scales=d.k_scales, k_biases=d.k_biases, v_scales=d.v_scales,
+                                    v_biases=d.v_biases, partition_tokens=64, stream=stream))
+    torch.cuda.synchronize()
+    for _ in range(2):
+        for st in steps:
+            st.out_host.fill_(float("nan"))
+        for st in steps:
+            st()
+        stream.synchronize()
+        for st, ref in zip(steps, refs):
+            assert torch.equal(st.out_host.view(torch.int16), ref.view(torch.int16))
+
+
 def test_host_driven_fused_step_matches_device_fused_step():
     from quantized_kv_decode_partial_gb300 import HostDecodeStep
     sp = spec("host_fused", num_q_heads=8, num_kv_heads=2, n_query=2, length_range=(3, 300))
