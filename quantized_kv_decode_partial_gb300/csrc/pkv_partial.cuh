@@ -286,7 +286,7 @@ __device__ __forceinline__ void load_group_row(uint32_t addr, float (&v)[G]) {
 // memory the host wrote before the launch (no kernel writes them): they are read before
 // the wait for the previous kernel on the stream, so their NVLink-C2C latency overlaps it.
 template <int BITS, int D, int DV, int NT, int WQ, bool SOLO, bool HOSTIN>
-__global__ void __maxnreg__(SOLO ? 255 : 200)
+__global__ void __maxnreg__(255)
     pkv_partial_kernel(const __grid_constant__ PartialParams p, const __grid_constant__ CUtensorMap tmap_k,
                        const __grid_constant__ CUtensorMap tmap_v) {
   using C = PartialCfg<BITS, D, DV, NT, WQ, SOLO>;
