@@ -33,7 +33,9 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "paged decode attention K/V GB/s and steps/s; % of GB300 HBM roofline"
-DEFAULT_WORKLOAD = "affine4_g64_1x8192_hq16_d256"
+# The largest single-GPU configuration: 64 sequences of 1024-32768 rows, HQ=32 HK=8
+# D=256, one 4-bit and one 8-bit affine layer per step (7.55 GB of K/V per step).
+DEFAULT_WORKLOAD = "affine_batch64_hq32_d256"
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -53,11 +55,20 @@ def parse_args(argv=None):
     ap.add_argument("--partition-tokens", type=int, default=-2,
                     help="rows per partition instead of the workload's choice (0: the library's plan)")
     ap.add_argument("--print-kernel-hash", action="store_true",
-                    help="print the hash of the CUDA sources that profiles/dram_traffic.md rows refer to, and exit")
+                    help="print the hash of the CUDA sources that profiles/dram_traffic.json rows refer to, and exit")
+    ap.add_argument("--record-traffic", nargs="+", metavar="NCU_CSV",
+                    help="store the DRAM bytes of one step of --workload, summed over these ncu CSV logs, in "
+                         "profiles/dram_traffic.json for the current kernel sources, and exit")
+    ap.add_argument("--contraction", choices=["auto", "tensor", "cuda_core"], default="auto",
+                    help="the contraction the kernels run: the library's choice, tensor-core MMA, or per-lane "
+                         "f32 FMAs with warp-shuffle reductions (bf16 pages, at most 4 query rows per KV head)")
     ap.add_argument("--step", choices=["decode", "fused"], default="decode",
                     help="decode: the decode call; fused: the decode step with its write "
                          "(pkv_paged_decode_append_attention: append the N new K/V rows, then attend)")
     return ap.parse_args(argv)
+
+
+CONTRACTIONS = {"auto": 0, "tensor": 1, "cuda_core": 2}
 
 
 def workload_specs(name):
@@ -82,29 +93,85 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.md")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
 
 
-def recorded_traffic(workload, step):
+def recorded_traffic(workload, step, path=TRAFFIC_FILE):
     """DRAM bytes (read + write) of the partial-pass launches of one step, from the ncu
-    capture recorded in profiles/dram_traffic.md for the current kernel sources, or None
+    capture recorded in profiles/dram_traffic.json for the current kernel sources, or None
     (no capture, or the kernels changed since)."""
     if step != "decode":
         return None
     try:
-        with open(TRAFFIC_FILE) as f:
-            lines = f.read().splitlines()
-    except OSError:
+        with open(path) as f:
+            rows = json.load(f)["rows"]
+    except (OSError, ValueError, KeyError, TypeError):
         return None
     want = kernel_source_hash()
-    for line in lines:
-        cells = [c.strip().strip("`") for c in line.strip().strip("|").split("|")]
-        if len(cells) >= 3 and cells[0] == workload and cells[1] == want:
-            try:
-                return int(cells[2].replace(",", ""))
-            except ValueError:
-                return None
+    for row in rows if isinstance(rows, list) else []:
+        if isinstance(row, dict) and row.get("workload") == workload and row.get("kernel_sources") == want:
+            value = row.get("dram_bytes")
+            return int(value) if isinstance(value, int) and value > 0 else None
     return None
+
+
+NCU_UNITS = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "Tbyte": 1e12}
+
+
+def ncu_dram_bytes(csv_paths):
+    """DRAM bytes read + written by the partial-pass launches in ncu CSV logs
+    (``--metrics dram__bytes_read.sum,dram__bytes_write.sum --csv --log-file``)."""
+    import csv
+    total = 0.0
+    for path in csv_paths:
+        with open(path) as f:
+            lines = [line for line in f if line.startswith('"')]
+        for row in csv.DictReader(lines):
+            if "pkv_partial" not in row.get("Kernel Name", ""):
+                continue
+            if row.get("Metric Name") in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+                total += float(row["Metric Value"].replace(",", "")) * NCU_UNITS[row["Metric Unit"]]
+    return int(round(total))
+
+
+def record_traffic(workload, csv_paths, path=TRAFFIC_FILE):
+    """Stores the DRAM bytes of one step of `workload` (the sum over the given ncu logs,
+    one per layer) for the current kernel sources in profiles/dram_traffic.json."""
+    from quantized_kv_decode_partial_gb300.workloads import draw_lengths, required_kv_bytes
+    dram = ncu_dram_bytes(csv_paths)
+    if dram <= 0:
+        raise SystemExit(f"no pkv_partial DRAM metrics in {csv_paths}")
+    algo = sum(required_kv_bytes(sp, draw_lengths(sp)) for sp in workload_specs(workload))
+    try:
+        with open(path) as f:
+            doc = json.load(f)
+    except (OSError, ValueError):
+        doc = {}
+    rows = [r for r in doc.get("rows", []) if r.get("workload") != workload]
+    rows.append({"workload": workload, "kernel_sources": kernel_source_hash(), "dram_bytes": dram,
+                 "algorithmic_bytes": algo, "ratio": round(dram / algo, 4)})
+    doc = {"what": "DRAM bytes read + written by the partial-pass launches of one decode step (ncu "
+                   "dram__bytes_read.sum + dram__bytes_write.sum, one capture per layer, each launch "
+                   "profiled in one pass), for the CUDA sources whose hash is kernel_sources",
+           "rows": sorted(rows, key=lambda r: r["workload"])}
+    with open(path, "w") as f:
+        json.dump(doc, f, indent=1)
+        f.write("\n")
+    return rows[-1]
+
+
+def compute_dtype(bits_list, contractions=None):
+    """The arithmetic the timed kernels run, per page format (and contraction) of the
+    step's layers."""
+    names = []
+    for i, bits in enumerate(bits_list):
+        cuda_cores = contractions is not None and contractions[i] == 2
+        name = ("bf16 pages: f32 FMAs on CUDA cores (f32 products of bf16 values)" if cuda_cores else
+                "bf16 pages: bf16 tensor-core products" if bits == 16 else
+                f"{bits}-bit affine pages: fp16 tensor-core products on exact-subnormal codes")
+        if name not in names:
+            names.append(name)
+    return "; ".join(names) + "; f32 softmax and accumulation; bf16 output"
 
 
 def measured_hbm_peak():
@@ -120,15 +187,95 @@ def measured_hbm_peak():
 # clocks during the timed region
 # ---------------------------------------------------------------------------
 
+class NvmlClockPoller:
+    """Reads the SM clock and the clock-event reasons through NVML (the driver's
+    libnvidia-ml, read-only calls) every few milliseconds in a thread, so that a timed
+    region of a few tens of milliseconds still gets many samples."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown"}
+
+    def __init__(self, torch_device, period_s=0.002):
+        import ctypes
+        import threading
+        self.samples = []
+        self.period = period_s
+        self._stop = threading.Event()
+        self._thread = None
+        self.handle = None
+        self.max_mhz = None
+        try:
+            self.nvml = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nvml.nvmlInit_v2() != 0:
+                return
+            handle = ctypes.c_void_p()
+            uuid = None
+            try:
+                import torch
+                uuid = str(torch.cuda.get_device_properties(torch_device).uuid)
+            except Exception:
+                uuid = None
+            ok = False
+            if uuid:
+                ok = self.nvml.nvmlDeviceGetHandleByUUID(("GPU-" + uuid).encode(), ctypes.byref(handle)) == 0
+            if not ok:
+                ok = self.nvml.nvmlDeviceGetHandleByIndex_v2(int(torch_device.index or 0), ctypes.byref(handle)) == 0
+            if not ok:
+                return
+            self.handle = handle
+            mx = ctypes.c_uint()
+            if self.nvml.nvmlDeviceGetMaxClockInfo(self.handle, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = float(mx.value)
+        except OSError:
+            self.handle = None
+
+    def _read(self):
+        import ctypes
+        clk = ctypes.c_uint()
+        reasons = ctypes.c_ulonglong()
+        if self.nvml.nvmlDeviceGetClockInfo(self.handle, 1, ctypes.byref(clk)) != 0:
+            return None
+        fn = getattr(self.nvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.nvml.nvmlDeviceGetCurrentClocksThrottleReasons
+        if fn(self.handle, ctypes.byref(reasons)) != 0:
+            reasons.value = 0
+        return float(clk.value), int(reasons.value)
+
+    def _run(self):
+        while not self._stop.is_set():
+            r = self._read()
+            if r is not None:
+                self.samples.append(r)
+            self._stop.wait(self.period)
+
+    def start(self):
+        if self.handle is None:
+            return
+        import threading
+        self._thread = threading.Thread(target=self._run, daemon=True)
+        self._thread.start()
+
+    def stop(self):
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join(timeout=5)
+        reasons = set()
+        for _, bits in self.samples:
+            for bit, name in self.REASONS.items():
+                if bits & bit:
+                    reasons.add(name)
+        return [mhz for mhz, _ in self.samples], sorted(reasons)
+
+
 class ClockSampler:
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, torch_device=None):
         self.gpu = gpu_index
         self.proc = None
         self.path = None
+        self.poller = NvmlClockPoller(torch_device) if torch_device is not None else None
 
     def _once(self):
         try:
@@ -140,6 +287,8 @@ class ClockSampler:
 
     def start(self):
         self.lines = self._once()
+        if self.poller is not None:
+            self.poller.start()
         fd, self.path = tempfile.mkstemp(suffix=".csv")
         os.close(fd)
         try:
@@ -150,6 +299,7 @@ class ClockSampler:
             self.proc = None
 
     def stop(self):
+        self.nvml = self.poller.stop() if self.poller is not None else ([], [])
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -181,10 +331,18 @@ class ClockSampler:
             for name, flag in zip(names, parts[5:9]):
                 if flag.lower() == "active":
                     reasons.add(name)
+        nvml_mhz, nvml_reasons = getattr(self, "nvml", ([], []))
+        reasons.update(nvml_reasons)
+        if nvml_mhz:  # NVML polled every few ms during the timed region: the denser record
+            mx_nvml = self.poller.max_mhz or (max(mx) if mx else None)
+            return {"sm_mhz": statistics.median(nvml_mhz), "sm_max_mhz": mx_nvml, "reasons": sorted(reasons),
+                    "samples": len(nvml_mhz), "sm_mhz_min": min(nvml_mhz),
+                    "source": "NVML every 2 ms during the timed region (plus nvidia-smi every 100 ms: "
+                              f"{len(sm)} samples, reasons included)"}
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "source": "nvidia-smi every 100 ms during the timed region"}
 
 
 # ---------------------------------------------------------------------------
@@ -331,7 +489,7 @@ def run_ours(args):
                                     lengths=base.lens_host) for c in range(copies - 1)]
         layout = layout_for(base.k_pool, sp.head_dim, sp.bits, sp.group_size, v_pool=base.v_pool)
         params = DecodeParams(sp.num_seqs, sp.num_q_heads, sp.n_query, base.block_tables.shape[1],
-                              base.partition_tokens, sp.window)
+                              base.partition_tokens, sp.window, CONTRACTIONS[args.contraction])
         plan = make_plan(layout, params)
         ws = torch.empty(max(1, plan.workspace_bytes), dtype=torch.uint8, device=dev)
         out = torch.empty(base.q.shape[:-1] + (sp.dv,), dtype=base.q.dtype, device=dev)
@@ -351,7 +509,7 @@ def run_ours(args):
         sp = L["spec"]
         kw = dict(bits=sp.bits, group_size=sp.group_size, k_scales=c.k_scales, k_biases=c.k_biases,
                   v_scales=c.v_scales, v_biases=c.v_biases, partition_tokens=c.partition_tokens, window=sp.window,
-                  out=L["out"], workspace=L["ws"])
+                  out=L["out"], workspace=L["ws"], contraction=CONTRACTIONS[args.contraction])
         if args.step == "fused":
             paged_decode_append_attention(c.q, c.k_new, c.v_new, c.k_pool, c.v_pool, c.block_tables, c.seq_lens,
                                           c.scale, **kw)
@@ -360,17 +518,17 @@ def run_ours(args):
         else:
             paged_decode_passes(c.q, c.k_pool, c.v_pool, c.block_tables, c.seq_lens, c.scale, passes=passes, **kw)
 
-    def step(i, passes=None):
-        for L in layers:
+    def step(i, passes=None, only=None):
+        for L in layers if only is None else [only]:
             call(L, i, passes)
 
     stream = torch.cuda.Stream(device=dev)
 
-    def capture(n, passes=None, offset=0):
+    def capture(n, passes=None, offset=0, only=None):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             for i in range(n):
-                step(offset + i, passes)
+                step(offset + i, passes, only)
         return g
 
     def replay_timed(graphs_reps):
@@ -408,7 +566,7 @@ def run_ours(args):
         g_rest.replay()
     torch.cuda.synchronize(dev)
 
-    clocks = ClockSampler(local)
+    clocks = ClockSampler(local, dev)
     clocks.start()
     ms = replay_timed([(g_full, K // chunk)] + ([(g_rest, 1)] if g_rest else []))
     clk = clocks.stop()
@@ -423,6 +581,19 @@ def run_ours(args):
         g_part.replay()
         torch.cuda.synchronize(dev)
         ms_partial = replay_timed([(g_part, K // chunk)] + ([(g_part_rest, 1)] if g_part_rest else []))
+        del g_part, g_part_rest
+
+    # each layer's partial pass alone, when a step has several layers
+    layer_rows = []
+    if len(layers) > 1 and args.step != "fused":
+        for L in layers:
+            g1 = capture(chunk, passes="partial", only=L)
+            g1_rest = capture(rest, passes="partial", only=L) if rest else None
+            g1.replay()
+            torch.cuda.synchronize(dev)
+            ms1 = replay_timed([(g1, K // chunk)] + ([(g1_rest, 1)] if g1_rest else [])) / K
+            del g1, g1_rest
+            layer_rows.append((L, ms1))
 
     # end to end through the public host-driven step (pkv_step_run): per step the
     # kernels read the step's inputs (q, block tables, lengths and, for the fused step,
@@ -436,7 +607,7 @@ def run_ours(args):
             k_new=c.k_new if args.step == "fused" else None, v_new=c.v_new if args.step == "fused" else None,
             bits=sp.bits, group_size=sp.group_size, k_scales=c.k_scales, k_biases=c.k_biases, v_scales=c.v_scales,
             v_biases=c.v_biases, partition_tokens=c.partition_tokens, window=sp.window, workspace=L["ws"],
-            stream=stream) for c in L["insts"]])
+            stream=stream, contraction=CONTRACTIONS[args.contraction]) for c in L["insts"]])
     h2d = sum(hs[0].h2d_bytes for hs in host_steps)
     d2h = sum(hs[0].d2h_bytes for hs in host_steps)
     e2e_steps = min(K, max(50, n_copies))
@@ -472,7 +643,7 @@ def run_ours(args):
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
             "ms_per_step": ms_step, "steps_per_s": 1e3 / ms_step * world, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16 tensor-core products, f32 softmax/accumulate",
+            "scaling": "weak", "vs_baseline": None, "dtype": compute_dtype([L["spec"].bits for L in layers], [L["plan"].contraction for L in layers]),
             "data": "synthetic",
             "config": {
                 "workload": args.workload,
@@ -487,11 +658,12 @@ def run_ours(args):
                          "decode step with its write (pkv_paged_decode_append_attention): the N new K/V rows of "
                          "every (sequence, KV head) are written into their pages, then the grown cache is read"),
                 "parallelism": f"dp{world} (independent instances)",
+                "contraction": ["cuda cores" if L["plan"].contraction == 2 else "tensor cores" for L in layers],
             },
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": recorded_traffic(args.workload, args.step),
                          "traffic_unit": "DRAM bytes read + written by the partial-pass launches of one step "
-                                         "(ncu, profiles/dram_traffic.md); algorithmic bytes per step: "
+                                         "(ncu, profiles/dram_traffic.json); algorithmic bytes per step: "
                                          f"{step_bytes}",
                          "kernel": (f"pkv_partial_kernel (partial pass alone, {part_ms * 1e3:.2f} us per step)"
                                     if args.step == "decode" else
@@ -508,6 +680,12 @@ def run_ours(args):
             "gpu_launches": launches_per_step * K,
             "clocks": clk,
         }
+        if layer_rows:  # per layer: its partial pass alone, timed the same way
+            line["roofline"]["layers"] = [
+                {"workload": L["spec"].name, "kv_bytes": L["kv_bytes"], "us_partial": ms1 * 1e3,
+                 "achieved": L["kv_bytes"] / (ms1 * 1e-3) / 1e9,
+                 "frac": L["kv_bytes"] / (ms1 * 1e-3) / 1e9 / peak,
+                 "traffic": recorded_traffic(L["spec"].name, args.step)} for L, ms1 in layer_rows]
         if cpu is not None:
             line["cpu_baseline"] = {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")}
         print(json.dumps(line), flush=True)
@@ -540,7 +718,7 @@ def run_profile_calls(args):
             paged_decode_attention(c.q, c.k_pool, c.v_pool, c.block_tables, c.seq_lens, c.scale, bits=sp.bits,
                                    group_size=sp.group_size, k_scales=c.k_scales, k_biases=c.k_biases,
                                    v_scales=c.v_scales, v_biases=c.v_biases, partition_tokens=c.partition_tokens,
-                                   window=sp.window)
+                                   window=sp.window, contraction=CONTRACTIONS[args.contraction])
         torch.cuda.synchronize()
         print(json.dumps({"profile_calls": args.profile_calls, "workload": sp.name, "num_seqs": sp.num_seqs,
                           "kv_bytes_per_call": required_kv_bytes(sp, c.lens_host)}), flush=True)
@@ -550,6 +728,8 @@ def main(argv=None):
     args = parse_args(argv)
     if args.print_kernel_hash:
         print(kernel_source_hash())
+    elif args.record_traffic:
+        print(json.dumps(record_traffic(args.workload, args.record_traffic)))
     elif args.profile_calls:
         run_profile_calls(args)
     elif args.impl == "reference":

@@ -88,15 +88,17 @@ extern "C" {
 /* Device-side error bits, OR-ed into *error_flag. */
 #define PKV_DEVERR_BAD_BLOCK 1   /* a referenced block id outside [0, num_blocks): its rows were skipped */
 #define PKV_DEVERR_BAD_SEQ_LEN 2 /* seq_len < n_query or > max_blocks_per_seq*block_size: outputs zeroed */
-#define PKV_DEVERR_TIMEOUT 4     /* an internal pipeline wait gave up after about a second */
+#define PKV_DEVERR_TIMEOUT 4     /* an internal pipeline wait gave up (after about a second by
+                                    default, see pkv_set_wait_limit_ns); the outputs of that call
+                                    are then unspecified */
 
 /* Pool layout descriptor (the pages' PagedAttentionStorage: blockSize, headDim,
  * vHeadDim, quantization {bits, groupSize}).
- * Head dims with a kernel (key/value; the host rejects the rest):
- *   equal dims: 64, 128, 256 (bf16) and 128, 256 (affine), with up to 64 / 64 / 32
- *   query rows per KV head (64 / 32 for affine);
- *   bf16 192/128 (up to 32 query rows), 256/128 and 128/256 (up to 8);
- *   affine 256/128 and 128/256 (up to 8). */
+ * Head dims with a kernel (key/value; the host rejects the rest), each with up to 64
+ * query rows per KV head ((num_q_heads / num_kv_heads) * n_query, the pages' limit for
+ * the few-query kernel, kernels/attention/multi-query.ts):
+ *   equal dims: 64, 128, 256 (bf16) and 128, 256 (affine);
+ *   bf16 192/128, 256/128 and 128/256; affine 256/128 and 128/256. */
 typedef struct pkv_pool_layout {
   int32_t num_blocks;   /* blocks in the pool, > 0 */
   int32_t num_kv_heads; /* HK, > 0 */
@@ -120,7 +122,19 @@ typedef struct pkv_decode_params {
                                  t with len-N+i-W < t <= len-N+i (the W most recent positions,
                                  its own included), as the pages' causal mask with a window
                                  size (kernels/attention/masks.ts, createCausalMask) */
+  int32_t contraction;        /* how the dot products and the weighted value sums run:
+                                 PKV_CONTRACTION_AUTO (0, the library's choice per shape),
+                                 PKV_CONTRACTION_TENSOR (1, warp-level tensor-core MMA) or
+                                 PKV_CONTRACTION_CUDA_CORE (2, per-lane f32 FMAs with warp-shuffle
+                                 reductions, the form of the pages' direct paged kernel,
+                                 kernels/attention/paged.ts; bf16 pages with equal key/value head
+                                 dims and at most 4 query rows per KV head, else
+                                 PKV_ERR_UNSUPPORTED_SHAPE) */
 } pkv_decode_params;
+
+#define PKV_CONTRACTION_AUTO 0
+#define PKV_CONTRACTION_TENSOR 1
+#define PKV_CONTRACTION_CUDA_CORE 2
 
 /* How a call will be carried out. */
 typedef struct pkv_plan {
@@ -136,6 +150,8 @@ typedef struct pkv_plan {
   int32_t merge_in_cluster; /* 1: the partitions of each (sequence, KV head) form one thread-block
                                cluster and merge through distributed shared memory inside the
                                partial kernel (2..16 partitions on a grid of at most one wave) */
+  int32_t contraction;      /* the contraction the call runs: PKV_CONTRACTION_TENSOR or
+                               PKV_CONTRACTION_CUDA_CORE */
   size_t workspace_bytes;   /* device scratch for the partition states; 0 with one partition
                                or with merge_in_cluster */
 } pkv_plan;
@@ -261,8 +277,10 @@ void pkv_step_destroy(pkv_step* step);
  * rejected with PKV_ERR_SCRATCH_TOO_SMALL.
  *
  * Set-up: the first call on each device looks up the scratch's device address
- * (cudaGetSymbolAddress, with that device current) and caches it. Make that
- * first call before any stream capture on the device.
+ * (cudaGetSymbolAddress, with that device current) and caches it, keyed on the
+ * device's current context; a call after a device reset (which makes a new
+ * context and loads the module again) looks it up anew. Make the first call on a
+ * device, and the first after a reset, before any stream capture on it.
  *
  * Sharing: every call on a device uses the same scratch, which keeps the last
  * call's contents; nothing in it needs to start at zero. Calls whose kernels
@@ -345,6 +363,19 @@ const char* pkv_strerror(int code);
 
 /* Text of the last PKV_ERR_CUDA failure on this thread (static per-thread storage). */
 const char* pkv_last_cuda_error(void);
+
+/* Sets the bound, in nanoseconds, of one wait of the partial kernel's main loop for
+ * the data of a pipeline stage, for every decode call prepared after it in this
+ * process (a pkv_step keeps the bound it was created with), and returns the previous
+ * bound; 0 restores the default of one second. The pages have no counterpart of it.
+ * A wait that runs out gives up without a fault: the kernel sets PKV_DEVERR_TIMEOUT
+ * in *error_flag, stops reading, lets every copy it has issued land (that drain waits
+ * up to the default bound), finishes its epilogue and returns, so the stream and the
+ * context stay usable and the output of that call is unspecified. It exists to check
+ * this give-up path on a working GPU: a bound shorter than the time a stage takes
+ * to arrive from HBM (a few microseconds) makes it run out on any input. Not
+ * thread-safe against calls being prepared on other threads. */
+uint64_t pkv_set_wait_limit_ns(uint64_t ns);
 
 /* Library version, major*10000 + minor*100 + patch. */
 int pkv_version(void);

@@ -17,4 +17,5 @@ from .binding import (  # noqa: F401
     HostDecodeStep,
     paged_append,
     paged_gather,
+    set_wait_limit_ns,
 )

@@ -32,6 +32,7 @@ EXPORTS = (
     "pkv_paged_gather",
     "pkv_strerror",
     "pkv_last_cuda_error",
+    "pkv_set_wait_limit_ns",
     "pkv_version",
 )
 
@@ -45,6 +46,10 @@ PKV_ERR_WORKSPACE_TOO_SMALL = -6
 PKV_ERR_CUDA = -7
 PKV_ERR_SCRATCH_TOO_SMALL = -8
 PKV_STATIC_SCRATCH_BYTES = 16 << 20
+
+PKV_CONTRACTION_AUTO = 0
+PKV_CONTRACTION_TENSOR = 1
+PKV_CONTRACTION_CUDA_CORE = 2
 
 PKV_DEVERR_BAD_BLOCK = 1
 PKV_DEVERR_BAD_SEQ_LEN = 2
@@ -68,13 +73,14 @@ class PoolLayout(ctypes.Structure):
 
 class DecodeParams(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in
-                ("num_seqs", "num_q_heads", "n_query", "max_blocks_per_seq", "partition_tokens", "window")]
+                ("num_seqs", "num_q_heads", "n_query", "max_blocks_per_seq", "partition_tokens", "window",
+                 "contraction")]
 
 
 class Plan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in
                 ("partition_tokens", "max_partitions", "chunk_rows", "sm_count", "threads_per_cta",
-                 "smem_bytes", "merge_in_cluster")] + [("workspace_bytes", ctypes.c_size_t)]
+                 "smem_bytes", "merge_in_cluster", "contraction")] + [("workspace_bytes", ctypes.c_size_t)]
 
 
 _lib = None
@@ -131,6 +137,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.pkv_last_cuda_error.restype = ctypes.c_char_p
     lib.pkv_version.argtypes = []
     lib.pkv_version.restype = ctypes.c_int
+    lib.pkv_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+    lib.pkv_set_wait_limit_ns.restype = ctypes.c_uint64
     if path == LIB_PATH:
         _lib = lib
     return lib
@@ -185,6 +193,13 @@ def _cached_plan(layout: PoolLayout, params: DecodeParams) -> Plan:
     return plan
 
 
+def set_wait_limit_ns(ns: int) -> int:
+    """Bound of one main-loop pipeline wait for decode calls made from now on
+    (pkv_set_wait_limit_ns; 0 restores the default of one second). Returns the
+    previous bound."""
+    return int(load_library().pkv_set_wait_limit_ns(int(ns)))
+
+
 def make_plan(layout: PoolLayout, params: DecodeParams, sm_count: Optional[int] = None) -> Plan:
     """The library's plan (partition size, workspace bytes) for these shapes."""
     lib = load_library()
@@ -204,7 +219,7 @@ def paged_decode_attention(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.
                            v_scales: Optional[torch.Tensor] = None, v_biases: Optional[torch.Tensor] = None,
                            partition_tokens: int = 0, window: int = 0, out: Optional[torch.Tensor] = None,
                            workspace: Optional[torch.Tensor] = None,
-                           error_flag: Optional[torch.Tensor] = None) -> torch.Tensor:
+                           error_flag: Optional[torch.Tensor] = None, contraction: int = 0) -> torch.Tensor:
     """Decode attention over a paged cache (see include/pkv_decode.h).
 
     q bf16 [B, HQ, N, D]; pools bf16 [NB, HK, BS, D] (bits=16) or int32 code
@@ -215,7 +230,7 @@ def paged_decode_attention(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.
     lib = load_library()
     B, HQ, N, D = q.shape
     layout = layout_for(k_pool, D, bits, group_size, v_pool)
-    params = DecodeParams(B, HQ, N, block_tables.shape[1], partition_tokens, window)
+    params = DecodeParams(B, HQ, N, block_tables.shape[1], partition_tokens, window, contraction)
     with _on_device(q.device):
         plan = _cached_plan(layout, params)
         if out is None:
@@ -239,14 +254,14 @@ def paged_decode_append_attention(q: torch.Tensor, k_new: torch.Tensor, v_new: t
                                   v_scales: Optional[torch.Tensor] = None, v_biases: Optional[torch.Tensor] = None,
                                   partition_tokens: int = 0, window: int = 0, out: Optional[torch.Tensor] = None,
                                   workspace: Optional[torch.Tensor] = None,
-                                  error_flag: Optional[torch.Tensor] = None) -> torch.Tensor:
+                                  error_flag: Optional[torch.Tensor] = None, contraction: int = 0) -> torch.Tensor:
     """One decode step with its write (pkv_paged_decode_append_attention): writes
     k_new/v_new bf16 [B, HK, N, D] at cache positions seq_lens[b]-N .. seq_lens[b]-1
     (seq_lens counts the new rows), then attends as ``paged_decode_attention``."""
     lib = load_library()
     B, HQ, N, D = q.shape
     layout = layout_for(k_pool, D, bits, group_size, v_pool)
-    params = DecodeParams(B, HQ, N, block_tables.shape[1], partition_tokens, window)
+    params = DecodeParams(B, HQ, N, block_tables.shape[1], partition_tokens, window, contraction)
     with _on_device(q.device):
         plan = _cached_plan(layout, params)
         if out is None:
@@ -284,12 +299,12 @@ class HostDecodeStep:
                  v_new: Optional[torch.Tensor] = None, bits: int = 16, group_size: int = 64, k_scales=None,
                  k_biases=None, v_scales=None, v_biases=None, partition_tokens: int = 0, window: int = 0,
                  workspace: Optional[torch.Tensor] = None, error_flag: Optional[torch.Tensor] = None, stream=None,
-                 copy_tables: bool = True):
+                 copy_tables: bool = True, contraction: int = 0):
         self.lib = lib = load_library()
         dev = k_pool.device
         B, HQ, N, D = q.shape
         self.layout = layout_for(k_pool, D, bits, group_size, v_pool)
-        self.params = DecodeParams(B, HQ, N, block_tables.shape[1], partition_tokens, window)
+        self.params = DecodeParams(B, HQ, N, block_tables.shape[1], partition_tokens, window, contraction)
         named = [("q", q), ("seq_lens", seq_lens)]
         if k_new is not None:
             named += [("k_new", k_new), ("v_new", v_new)]
@@ -381,14 +396,14 @@ def paged_decode_passes(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Ten
                         v_biases=None, partition_tokens: int = 0, window: int = 0,
                         out: Optional[torch.Tensor] = None,
                         workspace: Optional[torch.Tensor] = None,
-                        error_flag: Optional[torch.Tensor] = None) -> torch.Tensor:
+                        error_flag: Optional[torch.Tensor] = None, contraction: int = 0) -> torch.Tensor:
     """One pass of the decode: ``passes="partial"`` (pkv_paged_decode_partial) or
     ``"merge"`` (pkv_merge_partitions). ``out`` and, with more than one
     partition, ``workspace`` must be given so the two calls share them."""
     lib = load_library()
     B, HQ, N, D = q.shape
     layout = layout_for(k_pool, D, bits, group_size, v_pool)
-    params = DecodeParams(B, HQ, N, block_tables.shape[1], partition_tokens, window)
+    params = DecodeParams(B, HQ, N, block_tables.shape[1], partition_tokens, window, contraction)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     with _on_device(q.device):
         stream = torch.cuda.current_stream(q.device).cuda_stream

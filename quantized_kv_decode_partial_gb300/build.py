@@ -26,6 +26,7 @@ SOURCES = [
     "pkv_merge_gather.cu",
     "pkv_append.cu",
     "pkv_partial_bf16.cu",
+    "pkv_partial_bf16_cc.cu",
     "pkv_partial_u4.cu",
     "pkv_partial_u8.cu",
 ]

@@ -28,7 +28,9 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
 
-PartialInfo partial_info(int bits, int dk, int dv, int nq, bool solo = false) {
+// cc: the CUDA-core contraction (bf16 pages only), else the tensor-core one.
+PartialInfo partial_info(int bits, int dk, int dv, int nq, bool solo = false, bool cc = false) {
+  if (cc) return bits == 16 ? pkv::partial_info_bf16_cc(dk, dv, nq, solo) : PartialInfo{false, 0, 0, 0, 0, 0, 0};
   if (bits == 16) return pkv::partial_info_bf16(dk, dv, nq, solo);
   if (bits == 4) return pkv::partial_info_u4(dk, dv, nq, solo);
   if (bits == 8) return pkv::partial_info_u8(dk, dv, nq, solo);
@@ -71,13 +73,27 @@ int check_params(const pkv_pool_layout* L, const pkv_decode_params* P) {
   if (P->n_query < 1 || P->max_blocks_per_seq <= 0 || P->partition_tokens < 0 || P->window < 0)
     return PKV_ERR_BAD_PARAMS;
   if (static_cast<long long>(P->max_blocks_per_seq) * L->block_size >= (1ll << 31)) return PKV_ERR_BAD_PARAMS;
+  if (P->contraction < PKV_CONTRACTION_AUTO || P->contraction > PKV_CONTRACTION_CUDA_CORE) return PKV_ERR_BAD_PARAMS;
   const long long nq = static_cast<long long>(P->num_q_heads / L->num_kv_heads) * P->n_query;
   if (nq > 64) return PKV_ERR_UNSUPPORTED_SHAPE;
-  if (!partial_info(L->bits, L->head_dim, v_dim(L), static_cast<int>(nq)).exists) return PKV_ERR_UNSUPPORTED_SHAPE;
+  const bool cc = P->contraction == PKV_CONTRACTION_CUDA_CORE;
+  if (!partial_info(L->bits, L->head_dim, v_dim(L), static_cast<int>(nq), false, cc).exists)
+    return PKV_ERR_UNSUPPORTED_SHAPE;
   return PKV_OK;
 }
 
-int round_up(long long x, int m) { return static_cast<int>((x + m - 1) / m * m); }
+// Whether a call runs the CUDA-core contraction: when the caller asks for it, or, left to
+// the library, for the shapes where it measured faster than the tensor cores.
+bool use_cuda_cores(const pkv_pool_layout* L, const pkv_decode_params* P, long long ctas, int sm_count) {
+  if (P->contraction == PKV_CONTRACTION_CUDA_CORE) return true;
+  if (P->contraction == PKV_CONTRACTION_TENSOR) return false;
+  (void)L;
+  (void)ctas;
+  (void)sm_count;
+  return false;
+}
+
+long long round_up(long long x, long long m) { return (x + m - 1) / m * m; }
 
 // Rows a step can read per sequence, counted from its partition base: the whole
 // table, or with a window the span of W + N - 1 rows its queries see plus the
@@ -95,7 +111,8 @@ int plan_impl(const pkv_pool_layout* L, const pkv_decode_params* P, int sm_count
   const long long max_len = static_cast<long long>(P->max_blocks_per_seq) * L->block_size;
   long long part;
   if (P->partition_tokens > 0) {
-    part = round_up(P->partition_tokens, ch);
+    // A caller's size past the table means one partition (INT_MAX included).
+    part = round_up(std::min<long long>(P->partition_tokens, max_len), ch);
   } else {
     // Halve the partition until the grid covers the GPU about four times over (two
     // CTAs per SM), never below 256 rows. Once the grid fills a wave, stop before a
@@ -123,7 +140,8 @@ int plan_impl(const pkv_pool_layout* L, const pkv_decode_params* P, int sm_count
     // at least 512 KB, take the most partitions that do: the partitions then merge
     // inside their clusters, with no workspace and no second launch.
     const long long nq_rows = static_cast<long long>(P->num_q_heads / L->num_kv_heads) * P->n_query;
-    const PartialInfo two = partial_info(L->bits, L->head_dim, v_dim(L), static_cast<int>(nq_rows), false);
+    const PartialInfo two = partial_info(L->bits, L->head_dim, v_dim(L), static_cast<int>(nq_rows), false,
+                                         P->contraction == PKV_CONTRACTION_CUDA_CORE);
     const long long default_ctas = units * ((span + part - 1) / part);
     if (P->window > 0 && default_ctas <= 2 * slots && two.exists && two.smem_bytes <= 114 * 1024) {
       for (int k = pkv::kMaxClusterParts; k >= 2; --k) {
@@ -145,10 +163,12 @@ int plan_impl(const pkv_pool_layout* L, const pkv_decode_params* P, int sm_count
   // per CTA, where there is one for this shape.
   const long long sms = sm_count > 0 ? sm_count : 1;
   const long long ctas = static_cast<long long>(P->num_seqs) * L->num_kv_heads * max_parts;
+  const bool cc = use_cuda_cores(L, P, ctas, sm_count);
   const bool use_solo =
-      ctas <= sms && partial_info(L->bits, L->head_dim, v_dim(L), static_cast<int>(nq), true).exists;
+      ctas <= sms && partial_info(L->bits, L->head_dim, v_dim(L), static_cast<int>(nq), true, cc).exists;
   if (solo) *solo = use_solo;
-  const PartialInfo info = partial_info(L->bits, L->head_dim, v_dim(L), static_cast<int>(nq), use_solo);
+  const PartialInfo info = partial_info(L->bits, L->head_dim, v_dim(L), static_cast<int>(nq), use_solo, cc);
+  out->contraction = cc ? PKV_CONTRACTION_CUDA_CORE : PKV_CONTRACTION_TENSOR;
   out->partition_tokens = static_cast<int32_t>(part);
   out->max_partitions = max_parts;
   out->chunk_rows = info.chunk_rows;
@@ -338,6 +358,10 @@ pkv::AppendTarget append_target(bool quant, void* k_pool, void* v_pool, void* k_
 constexpr int kPassPartial = 1;
 constexpr int kPassMerge = 2;
 
+// Bound of one main-loop pipeline wait in the partial kernels launched from now on
+// (pkv_set_wait_limit_ns).
+std::atomic<unsigned long long> g_wait_limit_ns{pkv::kWaitLimitNs};
+
 // Everything one decode call launches, resolved from its arguments: the kernels'
 // parameter blocks, the TMA descriptors of the pools and the launch shapes.
 struct PreparedDecode {
@@ -346,7 +370,7 @@ struct PreparedDecode {
   CUtensorMap tk, tv;
   dim3 grid;
   int bits, dk, dv, nq, device, merge_rows;
-  bool solo, partial, merge;
+  bool solo, cc, partial, merge;
 };
 
 // Checks the arguments of a decode call (the passes in `passes`) and prepares its
@@ -388,7 +412,8 @@ int prepare_decode(const pkv_pool_layout* layout, const pkv_decode_params* param
 
   const int D = layout->head_dim, DV = v_dim(layout), HK = layout->num_kv_heads;
   const int nq = (params->num_q_heads / HK) * params->n_query;
-  const PartialInfo info = partial_info(layout->bits, D, DV, nq, solo);
+  const bool cc = plan.contraction == PKV_CONTRACTION_CUDA_CORE;
+  const PartialInfo info = partial_info(layout->bits, D, DV, nq, solo, cc);
   const long long rows = static_cast<long long>(layout->num_blocks) * HK * layout->block_size;
   const int elem = info.tensor_elem_bytes;
   const long long row_elems_k = quant ? static_cast<long long>(D) * layout->bits / 8 : D;
@@ -429,6 +454,7 @@ int prepare_decode(const pkv_pool_layout* layout, const pkv_decode_params* param
   p.partition_tokens = plan.partition_tokens;
   p.max_partitions = plan.max_partitions;
   p.score_scale = scale * 1.4426950408889634f;  // log2(e): scores run in base 2
+  p.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
   if (k_new) {  // the pools are the caller's writable planes (the fused entry takes them non-const)
     p.k_new = static_cast<const __nv_bfloat16*>(k_new);
     p.v_new = static_cast<const __nv_bfloat16*>(v_new);
@@ -443,6 +469,7 @@ int prepare_decode(const pkv_pool_layout* layout, const pkv_decode_params* param
   pd->nq = nq;
   pd->device = dev;
   pd->solo = solo;
+  pd->cc = cc;
   pd->partial = partial;
   pd->merge = (passes & kPassMerge) && mode == pkv::kModeWorkspace;
   if (pd->merge) {
@@ -470,7 +497,9 @@ int launch_prepared(const PreparedDecode& pd, cudaStream_t st) {
   (void)cudaGetLastError();  // start from a clean error state
   cudaError_t e = cudaSuccess;
   if (pd.partial) {
-    if (pd.bits == 16)
+    if (pd.cc)
+      e = pkv::launch_partial_bf16_cc(pd.dk, pd.dv, pd.nq, pd.solo, pd.p, pd.tk, pd.tv, pd.grid, st, pd.device);
+    else if (pd.bits == 16)
       e = pkv::launch_partial_bf16(pd.dk, pd.dv, pd.nq, pd.solo, pd.p, pd.tk, pd.tv, pd.grid, st, pd.device);
     else if (pd.bits == 4)
       e = pkv::launch_partial_u4(pd.dk, pd.dv, pd.nq, pd.solo, pd.p, pd.tk, pd.tv, pd.grid, st, pd.device);
@@ -747,22 +776,52 @@ static __device__ __align__(256) unsigned char g_static_scratch[PKV_STATIC_SCRAT
 
 constexpr int kMaxScratchDevices = 256;
 std::mutex g_scratch_mutex;
+// Per device: the context the address was looked up in, and the address.
+CUcontext g_scratch_context[kMaxScratchDevices] = {};
 void* g_scratch_address[kMaxScratchDevices] = {};
 
+// The driver's cuCtxGetCurrent, reached through the runtime (the library links no
+// driver library).
+PFN_cuCtxGetCurrent_v4000 current_context_getter() {
+  static PFN_cuCtxGetCurrent_v4000 fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<PFN_cuCtxGetCurrent_v4000>(nullptr);
+    return reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+  }();
+  return fn;
+}
+
 // Device address of g_static_scratch on the current device. Host code only has a
-// host-side stand-in for the array's name, so the address is looked up once per
-// device, with that device current, and cached.
+// host-side stand-in for the array's name, so the address is looked up with the
+// device current and cached per device, keyed on the device's current context: a
+// reset of the device (cudaDeviceReset) makes a new primary context, which loads the
+// module again, so the address is looked up again there.
 int static_scratch_address(void** ptr) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail("cudaGetDevice", e);
   if (dev < 0 || dev >= kMaxScratchDevices) return PKV_ERR_BAD_PARAMS;
+  auto get_ctx = current_context_getter();
+  if (!get_ctx) {
+    std::snprintf(g_cuda_error, sizeof(g_cuda_error), "cuCtxGetCurrent entry point unavailable");
+    return PKV_ERR_CUDA;
+  }
+  CUcontext ctx = nullptr;
+  if (get_ctx(&ctx) != CUDA_SUCCESS) ctx = nullptr;
   std::lock_guard<std::mutex> lock(g_scratch_mutex);
-  if (!g_scratch_address[dev]) {
+  // No context current on this thread yet (the runtime makes it current on first
+  // use), or another one than at the last look-up: look the address up again, which
+  // also makes the device's primary context current.
+  if (!ctx || !g_scratch_address[dev] || g_scratch_context[dev] != ctx) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_static_scratch);
     if (e != cudaSuccess) return cuda_fail("cudaGetSymbolAddress", e);
+    if (get_ctx(&ctx) != CUDA_SUCCESS) ctx = nullptr;
     g_scratch_address[dev] = p;
+    g_scratch_context[dev] = ctx;
   }
   *ptr = g_scratch_address[dev];
   return PKV_OK;
@@ -802,10 +861,14 @@ int pkv_paged_decode_attention_no_alloc(const pkv_pool_layout* layout, const pkv
     if (params->partition_tokens > 0) return PKV_ERR_SCRATCH_TOO_SMALL;  // the caller's partition size does not fit
     // A library-chosen plan coarsens its partitions until their states fit
     // (a single partition needs no scratch at all).
+    // Doubling stops at the table's length, where one partition needs no scratch, so
+    // the loop ends within 32 rounds; the bound on the rounds states it.
+    const long long max_len = static_cast<long long>(params->max_blocks_per_seq) * layout->block_size;
     long long part = plan.partition_tokens;
-    while (plan.workspace_bytes > PKV_STATIC_SCRATCH_BYTES) {
-      part *= 2;
-      local.partition_tokens = static_cast<int32_t>(part < (1ll << 30) ? part : (1ll << 30));
+    for (int round = 0; plan.workspace_bytes > PKV_STATIC_SCRATCH_BYTES; ++round) {
+      if (round >= 40 || part >= max_len) return PKV_ERR_SCRATCH_TOO_SMALL;
+      part = std::min(2 * part, max_len);
+      local.partition_tokens = static_cast<int32_t>(part);
       rc = plan_impl(layout, &local, sms, &plan);
       if (rc) return rc;
     }
@@ -837,6 +900,10 @@ const char* pkv_strerror(int code) {
 }
 
 const char* pkv_last_cuda_error(void) { return g_cuda_error; }
+
+uint64_t pkv_set_wait_limit_ns(uint64_t ns) {
+  return g_wait_limit_ns.exchange(ns == 0 ? pkv::kWaitLimitNs : ns, std::memory_order_relaxed);
+}
 
 int pkv_version(void) { return 200; }
 

@@ -15,7 +15,9 @@ constexpr int kDevErrBadBlock = 1;
 constexpr int kDevErrBadSeqLen = 2;
 constexpr int kDevErrTimeout = 4;
 
-// Upper bound of one pipeline wait before the kernel gives up (nanoseconds).
+// Default upper bound of one pipeline wait before the kernel gives up (nanoseconds).
+// The main loop of the partial kernel takes its bound from PartialParams (the host
+// may lower it); draining copies in flight after a give-up always uses this one.
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
 
 // Where appended rows are written: the pools and, for affine pages, the scale and
@@ -51,6 +53,7 @@ struct PartialParams {
   int window;         // sliding window in rows (0: none)
   int host_inputs;    // kHost* bits: inputs a host-driven step keeps in host memory
   float score_scale;  // softmax scale * log2(e)
+  unsigned long long wait_limit_ns;  // bound of one main-loop pipeline wait
   // Fused append (k_new != nullptr): the N new rows of every (sequence, KV head),
   // cache rows len-N .. len-1, are written into their pages by the CTA whose
   // partition holds them, before it reads that partition.
@@ -156,39 +159,44 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return done != 0;
 }
 
-// Waits for the phase with the given parity. Gives up when `abort_flag` is set
-// by another warp or after kWaitLimitNs, in which case it raises the abort
-// flag and the timeout error bit. Returns true when the phase completed.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
-                                                  volatile int* abort_flag, int32_t* error_flag) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long start = global_timer_ns();
-  while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (*abort_flag) return false;
-    if (global_timer_ns() - start > kWaitLimitNs) {
-      *abort_flag = 1;
-      if (error_flag) atomicOr(error_flag, kDevErrTimeout);
-      return false;
-    }
-  }
+// try_wait with an explicit bound on how long the thread may be suspended in it
+// (suspendTimeHint, nanoseconds), instead of the system's own.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return done != 0;
 }
 
-// Warp-collective form of mbar_wait_bounded: every lane observes the phase, and
-// the give-up decision is taken by lane 0 and shared, so the warp never splits.
+// Bounds below this one (nanoseconds) also bound each suspension inside try_wait, which
+// may otherwise outlast them.
+constexpr unsigned long long kShortWaitLimitNs = 1000000ull;
+
+// Waits, as a whole warp, for the phase of the mbarrier with the given parity. Gives
+// up when `abort_flag` is set by another warp or after `limit_ns`, in which case it
+// raises the abort flag and the timeout error bit; returns true when the phase
+// completed. Every lane observes the phase, and the give-up decision is taken by lane
+// 0 and shared, so the warp never splits.
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                               int32_t* error_flag) {
-  bool done = mbar_try_wait(bar, parity);
+                                               int32_t* error_flag, unsigned long long limit_ns) {
+  const bool short_limit = limit_ns < kShortWaitLimitNs;  // warp-uniform (a kernel parameter)
+  const uint32_t hint = static_cast<uint32_t>(short_limit ? limit_ns : 0ull);
+  bool done = short_limit ? mbar_try_wait_hint(bar, parity, hint) : mbar_try_wait(bar, parity);
   if (__all_sync(0xffffffffu, done)) return true;
   const bool leader = (threadIdx.x & 31) == 0;
   const unsigned long long start = leader ? global_timer_ns() : 0ull;
   while (true) {
-    if (!done) done = mbar_try_wait(bar, parity);
+    if (!done) done = short_limit ? mbar_try_wait_hint(bar, parity, hint) : mbar_try_wait(bar, parity);
     int stop = 0;
     if (leader) {
       if (*abort_flag) {
         stop = 1;
-      } else if (global_timer_ns() - start > kWaitLimitNs) {
+      } else if (global_timer_ns() - start > limit_ns) {
         *abort_flag = 1;
         if (error_flag) atomicOr(error_flag, kDevErrTimeout);
         stop = 1;

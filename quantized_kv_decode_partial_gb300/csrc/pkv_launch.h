@@ -26,6 +26,8 @@ struct PartialInfo {
 PartialInfo partial_info_bf16(int dk, int dv, int nq, bool solo);
 PartialInfo partial_info_u4(int dk, int dv, int nq, bool solo);
 PartialInfo partial_info_u8(int dk, int dv, int nq, bool solo);
+// bf16 pages with the CUDA-core contraction (up to 4 query rows per KV head, equal head dims)
+PartialInfo partial_info_bf16_cc(int dk, int dv, int nq, bool solo);
 
 cudaError_t launch_partial_bf16(int dk, int dv, int nq, bool solo, const PartialParams& p, const CUtensorMap& tk,
                                 const CUtensorMap& tv, dim3 grid, cudaStream_t stream, int device);
@@ -33,6 +35,8 @@ cudaError_t launch_partial_u4(int dk, int dv, int nq, bool solo, const PartialPa
                               const CUtensorMap& tv, dim3 grid, cudaStream_t stream, int device);
 cudaError_t launch_partial_u8(int dk, int dv, int nq, bool solo, const PartialParams& p, const CUtensorMap& tk,
                               const CUtensorMap& tv, dim3 grid, cudaStream_t stream, int device);
+cudaError_t launch_partial_bf16_cc(int dk, int dv, int nq, bool solo, const PartialParams& p, const CUtensorMap& tk,
+                                   const CUtensorMap& tv, dim3 grid, cudaStream_t stream, int device);
 
 cudaError_t launch_merge(const MergeParams& p, int rows, cudaStream_t stream);
 cudaError_t launch_gather(const GatherParams& p, int num_seqs, cudaStream_t stream);

@@ -51,6 +51,7 @@
 
 #include "pkv_append.cuh"
 #include "pkv_common.cuh"
+#include "pkv_partial_cc.cuh"
 
 namespace pkv {
 
@@ -60,8 +61,10 @@ namespace pkv {
 // as many stages per warp (up to 4) as fit, up to 255 registers per thread, and a
 // receive area for the push-form cluster merge.
 // D is the key (and query) head dim, DV the value head dim. Names without a V
-// describe the K plane, names with one the V plane.
-template <int BITS, int D, int DV, int NT, int WQ, bool SOLO>
+// describe the K plane, names with one the V plane. CCQ = 0 takes the tensor-core
+// contraction; CCQ = 2 or 4 the CUDA-core one (pkv_partial_cc.cuh) for bf16 pages
+// with up to that many query rows per KV head (NT = WQ = 1).
+template <int BITS, int D, int DV, int NT, int WQ, bool SOLO, int CCQ = 0>
 struct PartialCfg {
   static constexpr bool kQuant = BITS != 16;
   static constexpr int kElemBytes = kQuant ? 1 : 2;                    // tensor-map element size
@@ -99,11 +102,15 @@ struct PartialCfg {
   // write into (their (m, l) of every row, and their o runs of this CTA's share of the
   // outputs) while this CTA may still be streaming.
   static constexpr int kRecvNeedBytes = (2 * kMaxClusterParts * kNqAll + kNqAll * DV + 4 * kMaxClusterParts) * 4;
+  // CUDA-core contraction: each warp's weights of one chunk (16 rows x 4 query rows of f32)
+  static constexpr int kPBufBytes = CCQ ? 8 * 256 : 0;
   // stage ring of a CTA alone on its SM, which always has a receive area
-  static constexpr int kSoloBudget = 227 * 1024 - kBarrierBytes - 1024 - (SOLO ? kRecvNeedBytes : 0);
+  static constexpr int kSoloBudget = 227 * 1024 - kBarrierBytes - 1024 - (SOLO ? kRecvNeedBytes : 0) - kPBufBytes;
   // every warp computes: 8 when two stages per warp fit a CTA alone on its SM, else 6 (two
-  // of the four schedulers then hold two warps), else 4
-  static constexpr int kWarps = !SOLO                                ? 4
+  // of the four schedulers then hold two warps), else 4; a query group of 8 warps (up to
+  // 64 query rows of 256-dim heads) is the whole CTA
+  static constexpr int kWarps = WQ == 8                              ? 8
+                                : !SOLO                              ? 4
                                 : 8 * 2 * kStageBytes <= kSoloBudget ? 8
                                 : 6 * 2 * kStageBytes <= kSoloBudget ? 6
                                                                      : 4;
@@ -112,7 +119,10 @@ struct PartialCfg {
   // its WQ warps read each of its chunks, each for its own 8*NT query rows.
   static constexpr int kWP = kWarps / WQ;
   static constexpr int kSoloStages = kSoloBudget / (kWarps * kStageBytes);
-  static constexpr int kStagesPerWarp = SOLO ? (kSoloStages < 4 ? kSoloStages : 4) : (kStageBytes <= 9 * 1024 ? 3 : 2);
+  // (a query group of 8 warps shares one ring of 8 or 16 stages, within 144 KB)
+  static constexpr int kStagesPerWarp = WQ == 8 ? (8 * 2 * kStageBytes <= 144 * 1024 ? 2 : 1)
+                                        : SOLO  ? (kSoloStages < 4 ? kSoloStages : 4)
+                                                : (kStageBytes <= 9 * 1024 ? 3 : 2);
   static constexpr int kStagesPerGroup = kStagesPerWarp * WQ;  // each page group's private ring
   static constexpr int kMt = DV / 16;       // 16-dim m-tiles of O^T
   static constexpr int kKs = D / 16;        // k16 steps of Q K^T
@@ -137,7 +147,7 @@ struct PartialCfg {
                                 (kBaseSmem > 114 * 1024 && kBaseSmem + kRecvNeedBytes <= 227 * 1024);
   static constexpr int kRecvBytes = kPush ? kRecvNeedBytes : 0;
   static constexpr int kDataBytes = kWorkBytes + kRecvBytes;
-  static constexpr int kSmemBytes = kDataBytes + kBarrierBytes + 1024;  // + alignment slack
+  static constexpr int kSmemBytes = kDataBytes + kBarrierBytes + kPBufBytes + 1024;  // + alignment slack
   static constexpr float kCodeUnit = 5.9604644775390625e-8f;  // 2^-24: value of fp16 bit pattern 1
 
   static_assert((kRB == 128 || kRB == 64) && (kRBV == 128 || kRBV == 64), "box rows of 64 or 128 bytes");
@@ -145,9 +155,13 @@ struct PartialCfg {
   static_assert(kWarps * kStagesPerWarp * 12 + 4 <= kBarrierBytes, "barrier area");
   static_assert(!kQuant || (D % 64 == 0 && DV % 64 == 0), "affine head dims are whole 64-dim groups");
   static_assert(DV % 64 == 0, "value head dims are whole 4-m-tile groups");
-  static_assert(WQ == 1 || WQ == 2 || WQ == 4, "query groups of 1, 2 or 4 warps");
-  static_assert(kStagesPerWarp >= 2, "at least two stages per warp");
+  static_assert(WQ == 1 || WQ == 2 || WQ == 4 || WQ == 8, "query groups of 1, 2, 4 or 8 warps");
+  static_assert(kStagesPerWarp >= 2 || WQ == 8, "at least two stages per warp (a ring of 8 for 8-warp groups)");
+  static_assert(!(WQ == 8 && SOLO), "a query group of 8 warps is its CTA already");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory of one CTA");
+  static_assert(CCQ == 0 || (BITS == 16 && D == DV && NT == 1 && WQ == 1 && kCh == 16 && kRB == 128),
+                "CUDA-core contraction: bf16 pages, equal head dims, 128-byte rows, one warp per query group");
+  static_assert(!CCQ || kWarps <= 8, "weight buffers of at most 8 warps");
 };
 
 // Physical head dim held by row `half` (0: g, 1: g + 8) of O^T m-tile `mt`.
@@ -285,11 +299,11 @@ __device__ __forceinline__ void load_group_row(uint32_t addr, float (&v)[G]) {
 // HOSTIN: a host-driven step whose length, query and block tables all live in host
 // memory the host wrote before the launch (no kernel writes them): they are read before
 // the wait for the previous kernel on the stream, so their NVLink-C2C latency overlaps it.
-template <int BITS, int D, int DV, int NT, int WQ, bool SOLO, bool HOSTIN>
+template <int BITS, int D, int DV, int NT, int WQ, bool SOLO, bool HOSTIN, int CCQ = 0>
 __global__ void __maxnreg__(255)
     pkv_partial_kernel(const __grid_constant__ PartialParams p, const __grid_constant__ CUtensorMap tmap_k,
                        const __grid_constant__ CUtensorMap tmap_v) {
-  using C = PartialCfg<BITS, D, DV, NT, WQ, SOLO>;
+  using C = PartialCfg<BITS, D, DV, NT, WQ, SOLO, CCQ>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + C::kDataBytes);  // [warp][stage]
@@ -319,11 +333,19 @@ __global__ void __maxnreg__(255)
   // This lane's query values, fetched now so their latency overlaps the length's:
   // 2 * kKs words of bf16 pairs per n-tile, in the order q_load_words reads them.
   uint32_t qw[NT][2 * C::kKs];
+  uint4 qcw[CCQ ? CCQ : 1];  // CUDA-core contraction: this lane's 8 dims of each query row
+  if constexpr (CCQ) {
+    const int d0 = (lane % (D / 8)) * 8;
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    const int r = rbase + 8 * nt + g;
-    const __nv_bfloat16* qrow = p.q + (row0 + (r < p.nq ? r : 0)) * D;
-    q_load_words<BITS, D>(qrow, t, r < p.nq, qw[nt]);
+    for (int qi = 0; qi < CCQ; ++qi)
+      qcw[qi] = qi < p.nq ? ld_nc_keep_v4(p.q + (row0 + qi) * D + d0) : make_uint4(0u, 0u, 0u, 0u);
+  } else {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int r = rbase + 8 * nt + g;
+      const __nv_bfloat16* qrow = p.q + (row0 + (r < p.nq ? r : 0)) * D;
+      q_load_words<BITS, D>(qrow, t, r < p.nq, qw[nt]);
+    }
   }
   // Without a window the partition (and so this warp's first 32 chunks) does not
   // depend on len: fetch their block-table entries while len is still in flight.
@@ -385,6 +407,11 @@ __global__ void __maxnreg__(255)
   float o[C::kMt][NT][4];
   float m_run[NT][2], l_run[NT][2];
   float corr_v[C::kQuant ? C::kGroupsV : 1][NT][2];
+  // CUDA-core contraction: per query row, this lane's 8 dims of o, the running maximum
+  // and this lane's share of the normaliser.
+  constexpr int kCcq = CCQ ? CCQ : 1;
+  float2 cco[kCcq][4];
+  float ccm[kCcq], ccl[kCcq];
 
   {
     // ------------------------------------------------------------------ this warp's pipeline
@@ -496,7 +523,20 @@ __global__ void __maxnreg__(255)
     float colscale[NT][2];  // factor from accumulator to base-2 score, per query column 2t, 2t+1
     // affine: B fragment (k 0-7) of the K-bias MMA, per n-tile (k 8-15 are zero)
     uint32_t qsb[C::kQuant ? NT : 1];
-    {
+    float2 ccq[kCcq][4];  // CUDA-core contraction: q as f32 pairs
+    if constexpr (CCQ) {
+#pragma unroll
+      for (int qi = 0; qi < CCQ; ++qi) {
+        ccq[qi][0] = bf16x2_pair(qcw[qi].x);
+        ccq[qi][1] = bf16x2_pair(qcw[qi].y);
+        ccq[qi][2] = bf16x2_pair(qcw[qi].z);
+        ccq[qi][3] = bf16x2_pair(qcw[qi].w);
+        ccm[qi] = -INFINITY;
+        ccl[qi] = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) cco[qi][i] = make_float2(0.f, 0.f);
+      }
+    } else {
       float qsum[C::kQuant ? C::kGroups : 1][NT][2];  // affine: 2^-24 * sum of prescaled q over each group
       float qv[C::kKs][NT][4];
 #pragma unroll
@@ -616,7 +656,7 @@ __global__ void __maxnreg__(255)
     for (; done < my_chunks; ++done) {
       const int cs = done % C::kStagesPerGroup;  // its stage
       const bool landed = mbar_wait_warp(smem_addr(&my_full[cs]), (done / C::kStagesPerGroup) & 1, abort_flag,
-                                         p.error_flag);
+                                         p.error_flag, p.wait_limit_ns);
       if (landed && my_ok[cs]) {
         uint8_t* stage = my_ring + cs * C::kStageBytes;
         const uint32_t kpl = smem_addr(stage);
@@ -625,7 +665,11 @@ __global__ void __maxnreg__(255)
         const int kbase = chunk_row(done);
         const bool full_vis = kbase + C::kCh <= vis_base && (win == 0 || kbase >= vis_base + N - 1 - win);
         const bool stale = kbase + C::kCh > len;
-
+        if constexpr (CCQ) {
+          float* pbuf = reinterpret_cast<float*>(smem + C::kDataBytes + C::kBarrierBytes) + warp * 64;
+          cc_chunk<D, CCQ>(kpl, vpl, pbuf, ccq, cco, ccm, ccl, lane, kbase, len, vis_base, win, N, full_vis, stale,
+                           p.score_scale);
+        } else {
         // ---- scores x = (K q) * scale * log2(e), keys on rows
         float x[C::kTiles][NT][4];
 #pragma unroll
@@ -755,30 +799,61 @@ __global__ void __maxnreg__(255)
         float pr[C::kTiles][NT][4];
         float corr[NT][2];
         bool grew = false;
+        // This lane's maxima of the chunk. When no lane's exceeds the running maximum, the
+        // chunk's maximum does not either: the running maximum stays and nothing is
+        // rescaled, which is what the general path below computes too, without its
+        // cross-lane reduction (so the results are the same bit for bit).
+        float lmx[NT][2];
+        bool below = true;
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
+        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
           for (int e2 = 0; e2 < 2; ++e2) {
             float mx = -INFINITY;
 #pragma unroll
             for (int tile = 0; tile < C::kTiles; ++tile) mx = fmaxf(mx, fmaxf(x[tile][nt][e2], x[tile][nt][e2 + 2]));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-            const float mnew = fmaxf(m_run[nt][e2], mx);
-            const float muse = mnew == -INFINITY ? 0.f : mnew;
-            const float c = fast_exp2(m_run[nt][e2] - muse);
-            m_run[nt][e2] = mnew;
-            float ls = 0.f;
+            lmx[nt][e2] = mx;
+            below &= mx <= m_run[nt][e2];
+          }
+        if (__all_sync(0xffffffffu, below)) {
 #pragma unroll
-            for (int tile = 0; tile < C::kTiles; ++tile) {
-              pr[tile][nt][e2] = fast_exp2(x[tile][nt][e2] - muse);
-              pr[tile][nt][e2 + 2] = fast_exp2(x[tile][nt][e2 + 2] - muse);
-              ls += pr[tile][nt][e2] + pr[tile][nt][e2 + 2];
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e2 = 0; e2 < 2; ++e2) {
+              const float muse = m_run[nt][e2] == -INFINITY ? 0.f : m_run[nt][e2];
+              float ls = 0.f;
+#pragma unroll
+              for (int tile = 0; tile < C::kTiles; ++tile) {
+                pr[tile][nt][e2] = fast_exp2(x[tile][nt][e2] - muse);
+                pr[tile][nt][e2 + 2] = fast_exp2(x[tile][nt][e2 + 2] - muse);
+                ls += pr[tile][nt][e2] + pr[tile][nt][e2 + 2];
+              }
+              l_run[nt][e2] += ls;
             }
-            l_run[nt][e2] = fmaf(l_run[nt][e2], c, ls);
-            corr[nt][e2] = c;
-            grew |= c != 1.f;
+        } else {
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+            for (int e2 = 0; e2 < 2; ++e2) {
+              float mx = lmx[nt][e2];
+              mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+              mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+              mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+              const float mnew = fmaxf(m_run[nt][e2], mx);
+              const float muse = mnew == -INFINITY ? 0.f : mnew;
+              const float c = fast_exp2(m_run[nt][e2] - muse);
+              m_run[nt][e2] = mnew;
+              float ls = 0.f;
+#pragma unroll
+              for (int tile = 0; tile < C::kTiles; ++tile) {
+                pr[tile][nt][e2] = fast_exp2(x[tile][nt][e2] - muse);
+                pr[tile][nt][e2 + 2] = fast_exp2(x[tile][nt][e2 + 2] - muse);
+                ls += pr[tile][nt][e2] + pr[tile][nt][e2 + 2];
+              }
+              l_run[nt][e2] = fmaf(l_run[nt][e2], c, ls);
+              corr[nt][e2] = c;
+              grew |= c != 1.f;
+            }
           }
         }
         if (__any_sync(0xffffffffu, grew)) {
@@ -890,6 +965,7 @@ __global__ void __maxnreg__(255)
             }
           }
         }
+        }  // tensor-core contraction
       }
       if constexpr (WQ == 1) {
         if (!landed) break;
@@ -911,6 +987,25 @@ __global__ void __maxnreg__(255)
       }
     }
 
+    if constexpr (CCQ) {
+      // ---- per-warp totals: the normaliser over all lanes, o over the lanes that hold
+      // the same dims of other rows
+      using S = CcShape<D, CCQ>;
+#pragma unroll
+      for (int qi = 0; qi < CCQ; ++qi) {
+        float l = ccl[qi];
+#pragma unroll
+        for (int delta = 1; delta < 32; delta <<= 1) l += __shfl_xor_sync(0xffffffffu, l, delta);
+        ccl[qi] = l;
+#pragma unroll
+        for (int delta = S::kLanesPerRow; delta < 32; delta <<= 1)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            cco[qi][i].x += __shfl_xor_sync(0xffffffffu, cco[qi][i].x, delta);
+            cco[qi][i].y += __shfl_xor_sync(0xffffffffu, cco[qi][i].y, delta);
+          }
+      }
+    } else {
     // ---- per-warp totals: normaliser and value corrections summed over the 8 key lanes
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
@@ -942,6 +1037,7 @@ __global__ void __maxnreg__(255)
           for (int e = 0; e < 4; ++e)
             o[mt][nt][e] = fmaf(o[mt][nt][e], (1.f / C::kCodeUnit) * v_tile_factor<BITS>(mt), corr_v[mt >> 2][nt][e & 1]);
     }
+    }  // tensor-core contraction
   }
 
   allow_dependent_launch();  // the merge pass may be scheduled while this epilogue runs
@@ -964,6 +1060,22 @@ __global__ void __maxnreg__(255)
     float* const cm = gstate(pg);
     float* const cl = cm + C::kNqAll;
     float* const co = cl + C::kNqAll;
+    if constexpr (CCQ) {
+      const int d0 = (lane % (D / 8)) * 8;
+#pragma unroll
+      for (int qi = 0; qi < CCQ; ++qi) {
+        if (qi >= p.nq) continue;
+        if (lane == 0) {
+          cm[qi] = ccm[qi];
+          cl[qi] = ccl[qi];
+        }
+        if (lane < D / 8) {
+          float* dst = co + qi * C::kCoStride + d0;
+          *reinterpret_cast<float4*>(dst) = make_float4(cco[qi][0].x, cco[qi][0].y, cco[qi][1].x, cco[qi][1].y);
+          *reinterpret_cast<float4*>(dst + 4) = make_float4(cco[qi][2].x, cco[qi][2].y, cco[qi][3].x, cco[qi][3].y);
+        }
+      }
+    } else {
     if (g == 0) {
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
@@ -995,6 +1107,7 @@ __global__ void __maxnreg__(255)
             *dst = o[mt][nt][e];
           }
         }
+    }  // tensor-core contraction
   }
   __syncthreads();
 

@@ -1,5 +1,5 @@
-// Affine 4-bit pages: head dims 128 / 256 with up to 64 / 32 query rows per KV head, and
-// key/value head dims 256/128 and 128/256.
+// Affine 4-bit pages: head dims 128 / 256 and key/value head dims 256/128 and 128/256,
+// each with up to 64 query rows per KV head.
 // The SOLO instances serve grids of at most one CTA per SM (see PartialCfg).
 #include "pkv_partial_instances.cuh"
 
@@ -7,8 +7,9 @@ namespace pkv {
 
 #define PKV_U4_INSTANCES(X) \
   X(128, 128, 1, 1, false) X(128, 128, 2, 1, false) X(128, 128, 2, 2, false) X(128, 128, 2, 4, false) \
-  X(256, 256, 1, 1, false) X(256, 256, 1, 2, false) X(256, 256, 1, 4, false) \
-  X(256, 128, 1, 1, false) X(128, 256, 1, 1, false) \
+  X(256, 256, 1, 1, false) X(256, 256, 1, 2, false) X(256, 256, 1, 4, false) X(256, 256, 1, 8, false) \
+  X(256, 128, 1, 1, false) X(256, 128, 1, 2, false) X(256, 128, 1, 4, false) X(256, 128, 1, 8, false) \
+  X(128, 256, 1, 1, false) X(128, 256, 1, 2, false) X(128, 256, 1, 4, false) X(128, 256, 1, 8, false) \
   X(128, 128, 1, 1, true) X(256, 256, 1, 1, true)
 
 PartialInfo partial_info_u4(int dk, int dv, int nq, bool solo) {

@@ -121,8 +121,8 @@ def test_single_sequence_plans_merge_in_a_cluster(lib):
     assert B.make_plan(_layout(sp), _params(sp, 256), sm_count=16).merge_in_cluster == 0
 
 
-@pytest.mark.parametrize("bits,head_dim,max_rows", [(16, 64, 64), (16, 128, 64), (16, 256, 32), (4, 128, 64),
-                                                     (4, 256, 32), (8, 128, 64), (8, 256, 32)])
+@pytest.mark.parametrize("bits,head_dim,max_rows", [(16, 64, 64), (16, 128, 64), (16, 256, 64), (4, 128, 64),
+                                                     (4, 256, 64), (8, 128, 64), (8, 256, 64)])
 def test_query_rows_per_kv_head_limits(lib, bits, head_dim, max_rows):
     for nq in (1, 8, 9, 16, 17, 32, 33, 64, 65):
         lay = B.PoolLayout(100, 1, 32, head_dim, bits, 64)
@@ -132,16 +132,18 @@ def test_query_rows_per_kv_head_limits(lib, bits, head_dim, max_rows):
         assert rc == (B.PKV_OK if nq <= max_rows else B.PKV_ERR_UNSUPPORTED_SHAPE), (nq, rc)
 
 
-@pytest.mark.parametrize("bits,dk,dv,max_rows", [(16, 192, 128, 32), (16, 256, 128, 8), (16, 128, 256, 8),
-                                                  (4, 256, 128, 8), (4, 128, 256, 8), (8, 256, 128, 8),
-                                                  (8, 128, 256, 8)])
+@pytest.mark.parametrize("bits,dk,dv,max_rows", [(16, 192, 128, 64), (16, 256, 128, 64), (16, 128, 256, 64),
+                                                  (4, 256, 128, 64), (4, 128, 256, 64), (8, 256, 128, 64),
+                                                  (8, 128, 256, 64)])
 def test_key_and_value_head_dims_may_differ(lib, bits, dk, dv, max_rows):
-    for nq in (1, 8, 9, 32, 33):
+    for nq in (1, 8, 9, 32, 33, 64, 65):
         lay = B.PoolLayout(100, 2, 32, dk, bits, 64, dv)
         par = B.DecodeParams(1, 2 * nq, 1, 4, 64, 0)
         plan = B.Plan()
         rc = lib.pkv_make_plan(ctypes.byref(lay), ctypes.byref(par), 1, ctypes.byref(plan))  # 1 SM: no cluster
         assert rc == (B.PKV_OK if nq <= max_rows else B.PKV_ERR_UNSUPPORTED_SHAPE), (nq, rc)
+        if rc == B.PKV_OK:  # 33..64 rows: one query group of 8 warps (256 threads)
+            assert plan.threads_per_cta == (256 if nq > 32 else 128)
         if rc == B.PKV_OK:  # partition states hold value-dim rows: 2 partitions x 2 nq query heads
             slots = 2 * 2 * nq
             assert plan.max_partitions == 2 and plan.merge_in_cluster == 0
@@ -182,11 +184,11 @@ def test_plan_rejects_bad_layouts(lib, field, value, code):
 @pytest.mark.parametrize("field,value,code", [
     ("num_q_heads", 6, B.PKV_ERR_BAD_PARAMS), ("n_query", 0, B.PKV_ERR_BAD_PARAMS),
     ("num_seqs", 0, B.PKV_ERR_BAD_PARAMS), ("max_blocks_per_seq", 0, B.PKV_ERR_BAD_PARAMS),
-    ("partition_tokens", -1, B.PKV_ERR_BAD_PARAMS), ("n_query", 9, B.PKV_ERR_UNSUPPORTED_SHAPE),
+    ("partition_tokens", -1, B.PKV_ERR_BAD_PARAMS), ("n_query", 17, B.PKV_ERR_UNSUPPORTED_SHAPE),
     ("window", -1, B.PKV_ERR_BAD_PARAMS),
 ])
 def test_plan_rejects_bad_params(lib, field, value, code):
-    sp = WORKLOADS["affine4_g64_1x8192_hq16_d256"]  # HQ 16 / HK 4: REP 4, so n_query 9 asks for 36 > 32 rows at D 256
+    sp = WORKLOADS["affine4_g64_1x8192_hq16_d256"]  # HQ 16 / HK 4: REP 4, so n_query 17 asks for 68 > 64 rows
     par = _params(sp, 256)
     setattr(par, field, value)
     plan = B.Plan()
@@ -258,3 +260,51 @@ def test_gather_validates(lib):
 def test_missing_library_raises(tmp_path):
     with pytest.raises(B.LibraryNotBuilt):
         B.load_library(str(tmp_path / "nope.so"))
+
+
+@pytest.mark.parametrize("bits,block_size", [(16, 16), (4, 32)])
+def test_partition_tokens_past_the_table_give_one_partition(lib, bits, block_size):
+    # A caller's partition size of INT_MAX (or anything past the table) means one
+    # partition, never a size that wraps around int32.
+    lay = B.PoolLayout(1000, 2, block_size, 128, bits, 64)
+    for max_blocks in (4, 1 << 20):
+        max_len = max_blocks * block_size
+        for pt in (max_len, max_len + 1, 2**31 - 1, 2**31 - block_size + 1):
+            plan = B.Plan()
+            rc = lib.pkv_make_plan(ctypes.byref(lay), ctypes.byref(B.DecodeParams(3, 8, 1, max_blocks, pt, 0)), 152,
+                                   ctypes.byref(plan))
+            assert rc == B.PKV_OK
+            assert plan.max_partitions == 1 and plan.partition_tokens == max_len and plan.workspace_bytes == 0
+
+
+def test_wait_limit_setter_round_trip(lib):
+    # 0 restores the default bound of one second; the previous bound comes back.
+    first = lib.pkv_set_wait_limit_ns(0)
+    assert lib.pkv_set_wait_limit_ns(123) == 10**9
+    assert lib.pkv_set_wait_limit_ns(0) == 123
+    assert lib.pkv_set_wait_limit_ns(first) == 10**9
+    assert lib.pkv_set_wait_limit_ns(0) == first
+
+
+@pytest.mark.parametrize("bits,dk,dv,nq,ok", [(16, 128, 128, 4, True), (16, 256, 256, 2, True), (16, 64, 64, 1, True),
+                                             (16, 128, 128, 5, False), (16, 192, 128, 2, False),
+                                             (4, 256, 256, 4, False), (8, 128, 128, 2, False)])
+def test_cuda_core_contraction_shapes(lib, bits, dk, dv, nq, ok):
+    lay = B.PoolLayout(100, 1, 32, dk, bits, 64, 0 if dv == dk else dv)
+    plan = B.Plan()
+    par = B.DecodeParams(1, nq, 1, 4, 64, 0, B.PKV_CONTRACTION_CUDA_CORE)
+    rc = lib.pkv_make_plan(ctypes.byref(lay), ctypes.byref(par), 152, ctypes.byref(plan))
+    assert rc == (B.PKV_OK if ok else B.PKV_ERR_UNSUPPORTED_SHAPE)
+    if ok:
+        assert plan.contraction == B.PKV_CONTRACTION_CUDA_CORE
+    tc = B.DecodeParams(1, nq, 1, 4, 64, 0, B.PKV_CONTRACTION_TENSOR)
+    if lib.pkv_make_plan(ctypes.byref(lay), ctypes.byref(tc), 152, ctypes.byref(plan)) == B.PKV_OK:
+        assert plan.contraction == B.PKV_CONTRACTION_TENSOR
+
+
+def test_contraction_field_is_validated(lib):
+    lay = B.PoolLayout(100, 1, 32, 128, 16, 64)
+    plan = B.Plan()
+    for bad in (-1, 3):
+        par = B.DecodeParams(1, 2, 1, 4, 64, 0, bad)
+        assert lib.pkv_make_plan(ctypes.byref(lay), ctypes.byref(par), 152, ctypes.byref(plan)) == B.PKV_ERR_BAD_PARAMS

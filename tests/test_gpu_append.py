@@ -136,6 +136,9 @@ FUSED = [
     (16, 128, 4, 8, 2, 32, 40, 0),
     (16, 192, 2, 8, 2, 32, 0, 128),
     (4, 256, 1, 8, 2, 64, 0, 128),
+    # one query group of 8 warps (33..64 query rows at 256-dim heads)
+    (16, 256, 2, 64, 2, 64, 0, 0),
+    (4, 256, 4, 24, 2, 64, 0, 128),
 ]
 
 

@@ -77,6 +77,31 @@ SMALL = [
     (spec("u8_dk256_dv128", head_dim=256, v_head_dim=128, bits=8, block_size=32, length_range=(1, 500)), [-1, 32]),
     (spec("u8_dk128_dv256_n2", num_q_heads=4, head_dim=128, v_head_dim=256, bits=8, n_query=2, block_size=32,
           length_range=(2, 500)), [-1, 64]),
+    # 33..64 query rows per KV head at 256-dim heads: one query group of 8 warps
+    (spec("bf16_d256_nq64_n2", num_q_heads=32, num_kv_heads=1, head_dim=256, n_query=2, length_range=(2, 300)),
+     [-1, 48, 0]),
+    (spec("bf16_d256_nq40", num_q_heads=40, num_kv_heads=1, head_dim=256, length_range=(1, 300)), [-1, 64]),
+    (spec("u4_d256_nq64", num_q_heads=64, num_kv_heads=1, head_dim=256, bits=4, block_size=32,
+          length_range=(1, 400)), [-1, 64, 0]),
+    (spec("u8_d256_nq48_n4", num_q_heads=12, num_kv_heads=1, head_dim=256, bits=8, n_query=4, block_size=32,
+          length_range=(4, 400)), [-1, 32]),
+    # key/value head dims that differ, with more than 8 query rows per KV head
+    (spec("bf16_dk256_dv128_nq16", num_q_heads=16, num_kv_heads=1, head_dim=256, v_head_dim=128,
+          length_range=(1, 400)), [-1, 64]),
+    (spec("bf16_dk128_dv256_nq32_n2", num_q_heads=16, num_kv_heads=1, head_dim=128, v_head_dim=256, n_query=2,
+          length_range=(2, 400)), [-1, 48]),
+    (spec("bf16_dk192_dv128_nq64", num_q_heads=64, num_kv_heads=1, head_dim=192, v_head_dim=128,
+          length_range=(1, 300)), [-1, 32]),
+    (spec("bf16_dk256_dv128_nq64_n4", num_q_heads=16, num_kv_heads=1, head_dim=256, v_head_dim=128, n_query=4,
+          length_range=(4, 300)), [-1, 64]),
+    (spec("u4_dk256_dv128_nq32", num_q_heads=32, num_kv_heads=1, head_dim=256, v_head_dim=128, bits=4,
+          block_size=32, length_range=(1, 500)), [-1, 64]),
+    (spec("u4_dk128_dv256_nq64", num_q_heads=64, num_kv_heads=1, head_dim=128, v_head_dim=256, bits=4,
+          block_size=32, length_range=(1, 400)), [-1, 96]),
+    (spec("u8_dk256_dv128_nq24_n3", num_q_heads=8, num_kv_heads=1, head_dim=256, v_head_dim=128, bits=8, n_query=3,
+          block_size=32, length_range=(3, 500)), [-1, 32]),
+    (spec("u8_dk128_dv256_nq64", num_q_heads=64, num_kv_heads=1, head_dim=128, v_head_dim=256, bits=8,
+          block_size=32, length_range=(1, 400)), [-1, 64]),
 ]
 
 
@@ -98,7 +123,7 @@ def test_small_cases_match_oracle(sp, parts):
 # which takes the eight-warp variant; these grids of more than one CTA per SM take the
 # four-warp one for the same shapes.
 BIG_GRID = [(16, 64, 0), (16, 128, 0), (16, 256, 0), (4, 128, 0), (4, 256, 0), (8, 128, 0), (8, 256, 0),
-            (16, 192, 128)]
+            (16, 192, 128), (16, 256, 128), (4, 128, 256)]
 
 
 @pytest.mark.parametrize("bits,D,DV", BIG_GRID, ids=[f"b{b}_d{d}_{v}" for b, d, v in BIG_GRID])
@@ -119,13 +144,14 @@ def test_grids_of_several_ctas_per_sm_match_oracle(bits, D, DV):
         assert_close(out.double().cpu().numpy(), ref, f"{sp.name} partition={pt}")
 
 
-@pytest.mark.parametrize("bits,parts,head_dim", [(16, 16, 128), (4, 16, 256), (8, 2, 128), (16, 9, 128),
-                                                  (16, 12, 256), (16, 5, 64)])
-def test_cluster_merge_matches_oracle(bits, parts, head_dim):
+@pytest.mark.parametrize("bits,parts,head_dim,rep", [(16, 16, 128, 4), (4, 16, 256, 4), (8, 2, 128, 4),
+                                                      (16, 9, 128, 4), (16, 12, 256, 4), (16, 5, 64, 4),
+                                                      (16, 8, 256, 64), (4, 6, 256, 48)])
+def test_cluster_merge_matches_oracle(bits, parts, head_dim, rep):
     # one sequence: the partitions of each KV head merge inside a thread-block cluster (CTAs alone on
-    # their SMs: 8 warps, or 6 for bf16 D=256)
-    sp = spec(f"cluster_{bits}_{parts}_{head_dim}", num_seqs=1, head_dim=head_dim, bits=bits, block_size=32,
-              lengths=(parts * 64 - 5,), length_range=None)
+    # their SMs: 8 warps, or 6 for bf16 D=256; 8 warps in one query group for 33..64 rows)
+    sp = spec(f"cluster_{bits}_{parts}_{head_dim}_{rep}", num_seqs=1, head_dim=head_dim, bits=bits, block_size=32,
+              lengths=(parts * 64 - 5,), length_range=None, num_q_heads=2 * rep)
     case = make_case(sp)
     plan = B.make_plan(B.layout_for(case.k_pool, sp.head_dim, bits),
                        B.DecodeParams(1, sp.num_q_heads, 1, case.block_tables.shape[1], 64))
@@ -192,7 +218,9 @@ def test_full_size_workloads_sampled(name):
         sub = subcase(case, b, kv)
         ref = oracle_out(sub)
         got = out[b:b + 1, kv * sp.rep:(kv + 1) * sp.rep].double().cpu().numpy()
-        assert_close(got, ref, f"{name} b={b} kv={kv}")
+        # bf16 and 4-bit outputs stay below 2 in magnitude here, where the plain bound
+        # needs no allowance for the output's own rounding; 8-bit outputs reach 40
+        assert_close(got, ref, f"{name} b={b} kv={kv}", strict=sp.bits != 8)
 
 
 # ---------------------------------------------------------------------------

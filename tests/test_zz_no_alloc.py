@@ -16,7 +16,7 @@ import torch
 
 from helpers import assert_close, run_gpu
 from quantized_kv_decode_partial_gb300 import binding as B
-from quantized_kv_decode_partial_gb300.workloads import DecodeSpec, make_case
+from quantized_kv_decode_partial_gb300.workloads import DecodeCase, DecodeSpec, make_case
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
@@ -79,3 +79,36 @@ def test_no_alloc_coarsens_library_partitions_and_rejects_oversized_ones():
         assert no_alloc_call(lib, case, 0, out) == B.PKV_OK
         torch.cuda.synchronize()
         assert_close(out.double().cpu().numpy(), ref, "na_big auto")
+
+
+def test_no_alloc_coarsening_stops_at_one_partition_for_tables_past_2_pow_30():
+    # Tables longer than 2^30 rows (16385 blocks of 65536 rows) with 64 query rows for each of
+    # 256 sequences: the library's plan needs two partitions even at 2^30 rows each, whose
+    # states (17 MB) still exceed the 16 MiB scratch. Coarsening must go on to a single
+    # partition (no scratch at all) and return, not loop. Every sequence reads the first
+    # rows of block 0; table entries past the lengths are never used.
+    lib = B.load_library()
+    seqs, rep, d, bs, max_blocks = 256, 64, 128, 65536, 16385
+    g = torch.Generator().manual_seed(7)
+    lens = torch.randint(50, 300, (seqs,), generator=g, dtype=torch.int32)
+    k_pool = torch.randn((1, 1, bs, d), generator=g).to(torch.bfloat16)
+    v_pool = torch.randn((1, 1, bs, d), generator=g).to(torch.bfloat16)
+    q = torch.randn((seqs, rep, 1, d), generator=g).to(torch.bfloat16)
+    tables = torch.zeros((seqs, max_blocks), dtype=torch.int32)
+    sp = DecodeSpec(name="na_2p30", num_seqs=seqs, num_q_heads=rep, num_kv_heads=1, head_dim=d, n_query=1,
+                    block_size=bs, bits=16, lengths=tuple(int(x) for x in lens))
+    case = DecodeCase(spec=sp, q=q, k_pool=k_pool, v_pool=v_pool, block_tables=tables, seq_lens=lens,
+                      scale=d ** -0.5, num_blocks=1, lens_host=[int(x) for x in lens]).to(DEV)
+    layout = B.layout_for(case.k_pool, d, 16)
+    auto = B.make_plan(layout, B.DecodeParams(seqs, rep, 1, max_blocks, 0))
+    assert auto.workspace_bytes > B.PKV_STATIC_SCRATCH_BYTES
+    two = B.make_plan(layout, B.DecodeParams(seqs, rep, 1, max_blocks, 1 << 30))
+    assert two.max_partitions == 2 and two.workspace_bytes > B.PKV_STATIC_SCRATCH_BYTES
+    ref = run_gpu(case, partition_tokens=max_blocks * bs)  # one partition
+    for _ in range(2):
+        out = torch.full_like(case.q, float("nan"))
+        err = torch.zeros(1, dtype=torch.int32, device=DEV)
+        assert no_alloc_call(lib, case, 0, out, err) == B.PKV_OK
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
