@@ -442,6 +442,30 @@ __global__ void __maxnreg__(255)
     }
     int issued = 0;  // chunks issued so far
 
+    // Affine pages: this lane's share of the 16-byte copies that bring a chunk's scale and
+    // bias rows, fixed for the whole loop: copy j (lane + 32 j) reads plane row `row` at
+    // sb_src[j] + row * sb_pitch[j] bytes and lands at sb_dst[j] within the stage.
+    constexpr int kSbPerLane = C::kQuant ? (C::kSbCopies + 31) / 32 : 1;
+    const char* sb_src[kSbPerLane];
+    int sb_pitch[kSbPerLane], sb_dst[kSbPerLane];
+    if constexpr (C::kQuant) {
+      constexpr int nk = C::kSbBytes / 16, nv = C::kSbBytesV / 16;
+#pragma unroll
+      for (int j = 0; j < kSbPerLane; ++j) {
+        const int c = 32 * j + lane;
+        const int cc = c < C::kSbCopies ? c : 0;
+        const int plane = cc < 2 * nk ? cc / nk : 2 + (cc - 2 * nk) / nv;
+        const int k = cc < 2 * nk ? cc % nk : (cc - 2 * nk) % nv;
+        const __nv_bfloat16* src = plane == 0   ? p.k_scales
+                                   : plane == 1 ? p.k_biases
+                                   : plane == 2 ? p.v_scales
+                                                : p.v_biases;
+        sb_src[j] = reinterpret_cast<const char*>(src) + 16 * k;
+        sb_pitch[j] = 2 * (plane < 2 ? C::kGroups : C::kGroupsV);
+        sb_dst[j] = (plane == 0 ? C::kOffKs : plane == 1 ? C::kOffKb : plane == 2 ? C::kOffVs : C::kOffVb) + 16 * k;
+      }
+    }
+
     // Issues the next chunk into stage `is` (the one just consumed: with one stage per
     // chunk in flight, chunk i always lands in stage i mod kStagesPerGroup).
     auto issue_next = [&](int is) {  // the leader warp, warp-uniform
@@ -477,21 +501,10 @@ __global__ void __maxnreg__(255)
         // barrier wait for its copies before lane 0 arrives, so the phase cannot complete
         // without them.
         if (row >= 0) {
-          constexpr int nk = C::kSbBytes / 16, nv = C::kSbBytesV / 16;
-          const size_t sk = static_cast<size_t>(row) * C::kGroups, sv = static_cast<size_t>(row) * C::kGroupsV;
 #pragma unroll
-          for (int c0 = 0; c0 < C::kSbCopies; c0 += 32) {
-            const int c = c0 + lane;
-            if (c < C::kSbCopies) {
-              const int plane = c < 2 * nk ? c / nk : 2 + (c - 2 * nk) / nv;
-              const int k = c < 2 * nk ? c % nk : (c - 2 * nk) % nv;
-              const __nv_bfloat16* src = plane == 0   ? p.k_scales + sk
-                                         : plane == 1 ? p.k_biases + sk
-                                         : plane == 2 ? p.v_scales + sv
-                                                      : p.v_biases + sv;
-              const int off = plane == 0 ? C::kOffKs : plane == 1 ? C::kOffKb : plane == 2 ? C::kOffVs : C::kOffVb;
-              cp_async_16(st + off + 16 * k, reinterpret_cast<const char*>(src) + 16 * k, policy);
-            }
+          for (int j = 0; j < kSbPerLane; ++j) {
+            if (32 * j + lane < C::kSbCopies)
+              cp_async_16(st + sb_dst[j], sb_src[j] + static_cast<size_t>(row) * sb_pitch[j], policy);
           }
           cp_async_mbar_arrive(fb);
         }
@@ -651,12 +664,329 @@ __global__ void __maxnreg__(255)
     // ldmatrix row/chunk of this lane: non-transposed (keys on M) and transposed (keys on K).
     const int lrow_n = (lane & 7) + ((lane >> 3) & 1) * 8, lch_n = lane >> 4;
     const int lrow_t = (lane & 7) + (lane >> 4) * 8, lch_t = (lane >> 3) & 1;
+    // 4-bit pages: this lane's ldmatrix offsets within the K and V planes of a stage, per
+    // 64-dim group, for the first 16-key tile (tile t adds 16 rows: the swizzle pattern
+    // repeats every 8 rows), fixed for the whole loop.
+    int k4ofs[BITS == 4 ? C::kGroups : 1], v4ofs[BITS == 4 ? C::kGroupsV : 1];
+    if constexpr (BITS == 4) {
+#pragma unroll
+      for (int grp = 0; grp < C::kGroups; ++grp) k4ofs[grp] = swizzled<C::kRB>(0u, lrow_n, 2 * grp + lch_n);
+#pragma unroll
+      for (int grp = 0; grp < C::kGroupsV; ++grp) v4ofs[grp] = swizzled<C::kRBV>(0u, lrow_t, 2 * grp + lch_t);
+    }
+
+    // The tensor-core contraction of one staged chunk, in three parts. score_chunk: the
+    // scores (keys on rows, base 2), the causal tail / window mask and the online-softmax
+    // update of (m_run, l_run), giving the chunk's weights pr and, where a running maximum
+    // grew, the factors corr (returns whether any did, warp-uniform). rescale: applies corr
+    // to the value accumulators. value_chunk: O^T += V^T P^T over the chunk's value rows.
+    auto score_chunk = [&](uint32_t kpl, uint32_t sbq, int kbase, bool full_vis, float (&pr)[C::kTiles][NT][4],
+                           float (&corr)[NT][2]) -> bool {
+      // ---- scores x = (K q) * scale * log2(e), keys on rows
+      float x[C::kTiles][NT][4];
+#pragma unroll
+      for (int tile = 0; tile < C::kTiles; ++tile) {
+        float sacc[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) sacc[nt][e] = 0.f;
+        const int lrow = tile * 16 + lrow_n;
+        if constexpr (BITS == 16) {
+          // A CTA alone on its SM is bound by latency: two accumulators (even and odd
+          // k-steps) halve its dependent MMA chain. Elsewhere one chain costs fewer
+          // instructions.
+          constexpr int kChains = SOLO ? 2 : 1;
+          float sacc2[NT][4];
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sacc2[nt][e] = 0.f;
+#pragma unroll
+          for (int kk = 0; kk < C::kKs; ++kk) {
+            uint32_t a[4];
+            ldsm_x4(swizzled<C::kRB>(kpl + (kk >> 2) * C::kBoxBytes, lrow, (kk & 3) * 2 + lch_n), a);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+              mma_bf16((kChains == 2 && (kk & 1)) ? sacc2[nt] : sacc[nt], a[0], a[1], a[2], a[3], qf[kk][nt][0],
+                       qf[kk][nt][1]);
+          }
+          if constexpr (kChains == 2) {
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) sacc[nt][e] += sacc2[nt][e];
+          }
+        } else {
+          // scales of keys g and g + 8 of this tile, all groups
+          float ks0[C::kGroups], ks1[C::kGroups];
+          load_group_row<C::kGroups>(sbq + (tile * 16 + g) * C::kGroups * 2, ks0);
+          load_group_row<C::kGroups>(sbq + (tile * 16 + g + 8) * C::kGroups * 2, ks1);
+          {
+            // bias MMA: this lane's A words are the biases of k slots 2t, 2t+1 (groups
+            // 2t mod G, 2t mod G + 1) of keys g and g + 8
+            uint32_t ba0 = 0u, ba1 = 0u;
+            const uint32_t kb = kpl + C::kOffKb + (tile * 16 + g) * C::kGroups * 2;
+            if (C::kGroups == 4 || t < 2) {
+              const uint32_t off = C::kGroups == 4 ? (t & 1) * 4 : 0;
+              ba0 = ld_shared_u32(kb + off);
+              ba1 = ld_shared_u32(kb + 8 * C::kGroups * 2 + off);
+            }
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) mma_bf16(sacc[nt], ba0, ba1, 0u, 0u, qsb[nt], 0u);
+          }
+#pragma unroll
+          for (int grp = 0; grp < C::kGroups; ++grp) {
+            float sg[NT][4];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) sg[nt][e] = 0.f;
+            if constexpr (BITS == 4) {
+              // words t of chunks 2 grp, 2 grp + 1 for rows g, g + 8
+              uint32_t xk[4];
+              ldsm_x4(kpl + k4ofs[grp] + tile * 16 * C::kRB, xk);  // rows g, g + 8 of the tile
+#pragma unroll
+              for (int cc = 0; cc < 2; ++cc) {
+                const uint32_t xg = xk[2 * cc], x8 = xk[2 * cc + 1];
+                const uint32_t xg8 = xg >> 8, x88 = x8 >> 8;
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                  const int kk = 4 * grp + 2 * cc;
+                  mma_f16(sg[nt], xg & 0x000F000Fu, x8 & 0x000F000Fu, xg8 & 0x000F000Fu, x88 & 0x000F000Fu,
+                          qf[kk][nt][0], qf[kk][nt][1]);
+                  mma_f16(sg[nt], xg & 0x00F000F0u, x8 & 0x00F000F0u, xg8 & 0x00F000F0u, x88 & 0x00F000F0u,
+                          qf[kk + 1][nt][0], qf[kk + 1][nt][1]);
+                }
+              }
+            } else {
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                uint32_t xk[4];
+                ldsm_x4(swizzled<C::kRB>(kpl + (grp >> 1) * C::kBoxBytes, lrow, (grp & 1) * 4 + 2 * h + lch_n), xk);
+#pragma unroll
+                for (int cc = 0; cc < 2; ++cc) {
+                  const int kk = 4 * grp + 2 * h + cc;
+                  const uint32_t xg = xk[2 * cc], x8 = xk[2 * cc + 1];
+                  // bytes (0, 2) and (1, 3) of a word: dims (4t, 4t+2) and (4t+1, 4t+3)
+#pragma unroll
+                  for (int nt = 0; nt < NT; ++nt)
+                    mma_f16(sg[nt], __byte_perm(xg, 0u, 0x4240), __byte_perm(x8, 0u, 0x4240),
+                            __byte_perm(xg, 0u, 0x4341), __byte_perm(x8, 0u, 0x4341), qf[kk][nt][0], qf[kk][nt][1]);
+                }
+              }
+            }
+            // fold the scale of group grp for keys g and g + 8 of this tile
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              sacc[nt][0] = fmaf(ks0[grp], sg[nt][0], sacc[nt][0]);
+              sacc[nt][1] = fmaf(ks0[grp], sg[nt][1], sacc[nt][1]);
+              sacc[nt][2] = fmaf(ks1[grp], sg[nt][2], sacc[nt][2]);
+              sacc[nt][3] = fmaf(ks1[grp], sg[nt][3], sacc[nt][3]);
+            }
+          }
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) x[tile][nt][e] = sacc[nt][e] * colscale[nt][e & 1];
+      }
+
+
+      // ---- causal tail and stale rows
+      if (!full_vis) {
+#pragma unroll
+        for (int tile = 0; tile < C::kTiles; ++tile)
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int key = kbase + tile * 16 + g + 8 * (e >> 1);
+              const int qi = (rbase + 8 * nt + 2 * t + (e & 1)) % N;
+              const bool vis = key < vis_base + qi && (win == 0 || key >= vis_base + qi - win);
+              x[tile][nt][e] = vis ? x[tile][nt][e] : -INFINITY;
+            }
+      }
+
+      // ---- online softmax (base 2)
+      bool grew = false;
+      // This lane's maxima of the chunk. When no lane's exceeds the running maximum, the
+      // chunk's maximum does not either: the running maximum stays and nothing is
+      // rescaled, which is what the general path below computes too, without its
+      // cross-lane reduction (so the results are the same bit for bit).
+      float lmx[NT][2];
+      bool below = true;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e2 = 0; e2 < 2; ++e2) {
+          float mx = -INFINITY;
+#pragma unroll
+          for (int tile = 0; tile < C::kTiles; ++tile) mx = fmaxf(mx, fmaxf(x[tile][nt][e2], x[tile][nt][e2 + 2]));
+          lmx[nt][e2] = mx;
+          below &= mx <= m_run[nt][e2];
+        }
+      if (__all_sync(0xffffffffu, below)) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int e2 = 0; e2 < 2; ++e2) {
+            const float muse = m_run[nt][e2] == -INFINITY ? 0.f : m_run[nt][e2];
+            float ls = 0.f;
+#pragma unroll
+            for (int tile = 0; tile < C::kTiles; ++tile) {
+              pr[tile][nt][e2] = fast_exp2(x[tile][nt][e2] - muse);
+              pr[tile][nt][e2 + 2] = fast_exp2(x[tile][nt][e2 + 2] - muse);
+              ls += pr[tile][nt][e2] + pr[tile][nt][e2 + 2];
+            }
+            l_run[nt][e2] += ls;
+          }
+      } else {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+          for (int e2 = 0; e2 < 2; ++e2) {
+            float mx = lmx[nt][e2];
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+            const float mnew = fmaxf(m_run[nt][e2], mx);
+            const float muse = mnew == -INFINITY ? 0.f : mnew;
+            const float c = fast_exp2(m_run[nt][e2] - muse);
+            m_run[nt][e2] = mnew;
+            float ls = 0.f;
+#pragma unroll
+            for (int tile = 0; tile < C::kTiles; ++tile) {
+              pr[tile][nt][e2] = fast_exp2(x[tile][nt][e2] - muse);
+              pr[tile][nt][e2 + 2] = fast_exp2(x[tile][nt][e2 + 2] - muse);
+              ls += pr[tile][nt][e2] + pr[tile][nt][e2 + 2];
+            }
+            l_run[nt][e2] = fmaf(l_run[nt][e2], c, ls);
+            corr[nt][e2] = c;
+            grew |= c != 1.f;
+          }
+        }
+        grew = __any_sync(0xffffffffu, grew);
+      }
+      return grew;
+
+    };
+    auto rescale = [&](const float (&corr)[NT][2]) {
+#pragma unroll
+      for (int mt = 0; mt < C::kMt; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) o[mt][nt][e] *= corr[nt][e & 1];
+      if constexpr (C::kQuant) {
+#pragma unroll
+        for (int grp = 0; grp < C::kGroupsV; ++grp)
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e2 = 0; e2 < 2; ++e2) corr_v[grp][nt][e2] *= corr[nt][e2];
+      }
+    };
+    auto value_chunk = [&](uint32_t kpl, uint32_t vpl, int kbase, bool stale, const float (&pr)[C::kTiles][NT][4]) {
+      // ---- O^T += V^T P^T
+#pragma unroll
+      for (int tile = 0; tile < C::kTiles; ++tile) {
+        const int lrow = tile * 16 + lrow_t;
+        if constexpr (BITS == 16) {
+          uint32_t pb[NT][2];
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            pb[nt][0] = movmatrix_trans(pack_bf16x2(pr[tile][nt][0], pr[tile][nt][1]));
+            pb[nt][1] = movmatrix_trans(pack_bf16x2(pr[tile][nt][2], pr[tile][nt][3]));
+          }
+          uint32_t m01 = 0xffffffffu, m23 = 0xffffffffu;
+          if (stale) {
+            const int k0 = kbase + tile * 16 + 2 * t;
+            m01 = (k0 < len ? 0x0000ffffu : 0u) | (k0 + 1 < len ? 0xffff0000u : 0u);
+            m23 = (k0 + 8 < len ? 0x0000ffffu : 0u) | (k0 + 9 < len ? 0xffff0000u : 0u);
+          }
+#pragma unroll
+          for (int mt = 0; mt < C::kMt; ++mt) {
+            uint32_t a[4];
+            ldsm_x4_t(swizzled<C::kRBV>(vpl + (mt >> 2) * C::kBoxBytesV, lrow, (mt & 3) * 2 + lch_t), a);
+            a[0] &= m01;
+            a[1] &= m01;
+            a[2] &= m23;
+            a[3] &= m23;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) mma_bf16(o[mt][nt], a[0], a[1], a[2], a[3], pb[nt][0], pb[nt][1]);
+          }
+        } else {
+          const int r_a = tile * 16 + g, r_b = r_a + 8;
+          float vs0[C::kGroupsV], vs1[C::kGroupsV], vb0[C::kGroupsV], vb1[C::kGroupsV];
+          load_group_row<C::kGroupsV>(kpl + C::kOffVs + r_a * C::kGroupsV * 2, vs0);
+          load_group_row<C::kGroupsV>(kpl + C::kOffVs + r_b * C::kGroupsV * 2, vs1);
+          load_group_row<C::kGroupsV>(kpl + C::kOffVb + r_a * C::kGroupsV * 2, vb0);
+          load_group_row<C::kGroupsV>(kpl + C::kOffVb + r_b * C::kGroupsV * 2, vb1);
+          if (stale) {  // rows at or past len may hold anything: keep them out of P' and the bias sums
+            const bool va = kbase + r_a < len, vb = kbase + r_b < len;
+#pragma unroll
+            for (int grp = 0; grp < C::kGroupsV; ++grp) {
+              vs0[grp] = va ? vs0[grp] : 0.f;
+              vb0[grp] = va ? vb0[grp] : 0.f;
+              vs1[grp] = vb ? vs1[grp] : 0.f;
+              vb1[grp] = vb ? vb1[grp] : 0.f;
+            }
+          }
+#pragma unroll
+          for (int grp = 0; grp < C::kGroupsV; ++grp) {
+            uint32_t pb[NT][2];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              pb[nt][0] = movmatrix_trans(pack_f16x2(pr[tile][nt][0] * vs0[grp], pr[tile][nt][1] * vs0[grp]));
+              pb[nt][1] = movmatrix_trans(pack_f16x2(pr[tile][nt][2] * vs1[grp], pr[tile][nt][3] * vs1[grp]));
+              corr_v[grp][nt][0] = fmaf(pr[tile][nt][0], vb0[grp], fmaf(pr[tile][nt][2], vb1[grp], corr_v[grp][nt][0]));
+              corr_v[grp][nt][1] = fmaf(pr[tile][nt][1], vb0[grp], fmaf(pr[tile][nt][3], vb1[grp], corr_v[grp][nt][1]));
+            }
+            if constexpr (BITS == 4) {
+              // y: unit g (dims 4g..4g+3) of keys 2t (low half) and 2t+1 (high half),
+              // chunks 2 grp / 2 grp + 1, keys 0-7 / 8-15 of the tile
+              uint32_t y[4];
+              ldsm_x4_t(vpl + v4ofs[grp] + tile * 16 * C::kRBV, y);
+              uint32_t y8[4];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) y8[i] = y[i] >> 8;
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt) {
+                mma_f16(o[4 * grp + 0][nt], y[0] & 0x000F000Fu, y[1] & 0x000F000Fu, y[2] & 0x000F000Fu,
+                        y[3] & 0x000F000Fu, pb[nt][0], pb[nt][1]);
+                mma_f16(o[4 * grp + 1][nt], y[0] & 0x00F000F0u, y[1] & 0x00F000F0u, y[2] & 0x00F000F0u,
+                        y[3] & 0x00F000F0u, pb[nt][0], pb[nt][1]);
+                mma_f16(o[4 * grp + 2][nt], y8[0] & 0x000F000Fu, y8[1] & 0x000F000Fu, y8[2] & 0x000F000Fu,
+                        y8[3] & 0x000F000Fu, pb[nt][0], pb[nt][1]);
+                mma_f16(o[4 * grp + 3][nt], y8[0] & 0x00F000F0u, y8[1] & 0x00F000F0u, y8[2] & 0x00F000F0u,
+                        y8[3] & 0x00F000F0u, pb[nt][0], pb[nt][1]);
+              }
+            } else {
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                uint32_t y[4];
+                ldsm_x4_t(swizzled<C::kRBV>(vpl + (grp >> 1) * C::kBoxBytesV, lrow, (grp & 1) * 4 + 2 * h + lch_t), y);
+                // byte 0 / byte 2 of y: dim 2g of keys 2t / 2t+1; bytes 1 / 3: dim 2g + 1
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                  mma_f16(o[4 * grp + 2 * h][nt], __byte_perm(y[0], 0u, 0x4240), __byte_perm(y[1], 0u, 0x4240),
+                          __byte_perm(y[2], 0u, 0x4240), __byte_perm(y[3], 0u, 0x4240), pb[nt][0], pb[nt][1]);
+                  mma_f16(o[4 * grp + 2 * h + 1][nt], __byte_perm(y[0], 0u, 0x4341), __byte_perm(y[1], 0u, 0x4341),
+                          __byte_perm(y[2], 0u, 0x4341), __byte_perm(y[3], 0u, 0x4341), pb[nt][0], pb[nt][1]);
+                }
+              }
+            }
+          }
+        }
+      }
+    };
 
     int done = 0;  // local chunks consumed
-    for (; done < my_chunks; ++done) {
-      const int cs = done % C::kStagesPerGroup;  // its stage
-      const bool landed = mbar_wait_warp(smem_addr(&my_full[cs]), (done / C::kStagesPerGroup) & 1, abort_flag,
-                                         p.error_flag, p.wait_limit_ns);
+    int cs = 0;               // its stage: done mod kStagesPerGroup
+    uint32_t cs_parity = 0;   // the phase it waits for: (done / kStagesPerGroup) & 1
+    for (; done < my_chunks; ++done, cs_parity ^= (cs == C::kStagesPerGroup - 1), cs = cs == C::kStagesPerGroup - 1 ? 0 : cs + 1) {
+      const bool landed = mbar_wait_warp(smem_addr(&my_full[cs]), cs_parity, abort_flag, p.error_flag, p.wait_limit_ns);
       if (landed && my_ok[cs]) {
         uint8_t* stage = my_ring + cs * C::kStageBytes;
         const uint32_t kpl = smem_addr(stage);
@@ -670,301 +1000,10 @@ __global__ void __maxnreg__(255)
           cc_chunk<D, CCQ>(kpl, vpl, pbuf, ccq, cco, ccm, ccl, lane, kbase, len, vis_base, win, N, full_vis, stale,
                            p.score_scale);
         } else {
-        // ---- scores x = (K q) * scale * log2(e), keys on rows
-        float x[C::kTiles][NT][4];
-#pragma unroll
-        for (int tile = 0; tile < C::kTiles; ++tile) {
-          float sacc[NT][4];
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) sacc[nt][e] = 0.f;
-          const int lrow = tile * 16 + lrow_n;
-          if constexpr (BITS == 16) {
-            // A CTA alone on its SM is bound by latency: two accumulators (even and odd
-            // k-steps) halve its dependent MMA chain. Elsewhere one chain costs fewer
-            // instructions.
-            constexpr int kChains = SOLO ? 2 : 1;
-            float sacc2[NT][4];
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-              for (int e = 0; e < 4; ++e) sacc2[nt][e] = 0.f;
-#pragma unroll
-            for (int kk = 0; kk < C::kKs; ++kk) {
-              uint32_t a[4];
-              ldsm_x4(swizzled<C::kRB>(kpl + (kk >> 2) * C::kBoxBytes, lrow, (kk & 3) * 2 + lch_n), a);
-#pragma unroll
-              for (int nt = 0; nt < NT; ++nt)
-                mma_bf16((kChains == 2 && (kk & 1)) ? sacc2[nt] : sacc[nt], a[0], a[1], a[2], a[3], qf[kk][nt][0],
-                         qf[kk][nt][1]);
-            }
-            if constexpr (kChains == 2) {
-#pragma unroll
-              for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) sacc[nt][e] += sacc2[nt][e];
-            }
-          } else {
-            // scales of keys g and g + 8 of this tile, all groups
-            float ks0[C::kGroups], ks1[C::kGroups];
-            load_group_row<C::kGroups>(sbq + (tile * 16 + g) * C::kGroups * 2, ks0);
-            load_group_row<C::kGroups>(sbq + (tile * 16 + g + 8) * C::kGroups * 2, ks1);
-            {
-              // bias MMA: this lane's A words are the biases of k slots 2t, 2t+1 (groups
-              // 2t mod G, 2t mod G + 1) of keys g and g + 8
-              uint32_t ba0 = 0u, ba1 = 0u;
-              const uint32_t kb = kpl + C::kOffKb + (tile * 16 + g) * C::kGroups * 2;
-              if (C::kGroups == 4 || t < 2) {
-                const uint32_t off = C::kGroups == 4 ? (t & 1) * 4 : 0;
-                ba0 = ld_shared_u32(kb + off);
-                ba1 = ld_shared_u32(kb + 8 * C::kGroups * 2 + off);
-              }
-#pragma unroll
-              for (int nt = 0; nt < NT; ++nt) mma_bf16(sacc[nt], ba0, ba1, 0u, 0u, qsb[nt], 0u);
-            }
-#pragma unroll
-            for (int grp = 0; grp < C::kGroups; ++grp) {
-              float sg[NT][4];
-#pragma unroll
-              for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) sg[nt][e] = 0.f;
-              if constexpr (BITS == 4) {
-                // words t of chunks 2 grp, 2 grp + 1 for rows g, g + 8
-                uint32_t xk[4];
-                ldsm_x4(swizzled<C::kRB>(kpl, lrow, 2 * grp + lch_n), xk);
-#pragma unroll
-                for (int cc = 0; cc < 2; ++cc) {
-                  const uint32_t xg = xk[2 * cc], x8 = xk[2 * cc + 1];
-                  const uint32_t xg8 = xg >> 8, x88 = x8 >> 8;
-#pragma unroll
-                  for (int nt = 0; nt < NT; ++nt) {
-                    const int kk = 4 * grp + 2 * cc;
-                    mma_f16(sg[nt], xg & 0x000F000Fu, x8 & 0x000F000Fu, xg8 & 0x000F000Fu, x88 & 0x000F000Fu,
-                            qf[kk][nt][0], qf[kk][nt][1]);
-                    mma_f16(sg[nt], xg & 0x00F000F0u, x8 & 0x00F000F0u, xg8 & 0x00F000F0u, x88 & 0x00F000F0u,
-                            qf[kk + 1][nt][0], qf[kk + 1][nt][1]);
-                  }
-                }
-              } else {
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                  uint32_t xk[4];
-                  ldsm_x4(swizzled<C::kRB>(kpl + (grp >> 1) * C::kBoxBytes, lrow, (grp & 1) * 4 + 2 * h + lch_n), xk);
-#pragma unroll
-                  for (int cc = 0; cc < 2; ++cc) {
-                    const int kk = 4 * grp + 2 * h + cc;
-                    const uint32_t xg = xk[2 * cc], x8 = xk[2 * cc + 1];
-                    // bytes (0, 2) and (1, 3) of a word: dims (4t, 4t+2) and (4t+1, 4t+3)
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt)
-                      mma_f16(sg[nt], __byte_perm(xg, 0u, 0x4240), __byte_perm(x8, 0u, 0x4240),
-                              __byte_perm(xg, 0u, 0x4341), __byte_perm(x8, 0u, 0x4341), qf[kk][nt][0], qf[kk][nt][1]);
-                  }
-                }
-              }
-              // fold the scale of group grp for keys g and g + 8 of this tile
-#pragma unroll
-              for (int nt = 0; nt < NT; ++nt) {
-                sacc[nt][0] = fmaf(ks0[grp], sg[nt][0], sacc[nt][0]);
-                sacc[nt][1] = fmaf(ks0[grp], sg[nt][1], sacc[nt][1]);
-                sacc[nt][2] = fmaf(ks1[grp], sg[nt][2], sacc[nt][2]);
-                sacc[nt][3] = fmaf(ks1[grp], sg[nt][3], sacc[nt][3]);
-              }
-            }
-          }
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) x[tile][nt][e] = sacc[nt][e] * colscale[nt][e & 1];
-        }
-
-        // ---- causal tail and stale rows
-        if (!full_vis) {
-#pragma unroll
-          for (int tile = 0; tile < C::kTiles; ++tile)
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int key = kbase + tile * 16 + g + 8 * (e >> 1);
-                const int qi = (rbase + 8 * nt + 2 * t + (e & 1)) % N;
-                const bool vis = key < vis_base + qi && (win == 0 || key >= vis_base + qi - win);
-                x[tile][nt][e] = vis ? x[tile][nt][e] : -INFINITY;
-              }
-        }
-
-        // ---- online softmax (base 2)
         float pr[C::kTiles][NT][4];
         float corr[NT][2];
-        bool grew = false;
-        // This lane's maxima of the chunk. When no lane's exceeds the running maximum, the
-        // chunk's maximum does not either: the running maximum stays and nothing is
-        // rescaled, which is what the general path below computes too, without its
-        // cross-lane reduction (so the results are the same bit for bit).
-        float lmx[NT][2];
-        bool below = true;
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int e2 = 0; e2 < 2; ++e2) {
-            float mx = -INFINITY;
-#pragma unroll
-            for (int tile = 0; tile < C::kTiles; ++tile) mx = fmaxf(mx, fmaxf(x[tile][nt][e2], x[tile][nt][e2 + 2]));
-            lmx[nt][e2] = mx;
-            below &= mx <= m_run[nt][e2];
-          }
-        if (__all_sync(0xffffffffu, below)) {
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int e2 = 0; e2 < 2; ++e2) {
-              const float muse = m_run[nt][e2] == -INFINITY ? 0.f : m_run[nt][e2];
-              float ls = 0.f;
-#pragma unroll
-              for (int tile = 0; tile < C::kTiles; ++tile) {
-                pr[tile][nt][e2] = fast_exp2(x[tile][nt][e2] - muse);
-                pr[tile][nt][e2 + 2] = fast_exp2(x[tile][nt][e2 + 2] - muse);
-                ls += pr[tile][nt][e2] + pr[tile][nt][e2 + 2];
-              }
-              l_run[nt][e2] += ls;
-            }
-        } else {
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-#pragma unroll
-            for (int e2 = 0; e2 < 2; ++e2) {
-              float mx = lmx[nt][e2];
-              mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-              mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-              mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-              const float mnew = fmaxf(m_run[nt][e2], mx);
-              const float muse = mnew == -INFINITY ? 0.f : mnew;
-              const float c = fast_exp2(m_run[nt][e2] - muse);
-              m_run[nt][e2] = mnew;
-              float ls = 0.f;
-#pragma unroll
-              for (int tile = 0; tile < C::kTiles; ++tile) {
-                pr[tile][nt][e2] = fast_exp2(x[tile][nt][e2] - muse);
-                pr[tile][nt][e2 + 2] = fast_exp2(x[tile][nt][e2 + 2] - muse);
-                ls += pr[tile][nt][e2] + pr[tile][nt][e2 + 2];
-              }
-              l_run[nt][e2] = fmaf(l_run[nt][e2], c, ls);
-              corr[nt][e2] = c;
-              grew |= c != 1.f;
-            }
-          }
-        }
-        if (__any_sync(0xffffffffu, grew)) {
-#pragma unroll
-          for (int mt = 0; mt < C::kMt; ++mt)
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-              for (int e = 0; e < 4; ++e) o[mt][nt][e] *= corr[nt][e & 1];
-          if constexpr (C::kQuant) {
-#pragma unroll
-            for (int grp = 0; grp < C::kGroupsV; ++grp)
-#pragma unroll
-              for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                for (int e2 = 0; e2 < 2; ++e2) corr_v[grp][nt][e2] *= corr[nt][e2];
-          }
-        }
-
-        // ---- O^T += V^T P^T
-#pragma unroll
-        for (int tile = 0; tile < C::kTiles; ++tile) {
-          const int lrow = tile * 16 + lrow_t;
-          if constexpr (BITS == 16) {
-            uint32_t pb[NT][2];
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-              pb[nt][0] = movmatrix_trans(pack_bf16x2(pr[tile][nt][0], pr[tile][nt][1]));
-              pb[nt][1] = movmatrix_trans(pack_bf16x2(pr[tile][nt][2], pr[tile][nt][3]));
-            }
-            uint32_t m01 = 0xffffffffu, m23 = 0xffffffffu;
-            if (stale) {
-              const int k0 = kbase + tile * 16 + 2 * t;
-              m01 = (k0 < len ? 0x0000ffffu : 0u) | (k0 + 1 < len ? 0xffff0000u : 0u);
-              m23 = (k0 + 8 < len ? 0x0000ffffu : 0u) | (k0 + 9 < len ? 0xffff0000u : 0u);
-            }
-#pragma unroll
-            for (int mt = 0; mt < C::kMt; ++mt) {
-              uint32_t a[4];
-              ldsm_x4_t(swizzled<C::kRBV>(vpl + (mt >> 2) * C::kBoxBytesV, lrow, (mt & 3) * 2 + lch_t), a);
-              a[0] &= m01;
-              a[1] &= m01;
-              a[2] &= m23;
-              a[3] &= m23;
-#pragma unroll
-              for (int nt = 0; nt < NT; ++nt) mma_bf16(o[mt][nt], a[0], a[1], a[2], a[3], pb[nt][0], pb[nt][1]);
-            }
-          } else {
-            const int r_a = tile * 16 + g, r_b = r_a + 8;
-            float vs0[C::kGroupsV], vs1[C::kGroupsV], vb0[C::kGroupsV], vb1[C::kGroupsV];
-            load_group_row<C::kGroupsV>(kpl + C::kOffVs + r_a * C::kGroupsV * 2, vs0);
-            load_group_row<C::kGroupsV>(kpl + C::kOffVs + r_b * C::kGroupsV * 2, vs1);
-            load_group_row<C::kGroupsV>(kpl + C::kOffVb + r_a * C::kGroupsV * 2, vb0);
-            load_group_row<C::kGroupsV>(kpl + C::kOffVb + r_b * C::kGroupsV * 2, vb1);
-            if (stale) {  // rows at or past len may hold anything: keep them out of P' and the bias sums
-              const bool va = kbase + r_a < len, vb = kbase + r_b < len;
-#pragma unroll
-              for (int grp = 0; grp < C::kGroupsV; ++grp) {
-                vs0[grp] = va ? vs0[grp] : 0.f;
-                vb0[grp] = va ? vb0[grp] : 0.f;
-                vs1[grp] = vb ? vs1[grp] : 0.f;
-                vb1[grp] = vb ? vb1[grp] : 0.f;
-              }
-            }
-#pragma unroll
-            for (int grp = 0; grp < C::kGroupsV; ++grp) {
-              uint32_t pb[NT][2];
-#pragma unroll
-              for (int nt = 0; nt < NT; ++nt) {
-                pb[nt][0] = movmatrix_trans(pack_f16x2(pr[tile][nt][0] * vs0[grp], pr[tile][nt][1] * vs0[grp]));
-                pb[nt][1] = movmatrix_trans(pack_f16x2(pr[tile][nt][2] * vs1[grp], pr[tile][nt][3] * vs1[grp]));
-                corr_v[grp][nt][0] = fmaf(pr[tile][nt][0], vb0[grp], fmaf(pr[tile][nt][2], vb1[grp], corr_v[grp][nt][0]));
-                corr_v[grp][nt][1] = fmaf(pr[tile][nt][1], vb0[grp], fmaf(pr[tile][nt][3], vb1[grp], corr_v[grp][nt][1]));
-              }
-              if constexpr (BITS == 4) {
-                // y: unit g (dims 4g..4g+3) of keys 2t (low half) and 2t+1 (high half),
-                // chunks 2 grp / 2 grp + 1, keys 0-7 / 8-15 of the tile
-                uint32_t y[4];
-                ldsm_x4_t(swizzled<C::kRBV>(vpl, lrow, 2 * grp + lch_t), y);
-                uint32_t y8[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) y8[i] = y[i] >> 8;
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                  mma_f16(o[4 * grp + 0][nt], y[0] & 0x000F000Fu, y[1] & 0x000F000Fu, y[2] & 0x000F000Fu,
-                          y[3] & 0x000F000Fu, pb[nt][0], pb[nt][1]);
-                  mma_f16(o[4 * grp + 1][nt], y[0] & 0x00F000F0u, y[1] & 0x00F000F0u, y[2] & 0x00F000F0u,
-                          y[3] & 0x00F000F0u, pb[nt][0], pb[nt][1]);
-                  mma_f16(o[4 * grp + 2][nt], y8[0] & 0x000F000Fu, y8[1] & 0x000F000Fu, y8[2] & 0x000F000Fu,
-                          y8[3] & 0x000F000Fu, pb[nt][0], pb[nt][1]);
-                  mma_f16(o[4 * grp + 3][nt], y8[0] & 0x00F000F0u, y8[1] & 0x00F000F0u, y8[2] & 0x00F000F0u,
-                          y8[3] & 0x00F000F0u, pb[nt][0], pb[nt][1]);
-                }
-              } else {
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                  uint32_t y[4];
-                  ldsm_x4_t(swizzled<C::kRBV>(vpl + (grp >> 1) * C::kBoxBytesV, lrow, (grp & 1) * 4 + 2 * h + lch_t), y);
-                  // byte 0 / byte 2 of y: dim 2g of keys 2t / 2t+1; bytes 1 / 3: dim 2g + 1
-#pragma unroll
-                  for (int nt = 0; nt < NT; ++nt) {
-                    mma_f16(o[4 * grp + 2 * h][nt], __byte_perm(y[0], 0u, 0x4240), __byte_perm(y[1], 0u, 0x4240),
-                            __byte_perm(y[2], 0u, 0x4240), __byte_perm(y[3], 0u, 0x4240), pb[nt][0], pb[nt][1]);
-                    mma_f16(o[4 * grp + 2 * h + 1][nt], __byte_perm(y[0], 0u, 0x4341), __byte_perm(y[1], 0u, 0x4341),
-                            __byte_perm(y[2], 0u, 0x4341), __byte_perm(y[3], 0u, 0x4341), pb[nt][0], pb[nt][1]);
-                  }
-                }
-              }
-            }
-          }
-        }
+        if (score_chunk(kpl, sbq, kbase, full_vis, pr, corr)) rescale(corr);
+        value_chunk(kpl, vpl, kbase, stale, pr);
         }  // tensor-core contraction
       }
       if constexpr (WQ == 1) {
