@@ -124,28 +124,32 @@ def setup_fused(bits, D, N, hq, hk, seed_name, num_seqs=3, length_range=(1, 300)
 
 
 FUSED = [
-    # bits, D, N, HQ, HK, partition_tokens (-1 single, 0 auto), window, value head dim (0: D)
-    (16, 128, 1, 8, 2, -1, 0, 0),
-    (16, 128, 4, 8, 2, 32, 0, 0),
-    (16, 256, 2, 4, 2, 64, 0, 0),
-    (16, 64, 3, 8, 1, 48, 0, 0),
-    (4, 256, 2, 8, 2, 64, 0, 0),
-    (4, 128, 1, 4, 1, 0, 0, 0),
-    (8, 128, 3, 8, 2, 32, 0, 0),
-    (8, 256, 1, 8, 2, -1, 0, 0),
-    (16, 128, 4, 8, 2, 32, 40, 0),
-    (16, 192, 2, 8, 2, 32, 0, 128),
-    (4, 256, 1, 8, 2, 64, 0, 128),
+    # bits, D, N, HQ, HK, partition_tokens (-1 single, 0 auto), window, value head dim (0: D), sequences
+    (16, 128, 1, 8, 2, -1, 0, 0, 3),
+    (16, 128, 4, 8, 2, 32, 0, 0, 3),
+    (16, 256, 2, 4, 2, 64, 0, 0, 3),
+    (16, 64, 3, 8, 1, 48, 0, 0, 3),
+    (4, 256, 2, 8, 2, 64, 0, 0, 3),
+    (4, 128, 1, 4, 1, 0, 0, 0, 3),
+    (8, 128, 3, 8, 2, 32, 0, 0, 3),
+    (8, 256, 1, 8, 2, -1, 0, 0, 3),
+    (16, 128, 4, 8, 2, 32, 40, 0, 3),
+    (16, 192, 2, 8, 2, 32, 0, 128, 3),
+    (4, 256, 1, 8, 2, 64, 0, 128, 3),
     # one query group of 8 warps (33..64 query rows at 256-dim heads)
-    (16, 256, 2, 64, 2, 64, 0, 0),
-    (4, 256, 4, 24, 2, 64, 0, 128),
+    (16, 256, 2, 64, 2, 64, 0, 0, 3),
+    (4, 256, 4, 24, 2, 64, 0, 128, 3),
+    # affine, 8 query rows, grids of several waves
+    (4, 256, 2, 8, 2, 32, 0, 0, 120),
+    (8, 128, 1, 8, 2, 32, 0, 0, 120),
 ]
 
 
-@pytest.mark.parametrize("bits,D,N,hq,hk,part,window,dv", FUSED,
-                         ids=[f"b{c[0]}_d{c[1]}_n{c[2]}_p{c[5]}_w{c[6]}_v{c[7]}" for c in FUSED])
-def test_fused_append_attend_matches_append_then_decode(bits, D, N, hq, hk, part, window, dv):
-    sp, case, lens, k_new, v_new = setup_fused(bits, D, N, hq, hk, f"p{part}w{window}", window=window, dv=dv)
+@pytest.mark.parametrize("bits,D,N,hq,hk,part,window,dv,seqs", FUSED,
+                         ids=[f"b{c[0]}_d{c[1]}_n{c[2]}_p{c[5]}_w{c[6]}_v{c[7]}_s{c[8]}" for c in FUSED])
+def test_fused_append_attend_matches_append_then_decode(bits, D, N, hq, hk, part, window, dv, seqs):
+    sp, case, lens, k_new, v_new = setup_fused(bits, D, N, hq, hk, f"p{part}w{window}", window=window, dv=dv,
+                                               num_seqs=seqs)
     part = 1 << 20 if part < 0 else part  # one partition: any size past the table
     # the write oracle's pools, then the attention oracle over them
     ref = pw.append_rows(k_new.float().numpy(), v_new.float().numpy(), case.block_tables.numpy(), lens,

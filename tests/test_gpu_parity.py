@@ -160,6 +160,55 @@ def test_cluster_merge_matches_oracle(bits, parts, head_dim, rep):
     assert_close(out.double().cpu().numpy(), oracle_out(case), f"cluster {bits} {parts} {head_dim}")
 
 
+# Affine pages on grids of several waves of two CTAs per SM, with 1..8 query rows, windows
+# and partitions of one or a few chunks.
+MANY_CTAS = [
+    (spec("many_u4_d256_nq4", num_seqs=120, head_dim=256, bits=4, block_size=32, length_range=(1, 700)), [32, 96]),
+    (spec("many_u4_d128_nq8_n2", num_seqs=120, num_q_heads=8, head_dim=128, bits=4, n_query=2, block_size=32,
+          length_range=(2, 600)), [32, 64]),
+    (spec("many_u8_d256_nq1", num_seqs=120, num_q_heads=2, head_dim=256, bits=8, block_size=32,
+          length_range=(1, 700)), [32, 64]),
+    (spec("many_u8_d128_nq4_n4", num_seqs=160, num_q_heads=2, num_kv_heads=2, head_dim=128, bits=8, n_query=4,
+          block_size=64, length_range=(4, 500)), [32]),
+    (spec("many_u4_window", num_seqs=120, head_dim=256, bits=4, block_size=32, length_range=(50, 900), window=300),
+     [32, 64]),
+]
+
+
+@pytest.mark.parametrize("sp,parts", MANY_CTAS, ids=[s.name for s, _ in MANY_CTAS])
+def test_affine_grids_of_several_waves_match_oracle(sp, parts):
+    case = make_case(sp)
+    ref = oracle_out(case)
+    dcase = case.to(DEV)
+    sms = torch.cuda.get_device_properties(DEV).multi_processor_count
+    for pt in parts:
+        plan = B.make_plan(B.layout_for(case.k_pool, sp.head_dim, sp.bits),
+                           B.DecodeParams(sp.num_seqs, sp.num_q_heads, sp.n_query, case.block_tables.shape[1], pt,
+                                          sp.window))
+        assert sp.num_seqs * sp.num_kv_heads * plan.max_partitions > 2 * sms and plan.threads_per_cta == 128
+        err = torch.zeros(1, dtype=torch.int32, device=DEV)
+        out = run_gpu(dcase, partition_tokens=pt, error_flag=err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        # 8-bit outputs reach |40|, where a bf16 output's own rounding passes 1e-2
+        assert_close(out.double().cpu().numpy(), ref, f"{sp.name} partition={pt}", strict=sp.bits != 8)
+
+
+def test_affine_grid_of_several_waves_flags_a_bad_block():
+    sp = spec("many_badblock", num_seqs=120, head_dim=256, bits=4, block_size=32, length_range=(100, 300))
+    case = make_case(sp).to(DEV)
+    good = run_gpu(case, partition_tokens=32)
+    tb = case.block_tables.clone()
+    tb[7, 2] = case.num_blocks + 3
+    case.block_tables = tb
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = run_gpu(case, partition_tokens=32, error_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & B.PKV_DEVERR_BAD_BLOCK
+    keep = [i for i in range(sp.num_seqs) if i != 7]
+    assert torch.equal(out[keep].view(torch.int16), good[keep].view(torch.int16))
+
+
 WINDOWED = [
     (spec("win_bf16_n1", length_range=(20, 900), window=100), [-1, 64, 0]),
     (spec("win_bf16_n4", num_q_heads=4, num_kv_heads=1, n_query=4, length_range=(4, 700), window=37), [-1, 32, 96]),
