@@ -299,11 +299,18 @@ __device__ __forceinline__ void load_group_row(uint32_t addr, float (&v)[G]) {
 // HOSTIN: a host-driven step whose length, query and block tables all live in host
 // memory the host wrote before the launch (no kernel writes them): they are read before
 // the wait for the previous kernel on the stream, so their NVLink-C2C latency overlaps it.
-template <int BITS, int D, int DV, int NT, int WQ, bool SOLO, bool HOSTIN, int CCQ = 0>
+// PV: 4-bit pages with at most 4 query rows per KV head (NT = WQ = 1). The 8 columns of
+// the MMAs then hold the query rows twice (columns 4-7 repeat rows 0-3), so the scores
+// give every weight twice, and one transposed weight fragment serves a pair of 64-dim
+// groups: columns 0-3 carry the weights scaled by the even group's value scales, columns
+// 4-7 by the odd group's; each group's MMAs keep the columns of their own group.
+template <int BITS, int D, int DV, int NT, int WQ, bool SOLO, bool HOSTIN, int CCQ = 0, bool PV = false>
 __global__ void __maxnreg__(255)
     pkv_partial_kernel(const __grid_constant__ PartialParams p, const __grid_constant__ CUtensorMap tmap_k,
                        const __grid_constant__ CUtensorMap tmap_v) {
   using C = PartialCfg<BITS, D, DV, NT, WQ, SOLO, CCQ>;
+  static_assert(!PV || (BITS == 4 && NT == 1 && WQ == 1 && CCQ == 0 && C::kGroupsV % 2 == 0),
+                "paired value groups: 4-bit pages, one warp of 8 query columns, whole group pairs");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + C::kDataBytes);  // [warp][stage]
@@ -342,7 +349,7 @@ __global__ void __maxnreg__(255)
   } else {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      const int r = rbase + 8 * nt + g;
+      const int r = PV ? g & 3 : rbase + 8 * nt + g;  // PV: columns 4-7 repeat query rows 0-3
       const __nv_bfloat16* qrow = p.q + (row0 + (r < p.nq ? r : 0)) * D;
       q_load_words<BITS, D>(qrow, t, r < p.nq, qw[nt]);
     }
@@ -802,7 +809,7 @@ __global__ void __maxnreg__(255)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int key = kbase + tile * 16 + g + 8 * (e >> 1);
-              const int qi = (rbase + 8 * nt + 2 * t + (e & 1)) % N;
+              const int qi = (PV ? (2 * t + (e & 1)) & 3 : rbase + 8 * nt + 2 * t + (e & 1)) % N;
               const bool vis = key < vis_base + qi && (win == 0 || key >= vis_base + qi - win);
               x[tile][nt][e] = vis ? x[tile][nt][e] : -INFINITY;
             }
@@ -933,6 +940,38 @@ __global__ void __maxnreg__(255)
               vb1[grp] = vb ? vb1[grp] : 0.f;
             }
           }
+          if constexpr (PV) {
+            // One weight fragment per group pair: columns 0-3 (lanes with t < 2) scaled by
+            // the even group's value scales, columns 4-7 (t >= 2) by the odd group's; each
+            // lane also sums the biases of its own group of the pair.
+            const int odd = t >> 1;
+#pragma unroll
+            for (int pp = 0; pp < C::kGroupsV / 2; ++pp) {
+              const float sa = odd ? vs0[2 * pp + 1] : vs0[2 * pp], sb = odd ? vs1[2 * pp + 1] : vs1[2 * pp];
+              const float ba = odd ? vb0[2 * pp + 1] : vb0[2 * pp], bb = odd ? vb1[2 * pp + 1] : vb1[2 * pp];
+              const uint32_t pb0 = movmatrix_trans(pack_f16x2(pr[tile][0][0] * sa, pr[tile][0][1] * sa));
+              const uint32_t pb1 = movmatrix_trans(pack_f16x2(pr[tile][0][2] * sb, pr[tile][0][3] * sb));
+              corr_v[pp][0][0] = fmaf(pr[tile][0][0], ba, fmaf(pr[tile][0][2], bb, corr_v[pp][0][0]));
+              corr_v[pp][0][1] = fmaf(pr[tile][0][1], ba, fmaf(pr[tile][0][3], bb, corr_v[pp][0][1]));
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const int grp = 2 * pp + h;
+                uint32_t y[4];
+                ldsm_x4_t(vpl + v4ofs[grp] + tile * 16 * C::kRBV, y);
+                uint32_t y8[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) y8[i] = y[i] >> 8;
+                mma_f16(o[4 * grp + 0][0], y[0] & 0x000F000Fu, y[1] & 0x000F000Fu, y[2] & 0x000F000Fu,
+                        y[3] & 0x000F000Fu, pb0, pb1);
+                mma_f16(o[4 * grp + 1][0], y[0] & 0x00F000F0u, y[1] & 0x00F000F0u, y[2] & 0x00F000F0u,
+                        y[3] & 0x00F000F0u, pb0, pb1);
+                mma_f16(o[4 * grp + 2][0], y8[0] & 0x000F000Fu, y8[1] & 0x000F000Fu, y8[2] & 0x000F000Fu,
+                        y8[3] & 0x000F000Fu, pb0, pb1);
+                mma_f16(o[4 * grp + 3][0], y8[0] & 0x00F000F0u, y8[1] & 0x00F000F0u, y8[2] & 0x00F000F0u,
+                        y8[3] & 0x00F000F0u, pb0, pb1);
+              }
+            }
+          } else {
 #pragma unroll
           for (int grp = 0; grp < C::kGroupsV; ++grp) {
             uint32_t pb[NT][2];
@@ -978,6 +1017,7 @@ __global__ void __maxnreg__(255)
               }
             }
           }
+          }  // unpaired groups
         }
       }
     };
@@ -1074,7 +1114,8 @@ __global__ void __maxnreg__(255)
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
           for (int e = 0; e < 4; ++e)
-            o[mt][nt][e] = fmaf(o[mt][nt][e], (1.f / C::kCodeUnit) * v_tile_factor<BITS>(mt), corr_v[mt >> 2][nt][e & 1]);
+            o[mt][nt][e] = fmaf(o[mt][nt][e], (1.f / C::kCodeUnit) * v_tile_factor<BITS>(mt),
+                                corr_v[PV ? mt >> 3 : mt >> 2][nt][e & 1]);
     }
     }  // tensor-core contraction
   }
@@ -1135,7 +1176,10 @@ __global__ void __maxnreg__(255)
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int r = 8 * nt + 2 * t + (e & 1);
+          // PV: a lane holds the columns of one group of each pair (t < 2: even groups,
+          // columns 0-3; t >= 2: odd groups, columns 4-7, query rows 0-3 again)
+          if (PV && ((mt >> 2) & 1) != (t >> 1)) continue;
+          const int r = PV ? (2 * t + (e & 1)) & 3 : 8 * nt + 2 * t + (e & 1);
           if (rbase + r >= p.nq) continue;
           float* dst = co + (rbase + r) * C::kCoStride + out_dim<BITS>(mt, e >> 1, g);
           if constexpr (kRun == 4) {

@@ -63,6 +63,16 @@ SMALL = [
           length_range=(2, 400)), [-1, 64]),
     (spec("u8_d128_nq32", num_q_heads=32, num_kv_heads=1, head_dim=128, bits=8, block_size=32,
           length_range=(1, 400)), [-1, 32]),
+    # 4-bit pages with at most 4 query rows: the paired-value-group form (query columns 4-7
+    # repeat rows 0-3), with causal tails of 2 and 3 new rows and a padding column
+    (spec("u4_pv_rep2_n2", num_q_heads=4, num_kv_heads=2, head_dim=256, bits=4, n_query=2, block_size=32,
+          length_range=(2, 500)), [-1, 32, 0]),
+    (spec("u4_pv_rep1_n3", num_q_heads=2, num_kv_heads=2, head_dim=128, bits=4, n_query=3, block_size=32,
+          length_range=(3, 500)), [-1, 64]),
+    (spec("u4_pv_nq1", num_q_heads=2, num_kv_heads=2, head_dim=256, bits=4, block_size=64,
+          length_range=(1, 500)), [-1, 96]),
+    (spec("u4_pv_nq2_d128", num_q_heads=4, num_kv_heads=2, head_dim=128, bits=4, block_size=32,
+          length_range=(1, 400)), [-1, 32]),
     # key and value head dims that differ (the pages' vHeadDim)
     (spec("bf16_dk192_dv128_nq4", head_dim=192, v_head_dim=128), [-1, 32, 0]),
     (spec("bf16_dk192_dv128_nq16_n2", num_q_heads=16, head_dim=192, v_head_dim=128, n_query=2,
@@ -213,6 +223,8 @@ WINDOWED = [
     (spec("win_bf16_n1", length_range=(20, 900), window=100), [-1, 64, 0]),
     (spec("win_bf16_n4", num_q_heads=4, num_kv_heads=1, n_query=4, length_range=(4, 700), window=37), [-1, 32, 96]),
     (spec("win_u4", head_dim=256, bits=4, block_size=32, length_range=(50, 900), window=300), [-1, 64, 0]),
+    (spec("win_u4_pv_n2", num_q_heads=2, num_kv_heads=1, head_dim=256, bits=4, n_query=2, block_size=32,
+          length_range=(20, 700), window=90), [-1, 32]),
     (spec("win_u8_n2", head_dim=128, bits=8, block_size=32, n_query=2, length_range=(2, 600), window=1), [-1, 96]),
     (spec("win_bf16_one_seq", num_seqs=1, lengths=(2000,), length_range=None, window=700), [128, 256]),
 ]
