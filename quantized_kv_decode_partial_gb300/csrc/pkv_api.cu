@@ -369,7 +369,7 @@ struct PreparedDecode {
   pkv::MergeParams m;
   CUtensorMap tk, tv;
   dim3 grid;
-  int bits, dk, dv, nq, device, merge_rows;
+  int bits, dk, dv, nq, device;
   bool solo, cc, partial, merge;
 };
 
@@ -486,7 +486,8 @@ int prepare_decode(const pkv_pool_layout* layout, const pkv_decode_params* param
     m.partition_tokens = plan.partition_tokens;
     m.max_partitions = plan.max_partitions;
     m.window = params->window;
-    pd->merge_rows = params->num_seqs * params->num_q_heads * params->n_query;
+    m.rows = params->num_seqs * params->num_q_heads * params->n_query;
+    m.groups = pkv::merge_groups(DV, plan.max_partitions);
   }
   return PKV_OK;
 }
@@ -508,7 +509,7 @@ int launch_prepared(const PreparedDecode& pd, cudaStream_t st) {
     if (e != cudaSuccess) return cuda_fail("partial kernel launch", e);
   }
   if (pd.merge) {
-    e = pkv::launch_merge(pd.m, pd.merge_rows, st);
+    e = pkv::launch_merge(pd.m, st);
     if (e != cudaSuccess) return cuda_fail("merge kernel launch", e);
   }
   return PKV_OK;

@@ -85,6 +85,8 @@ struct MergeParams {
   int rows_per_seq;  // HQ * N
   int n_query, head_dim, max_len, partition_tokens, max_partitions;
   int window;  // sliding window in rows (0: none)
+  int rows;    // output rows (B * HQ * N)
+  int groups;  // partition groups per output row (merge_groups)
 };
 
 struct AppendParams {

@@ -38,7 +38,8 @@ cudaError_t launch_partial_u8(int dk, int dv, int nq, bool solo, const PartialPa
 cudaError_t launch_partial_bf16_cc(int dk, int dv, int nq, bool solo, const PartialParams& p, const CUtensorMap& tk,
                                    const CUtensorMap& tv, dim3 grid, cudaStream_t stream, int device);
 
-cudaError_t launch_merge(const MergeParams& p, int rows, cudaStream_t stream);
+int merge_groups(int head_dim, int max_partitions);
+cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream);
 cudaError_t launch_gather(const GatherParams& p, int num_seqs, cudaStream_t stream);
 
 bool append_supported(int bits, int head_dim, int v_head_dim);

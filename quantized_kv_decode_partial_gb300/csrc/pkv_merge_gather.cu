@@ -4,18 +4,21 @@
 
 namespace pkv {
 
-// One CTA per output row (sequence, query head, query index). The partition states
-// hold the running maximum in log2 units, the normaliser and the unnormalised
-// output; partitions whose maximum is -inf saw no visible key and are skipped
-// (kvq4-decode.ts and multi-query.ts merge kernels).
+// A thread owns four consecutive head dims of one output row (sequence, query head,
+// query index) and every groups-th of its partitions: a row takes `groups` groups of
+// D/4 threads, a CTA 256 / (groups * D/4) rows. The partition states hold the running
+// maximum in log2 units, the normaliser and the unnormalised output; partitions whose
+// maximum is -inf saw no visible key and are skipped (kvq4-decode.ts and
+// multi-query.ts merge kernels).
 // Output = sum_p 2^(m_p-M) o_p / sum_p 2^(m_p-M) l_p.
-// The CTA's threads form 256 / (D/4) groups of D/4 threads; a thread owns four
-// consecutive head dims and every groups-th partition. Each group merges its
-// partitions online against its own running maximum, and the groups' states are
-// combined once in shared memory. A thread's first kMergeUnroll partition slots are
-// requested together with the sequence length (the slots exist for every row; those
-// past the row's partition count are dropped once the length arrives), so a row with
-// at most kMergeUnroll partitions per group costs one memory round trip.
+// Each group merges its partitions online against its own running maximum; with more
+// than one group per row the groups' states are combined once in shared memory. A
+// thread's first kMergeUnroll partition slots are requested together with the sequence
+// length (the slots exist for every row; those past the row's partition count are
+// dropped once the length arrives), so a row with at most groups * kMergeUnroll
+// partitions costs one memory round trip. The host takes the fewest groups that cover
+// the partitions in that round trip, so that short rows pack several to a CTA and the
+// grid stays within one wave.
 constexpr int kMergeThreads = 256;
 constexpr int kMergeUnroll = 4;
 
@@ -42,12 +45,14 @@ __global__ void __launch_bounds__(kMergeThreads) pkv_merge_kernel(const __grid_c
   __shared__ float red_m[kMergeThreads];
   __shared__ float4 red_o[kMergeThreads];
   __shared__ float red_l[kMergeThreads];
-  const int row = blockIdx.x;
-  const int lanes = p.head_dim / 4;         // threads per group
-  const int groups = kMergeThreads / lanes;  // 4 (D=256), 8 (D=128), 16 (D=64)
-  const int grp = threadIdx.x / lanes, d = (threadIdx.x % lanes) * 4;
-  wait_for_prerequisite_grids();  // launched early behind the partial pass; its states are ready after this
-  const int b = row / p.rows_per_seq;
+  const int lanes = p.head_dim / 4;    // threads per group
+  const int span = lanes * p.groups;  // threads per row
+  const int row = blockIdx.x * (kMergeThreads / span) + threadIdx.x / span;
+  const int grp = (threadIdx.x % span) / lanes, d = (threadIdx.x % lanes) * 4;
+  const bool live = row < p.rows;  // the last CTA may hold fewer rows
+  wait_for_prerequisite_grids();   // launched early behind the partial pass; its states are ready after this
+  const int b = live ? row / p.rows_per_seq : 0;
+  const int slots = live ? p.max_partitions : 0;
   const float2* ml = reinterpret_cast<const float2*>(p.ws_ml) + static_cast<size_t>(row) * p.max_partitions;
   const float4* ob = reinterpret_cast<const float4*>(p.ws_o + static_cast<size_t>(row) * p.max_partitions * p.head_dim + d);
   const int ostride = p.head_dim / 4;
@@ -55,63 +60,61 @@ __global__ void __launch_bounds__(kMergeThreads) pkv_merge_kernel(const __grid_c
   float4 v[kMergeUnroll];
 #pragma unroll
   for (int u = 0; u < kMergeUnroll; ++u) {
-    const int i = grp + u * groups;
-    s[u] = i < p.max_partitions ? ml[i] : make_float2(-INFINITY, 0.f);
-    v[u] = i < p.max_partitions ? ob[static_cast<size_t>(i) * ostride] : make_float4(0.f, 0.f, 0.f, 0.f);
+    const int i = grp + u * p.groups;
+    s[u] = i < slots ? ml[i] : make_float2(-INFINITY, 0.f);
+    v[u] = i < slots ? ob[static_cast<size_t>(i) * ostride] : make_float4(0.f, 0.f, 0.f, 0.f);
   }
   const int len = p.seq_lens[b];
-  const size_t o_off = static_cast<size_t>(row) * p.head_dim + d;
-  __nv_bfloat162* out = reinterpret_cast<__nv_bfloat162*>(p.out + o_off);
-  __nv_bfloat162* mirror = p.out_mirror ? reinterpret_cast<__nv_bfloat162*>(p.out_mirror + o_off) : nullptr;
-  if (len < p.n_query || len > p.max_len) {  // flagged by the partial pass
-    if (grp == 0) {
-      out[0] = out[1] = __floats2bfloat162_rn(0.f, 0.f);
-      if (mirror) mirror[0] = mirror[1] = __floats2bfloat162_rn(0.f, 0.f);
-    }
-    return;
-  }
+  const bool bad = len < p.n_query || len > p.max_len;  // flagged by the partial pass; the row is zeroed
   // Slot i holds the partition of rows [base + i P, base + (i + 1) P).
-  const int base = partition_base(len, p.n_query, p.window);
-  const int np = (len - base + p.partition_tokens - 1) / p.partition_tokens;
+  const int base = bad ? 0 : partition_base(len, p.n_query, p.window);
+  const int np = live && !bad ? (len - base + p.partition_tokens - 1) / p.partition_tokens : 0;
 
   float M = -INFINITY, den = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
   for (int u = 0; u < kMergeUnroll; ++u)
-    if (grp + u * groups < np) merge_one(s[u], v[u], M, den, acc);
-  for (int i0 = grp + kMergeUnroll * groups; i0 < np; i0 += groups * kMergeUnroll) {
+    if (grp + u * p.groups < np) merge_one(s[u], v[u], M, den, acc);
+  for (int i0 = grp + kMergeUnroll * p.groups; i0 < np; i0 += p.groups * kMergeUnroll) {
 #pragma unroll
     for (int u = 0; u < kMergeUnroll; ++u) {
-      const int i = i0 + u * groups;
+      const int i = i0 + u * p.groups;
       s[u] = i < np ? ml[i] : make_float2(-INFINITY, 0.f);
       v[u] = i < np ? ob[static_cast<size_t>(i) * ostride] : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
     for (int u = 0; u < kMergeUnroll; ++u) merge_one(s[u], v[u], M, den, acc);
   }
-  red_m[threadIdx.x] = M;
-  red_o[threadIdx.x] = acc;
-  red_l[threadIdx.x] = den;
-  __syncthreads();
-  if (grp != 0) return;
-  float Mall = M;
-  for (int g = 1; g < groups; ++g) Mall = fmaxf(Mall, red_m[g * lanes + threadIdx.x]);
-  den = 0.f;
-  acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (Mall != -INFINITY) {
-    for (int g = 0; g < groups; ++g) {
-      const int k = g * lanes + threadIdx.x;
-      const float mg = red_m[k];
-      if (mg == -INFINITY) continue;
-      const float w = fast_exp2(mg - Mall);
-      const float4 o = red_o[k];
-      den = fmaf(w, red_l[k], den);
-      acc.x = fmaf(w, o.x, acc.x);
-      acc.y = fmaf(w, o.y, acc.y);
-      acc.z = fmaf(w, o.z, acc.z);
-      acc.w = fmaf(w, o.w, acc.w);
+  if (p.groups > 1) {  // the same for the whole CTA
+    red_m[threadIdx.x] = M;
+    red_o[threadIdx.x] = acc;
+    red_l[threadIdx.x] = den;
+    __syncthreads();
+    if (grp != 0) return;
+    float Mall = M;
+    for (int g = 1; g < p.groups; ++g) Mall = fmaxf(Mall, red_m[threadIdx.x + g * lanes]);
+    den = 0.f;
+    acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (Mall != -INFINITY) {
+      for (int g = 0; g < p.groups; ++g) {
+        const int k = threadIdx.x + g * lanes;
+        const float mg = red_m[k];
+        if (mg == -INFINITY) continue;
+        const float w = fast_exp2(mg - Mall);
+        const float4 o = red_o[k];
+        den = fmaf(w, red_l[k], den);
+        acc.x = fmaf(w, o.x, acc.x);
+        acc.y = fmaf(w, o.y, acc.y);
+        acc.z = fmaf(w, o.z, acc.z);
+        acc.w = fmaf(w, o.w, acc.w);
+      }
     }
   }
+  if (!live) return;
+  const size_t o_off = static_cast<size_t>(row) * p.head_dim + d;
+  __nv_bfloat162* out = reinterpret_cast<__nv_bfloat162*>(p.out + o_off);
+  __nv_bfloat162* mirror = p.out_mirror ? reinterpret_cast<__nv_bfloat162*>(p.out_mirror + o_off) : nullptr;
+  // den is 0 for a bad length (no partition merged) and for a row that saw no key
   const __nv_bfloat162 v0 = den > 0.f ? __floats2bfloat162_rn(acc.x / den, acc.y / den) : __floats2bfloat162_rn(0.f, 0.f);
   const __nv_bfloat162 v1 = den > 0.f ? __floats2bfloat162_rn(acc.z / den, acc.w / den) : __floats2bfloat162_rn(0.f, 0.f);
   out[0] = v0;
@@ -122,9 +125,19 @@ __global__ void __launch_bounds__(kMergeThreads) pkv_merge_kernel(const __grid_c
   }
 }
 
-cudaError_t launch_merge(const MergeParams& p, int rows, cudaStream_t stream) {
+// Partition groups per output row: the fewest (a power of two) whose first round of
+// loads covers `max_partitions`, at most one group per thread of a row's dims.
+int merge_groups(int head_dim, int max_partitions) {
+  const int most = kMergeThreads / (head_dim / 4);
+  int g = 1;
+  while (g < most && g * kMergeUnroll < max_partitions) g *= 2;
+  return g;
+}
+
+cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream) {
+  const int rows_per_cta = kMergeThreads / (p.head_dim / 4 * p.groups);
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(rows);
+  cfg.gridDim = dim3((p.rows + rows_per_cta - 1) / rows_per_cta);
   cfg.blockDim = dim3(kMergeThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;

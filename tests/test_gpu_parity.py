@@ -518,6 +518,57 @@ def test_workspace_writes_stay_inside_the_planned_bytes(bits, D, DV):
     assert_close(out.double().cpu().numpy(), oracle_out(case), f"{sp.name}")
 
 
+def merge_groups(dv, parts):
+    """Partition groups per output row the merge pass takes: the fewest g (a power of
+    two) with 4 g >= the partition count, at most 256 / (dv / 4)."""
+    g = 1
+    while g < 256 // (dv // 4) and 4 * g < parts:
+        g *= 2
+    return g
+
+
+# (bits, key dim, value dim, partitions, groups per merged row): 61 sequences of 9 query
+# heads on 3 KV heads give 549 output rows, a ragged last merge CTA for every row packing
+# (16, 8, 4, 2 or 1 rows per CTA), and a grid of several waves, so the states go through
+# the workspace and the merge kernel.
+MERGE_PACK = [(16, 64, 0, 3, 1), (16, 128, 0, 4, 1), (16, 256, 0, 2, 1), (16, 256, 0, 7, 2), (16, 64, 0, 13, 4),
+              (16, 192, 128, 6, 2), (4, 256, 0, 4, 1), (8, 128, 0, 20, 8), (16, 64, 0, 40, 16), (4, 128, 256, 9, 4)]
+
+
+@pytest.mark.parametrize("bits,D,DV,parts,groups", MERGE_PACK,
+                         ids=[f"b{b}_d{d}_{v}_p{p}" for b, d, v, p, _ in MERGE_PACK])
+def test_merge_packs_rows_and_zeroes_a_bad_length(bits, D, DV, parts, groups):
+    pt = 32
+    rng = np.random.default_rng(zlib.crc32(f"pack{bits}{D}{DV}{parts}".encode()))
+    lens = rng.integers(1, parts * pt + 1, 61)
+    lens[7] = parts * pt  # the table is exactly parts partitions wide
+    sp = spec(f"merge_pack_{bits}_{D}_{DV}_{parts}", num_seqs=61, num_q_heads=9, num_kv_heads=3, head_dim=D,
+              v_head_dim=DV, bits=bits, block_size=16 if bits == 16 else 32, lengths=tuple(int(x) for x in lens),
+              length_range=None)
+    case = make_case(sp)
+    d = case.to(DEV)
+    plan = B.make_plan(B.layout_for(d.k_pool, D, bits, v_pool=d.v_pool),
+                       B.DecodeParams(sp.num_seqs, sp.num_q_heads, 1, d.block_tables.shape[1], pt))
+    assert plan.merge_in_cluster == 0 and plan.max_partitions == parts
+    assert merge_groups(DV or D, parts) == groups
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    good = run_gpu(d, partition_tokens=pt, error_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert_close(good.double().cpu().numpy(), oracle_out(case), sp.name)
+    # a length below n_query in the middle of a packed merge CTA: that sequence's rows
+    # are zero, every other row is unchanged bit for bit
+    bad = case.to(DEV)
+    bad.seq_lens = d.seq_lens.clone()
+    bad.seq_lens[30] = 0
+    out = run_gpu(bad, partition_tokens=pt, error_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & B.PKV_DEVERR_BAD_SEQ_LEN
+    assert not out[30].float().any()
+    keep = [i for i in range(sp.num_seqs) if i != 30]
+    assert torch.equal(out[keep].view(torch.int16), good[keep].view(torch.int16))
+
+
 @pytest.mark.parametrize("pinned", [True, False], ids=["mapped_pinned", "pageable"])
 def test_one_shot_host_entry_with_pinned_and_pageable_memory(pinned):
     # mapped page-locked memory is copied by the SMs, pageable memory by the copy engine
