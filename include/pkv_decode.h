@@ -130,11 +130,29 @@ typedef struct pkv_decode_params {
                                  kernels/attention/paged.ts; bf16 pages with equal key/value head
                                  dims and at most 4 query rows per KV head, else
                                  PKV_ERR_UNSUPPORTED_SHAPE) */
+  int32_t schedule;           /* how the rows are split over the CTAs, when partition_tokens = 0:
+                                 PKV_SCHEDULE_AUTO (0): balanced for 4-bit pages where the plan
+                                 would otherwise write partition states to the workspace, else
+                                 partitions;
+                                 PKV_SCHEDULE_PARTITIONS (1): fixed-size partitions of every
+                                 (sequence, KV head);
+                                 PKV_SCHEDULE_BALANCED (2): balanced wherever it is available.
+                                 Balanced: one wave of CTAs, each of whose page groups reads an
+                                 equal run of the list of all (sequence, KV head, chunk)
+                                 triples, whatever the lengths; a run's state per (sequence, KV
+                                 head) goes to the workspace and the merge pass combines them.
+                                 Available for up to 256 sequences, the tensor-core contraction
+                                 and the unfused entry points (the fused append-and-attend call
+                                 runs partitions). Ignored when partition_tokens > 0. */
 } pkv_decode_params;
 
 #define PKV_CONTRACTION_AUTO 0
 #define PKV_CONTRACTION_TENSOR 1
 #define PKV_CONTRACTION_CUDA_CORE 2
+
+#define PKV_SCHEDULE_AUTO 0
+#define PKV_SCHEDULE_PARTITIONS 1
+#define PKV_SCHEDULE_BALANCED 2
 
 /* How a call will be carried out. */
 typedef struct pkv_plan {
@@ -153,7 +171,11 @@ typedef struct pkv_plan {
   int32_t contraction;      /* the contraction the call runs: PKV_CONTRACTION_TENSOR or
                                PKV_CONTRACTION_CUDA_CORE */
   size_t workspace_bytes;   /* device scratch for the partition states; 0 with one partition
-                               or with merge_in_cluster */
+                               or with merge_in_cluster; with balanced = 1, enough for either
+                               schedule (the fused call runs partitions) */
+  int32_t balanced;         /* 1: the balanced schedule (pkv_decode_params.schedule); then
+                               partition_tokens, max_partitions and merge_in_cluster describe the
+                               partitions the fused call would run */
 } pkv_plan;
 
 /* Makes the plan for (layout, params) on a GPU with sm_count SMs. Pure host

@@ -51,6 +51,10 @@ PKV_CONTRACTION_AUTO = 0
 PKV_CONTRACTION_TENSOR = 1
 PKV_CONTRACTION_CUDA_CORE = 2
 
+PKV_SCHEDULE_AUTO = 0
+PKV_SCHEDULE_PARTITIONS = 1
+PKV_SCHEDULE_BALANCED = 2
+
 PKV_DEVERR_BAD_BLOCK = 1
 PKV_DEVERR_BAD_SEQ_LEN = 2
 PKV_DEVERR_TIMEOUT = 4
@@ -74,13 +78,14 @@ class PoolLayout(ctypes.Structure):
 class DecodeParams(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in
                 ("num_seqs", "num_q_heads", "n_query", "max_blocks_per_seq", "partition_tokens", "window",
-                 "contraction")]
+                 "contraction", "schedule")]
 
 
 class Plan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in
                 ("partition_tokens", "max_partitions", "chunk_rows", "sm_count", "threads_per_cta",
-                 "smem_bytes", "merge_in_cluster", "contraction")] + [("workspace_bytes", ctypes.c_size_t)]
+                 "smem_bytes", "merge_in_cluster", "contraction")] + [("workspace_bytes", ctypes.c_size_t),
+                                                                      ("balanced", ctypes.c_int32)]
 
 
 _lib = None
@@ -219,7 +224,8 @@ def paged_decode_attention(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.
                            v_scales: Optional[torch.Tensor] = None, v_biases: Optional[torch.Tensor] = None,
                            partition_tokens: int = 0, window: int = 0, out: Optional[torch.Tensor] = None,
                            workspace: Optional[torch.Tensor] = None,
-                           error_flag: Optional[torch.Tensor] = None, contraction: int = 0) -> torch.Tensor:
+                           error_flag: Optional[torch.Tensor] = None, contraction: int = 0,
+                           schedule: int = 0) -> torch.Tensor:
     """Decode attention over a paged cache (see include/pkv_decode.h).
 
     q bf16 [B, HQ, N, D]; pools bf16 [NB, HK, BS, D] (bits=16) or int32 code
@@ -230,7 +236,7 @@ def paged_decode_attention(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.
     lib = load_library()
     B, HQ, N, D = q.shape
     layout = layout_for(k_pool, D, bits, group_size, v_pool)
-    params = DecodeParams(B, HQ, N, block_tables.shape[1], partition_tokens, window, contraction)
+    params = DecodeParams(B, HQ, N, block_tables.shape[1], partition_tokens, window, contraction, schedule)
     with _on_device(q.device):
         plan = _cached_plan(layout, params)
         if out is None:
@@ -254,14 +260,15 @@ def paged_decode_append_attention(q: torch.Tensor, k_new: torch.Tensor, v_new: t
                                   v_scales: Optional[torch.Tensor] = None, v_biases: Optional[torch.Tensor] = None,
                                   partition_tokens: int = 0, window: int = 0, out: Optional[torch.Tensor] = None,
                                   workspace: Optional[torch.Tensor] = None,
-                                  error_flag: Optional[torch.Tensor] = None, contraction: int = 0) -> torch.Tensor:
+                                  error_flag: Optional[torch.Tensor] = None, contraction: int = 0,
+                                  schedule: int = 0) -> torch.Tensor:
     """One decode step with its write (pkv_paged_decode_append_attention): writes
     k_new/v_new bf16 [B, HK, N, D] at cache positions seq_lens[b]-N .. seq_lens[b]-1
     (seq_lens counts the new rows), then attends as ``paged_decode_attention``."""
     lib = load_library()
     B, HQ, N, D = q.shape
     layout = layout_for(k_pool, D, bits, group_size, v_pool)
-    params = DecodeParams(B, HQ, N, block_tables.shape[1], partition_tokens, window, contraction)
+    params = DecodeParams(B, HQ, N, block_tables.shape[1], partition_tokens, window, contraction, schedule)
     with _on_device(q.device):
         plan = _cached_plan(layout, params)
         if out is None:
@@ -299,12 +306,13 @@ class HostDecodeStep:
                  v_new: Optional[torch.Tensor] = None, bits: int = 16, group_size: int = 64, k_scales=None,
                  k_biases=None, v_scales=None, v_biases=None, partition_tokens: int = 0, window: int = 0,
                  workspace: Optional[torch.Tensor] = None, error_flag: Optional[torch.Tensor] = None, stream=None,
-                 copy_tables: bool = True, contraction: int = 0):
+                 copy_tables: bool = True, contraction: int = 0, schedule: int = 0):
         self.lib = lib = load_library()
         dev = k_pool.device
         B, HQ, N, D = q.shape
         self.layout = layout_for(k_pool, D, bits, group_size, v_pool)
-        self.params = DecodeParams(B, HQ, N, block_tables.shape[1], partition_tokens, window, contraction)
+        self.params = DecodeParams(B, HQ, N, block_tables.shape[1], partition_tokens, window, contraction,
+                                   schedule)
         named = [("q", q), ("seq_lens", seq_lens)]
         if k_new is not None:
             named += [("k_new", k_new), ("v_new", v_new)]
@@ -396,14 +404,15 @@ def paged_decode_passes(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Ten
                         v_biases=None, partition_tokens: int = 0, window: int = 0,
                         out: Optional[torch.Tensor] = None,
                         workspace: Optional[torch.Tensor] = None,
-                        error_flag: Optional[torch.Tensor] = None, contraction: int = 0) -> torch.Tensor:
+                        error_flag: Optional[torch.Tensor] = None, contraction: int = 0,
+                        schedule: int = 0) -> torch.Tensor:
     """One pass of the decode: ``passes="partial"`` (pkv_paged_decode_partial) or
     ``"merge"`` (pkv_merge_partitions). ``out`` and, with more than one
     partition, ``workspace`` must be given so the two calls share them."""
     lib = load_library()
     B, HQ, N, D = q.shape
     layout = layout_for(k_pool, D, bits, group_size, v_pool)
-    params = DecodeParams(B, HQ, N, block_tables.shape[1], partition_tokens, window, contraction)
+    params = DecodeParams(B, HQ, N, block_tables.shape[1], partition_tokens, window, contraction, schedule)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     with _on_device(q.device):
         stream = torch.cuda.current_stream(q.device).cuda_stream

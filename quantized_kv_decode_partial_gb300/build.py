@@ -29,6 +29,9 @@ SOURCES = [
     "pkv_partial_bf16_cc.cu",
     "pkv_partial_u4.cu",
     "pkv_partial_u8.cu",
+    "pkv_partial_bf16_bal.cu",
+    "pkv_partial_u4_bal.cu",
+    "pkv_partial_u8_bal.cu",
 ]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]

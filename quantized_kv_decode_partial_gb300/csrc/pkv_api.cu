@@ -28,17 +28,49 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
 
-// cc: the CUDA-core contraction (bf16 pages only), else the tensor-core one.
-PartialInfo partial_info(int bits, int dk, int dv, int nq, bool solo = false, bool cc = false) {
-  if (cc) return bits == 16 ? pkv::partial_info_bf16_cc(dk, dv, nq, solo) : PartialInfo{false, 0, 0, 0, 0, 0, 0};
+// cc: the CUDA-core contraction (bf16 pages only), else the tensor-core one; bal: the
+// balanced-schedule instantiation (tensor cores, several CTAs per SM).
+PartialInfo partial_info(int bits, int dk, int dv, int nq, bool solo = false, bool cc = false, bool bal = false) {
+  if (cc) return bits == 16 ? pkv::partial_info_bf16_cc(dk, dv, nq, solo) : PartialInfo{};
+  if (bal) {
+    if (solo) return PartialInfo{};
+    if (bits == 16) return pkv::partial_info_bf16_bal(dk, dv, nq);
+    if (bits == 4) return pkv::partial_info_u4_bal(dk, dv, nq);
+    if (bits == 8) return pkv::partial_info_u8_bal(dk, dv, nq);
+    return PartialInfo{};
+  }
   if (bits == 16) return pkv::partial_info_bf16(dk, dv, nq, solo);
   if (bits == 4) return pkv::partial_info_u4(dk, dv, nq, solo);
   if (bits == 8) return pkv::partial_info_u8(dk, dv, nq, solo);
-  return PartialInfo{false, 0, 0, 0, 0, 0, 0};
+  return PartialInfo{};
 }
 
 // Value head dim of a layout (0 in the descriptor means the key head dim).
 int v_dim(const pkv_pool_layout* L) { return L->v_head_dim > 0 ? L->v_head_dim : L->head_dim; }
+
+// Balanced schedule: CTAs of instantiation `bi` one SM can hold, as far as its shared
+// memory and threads tell (228 KB per SM, 1 KB of it reserved per CTA; 2048 threads).
+// The grid launched holds at most this many per SM (the occupancy the registers allow
+// may be lower), so the workspace sized from it suffices.
+long long bal_ctas_per_sm_bound(const PartialInfo& bi) {
+  const long long by_smem = (228ll * 1024) / (bi.smem_bytes + 1024);
+  const long long by_threads = 2048 / bi.threads;
+  return std::max(1ll, std::min(std::min(by_smem, by_threads), 32ll));
+}
+
+// Workspace of the balanced schedule with `runs` page groups: a state slot per (run,
+// unit) pair that can occur, runs + units in all, each holding nq query rows: o
+// [slot][nq][DV] floats, then (m, l) [slot][nq][2].
+struct BalancedWorkspace {
+  size_t o_bytes, bytes;
+};
+BalancedWorkspace balanced_workspace(long long runs, long long units, long long nq, int dv) {
+  const size_t slots = static_cast<size_t>(runs + units) * static_cast<size_t>(nq);
+  BalancedWorkspace w;
+  w.o_bytes = (slots * dv * sizeof(float) + 255) / 256 * 256;
+  w.bytes = w.o_bytes + slots * 2 * sizeof(float);
+  return w;
+}
 
 // Stored bytes of one row of head dim `d`: bf16 values, or codes plus bf16 scale and bias.
 long long stored_row_bytes(const pkv_pool_layout* L, int d) {
@@ -74,6 +106,7 @@ int check_params(const pkv_pool_layout* L, const pkv_decode_params* P) {
     return PKV_ERR_BAD_PARAMS;
   if (static_cast<long long>(P->max_blocks_per_seq) * L->block_size >= (1ll << 31)) return PKV_ERR_BAD_PARAMS;
   if (P->contraction < PKV_CONTRACTION_AUTO || P->contraction > PKV_CONTRACTION_CUDA_CORE) return PKV_ERR_BAD_PARAMS;
+  if (P->schedule < PKV_SCHEDULE_AUTO || P->schedule > PKV_SCHEDULE_BALANCED) return PKV_ERR_BAD_PARAMS;
   const long long nq = static_cast<long long>(P->num_q_heads / L->num_kv_heads) * P->n_query;
   if (nq > 64) return PKV_ERR_UNSUPPORTED_SHAPE;
   const bool cc = P->contraction == PKV_CONTRACTION_CUDA_CORE;
@@ -189,6 +222,29 @@ int plan_impl(const pkv_pool_layout* L, const pkv_decode_params* P, int sm_count
     const size_t slots = static_cast<size_t>(P->num_seqs) * P->num_q_heads * P->n_query * max_parts;
     const size_t o_bytes = (slots * v_dim(L) * sizeof(float) + 255) / 256 * 256;
     out->workspace_bytes = o_bytes + slots * 2 * sizeof(float);
+  }
+  // Balanced schedule: with the library's choice of split, for 4-bit pages where the
+  // partitions would go through the workspace (or wherever the caller asks for it), and
+  // where there is an instantiation. The 4-bit kernels are bound by their arithmetic,
+  // which runs at the same rate on every SM, so equal runs end together and the tail of
+  // the partition waves goes away (4-bit batch layer 430.3 -> 392.7 us). The 8-bit and
+  // bf16 kernels stream at the memory's pace, which differs from SM to SM by up to a
+  // quarter; equal runs then end apart, while partition waves let the hardware hand the
+  // faster SMs more CTAs (balanced: 8-bit layer 718.8 -> 748.1 us, bf16 8 x 128K rows
+  // 609.6 -> 642.6 us). The chunk list must index in 32 bits: the longest unit reads at
+  // most the table, or with a window W + N - 1 rows plus the alignment of its first chunk.
+  out->balanced = 0;
+  if (P->partition_tokens == 0 && P->schedule != PKV_SCHEDULE_PARTITIONS && !cc &&
+      P->num_seqs <= pkv::kMaxBalancedSeqs &&
+      (P->schedule == PKV_SCHEDULE_BALANCED || (L->bits == 4 && max_parts > 1 && !out->merge_in_cluster))) {
+    const PartialInfo bi = partial_info(L->bits, L->head_dim, v_dim(L), static_cast<int>(nq), false, false, true);
+    const long long unit_chunks = (window_rows(P, max_len) + bi.chunk_rows - 1) / std::max(bi.chunk_rows, 1);
+    const long long units = static_cast<long long>(P->num_seqs) * L->num_kv_heads;
+    if (bi.exists && units * unit_chunks < (1ll << 31)) {
+      const long long runs = sms * bal_ctas_per_sm_bound(bi) * bi.page_groups;
+      out->balanced = 1;
+      out->workspace_bytes = std::max(out->workspace_bytes, balanced_workspace(runs, units, nq, v_dim(L)).bytes);
+    }
   }
   return PKV_OK;
 }
@@ -370,7 +426,7 @@ struct PreparedDecode {
   CUtensorMap tk, tv;
   dim3 grid;
   int bits, dk, dv, nq, device;
-  bool solo, cc, partial, merge;
+  bool solo, cc, bal, partial, merge;
 };
 
 // Checks the arguments of a decode call (the passes in `passes`) and prepares its
@@ -404,16 +460,29 @@ int prepare_decode(const pkv_pool_layout* layout, const pkv_decode_params* param
   bool solo = false;
   rc = plan_impl(layout, params, sms, &plan, &solo);
   if (rc) return rc;
-  const int mode = plan.max_partitions == 1 ? pkv::kModeSingle
+  const bool bal = plan.balanced && k_new == nullptr;  // the fused call runs partitions
+  const int mode = bal                       ? pkv::kModeBalanced
+                   : plan.max_partitions == 1 ? pkv::kModeSingle
                    : plan.merge_in_cluster   ? pkv::kModeCluster
                                              : pkv::kModeWorkspace;
-  if (mode == pkv::kModeWorkspace && (!workspace || workspace_bytes < plan.workspace_bytes))
-    return PKV_ERR_WORKSPACE_TOO_SMALL;
+  const bool ws_mode = mode == pkv::kModeWorkspace || mode == pkv::kModeBalanced;
+  if (ws_mode && (!workspace || workspace_bytes < plan.workspace_bytes)) return PKV_ERR_WORKSPACE_TOO_SMALL;
+  if (bal) solo = false;
 
   const int D = layout->head_dim, DV = v_dim(layout), HK = layout->num_kv_heads;
   const int nq = (params->num_q_heads / HK) * params->n_query;
   const bool cc = plan.contraction == PKV_CONTRACTION_CUDA_CORE;
-  const PartialInfo info = partial_info(layout->bits, D, DV, nq, solo, cc);
+  const PartialInfo info = partial_info(layout->bits, D, DV, nq, solo, cc, bal);
+  // Balanced schedule: one wave of CTAs, as many per SM as the instantiation's occupancy
+  // allows (within the bound the plan sized the workspace for).
+  int bal_ctas = 0;
+  if (bal) {
+    const int occ = layout->bits == 16  ? pkv::partial_bal_ctas_per_sm_bf16(D, DV, nq, dev)
+                    : layout->bits == 4 ? pkv::partial_bal_ctas_per_sm_u4(D, DV, nq, dev)
+                                        : pkv::partial_bal_ctas_per_sm_u8(D, DV, nq, dev);
+    if (occ <= 0) return cuda_fail("occupancy of the balanced partial kernel", cudaGetLastError());
+    bal_ctas = sms * static_cast<int>(std::min<long long>(occ, bal_ctas_per_sm_bound(info)));
+  }
   const long long rows = static_cast<long long>(layout->num_blocks) * HK * layout->block_size;
   const int elem = info.tensor_elem_bytes;
   const long long row_elems_k = quant ? static_cast<long long>(D) * layout->bits / 8 : D;
@@ -437,10 +506,14 @@ int prepare_decode(const pkv_pool_layout* layout, const pkv_decode_params* param
   p.v_biases = static_cast<const __nv_bfloat16*>(v_biases);
   p.out = static_cast<__nv_bfloat16*>(out);
   const size_t slots = static_cast<size_t>(params->num_seqs) * params->num_q_heads * params->n_query * plan.max_partitions;
-  const size_t o_bytes = (slots * DV * sizeof(float) + 255) / 256 * 256;  // as plan_impl sizes it
-  p.ws_o = mode == pkv::kModeWorkspace ? static_cast<float*>(workspace) : nullptr;
-  p.ws_ml = mode == pkv::kModeWorkspace ? reinterpret_cast<float*>(static_cast<char*>(workspace) + o_bytes) : nullptr;
+  const size_t o_bytes = bal ? balanced_workspace(static_cast<long long>(bal_ctas) * info.page_groups,
+                                                  static_cast<long long>(params->num_seqs) * HK, nq, DV)
+                                   .o_bytes
+                             : (slots * DV * sizeof(float) + 255) / 256 * 256;  // as plan_impl sizes it
+  p.ws_o = ws_mode ? static_cast<float*>(workspace) : nullptr;
+  p.ws_ml = ws_mode ? reinterpret_cast<float*>(static_cast<char*>(workspace) + o_bytes) : nullptr;
   p.mode = mode;
+  p.num_seqs = params->num_seqs;
   p.window = params->window;
   p.host_inputs = 0;
   p.error_flag = error_flag;
@@ -462,7 +535,7 @@ int prepare_decode(const pkv_pool_layout* layout, const pkv_decode_params* param
                           const_cast<void*>(k_biases), const_cast<void*>(v_scales), const_cast<void*>(v_biases));
   }
 
-  pd->grid = dim3(plan.max_partitions, HK, params->num_seqs);
+  pd->grid = bal ? dim3(bal_ctas) : dim3(plan.max_partitions, HK, params->num_seqs);
   pd->bits = layout->bits;
   pd->dk = D;
   pd->dv = DV;
@@ -470,8 +543,9 @@ int prepare_decode(const pkv_pool_layout* layout, const pkv_decode_params* param
   pd->device = dev;
   pd->solo = solo;
   pd->cc = cc;
+  pd->bal = bal;
   pd->partial = partial;
-  pd->merge = (passes & kPassMerge) && mode == pkv::kModeWorkspace;
+  pd->merge = (passes & kPassMerge) && ws_mode;
   if (pd->merge) {
     pkv::MergeParams& m = pd->m;
     m.ws_o = p.ws_o;
@@ -488,6 +562,16 @@ int prepare_decode(const pkv_pool_layout* layout, const pkv_decode_params* param
     m.window = params->window;
     m.rows = params->num_seqs * params->num_q_heads * params->n_query;
     m.groups = pkv::merge_groups(DV, plan.max_partitions);
+    if (bal) {
+      // a unit's runs: about its share of the page groups plus one; two groups per row
+      // take up to 8 in the first round of loads
+      m.bal_runs = bal_ctas * info.page_groups;
+      m.num_seqs = params->num_seqs;
+      m.num_kv_heads = HK;
+      m.nq = nq;
+      m.chunk_rows = info.chunk_rows;
+      m.groups = pkv::merge_groups(DV, 8);
+    }
   }
   return PKV_OK;
 }
@@ -498,7 +582,11 @@ int launch_prepared(const PreparedDecode& pd, cudaStream_t st) {
   (void)cudaGetLastError();  // start from a clean error state
   cudaError_t e = cudaSuccess;
   if (pd.partial) {
-    if (pd.cc)
+    if (pd.bal)
+      e = pd.bits == 16  ? pkv::launch_partial_bf16_bal(pd.dk, pd.dv, pd.nq, pd.p, pd.tk, pd.tv, pd.grid, st, pd.device)
+          : pd.bits == 4 ? pkv::launch_partial_u4_bal(pd.dk, pd.dv, pd.nq, pd.p, pd.tk, pd.tv, pd.grid, st, pd.device)
+                         : pkv::launch_partial_u8_bal(pd.dk, pd.dv, pd.nq, pd.p, pd.tk, pd.tv, pd.grid, st, pd.device);
+    else if (pd.cc)
       e = pkv::launch_partial_bf16_cc(pd.dk, pd.dv, pd.nq, pd.solo, pd.p, pd.tk, pd.tv, pd.grid, st, pd.device);
     else if (pd.bits == 16)
       e = pkv::launch_partial_bf16(pd.dk, pd.dv, pd.nq, pd.solo, pd.p, pd.tk, pd.tv, pd.grid, st, pd.device);

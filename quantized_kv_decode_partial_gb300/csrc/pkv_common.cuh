@@ -49,7 +49,8 @@ struct PartialParams {
   int num_blocks, num_kv_heads, block_size, max_blocks;
   int num_q_heads, n_query, nq;  // nq = (HQ/HK) * n_query rows served per KV head
   int partition_tokens, max_partitions;
-  int mode;           // kModeSingle / kModeWorkspace / kModeCluster
+  int mode;           // kModeSingle / kModeWorkspace / kModeCluster / kModeBalanced
+  int num_seqs;       // B (read by the balanced schedule)
   int window;         // sliding window in rows (0: none)
   int host_inputs;    // kHost* bits: inputs a host-driven step keeps in host memory
   float score_scale;  // softmax scale * log2(e)
@@ -73,7 +74,10 @@ constexpr int kModeSingle = 0;     // one partition: the CTA writes bf16 output
 constexpr int kModeWorkspace = 1;  // partition states go to the workspace; the merge kernel follows
 constexpr int kModeCluster = 2;    // the partitions of a (sequence, KV head) form one thread-block
                                    // cluster and merge through distributed shared memory
+constexpr int kModeBalanced = 3;   // equal runs of the flattened chunk list per page group; states to
+                                   // the workspace, one per (page group, unit) run; the merge kernel follows
 constexpr int kMaxClusterParts = 16;  // largest cluster (non-portable size)
+constexpr int kMaxBalancedSeqs = 256;  // sequences a balanced schedule takes (its prefix lives in shared memory)
 
 struct MergeParams {
   const float* ws_o;
@@ -87,6 +91,10 @@ struct MergeParams {
   int window;  // sliding window in rows (0: none)
   int rows;    // output rows (B * HQ * N)
   int groups;  // partition groups per output row (merge_groups)
+  // Balanced schedule (bal_runs > 0): the states of a unit's runs sit in consecutive
+  // workspace slots; the rest describes the partial pass's chunk list.
+  int bal_runs;  // page groups of the partial grid (0: partitions)
+  int num_seqs, num_kv_heads, nq, chunk_rows;
 };
 
 struct AppendParams {
@@ -411,6 +419,87 @@ __host__ __device__ __forceinline__ int partition_base(int len, int n_query, int
   if (window <= 0) return 0;
   const int lo = len - n_query + 1 - window;
   return lo > 0 ? lo / kWindowAlign * kWindowAlign : 0;
+}
+
+// ---- balanced schedule
+// The partial pass reads, for every (sequence b, KV head) unit, the chunks of kCh rows
+// from bal_first_row (0, or with a window the chunk boundary at or below the lowest
+// row any query sees) up to the length. Units are listed sequence-major, KV heads
+// within a sequence, chunks within a unit, giving T chunks in all; page group v of V
+// takes the run [v T / V, (v + 1) T / V) of that list, split where it crosses units.
+// The merge pass recomputes the same list from the lengths.
+__host__ __device__ __forceinline__ int bal_first_row(int len, int n_query, int window, int ch) {
+  const int lo = len - n_query + 1 - window;
+  return window > 0 && lo > 0 ? lo / ch * ch : 0;
+}
+
+// Chunks of one unit of a sequence of length len; 0 for a length the partial pass rejects.
+__host__ __device__ __forceinline__ int bal_unit_chunks(int len, int n_query, int window, int max_len, int ch) {
+  if (len < n_query || len > max_len) return 0;
+  return (len - bal_first_row(len, n_query, window, ch) + ch - 1) / ch;
+}
+
+// Fills S[0..B] with the index of each sequence's first chunk in the list (S[B] = T)
+// and lens[0..B-1] with the lengths. Called by every thread of the block; B <=
+// kMaxBalancedSeqs; ends with a block barrier.
+__device__ __forceinline__ void bal_scan(const int32_t* seq_lens, int B, int HK, int n_query, int window, int max_len,
+                                         int ch, int* S, int* lens) {
+  for (int b = threadIdx.x; b < B; b += blockDim.x) {
+    const int len = seq_lens[b];
+    lens[b] = len;
+    S[b + 1] = HK * bal_unit_chunks(len, n_query, window, max_len, ch);
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) {  // one warp: lane l sums entries 8l .. 8l+7, then a warp scan
+    constexpr int kPer = kMaxBalancedSeqs / 32;
+    const int lane = threadIdx.x;
+    int v[kPer];
+    int sum = 0;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int b = lane * kPer + j;
+      v[j] = b < B ? S[b + 1] : 0;
+      sum += v[j];
+    }
+    int incl = sum;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += n;
+    }
+    __syncwarp();  // every lane has read its entries before any lane writes
+    int run = incl - sum;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int b = lane * kPer + j;
+      if (b < B) S[b] = run;
+      run += v[j];
+    }
+    if (lane == 31) S[B] = incl;
+  }
+  __syncthreads();
+}
+
+// The sequence whose units hold chunk x (0 <= x < S[B]): the last b with S[b] <= x.
+__device__ __forceinline__ int bal_seq_of(const int* S, int B, int x) {
+  int lo = 0, hi = B;  // S[lo] <= x < S[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (S[mid] <= x) {
+      lo = mid;
+    } else {
+      hi = mid;
+    }
+  }
+  return lo;
+}
+
+// First chunk of page group v's run, and the page group whose run holds chunk x.
+__host__ __device__ __forceinline__ int bal_run_start(int v, int T, int V) {
+  return static_cast<int>(static_cast<long long>(v) * T / V);
+}
+__host__ __device__ __forceinline__ int bal_run_of(int x, int T, int V) {
+  return static_cast<int>(((static_cast<long long>(x) + 1) * V - 1) / T);
 }
 
 __device__ __forceinline__ float fast_exp2(float x) {

@@ -18,6 +18,7 @@ struct PartialInfo {
   int box_row_bytes;    // bytes of one TMA box row of the K plane (64 or 128)
   int box_row_bytes_v;  // ... of the V plane
   int tensor_elem_bytes;  // element size of the pool tensor maps (2 bf16, 1 affine codes)
+  int page_groups;        // page groups per CTA (rings of stages, each read by its query-group warps)
 };
 
 // Partial-kernel instantiation for key head dim dk, value head dim dv and `nq` query
@@ -37,6 +38,21 @@ cudaError_t launch_partial_u8(int dk, int dv, int nq, bool solo, const PartialPa
                               const CUtensorMap& tv, dim3 grid, cudaStream_t stream, int device);
 cudaError_t launch_partial_bf16_cc(int dk, int dv, int nq, bool solo, const PartialParams& p, const CUtensorMap& tk,
                                    const CUtensorMap& tv, dim3 grid, cudaStream_t stream, int device);
+
+// Balanced-schedule instantiations (kModeBalanced) for the same shapes' grids of several
+// CTAs per SM; the CTAs of one per SM on `device` (the current device; 0 on an error).
+PartialInfo partial_info_bf16_bal(int dk, int dv, int nq);
+PartialInfo partial_info_u4_bal(int dk, int dv, int nq);
+PartialInfo partial_info_u8_bal(int dk, int dv, int nq);
+int partial_bal_ctas_per_sm_bf16(int dk, int dv, int nq, int device);
+int partial_bal_ctas_per_sm_u4(int dk, int dv, int nq, int device);
+int partial_bal_ctas_per_sm_u8(int dk, int dv, int nq, int device);
+cudaError_t launch_partial_bf16_bal(int dk, int dv, int nq, const PartialParams& p, const CUtensorMap& tk,
+                                    const CUtensorMap& tv, dim3 grid, cudaStream_t stream, int device);
+cudaError_t launch_partial_u4_bal(int dk, int dv, int nq, const PartialParams& p, const CUtensorMap& tk,
+                                  const CUtensorMap& tv, dim3 grid, cudaStream_t stream, int device);
+cudaError_t launch_partial_u8_bal(int dk, int dv, int nq, const PartialParams& p, const CUtensorMap& tk,
+                                  const CUtensorMap& tv, dim3 grid, cudaStream_t stream, int device);
 
 int merge_groups(int head_dim, int max_partitions);
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream);

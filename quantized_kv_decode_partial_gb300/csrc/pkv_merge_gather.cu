@@ -52,23 +52,62 @@ __global__ void __launch_bounds__(kMergeThreads) pkv_merge_kernel(const __grid_c
   const bool live = row < p.rows;  // the last CTA may hold fewer rows
   wait_for_prerequisite_grids();   // launched early behind the partial pass; its states are ready after this
   const int b = live ? row / p.rows_per_seq : 0;
-  const int slots = live ? p.max_partitions : 0;
-  const float2* ml = reinterpret_cast<const float2*>(p.ws_ml) + static_cast<size_t>(row) * p.max_partitions;
-  const float4* ob = reinterpret_cast<const float4*>(p.ws_o + static_cast<size_t>(row) * p.max_partitions * p.head_dim + d);
-  const int ostride = p.head_dim / 4;
+  // The row's states: state i at ml[i * mstride] (m, l) and ob[i * ostride] (its four dims).
+  const float2* ml;
+  const float4* ob;
+  int mstride, ostride, np;
+  int run0 = 0, T = 0;  // balanced: the first run over the row's unit, and the list's length
+  // Whether state i exists. A balanced run over fewer chunks than page groups may be
+  // empty, and an empty run writes no state.
+  auto has_state = [&](int i) {
+    return i < np && (p.bal_runs == 0 ||
+                      bal_run_start(run0 + i, T, p.bal_runs) < bal_run_start(run0 + i + 1, T, p.bal_runs));
+  };
   float2 s[kMergeUnroll];
   float4 v[kMergeUnroll];
+  if (p.bal_runs > 0) {
+    // Balanced schedule: the runs that cover this row's unit, from the same chunk list
+    // the partial pass split. Their states sit in consecutive slots, nq rows apart.
+    __shared__ int bal_S[kMaxBalancedSeqs + 1], bal_len[kMaxBalancedSeqs];
+    bal_scan(p.seq_lens, p.num_seqs, p.num_kv_heads, p.n_query, p.window, p.max_len, p.chunk_rows, bal_S, bal_len);
+    const int in_seq = row - b * p.rows_per_seq;  // (query head, query index) within the sequence
+    const int h = in_seq / p.n_query, rep = p.rows_per_seq / p.n_query / p.num_kv_heads;
+    const int hk = h / rep, r = in_seq - hk * rep * p.n_query;  // KV head, row within its nq
+    const int n = (bal_S[b + 1] - bal_S[b]) / p.num_kv_heads;  // 0 for a rejected length: zeroed
+    const int first = bal_S[b] + hk * n;
+    T = bal_S[p.num_seqs];
+    run0 = n > 0 ? bal_run_of(first, T, p.bal_runs) : 0;
+    np = live && n > 0 ? bal_run_of(first + n - 1, T, p.bal_runs) - run0 + 1 : 0;
+    const size_t st = (static_cast<size_t>(run0) + static_cast<size_t>(b) * p.num_kv_heads + hk) * p.nq + r;
+    ml = reinterpret_cast<const float2*>(p.ws_ml) + st;
+    ob = reinterpret_cast<const float4*>(p.ws_o + st * p.head_dim + d);
+    mstride = p.nq;
+    ostride = p.nq * p.head_dim / 4;
 #pragma unroll
-  for (int u = 0; u < kMergeUnroll; ++u) {
-    const int i = grp + u * p.groups;
-    s[u] = i < slots ? ml[i] : make_float2(-INFINITY, 0.f);
-    v[u] = i < slots ? ob[static_cast<size_t>(i) * ostride] : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int u = 0; u < kMergeUnroll; ++u) {
+      const int i = grp + u * p.groups;
+      const bool has = has_state(i);
+      s[u] = has ? ml[static_cast<size_t>(i) * mstride] : make_float2(-INFINITY, 0.f);
+      v[u] = has ? ob[static_cast<size_t>(i) * ostride] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  } else {
+    const int slots = live ? p.max_partitions : 0;
+    ml = reinterpret_cast<const float2*>(p.ws_ml) + static_cast<size_t>(row) * p.max_partitions;
+    ob = reinterpret_cast<const float4*>(p.ws_o + static_cast<size_t>(row) * p.max_partitions * p.head_dim + d);
+    mstride = 1;
+    ostride = p.head_dim / 4;
+#pragma unroll
+    for (int u = 0; u < kMergeUnroll; ++u) {
+      const int i = grp + u * p.groups;
+      s[u] = i < slots ? ml[i] : make_float2(-INFINITY, 0.f);
+      v[u] = i < slots ? ob[static_cast<size_t>(i) * ostride] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    const int len = p.seq_lens[b];
+    const bool bad = len < p.n_query || len > p.max_len;  // flagged by the partial pass; the row is zeroed
+    // Slot i holds the partition of rows [base + i P, base + (i + 1) P).
+    const int base = bad ? 0 : partition_base(len, p.n_query, p.window);
+    np = live && !bad ? (len - base + p.partition_tokens - 1) / p.partition_tokens : 0;
   }
-  const int len = p.seq_lens[b];
-  const bool bad = len < p.n_query || len > p.max_len;  // flagged by the partial pass; the row is zeroed
-  // Slot i holds the partition of rows [base + i P, base + (i + 1) P).
-  const int base = bad ? 0 : partition_base(len, p.n_query, p.window);
-  const int np = live && !bad ? (len - base + p.partition_tokens - 1) / p.partition_tokens : 0;
 
   float M = -INFINITY, den = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -79,8 +118,9 @@ __global__ void __launch_bounds__(kMergeThreads) pkv_merge_kernel(const __grid_c
 #pragma unroll
     for (int u = 0; u < kMergeUnroll; ++u) {
       const int i = i0 + u * p.groups;
-      s[u] = i < np ? ml[i] : make_float2(-INFINITY, 0.f);
-      v[u] = i < np ? ob[static_cast<size_t>(i) * ostride] : make_float4(0.f, 0.f, 0.f, 0.f);
+      const bool has = has_state(i);
+      s[u] = has ? ml[static_cast<size_t>(i) * mstride] : make_float2(-INFINITY, 0.f);
+      v[u] = has ? ob[static_cast<size_t>(i) * ostride] : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
     for (int u = 0; u < kMergeUnroll; ++u) merge_one(s[u], v[u], M, den, acc);

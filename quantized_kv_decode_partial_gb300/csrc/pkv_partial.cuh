@@ -64,7 +64,7 @@ namespace pkv {
 // describe the K plane, names with one the V plane. CCQ = 0 takes the tensor-core
 // contraction; CCQ = 2 or 4 the CUDA-core one (pkv_partial_cc.cuh) for bf16 pages
 // with up to that many query rows per KV head (NT = WQ = 1).
-template <int BITS, int D, int DV, int NT, int WQ, bool SOLO, int CCQ = 0>
+template <int BITS, int D, int DV, int NT, int WQ, bool SOLO, int CCQ = 0, bool BAL = false>
 struct PartialCfg {
   static constexpr bool kQuant = BITS != 16;
   static constexpr int kElemBytes = kQuant ? 1 : 2;                    // tensor-map element size
@@ -143,11 +143,13 @@ struct PartialCfg {
   // The receive area (after the ring) is there when the CTA is alone on its SM, or when it
   // does not cost the second CTA per SM (or the CTA already has its SM to itself).
   static constexpr int kBaseSmem = kWorkBytes + kBarrierBytes + 1024;
-  static constexpr bool kPush = SOLO || kBaseSmem + kRecvNeedBytes <= 114 * 1024 ||
-                                (kBaseSmem > 114 * 1024 && kBaseSmem + kRecvNeedBytes <= 227 * 1024);
+  static constexpr bool kPush = !BAL && (SOLO || kBaseSmem + kRecvNeedBytes <= 114 * 1024 ||
+                                         (kBaseSmem > 114 * 1024 && kBaseSmem + kRecvNeedBytes <= 227 * 1024));
   static constexpr int kRecvBytes = kPush ? kRecvNeedBytes : 0;
   static constexpr int kDataBytes = kWorkBytes + kRecvBytes;
-  static constexpr int kSmemBytes = kDataBytes + kBarrierBytes + kPBufBytes + 1024;  // + alignment slack
+  // balanced schedule: the chunk-list prefix over the sequences and their lengths
+  static constexpr int kBalBytes = BAL ? (2 * kMaxBalancedSeqs + 4) * 4 : 0;
+  static constexpr int kSmemBytes = kDataBytes + kBarrierBytes + kPBufBytes + kBalBytes + 1024;  // + alignment slack
   static constexpr float kCodeUnit = 5.9604644775390625e-8f;  // 2^-24: value of fp16 bit pattern 1
 
   static_assert((kRB == 128 || kRB == 64) && (kRBV == 128 || kRBV == 64), "box rows of 64 or 128 bytes");
@@ -162,6 +164,7 @@ struct PartialCfg {
   static_assert(CCQ == 0 || (BITS == 16 && D == DV && NT == 1 && WQ == 1 && kCh == 16 && kRB == 128),
                 "CUDA-core contraction: bf16 pages, equal head dims, 128-byte rows, one warp per query group");
   static_assert(!CCQ || kWarps <= 8, "weight buffers of at most 8 warps");
+  static_assert(!BAL || (!SOLO && CCQ == 0), "balanced schedule: grids of several CTAs per SM, tensor cores");
 };
 
 // Physical head dim held by row `half` (0: g, 1: g + 8) of O^T m-tile `mt`.
@@ -304,11 +307,12 @@ __device__ __forceinline__ void load_group_row(uint32_t addr, float (&v)[G]) {
 // give every weight twice, and one transposed weight fragment serves a pair of 64-dim
 // groups: columns 0-3 carry the weights scaled by the even group's value scales, columns
 // 4-7 by the odd group's; each group's MMAs keep the columns of their own group.
-template <int BITS, int D, int DV, int NT, int WQ, bool SOLO, bool HOSTIN, int CCQ = 0, bool PV = false>
+template <int BITS, int D, int DV, int NT, int WQ, bool SOLO, bool HOSTIN, int CCQ = 0, bool PV = false,
+          bool BAL = false>
 __global__ void __maxnreg__(255)
     pkv_partial_kernel(const __grid_constant__ PartialParams p, const __grid_constant__ CUtensorMap tmap_k,
                        const __grid_constant__ CUtensorMap tmap_v) {
-  using C = PartialCfg<BITS, D, DV, NT, WQ, SOLO, CCQ>;
+  using C = PartialCfg<BITS, D, DV, NT, WQ, SOLO, CCQ, BAL>;
   static_assert(!PV || (BITS == 4 && NT == 1 && WQ == 1 && CCQ == 0 && C::kGroupsV % 2 == 0),
                 "paired value groups: 4-bit pages, one warp of 8 query columns, whole group pairs");
   extern __shared__ uint8_t smem_raw[];
@@ -317,7 +321,10 @@ __global__ void __maxnreg__(255)
   int* stage_ok = reinterpret_cast<int*>(full_bar + C::kWarps * C::kStagesPerWarp);
   volatile int* abort_flag = stage_ok + C::kWarps * C::kStagesPerWarp;
 
-  const int slot = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;  // slot: rank in the cluster / workspace
+  // slot: rank in the cluster / workspace. Under the balanced schedule (b, hk) name the
+  // unit the page group is working on, which changes along its run.
+  const int slot = BAL ? 0 : blockIdx.x;
+  int hk = BAL ? 0 : blockIdx.y, b = BAL ? 0 : blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
   const int qg = warp % WQ, pg = warp / WQ;  // query group, page group
@@ -325,7 +332,7 @@ __global__ void __maxnreg__(255)
   const bool leader = qg == 0;               // issues its page group's copies
   const int N = p.n_query;
   const int rep = p.nq / N;
-  const size_t row0 = (static_cast<size_t>(b) * p.num_q_heads + static_cast<size_t>(hk) * rep) * N;
+  size_t row0 = (static_cast<size_t>(b) * p.num_q_heads + static_cast<size_t>(hk) * rep) * N;
   const bool single = p.mode == kModeSingle;
   const bool in_cluster = p.mode == kModeCluster;
   // When launched as a programmatic dependent (grids of one CTA per SM), everything the
@@ -336,28 +343,32 @@ __global__ void __maxnreg__(255)
     prefetch_tensormap(&tmap_v);
   }
   if constexpr (!HOSTIN) wait_for_prerequisite_grids();
-  const int len = p.seq_lens[b];
-  // This lane's query values, fetched now so their latency overlaps the length's:
+  int len = BAL ? 0 : p.seq_lens[b];
+  // This lane's query values, fetched now so their latency overlaps the length's (under
+  // the balanced schedule, at the start of each unit of the run):
   // 2 * kKs words of bf16 pairs per n-tile, in the order q_load_words reads them.
   uint32_t qw[NT][2 * C::kKs];
   uint4 qcw[CCQ ? CCQ : 1];  // CUDA-core contraction: this lane's 8 dims of each query row
-  if constexpr (CCQ) {
-    const int d0 = (lane % (D / 8)) * 8;
+  auto load_q = [&]() {
+    if constexpr (CCQ) {
+      const int d0 = (lane % (D / 8)) * 8;
 #pragma unroll
-    for (int qi = 0; qi < CCQ; ++qi)
-      qcw[qi] = qi < p.nq ? ld_nc_keep_v4(p.q + (row0 + qi) * D + d0) : make_uint4(0u, 0u, 0u, 0u);
-  } else {
+      for (int qi = 0; qi < CCQ; ++qi)
+        qcw[qi] = qi < p.nq ? ld_nc_keep_v4(p.q + (row0 + qi) * D + d0) : make_uint4(0u, 0u, 0u, 0u);
+    } else {
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const int r = PV ? g & 3 : rbase + 8 * nt + g;  // PV: columns 4-7 repeat query rows 0-3
-      const __nv_bfloat16* qrow = p.q + (row0 + (r < p.nq ? r : 0)) * D;
-      q_load_words<BITS, D>(qrow, t, r < p.nq, qw[nt]);
+      for (int nt = 0; nt < NT; ++nt) {
+        const int r = PV ? g & 3 : rbase + 8 * nt + g;  // PV: columns 4-7 repeat query rows 0-3
+        const __nv_bfloat16* qrow = p.q + (row0 + (r < p.nq ? r : 0)) * D;
+        q_load_words<BITS, D>(qrow, t, r < p.nq, qw[nt]);
+      }
     }
-  }
+  };
+  if constexpr (!BAL) load_q();
   // Without a window the partition (and so this warp's first 32 chunks) does not
   // depend on len: fetch their block-table entries while len is still in flight.
   int tbl_pre = 0;
-  if (p.window == 0 && leader) {
+  if (!BAL && p.window == 0 && leader) {
     const long long r = static_cast<long long>(slot) * p.partition_tokens + (pg + lane * C::kWP) * C::kCh;
     const long long blk = r / p.block_size < p.max_blocks ? r / p.block_size : p.max_blocks - 1;
     tbl_pre = static_cast<int>(ld_nc_keep_u32(p.block_tables + static_cast<size_t>(b) * p.max_blocks + blk));
@@ -365,7 +376,7 @@ __global__ void __maxnreg__(255)
   if constexpr (HOSTIN) wait_for_prerequisite_grids();  // the host inputs are in flight; the rest may depend on it
   // Fused append: the step's new K/V rows of this (sequence, KV head) are read by the
   // warp whose chunk holds them just before it issues that chunk; fetch them now.
-  if (p.k_new != nullptr) {
+  if (!BAL && p.k_new != nullptr) {
     const size_t nrow = (static_cast<size_t>(b) * p.num_kv_heads + hk) * N;
     const int k_lines = (N * D * 2 + 127) / 128, v_lines = (N * DV * 2 + 127) / 128;
     const int i = threadIdx.x;
@@ -373,6 +384,18 @@ __global__ void __maxnreg__(255)
       prefetch_l1(reinterpret_cast<const char*>(p.k_new + nrow * D) + 128 * i);
     } else if (i < k_lines + v_lines) {
       prefetch_l1(reinterpret_cast<const char*>(p.v_new + nrow * DV) + 128 * (i - k_lines));
+    }
+  }
+  // Balanced schedule: every sequence's first chunk in the list of (sequence, KV head,
+  // chunk), and its length, in shared memory.
+  int* const bal_S = reinterpret_cast<int*>(smem + C::kDataBytes + C::kBarrierBytes + C::kPBufBytes);
+  int* const bal_len = bal_S + kMaxBalancedSeqs + 1;
+  if constexpr (BAL) {
+    bal_scan(p.seq_lens, p.num_seqs, p.num_kv_heads, N, p.window, p.max_blocks * p.block_size, C::kCh, bal_S,
+             bal_len);
+    if (blockIdx.x == 0 && p.error_flag) {  // lengths the list leaves out
+      for (int i = threadIdx.x; i < p.num_seqs; i += C::kThreads)
+        if (bal_len[i] < N || bal_len[i] > p.max_blocks * p.block_size) atomicOr(p.error_flag, kDevErrBadSeqLen);
     }
   }
   // The stage barriers do not depend on len either: set them up while it is in flight.
@@ -388,7 +411,7 @@ __global__ void __maxnreg__(255)
     if (in_cluster) cluster_arrive_relaxed();
   }
 
-  if (len < N || len > p.max_blocks * p.block_size) {
+  if (!BAL && (len < N || len > p.max_blocks * p.block_size)) {
     // Every CTA of this sequence sees the same length and leaves here (before any
     // cluster barrier); the CTA of partition 0 zeroes the outputs unless the merge
     // pass does.
@@ -404,11 +427,21 @@ __global__ void __maxnreg__(255)
   const int win_lo = p.window > 0 ? max(0, len - N + 1 - p.window) : 0;
   const int t0 = partition_base(len, N, p.window) + slot * p.partition_tokens;
   const int t_end = min(len, t0 + p.partition_tokens);
-  const bool empty = t0 >= len;
+  const bool empty = !BAL && t0 >= len;
   if (empty && !in_cluster) return;  // the merge pass never reads this partition
   // first row this CTA reads: the partition start, or the chunk holding the window's lowest row
   const int t_first = max(t0, win_lo / C::kCh * C::kCh);
   const int nchunks = empty ? 0 : (t_end - t_first + C::kCh - 1) / C::kCh;  // an empty cluster member still merges
+
+  // Balanced schedule: page group bal_v's run [x0, x1) of the chunk list.
+  int bal_v = 0, x0 = 0, x1 = 0;
+  if constexpr (BAL) {
+    const int T = bal_S[p.num_seqs];
+    const int V = static_cast<int>(gridDim.x) * C::kWP;
+    bal_v = static_cast<int>(blockIdx.x) * C::kWP + pg;
+    x0 = bal_run_start(bal_v, T, V);
+    x1 = bal_run_start(bal_v + 1, T, V);
+  }
 
   // O^T accumulators and softmax state.
   float o[C::kMt][NT][4];
@@ -425,7 +458,7 @@ __global__ void __maxnreg__(255)
     // Page group pg owns chunks pg, pg + kWP, pg + 2 kWP, ... of the partition and a
     // private ring of kStagesPerGroup stages; its leader warp issues the TMA copies
     // kStagesPerGroup chunks ahead, so no group waits on another group's progress.
-    const int my_chunks = nchunks > pg ? (nchunks - pg + C::kWP - 1) / C::kWP : 0;
+    const int my_chunks = BAL ? x1 - x0 : nchunks > pg ? (nchunks - pg + C::kWP - 1) / C::kWP : 0;
     uint64_t* my_full = full_bar + pg * C::kStagesPerGroup;
     int* my_ok = stage_ok + pg * C::kStagesPerGroup;
     uint8_t* my_ring = smem + pg * C::kStagesPerGroup * C::kStageBytes;
@@ -441,11 +474,36 @@ __global__ void __maxnreg__(255)
                  ? (ph * p.num_kv_heads + hk) * p.block_size + chunk_row(i) % p.block_size
                  : -1;
     };
-    int crd_cur = 0, tbl_next = 0;
+    // Balanced schedule: the raw block id of local chunk i (< my_chunks), with its KV head
+    // and row within the block packed into *pk as hk * block_size + row % block_size, and
+    // the TMA row coordinate from the two.
+    auto bal_entry = [&](int i, int* pk) {
+      const int x = x0 + i;
+      const int bb = bal_seq_of(bal_S, p.num_seqs, x);
+      const int n = (bal_S[bb + 1] - bal_S[bb]) / p.num_kv_heads;
+      const int rel = x - bal_S[bb];
+      const int h = rel / n;
+      const int row = bal_first_row(bal_len[bb], N, p.window, C::kCh) + (rel - h * n) * C::kCh;
+      *pk = h * p.block_size + row % p.block_size;
+      return static_cast<int>(__ldg(p.block_tables + static_cast<size_t>(bb) * p.max_blocks + row / p.block_size));
+    };
+    auto bal_coord = [&](int ph, int pk) {
+      return static_cast<unsigned>(ph) < static_cast<unsigned>(p.num_blocks) ? ph * p.num_kv_heads * p.block_size + pk
+                                                                              : -1;
+    };
+    int crd_cur = 0, tbl_next = 0, pk_next = 0;
     if (leader) {
-      const int ph0 = p.window == 0 ? tbl_pre : (lane < my_chunks ? __ldg(table + chunk_row(lane) / p.block_size) : 0);
-      tbl_next = 32 + lane < my_chunks ? __ldg(table + chunk_row(32 + lane) / p.block_size) : 0;
-      crd_cur = coord_of(ph0, lane);
+      if constexpr (BAL) {
+        int pk0 = 0;
+        const int ph0 = lane < my_chunks ? bal_entry(lane, &pk0) : 0;
+        tbl_next = 32 + lane < my_chunks ? bal_entry(32 + lane, &pk_next) : 0;
+        crd_cur = bal_coord(ph0, pk0);
+      } else {
+        const int ph0 =
+            p.window == 0 ? tbl_pre : (lane < my_chunks ? __ldg(table + chunk_row(lane) / p.block_size) : 0);
+        tbl_next = 32 + lane < my_chunks ? __ldg(table + chunk_row(32 + lane) / p.block_size) : 0;
+        crd_cur = coord_of(ph0, lane);
+      }
     }
     int issued = 0;  // chunks issued so far
 
@@ -478,12 +536,17 @@ __global__ void __maxnreg__(255)
     auto issue_next = [&](int is) {  // the leader warp, warp-uniform
       if (issued >= my_chunks) return;
       if (issued > 0 && (issued & 31) == 0) {
-        crd_cur = coord_of(tbl_next, issued + lane);
         const int k = issued + 32 + lane;
-        tbl_next = k < my_chunks ? __ldg(table + chunk_row(k) / p.block_size) : 0;
+        if constexpr (BAL) {
+          crd_cur = bal_coord(tbl_next, pk_next);
+          tbl_next = k < my_chunks ? bal_entry(k, &pk_next) : 0;
+        } else {
+          crd_cur = coord_of(tbl_next, issued + lane);
+          tbl_next = k < my_chunks ? __ldg(table + chunk_row(k) / p.block_size) : 0;
+        }
       }
       const int row = __shfl_sync(0xffffffffu, crd_cur, issued & 31);
-      if (p.k_new != nullptr) {
+      if (!BAL && p.k_new != nullptr) {
         // Fused append: the step's new rows len-N .. len-1 that fall in this chunk are
         // written into its page first (the warp writes, fences its generic-proxy stores
         // against the async proxy, then lane 0 copies the chunk). Chunks lie inside one
@@ -535,6 +598,33 @@ __global__ void __maxnreg__(255)
 #pragma unroll 1
     for (int s = 0; s < C::kStagesPerGroup; ++s)
       if (leader) issue_next(s);
+
+    int done = 0;             // local chunks consumed
+    int cs = 0;               // its stage: done mod kStagesPerGroup
+    uint32_t cs_parity = 0;   // the phase it waits for: (done / kStagesPerGroup) & 1
+    int seg_end = my_chunks;  // local index past the current unit's chunks
+    int seg_start = 0, seg_row = 0;  // balanced: local index and cache row of the unit's first chunk in the run
+    // The units of this page group's run, one at a time: one unit (its partition),
+    // except under the balanced schedule. The copies run on across units; at each
+    // unit's start the warp loads that unit's query rows, and at its end it writes the
+    // unit's state for this run to the workspace.
+#pragma unroll 1
+    for (;;) {
+    if constexpr (BAL) {
+      if (done >= my_chunks) break;
+      const int x = x0 + done;
+      b = bal_seq_of(bal_S, p.num_seqs, x);
+      const int n = (bal_S[b + 1] - bal_S[b]) / p.num_kv_heads;
+      const int rel = x - bal_S[b];
+      hk = rel / n;
+      const int off = rel - hk * n;
+      len = bal_len[b];
+      row0 = (static_cast<size_t>(b) * p.num_q_heads + static_cast<size_t>(hk) * rep) * N;
+      seg_start = done;
+      seg_end = min(my_chunks, done + n - off);
+      seg_row = bal_first_row(len, N, p.window, C::kCh) + off * C::kCh;
+      load_q();
+    }
 
     // B fragments of Q^T for every k-step, rows r = 8*nt + g of this KV head: bf16 as
     // stored for bf16 pages; for affine pages fp16, after an exact power-of-two
@@ -1022,17 +1112,14 @@ __global__ void __maxnreg__(255)
       }
     };
 
-    int done = 0;  // local chunks consumed
-    int cs = 0;               // its stage: done mod kStagesPerGroup
-    uint32_t cs_parity = 0;   // the phase it waits for: (done / kStagesPerGroup) & 1
-    for (; done < my_chunks; ++done, cs_parity ^= (cs == C::kStagesPerGroup - 1), cs = cs == C::kStagesPerGroup - 1 ? 0 : cs + 1) {
+    for (; done < seg_end; ++done, cs_parity ^= (cs == C::kStagesPerGroup - 1), cs = cs == C::kStagesPerGroup - 1 ? 0 : cs + 1) {
       const bool landed = mbar_wait_warp(smem_addr(&my_full[cs]), cs_parity, abort_flag, p.error_flag, p.wait_limit_ns);
       if (landed && my_ok[cs]) {
         uint8_t* stage = my_ring + cs * C::kStageBytes;
         const uint32_t kpl = smem_addr(stage);
         const uint32_t vpl = kpl + C::kOffV;
         const uint32_t sbq = kpl + C::kOffKs;  // scale/bias planes (affine pages)
-        const int kbase = chunk_row(done);
+        const int kbase = BAL ? seg_row + (done - seg_start) * C::kCh : chunk_row(done);
         const bool full_vis = kbase + C::kCh <= vis_base && (win == 0 || kbase >= vis_base + N - 1 - win);
         const bool stale = kbase + C::kCh > len;
         if constexpr (CCQ) {
@@ -1056,7 +1143,7 @@ __global__ void __maxnreg__(255)
         if (leader) issue_next(cs);
       }
     }
-    if (leader && done < issued && lane == 0) {
+    if (leader && done < seg_end && done < issued && lane == 0) {
       // Aborted: let this group's copies still in flight land before the ring is reused.
       for (int c = done; c < issued; ++c) {
         const uint32_t bar = smem_addr(&my_full[c % C::kStagesPerGroup]);
@@ -1118,9 +1205,66 @@ __global__ void __maxnreg__(255)
                                 corr_v[PV ? mt >> 3 : mt >> 2][nt][e & 1]);
     }
     }  // tensor-core contraction
+    if constexpr (BAL) {
+      // This run's state of the unit, into workspace slot bal_v + unit (the runs of one
+      // unit take consecutive slots): (m, l) per query row, then o. After a wait gave up,
+      // the unit and the rest of the run get a maximum of -inf (no state), which the
+      // merge pass skips.
+      const bool aborted = done < seg_end;
+      float2* const wml = reinterpret_cast<float2*>(p.ws_ml);
+      const size_t sbase = (static_cast<size_t>(bal_v) + static_cast<size_t>(b) * p.num_kv_heads + hk) * p.nq;
+      if (g == 0) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int e2 = 0; e2 < 2; ++e2) {
+            const int r = PV ? 2 * t + e2 : rbase + 8 * nt + 2 * t + e2;
+            if (r < p.nq && (!PV || t < 2))
+              wml[sbase + r] = aborted ? make_float2(-INFINITY, 0.f) : make_float2(m_run[nt][e2], l_run[nt][e2]);
+          }
+      }
+      if (aborted) {
+        for (int i = seg_end; i < my_chunks;) {
+          const int x = x0 + i;
+          const int bb = bal_seq_of(bal_S, p.num_seqs, x);
+          const int n = (bal_S[bb + 1] - bal_S[bb]) / p.num_kv_heads;
+          const int h = (x - bal_S[bb]) / n;
+          const size_t base = (static_cast<size_t>(bal_v) + static_cast<size_t>(bb) * p.num_kv_heads + h) * p.nq;
+          for (int r = rbase + lane; r < rbase + C::kNqp && r < p.nq; r += 32) wml[base + r] = make_float2(-INFINITY, 0.f);
+          i += n - (x - bal_S[bb] - h * n);
+        }
+        break;
+      }
+      // o: four (4-bit pages) or two (8-bit) consecutive head dims per store where the
+      // accumulator layout puts them in one thread, as in the combine below
+      constexpr int kRun = BITS == 4 ? 4 : BITS == 8 ? 2 : 1;
+#pragma unroll
+      for (int mt = 0; mt < C::kMt; mt += kRun)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            if (PV && ((mt >> 2) & 1) != (t >> 1)) continue;
+            const int r = PV ? (2 * t + (e & 1)) & 3 : rbase + 8 * nt + 2 * t + (e & 1);
+            if (r >= p.nq) continue;
+            float* dst = p.ws_o + (sbase + r) * DV + out_dim<BITS>(mt, e >> 1, g);
+            if constexpr (kRun == 4) {
+              *reinterpret_cast<float4*>(dst) =
+                  make_float4(o[mt][nt][e], o[mt + 1][nt][e], o[mt + 2][nt][e], o[mt + 3][nt][e]);
+            } else if constexpr (kRun == 2) {
+              *reinterpret_cast<float2*>(dst) = make_float2(o[mt][nt][e], o[mt + 1][nt][e]);
+            } else {
+              *dst = o[mt][nt][e];
+            }
+          }
+      continue;
+    }
+    break;
+    }  // units of the run
   }
 
   allow_dependent_launch();  // the merge pass may be scheduled while this epilogue runs
+  if constexpr (BAL) return;  // every state went to the workspace
   // ---- combine the page groups' states and write out. Group w's state is m[kNqAll],
   // l[kNqAll], o[kNqAll][kCoStride] at gstate(w): in its own ring region when it fits
   // there (free once the group's chunks are consumed and its copies have landed), else

@@ -22,7 +22,7 @@ PartialInfo partial_info_bf16(int dk, int dv, int nq, bool solo) {
     return info_of<16, DK_, DV_, NT_, WQ_, SOLO_>();
   PKV_BF16_INSTANCES(X)
 #undef X
-  return PartialInfo{false, 0, 0, 0, 0, 0, 0};
+  return PartialInfo{};
 }
 
 cudaError_t launch_partial_bf16(int dk, int dv, int nq, bool solo, const PartialParams& p, const CUtensorMap& tk,

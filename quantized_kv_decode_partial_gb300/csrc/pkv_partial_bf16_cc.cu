@@ -19,7 +19,7 @@ PartialInfo partial_info_bf16_cc(int dk, int dv, int nq, bool solo) {
   if (dk == D_ && q == Q_ && solo == SOLO_) return info_of<16, D_, D_, 1, 1, SOLO_, Q_>();
   PKV_BF16_CC_INSTANCES(X)
 #undef X
-  return PartialInfo{false, 0, 0, 0, 0, 0, 0};
+  return PartialInfo{};
 }
 
 cudaError_t launch_partial_bf16_cc(int dk, int dv, int nq, bool solo, const PartialParams& p, const CUtensorMap& tk,

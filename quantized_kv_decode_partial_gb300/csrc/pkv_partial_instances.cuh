@@ -10,36 +10,37 @@
 namespace pkv {
 namespace {
 
-template <int BITS, int D, int DV, int NT, int WQ, bool SOLO, int CCQ = 0>
+template <int BITS, int D, int DV, int NT, int WQ, bool SOLO, int CCQ = 0, bool BAL = false>
 PartialInfo info_of() {
-  using C = PartialCfg<BITS, D, DV, NT, WQ, SOLO, CCQ>;
-  return PartialInfo{true, C::kThreads, C::kSmemBytes, C::kCh, C::kRB, C::kRBV, C::kElemBytes};
+  using C = PartialCfg<BITS, D, DV, NT, WQ, SOLO, CCQ, BAL>;
+  return PartialInfo{true, C::kThreads, C::kSmemBytes, C::kCh, C::kRB, C::kRBV, C::kElemBytes, C::kWP};
 }
 
 // Devices on which an instantiation's function attributes are set (bit per device < 64).
-template <int BITS, int D, int DV, int NT, int WQ, bool SOLO, bool HOSTIN, int CCQ, bool PV>
+template <int BITS, int D, int DV, int NT, int WQ, bool SOLO, bool HOSTIN, int CCQ, bool PV, bool BAL>
 std::atomic<unsigned long long> g_configured{0};
 
-template <int BITS, int D, int DV, int NT, int WQ, bool SOLO, bool HOSTIN, int CCQ = 0, bool PV = false>
+template <int BITS, int D, int DV, int NT, int WQ, bool SOLO, bool HOSTIN, int CCQ = 0, bool PV = false,
+          bool BAL = false>
 cudaError_t configure_once(int device) {
-  using C = PartialCfg<BITS, D, DV, NT, WQ, SOLO, CCQ>;
-  auto kern = pkv_partial_kernel<BITS, D, DV, NT, WQ, SOLO, HOSTIN, CCQ, PV>;
+  using C = PartialCfg<BITS, D, DV, NT, WQ, SOLO, CCQ, BAL>;
+  auto kern = pkv_partial_kernel<BITS, D, DV, NT, WQ, SOLO, HOSTIN, CCQ, PV, BAL>;
   const unsigned long long bit = device >= 0 && device < 64 ? (1ull << device) : 0ull;
-  if (bit && (g_configured<BITS, D, DV, NT, WQ, SOLO, HOSTIN, CCQ, PV>.load(std::memory_order_acquire) & bit))
+  if (bit && (g_configured<BITS, D, DV, NT, WQ, SOLO, HOSTIN, CCQ, PV, BAL>.load(std::memory_order_acquire) & bit))
     return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);  // clusters of up to 16
   if (e != cudaSuccess) return e;
-  if (bit) g_configured<BITS, D, DV, NT, WQ, SOLO, HOSTIN, CCQ, PV>.fetch_or(bit, std::memory_order_acq_rel);
+  if (bit) g_configured<BITS, D, DV, NT, WQ, SOLO, HOSTIN, CCQ, PV, BAL>.fetch_or(bit, std::memory_order_acq_rel);
   return cudaSuccess;
 }
 
-template <int BITS, int D, int DV, int NT, int WQ, bool SOLO, int CCQ = 0, bool PV = false>
+template <int BITS, int D, int DV, int NT, int WQ, bool SOLO, int CCQ = 0, bool PV = false, bool BAL = false>
 cudaError_t launch_of(const PartialParams& p, const CUtensorMap& tk, const CUtensorMap& tv, dim3 grid,
                       cudaStream_t stream, int device) {
-  using C = PartialCfg<BITS, D, DV, NT, WQ, SOLO, CCQ>;
-  auto kern = pkv_partial_kernel<BITS, D, DV, NT, WQ, SOLO, false, CCQ, PV>;
+  using C = PartialCfg<BITS, D, DV, NT, WQ, SOLO, CCQ, BAL>;
+  auto kern = pkv_partial_kernel<BITS, D, DV, NT, WQ, SOLO, false, CCQ, PV, BAL>;
   cudaError_t e;
   // A grid of one CTA per SM launches as a programmatic dependent (below); when all of
   // its length, query and block tables are host memory of a host-driven step, the
@@ -53,7 +54,7 @@ cudaError_t launch_of(const PartialParams& p, const CUtensorMap& tk, const CUten
       e = configure_once<BITS, D, DV, NT, WQ, SOLO, false, CCQ, PV>(device);
     }
   } else {
-    e = configure_once<BITS, D, DV, NT, WQ, SOLO, false, CCQ, PV>(device);
+    e = configure_once<BITS, D, DV, NT, WQ, SOLO, false, CCQ, PV, BAL>(device);
   }
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg{};
@@ -82,6 +83,27 @@ cudaError_t launch_of(const PartialParams& p, const CUtensorMap& tk, const CUten
     ++cfg.numAttrs;
   }
   return cudaLaunchKernelEx(&cfg, kern, p, tk, tv);
+}
+
+// CTAs of the balanced-schedule instantiation that one SM of `device` (the current
+// device) holds at once; 0 on an error.
+template <int BITS, int D, int DV, int NT, int WQ, bool PV = false>
+int bal_ctas_per_sm(int device) {
+  using C = PartialCfg<BITS, D, DV, NT, WQ, false, 0, true>;
+  static std::atomic<int> known[64];  // per device < 64, 0 until first asked
+  const bool cache = device >= 0 && device < 64;
+  if (cache) {
+    const int n = known[device].load(std::memory_order_relaxed);
+    if (n > 0) return n;
+  }
+  if (configure_once<BITS, D, DV, NT, WQ, false, false, 0, PV, true>(device) != cudaSuccess) return 0;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+          &n, pkv_partial_kernel<BITS, D, DV, NT, WQ, false, false, 0, PV, true>, C::kThreads, C::kSmemBytes) !=
+      cudaSuccess)
+    return 0;
+  if (cache && n > 0) known[device].store(n, std::memory_order_relaxed);
+  return n;
 }
 
 // Instantiation for `nq` query rows per KV head: NT n-tiles of 8 rows per warp and

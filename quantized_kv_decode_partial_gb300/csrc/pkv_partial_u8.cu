@@ -20,7 +20,7 @@ PartialInfo partial_info_u8(int dk, int dv, int nq, bool solo) {
     return info_of<8, DK_, DV_, NT_, WQ_, SOLO_>();
   PKV_U8_INSTANCES(X)
 #undef X
-  return PartialInfo{false, 0, 0, 0, 0, 0, 0};
+  return PartialInfo{};
 }
 
 cudaError_t launch_partial_u8(int dk, int dv, int nq, bool solo, const PartialParams& p, const CUtensorMap& tk,

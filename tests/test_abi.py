@@ -308,3 +308,75 @@ def test_contraction_field_is_validated(lib):
     for bad in (-1, 3):
         par = B.DecodeParams(1, 2, 1, 4, 64, 0, bad)
         assert lib.pkv_make_plan(ctypes.byref(lay), ctypes.byref(par), 152, ctypes.byref(plan)) == B.PKV_ERR_BAD_PARAMS
+
+
+def test_schedule_field_is_validated(lib):
+    lay = B.PoolLayout(100, 1, 32, 128, 16, 64)
+    plan = B.Plan()
+    for bad in (-1, 3):
+        par = B.DecodeParams(1, 2, 1, 4, 64, 0, 0, bad)
+        assert lib.pkv_make_plan(ctypes.byref(lay), ctypes.byref(par), 152, ctypes.byref(plan)) == B.PKV_ERR_BAD_PARAMS
+
+
+def _balanced_bytes(runs, units, nq, dv):
+    slots = (runs + units) * nq
+    return -(-slots * dv * 4 // 256) * 256 + slots * 2 * 4
+
+
+@pytest.mark.parametrize("name", sorted(WORKLOADS))
+def test_balanced_schedule_where_partitions_would_use_the_workspace(lib, name):
+    # The library's split (partition_tokens = 0) of a 4-bit workload whose partitions would
+    # go through the workspace and the merge kernel takes the balanced schedule; its
+    # workspace then holds a state slot per (run, unit) pair for the largest grid the
+    # shared memory allows (runs = SMs x CTAs per SM x page groups), and the partitions'
+    # states as well (the fused call runs those).
+    sp = WORKLOADS[name]
+    lmax = max(sp.lengths) if sp.lengths else sp.length_range[1]
+    max_blocks = -(-lmax // sp.block_size)
+    auto = B.make_plan(_layout(sp), _params(sp, max_blocks, 0), sm_count=152)
+    parts = B.make_plan(_layout(sp), B.DecodeParams(sp.num_seqs, sp.num_q_heads, sp.n_query, max_blocks, 0,
+                                                    sp.window, 0, B.PKV_SCHEDULE_PARTITIONS), sm_count=152)
+    assert parts.balanced == 0
+    workspace_partitions = parts.max_partitions > 1 and not parts.merge_in_cluster
+    assert auto.balanced == int(workspace_partitions and sp.bits == 4)
+    assert (auto.partition_tokens, auto.max_partitions, auto.merge_in_cluster) == \
+        (parts.partition_tokens, parts.max_partitions, parts.merge_in_cluster)
+    if auto.balanced:
+        per_sm = max(1, min(228 * 1024 // (auto.smem_bytes + 1024), 2048 // auto.threads_per_cta, 32))
+        nq = sp.rep * sp.n_query
+        wq = 8 if auto.threads_per_cta == 256 and nq > 32 else 1  # a query group of 8 warps is its CTA
+        page_groups = auto.threads_per_cta // 32 // wq
+        need = _balanced_bytes(152 * per_sm * page_groups, sp.num_seqs * sp.num_kv_heads, nq, sp.dv)
+        assert auto.workspace_bytes >= max(need, parts.workspace_bytes)
+    else:
+        assert auto.workspace_bytes == parts.workspace_bytes
+
+
+def test_balanced_schedule_conditions(lib):
+    # 4-bit pages, one KV head of 4 query heads, tables of 8192 rows: 64 to 257 units, so
+    # the library's split makes several partitions per unit, several waves of CTAs
+    lay = B.PoolLayout(4096, 1, 32, 128, 4, 64)
+
+    def plan(num_seqs, partition=0, schedule=0, contraction=0):
+        return B.make_plan(lay, B.DecodeParams(num_seqs, 4, 1, 256, partition, 0, contraction, schedule),
+                           sm_count=152)
+
+    assert plan(64).balanced == 1 and plan(64).max_partitions > 1
+    assert plan(64, partition=1024).balanced == 0        # a caller's partition size is kept
+    assert plan(64, schedule=B.PKV_SCHEDULE_PARTITIONS).balanced == 0
+    assert plan(256).balanced == 1
+    assert plan(257).balanced == 0                       # more sequences than the prefix holds
+    # bf16 pages stream at the memory's pace: partitions, unless asked for; never with the
+    # CUDA-core contraction
+    bf16 = B.PoolLayout(4096, 1, 16, 128, 16, 64)
+    assert B.make_plan(bf16, B.DecodeParams(64, 4, 1, 512, 0, 0), sm_count=152).balanced == 0
+    assert B.make_plan(bf16, B.DecodeParams(64, 4, 1, 512, 0, 0, 0, B.PKV_SCHEDULE_BALANCED),
+                       sm_count=152).balanced == 1
+    assert B.make_plan(bf16, B.DecodeParams(64, 4, 1, 512, 0, 0, B.PKV_CONTRACTION_CUDA_CORE,
+                                            B.PKV_SCHEDULE_BALANCED), sm_count=152).balanced == 0
+    # one sequence of 8 KV heads and 4096 rows: 16 partitions per head merge in a cluster
+    lay8 = B.PoolLayout(4096, 8, 16, 128, 16, 64)
+    one = B.make_plan(lay8, B.DecodeParams(1, 8, 1, 256, 0, 0), sm_count=152)
+    assert one.merge_in_cluster == 1 and one.balanced == 0 and one.workspace_bytes == 0
+    forced = B.make_plan(lay8, B.DecodeParams(1, 8, 1, 256, 0, 0, 0, B.PKV_SCHEDULE_BALANCED), sm_count=152)
+    assert forced.balanced == 1 and forced.merge_in_cluster == 1 and forced.workspace_bytes > 0

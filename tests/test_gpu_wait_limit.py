@@ -32,14 +32,17 @@ def spec(name, **kw):
 
 # The finishing forms of the partial pass: partition states through the workspace and
 # the merge kernel (many CTAs per SM; bf16 and 8-bit pages), a thread-block cluster merge
-# (one CTA per SM), query rows shared by several warps, and a single partition writing
-# the output. Every case streams enough K/V per SM that its warps wait on HBM.
+# (one CTA per SM), query rows shared by several warps, a single partition writing the
+# output, and the balanced schedule (the library's own split of a batch; a page group
+# that gives up marks the rest of its run as empty). Every case streams enough K/V per
+# SM that its warps wait on HBM.
 CASES = [
     (spec("wait_bf16_workspace"), 256),
     (spec("wait_u8_workspace", head_dim=256, bits=8, block_size=32), 512),
     (spec("wait_bf16_cluster", num_seqs=1, lengths=(131072,), length_range=None, pool_factor=1.0), 8192),
     (spec("wait_bf16_query_groups", num_seqs=32, num_kv_heads=1), 1024),
     (spec("wait_bf16_single", num_seqs=32, length_range=(2000, 4000)), 8192),
+    (spec("wait_u4_balanced", head_dim=256, bits=4, block_size=32, num_seqs=32), 0),
 ]
 
 
@@ -50,8 +53,9 @@ def test_cases_take_the_finishing_forms_they_name():
         layout = B.PoolLayout(1 << 16, sp.num_kv_heads, sp.block_size, sp.head_dim, sp.bits, 64)
         plan = B.make_plan(layout, B.DecodeParams(sp.num_seqs, sp.num_q_heads, 1, max_blocks, partition),
                            sm_count=torch.cuda.get_device_properties(DEV).multi_processor_count)
-        forms.append("single" if plan.max_partitions == 1 else "cluster" if plan.merge_in_cluster else "workspace")
-    assert forms == ["workspace", "workspace", "cluster", "workspace", "single"]
+        forms.append("balanced" if plan.balanced else "single" if plan.max_partitions == 1
+                     else "cluster" if plan.merge_in_cluster else "workspace")
+    assert forms == ["workspace", "workspace", "cluster", "workspace", "single", "balanced"]
 
 
 @pytest.mark.parametrize("sp,partition", CASES, ids=[s.name for s, _ in CASES])
