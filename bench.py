@@ -59,6 +59,9 @@ def parse_args(argv=None):
     ap.add_argument("--record-traffic", nargs="+", metavar="NCU_CSV",
                     help="store the DRAM bytes of one step of --workload, summed over these ncu CSV logs, in "
                          "profiles/dram_traffic.json for the current kernel sources, and exit")
+    ap.add_argument("--schedule", choices=["auto", "partitions", "balanced"], default="auto",
+                    help="how rows are split over the CTAs: the library's choice, partitions of every (sequence, KV "
+                         "head), or equal runs of the whole chunk list (pkv_decode_params.schedule)")
     ap.add_argument("--contraction", choices=["auto", "tensor", "cuda_core"], default="auto",
                     help="the contraction the kernels run: the library's choice, tensor-core MMA, or per-lane "
                          "f32 FMAs with warp-shuffle reductions (bf16 pages, at most 4 query rows per KV head)")
@@ -69,6 +72,7 @@ def parse_args(argv=None):
 
 
 CONTRACTIONS = {"auto": 0, "tensor": 1, "cuda_core": 2}
+SCHEDULES = {"auto": 0, "partitions": 1, "balanced": 2}
 
 
 def workload_specs(name):
@@ -489,7 +493,8 @@ def run_ours(args):
                                     lengths=base.lens_host) for c in range(copies - 1)]
         layout = layout_for(base.k_pool, sp.head_dim, sp.bits, sp.group_size, v_pool=base.v_pool)
         params = DecodeParams(sp.num_seqs, sp.num_q_heads, sp.n_query, base.block_tables.shape[1],
-                              base.partition_tokens, sp.window, CONTRACTIONS[args.contraction])
+                              base.partition_tokens, sp.window, CONTRACTIONS[args.contraction],
+                              SCHEDULES[args.schedule])
         plan = make_plan(layout, params)
         ws = torch.empty(max(1, plan.workspace_bytes), dtype=torch.uint8, device=dev)
         out = torch.empty(base.q.shape[:-1] + (sp.dv,), dtype=base.q.dtype, device=dev)
@@ -509,7 +514,8 @@ def run_ours(args):
         sp = L["spec"]
         kw = dict(bits=sp.bits, group_size=sp.group_size, k_scales=c.k_scales, k_biases=c.k_biases,
                   v_scales=c.v_scales, v_biases=c.v_biases, partition_tokens=c.partition_tokens, window=sp.window,
-                  out=L["out"], workspace=L["ws"], contraction=CONTRACTIONS[args.contraction])
+                  out=L["out"], workspace=L["ws"], contraction=CONTRACTIONS[args.contraction],
+                  schedule=SCHEDULES[args.schedule])
         if args.step == "fused":
             paged_decode_append_attention(c.q, c.k_new, c.v_new, c.k_pool, c.v_pool, c.block_tables, c.seq_lens,
                                           c.scale, **kw)
@@ -607,7 +613,8 @@ def run_ours(args):
             k_new=c.k_new if args.step == "fused" else None, v_new=c.v_new if args.step == "fused" else None,
             bits=sp.bits, group_size=sp.group_size, k_scales=c.k_scales, k_biases=c.k_biases, v_scales=c.v_scales,
             v_biases=c.v_biases, partition_tokens=c.partition_tokens, window=sp.window, workspace=L["ws"],
-            stream=stream, contraction=CONTRACTIONS[args.contraction]) for c in L["insts"]])
+            stream=stream, contraction=CONTRACTIONS[args.contraction], schedule=SCHEDULES[args.schedule])
+            for c in L["insts"]])
     h2d = sum(hs[0].h2d_bytes for hs in host_steps)
     d2h = sum(hs[0].d2h_bytes for hs in host_steps)
     e2e_steps = min(K, max(50, n_copies))
@@ -637,7 +644,10 @@ def run_ours(args):
     part_ms = ms_partial / K
     peak, peak_kind = measured_hbm_peak()
     achieved = step_bytes / (part_ms * 1e-3) / 1e9
-    launches_per_step = sum(1 + (L["plan"].max_partitions > 1 and not L["plan"].merge_in_cluster) for L in layers)
+    # the merge kernel runs after a partial pass through the workspace: balanced (not for the
+    # fused step, which runs partitions), or partitions that do not merge in a cluster
+    launches_per_step = sum(1 + ((L["plan"].balanced and args.step == "decode") or
+                                 (L["plan"].max_partitions > 1 and not L["plan"].merge_in_cluster)) for L in layers)
     if rank == 0:
         sp0 = layers[0]["spec"]
         line = {
@@ -659,6 +669,8 @@ def run_ours(args):
                          "every (sequence, KV head) are written into their pages, then the grown cache is read"),
                 "parallelism": f"dp{world} (independent instances)",
                 "contraction": ["cuda cores" if L["plan"].contraction == 2 else "tensor cores" for L in layers],
+                "schedule": ["balanced" if L["plan"].balanced and args.step == "decode" else "partitions"
+                             for L in layers],
             },
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": recorded_traffic(args.workload, args.step),
@@ -718,7 +730,8 @@ def run_profile_calls(args):
             paged_decode_attention(c.q, c.k_pool, c.v_pool, c.block_tables, c.seq_lens, c.scale, bits=sp.bits,
                                    group_size=sp.group_size, k_scales=c.k_scales, k_biases=c.k_biases,
                                    v_scales=c.v_scales, v_biases=c.v_biases, partition_tokens=c.partition_tokens,
-                                   window=sp.window, contraction=CONTRACTIONS[args.contraction])
+                                   window=sp.window, contraction=CONTRACTIONS[args.contraction],
+                                   schedule=SCHEDULES[args.schedule])
         torch.cuda.synchronize()
         print(json.dumps({"profile_calls": args.profile_calls, "workload": sp.name, "num_seqs": sp.num_seqs,
                           "kv_bytes_per_call": required_kv_bytes(sp, c.lens_host)}), flush=True)
