@@ -85,15 +85,19 @@ def workload_specs(name):
 
 
 def kernel_source_hash():
-    """Hash of the CUDA sources: DRAM traffic recorded for one version of the kernels
-    applies to that version only."""
+    """Hash of the CUDA sources' code (comments and blank lines left out): DRAM traffic
+    recorded for one version of the kernels applies to that version only."""
     import hashlib
+    import re
     csrc = os.path.join(ROOT, "quantized_kv_decode_partial_gb300", "csrc")
     h = hashlib.sha256()
     for name in sorted(os.listdir(csrc)):
         if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+            with open(os.path.join(csrc, name), encoding="utf-8") as f:
+                text = re.sub(r"/\*.*?\*/", "", f.read(), flags=re.S)  # the sources hold no "//" or "/*" in strings
+            lines = [re.sub(r"//.*", "", line).rstrip() for line in text.splitlines()]
+            code = "\n".join(line for line in lines if line)
+            h.update(name.encode() + b"\0" + code.encode())
     return h.hexdigest()[:16]
 
 

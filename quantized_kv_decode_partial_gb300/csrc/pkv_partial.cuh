@@ -7,7 +7,10 @@
 // kvq4-decode.ts partial kernel): for every query row served by its KV head, the
 // running maximum of the scores, the normaliser and the unnormalised output over
 // the partition's visible keys. With a single partition the CTA finishes the
-// softmax itself and writes bf16 output.
+// softmax itself and writes bf16 output. Under the balanced schedule (BAL) a CTA
+// instead serves one wave's share of the list of all (sequence, KV head, chunk)
+// triples: each of its page groups reads an equal run of that list and writes one
+// such state per (sequence, KV head) the run crosses.
 //
 // Design (GB300):
 //  * Four warps per CTA (six or eight for grids of at most one CTA per SM); with W warps,
