@@ -112,7 +112,7 @@ typedef struct pkv_pool_layout {
 /* Per-call decode parameters. */
 typedef struct pkv_decode_params {
   int32_t num_seqs;           /* B, > 0 */
-  int32_t num_q_heads;        /* HQ, a multiple of num_kv_heads */
+  int32_t num_q_heads;        /* HQ, a multiple of num_kv_heads; num_seqs * HQ * n_query < 2^31 */
   int32_t n_query;            /* N >= 1 new query rows per sequence */
   int32_t max_blocks_per_seq; /* row stride of block_tables, > 0 */
   int32_t partition_tokens;   /* rows per partition: 0 = chosen from lengths and SM count;

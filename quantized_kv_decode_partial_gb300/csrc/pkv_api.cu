@@ -107,6 +107,8 @@ int check_params(const pkv_pool_layout* L, const pkv_decode_params* P) {
   if (static_cast<long long>(P->max_blocks_per_seq) * L->block_size >= (1ll << 31)) return PKV_ERR_BAD_PARAMS;
   if (P->contraction < PKV_CONTRACTION_AUTO || P->contraction > PKV_CONTRACTION_CUDA_CORE) return PKV_ERR_BAD_PARAMS;
   if (P->schedule < PKV_SCHEDULE_AUTO || P->schedule > PKV_SCHEDULE_BALANCED) return PKV_ERR_BAD_PARAMS;
+  // output rows (and the merge grid) are counted in int
+  if (static_cast<long long>(P->num_seqs) * P->num_q_heads * P->n_query >= (1ll << 31)) return PKV_ERR_BAD_PARAMS;
   const long long nq = static_cast<long long>(P->num_q_heads / L->num_kv_heads) * P->n_query;
   if (nq > 64) return PKV_ERR_UNSUPPORTED_SHAPE;
   const bool cc = P->contraction == PKV_CONTRACTION_CUDA_CORE;

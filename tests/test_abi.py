@@ -310,6 +310,14 @@ def test_contraction_field_is_validated(lib):
         assert lib.pkv_make_plan(ctypes.byref(lay), ctypes.byref(par), 152, ctypes.byref(plan)) == B.PKV_ERR_BAD_PARAMS
 
 
+def test_output_rows_past_int32_are_rejected(lib):
+    lay = B.PoolLayout(100, 65535, 16, 64, 16, 64)
+    plan = B.Plan()
+    # 65535 sequences x 65535 query heads: 4.3e9 output rows
+    par = B.DecodeParams(65535, 65535, 1, 4, 64, 0)
+    assert lib.pkv_make_plan(ctypes.byref(lay), ctypes.byref(par), 152, ctypes.byref(plan)) == B.PKV_ERR_BAD_PARAMS
+
+
 def test_schedule_field_is_validated(lib):
     lay = B.PoolLayout(100, 1, 32, 128, 16, 64)
     plan = B.Plan()
