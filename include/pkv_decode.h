@@ -102,7 +102,11 @@ extern "C" {
 typedef struct pkv_pool_layout {
   int32_t num_blocks;   /* blocks in the pool, > 0 */
   int32_t num_kv_heads; /* HK, > 0 */
-  int32_t block_size;   /* BS: rows per block; a multiple of 16 (bf16) or 32 (affine) */
+  int32_t block_size;   /* BS: rows per block; a multiple of the chunk the kernels stage (16 rows
+                           bf16, 32 affine), or 8 (bf16) / 8 or 16 (affine) rows, a chunk then
+                           spanning several blocks: such pools run partitions (not the balanced
+                           schedule), and neither the CUDA-core contraction nor the fused
+                           append-and-attend call takes them (PKV_ERR_UNSUPPORTED_SHAPE) */
   int32_t head_dim;     /* D: key (and query) head dim */
   int32_t bits;         /* 16 = bf16 pages; 4 or 8 = affine codes */
   int32_t group_size;   /* affine group; must be 64 (ignored for bf16) */

@@ -32,6 +32,9 @@ SOURCES = [
     "pkv_partial_bf16_bal.cu",
     "pkv_partial_u4_bal.cu",
     "pkv_partial_u8_bal.cu",
+    "pkv_partial_bf16_pc.cu",
+    "pkv_partial_u4_pc.cu",
+    "pkv_partial_u8_pc.cu",
 ]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]

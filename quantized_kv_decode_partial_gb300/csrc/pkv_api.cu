@@ -91,7 +91,10 @@ int check_layout(const pkv_pool_layout* L) {
     if (L->head_dim != 128 && L->head_dim != 256) return PKV_ERR_BAD_LAYOUT;
     if (v_dim(L) != 128 && v_dim(L) != 256) return PKV_ERR_BAD_LAYOUT;
   }
-  if (L->block_size % chunk_rows_of(L->bits)) return PKV_ERR_BAD_LAYOUT;
+  // Blocks of whole chunks, or smaller blocks of 8 or more rows that divide a chunk (a
+  // chunk then spans several blocks and is copied block by block).
+  const int ch = chunk_rows_of(L->bits);
+  if (L->block_size % ch && (ch % L->block_size || L->block_size < 8)) return PKV_ERR_BAD_LAYOUT;
   const long long rows = static_cast<long long>(L->num_blocks) * L->num_kv_heads * L->block_size;
   if (rows >= (1ll << 31)) return PKV_ERR_BAD_LAYOUT;  // TMA row coordinates are int32
   if (L->num_kv_heads > 65535) return PKV_ERR_BAD_LAYOUT;
@@ -198,9 +201,15 @@ int plan_impl(const pkv_pool_layout* L, const pkv_decode_params* P, int sm_count
   // per CTA, where there is one for this shape.
   const long long sms = sm_count > 0 ? sm_count : 1;
   const long long ctas = static_cast<long long>(P->num_seqs) * L->num_kv_heads * max_parts;
+  // Blocks smaller than the chunk the grids of several CTAs per SM stage: those grids'
+  // instantiations for such pools (no CTA-alone variant, no balanced schedule, no
+  // CUDA-core contraction).
+  const bool pieces =
+      L->block_size < partial_info(L->bits, L->head_dim, v_dim(L), static_cast<int>(nq), false, false).chunk_rows;
+  if (pieces && P->contraction == PKV_CONTRACTION_CUDA_CORE) return PKV_ERR_UNSUPPORTED_SHAPE;
   const bool cc = use_cuda_cores(L, P, ctas, sm_count);
-  const bool use_solo =
-      ctas <= sms && partial_info(L->bits, L->head_dim, v_dim(L), static_cast<int>(nq), true, cc).exists;
+  const bool use_solo = !pieces && ctas <= sms &&
+                        partial_info(L->bits, L->head_dim, v_dim(L), static_cast<int>(nq), true, cc).exists;
   if (solo) *solo = use_solo;
   const PartialInfo info = partial_info(L->bits, L->head_dim, v_dim(L), static_cast<int>(nq), use_solo, cc);
   out->contraction = cc ? PKV_CONTRACTION_CUDA_CORE : PKV_CONTRACTION_TENSOR;
@@ -236,7 +245,7 @@ int plan_impl(const pkv_pool_layout* L, const pkv_decode_params* P, int sm_count
   // 609.6 -> 642.6 us). The chunk list must index in 32 bits: the longest unit reads at
   // most the table, or with a window W + N - 1 rows plus the alignment of its first chunk.
   out->balanced = 0;
-  if (P->partition_tokens == 0 && P->schedule != PKV_SCHEDULE_PARTITIONS && !cc &&
+  if (P->partition_tokens == 0 && P->schedule != PKV_SCHEDULE_PARTITIONS && !cc && !pieces &&
       P->num_seqs <= pkv::kMaxBalancedSeqs &&
       (P->schedule == PKV_SCHEDULE_BALANCED || (L->bits == 4 && max_parts > 1 && !out->merge_in_cluster))) {
     const PartialInfo bi = partial_info(L->bits, L->head_dim, v_dim(L), static_cast<int>(nq), false, false, true);
@@ -291,8 +300,11 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 // pitch, then the segment width). One box takes `box_rows` rows of every segment and
 // lands segment-major ([segment][row][box_row_bytes], swizzled to match), so a chunk
 // of a plane is one TMA copy whatever its width.
+// The box is box_rows rows of every segment of a row (one copy per chunk), or with
+// one_segment, of a single segment (blocks smaller than a chunk: one copy per block piece
+// and segment).
 int encode_pool_tensor_map(CUtensorMap* map, const void* base, int elem_bytes, long long row_elems, long long rows,
-                           int box_row_bytes, int box_rows) {
+                           int box_row_bytes, int box_rows, bool one_segment) {
   auto encode = tensor_map_encoder();
   if (!encode) {
     std::snprintf(g_cuda_error, sizeof(g_cuda_error), "cuTensorMapEncodeTiled entry point unavailable");
@@ -305,7 +317,7 @@ int encode_pool_tensor_map(CUtensorMap* map, const void* base, int elem_bytes, l
                         static_cast<cuuint64_t>(segments)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(box_row_bytes)};
   cuuint32_t box[3] = {static_cast<cuuint32_t>(box_row_bytes / elem_bytes), static_cast<cuuint32_t>(box_rows),
-                       static_cast<cuuint32_t>(segments)};
+                       static_cast<cuuint32_t>(one_segment ? 1 : segments)};
   cuuint32_t estr[3] = {1, 1, 1};
   const CUtensorMapSwizzle sw = box_row_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
   CUresult r = encode(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -323,6 +335,7 @@ struct TensorMapEntry {
   const void* base;
   long long row_elems, rows;
   int elem_bytes, box_row_bytes, chunk_rows;
+  bool one_segment;
   CUtensorMap map;
 };
 constexpr int kTensorMapCacheSize = 16;
@@ -331,23 +344,23 @@ TensorMapEntry g_tmap_cache[kTensorMapCacheSize];
 int g_tmap_next = 0;
 
 int pool_tensor_map(CUtensorMap* map, const void* base, int elem_bytes, long long row_elems, long long rows,
-                    int box_row_bytes, int box_rows) {
+                    int box_row_bytes, int box_rows, bool one_segment) {
   {
     std::lock_guard<std::mutex> lock(g_tmap_mutex);
     for (const TensorMapEntry& e : g_tmap_cache) {
       if (e.base == base && e.row_elems == row_elems && e.rows == rows && e.elem_bytes == elem_bytes &&
-          e.box_row_bytes == box_row_bytes && e.chunk_rows == box_rows) {
+          e.box_row_bytes == box_row_bytes && e.chunk_rows == box_rows && e.one_segment == one_segment) {
         *map = e.map;
         return PKV_OK;
       }
     }
   }
-  int rc = encode_pool_tensor_map(map, base, elem_bytes, row_elems, rows, box_row_bytes, box_rows);
+  int rc = encode_pool_tensor_map(map, base, elem_bytes, row_elems, rows, box_row_bytes, box_rows, one_segment);
   if (rc) return rc;
   std::lock_guard<std::mutex> lock(g_tmap_mutex);
   TensorMapEntry& e = g_tmap_cache[g_tmap_next];
   g_tmap_next = (g_tmap_next + 1) % kTensorMapCacheSize;
-  e = TensorMapEntry{base, row_elems, rows, elem_bytes, box_row_bytes, box_rows, *map};
+  e = TensorMapEntry{base, row_elems, rows, elem_bytes, box_row_bytes, box_rows, one_segment, *map};
   return PKV_OK;
 }
 
@@ -428,7 +441,7 @@ struct PreparedDecode {
   CUtensorMap tk, tv;
   dim3 grid;
   int bits, dk, dv, nq, device;
-  bool solo, cc, bal, partial, merge;
+  bool solo, cc, bal, pc, partial, merge;
 };
 
 // Checks the arguments of a decode call (the passes in `passes`) and prepares its
@@ -475,6 +488,12 @@ int prepare_decode(const pkv_pool_layout* layout, const pkv_decode_params* param
   const int nq = (params->num_q_heads / HK) * params->n_query;
   const bool cc = plan.contraction == PKV_CONTRACTION_CUDA_CORE;
   const PartialInfo info = partial_info(layout->bits, D, DV, nq, solo, cc, bal);
+  // Blocks smaller than the instantiation's chunk: a chunk spans 2^piece_log2 blocks. The
+  // fused call writes a chunk's new rows into one block, so it needs whole chunks.
+  int piece_log2 = 0;
+  while ((info.chunk_rows >> piece_log2) > layout->block_size) ++piece_log2;
+  const int piece_rows = info.chunk_rows >> piece_log2;
+  if (piece_log2 > 0 && k_new) return PKV_ERR_UNSUPPORTED_SHAPE;
   // Balanced schedule: one wave of CTAs, as many per SM as the instantiation's occupancy
   // allows (within the bound the plan sized the workspace for).
   int bal_ctas = 0;
@@ -492,9 +511,9 @@ int prepare_decode(const pkv_pool_layout* layout, const pkv_decode_params* param
 
   *pd = PreparedDecode{};
   if (partial) {
-    rc = pool_tensor_map(&pd->tk, k_pool, elem, row_elems_k, rows, info.box_row_bytes, info.chunk_rows);
+    rc = pool_tensor_map(&pd->tk, k_pool, elem, row_elems_k, rows, info.box_row_bytes, piece_rows, piece_log2 > 0);
     if (rc) return rc;
-    rc = pool_tensor_map(&pd->tv, v_pool, elem, row_elems_v, rows, info.box_row_bytes_v, info.chunk_rows);
+    rc = pool_tensor_map(&pd->tv, v_pool, elem, row_elems_v, rows, info.box_row_bytes_v, piece_rows, piece_log2 > 0);
     if (rc) return rc;
   }
 
@@ -515,6 +534,7 @@ int prepare_decode(const pkv_pool_layout* layout, const pkv_decode_params* param
   p.ws_o = ws_mode ? static_cast<float*>(workspace) : nullptr;
   p.ws_ml = ws_mode ? reinterpret_cast<float*>(static_cast<char*>(workspace) + o_bytes) : nullptr;
   p.mode = mode;
+  p.piece_log2 = piece_log2;
   p.num_seqs = params->num_seqs;
   p.window = params->window;
   p.host_inputs = 0;
@@ -546,6 +566,7 @@ int prepare_decode(const pkv_pool_layout* layout, const pkv_decode_params* param
   pd->solo = solo;
   pd->cc = cc;
   pd->bal = bal;
+  pd->pc = piece_log2 > 0;
   pd->partial = partial;
   pd->merge = (passes & kPassMerge) && ws_mode;
   if (pd->merge) {
@@ -584,7 +605,11 @@ int launch_prepared(const PreparedDecode& pd, cudaStream_t st) {
   (void)cudaGetLastError();  // start from a clean error state
   cudaError_t e = cudaSuccess;
   if (pd.partial) {
-    if (pd.bal)
+    if (pd.pc)
+      e = pd.bits == 16  ? pkv::launch_partial_bf16_pc(pd.dk, pd.dv, pd.nq, pd.p, pd.tk, pd.tv, pd.grid, st, pd.device)
+          : pd.bits == 4 ? pkv::launch_partial_u4_pc(pd.dk, pd.dv, pd.nq, pd.p, pd.tk, pd.tv, pd.grid, st, pd.device)
+                         : pkv::launch_partial_u8_pc(pd.dk, pd.dv, pd.nq, pd.p, pd.tk, pd.tv, pd.grid, st, pd.device);
+    else if (pd.bal)
       e = pd.bits == 16  ? pkv::launch_partial_bf16_bal(pd.dk, pd.dv, pd.nq, pd.p, pd.tk, pd.tv, pd.grid, st, pd.device)
           : pd.bits == 4 ? pkv::launch_partial_u4_bal(pd.dk, pd.dv, pd.nq, pd.p, pd.tk, pd.tv, pd.grid, st, pd.device)
                          : pkv::launch_partial_u8_bal(pd.dk, pd.dv, pd.nq, pd.p, pd.tk, pd.tv, pd.grid, st, pd.device);

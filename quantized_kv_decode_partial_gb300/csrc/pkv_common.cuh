@@ -50,6 +50,7 @@ struct PartialParams {
   int num_q_heads, n_query, nq;  // nq = (HQ/HK) * n_query rows served per KV head
   int partition_tokens, max_partitions;
   int mode;           // kModeSingle / kModeWorkspace / kModeCluster / kModeBalanced
+  int piece_log2;     // blocks smaller than a chunk: a chunk spans 2^piece_log2 blocks (else 0)
   int num_seqs;       // B (read by the balanced schedule)
   int window;         // sliding window in rows (0: none)
   int host_inputs;    // kHost* bits: inputs a host-driven step keeps in host memory

@@ -54,6 +54,15 @@ cudaError_t launch_partial_u4_bal(int dk, int dv, int nq, const PartialParams& p
 cudaError_t launch_partial_u8_bal(int dk, int dv, int nq, const PartialParams& p, const CUtensorMap& tk,
                                   const CUtensorMap& tv, dim3 grid, cudaStream_t stream, int device);
 
+// Instantiations for pools of blocks smaller than a chunk (PartialParams.piece_log2 > 0) of
+// the same shapes' grids of several CTAs per SM; their PartialInfo is that of those grids.
+cudaError_t launch_partial_bf16_pc(int dk, int dv, int nq, const PartialParams& p, const CUtensorMap& tk,
+                                   const CUtensorMap& tv, dim3 grid, cudaStream_t stream, int device);
+cudaError_t launch_partial_u4_pc(int dk, int dv, int nq, const PartialParams& p, const CUtensorMap& tk,
+                                 const CUtensorMap& tv, dim3 grid, cudaStream_t stream, int device);
+cudaError_t launch_partial_u8_pc(int dk, int dv, int nq, const PartialParams& p, const CUtensorMap& tk,
+                                 const CUtensorMap& tv, dim3 grid, cudaStream_t stream, int device);
+
 int merge_groups(int head_dim, int max_partitions);
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream);
 cudaError_t launch_gather(const GatherParams& p, int num_seqs, cudaStream_t stream);

@@ -311,13 +311,14 @@ __device__ __forceinline__ void load_group_row(uint32_t addr, float (&v)[G]) {
 // groups: columns 0-3 carry the weights scaled by the even group's value scales, columns
 // 4-7 by the odd group's; each group's MMAs keep the columns of their own group.
 template <int BITS, int D, int DV, int NT, int WQ, bool SOLO, bool HOSTIN, int CCQ = 0, bool PV = false,
-          bool BAL = false>
+          bool BAL = false, bool PC = false>
 __global__ void __maxnreg__(255)
     pkv_partial_kernel(const __grid_constant__ PartialParams p, const __grid_constant__ CUtensorMap tmap_k,
                        const __grid_constant__ CUtensorMap tmap_v) {
   using C = PartialCfg<BITS, D, DV, NT, WQ, SOLO, CCQ, BAL>;
   static_assert(!PV || (BITS == 4 && NT == 1 && WQ == 1 && CCQ == 0 && C::kGroupsV % 2 == 0),
                 "paired value groups: 4-bit pages, one warp of 8 query columns, whole group pairs");
+  static_assert(!PC || (!SOLO && !BAL && CCQ == 0), "blocks smaller than a chunk: partitions, tensor cores");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + C::kDataBytes);  // [warp][stage]
@@ -372,7 +373,10 @@ __global__ void __maxnreg__(255)
   // depend on len: fetch their block-table entries while len is still in flight.
   int tbl_pre = 0;
   if (!BAL && p.window == 0 && leader) {
-    const long long r = static_cast<long long>(slot) * p.partition_tokens + (pg + lane * C::kWP) * C::kCh;
+    const int pl = PC ? p.piece_log2 : 0;
+    const int lq = lane >> pl, lj = lane & ((1 << pl) - 1);  // piece `lane`: its chunk, and the piece in it
+    const long long r =
+        static_cast<long long>(slot) * p.partition_tokens + (pg + lq * C::kWP) * C::kCh + lj * (C::kCh >> pl);
     const long long blk = r / p.block_size < p.max_blocks ? r / p.block_size : p.max_blocks - 1;
     tbl_pre = static_cast<int>(ld_nc_keep_u32(p.block_tables + static_cast<size_t>(b) * p.max_blocks + blk));
   }
@@ -468,54 +472,74 @@ __global__ void __maxnreg__(255)
     const int32_t* table = p.block_tables + static_cast<size_t>(b) * p.max_blocks;
     const uint64_t policy = l2_evict_first_policy();
     auto chunk_row = [&](int i) { return t_first + (pg + i * C::kWP) * C::kCh; };  // first cache row of local chunk i
-    // TMA row coordinate of local chunk i in physical block ph (the block's rows of this
-    // KV head plus the chunk's offset in the block), or -1 for a bad block id. Each lane
-    // of the leader warp holds the coordinate of one of the next 32 chunks to issue,
-    // and the raw block ids of the 32 after those.
-    auto coord_of = [&](int ph, int i) {
-      return static_cast<unsigned>(ph) < static_cast<unsigned>(p.num_blocks)
-                 ? (ph * p.num_kv_heads + hk) * p.block_size + chunk_row(i) % p.block_size
+    // Blocks smaller than a chunk: a chunk spans nb = 2^piece_log2 blocks, and is copied
+    // as nb pieces of pb rows, one per block. Pieces are numbered chunk-major (piece q is
+    // piece q mod nb of local chunk q / nb); with blocks of a chunk or more, piece q is
+    // chunk q.
+    const int nbl = PC ? p.piece_log2 : 0, nb = 1 << nbl, pb = C::kCh >> nbl;  // PC: instantiations for such pools
+    auto piece_row = [&](int q) { return chunk_row(q >> nbl) + (q & (nb - 1)) * pb; };  // its first cache row
+    // TMA row coordinate of local piece q in physical block ph (the block's rows of this
+    // KV head plus the piece's offset in the block), -1 for a bad block id, or -2 for a
+    // piece wholly at or past the length (a chunk's first piece never is): its block may
+    // not exist, and its rows are masked like any stale row, so it is not copied. Each
+    // lane of the leader warp holds the coordinate of one of the next 32 pieces to
+    // issue, and the raw block ids of the 32 after those (0 for pieces past the length,
+    // whose table entries are not read).
+    auto coord_of = [&](int ph, int q) {
+      return PC && piece_row(q) >= len ? -2
+             : static_cast<unsigned>(ph) < static_cast<unsigned>(p.num_blocks)
+                 ? (ph * p.num_kv_heads + hk) * p.block_size + piece_row(q) % p.block_size
                  : -1;
     };
-    // Balanced schedule: the raw block id of local chunk i (< my_chunks), with its KV head
-    // and row within the block packed into *pk as hk * block_size + row % block_size, and
-    // the TMA row coordinate from the two.
-    auto bal_entry = [&](int i, int* pk) {
-      const int x = x0 + i;
+    auto stored = [&](int q) { return !PC || piece_row(q) < len; };
+    // Balanced schedule: the raw block id of local piece q (of a chunk < my_chunks), with
+    // its KV head and row within the block packed into *pk as hk * block_size + row %
+    // block_size, and the TMA row coordinate from the two.
+    auto bal_entry = [&](int q, int* pk) {
+      const int x = x0 + (q >> nbl);
       const int bb = bal_seq_of(bal_S, p.num_seqs, x);
       const int n = (bal_S[bb + 1] - bal_S[bb]) / p.num_kv_heads;
       const int rel = x - bal_S[bb];
       const int h = rel / n;
-      const int row = bal_first_row(bal_len[bb], N, p.window, C::kCh) + (rel - h * n) * C::kCh;
+      const int row = bal_first_row(bal_len[bb], N, p.window, C::kCh) + (rel - h * n) * C::kCh + (q & (nb - 1)) * pb;
+      if (PC && row >= bal_len[bb]) {  // a piece past the length: not copied (pk -1)
+        *pk = -1;
+        return 0;
+      }
       *pk = h * p.block_size + row % p.block_size;
       return static_cast<int>(__ldg(p.block_tables + static_cast<size_t>(bb) * p.max_blocks + row / p.block_size));
     };
     auto bal_coord = [&](int ph, int pk) {
-      return static_cast<unsigned>(ph) < static_cast<unsigned>(p.num_blocks) ? ph * p.num_kv_heads * p.block_size + pk
-                                                                              : -1;
+      return pk < 0 ? -2
+             : static_cast<unsigned>(ph) < static_cast<unsigned>(p.num_blocks) ? ph * p.num_kv_heads * p.block_size + pk
+                                                                                : -1;
     };
+    const int my_pieces = my_chunks << nbl;
     int crd_cur = 0, tbl_next = 0, pk_next = 0;
     if (leader) {
       if constexpr (BAL) {
         int pk0 = 0;
-        const int ph0 = lane < my_chunks ? bal_entry(lane, &pk0) : 0;
-        tbl_next = 32 + lane < my_chunks ? bal_entry(32 + lane, &pk_next) : 0;
+        const int ph0 = lane < my_pieces ? bal_entry(lane, &pk0) : 0;
+        tbl_next = 32 + lane < my_pieces ? bal_entry(32 + lane, &pk_next) : 0;
         crd_cur = bal_coord(ph0, pk0);
       } else {
-        const int ph0 =
-            p.window == 0 ? tbl_pre : (lane < my_chunks ? __ldg(table + chunk_row(lane) / p.block_size) : 0);
-        tbl_next = 32 + lane < my_chunks ? __ldg(table + chunk_row(32 + lane) / p.block_size) : 0;
+        const int ph0 = p.window == 0 ? tbl_pre
+                        : lane < my_pieces && stored(lane) ? __ldg(table + piece_row(lane) / p.block_size)
+                                                           : 0;
+        tbl_next = 32 + lane < my_pieces && stored(32 + lane) ? __ldg(table + piece_row(32 + lane) / p.block_size) : 0;
         crd_cur = coord_of(ph0, lane);
       }
     }
     int issued = 0;  // chunks issued so far
 
     // Affine pages: this lane's share of the 16-byte copies that bring a chunk's scale and
-    // bias rows, fixed for the whole loop: copy j (lane + 32 j) reads plane row `row` at
-    // sb_src[j] + row * sb_pitch[j] bytes and lands at sb_dst[j] within the stage.
+    // bias rows, fixed for the whole loop: copy j (lane + 32 j) belongs to piece
+    // sb_piece[j] of the chunk, reads that piece's plane row `row` at sb_src[j] + row *
+    // sb_pitch[j] bytes and lands at sb_dst[j] within the stage (a piece of at least 8
+    // rows holds whole 16-byte copies).
     constexpr int kSbPerLane = C::kQuant ? (C::kSbCopies + 31) / 32 : 1;
     const char* sb_src[kSbPerLane];
-    int sb_pitch[kSbPerLane], sb_dst[kSbPerLane];
+    int sb_pitch[kSbPerLane], sb_dst[kSbPerLane];  // sb_dst: the piece in bits 16 and up
     if constexpr (C::kQuant) {
       constexpr int nk = C::kSbBytes / 16, nv = C::kSbBytesV / 16;
 #pragma unroll
@@ -528,9 +552,11 @@ __global__ void __maxnreg__(255)
                                    : plane == 1 ? p.k_biases
                                    : plane == 2 ? p.v_scales
                                                 : p.v_biases;
-        sb_src[j] = reinterpret_cast<const char*>(src) + 16 * k;
         sb_pitch[j] = 2 * (plane < 2 ? C::kGroups : C::kGroupsV);
-        sb_dst[j] = (plane == 0 ? C::kOffKs : plane == 1 ? C::kOffKb : plane == 2 ? C::kOffVs : C::kOffVb) + 16 * k;
+        const int piece = 16 * k / (sb_pitch[j] * pb);
+        sb_src[j] = reinterpret_cast<const char*>(src) + 16 * k - piece * pb * sb_pitch[j];
+        sb_dst[j] = ((plane == 0 ? C::kOffKs : plane == 1 ? C::kOffKb : plane == 2 ? C::kOffVs : C::kOffVb) + 16 * k) |
+                    (piece << 16);
       }
     }
 
@@ -538,17 +564,25 @@ __global__ void __maxnreg__(255)
     // chunk in flight, chunk i always lands in stage i mod kStagesPerGroup).
     auto issue_next = [&](int is) {  // the leader warp, warp-uniform
       if (issued >= my_chunks) return;
-      if (issued > 0 && (issued & 31) == 0) {
-        const int k = issued + 32 + lane;
+      const int ip = issued << nbl;  // the chunk's first piece
+      if (ip > 0 && (ip & 31) == 0) {
+        const int k = ip + 32 + lane;
         if constexpr (BAL) {
           crd_cur = bal_coord(tbl_next, pk_next);
-          tbl_next = k < my_chunks ? bal_entry(k, &pk_next) : 0;
+          tbl_next = k < my_pieces ? bal_entry(k, &pk_next) : 0;
         } else {
-          crd_cur = coord_of(tbl_next, issued + lane);
-          tbl_next = k < my_chunks ? __ldg(table + chunk_row(k) / p.block_size) : 0;
+          crd_cur = coord_of(tbl_next, ip + lane);
+          tbl_next = k < my_pieces && stored(k) ? __ldg(table + piece_row(k) / p.block_size) : 0;
         }
       }
-      const int row = __shfl_sync(0xffffffffu, crd_cur, issued & 31);
+      // row: the first piece's coordinate, -1 when a stored piece has a bad block id
+      int row = __shfl_sync(0xffffffffu, crd_cur, ip & 31);
+      int pieces_in = 1;  // pieces copied
+      if (nbl > 0) {
+        const int mine = __shfl_sync(0xffffffffu, crd_cur, (ip + (lane & (nb - 1))) & 31);
+        if (!__all_sync(0xffffffffu, mine >= 0 || mine == -2)) row = -1;
+        pieces_in = __popc(__ballot_sync(0xffffffffu, lane < nb && mine >= 0));
+      }
       if (!BAL && p.k_new != nullptr) {
         // Fused append: the step's new rows len-N .. len-1 that fall in this chunk are
         // written into its page first (the warp writes, fences its generic-proxy stores
@@ -576,14 +610,35 @@ __global__ void __maxnreg__(255)
         if (row >= 0) {
 #pragma unroll
           for (int j = 0; j < kSbPerLane; ++j) {
-            if (32 * j + lane < C::kSbCopies)
-              cp_async_16(st + sb_dst[j], sb_src[j] + static_cast<size_t>(row) * sb_pitch[j], policy);
+            const int prow = nbl > 0 ? __shfl_sync(0xffffffffu, crd_cur, (ip + (sb_dst[j] >> 16)) & 31) : row;
+            if (32 * j + lane < C::kSbCopies && prow >= 0)
+              cp_async_16(st + (PC ? sb_dst[j] & 0xFFFF : sb_dst[j]), sb_src[j] + static_cast<size_t>(prow) * sb_pitch[j],
+                          policy);
           }
           cp_async_mbar_arrive(fb);
         }
         __syncwarp();
       }
-      if (lane == 0) {
+      if (nbl > 0 && row >= 0) {
+        // one copy per piece and segment: the piece's rows land at their place in each
+        // segment of the chunk (a multiple of 8 rows: whole swizzle atoms)
+        if (lane == 0) {
+          my_ok[is] = 1;
+          fence_proxy_async_smem();
+          mbar_arrive_expect_tx(fb, pieces_in * (C::kTmaBytes >> nbl));
+        }
+        for (int j = 0; j < nb; ++j) {
+          const int prow = __shfl_sync(0xffffffffu, crd_cur, (ip + j) & 31);
+          if (lane == 0 && prow >= 0) {
+#pragma unroll
+            for (int sg = 0; sg < C::kBoxes; ++sg)
+              tma_load_3d(st + (sg * C::kCh + j * pb) * C::kRB, &tmap_k, 0, prow, sg, fb, policy);
+#pragma unroll
+            for (int sg = 0; sg < C::kBoxesV; ++sg)
+              tma_load_3d(st + C::kOffV + (sg * C::kCh + j * pb) * C::kRBV, &tmap_v, 0, prow, sg, fb, policy);
+          }
+        }
+      } else if (lane == 0) {
         my_ok[is] = row >= 0 ? 1 : 0;
         if (row >= 0) {
           fence_proxy_async_smem();  // this warp's reads of the stage precede the copies into it

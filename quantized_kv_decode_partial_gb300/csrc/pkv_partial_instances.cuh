@@ -17,30 +17,32 @@ PartialInfo info_of() {
 }
 
 // Devices on which an instantiation's function attributes are set (bit per device < 64).
-template <int BITS, int D, int DV, int NT, int WQ, bool SOLO, bool HOSTIN, int CCQ, bool PV, bool BAL>
+template <int BITS, int D, int DV, int NT, int WQ, bool SOLO, bool HOSTIN, int CCQ, bool PV, bool BAL, bool PC>
 std::atomic<unsigned long long> g_configured{0};
 
 template <int BITS, int D, int DV, int NT, int WQ, bool SOLO, bool HOSTIN, int CCQ = 0, bool PV = false,
-          bool BAL = false>
+          bool BAL = false, bool PC = false>
 cudaError_t configure_once(int device) {
   using C = PartialCfg<BITS, D, DV, NT, WQ, SOLO, CCQ, BAL>;
-  auto kern = pkv_partial_kernel<BITS, D, DV, NT, WQ, SOLO, HOSTIN, CCQ, PV, BAL>;
+  auto kern = pkv_partial_kernel<BITS, D, DV, NT, WQ, SOLO, HOSTIN, CCQ, PV, BAL, PC>;
   const unsigned long long bit = device >= 0 && device < 64 ? (1ull << device) : 0ull;
-  if (bit && (g_configured<BITS, D, DV, NT, WQ, SOLO, HOSTIN, CCQ, PV, BAL>.load(std::memory_order_acquire) & bit))
+  if (bit &&
+      (g_configured<BITS, D, DV, NT, WQ, SOLO, HOSTIN, CCQ, PV, BAL, PC>.load(std::memory_order_acquire) & bit))
     return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);  // clusters of up to 16
   if (e != cudaSuccess) return e;
-  if (bit) g_configured<BITS, D, DV, NT, WQ, SOLO, HOSTIN, CCQ, PV, BAL>.fetch_or(bit, std::memory_order_acq_rel);
+  if (bit) g_configured<BITS, D, DV, NT, WQ, SOLO, HOSTIN, CCQ, PV, BAL, PC>.fetch_or(bit, std::memory_order_acq_rel);
   return cudaSuccess;
 }
 
-template <int BITS, int D, int DV, int NT, int WQ, bool SOLO, int CCQ = 0, bool PV = false, bool BAL = false>
+template <int BITS, int D, int DV, int NT, int WQ, bool SOLO, int CCQ = 0, bool PV = false, bool BAL = false,
+          bool PC = false>
 cudaError_t launch_of(const PartialParams& p, const CUtensorMap& tk, const CUtensorMap& tv, dim3 grid,
                       cudaStream_t stream, int device) {
   using C = PartialCfg<BITS, D, DV, NT, WQ, SOLO, CCQ, BAL>;
-  auto kern = pkv_partial_kernel<BITS, D, DV, NT, WQ, SOLO, false, CCQ, PV, BAL>;
+  auto kern = pkv_partial_kernel<BITS, D, DV, NT, WQ, SOLO, false, CCQ, PV, BAL, PC>;
   cudaError_t e;
   // A grid of one CTA per SM launches as a programmatic dependent (below); when all of
   // its length, query and block tables are host memory of a host-driven step, the
@@ -54,7 +56,7 @@ cudaError_t launch_of(const PartialParams& p, const CUtensorMap& tk, const CUten
       e = configure_once<BITS, D, DV, NT, WQ, SOLO, false, CCQ, PV>(device);
     }
   } else {
-    e = configure_once<BITS, D, DV, NT, WQ, SOLO, false, CCQ, PV, BAL>(device);
+    e = configure_once<BITS, D, DV, NT, WQ, SOLO, false, CCQ, PV, BAL, PC>(device);
   }
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg{};

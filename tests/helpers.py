@@ -49,12 +49,13 @@ def oracle_out(case: DecodeCase, partition_tokens=None, rows=None):
     return oracle.paged_decode_attention(*args, rows=rows, **kw)
 
 
-def run_gpu(case: DecodeCase, partition_tokens=None, error_flag=None):
+def run_gpu(case: DecodeCase, partition_tokens=None, error_flag=None, schedule=0):
     pt = case.partition_tokens if partition_tokens is None else partition_tokens
     return paged_decode_attention(case.q, case.k_pool, case.v_pool, case.block_tables, case.seq_lens, case.scale,
                                   bits=case.spec.bits, group_size=case.spec.group_size, k_scales=case.k_scales,
                                   k_biases=case.k_biases, v_scales=case.v_scales, v_biases=case.v_biases,
-                                  partition_tokens=pt, window=case.spec.window, error_flag=error_flag)
+                                  partition_tokens=pt, window=case.spec.window, error_flag=error_flag,
+                                  schedule=schedule)
 
 
 def assert_close(got, ref, what="", strict=False):

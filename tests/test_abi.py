@@ -170,7 +170,8 @@ def test_plan_auto_is_monotone_in_sm_count(lib):
 
 @pytest.mark.parametrize("field,value,code", [
     ("bits", 3, B.PKV_ERR_BAD_LAYOUT), ("bits", 2, B.PKV_ERR_BAD_LAYOUT), ("group_size", 32, B.PKV_ERR_BAD_LAYOUT),
-    ("head_dim", 96, B.PKV_ERR_BAD_LAYOUT), ("block_size", 8, B.PKV_ERR_BAD_LAYOUT),
+    ("head_dim", 96, B.PKV_ERR_BAD_LAYOUT), ("block_size", 4, B.PKV_ERR_BAD_LAYOUT),
+    ("block_size", 24, B.PKV_ERR_BAD_LAYOUT), ("block_size", 48, B.PKV_ERR_BAD_LAYOUT),
     ("num_blocks", 0, B.PKV_ERR_BAD_LAYOUT), ("num_blocks", 1 << 28, B.PKV_ERR_BAD_LAYOUT),
 ])
 def test_plan_rejects_bad_layouts(lib, field, value, code):
@@ -316,6 +317,27 @@ def test_output_rows_past_int32_are_rejected(lib):
     # 65535 sequences x 65535 query heads: 4.3e9 output rows
     par = B.DecodeParams(65535, 65535, 1, 4, 64, 0)
     assert lib.pkv_make_plan(ctypes.byref(lay), ctypes.byref(par), 152, ctypes.byref(plan)) == B.PKV_ERR_BAD_PARAMS
+
+
+@pytest.mark.parametrize("bits,block_size", [(16, 8), (4, 8), (4, 16), (8, 8), (8, 16), (16, 48), (4, 96)])
+def test_blocks_of_8_rows_or_more_that_divide_a_chunk_are_accepted(lib, bits, block_size):
+    # a chunk (16 rows for bf16 pages, 32 for affine) spans several such blocks; or blocks
+    # of whole chunks. Pools of smaller blocks take the instantiations of grids of several
+    # CTAs per SM (128 threads, even for one CTA per SM), neither the balanced schedule nor
+    # the CUDA-core contraction.
+    lay = B.PoolLayout(1000, 2, block_size, 128, bits, 64)
+    plan = B.Plan()
+    par = B.DecodeParams(2, 8, 1, 4096 // block_size, 0, 0, 0, B.PKV_SCHEDULE_BALANCED)
+    assert lib.pkv_make_plan(ctypes.byref(lay), ctypes.byref(par), 152, ctypes.byref(plan)) == B.PKV_OK
+    assert plan.partition_tokens % (16 if bits == 16 else 32) == 0
+    small = block_size < plan.chunk_rows
+    assert plan.balanced == int(not small)
+    if small:
+        assert plan.threads_per_cta == 128
+        if bits == 16:
+            cc = B.DecodeParams(2, 4, 1, 4096 // block_size, 0, 0, B.PKV_CONTRACTION_CUDA_CORE)
+            assert lib.pkv_make_plan(ctypes.byref(lay), ctypes.byref(cc), 152, ctypes.byref(plan)) == \
+                B.PKV_ERR_UNSUPPORTED_SHAPE
 
 
 def test_schedule_field_is_validated(lib):

@@ -27,10 +27,10 @@ def bits_of(t):
     return t.detach().cpu().numpy()
 
 
-def setup(bits, D, n_new, num_seqs=3, seed_name="", dv=0):
-    name = f"app_{bits}_{D}_{n_new}_{seed_name}" + (f"_dv{dv}" if dv else "")
+def setup(bits, D, n_new, num_seqs=3, seed_name="", dv=0, bs=0):
+    name = f"app_{bits}_{D}_{n_new}_{seed_name}" + (f"_dv{dv}" if dv else "") + (f"_bs{bs}" if bs else "")
     seed = zlib.crc32(name.encode()) % 10000
-    bs = 16 if bits == 16 else 32
+    bs = bs or (16 if bits == 16 else 32)
     DV = dv or D
     sp = DecodeSpec(name=name, num_seqs=num_seqs, num_q_heads=4, num_kv_heads=2, head_dim=D, n_query=1,
                     block_size=bs, bits=bits, length_range=(1, 150), pool_factor=2.0, seed=seed, v_head_dim=dv)
@@ -45,13 +45,15 @@ def setup(bits, D, n_new, num_seqs=3, seed_name="", dv=0):
     return sp, case, lens, k_new.to(torch.bfloat16), v_new.to(torch.bfloat16)
 
 
-CASES = [(16, 128, 1, 0), (16, 64, 3, 0), (16, 256, 2, 0), (4, 256, 1, 0), (4, 128, 3, 0), (8, 256, 2, 0),
-         (8, 128, 1, 0), (16, 192, 2, 128), (4, 128, 2, 256), (8, 256, 1, 128)]
+# (bits, D, new rows, value head dim, block size; 0: a chunk's rows)
+CASES = [(16, 128, 1, 0, 0), (16, 64, 3, 0, 0), (16, 256, 2, 0, 0), (4, 256, 1, 0, 0), (4, 128, 3, 0, 0),
+         (8, 256, 2, 0, 0), (8, 128, 1, 0, 0), (16, 192, 2, 128, 0), (4, 128, 2, 256, 0), (8, 256, 1, 128, 0),
+         (16, 128, 3, 0, 8), (4, 256, 2, 0, 16), (4, 128, 3, 0, 8), (8, 256, 2, 0, 8)]
 
 
-@pytest.mark.parametrize("bits,D,n_new,dv", CASES)
-def test_append_is_bit_exact(bits, D, n_new, dv):
-    sp, case, lens, k_new, v_new = setup(bits, D, n_new, dv=dv)
+@pytest.mark.parametrize("bits,D,n_new,dv,bs", CASES)
+def test_append_is_bit_exact(bits, D, n_new, dv, bs):
+    sp, case, lens, k_new, v_new = setup(bits, D, n_new, dv=dv, bs=bs)
     ref = pw.append_rows(k_new.float().numpy(), v_new.float().numpy(), case.block_tables.numpy(), lens,
                          bits_of(case.k_pool), bits_of(case.v_pool), bits=bits,
                          k_scales=bits_of(case.k_scales), k_biases=bits_of(case.k_biases),

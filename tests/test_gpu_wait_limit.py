@@ -33,35 +33,38 @@ def spec(name, **kw):
 # The finishing forms of the partial pass: partition states through the workspace and
 # the merge kernel (many CTAs per SM; bf16 and 8-bit pages), a thread-block cluster merge
 # (one CTA per SM), query rows shared by several warps, a single partition writing the
-# output, and the balanced schedule (the library's own split of a batch; a page group
-# that gives up marks the rest of its run as empty). Every case streams enough K/V per
-# SM that its warps wait on HBM.
-CASES = [
-    (spec("wait_bf16_workspace"), 256),
-    (spec("wait_u8_workspace", head_dim=256, bits=8, block_size=32), 512),
-    (spec("wait_bf16_cluster", num_seqs=1, lengths=(131072,), length_range=None, pool_factor=1.0), 8192),
-    (spec("wait_bf16_query_groups", num_seqs=32, num_kv_heads=1), 1024),
-    (spec("wait_bf16_single", num_seqs=32, length_range=(2000, 4000)), 8192),
-    (spec("wait_u4_balanced", head_dim=256, bits=4, block_size=32, num_seqs=32), 0),
+# output, and the balanced schedule (asked for on a bf16 batch; a page group that gives
+# up marks the rest of its run as empty). Every case streams enough K/V per SM that its
+# warps wait on HBM (the 4-bit kernels compute long enough per chunk that their stages
+# have landed before they are waited for).
+BAL = B.PKV_SCHEDULE_BALANCED
+CASES = [  # (spec, partition rows, schedule)
+    (spec("wait_bf16_workspace"), 256, 0),
+    (spec("wait_u8_workspace", head_dim=256, bits=8, block_size=32), 512, 0),
+    (spec("wait_bf16_cluster", num_seqs=1, lengths=(131072,), length_range=None, pool_factor=1.0), 8192, 0),
+    (spec("wait_bf16_query_groups", num_seqs=32, num_kv_heads=1), 1024, 0),
+    (spec("wait_bf16_single", num_seqs=32, length_range=(2000, 4000)), 8192, 0),
+    (spec("wait_bf16_balanced", num_seqs=32), 0, BAL),
 ]
 
 
 def test_cases_take_the_finishing_forms_they_name():
     forms = []
-    for sp, partition in CASES:
+    for sp, partition, schedule in CASES:
         max_blocks = -(-max(draw_lengths(sp)) // sp.block_size)
         layout = B.PoolLayout(1 << 16, sp.num_kv_heads, sp.block_size, sp.head_dim, sp.bits, 64)
-        plan = B.make_plan(layout, B.DecodeParams(sp.num_seqs, sp.num_q_heads, 1, max_blocks, partition),
+        plan = B.make_plan(layout, B.DecodeParams(sp.num_seqs, sp.num_q_heads, 1, max_blocks, partition, 0, 0,
+                                                  schedule),
                            sm_count=torch.cuda.get_device_properties(DEV).multi_processor_count)
         forms.append("balanced" if plan.balanced else "single" if plan.max_partitions == 1
                      else "cluster" if plan.merge_in_cluster else "workspace")
     assert forms == ["workspace", "workspace", "cluster", "workspace", "single", "balanced"]
 
 
-@pytest.mark.parametrize("sp,partition", CASES, ids=[s.name for s, _ in CASES])
-def test_short_wait_bound_gives_up_without_a_fault(sp, partition):
+@pytest.mark.parametrize("sp,partition,schedule", CASES, ids=[s.name for s, _, _ in CASES])
+def test_short_wait_bound_gives_up_without_a_fault(sp, partition, schedule):
     case = make_case(sp, poison=False).to(DEV)
-    ref = run_gpu(case, partition_tokens=partition)
+    ref = run_gpu(case, partition_tokens=partition, schedule=schedule)
     torch.cuda.synchronize()
     # Evict the inputs from L2 (129 MB on a GB300) by writing a larger buffer, so that the
     # stages come from HBM and take microseconds to arrive.
@@ -70,7 +73,7 @@ def test_short_wait_bound_gives_up_without_a_fault(sp, partition):
     previous = B.set_wait_limit_ns(1)
     try:
         err = torch.zeros(1, dtype=torch.int32, device=DEV)
-        out = run_gpu(case, partition_tokens=partition, error_flag=err)
+        out = run_gpu(case, partition_tokens=partition, error_flag=err, schedule=schedule)
         torch.cuda.synchronize()  # the kernel returned: no hang, no fault
     finally:
         B.set_wait_limit_ns(previous)
@@ -78,7 +81,7 @@ def test_short_wait_bound_gives_up_without_a_fault(sp, partition):
     assert out.shape == ref.shape
     # the stream and the context are still good: the next call is the one from before
     err2 = torch.zeros(1, dtype=torch.int32, device=DEV)
-    again = run_gpu(case, partition_tokens=partition, error_flag=err2)
+    again = run_gpu(case, partition_tokens=partition, error_flag=err2, schedule=schedule)
     torch.cuda.synchronize()
     assert int(err2.item()) == 0
     assert torch.equal(again.view(torch.int16), ref.view(torch.int16))
