@@ -153,11 +153,16 @@ int plan_impl(const pkv_pool_layout* L, const pkv_decode_params* P, int sm_count
     part = round_up(std::min<long long>(P->partition_tokens, max_len), ch);
   } else {
     // Halve the partition until the grid covers the GPU about four times over (two
-    // CTAs per SM), never below 256 rows. Once the grid fills a wave, stop before a
-    // CTA would get less than 512 KB of K/V: below that its fixed costs (prologue,
-    // pipeline fill, epilogue) start to show (measured on the windowed workload).
+    // CTAs per SM) and no CTA gets more than 3 MB of K/V, never below 256 rows. Once
+    // the grid fills a wave, stop before a CTA would get less than 512 KB: below that
+    // its fixed costs (prologue, pipeline fill, epilogue) start to show (measured on the
+    // windowed workload). The 3 MB cap keeps the last CTAs of a batch of mixed lengths
+    // short: the 8-bit affine batch (8160-row partitions of 4.4 MB at four waves) went
+    // from 717.2 to 697.9 us with 4080-row ones, while 2 MB CTAs (bf16 8 x 128K) were
+    // 2% slower halved again.
     const long long slots = 2ll * (sm_count > 0 ? sm_count : 1);
     const long long target = 4 * slots;
+    constexpr long long kMaxCtaBytes = 3ll << 20;
     const long long units = static_cast<long long>(P->num_seqs) * L->num_kv_heads;
     const long long kv_row = stored_row_bytes(L, L->head_dim) + stored_row_bytes(L, v_dim(L));  // K + V
     const long long floor_rows = 256;
@@ -166,7 +171,7 @@ int plan_impl(const pkv_pool_layout* L, const pkv_decode_params* P, int sm_count
     part = round_up(span, ch);
     while (part > floor_rows) {
       const long long ctas = units * ((span + part - 1) / part);
-      if (ctas >= target) break;
+      if (ctas >= target && part * kv_row <= kMaxCtaBytes) break;
       const long long half = std::max<long long>(floor_rows, round_up(part / 2, ch));
       if (half < rich_rows && ctas >= slots) break;
       part = half;

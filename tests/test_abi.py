@@ -94,6 +94,9 @@ def test_plan_for_workloads(lib, name):
             kv_row = sum(2 * d if sp.bits == 16 else d * sp.bits // 8 + d // 16 for d in (sp.head_dim, sp.dv))
             assert (ctas >= 8 * 152 or plan.partition_tokens == 256
                     or (ctas >= 2 * 152 and plan.partition_tokens // 2 < (512 << 10) // kv_row))
+            # and no CTA above 3 MB of K/V unless halving would go below the 512 KB floor
+            assert (plan.partition_tokens * kv_row <= 3 << 20
+                    or plan.partition_tokens // 2 < max(256, (512 << 10) // kv_row))
     assert plan.threads_per_cta in (128, 192, 256) and 0 < plan.smem_bytes <= 227 * 1024
     if not solo and not (sp.bits == 16 and sp.head_dim == 256):  # 16 KB stages of bf16 D=256: one CTA per SM
         assert plan.smem_bytes <= 114 * 1024  # two CTAs per SM
