@@ -31,6 +31,31 @@ def test_header_declares_the_binding_exports():
     assert declared_functions() == sorted(B.EXPORTS)
 
 
+def test_binding_constants_match_the_header():
+    # every integer #define of the header that the binding mirrors has the header's value
+    text = open(HEADER).read()
+    defines = {m.group(1): int(m.group(2), 0) for m in re.finditer(r"^#define (PKV_\w+) \(?(-?\w+)\)?", text, re.M)
+               if re.fullmatch(r"-?(0x[0-9a-fA-F]+|\d+)", m.group(2))}
+    mirrored = {name: value for name, value in defines.items() if hasattr(B, name)}
+    assert {"PKV_SCHEDULE_BALANCED", "PKV_CONTRACTION_CUDA_CORE", "PKV_ERR_UNSUPPORTED_SHAPE",
+            "PKV_DEVERR_TIMEOUT"} <= set(mirrored)
+    for name, value in mirrored.items():
+        assert getattr(B, name) == value, name
+
+
+def test_struct_layouts_match_the_header():
+    # the binding's ctypes structures list the header's fields in order
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    for cname, cls in (("pkv_pool_layout", B.PoolLayout), ("pkv_decode_params", B.DecodeParams), ("pkv_plan", B.Plan)):
+        body = re.search(r"typedef struct %s \{(.*?)\} %s;" % (cname, cname), text, re.S).group(1)
+        names = []
+        for decl in body.split(";"):
+            decl = decl.strip()
+            if decl:
+                names += [n.strip() for n in decl.split(None, 1)[1].split(",")]
+        assert names == [f for f, _ in cls._fields_], cname
+
+
 def test_every_declared_symbol_is_exported(lib):
     for name in declared_functions():
         assert hasattr(lib, name), name
