@@ -67,12 +67,13 @@ cudaError_t launch_of(const PartialParams& p, const CUtensorMap& tk, const CUten
   cudaLaunchAttribute attr[2];
   cfg.attrs = attr;
   cfg.numAttrs = 0;
-  if constexpr (SOLO) {
-    // Programmatic dependent launch for grids of at most one CTA per SM: the CTAs may be
-    // placed on idle SMs while the previous kernel on the stream finishes, and wait for
-    // it (griddepcontrol.wait) before they touch global memory. The launch latency then
-    // hides behind that kernel's tail. (Grids of two CTAs per SM lost 2% this way: early
-    // CTAs take the slots the previous grid frees unevenly.)
+  if (SOLO || p.mode != kModeCluster) {
+    // Programmatic dependent launch: the CTAs may be placed on SMs while the previous
+    // kernel on the stream finishes, and wait for it (griddepcontrol.wait) before they
+    // touch global memory. The launch latency then hides behind that kernel's tail:
+    // host-driven steps of the batches took 2-4 us less, graph-replayed steps the same.
+    // (The cluster grid of two CTAs per SM of the windowed workload lost 2% this way:
+    // early CTAs take the slots the previous grid frees unevenly.)
     attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
     ++cfg.numAttrs;
