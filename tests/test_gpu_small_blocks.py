@@ -134,3 +134,33 @@ def test_fused_call_refuses_blocks_smaller_than_a_chunk():
         paged_decode_append_attention(d.q, k_new, k_new, d.k_pool, d.v_pool, d.block_tables, d.seq_lens, d.scale,
                                       partition_tokens=64)
     assert e.value.code == B.PKV_ERR_UNSUPPORTED_SHAPE
+
+
+def test_host_driven_step_and_two_passes_on_small_blocks():
+    # the host-driven step (inputs read from pinned host memory) and the two-pass entry
+    # points run the same instantiation as the one-call entry, bit for bit
+    from quantized_kv_decode_partial_gb300 import HostDecodeStep, paged_decode_passes
+    sp = spec("sb_host", num_seqs=12, num_q_heads=16, num_kv_heads=4, head_dim=256, bits=4, block_size=16,
+              length_range=(1, 1500))
+    case = make_case(sp)
+    d = case.to(DEV)
+    kw = dict(bits=4, k_scales=d.k_scales, k_biases=d.k_biases, v_scales=d.v_scales, v_biases=d.v_biases,
+              partition_tokens=64)
+    ref = paged_decode_attention(d.q, d.k_pool, d.v_pool, d.block_tables, d.seq_lens, case.scale, **kw)
+    torch.cuda.synchronize()
+    assert_close(ref.double().cpu().numpy(), oracle_out(case), sp.name)
+    stream = torch.cuda.Stream(device=DEV)
+    step = HostDecodeStep(case.q, case.block_tables, case.seq_lens, d.k_pool, d.v_pool, case.scale, stream=stream,
+                          **kw)
+    step()
+    stream.synchronize()
+    assert torch.equal(step.out_host.view(torch.int16), ref.cpu().view(torch.int16))
+    plan = B.make_plan(B.layout_for(d.k_pool, 256, 4), B.DecodeParams(sp.num_seqs, 16, 1, d.block_tables.shape[1],
+                                                                      64, 0))
+    ws = torch.empty(max(1, plan.workspace_bytes), dtype=torch.uint8, device=DEV)
+    out = torch.full_like(ref, float("nan"))
+    for passes in ("partial", "merge"):
+        paged_decode_passes(d.q, d.k_pool, d.v_pool, d.block_tables, d.seq_lens, case.scale, passes=passes, out=out,
+                            workspace=ws, **kw)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
