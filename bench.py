@@ -52,6 +52,9 @@ def parse_args(argv=None):
                     help="profiling mode: make the workload, run this many eager decode calls, exit")
     ap.add_argument("--num-seqs", type=int, default=0,
                     help="profiling mode: keep only the first N sequences of the workload")
+    ap.add_argument("--seq-len", type=int, default=0,
+                    help="profiling mode: give every kept sequence this length (with a window shorter than it, "
+                         "the kernels read the same rows from a smaller pool)")
     ap.add_argument("--partition-tokens", type=int, default=-2,
                     help="rows per partition instead of the workload's choice (0: the library's plan)")
     ap.add_argument("--print-kernel-hash", action="store_true",
@@ -727,6 +730,8 @@ def run_profile_calls(args):
         if args.num_seqs:
             lens = draw_lengths(sp)[:args.num_seqs]
             sp = replace(sp, num_seqs=len(lens), lengths=tuple(lens), length_range=None)
+        if args.seq_len:
+            sp = replace(sp, lengths=(args.seq_len,) * sp.num_seqs, length_range=None)
         if args.partition_tokens != -2:
             sp = replace(sp, partition_tokens=args.partition_tokens)
         c = make_case(sp, device=dev, poison=False)

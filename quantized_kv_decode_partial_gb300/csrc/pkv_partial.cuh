@@ -339,9 +339,10 @@ __global__ void __maxnreg__(255)
   size_t row0 = (static_cast<size_t>(b) * p.num_q_heads + static_cast<size_t>(hk) * rep) * N;
   const bool single = p.mode == kModeSingle;
   const bool in_cluster = p.mode == kModeCluster;
-  // When launched as a programmatic dependent (grids of one CTA per SM), everything the
-  // previous kernel on the stream writes (inputs, pools, the output) is read or written
-  // only after it has completed; otherwise the wait returns at once.
+  // When launched as a programmatic dependent (every grid but the clusters of several
+  // CTAs per SM), everything the previous kernel on the stream writes (inputs, pools, the
+  // output) is read or written only after it has completed; otherwise the wait returns
+  // at once.
   if (threadIdx.x == 0) {
     prefetch_tensormap(&tmap_k);  // kernel parameters: no dependence
     prefetch_tensormap(&tmap_v);

@@ -44,8 +44,8 @@ cudaError_t launch_of(const PartialParams& p, const CUtensorMap& tk, const CUten
   using C = PartialCfg<BITS, D, DV, NT, WQ, SOLO, CCQ, BAL>;
   auto kern = pkv_partial_kernel<BITS, D, DV, NT, WQ, SOLO, false, CCQ, PV, BAL, PC>;
   cudaError_t e;
-  // A grid of one CTA per SM launches as a programmatic dependent (below); when all of
-  // its length, query and block tables are host memory of a host-driven step, the
+  // Grids launch as programmatic dependents (below). For a grid of one CTA per SM whose
+  // length, query and block tables are all host memory of a host-driven step, the
   // variant that reads them before the dependency wait runs.
   constexpr int kAllHost = kHostSeqLens | kHostQuery | kHostTables;
   if constexpr (SOLO) {

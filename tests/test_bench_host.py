@@ -92,3 +92,23 @@ def test_reference_arm_prints_one_contract_line():
     assert d["impl"] == "reference" and d["value"] > 0 and d["config"]["workload"] == bench.DEFAULT_WORKLOAD
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+
+
+def test_profiling_length_override_keeps_the_windowed_plan():
+    # --seq-len lets the windowed workload's launch be captured from a smaller pool: with
+    # lengths past the window the plan (and the rows read) are those of the full workload
+    import ctypes
+
+    from quantized_kv_decode_partial_gb300 import binding as B
+    from quantized_kv_decode_partial_gb300.workloads import WORKLOADS
+    sp = WORKLOADS["bf16_8x131072_n4_w8192_hq32_d128"]
+    assert bench.parse_args(["--seq-len", "16384"]).seq_len == 16384
+    lay = B.PoolLayout(1000, sp.num_kv_heads, sp.block_size, sp.head_dim, sp.bits, sp.group_size)
+    plans = []
+    for length in (sp.lengths[0], 16384):
+        par = B.DecodeParams(sp.num_seqs, sp.num_q_heads, sp.n_query, length // sp.block_size, 0, sp.window)
+        plan = B.Plan()
+        assert B.load_library().pkv_make_plan(ctypes.byref(lay), ctypes.byref(par), 152, ctypes.byref(plan)) == 0
+        plans.append((plan.partition_tokens, plan.max_partitions, plan.merge_in_cluster, plan.threads_per_cta,
+                      plan.smem_bytes, plan.workspace_bytes))
+    assert plans[0] == plans[1]
