@@ -48,10 +48,11 @@
  * (a cudaStream_t passed as void*; NULL = the legacy default stream) and make
  * no allocation and no host synchronisation, so they can be captured in a
  * CUDA graph. Stream order holds as usual: the partial pass (unless its
- * partitions merge in clusters of several CTAs per SM) and the merge pass are
- * launched as programmatic dependents of the previous work on the stream (their
- * CTAs may be placed while that work finishes), and they touch no global memory
- * before that work has completed.
+ * partitions merge in clusters of several CTAs per SM outside a host-driven step
+ * that reads its inputs from host memory) and the merge pass are launched as
+ * programmatic dependents of the previous work on the stream (their CTAs may be
+ * placed while that work finishes), and they touch no global memory before that
+ * work has completed.
  *
  * Errors: host-side argument checks happen before any CUDA call and return a
  * negative PKV_ERR_* code without launching anything. Problems that only the

@@ -340,9 +340,9 @@ __global__ void __maxnreg__(255)
   const bool single = p.mode == kModeSingle;
   const bool in_cluster = p.mode == kModeCluster;
   // When launched as a programmatic dependent (every grid but the clusters of several
-  // CTAs per SM), everything the previous kernel on the stream writes (inputs, pools, the
-  // output) is read or written only after it has completed; otherwise the wait returns
-  // at once.
+  // CTAs per SM of device-input calls), everything the previous kernel on the stream
+  // writes (inputs, pools, the output) is read or written only after it has completed;
+  // otherwise the wait returns at once.
   if (threadIdx.x == 0) {
     prefetch_tensormap(&tmap_k);  // kernel parameters: no dependence
     prefetch_tensormap(&tmap_v);

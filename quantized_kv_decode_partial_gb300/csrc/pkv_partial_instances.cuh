@@ -67,13 +67,14 @@ cudaError_t launch_of(const PartialParams& p, const CUtensorMap& tk, const CUten
   cudaLaunchAttribute attr[2];
   cfg.attrs = attr;
   cfg.numAttrs = 0;
-  if (SOLO || p.mode != kModeCluster) {
+  if (SOLO || p.mode != kModeCluster || p.host_inputs != 0) {
     // Programmatic dependent launch: the CTAs may be placed on SMs while the previous
     // kernel on the stream finishes, and wait for it (griddepcontrol.wait) before they
     // touch global memory. The launch latency then hides behind that kernel's tail:
     // host-driven steps of the batches took 2-4 us less, graph-replayed steps the same.
-    // (The cluster grid of two CTAs per SM of the windowed workload lost 2% this way:
-    // early CTAs take the slots the previous grid frees unevenly.)
+    // (Under graph replay the cluster grid of two CTAs per SM of the windowed workload
+    // lost 2% this way: early CTAs take the slots the previous grid frees unevenly. A
+    // host-driven step, launched one by one, gains more from the hidden launch.)
     attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
     ++cfg.numAttrs;

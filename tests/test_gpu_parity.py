@@ -476,6 +476,47 @@ def test_back_to_back_host_driven_steps():
             assert torch.equal(st.out_host.view(torch.int16), ref.view(torch.int16))
 
 
+def test_back_to_back_host_steps_of_a_windowed_cluster_grid():
+    # A window gives every unit the same span, so the plan is one wave of clusters of
+    # several CTAs per SM; host-driven steps launch that grid as a programmatic dependent
+    # of the previous step. Steps of two instances enqueued back to back with no
+    # synchronisation must each equal the device entry bit for bit.
+    import ctypes
+
+    from quantized_kv_decode_partial_gb300 import HostDecodeStep
+    stream = torch.cuda.Stream(device=DEV)
+    steps, refs = [], []
+    for k in range(2):
+        sp = spec(f"host_win_{k}", num_seqs=8, num_q_heads=32, num_kv_heads=8, n_query=4, window=4096,
+                  lengths=(5000, 4200, 6000, 4100, 5500, 4500, 4800, 5200), length_range=None)
+        case = make_case(sp)
+        d = case.to(DEV)
+        if k == 0:
+            lay = B.layout_for(d.k_pool, 128, 16)
+            par = B.DecodeParams(sp.num_seqs, 32, 4, d.block_tables.shape[1], 0, 4096)
+            plan = B.Plan()
+            assert B.load_library().pkv_plan_for_current_device(ctypes.byref(lay), ctypes.byref(par),
+                                                                ctypes.byref(plan)) == 0
+            assert plan.merge_in_cluster == 1 and plan.threads_per_cta == 128 and plan.max_partitions >= 2
+            b, kv = 2, 5
+            ref_sub = oracle_out(subcase(d, b, kv))
+        refs.append(run_gpu(d, partition_tokens=0).cpu())
+        if k == 0:
+            got = refs[0][b, kv * 4:(kv + 1) * 4][None].double().numpy()
+            assert_close(got, ref_sub, "windowed cluster grid, one (sequence, KV head)")
+        steps.append(HostDecodeStep(case.q, case.block_tables, case.seq_lens, d.k_pool, d.v_pool, case.scale,
+                                    window=4096, stream=stream))
+    torch.cuda.synchronize()
+    for _ in range(3):
+        for st in steps:
+            st.out_host.fill_(float("nan"))
+        for st in steps:
+            st()
+        stream.synchronize()
+        for st, ref in zip(steps, refs):
+            assert torch.equal(st.out_host.view(torch.int16), ref.view(torch.int16))
+
+
 def test_host_driven_fused_step_matches_device_fused_step():
     from quantized_kv_decode_partial_gb300 import HostDecodeStep
     sp = spec("host_fused", num_q_heads=8, num_kv_heads=2, n_query=2, length_range=(3, 300))
