@@ -143,6 +143,43 @@ def test_rejected_length_is_zeroed_and_flagged():
     assert_close(good.double().cpu().numpy(), oracle_out(make_case(sp)), "bal_badlen good")
 
 
+@pytest.mark.parametrize("bits", [16, 4])
+def test_every_length_rejected_leaves_an_empty_list(bits):
+    # no sequence contributes a chunk: every run is empty, the merge writes zeros and the
+    # partial pass flags the lengths; the next call on the same buffers is unaffected
+    sp = spec(f"bal_allbad_{bits}", num_seqs=6, head_dim=256 if bits == 4 else 128, bits=bits,
+              block_size=32, n_query=2, length_range=(2, 700))
+    case = make_case(sp)
+    d = case.to(DEV)
+    good = run(d)
+    bad = make_case(sp).to(DEV)
+    bad.seq_lens = torch.tensor([0, 1, -3, 0, 1, d.block_tables.shape[1] * sp.block_size + 5], dtype=torch.int32,
+                                device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = run(bad, error_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & B.PKV_DEVERR_BAD_SEQ_LEN
+    assert not out.float().any()
+    again = run(d)
+    torch.cuda.synchronize()
+    assert torch.equal(again.view(torch.int16), good.view(torch.int16))
+    assert_close(good.double().cpu().numpy(), oracle_out(case), sp.name)
+
+
+def test_the_largest_sequence_count_the_list_holds():
+    # 256 sequences: every entry of the prefix over the lengths is used
+    sp = spec("bal_256_seqs", num_seqs=256, num_q_heads=4, num_kv_heads=2, head_dim=256, bits=4, block_size=32,
+              length_range=(1, 200))
+    case = make_case(sp)
+    d = case.to(DEV)
+    assert plan_of(d).balanced == 1
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = run(d, error_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert_close(out.double().cpu().numpy(), oracle_out(case), sp.name)
+
+
 def test_bad_block_is_flagged_and_isolated():
     sp = spec("bal_badblock", num_seqs=12, length_range=(300, 900))
     d = make_case(sp).to(DEV)
