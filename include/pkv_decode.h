@@ -127,7 +127,12 @@ typedef struct pkv_decode_params {
   int32_t window;             /* sliding window W in rows, 0 = none: query i then sees only keys
                                  t with len-N+i-W < t <= len-N+i (the W most recent positions,
                                  its own included), as the pages' causal mask with a window
-                                 size (kernels/attention/masks.ts, createCausalMask) */
+                                 size (kernels/attention/masks.ts, createCausalMask). Reads
+                                 start at the 32-row boundary at or below the lowest visible
+                                 row, so up to 31 rows below the window are read and masked:
+                                 their block-table entries must be valid and their values
+                                 finite, as for any row below len; rows further below are
+                                 never read */
   int32_t contraction;        /* how the dot products and the weighted value sums run:
                                  PKV_CONTRACTION_AUTO (0, the library's choice per shape),
                                  PKV_CONTRACTION_TENSOR (1, warp-level tensor-core MMA) or
