@@ -1,5 +1,6 @@
 """Test helpers: run the oracle on a workload instance, cut sampled sub-problems
-out of full-size instances, and compare against the benchmark spec's tolerances."""
+out of full-size instances, and compare against the parity bound (max-abs 1e-2,
+mean-abs 1e-3 on bf16 outputs)."""
 
 from __future__ import annotations
 
@@ -59,7 +60,7 @@ def run_gpu(case: DecodeCase, partition_tokens=None, error_flag=None, schedule=0
 
 
 def assert_close(got, ref, what="", strict=False):
-    """The benchmark spec's bound (max-abs 1e-2, mean-abs 1e-3) on the computation,
+    """The parity bound (max-abs 1e-2, mean-abs 1e-3) on the computation,
     on top of the bf16 output's own representation error: each element may also
     differ by half a bf16 ulp of the exact value (a correctly rounded result
     does), and the mean by a quarter ulp (the mean of a uniform rounding error).
