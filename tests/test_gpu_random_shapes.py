@@ -49,3 +49,28 @@ def test_random_shape_matches_oracle(i):
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     assert_close(out.double().cpu().numpy(), ref, f"{spec}")
+
+
+def draw_more(i):
+    # the same space with blocks smaller than the staged chunk (8 or 16 rows) and the
+    # schedule drawn too (the balanced schedule applies where partition_tokens is 0 and
+    # the blocks hold whole chunks; elsewhere the call runs partitions)
+    rnd = random.Random(19000 + i)
+    spec = draw(10000 + i)
+    bs = rnd.choice([8, 16, 32] if spec.bits == 16 else [8, 16, 32, 64])
+    part = rnd.choice([-1, 0, 0, 64, 160])
+    schedule = rnd.choice([B.PKV_SCHEDULE_AUTO, B.PKV_SCHEDULE_PARTITIONS, B.PKV_SCHEDULE_BALANCED])
+    return DecodeSpec(**{**spec.__dict__, "name": f"rand_more{i}", "block_size": bs, "partition_tokens": part,
+                         "seed": 19000 + i}), schedule
+
+
+@pytest.mark.parametrize("i", range(40))
+def test_random_shape_with_small_blocks_and_schedules_matches_oracle(i):
+    spec, schedule = draw_more(i)
+    case = make_case(spec)
+    ref = oracle_out(case)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = run_gpu(case.to(DEV), error_flag=err, schedule=schedule)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert_close(out.double().cpu().numpy(), ref, f"{spec} schedule={schedule}")
