@@ -60,9 +60,10 @@ namespace pkv {
 
 // SOLO: the variant for grids of at most one CTA per SM. Such a CTA has the SM to
 // itself, so it takes 8 warps (two per scheduler, so one warp's dependent chain
-// hides behind the other's) when two stages per warp fit in shared memory, else 6,
-// as many stages per warp (up to 4) as fit, up to 255 registers per thread, and a
-// receive area for the push-form cluster merge.
+// hides behind the other's) when two stages per warp fit in shared memory beside a
+// receive area for the push-form cluster merge, else 7 without that area (pull-form
+// merge), else 6, as many stages per warp (up to 4) as fit, and up to 255 registers
+// per thread.
 // D is the key (and query) head dim, DV the value head dim. Names without a V
 // describe the K plane, names with one the V plane. CCQ = 0 takes the tensor-core
 // contraction; CCQ = 2 or 4 the CUDA-core one (pkv_partial_cc.cuh) for bf16 pages
@@ -107,21 +108,30 @@ struct PartialCfg {
   static constexpr int kRecvNeedBytes = (2 * kMaxClusterParts * kNqAll + kNqAll * DV + 4 * kMaxClusterParts) * 4;
   // CUDA-core contraction: each warp's weights of one chunk (16 rows x 4 query rows of f32)
   static constexpr int kPBufBytes = CCQ ? 8 * 256 : 0;
-  // stage ring of a CTA alone on its SM, which always has a receive area
-  static constexpr int kSoloBudget = 227 * 1024 - kBarrierBytes - 1024 - (SOLO ? kRecvNeedBytes : 0) - kPBufBytes;
-  // every warp computes: 8 when two stages per warp fit a CTA alone on its SM, else 6 (two
-  // of the four schedulers then hold two warps), else 4; a query group of 8 warps (up to
-  // 64 query rows of 256-dim heads) is the whole CTA
+  // stage ring of a CTA alone on its SM, with the receive area of the push-form cluster
+  // merge (kSoloBudget) or without it (kSoloBase)
+  static constexpr int kSoloBase = 227 * 1024 - kBarrierBytes - 1024 - kPBufBytes;
+  static constexpr int kSoloBudget = kSoloBase - (SOLO ? kRecvNeedBytes : 0);
+  // A seventh warp where eight with two stages each do not fit beside the receive area
+  // but seven fit without it (bf16 D=256: 7 x 2 x 16 KB); the CTA then merges its cluster
+  // in the pull form. The single-CTA bf16 D=256 step went from 12.89 to 11.97 us; its
+  // cluster grids moved by +0.3% to -3.6%.
+  static constexpr bool kSeven = SOLO && WQ == 1 && CCQ == 0 && 8 * 2 * kStageBytes > kSoloBudget &&
+                                 7 * 2 * kStageBytes <= kSoloBase;
+  // every warp computes: 8 when two stages per warp fit a CTA alone on its SM, else 7 as
+  // above, else 6 (two of the four schedulers then hold two warps), else 4; a query group
+  // of 8 warps (up to 64 query rows of 256-dim heads) is the whole CTA
   static constexpr int kWarps = WQ == 8                              ? 8
                                 : !SOLO                              ? 4
                                 : 8 * 2 * kStageBytes <= kSoloBudget ? 8
+                                : kSeven                             ? 7
                                 : 6 * 2 * kStageBytes <= kSoloBudget ? 6
                                                                      : 4;
   static constexpr int kThreads = kWarps * 32;
   // The warps form kWP page groups of WQ warps. A page group takes every kWP-th chunk;
   // its WQ warps read each of its chunks, each for its own 8*NT query rows.
   static constexpr int kWP = kWarps / WQ;
-  static constexpr int kSoloStages = kSoloBudget / (kWarps * kStageBytes);
+  static constexpr int kSoloStages = (kSeven ? kSoloBase : kSoloBudget) / (kWarps * kStageBytes);
   // (a query group of 8 warps shares one ring of 8 or 16 stages, within 144 KB)
   static constexpr int kStagesPerWarp = WQ == 8 ? (8 * 2 * kStageBytes <= 144 * 1024 ? 2 : 1)
                                         : SOLO  ? (kSoloStages < 4 ? kSoloStages : 4)
@@ -146,7 +156,7 @@ struct PartialCfg {
   // The receive area (after the ring) is there when the CTA is alone on its SM, or when it
   // does not cost the second CTA per SM (or the CTA already has its SM to itself).
   static constexpr int kBaseSmem = kWorkBytes + kBarrierBytes + 1024;
-  static constexpr bool kPush = !BAL && (SOLO || kBaseSmem + kRecvNeedBytes <= 114 * 1024 ||
+  static constexpr bool kPush = !BAL && !kSeven && (SOLO || kBaseSmem + kRecvNeedBytes <= 114 * 1024 ||
                                          (kBaseSmem > 114 * 1024 && kBaseSmem + kRecvNeedBytes <= 227 * 1024));
   static constexpr int kRecvBytes = kPush ? kRecvNeedBytes : 0;
   static constexpr int kDataBytes = kWorkBytes + kRecvBytes;
@@ -161,6 +171,7 @@ struct PartialCfg {
   static_assert(!kQuant || (D % 64 == 0 && DV % 64 == 0), "affine head dims are whole 64-dim groups");
   static_assert(DV % 64 == 0, "value head dims are whole 4-m-tile groups");
   static_assert(WQ == 1 || WQ == 2 || WQ == 4 || WQ == 8, "query groups of 1, 2, 4 or 8 warps");
+  static_assert(kWarps % WQ == 0, "whole query groups");
   static_assert(kStagesPerWarp >= 2 || WQ == 8, "at least two stages per warp (a ring of 8 for 8-warp groups)");
   static_assert(!(WQ == 8 && SOLO), "a query group of 8 warps is its CTA already");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory of one CTA");

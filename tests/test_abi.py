@@ -122,12 +122,12 @@ def test_plan_for_workloads(lib, name):
             # and no CTA above 3 MB of K/V unless halving would go below the 512 KB floor
             assert (plan.partition_tokens * kv_row <= 3 << 20
                     or plan.partition_tokens // 2 < max(256, (512 << 10) // kv_row))
-    assert plan.threads_per_cta in (128, 192, 256) and 0 < plan.smem_bytes <= 227 * 1024
+    assert plan.threads_per_cta in (128, 192, 224, 256) and 0 < plan.smem_bytes <= 227 * 1024
     if not solo and not (sp.bits == 16 and sp.head_dim == 256):  # 16 KB stages of bf16 D=256: one CTA per SM
         assert plan.smem_bytes <= 114 * 1024  # two CTAs per SM
 
 
-@pytest.mark.parametrize("bits,head_dim,threads", [(16, 64, 256), (16, 128, 256), (16, 256, 192), (4, 128, 256),
+@pytest.mark.parametrize("bits,head_dim,threads", [(16, 64, 256), (16, 128, 256), (16, 256, 224), (4, 128, 256),
                                                    (4, 256, 256), (8, 128, 256), (8, 256, 256)])
 def test_small_grids_take_the_one_cta_per_sm_variant(lib, bits, head_dim, threads):
     lay = B.PoolLayout(4096, 4, 32, head_dim, bits, 64)
