@@ -108,20 +108,27 @@ struct PartialCfg {
   static constexpr int kRecvNeedBytes = (2 * kMaxClusterParts * kNqAll + kNqAll * DV + 4 * kMaxClusterParts) * 4;
   // CUDA-core contraction: each warp's weights of one chunk (16 rows x 4 query rows of f32)
   static constexpr int kPBufBytes = CCQ ? 8 * 256 : 0;
+  // balanced schedule: the chunk-list prefix over the sequences and their lengths
+  static constexpr int kBalBytes = BAL ? (2 * kMaxBalancedSeqs + 4) * 4 : 0;
   // stage ring of a CTA alone on its SM, with the receive area of the push-form cluster
   // merge (kSoloBudget) or without it (kSoloBase)
-  static constexpr int kSoloBase = 227 * 1024 - kBarrierBytes - 1024 - kPBufBytes;
+  static constexpr int kSoloBase = 227 * 1024 - kBarrierBytes - 1024 - kPBufBytes - kBalBytes;
   static constexpr int kSoloBudget = kSoloBase - (SOLO ? kRecvNeedBytes : 0);
+  // A CTA of a grid of several per SM whose four warps' two stages each already take more
+  // than half the SM's shared memory (16 KB stages: bf16 D=256) has its SM to itself anyway.
+  static constexpr bool kLone = !SOLO && 4 * 2 * kStageBytes > 114 * 1024;
   // A seventh warp where eight with two stages each do not fit beside the receive area
-  // but seven fit without it (bf16 D=256: 7 x 2 x 16 KB); the CTA then merges its cluster
-  // in the pull form. The single-CTA bf16 D=256 step went from 12.89 to 11.97 us; its
-  // cluster grids moved by +0.3% to -3.6%.
-  static constexpr bool kSeven = SOLO && WQ == 1 && CCQ == 0 && 8 * 2 * kStageBytes > kSoloBudget &&
+  // but seven fit without it (bf16 D=256: 7 x 2 x 16 KB), for a CTA alone on its SM; the
+  // CTA then merges its cluster in the pull form. The single-CTA bf16 D=256 step went
+  // from 12.89 to 11.97 us, its cluster grids moved by +0.3% to -3.6%, and bf16 D=256
+  // batches of several CTAs per SM (four warps before) took 4-5% less time.
+  static constexpr bool kSeven = (SOLO || kLone) && WQ == 1 && CCQ == 0 && 8 * 2 * kStageBytes > kSoloBudget &&
                                  7 * 2 * kStageBytes <= kSoloBase;
   // every warp computes: 8 when two stages per warp fit a CTA alone on its SM, else 7 as
   // above, else 6 (two of the four schedulers then hold two warps), else 4; a query group
   // of 8 warps (up to 64 query rows of 256-dim heads) is the whole CTA
   static constexpr int kWarps = WQ == 8                              ? 8
+                                : kSeven && !SOLO                    ? 7
                                 : !SOLO                              ? 4
                                 : 8 * 2 * kStageBytes <= kSoloBudget ? 8
                                 : kSeven                             ? 7
@@ -134,7 +141,7 @@ struct PartialCfg {
   static constexpr int kSoloStages = (kSeven ? kSoloBase : kSoloBudget) / (kWarps * kStageBytes);
   // (a query group of 8 warps shares one ring of 8 or 16 stages, within 144 KB)
   static constexpr int kStagesPerWarp = WQ == 8 ? (8 * 2 * kStageBytes <= 144 * 1024 ? 2 : 1)
-                                        : SOLO  ? (kSoloStages < 4 ? kSoloStages : 4)
+                                        : SOLO || kSeven ? (kSoloStages < 4 ? kSoloStages : 4)
                                                 : (kStageBytes <= 9 * 1024 ? 3 : 2);
   static constexpr int kStagesPerGroup = kStagesPerWarp * WQ;  // each page group's private ring
   static constexpr int kMt = DV / 16;       // 16-dim m-tiles of O^T
@@ -160,8 +167,6 @@ struct PartialCfg {
                                          (kBaseSmem > 114 * 1024 && kBaseSmem + kRecvNeedBytes <= 227 * 1024));
   static constexpr int kRecvBytes = kPush ? kRecvNeedBytes : 0;
   static constexpr int kDataBytes = kWorkBytes + kRecvBytes;
-  // balanced schedule: the chunk-list prefix over the sequences and their lengths
-  static constexpr int kBalBytes = BAL ? (2 * kMaxBalancedSeqs + 4) * 4 : 0;
   static constexpr int kSmemBytes = kDataBytes + kBarrierBytes + kPBufBytes + kBalBytes + 1024;  // + alignment slack
   static constexpr float kCodeUnit = 5.9604644775390625e-8f;  // 2^-24: value of fp16 bit pattern 1
 

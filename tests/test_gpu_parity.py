@@ -130,8 +130,9 @@ def test_small_cases_match_oracle(sp, parts):
 
 
 # The small cases above launch at most one CTA per SM for up to 8 query rows per KV head,
-# which takes the eight-warp variant; these grids of more than one CTA per SM take the
-# four-warp one for the same shapes.
+# which takes the eight-warp variant (seven for bf16 D=256); these grids of more than one
+# CTA per SM take the four-warp one for the same shapes (seven warps for bf16 D=256, whose
+# CTAs hold their SM alone).
 BIG_GRID = [(16, 64, 0), (16, 128, 0), (16, 256, 0), (4, 128, 0), (4, 256, 0), (8, 128, 0), (8, 256, 0),
             (16, 192, 128), (16, 256, 128), (4, 128, 256)]
 
@@ -146,7 +147,8 @@ def test_grids_of_several_ctas_per_sm_match_oracle(bits, D, DV):
     for pt in (max(case.lens_host) + 64, 32):
         plan = B.make_plan(B.layout_for(case.k_pool, D, bits, v_pool=case.v_pool),
                            B.DecodeParams(sp.num_seqs, 16, 1, case.block_tables.shape[1], pt))
-        assert plan.threads_per_cta == 128
+        # bf16 D=256 CTAs hold their SM alone anyway (16 KB stages) and take seven warps
+        assert plan.threads_per_cta == (224 if (bits, D, DV or D) == (16, 256, 256) else 128)
         err = torch.zeros(1, dtype=torch.int32, device=DEV)
         out = run_gpu(dcase, partition_tokens=pt, error_flag=err)
         torch.cuda.synchronize()
