@@ -131,9 +131,14 @@ struct PartialCfg {
   // takes three page groups, six warps, beside the receive area: its batches took 16-18%
   // less time than with four warps (0.64 -> 0.76 of the measured peak).
   static constexpr bool kSixLone = kLone && WQ == 2 && CCQ == 0 && 6 * 2 * kStageBytes + kRecvNeedBytes <= kSoloBase;
+  // And one of four-warp query groups (bf16 D=256 with 17-32 query rows) takes two page
+  // groups, eight warps, with a ring of four stages each: its batches took a third less
+  // time than with one group and a ring of eight (0.35 -> 0.53 of the measured peak).
+  static constexpr bool kEightLone = kLone && WQ == 4 && CCQ == 0 && 8 * kStageBytes + kRecvNeedBytes <= kSoloBase;
   static constexpr int kWarps = WQ == 8                              ? 8
                                 : kSeven && !SOLO                    ? 7
                                 : kSixLone                           ? 6
+                                : kEightLone                         ? 8
                                 : !SOLO                              ? 4
                                 : 8 * 2 * kStageBytes <= kSoloBudget ? 8
                                 : kSeven                             ? 7
@@ -147,6 +152,7 @@ struct PartialCfg {
                                      (kWarps * kStageBytes);
   // (a query group of 8 warps shares one ring of 8 or 16 stages, within 144 KB)
   static constexpr int kStagesPerWarp = WQ == 8 ? (8 * 2 * kStageBytes <= 144 * 1024 ? 2 : 1)
+                                        : kEightLone ? 1
                                         : SOLO || kSeven || kSixLone ? (kSoloStages < 4 ? kSoloStages : 4)
                                                 : (kStageBytes <= 9 * 1024 ? 3 : 2);
   static constexpr int kStagesPerGroup = kStagesPerWarp * WQ;  // each page group's private ring
@@ -183,7 +189,7 @@ struct PartialCfg {
   static_assert(DV % 64 == 0, "value head dims are whole 4-m-tile groups");
   static_assert(WQ == 1 || WQ == 2 || WQ == 4 || WQ == 8, "query groups of 1, 2, 4 or 8 warps");
   static_assert(kWarps % WQ == 0, "whole query groups");
-  static_assert(kStagesPerWarp >= 2 || WQ == 8, "at least two stages per warp (a ring of 8 for 8-warp groups)");
+  static_assert(kStagesPerWarp >= 2 || WQ >= 4, "at least two stages per warp (a ring of 4 or 8 for 4- or 8-warp groups)");
   static_assert(!(WQ == 8 && SOLO), "a query group of 8 warps is its CTA already");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory of one CTA");
   static_assert(CCQ == 0 || (BITS == 16 && D == DV && NT == 1 && WQ == 1 && kCh == 16 && kRB == 128),
