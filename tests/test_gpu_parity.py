@@ -137,6 +137,31 @@ BIG_GRID = [(16, 64, 0), (16, 128, 0), (16, 256, 0), (4, 128, 0), (4, 256, 0), (
             (16, 192, 128), (16, 256, 128), (4, 128, 256)]
 
 
+# bf16 D=256 CTAs hold their SM alone (16 KB stages) and take 7, 6 or 8 warps for query
+# groups of one, two or four warps: several waves of them through the workspace, the
+# balanced schedule, and blocks smaller than a chunk.
+LONE = [(8, 1), (8, 2), (16, 2)]  # (query heads per KV head, query rows): 8, 16 and 32 rows
+
+
+@pytest.mark.parametrize("rep,n_query", LONE, ids=[f"rows{r * n}" for r, n in LONE])
+@pytest.mark.parametrize("block_size", [16, 8])
+def test_lone_bf16_d256_ctas_on_grids_of_several_waves(rep, n_query, block_size):
+    sp = spec(f"lone_d256_{rep}_{n_query}_{block_size}", num_seqs=40, num_q_heads=rep, num_kv_heads=1, head_dim=256,
+              n_query=n_query, block_size=block_size, length_range=(n_query, 2000))
+    case = make_case(sp)
+    ref = oracle_out(case)
+    d = case.to(DEV)
+    plan = B.make_plan(B.layout_for(d.k_pool, 256, 16), B.DecodeParams(sp.num_seqs, rep, n_query,
+                                                                      d.block_tables.shape[1], 64, 0))
+    assert plan.threads_per_cta == {1: 224, 2: 192, 4: 256}[rep * n_query // 8] and plan.workspace_bytes > 0
+    for pt, schedule in ((64, 0), (0, B.PKV_SCHEDULE_BALANCED)):
+        err = torch.zeros(1, dtype=torch.int32, device=DEV)
+        out = run_gpu(d, partition_tokens=pt, error_flag=err, schedule=schedule)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        assert_close(out.double().cpu().numpy(), ref, f"{sp.name} partition={pt} schedule={schedule}")
+
+
 @pytest.mark.parametrize("bits,D,DV", BIG_GRID, ids=[f"b{b}_d{d}_{v}" for b, d, v in BIG_GRID])
 def test_grids_of_several_ctas_per_sm_match_oracle(bits, D, DV):
     sp = spec(f"big_grid_{bits}_{D}_{DV}", num_seqs=44, num_q_heads=16, num_kv_heads=4, head_dim=D, v_head_dim=DV,
