@@ -13,7 +13,9 @@
 // such state per (sequence, KV head) the run crosses.
 //
 // Design (GB300):
-//  * Four warps per CTA (six or eight for grids of at most one CTA per SM); with W warps,
+//  * Four warps per CTA (six to eight for grids of at most one CTA per SM and for CTAs
+//    whose stages fill more than half an SM anyway, eight for query groups of eight
+//    warps); with W warps,
 //    warp w takes chunks w, w+W, w+2W, ... of the partition (16 rows for bf16
 //    pages, 32 or 16 for affine pages) and runs its own pipeline: lane 0 issues
 //    the copies of its chunk `kStagesPerWarp` ahead into a private ring of
