@@ -180,19 +180,42 @@ int plan_impl(const pkv_pool_layout* L, const pkv_decode_params* P, int sm_count
     // (sequence, KV head) units carry even work. When the grid above is at most two
     // waves (a short step, where the merge launch shows) and 2..16 partitions per unit
     // make a grid of one wave that fills at least three quarters of it, with CTAs of
-    // at least 512 KB, take the most partitions that do: the partitions then merge
-    // inside their clusters, with no workspace and no second launch.
+    // at least 512 KB, take the most partitions that do (a wave of one CTA per SM
+    // first, below): the partitions then merge inside their clusters, with no
+    // workspace and no second launch.
     const long long nq_rows = static_cast<long long>(P->num_q_heads / L->num_kv_heads) * P->n_query;
     const PartialInfo two = partial_info(L->bits, L->head_dim, v_dim(L), static_cast<int>(nq_rows), false,
                                          P->contraction == PKV_CONTRACTION_CUDA_CORE);
     const long long default_ctas = units * ((span + part - 1) / part);
     if (P->window > 0 && default_ctas <= 2 * slots && two.exists && two.smem_bytes <= 114 * 1024) {
-      for (int k = pkv::kMaxClusterParts; k >= 2; --k) {
+      // First a grid of one CTA per SM, where there is a variant for it: the most
+      // partitions per unit (one included: no merge at all) that keep the grid within the
+      // SMs and fill three quarters of them with CTAs of at least 1 MB. Its CTAs have
+      // twice the warps, so the same rows stream from fewer, fuller SMs; on windowed
+      // batches (4 to 16 sequences of 20000 rows, windows of 4096 and 8192 rows, HQ=32,
+      // HK=8, N=4) that took 2-4% less time than two CTAs per SM, and host-driven steps
+      // 6% less on 8 sequences. With CTAs of under 1 MB (2 sequences: 928 rows) the
+      // per-CTA start and merge showed, and 496 short CTAs through the workspace were
+      // 14% faster.
+      const PartialInfo one = partial_info(L->bits, L->head_dim, v_dim(L), static_cast<int>(nq_rows), true,
+                                           P->contraction == PKV_CONTRACTION_CUDA_CORE);
+      const long long sms = sm_count > 0 ? sm_count : 1;
+      bool placed = false;
+      const bool whole_chunks = L->block_size >= two.chunk_rows;  // pools of smaller blocks have no such variant
+      for (int k = pkv::kMaxClusterParts; one.exists && whole_chunks && k >= 1 && !placed; --k) {
+        const long long pk = round_up((span + k - 1) / k, ch);
+        const long long ctas = units * ((span + pk - 1) / pk);
+        if (pk * kv_row >= (1ll << 20) && ctas <= sms && 4 * ctas >= 3 * sms) {
+          part = pk;
+          placed = true;
+        }
+      }
+      for (int k = pkv::kMaxClusterParts; k >= 2 && !placed; --k) {
         const long long pk = round_up((span + k - 1) / k, ch);
         const long long ctas = units * ((span + pk - 1) / pk);
         if (pk >= rich_rows && ctas <= slots && 4 * ctas >= 3 * slots) {
           part = pk;
-          break;
+          placed = true;
         }
       }
     }

@@ -101,7 +101,8 @@ def test_plan_for_workloads(lib, name):
     # grids of at most one CTA per SM take the variant with more warps and stages (4 query-row
     # tiles of 8 at most); one wave of CTAs with 2..16 partitions merges inside a thread-block cluster
     ctas = sp.num_seqs * sp.num_kv_heads * plan.max_partitions
-    solo = ctas <= 152 and sp.rep * sp.n_query <= 8
+    rows = sp.rep * sp.n_query
+    solo = ctas <= 152 and (rows <= 8 or (sp.bits == 16 and sp.head_dim == sp.dv == 128 and rows <= 16))
     assert (plan.smem_bytes > 114 * 1024) if solo else plan.threads_per_cta == 128
     two_per_sm = not solo and plan.smem_bytes <= 114 * 1024
     assert plan.merge_in_cluster == (2 <= plan.max_partitions <= (16 if two_per_sm or solo else 8)
